@@ -1,0 +1,427 @@
+#!/usr/bin/env python
+"""Benchmark of the speculate-and-verify step on GB300.
+
+One step = gate -> retrieval -> verification attention || acceptance for one
+batch of the chosen workload (default: the Llama-3.1-8B-shaped verify, batch 1,
+prefix 4096, W=4 D=20, V=128256). Prints ONE JSON line on rank 0.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Timing: each step is a CUDA-graph replay; R input copies rotate so that their
+total exceeds twice the L2 (each step reads data last touched R steps ago).
+K steps are bracketed by a barrier + synchronize and CUDA events; the maximum
+over ranks is taken. Every library kernel is bracketed by event nodes inside
+the graphs, which gives per-kernel durations over the timed region.
+`--impl reference` times the CPU oracle (the reference arm) instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify steps/s and candidate tokens/s on 1 GB300; % of HBM roofline"
+UNIT = "verify steps/s"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama8b")
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-worker", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-seconds", type=float, default=20.0, help=argparse.SUPPRESS)
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# shared helpers
+# ---------------------------------------------------------------------------
+def workload_config(wl, tokens_per_step, extra=None):
+    cfg = {"workload": f"{wl.name}: {wl.description}, {wl.mode} mode",
+           "batch": wl.B, "prefix": list(wl.ctx_len), "W": wl.W, "D": wl.D, "K_chain": wl.K,
+           "heads": f"{wl.Hq}q/{wl.Hkv}kv dh{wl.dh}", "vocab": wl.V,
+           "candidate_tokens_per_step": tokens_per_step}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d.get("hbm_gbs", FALLBACK_HBM_GBS)), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def oracle_worker(args):
+    """Time the CPU oracle on full steps of the workload (runs in a child process
+    pinned to one BLAS thread). Prints a JSON dict."""
+    import numpy as np  # noqa: F401
+    from oracle import ssd_oracle as O
+    from speculative_decoding_copy_gb300 import workloads as WL
+    wl = WL.WORKLOADS[args.workload]
+    inp = WL.make_inputs(wl)
+    budget = args.oracle_seconds
+    n, t0 = 0, time.perf_counter()
+    while True:
+        r = O.verify_step(inp, wl)
+        n += 1
+        if time.perf_counter() - t0 >= budget or n >= 1000:
+            break
+    dt = time.perf_counter() - t0
+    tokens = int(r["blk_len"].sum())
+    print(json.dumps({"steps": n, "seconds": dt, "tokens_per_step": tokens}))
+
+
+def run_oracle_subprocess(workload, seconds):
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
+        env[k] = "1"
+    env.pop("RANK", None)
+    env.pop("WORLD_SIZE", None)
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--oracle-worker", "--workload", workload,
+           "--oracle-seconds", str(seconds)]
+    r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=900)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle worker failed: {r.stderr[-2000:]}")
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from speculative_decoding_copy_gb300 import workloads as WL
+    wl = WL.WORKLOADS[args.workload]
+    seconds = max(10.0, min(60.0, 0.002 * args.steps))
+    res = run_oracle_subprocess(args.workload, seconds)
+    value = res["steps"] / res["seconds"]
+    sample = (f"{res['steps']} full oracle steps of the {wl.name} workload in {res['seconds']:.1f} s "
+              f"(one BLAS thread; warm-up not needed: no JIT)")
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": res["steps"],
+            "warmup": 0, "ms_per_step": 1000.0 / value, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(wl, res["tokens_per_step"]), "impl": "reference",
+            "candidate_tokens_per_s": value * res["tokens_per_step"],
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample,
+                             "cpu": cpu_model()},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons, power = [], None, set(), []
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for name, v in zip(["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"], f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+KERNELS = ["gate_match", "retrieve", "attn_prefix", "attn_combine", "vocab_stats", "accept_select", "sample_final"]
+
+
+def source_sha(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "speculative_decoding_copy_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {"vocab_stats": ("ssd_accept.cu", "ssd_accept.cuh", "ssd_common.cuh"),
+                  "attn_prefix": ("ssd_attn.cu", "ssd_attn_tc.cu", "ssd_attn.cuh", "ssd_common.cuh")}
+
+
+def dram_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p) or kernel not in KERNEL_SOURCES:
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(f"{kernel}/{workload}")
+    if not e or e.get("source_sha") != source_sha(*KERNEL_SOURCES[kernel]):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from speculative_decoding_copy_gb300 import _binding as ssd
+    from speculative_decoding_copy_gb300 import workloads as WL
+    from speculative_decoding_copy_gb300.step import VerifyStep
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    wl = WL.WORKLOADS[args.workload]
+    inp = WL.make_inputs(wl, WL.SEED_BASE + 1 + 1000 * rank)
+    ssd.lib()
+
+    # rotating copies: total bytes above twice the L2
+    probe = VerifyStep(wl, inp, device=dev)
+    main = torch.cuda.Stream(dev)
+    aux = torch.cuda.Stream(dev)
+    with torch.cuda.stream(main):
+        probe.run(main, aux)
+    torch.cuda.synchronize()
+    blk_len = probe.ret_out["blk_len"].cpu().numpy()
+    prefix = inp["prefix_len"]
+    ab = WL.algorithmic_bytes(wl, prefix, blk_len)
+    R = max(3, min(16, math.ceil(2 * L2_BYTES / max(ab["total"], 1)) + 1))
+    steps = [probe] + [VerifyStep(wl, inp, device=dev) for _ in range(R - 1)]
+    tokens = ab["tokens"]
+
+    # per-kernel events, one pair per kernel per copy
+    ev = [{k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for k in KERNELS}
+          for _ in range(R)]
+    for d in ev:
+        for s, e in d.values():
+            s.record(main)
+            e.record(main)
+    torch.cuda.synchronize()
+
+    # warm-up (eager) then capture one graph per copy
+    with torch.cuda.stream(main):
+        for i in range(max(3, args.warmup // 10)):
+            steps[i % R].run(main, aux)
+    torch.cuda.synchronize()
+    n0 = ssd.launch_count()
+    graphs = []
+    for i in range(R):
+        g = torch.cuda.CUDAGraph()
+        for k in KERNELS:
+            ssd.ssd_profile_kernel(k, *ev[i][k])
+        with torch.cuda.graph(g, stream=main):
+            steps[i].run(main, aux)
+        ssd.ssd_profile_kernel(None)
+        graphs.append(g)
+    launches_per_step = (ssd.launch_count() - n0) // R
+    torch.cuda.synchronize()
+
+    with torch.cuda.stream(main):
+        for i in range(args.warmup):
+            graphs[i % R].replay()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(main):
+        t_start.record(main)
+        for i in range(K):
+            graphs[i % R].replay()
+        t_end.record(main)
+    torch.cuda.synchronize()
+    time.sleep(0.2)
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / K
+    value = world * K / (ms / 1000.0)
+
+    # per-kernel durations over the last replay of each copy's graph
+    kern_us = {}
+    for k in KERNELS:
+        v = [ev[i][k][0].elapsed_time(ev[i][k][1]) * 1000.0 for i in range(R)]
+        v = [x for x in v if x > 0]
+        if v:
+            kern_us[k] = statistics.mean(v)
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(args, wl, inp, steps[0], main, aux, dev)
+
+    hbm, peak_kind = measured_peaks()
+    kb = {"vocab_stats": ab["logits"], "attn_prefix": ab["kv"] + (ab["q_o"] // 2)}
+    dom = max(kb, key=lambda k: kern_us.get(k, 0.0))
+    achieved = kb[dom] / (kern_us[dom] * 1e-6) / 1e9 if kern_us.get(dom) else None
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": (achieved / hbm) if achieved else None, "traffic": dram_traffic(dom, wl.name),
+                "algorithmic_bytes_per_launch": kb[dom], "peak_source": f"{peak_kind} hbm_gbs"}
+    step_bytes = ab["total"]
+    step_roof = {"algorithmic_bytes_per_step": step_bytes,
+                 "achieved_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
+                 "frac_of_measured_hbm": step_bytes / (ms_per_step * 1e-3) / 1e9 / hbm}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        try:
+            res = run_oracle_subprocess(args.workload, args.oracle_seconds)
+            cpu = {"value": res["steps"] / res["seconds"], "unit": UNIT, "cores": 1, "kind": "oracle",
+                   "sample": f"{res['steps']} full oracle steps (same workload, one BLAS thread) in "
+                             f"{res['seconds']:.1f} s", "cpu": cpu_model()}
+        except Exception as e:  # report, do not hide
+            cpu = {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": f"failed: {e}"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+                "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16/f32", "data": "synthetic",
+                "config": workload_config(wl, tokens, {
+                    "l2": f"{R} rotating input copies ({R * step_bytes / 2**20:.0f} MiB > 2x L2); no flush",
+                    "parallelism": f"replicas x{world} (independent batches per GPU)"}),
+                "candidate_tokens_per_s": value * tokens,
+                "hbm_roofline_step": step_roof,
+                "roofline": roofline,
+                "kernels_us": kern_us,
+                "e2e": e2e,
+                "gpu_launches": launches_per_step * K,
+                "clocks": clk,
+                "cpu_baseline": cpu}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, wl, inp, st, main, aux, dev):
+    """Same step through the public API with host inputs: every step copies its
+    inputs host->device (pinned) and reads the emitted tokens back."""
+    import torch
+    from speculative_decoding_copy_gb300.step import to_device  # noqa: F401
+
+    host = {}
+    for k, t in st.x.items():
+        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        h.copy_(t.cpu())
+        host[k] = h
+    out_h = torch.empty(st.acc_out["out_tok"].shape, dtype=torch.int32, pin_memory=True)
+    nout_h = torch.empty(st.acc_out["n_out"].shape, dtype=torch.int32, pin_memory=True)
+    h2d = sum(h.numel() * h.element_size() for h in host.values())
+    d2h = out_h.numel() * 4 + nout_h.numel() * 4
+    E = args.e2e_steps
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(main):
+        for rep in range(2):
+            if rep == 1:
+                torch.cuda.synchronize()
+                s0.record(main)
+            for _ in range(E if rep == 1 else 3):
+                for k, h in host.items():
+                    st.x[k].copy_(h, non_blocking=True)
+                st.run(main, aux)
+                out_h.copy_(st.acc_out["out_tok"], non_blocking=True)
+                nout_h.copy_(st.acc_out["n_out"], non_blocking=True)
+            if rep == 1:
+                s1.record(main)
+    torch.cuda.synchronize()
+    ms = s0.elapsed_time(s1)
+    return {"value": E / (ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": E}
+
+
+def main():
+    args = parse_args()
+    if args.oracle_worker:
+        oracle_worker(args)
+        return
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,264 @@
+/*
+ * ssd.h — C ABI of the GB300 speculate-and-verify step (SwitchSD copy mode +
+ * chain drafts), implemented by libssd.so (hand-written CUDA for sm_103a).
+ *
+ * The step, per sequence of a batch:
+ *   ssd_gate_match   probe score sigma(w.h) >= tau AND an earlier occurrence of
+ *                    the kappa-gram ending at the current token
+ *                    [SwitchSD page, "어떻게 동작하나" (probe p = sigma(w^T H)) and
+ *                     "무엇과 다른가" (copy path needs both conditions)]
+ *   ssd_retrieve     up to W continuations of length D, most recent first,
+ *                    plus an optional chain-draft block of K tokens
+ *                    [SwitchSD page, "무엇과 다른가"]
+ *   ssd_verify_attn  one attention pass for every candidate token under the
+ *                    block-triangular mask: the whole prefix plus the earlier
+ *                    tokens of its own block, never another block
+ *                    [SwitchSD page, "무엇과 다른가"; Speculative Decoding 해부
+ *                     page, §2 Phase 2 (one parallel target pass)]
+ *   ssd_accept       full-vocabulary rows, greedy or rejection-sampling
+ *                    acceptance (accept if u*q(x) < p(x)), residual
+ *                    max(0, p-q) or bonus draw, longest accepted block wins
+ *                    [Speculative Decoding 해부 page, §2 Phase 3, §3.1, §3.2;
+ *                     SwitchSD page, "무엇과 다른가" (longest verified
+ *                     continuation); 추측 디코딩은 왜… page, "2단계 · 일괄 검증"]
+ *
+ * Conventions for every entry point
+ *   - Pointers are DEVICE pointers unless a comment says otherwise. The caller
+ *     owns every buffer; the library allocates nothing and keeps no state
+ *     between calls (beyond per-process kernel attributes set on first use).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Every call is
+ *     asynchronous on that stream and never synchronises, except
+ *     ssd_read_device_error, which is documented as synchronous.
+ *   - Return value: SSD_OK or a negative ssd_status. Arguments are validated on
+ *     the host before any launch; on an error nothing is launched and no output
+ *     is written. SSD_ERR_CUDA means a launch failed (cudaGetLastError).
+ *   - Layouts are dense row-major with the shapes given below.
+ *     NB = number of blocks, Dmax = slots per block, NT = NB * Dmax.
+ *   - Calls are safe from several host threads on distinct streams with
+ *     distinct output and workspace buffers.
+ */
+#ifndef SSD_H
+#define SSD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+enum {
+  SSD_OK = 0,
+  SSD_ERR_INVALID = -1,      /* bad pointer, size or enum value               */
+  SSD_ERR_UNSUPPORTED = -2,  /* valid but not implemented (e.g. head dim 96)  */
+  SSD_ERR_CUDA = -3,         /* a CUDA launch or query failed                 */
+  SSD_ERR_WORKSPACE = -4,    /* workspace NULL, misaligned or too small       */
+  SSD_ERR_TIMEOUT = -5,      /* a device-side wait gave up (device error word) */
+  SSD_ERR_DEVICE = -6        /* a device-side check failed (device error word) */
+};
+
+/* element types */
+enum { SSD_F32 = 0, SSD_BF16 = 1 };
+/* what the vocabulary rows hold */
+enum { SSD_LOGITS_F32 = 0, SSD_LOGITS_BF16 = 1, SSD_PROBS_F32 = 2 };
+/* acceptance rule */
+enum { SSD_GREEDY = 0, SSD_SAMPLE = 1 };
+/* when the chain-draft block is present */
+enum { SSD_CHAIN_NONE = 0, SSD_CHAIN_WHEN_GATE_OFF = 1, SSD_CHAIN_ALWAYS = 2 };
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* ssd_status_string(int status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int ssd_version(void);
+
+/* Number of kernels this process has launched through the library (host
+ * counter, all threads). Kernels replayed from a captured CUDA graph are not
+ * counted again. */
+uint64_t ssd_launch_count(void);
+
+/*
+ * ssd_gate_match — probe gate and kappa-gram check.
+ *
+ * For each sequence b (n = ctx_len[b], the current token is ctx[b][n-1]):
+ *   S_b        = sum_i trunc(h[b][i] * w[i] * 2^32)  (each product exact in
+ *                fp64, summed as int64, so the result does not depend on the
+ *                summation order)
+ *   score[b]   = sigma(S_b * 2^-32)                   (fp32, informative)
+ *   probe_on   = S_b >= ceil(logit(tau) * 2^32), i.e. sigma >= tau; always on
+ *                for tau <= 0, never on for tau >= 1
+ *   last_match_end[b] = the largest j with kappa-1 <= j <= n-2 and
+ *                ctx[b][j-kappa+1 .. j] == ctx[b][n-kappa .. n-1], else -1
+ *                (reported whether or not the probe fires)
+ *   gate[b]    = probe_on AND last_match_end[b] >= 0
+ * Arguments
+ *   ctx [B][ctx_stride] int32, ctx_len [B] int32 (0 <= ctx_len <= ctx_stride)
+ *   h   [B][h_stride] elements of h_dtype (SSD_F32 or SSD_BF16), first d used
+ *   w   [d] fp32
+ *   1 <= kappa <= 64;  B >= 0 (B == 0 launches nothing);  d >= 1
+ *   score [B] fp32, gate [B] int32, last_match_end [B] int32: outputs;
+ *   probe_on [B] int32: optional output (may be NULL)
+ * Requires |h_i * w_i| < 2^31 and |S_b| < 2^63 (not checked).
+ */
+int ssd_gate_match(const int32_t* ctx, int64_t ctx_stride, const int32_t* ctx_len, int B,
+                   const void* h, int h_dtype, int64_t h_stride, const float* w, int d,
+                   float tau, int kappa,
+                   float* score, int32_t* gate, int32_t* last_match_end, int32_t* probe_on,
+                   void* stream);
+
+/*
+ * ssd_retrieve — copy candidates, most recent first, plus the chain block.
+ *
+ * Block layout per sequence: NB = W + (chain_policy != SSD_CHAIN_NONE),
+ * Dmax = chain_policy ? max(D, K) : D. Blocks 0..W-1 are copy candidates:
+ * if gate[b], the k-th largest match end j_k (same definition as
+ * ssd_gate_match) gives blk_tok[b][k][0..len-1] = ctx[b][j_k+1 ..] with
+ * len = min(D, n-1-j_k); up to W of them (n_cand[b] <= W). Block W (if
+ * present) is the chain draft chain_tok[b][0..K-1], present when the gate is
+ * off (SSD_CHAIN_WHEN_GATE_OFF) or always (SSD_CHAIN_ALWAYS). Absent blocks
+ * and unused slots have length 0 and tokens -1.
+ * Arguments
+ *   ctx, ctx_stride, ctx_len, B, kappa: as for ssd_gate_match
+ *   gate [B] int32 (from ssd_gate_match)
+ *   last_match_end [B] int32 or NULL: when given (from ssd_gate_match on the
+ *     same context) the scan starts there instead of at the end
+ *   1 <= W <= 64, 1 <= D <= 256, 0 <= K <= 256 (K >= 1 if chain_policy != 0)
+ *   chain_tok [B][K] int32, may be NULL when chain_policy == SSD_CHAIN_NONE
+ *   blk_tok [B][NB][Dmax], blk_len [B][NB], n_cand [B]: int32 outputs
+ */
+int ssd_retrieve(const int32_t* ctx, int64_t ctx_stride, const int32_t* ctx_len, int B,
+                 const int32_t* gate, const int32_t* last_match_end,
+                 int kappa, int W, int D, int K, int chain_policy, const int32_t* chain_tok,
+                 int32_t* blk_tok, int32_t* blk_len, int32_t* n_cand, void* stream);
+
+/*
+ * ssd_verify_attn — attention of every candidate token over its allowed keys.
+ *
+ * Token d (1-based) of block k of sequence b sits in slot t = k*Dmax + d-1 and
+ * is present iff d <= blk_len[b][k]. For each present token and q-head h
+ * (kv-head h / (Hq/Hkv)):
+ *   out = sum_j softmax_j(scale * q.k_j) v_j over the keys
+ *         {k_cache[b][kvh][0 .. prefix_len[b]-1]} U {k_cand[b][k*Dmax + 0 .. t][kvh]}
+ * Rows of absent tokens are not written.
+ * Layouts (elements of `dtype`; out has the same dtype):
+ *   q, out          [B][NT][Hq][dh]
+ *   k_cache,v_cache [B][Hkv][P_max][dh]      (prefix_len[b] <= P_max)
+ *   k_cand,v_cand   [B][NT][Hkv][dh]
+ *   prefix_len [B] int32, blk_len [B][NB] int32
+ * Supported: dh in {64, 128}; Hq % Hkv == 0; 1 <= Dmax <= 256.
+ * scale == 0 selects 1/sqrt(dh). Accumulation is fp32 whatever `dtype`.
+ * Workspace: ssd_verify_attn_workspace_size(a) bytes, 256-byte aligned; its
+ * contents need no initialisation. Device-side errors are recorded in it.
+ */
+typedef struct {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const void* k_cand;
+  const void* v_cand;
+  void* out;
+  const int32_t* prefix_len;
+  const int32_t* blk_len;
+  int dtype;
+  int B, NB, Dmax, Hq, Hkv, dh;
+  int64_t P_max;
+  float scale;
+} ssd_attn_args;
+
+size_t ssd_verify_attn_workspace_size(const ssd_attn_args* a);
+int ssd_verify_attn(const ssd_attn_args* a, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * ssd_accept — vocabulary rows, acceptance, choice of block, final token.
+ *
+ * Target row 0 is the current position (it predicts token 1 of every block);
+ * row 1 + k*Dmax + (d-1) is the position of token d of block k (it predicts
+ * token d+1, or the bonus after d tokens). Draft row i of drf is the draft
+ * distribution of chain token i+1.
+ *   p = softmax(row) in fp32 (rows given as logits) or the row itself
+ *       (SSD_PROBS_F32); q of a copy block is one-hot on its token; q of the
+ *       chain block is softmax(drf row).
+ *   greedy: token d is accepted iff it equals the argmax of its target row
+ *           (lowest index on ties);
+ *   sample: accepted iff u_acc[b][k][d-1] * q(x) < p(x), compared exactly.
+ *   acc_len[b][k] = leading accepted tokens of block k;
+ *   best_blk[b]   = the present block with the largest acc_len, lowest index
+ *                   on ties (-1 if no block is present);
+ *   out_tok[b][0..a-1] = its accepted tokens; out_tok[b][a] = the final token:
+ *     greedy: argmax of the stop row; sample: an inverse-CDF draw with
+ *     threshold floor(floor(u_fin 2^24) * S / 2^24) over integer weights
+ *     P_i = floor(p_i 2^40): residual max(0, P_i - Q_i) after a rejection (Q
+ *     one-hot 2^40 for a copy block), P_i for the bonus when all tokens of the
+ *     block were accepted, P_i again if the residual is all zero;
+ *   n_out[b] = a + 1; out_tok[b][n_out..Dmax] = -1.
+ * Layouts:
+ *   tgt [B][1 + NB*Dmax][V], drf [B][K][V] (NULL iff chain_blk < 0), of `kind`
+ *   blk_tok [B][NB][Dmax], blk_len [B][NB] (from ssd_retrieve)
+ *   u_acc [B][NB][Dmax] fp32, u_fin [B] fp32, uniforms in [0, 1)
+ *   acc_len [B][NB], best_blk [B], n_out [B], out_tok [B][Dmax+1]: int32 outputs
+ *   probs_out: optional fp32 [B][1 + NB*Dmax][V]; when given, p of every
+ *     needed target row is written there (diagnostics; costs a full write)
+ * Only the rows a present token needs are read. 2 <= V < 2^31; NB*Dmax < 4096;
+ * Dmax <= 256; 0 <= chain_blk < NB or chain_blk == -1.
+ * Workspace: ssd_accept_workspace_size(a) bytes, 256-byte aligned; its
+ * contents need no initialisation. The call may not overlap on the GPU with
+ * another call that uses the same workspace.
+ */
+typedef struct {
+  int mode;
+  int kind;
+  const void* tgt;
+  const void* drf;
+  int64_t V;
+  const int32_t* blk_tok;
+  const int32_t* blk_len;
+  int B, NB, Dmax, K;
+  int chain_blk;
+  const float* u_acc;
+  const float* u_fin;
+  int32_t* acc_len;
+  int32_t* best_blk;
+  int32_t* n_out;
+  int32_t* out_tok;
+  float* probs_out;
+} ssd_accept_args;
+
+size_t ssd_accept_workspace_size(const ssd_accept_args* a);
+int ssd_accept(const ssd_accept_args* a, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * ssd_read_device_error — SYNCHRONOUS: waits for `stream`, then reads and
+ * clears the device error word at the head of a workspace used by
+ * ssd_verify_attn or ssd_accept. *out receives SSD_OK, SSD_ERR_TIMEOUT or
+ * SSD_ERR_DEVICE. `ws` is a device pointer; `out` a host pointer.
+ */
+int ssd_read_device_error(void* ws, void* stream, int32_t* out);
+
+/*
+ * ssd_profile_kernel — measurement hook (no counterpart on the pages).
+ * From now on every launch of kernel `kernel_id` (SSD_KERNEL_*) is bracketed
+ * by cudaEventRecord(start_event) / cudaEventRecord(end_event) on the stream
+ * the kernel is launched on (as external event nodes while that stream is
+ * being captured into a CUDA graph). Each kernel id has its own pair; calling
+ * again replaces it. kernel_id 0 (events ignored) switches every hook off.
+ * The events are cudaEvent_t handles owned by the caller and must stay valid
+ * while hooked. Process-wide; not thread-safe against concurrent launches.
+ */
+enum {
+  SSD_KERNEL_NONE = 0,
+  SSD_KERNEL_VOCAB_STATS = 1,
+  SSD_KERNEL_ATTN_PREFIX = 2,
+  SSD_KERNEL_ATTN_COMBINE = 3,
+  SSD_KERNEL_ACCEPT_SELECT = 4,
+  SSD_KERNEL_SAMPLE_FINAL = 5,
+  SSD_KERNEL_GATE_MATCH = 6,
+  SSD_KERNEL_RETRIEVE = 7
+};
+int ssd_profile_kernel(int kernel_id, void* start_event, void* end_event);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_H */

@@ -1,0 +1,264 @@
+"""ctypes binding of libssd.so: argument marshalling only.
+
+Every function takes CUDA torch tensors (torch is used for device memory and
+streams only), checks shapes and dtypes, allocates missing outputs with torch
+and calls the C entry point of the same name on the current (or given) stream.
+All arithmetic happens in the library's kernels. If the library has not been
+built, every call raises; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import POINTER, c_float, c_int, c_int32, c_int64, c_size_t, c_uint64, c_void_p
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libssd.so")
+
+SSD_OK, SSD_ERR_INVALID, SSD_ERR_UNSUPPORTED, SSD_ERR_CUDA, SSD_ERR_WORKSPACE, SSD_ERR_TIMEOUT, SSD_ERR_DEVICE = (
+    0, -1, -2, -3, -4, -5, -6)
+SSD_F32, SSD_BF16 = 0, 1
+SSD_LOGITS_F32, SSD_LOGITS_BF16, SSD_PROBS_F32 = 0, 1, 2
+SSD_GREEDY, SSD_SAMPLE = 0, 1
+SSD_CHAIN_NONE, SSD_CHAIN_WHEN_GATE_OFF, SSD_CHAIN_ALWAYS = 0, 1, 2
+
+EXPORTED = ["ssd_status_string", "ssd_version", "ssd_launch_count", "ssd_gate_match", "ssd_retrieve",
+            "ssd_verify_attn_workspace_size", "ssd_verify_attn", "ssd_accept_workspace_size", "ssd_accept",
+            "ssd_read_device_error", "ssd_profile_kernel"]
+SSD_KERNEL = dict(vocab_stats=1, attn_prefix=2, attn_combine=3, accept_select=4, sample_final=5, gate_match=6,
+                  retrieve=7)
+
+
+class SsdError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn}: {status_string(status)} ({status})")
+        self.status = status
+
+
+class AttnArgs(ctypes.Structure):
+    _fields_ = [("q", c_void_p), ("k_cache", c_void_p), ("v_cache", c_void_p), ("k_cand", c_void_p),
+                ("v_cand", c_void_p), ("out", c_void_p), ("prefix_len", c_void_p), ("blk_len", c_void_p),
+                ("dtype", c_int), ("B", c_int), ("NB", c_int), ("Dmax", c_int), ("Hq", c_int), ("Hkv", c_int),
+                ("dh", c_int), ("P_max", c_int64), ("scale", c_float)]
+
+
+class AcceptArgs(ctypes.Structure):
+    _fields_ = [("mode", c_int), ("kind", c_int), ("tgt", c_void_p), ("drf", c_void_p), ("V", c_int64),
+                ("blk_tok", c_void_p), ("blk_len", c_void_p), ("B", c_int), ("NB", c_int), ("Dmax", c_int),
+                ("K", c_int), ("chain_blk", c_int), ("u_acc", c_void_p), ("u_fin", c_void_p),
+                ("acc_len", c_void_p), ("best_blk", c_void_p), ("n_out", c_void_p), ("out_tok", c_void_p),
+                ("probs_out", c_void_p)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libssd.so (once). Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with speculative_decoding_copy_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        L.ssd_status_string.restype = ctypes.c_char_p
+        L.ssd_status_string.argtypes = [c_int]
+        L.ssd_version.restype = c_int
+        L.ssd_launch_count.restype = c_uint64
+        L.ssd_gate_match.restype = c_int
+        L.ssd_gate_match.argtypes = [c_void_p, c_int64, c_void_p, c_int, c_void_p, c_int, c_int64, c_void_p, c_int,
+                                     c_float, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
+        L.ssd_retrieve.restype = c_int
+        L.ssd_retrieve.argtypes = [c_void_p, c_int64, c_void_p, c_int, c_void_p, c_void_p, c_int, c_int, c_int,
+                                   c_int, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
+        L.ssd_verify_attn_workspace_size.restype = c_size_t
+        L.ssd_verify_attn_workspace_size.argtypes = [POINTER(AttnArgs)]
+        L.ssd_verify_attn.restype = c_int
+        L.ssd_verify_attn.argtypes = [POINTER(AttnArgs), c_void_p, c_size_t, c_void_p]
+        L.ssd_accept_workspace_size.restype = c_size_t
+        L.ssd_accept_workspace_size.argtypes = [POINTER(AcceptArgs)]
+        L.ssd_accept.restype = c_int
+        L.ssd_accept.argtypes = [POINTER(AcceptArgs), c_void_p, c_size_t, c_void_p]
+        L.ssd_read_device_error.restype = c_int
+        L.ssd_read_device_error.argtypes = [c_void_p, c_void_p, POINTER(c_int32)]
+        L.ssd_profile_kernel.restype = c_int
+        L.ssd_profile_kernel.argtypes = [c_int, c_void_p, c_void_p]
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().ssd_status_string(int(status)).decode()
+
+
+def launch_count() -> int:
+    return int(lib().ssd_launch_count())
+
+
+def _check(fn: str, rc: int):
+    if rc != SSD_OK:
+        raise SsdError(fn, rc)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, name, dtypes, ndim=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+
+
+_HALF = (torch.bfloat16, torch.int16)
+
+
+def _elem_type(t) -> int:
+    return SSD_F32 if t.dtype == torch.float32 else SSD_BF16
+
+
+def _empty_like_dtype(shape, like, dtype=None):
+    return torch.empty(shape, dtype=dtype or like.dtype, device=like.device)
+
+
+# ---------------------------------------------------------------------------
+def ssd_gate_match(ctx, ctx_len, h, w, tau, kappa, *, out=None, stream=None):
+    """Probe gate and kappa-gram check; returns dict(score, gate, last_match_end, probe_on)."""
+    _need(ctx, "ctx", (torch.int32,), 2)
+    _need(ctx_len, "ctx_len", (torch.int32,), 1)
+    _need(h, "h", (torch.float32,) + _HALF, 2)
+    _need(w, "w", (torch.float32,), 1)
+    B = ctx.shape[0]
+    d = w.shape[0]
+    o = out or {}
+    score = o.get("score") if o.get("score") is not None else _empty_like_dtype((B,), ctx, torch.float32)
+    gate = o.get("gate") if o.get("gate") is not None else _empty_like_dtype((B,), ctx)
+    last = o.get("last_match_end") if o.get("last_match_end") is not None else _empty_like_dtype((B,), ctx)
+    on = o.get("probe_on") if o.get("probe_on") is not None else _empty_like_dtype((B,), ctx)
+    rc = lib().ssd_gate_match(_ptr(ctx), ctx.shape[1], _ptr(ctx_len), B, _ptr(h), _elem_type(h), h.shape[1],
+                              _ptr(w), d, float(tau), int(kappa), _ptr(score), _ptr(gate), _ptr(last), _ptr(on),
+                              _stream(stream))
+    _check("ssd_gate_match", rc)
+    return dict(score=score, gate=gate, last_match_end=last, probe_on=on)
+
+
+def ssd_retrieve(ctx, ctx_len, gate, last_match_end, kappa, W, D, K, chain_policy, chain_tok=None, *,
+                 out=None, stream=None):
+    """Copy candidates (most recent first) and the chain block; returns dict(blk_tok, blk_len, n_cand)."""
+    _need(ctx, "ctx", (torch.int32,), 2)
+    _need(gate, "gate", (torch.int32,), 1)
+    B = ctx.shape[0]
+    NB = W + (1 if chain_policy else 0)
+    Dmax = max(D, K) if chain_policy else D
+    o = out or {}
+    blk_tok = o.get("blk_tok") if o.get("blk_tok") is not None else _empty_like_dtype((B, NB, Dmax), ctx)
+    blk_len = o.get("blk_len") if o.get("blk_len") is not None else _empty_like_dtype((B, NB), ctx)
+    n_cand = o.get("n_cand") if o.get("n_cand") is not None else _empty_like_dtype((B,), ctx)
+    if chain_tok is not None:
+        _need(chain_tok, "chain_tok", (torch.int32,), 2)
+    rc = lib().ssd_retrieve(_ptr(ctx), ctx.shape[1], _ptr(ctx_len), B, _ptr(gate), _ptr(last_match_end),
+                            int(kappa), int(W), int(D), int(K), int(chain_policy), _ptr(chain_tok), _ptr(blk_tok),
+                            _ptr(blk_len), _ptr(n_cand), _stream(stream))
+    _check("ssd_retrieve", rc)
+    return dict(blk_tok=blk_tok, blk_len=blk_len, n_cand=n_cand)
+
+
+def attn_args(q, k_cache, v_cache, k_cand, v_cand, prefix_len, blk_len, Dmax, out, scale=0.0) -> AttnArgs:
+    B, NT, Hq, dh = q.shape
+    Hkv = k_cache.shape[1]
+    NB = blk_len.shape[1]
+    return AttnArgs(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_cand), _ptr(v_cand), _ptr(out),
+                    _ptr(prefix_len), _ptr(blk_len), _elem_type(q), B, NB, int(Dmax), Hq, Hkv, dh,
+                    k_cache.shape[2], float(scale))
+
+
+def ssd_verify_attn_workspace_size(args: AttnArgs) -> int:
+    return int(lib().ssd_verify_attn_workspace_size(ctypes.byref(args)))
+
+
+def ssd_verify_attn(q, k_cache, v_cache, k_cand, v_cand, prefix_len, blk_len, Dmax, *, out=None, ws=None,
+                    scale=0.0, stream=None):
+    """Block-triangular verification attention; returns the output tensor [B][NT][Hq][dh]."""
+    types = (torch.float32,) + _HALF
+    for n, t in [("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("k_cand", k_cand), ("v_cand", v_cand)]:
+        _need(t, n, types, 4)
+        if _elem_type(t) != _elem_type(q):
+            raise ValueError("all attention tensors must share one dtype")
+    _need(prefix_len, "prefix_len", (torch.int32,), 1)
+    _need(blk_len, "blk_len", (torch.int32,), 2)
+    if out is None:
+        out = torch.empty_like(q)
+    args = attn_args(q, k_cache, v_cache, k_cand, v_cand, prefix_len, blk_len, Dmax, out, scale)
+    need = ssd_verify_attn_workspace_size(args)
+    if ws is None:
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    rc = lib().ssd_verify_attn(ctypes.byref(args), _ptr(ws), ws.numel(), _stream(stream))
+    _check("ssd_verify_attn", rc)
+    return out
+
+
+def accept_args(mode, kind, tgt, drf, blk_tok, blk_len, K, chain_blk, u_acc, u_fin, outs, probs_out=None):
+    B, NR, V = tgt.shape
+    _, NB, Dmax = blk_tok.shape
+    return AcceptArgs(int(mode), int(kind), _ptr(tgt), _ptr(drf), V, _ptr(blk_tok), _ptr(blk_len), B, NB, Dmax,
+                      int(K), int(chain_blk), _ptr(u_acc), _ptr(u_fin), _ptr(outs["acc_len"]),
+                      _ptr(outs["best_blk"]), _ptr(outs["n_out"]), _ptr(outs["out_tok"]), _ptr(probs_out))
+
+
+def ssd_accept_workspace_size(args: AcceptArgs) -> int:
+    return int(lib().ssd_accept_workspace_size(ctypes.byref(args)))
+
+
+def alloc_accept_outputs(B, NB, Dmax, device):
+    z = lambda *s: torch.empty(s, dtype=torch.int32, device=device)
+    return dict(acc_len=z(B, NB), best_blk=z(B), n_out=z(B), out_tok=z(B, Dmax + 1))
+
+
+def ssd_accept(tgt, drf, blk_tok, blk_len, u_acc, u_fin, *, mode, kind, K=0, chain_blk=-1, out=None, ws=None,
+               probs_out=None, stream=None):
+    """Acceptance, choice of block and final token; returns dict(acc_len, best_blk, n_out, out_tok)."""
+    _need(tgt, "tgt", (torch.float32,) + _HALF, 3)
+    if drf is not None:
+        _need(drf, "drf", (tgt.dtype,), 3)
+    _need(blk_tok, "blk_tok", (torch.int32,), 3)
+    _need(blk_len, "blk_len", (torch.int32,), 2)
+    B, NR, V = tgt.shape
+    _, NB, Dmax = blk_tok.shape
+    outs = out or alloc_accept_outputs(B, NB, Dmax, tgt.device)
+    args = accept_args(mode, kind, tgt, drf, blk_tok, blk_len, K, chain_blk, u_acc, u_fin, outs, probs_out)
+    need = ssd_accept_workspace_size(args)
+    if ws is None:
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=tgt.device)
+    rc = lib().ssd_accept(ctypes.byref(args), _ptr(ws), ws.numel(), _stream(stream))
+    _check("ssd_accept", rc)
+    return outs
+
+
+def ssd_read_device_error(ws, stream=None) -> int:
+    v = c_int32(0)
+    rc = lib().ssd_read_device_error(_ptr(ws), _stream(stream), ctypes.byref(v))
+    _check("ssd_read_device_error", rc)
+    return int(v.value)
+
+
+def ssd_profile_kernel(kernel: str | None, start=None, end=None):
+    """Bracket every later launch of `kernel` with the given torch.cuda.Events
+    (created with enable_timing=True); None switches the hook off."""
+    if kernel is None:
+        _check("ssd_profile_kernel", lib().ssd_profile_kernel(0, None, None))
+        return
+    for ev in (start, end):
+        if ev.cuda_event == 0:     # torch creates the CUDA event lazily
+            ev.record()
+    rc = lib().ssd_profile_kernel(SSD_KERNEL[kernel], ctypes.c_void_p(start.cuda_event), ctypes.c_void_p(end.cuda_event))
+    _check("ssd_profile_kernel", rc)

@@ -1,0 +1,54 @@
+// Library-wide entry points: status strings, version, launch counter and the
+// device error word.
+#include "ssd_common.cuh"
+
+extern "C" const char* ssd_status_string(int status) {
+  switch (status) {
+    case SSD_OK: return "ok";
+    case SSD_ERR_INVALID: return "invalid argument";
+    case SSD_ERR_UNSUPPORTED: return "unsupported shape or type";
+    case SSD_ERR_CUDA: return "CUDA error";
+    case SSD_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case SSD_ERR_TIMEOUT: return "device-side wait timed out";
+    case SSD_ERR_DEVICE: return "device-side check failed";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int ssd_version(void) { return 100; }
+
+namespace ssd {
+ProfileHook g_profile;
+}
+
+extern "C" int ssd_profile_kernel(int kernel_id, void* start_event, void* end_event) {
+  using ssd::g_profile;
+  if (kernel_id < SSD_KERNEL_NONE || kernel_id > SSD_KERNEL_RETRIEVE) return SSD_ERR_INVALID;
+  if (kernel_id == SSD_KERNEL_NONE) {
+    for (int i = 0; i < ssd::kProfileSlots; ++i) g_profile.on[i].store(0);
+    return SSD_OK;
+  }
+  if (start_event == nullptr || end_event == nullptr) return SSD_ERR_INVALID;
+  g_profile.on[kernel_id].store(0);
+  g_profile.start[kernel_id] = static_cast<cudaEvent_t>(start_event);
+  g_profile.end[kernel_id] = static_cast<cudaEvent_t>(end_event);
+  g_profile.on[kernel_id].store(1);
+  return SSD_OK;
+}
+
+extern "C" uint64_t ssd_launch_count(void) { return ssd::g_launches.load(std::memory_order_relaxed); }
+
+extern "C" int ssd_read_device_error(void* ws, void* stream, int32_t* out) {
+  if (ws == nullptr || out == nullptr) return SSD_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t host[2] = {0, 0};
+  if (cudaMemcpyAsync(host, ws, sizeof(host), cudaMemcpyDeviceToHost, s) != cudaSuccess) return SSD_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SSD_ERR_CUDA;
+  const int32_t zero[2] = {0, 0};
+  if (host[0] != 0) {
+    if (cudaMemcpyAsync(ws, zero, sizeof(zero), cudaMemcpyHostToDevice, s) != cudaSuccess) return SSD_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SSD_ERR_CUDA;
+  }
+  *out = host[0];
+  return SSD_OK;
+}

@@ -1,0 +1,326 @@
+// Verification attention under the block-triangular mask.
+//
+// SwitchSD page, "무엇과 다른가": all W candidates are verified in one target
+// pass; a candidate token attends to the whole prefix and to the earlier tokens
+// of its own candidate, never to another candidate. A chain draft is one block
+// under the ordinary causal mask (Speculative Decoding 해부 page, §2 Phase 2).
+//
+// The work splits into a dense part (every token of a sequence sees the same
+// prefix keys, so q-heads of one kv head and all candidate tokens pack into
+// the rows of one matrix product against each prefix tile) and a tiny masked
+// part (at most Dmax own-block keys per token). Two kernels:
+//   prefix partial: split-KV flash pass over the prefix; per (row, split) it
+//                   leaves the running max m, sum l and un-normalised o
+//                   (log2 units) in the workspace;
+//   combine:        one warp per row merges the splits, adds the row's own
+//                   block keys, normalises and stores the output.
+// bf16 inputs use the tcgen05 prefix kernel (ssd_attn_tc.cu) when it applies;
+// the SIMT prefix kernel below serves fp32 and every other shape.
+#include <math.h>
+
+#include "ssd_attn.cuh"
+
+namespace ssd {
+
+std::atomic<uint64_t> g_launches{0};
+
+constexpr int kSimtThreads = 128;
+constexpr int kSimtRowsPerWarp = 2;
+constexpr int kSimtRows = (kSimtThreads / 32) * kSimtRowsPerWarp;   // 8 packed rows per CTA
+constexpr int kKeyTile = 32;
+
+template <typename T>
+__device__ __forceinline__ float ld_elem(const T* p, int64_t i);
+template <>
+__device__ __forceinline__ float ld_elem<float>(const float* p, int64_t i) { return __ldg(p + i); }
+template <>
+__device__ __forceinline__ float ld_elem<uint16_t>(const uint16_t* p, int64_t i) { return bf16_to_f32(__ldg(p + i)); }
+
+template <typename T>
+__device__ __forceinline__ void st_elem(T* p, int64_t i, float v);
+template <>
+__device__ __forceinline__ void st_elem<float>(float* p, int64_t i, float v) { p[i] = v; }
+template <>
+__device__ __forceinline__ void st_elem<uint16_t>(uint16_t* p, int64_t i, float v) { p[i] = f32_to_bf16(v); }
+
+__device__ __forceinline__ bool token_present(const int32_t* blk_len, int b, int NB, int Dmax, int t) {
+  const int k = t / Dmax, pos = t % Dmax;
+  return pos < blk_len[b * NB + k];
+}
+
+// grid (S, ceil(NT*G / 8), B*Hkv), block 128
+template <typename T, int DH>
+__global__ void __launch_bounds__(kSimtThreads)
+k_attn_prefix_simt(AttnParams p) {
+  constexpr int EPL = DH / 32;   // output dims per lane
+  __shared__ float q_s[kSimtRows][DH];
+  __shared__ float k_s[kKeyTile][DH + 1];
+  __shared__ float v_s[kKeyTile][DH];
+
+  const int split = blockIdx.x;
+  const int bk = blockIdx.z;
+  const int b = bk / p.Hkv, kvh = bk % p.Hkv;
+  const int G = p.Hq / p.Hkv;
+  const int NT = p.NB * p.Dmax;
+  const int rows_total = NT * G;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int P = p.prefix_len[b];
+  const int k0 = split * p.chunk;
+  const int k1 = min(P, k0 + p.chunk);
+
+  const T* q = static_cast<const T*>(p.q);
+  const T* kc = static_cast<const T*>(p.k_cache) + (static_cast<int64_t>(b) * p.Hkv + kvh) * p.P_max * DH;
+  const T* vc = static_cast<const T*>(p.v_cache) + (static_cast<int64_t>(b) * p.Hkv + kvh) * p.P_max * DH;
+
+  // stage the CTA's q rows, pre-scaled into log2 units
+  const int r_base = blockIdx.y * kSimtRows;
+  for (int i = tid; i < kSimtRows * DH; i += kSimtThreads) {
+    const int rr = i / DH, e = i % DH;
+    const int r = r_base + rr;
+    float v = 0.f;
+    if (r < rows_total) {
+      const int t = r / G, h = kvh * G + r % G;
+      v = ld_elem(q, ((static_cast<int64_t>(b) * NT + t) * p.Hq + h) * DH + e) * p.scale_log2;
+    }
+    q_s[rr][e] = v;
+  }
+
+  float m[kSimtRowsPerWarp], l[kSimtRowsPerWarp], o[kSimtRowsPerWarp][EPL];
+#pragma unroll
+  for (int j = 0; j < kSimtRowsPerWarp; ++j) {
+    m[j] = -INFINITY;
+    l[j] = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) o[j][e] = 0.f;
+  }
+
+  for (int kt = k0; kt < k1; kt += kKeyTile) {
+    __syncthreads();
+    for (int i = tid; i < kKeyTile * DH; i += kSimtThreads) {
+      const int kk = i / DH, e = i % DH;
+      const int key = kt + kk;
+      float kv = 0.f, vv = 0.f;
+      if (key < k1) {
+        kv = ld_elem(kc, static_cast<int64_t>(key) * DH + e);
+        vv = ld_elem(vc, static_cast<int64_t>(key) * DH + e);
+      }
+      k_s[kk][e] = kv;
+      v_s[kk][e] = vv;
+    }
+    __syncthreads();
+    const bool key_ok = (kt + lane) < k1;
+#pragma unroll
+    for (int j = 0; j < kSimtRowsPerWarp; ++j) {
+      const float* qr = q_s[wid * kSimtRowsPerWarp + j];
+      float s = 0.f;
+#pragma unroll 8
+      for (int e = 0; e < DH; ++e) s = fmaf(qr[e], k_s[lane][e], s);
+      s = key_ok ? s : -INFINITY;
+      const float m_new = fmaxf(m[j], warp_max(s));
+      const float corr = exp2f(m[j] - m_new);          // m = -inf -> 0
+      const float pj = exp2f(s - m_new);
+      l[j] = l[j] * corr + warp_sum(pj);
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) o[j][e] *= corr;
+      for (int kk = 0; kk < kKeyTile; ++kk) {
+        const float pk = __shfl_sync(0xffffffffu, pj, kk);
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) o[j][e] = fmaf(pk, v_s[kk][lane + 32 * e], o[j][e]);
+      }
+      m[j] = m_new;
+    }
+  }
+
+  // leave (m, l, o) for every packed row of a present token
+#pragma unroll
+  for (int j = 0; j < kSimtRowsPerWarp; ++j) {
+    const int r = r_base + wid * kSimtRowsPerWarp + j;
+    if (r >= rows_total) continue;
+    const int t = r / G, h = kvh * G + r % G;
+    if (!token_present(p.blk_len, b, p.NB, p.Dmax, t)) continue;
+    const int64_t R = (static_cast<int64_t>(b) * NT + t) * p.Hq + h;
+    float* ml = p.ws_ml + (R * p.S + split) * 2;
+    float* ow = p.ws_o + (R * p.S + split) * DH;
+    if (lane == 0) {
+      ml[0] = m[j];
+      ml[1] = l[j];
+    }
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) ow[lane + 32 * e] = o[j][e];
+  }
+}
+
+// one warp per (b, t, h); grid ceil(B*NT*Hq / 4), block 128
+template <typename T, int DH>
+__global__ void __launch_bounds__(128)
+k_attn_combine(AttnParams p) {
+  constexpr int EPL = DH / 32;
+  __shared__ float sc_s[4][256];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int NT = p.NB * p.Dmax;
+  const int64_t R = static_cast<int64_t>(blockIdx.x) * 4 + wid;
+  if (R >= static_cast<int64_t>(p.B) * NT * p.Hq) return;
+  const int h = static_cast<int>(R % p.Hq);
+  const int t = static_cast<int>((R / p.Hq) % NT);
+  const int b = static_cast<int>(R / (static_cast<int64_t>(p.Hq) * NT));
+  if (!token_present(p.blk_len, b, p.NB, p.Dmax, t)) return;
+  const int G = p.Hq / p.Hkv;
+  const int kvh = h / G;
+  const int k = t / p.Dmax, pos = t % p.Dmax;
+
+  const T* q = static_cast<const T*>(p.q) + R * DH;
+  float qv[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) qv[e] = ld_elem(q, lane + 32 * e) * p.scale_log2;
+
+  // own-block keys: slots k*Dmax .. t
+  const T* kd = static_cast<const T*>(p.k_cand);
+  const T* vd = static_cast<const T*>(p.v_cand);
+  float M = -INFINITY;
+  for (int c = 0; c <= pos; ++c) {
+    const int64_t base = ((static_cast<int64_t>(b) * NT + k * p.Dmax + c) * p.Hkv + kvh) * DH;
+    float s = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) s = fmaf(qv[e], ld_elem(kd, base + lane + 32 * e), s);
+    s = warp_sum(s);
+    if (lane == 0) sc_s[wid][c] = s;
+    M = fmaxf(M, s);
+  }
+  const float* ml = p.ws_ml + R * p.S * 2;
+  for (int s = 0; s < p.S; ++s) M = fmaxf(M, ml[2 * s]);
+  __syncwarp();
+
+  float L = 0.f, O[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) O[e] = 0.f;
+  const float* ow = p.ws_o + R * p.S * DH;
+  for (int s = 0; s < p.S; ++s) {
+    const float ms = ml[2 * s];
+    if (ms == -INFINITY) continue;
+    const float f = exp2f(ms - M);
+    L += ml[2 * s + 1] * f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) O[e] = fmaf(f, ow[s * DH + lane + 32 * e], O[e]);
+  }
+  for (int c = 0; c <= pos; ++c) {
+    const float f = exp2f(sc_s[wid][c] - M);
+    L += f;
+    const int64_t base = ((static_cast<int64_t>(b) * NT + k * p.Dmax + c) * p.Hkv + kvh) * DH;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) O[e] = fmaf(f, ld_elem(vd, base + lane + 32 * e), O[e]);
+  }
+  const float inv = 1.f / L;
+  T* out = static_cast<T*>(p.out) + R * DH;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) st_elem(out, lane + 32 * e, O[e] * inv);
+}
+
+// ---------------------------------------------------------------- host
+static int choose_splits(const ssd_attn_args* a, int* chunk_out) {
+  const int NT = a->NB * a->Dmax;
+  const int G = a->Hq / a->Hkv;
+  const long long rowgrps = (static_cast<long long>(NT) * G + kSimtRows - 1) / kSimtRows;
+  const long long ctas = rowgrps * a->B * a->Hkv;
+  const long long P = a->P_max > 0 ? a->P_max : 1;
+  long long S = (8LL * 152 + ctas - 1) / ctas;
+  const long long S_cap = (P + kKeyTile - 1) / kKeyTile;
+  if (S > S_cap) S = S_cap;
+  if (S > 64) S = 64;
+  if (S < 1) S = 1;
+  long long chunk = (P + S - 1) / S;
+  chunk = (chunk + kKeyTile - 1) / kKeyTile * kKeyTile;
+  S = (P + chunk - 1) / chunk;
+  if (S < 1) S = 1;
+  *chunk_out = static_cast<int>(chunk);
+  return static_cast<int>(S);
+}
+
+static int validate(const ssd_attn_args* a) {
+  if (a == nullptr) return SSD_ERR_INVALID;
+  if (a->B < 0 || a->NB < 1 || a->Dmax < 1 || a->Hq < 1 || a->Hkv < 1 || a->P_max < 0) return SSD_ERR_INVALID;
+  if (a->dtype != SSD_F32 && a->dtype != SSD_BF16) return SSD_ERR_INVALID;
+  if (a->Hq % a->Hkv != 0) return SSD_ERR_INVALID;
+  if (a->Dmax > 256) return SSD_ERR_UNSUPPORTED;
+  if (a->dh != 64 && a->dh != 128) return SSD_ERR_UNSUPPORTED;
+  if (a->P_max > (1LL << 30)) return SSD_ERR_UNSUPPORTED;
+  if (a->B == 0) return SSD_OK;
+  if (!a->q || !a->k_cand || !a->v_cand || !a->out || !a->prefix_len || !a->blk_len) return SSD_ERR_INVALID;
+  if (a->P_max > 0 && (!a->k_cache || !a->v_cache)) return SSD_ERR_INVALID;
+  return SSD_OK;
+}
+
+struct AttnLayout {
+  size_t ml_off, o_off, total;
+  int S, chunk;
+};
+
+static AttnLayout attn_layout(const ssd_attn_args* a) {
+  AttnLayout L{};
+  L.S = choose_splits(a, &L.chunk);
+  const size_t R = static_cast<size_t>(a->B) * a->NB * a->Dmax * a->Hq;
+  L.ml_off = sizeof(WsHeader);
+  L.o_off = round_up(L.ml_off + R * L.S * 2 * sizeof(float), 256);
+  L.total = round_up(L.o_off + R * L.S * a->dh * sizeof(float), 256);
+  return L;
+}
+
+}  // namespace ssd
+
+using namespace ssd;
+
+extern "C" size_t ssd_verify_attn_workspace_size(const ssd_attn_args* a) {
+  if (validate(a) != SSD_OK) return 0;
+  if (a->B == 0) return sizeof(WsHeader);
+  size_t s = attn_layout(a).total;
+  size_t t = attn_tc_workspace_size(a);
+  return s > t ? s : t;
+}
+
+extern "C" int ssd_verify_attn(const ssd_attn_args* a, void* ws, size_t ws_bytes, void* stream) {
+  int st = validate(a);
+  if (st != SSD_OK) return st;
+  if (a->B == 0) return SSD_OK;
+  if (ws == nullptr || !aligned(ws, 256)) return SSD_ERR_WORKSPACE;
+  if (ws_bytes < ssd_verify_attn_workspace_size(a)) return SSD_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  if (attn_tc_applies(a)) return attn_tc_launch(a, ws, s);
+
+  const AttnLayout L = attn_layout(a);
+  AttnParams p{};
+  p.q = a->q; p.k_cache = a->k_cache; p.v_cache = a->v_cache; p.k_cand = a->k_cand; p.v_cand = a->v_cand;
+  p.out = a->out; p.prefix_len = a->prefix_len; p.blk_len = a->blk_len;
+  p.B = a->B; p.NB = a->NB; p.Dmax = a->Dmax; p.Hq = a->Hq; p.Hkv = a->Hkv; p.P_max = a->P_max;
+  const float scale = a->scale != 0.f ? a->scale : 1.f / sqrtf(static_cast<float>(a->dh));
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.S = L.S; p.chunk = L.chunk;
+  char* base = static_cast<char*>(ws);
+  p.hdr = reinterpret_cast<WsHeader*>(base);
+  p.ws_ml = reinterpret_cast<float*>(base + L.ml_off);
+  p.ws_o = reinterpret_cast<float*>(base + L.o_off);
+
+  const int NT = a->NB * a->Dmax;
+  const int G = a->Hq / a->Hkv;
+  dim3 g1(L.S, (NT * G + kSimtRows - 1) / kSimtRows, a->B * a->Hkv);
+  const long long rows = static_cast<long long>(a->B) * NT * a->Hq;
+  dim3 g2(static_cast<unsigned>((rows + 3) / 4));
+  if (a->dtype == SSD_F32) {
+    if (a->dh == 64) {
+      { KernelTimer t(SSD_KERNEL_ATTN_PREFIX, s); k_attn_prefix_simt<float, 64><<<g1, kSimtThreads, 0, s>>>(p); }
+      { KernelTimer t(SSD_KERNEL_ATTN_COMBINE, s); k_attn_combine<float, 64><<<g2, 128, 0, s>>>(p); }
+    } else {
+      { KernelTimer t(SSD_KERNEL_ATTN_PREFIX, s); k_attn_prefix_simt<float, 128><<<g1, kSimtThreads, 0, s>>>(p); }
+      { KernelTimer t(SSD_KERNEL_ATTN_COMBINE, s); k_attn_combine<float, 128><<<g2, 128, 0, s>>>(p); }
+    }
+  } else {
+    if (a->dh == 64) {
+      { KernelTimer t(SSD_KERNEL_ATTN_PREFIX, s); k_attn_prefix_simt<uint16_t, 64><<<g1, kSimtThreads, 0, s>>>(p); }
+      { KernelTimer t(SSD_KERNEL_ATTN_COMBINE, s); k_attn_combine<uint16_t, 64><<<g2, 128, 0, s>>>(p); }
+    } else {
+      { KernelTimer t(SSD_KERNEL_ATTN_PREFIX, s); k_attn_prefix_simt<uint16_t, 128><<<g1, kSimtThreads, 0, s>>>(p); }
+      { KernelTimer t(SSD_KERNEL_ATTN_COMBINE, s); k_attn_combine<uint16_t, 128><<<g2, 128, 0, s>>>(p); }
+    }
+  }
+  count_launch(2);
+  return check_launch();
+}

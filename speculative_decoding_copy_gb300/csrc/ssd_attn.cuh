@@ -1,0 +1,31 @@
+// Internal interface between the attention host code and its kernels.
+#pragma once
+
+#include "ssd_common.cuh"
+
+namespace ssd {
+
+struct AttnParams {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const void* k_cand;
+  const void* v_cand;
+  void* out;
+  const int32_t* prefix_len;
+  const int32_t* blk_len;
+  int B, NB, Dmax, Hq, Hkv;
+  int64_t P_max;
+  float scale_log2;      // softmax scale times log2(e): scores are kept in log2 units
+  int S, chunk;          // KV splits and keys per split
+  WsHeader* hdr;
+  float* ws_ml;          // [rows][S][2]  running max and sum per split
+  float* ws_o;           // [rows][S][dh] un-normalised output per split
+};
+
+// tcgen05 prefix path (ssd_attn_tc.cu)
+bool attn_tc_applies(const ssd_attn_args* a);
+size_t attn_tc_workspace_size(const ssd_attn_args* a);
+int attn_tc_launch(const ssd_attn_args* a, void* ws, cudaStream_t s);
+
+}  // namespace ssd

@@ -1,0 +1,94 @@
+// Shared device/host helpers of libssd (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "ssd.h"
+
+namespace ssd {
+
+// ---------------------------------------------------------------- host side
+extern std::atomic<uint64_t> g_launches;
+
+inline void count_launch(uint64_t n = 1) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+inline int check_launch() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+// measurement hook: events recorded around chosen kernels (ssd_profile_kernel)
+constexpr int kProfileSlots = 8;
+struct ProfileHook {
+  std::atomic<int> on[kProfileSlots];
+  cudaEvent_t start[kProfileSlots];
+  cudaEvent_t end[kProfileSlots];
+};
+extern ProfileHook g_profile;
+
+inline void record_hook_event(cudaEvent_t ev, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(s, &cs);
+  if (cs == cudaStreamCaptureStatusActive) cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+  else cudaEventRecord(ev, s);
+}
+
+// RAII bracket: records the kernel's start event on construction and its end
+// event on destruction while kernel `id` is being profiled
+struct KernelTimer {
+  cudaStream_t s;
+  int id;
+  bool on;
+  KernelTimer(int kid, cudaStream_t st) : s(st), id(kid), on(g_profile.on[kid].load(std::memory_order_relaxed) != 0) {
+    if (on) record_hook_event(g_profile.start[id], s);
+  }
+  ~KernelTimer() {
+    if (on) record_hook_event(g_profile.end[id], s);
+  }
+};
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Every workspace starts with this header. err is the device error word.
+struct WsHeader {
+  int32_t err;        // SSD_OK or the first device-side error recorded
+  int32_t where;      // diagnostic: which wait / check recorded it
+  int32_t pad[62];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+// ---------------------------------------------------------------- device side
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// fp32 -> bf16, round to nearest even (finite inputs)
+__device__ __forceinline__ uint16_t f32_to_bf16(float f) {
+  uint32_t u = __float_as_uint(f);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return static_cast<uint16_t>(u >> 16);
+}
+
+__device__ __forceinline__ void record_error(WsHeader* h, int code, int where) {
+  if (h != nullptr && atomicCAS(&h->err, 0, code) == 0) h->where = where;
+}
+
+template <typename T>
+__device__ __forceinline__ T warp_sum(T v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+}  // namespace ssd

@@ -1,0 +1,130 @@
+"""One speculate-and-verify step on the GPU: device buffers for a batch and the
+launch order of the four C-ABI calls.
+
+    gate_match -> retrieve -> { verify_attn (aux stream) || accept (main stream) }
+
+Verification attention and acceptance both depend only on the retrieval
+output, so with an auxiliary stream they run concurrently. The step issues
+only library calls; it computes nothing itself.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import _binding as ssd
+
+
+def to_device(a: np.ndarray, device) -> torch.Tensor:
+    """numpy -> CUDA tensor; bf16 bit patterns (uint16) become int16 tensors."""
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+INPUT_KEYS = ["ctx", "ctx_len", "h", "w", "q", "k_cache", "v_cache", "k_cand", "v_cand", "prefix_len", "tgt", "drf",
+              "chain_tok", "u_acc", "u_fin"]
+
+
+class VerifyStep:
+    """Holds the inputs, outputs and workspaces of one batch of workload `wl`."""
+
+    def __init__(self, wl, inp: dict, device="cuda", mode=None, kind=None, with_attention=True,
+                 with_probs=False):
+        self.wl = wl
+        self.mode = ssd.SSD_SAMPLE if (mode or wl.mode) == "sample" else ssd.SSD_GREEDY
+        if kind is None:
+            kind = ssd.SSD_LOGITS_BF16 if wl.logit_dtype == "bf16" else ssd.SSD_LOGITS_F32
+        self.kind = kind
+        self.device = torch.device(device)
+        self.x = {}
+        for k in INPUT_KEYS:
+            v = inp.get(k)
+            if v is None:
+                continue
+            if not with_attention and k in ("q", "k_cache", "v_cache", "k_cand", "v_cand"):
+                continue
+            self.x[k] = to_device(np.asarray(v), self.device)
+        B = wl.B
+        self.with_attention = with_attention and "q" in self.x
+        i32 = lambda *s: torch.empty(s, dtype=torch.int32, device=self.device)
+        self.gate_out = dict(score=torch.empty(B, dtype=torch.float32, device=self.device), gate=i32(B),
+                             last_match_end=i32(B), probe_on=i32(B))
+        self.ret_out = dict(blk_tok=i32(B, wl.NB, wl.Dmax), blk_len=i32(B, wl.NB), n_cand=i32(B))
+        self.acc_out = ssd.alloc_accept_outputs(B, wl.NB, wl.Dmax, self.device)
+        self.chain_blk = wl.W if wl.chain_policy else -1
+        self.with_accept = "tgt" in self.x
+        self.probs = (torch.empty((B, wl.NR, wl.V), dtype=torch.float32, device=self.device)
+                      if (with_probs and self.with_accept) else None)
+        if self.with_accept:
+            a = ssd.accept_args(self.mode, self.kind, self.x["tgt"], self.x.get("drf"), self.ret_out["blk_tok"],
+                                self.ret_out["blk_len"], wl.K, self.chain_blk, self.x["u_acc"], self.x["u_fin"],
+                                self.acc_out, self.probs)
+            self.acc_ws = torch.empty(max(256, ssd.ssd_accept_workspace_size(a)), dtype=torch.uint8,
+                                      device=self.device)
+        if self.with_attention:
+            self.attn_out = torch.empty_like(self.x["q"])
+            a = ssd.attn_args(self.x["q"], self.x["k_cache"], self.x["v_cache"], self.x["k_cand"],
+                              self.x["v_cand"], self.x["prefix_len"], self.ret_out["blk_len"], wl.Dmax,
+                              self.attn_out)
+            self.attn_ws = torch.empty(max(256, ssd.ssd_verify_attn_workspace_size(a)), dtype=torch.uint8,
+                                       device=self.device)
+
+    # -------------------------------------------------------------------
+    def gate(self, stream=None):
+        wl, x = self.wl, self.x
+        return ssd.ssd_gate_match(x["ctx"], x["ctx_len"], x["h"], x["w"], wl.tau, wl.kappa, out=self.gate_out,
+                                  stream=stream)
+
+    def retrieve(self, stream=None):
+        wl, x = self.wl, self.x
+        ct = x.get("chain_tok") if wl.chain_policy else None
+        return ssd.ssd_retrieve(x["ctx"], x["ctx_len"], self.gate_out["gate"], self.gate_out["last_match_end"],
+                                wl.kappa, wl.W, wl.D, wl.K, wl.chain_policy, ct, out=self.ret_out, stream=stream)
+
+    def attention(self, stream=None):
+        x = self.x
+        return ssd.ssd_verify_attn(x["q"], x["k_cache"], x["v_cache"], x["k_cand"], x["v_cand"], x["prefix_len"],
+                                   self.ret_out["blk_len"], self.wl.Dmax, out=self.attn_out, ws=self.attn_ws,
+                                   stream=stream)
+
+    def accept(self, stream=None):
+        wl, x = self.wl, self.x
+        return ssd.ssd_accept(x["tgt"], x.get("drf") if wl.chain_policy else None, self.ret_out["blk_tok"],
+                              self.ret_out["blk_len"], x["u_acc"], x["u_fin"], mode=self.mode, kind=self.kind,
+                              K=wl.K, chain_blk=self.chain_blk, out=self.acc_out, ws=self.acc_ws,
+                              probs_out=self.probs, stream=stream)
+
+    def run(self, stream=None, aux: torch.cuda.Stream | None = None):
+        """Issue the whole step on `stream` (default: current), attention on `aux` if given."""
+        main = stream or torch.cuda.current_stream()
+        self.gate(main)
+        self.retrieve(main)
+        if self.with_attention and aux is not None:
+            ev = torch.cuda.Event()
+            ev.record(main)
+            aux.wait_event(ev)
+            self.attention(aux)
+            if self.with_accept:
+                self.accept(main)
+            ev2 = torch.cuda.Event()
+            ev2.record(aux)
+            main.wait_event(ev2)
+        else:
+            if self.with_attention:
+                self.attention(main)
+            if self.with_accept:
+                self.accept(main)
+
+    def results(self) -> dict:
+        """Copy every output to host numpy arrays (synchronises)."""
+        torch.cuda.synchronize()
+        outs = {**self.gate_out, **self.ret_out, **(self.acc_out if self.with_accept else {})}
+        r = {k: v.cpu().numpy() for k, v in outs.items()}
+        if self.with_attention:
+            o = self.attn_out
+            # fp32 output as float32; bf16 output as its uint16 bit patterns
+            r["attn"] = o.cpu().numpy() if o.dtype == torch.float32 else o.view(torch.int16).cpu().numpy().view(np.uint16)
+        if self.probs is not None:
+            r["probs"] = self.probs.cpu().numpy()
+        return r

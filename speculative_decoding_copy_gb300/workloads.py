@@ -149,8 +149,8 @@ WORKLOAD_ORDER = ["tiny", "llama8b", "batched", "llama70b", "qwen8b_mixed"]
 # ---------------------------------------------------------------------------
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round fp32 to bf16 (nearest-even) and return the 16-bit patterns."""
-    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    b = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    b = (b + np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)   # no overflow for finite x
     return b.astype(np.uint16)
 
 
@@ -334,6 +334,8 @@ def make_inputs(wl: Workload, seed: int | None = None, *, full_width: bool = Tru
         else:
             out["chain_tok"] = np.zeros((B, 0), dtype=np.int32)
             out["drf"] = None
+    if not with_logits:
+        out["chain_tok"] = rng.integers(0, wl.V, size=(B, wl.K)).astype(np.int32)
     out["u_acc"] = uniforms24(rng, (B, NB, Dmax))
     out["u_fin"] = uniforms24(rng, (B,))
     return out

@@ -1,0 +1,103 @@
+"""GPU verification attention against the fp64 oracle: max-abs error <= 1e-2
+(bf16 inputs, fp32 accumulation), on every present token for small shapes
+spanning several tiles with ragged tails, and on sampled tokens at the full
+workload sizes."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import ssd_oracle as O
+from speculative_decoding_copy_gb300 import _binding as S
+from speculative_decoding_copy_gb300 import workloads as WL
+from speculative_decoding_copy_gb300.step import VerifyStep, to_device
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2
+
+
+def _as_f64(x, dtype):
+    return O.to_f64(x, dtype)
+
+
+def _run_attn(case, blk_len, Dmax, dtype):
+    dev = "cuda"
+    t = {k: to_device(np.asarray(v), dev) for k, v in case.items()}
+    bl = to_device(blk_len, dev)
+    out = S.ssd_verify_attn(t["q"], t["k_cache"], t["v_cache"], t["k_cand"], t["v_cand"], t["prefix_len"], bl, Dmax)
+    torch.cuda.synchronize()
+    o = out.cpu()
+    return o.numpy() if dtype == "f32" else o.view(torch.int16).numpy().view(np.uint16)
+
+
+def _case(rng, B, NB, Dmax, Hq, Hkv, dh, prefix, dtype, q_scale=1.0):
+    P_max = max(1, max(prefix))
+    NT = NB * Dmax
+    f = lambda *s: rng.standard_normal(s).astype(np.float32)
+    cast = (lambda x: x) if dtype == "f32" else WL.f32_to_bf16_bits
+    return dict(q=cast(f(B, NT, Hq, dh) * np.float32(q_scale)), k_cache=cast(f(B, Hkv, P_max, dh)),
+                v_cache=cast(f(B, Hkv, P_max, dh)), k_cand=cast(f(B, NT, Hkv, dh)), v_cand=cast(f(B, NT, Hkv, dh)),
+                prefix_len=np.asarray(prefix, np.int32))
+
+
+def _check_all(case, blk_len, Dmax, dtype, slots=None):
+    got = _run_attn(case, blk_len, Dmax, dtype)
+    ref = O.verify_attention(case["q"], case["k_cache"], case["v_cache"], case["k_cand"], case["v_cand"],
+                             case["prefix_len"], blk_len, Dmax, dtype, slots)
+    g = _as_f64(got, dtype)
+    err = 0.0
+    for (b, t), o in ref.items():
+        err = max(err, float(np.max(np.abs(g[b, t] - o))))
+    assert err <= TOL, err
+    return err
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dh", [64, 128])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_attention_small_shapes(dtype, dh, G):
+    rng = np.random.default_rng(dh + G + (7 if dtype == "bf16" else 0))
+    Hkv = 2
+    B, NB, Dmax = 3, 3, 5
+    prefix = [0, 37, 300]             # empty prefix, ragged tails, several key tiles
+    case = _case(rng, B, NB, Dmax, Hkv * G, Hkv, dh, prefix, dtype, q_scale=2.0)
+    blk_len = np.array([[5, 0, 3], [1, 5, 5], [2, 4, 0]], np.int32)
+    _check_all(case, blk_len, Dmax, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_attention_sharp_and_long(dtype):
+    # sharper scores (q scaled) and a prefix spanning many splits
+    rng = np.random.default_rng(31)
+    case = _case(rng, 2, 2, 8, 8, 2, 128, [2049, 4100], dtype, q_scale=4.0)
+    blk_len = np.array([[8, 3], [6, 8]], np.int32)
+    _check_all(case, blk_len, 8, dtype)
+
+
+def test_attention_tiny_workload():
+    wl = WL.WORKLOADS["tiny"]
+    inp = WL.make_inputs(wl)
+    keys = ("q", "k_cache", "v_cache", "k_cand", "v_cand", "prefix_len")
+    blk_len = np.array([[wl.D, wl.D, 0]], np.int32)
+    _check_all({k: inp[k] for k in keys}, blk_len, wl.Dmax, wl.kv_dtype)
+
+
+@pytest.mark.parametrize("name", ["llama8b", "llama70b", "batched", "qwen8b_mixed"])
+def test_attention_full_size_sampled(name):
+    """Full workload size, the step's own launch path; 24 sampled tokens against the oracle."""
+    wl = WL.WORKLOADS[name]
+    inp = WL.make_inputs(wl, with_logits=False)
+    st = VerifyStep(wl, inp)
+    st.gate()
+    st.retrieve()
+    st.attention()
+    r = st.results()
+    bl = r["blk_len"]
+    present = [(b, k * wl.Dmax + d) for b in range(wl.B) for k in range(wl.NB) for d in range(bl[b, k])]
+    rng = np.random.default_rng(3)
+    pick = [present[i] for i in rng.choice(len(present), size=min(24, len(present)), replace=False)]
+    ref = O.verify_attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["k_cand"], inp["v_cand"],
+                             inp["prefix_len"], bl, wl.Dmax, wl.kv_dtype, pick)
+    g = _as_f64(r["attn"], wl.kv_dtype)
+    err = max(float(np.max(np.abs(g[b, t] - o))) for (b, t), o in ref.items())
+    assert err <= TOL, err
