@@ -45,6 +45,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="llama8b")
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--serial", action="store_true",
+                    help="run attention on the main stream too (clean per-kernel times; not the timed default)")
     ap.add_argument("--oracle-worker", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--oracle-seconds", type=float, default=20.0, help=argparse.SUPPRESS)
     return ap.parse_args(argv)
@@ -252,7 +254,7 @@ def run_ours(args):
     # rotating copies: total bytes above twice the L2
     probe = VerifyStep(wl, inp, device=dev)
     main = torch.cuda.Stream(dev)
-    aux = torch.cuda.Stream(dev)
+    aux = None if args.serial else torch.cuda.Stream(dev)
     with torch.cuda.stream(main):
         probe.run(main, aux)
     torch.cuda.synchronize()

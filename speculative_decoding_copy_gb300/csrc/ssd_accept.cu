@@ -80,9 +80,15 @@ __device__ __forceinline__ const void* row_ptr(const AcceptParams& p, int b, int
 }
 
 // ------------------------------------------------------------------ stats
+__device__ void vocab_stats_one(const AcceptParams& p, int b, int r, int c);
+
 __global__ void __launch_bounds__(kVocabThreads)
 k_vocab_stats(AcceptParams p) {
-  const int c = blockIdx.x, r = blockIdx.y, b = blockIdx.z;
+  const int c = blockIdx.x % p.nch, r = blockIdx.x / p.nch;
+  for (int b = blockIdx.y; b < p.B; b += gridDim.y) vocab_stats_one(p, b, r, c);
+}
+
+__device__ void vocab_stats_one(const AcceptParams& p, int b, int r, int c) {
   if (!row_needed(p, b, r)) return;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int64_t lo = static_cast<int64_t>(c) * p.chunk;
@@ -171,6 +177,7 @@ k_vocab_stats(AcceptParams p) {
     }
     p.part[(static_cast<int64_t>(b) * p.NRD + r) * p.nch + c] = RowStat{m, s, av, ai};
   }
+  __syncthreads();   // red[] is reused by the next sequence of this CTA
 }
 
 // ------------------------------------------------------------------ select
@@ -321,9 +328,17 @@ __device__ __forceinline__ void weights_at(const AcceptParams& p, const void* pr
   W = P > Q ? P - Q : 0LL;
 }
 
+__device__ void sample_final_one(const AcceptParams& p, int b, int c);
+
 __global__ void __launch_bounds__(kVocabThreads)
 k_sample_final(AcceptParams p) {
-  const int c = blockIdx.x, b = blockIdx.y;
+  for (int b = blockIdx.y; b < p.B; b += gridDim.y) {
+    sample_final_one(p, b, blockIdx.x);
+    __syncthreads();   // shared state is reused by the next sequence of this CTA
+  }
+}
+
+__device__ void sample_final_one(const AcceptParams& p, int b, int c) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   constexpr int nw = kVocabThreads / 32;
   __shared__ long long red_w[nw], red_p[nw];
@@ -430,15 +445,17 @@ k_sample_final(AcceptParams p) {
 // ------------------------------------------------------------------ diagnostics
 __global__ void __launch_bounds__(kVocabThreads)
 k_probs_out(AcceptParams p) {
-  const int c = blockIdx.x, r = blockIdx.y, b = blockIdx.z;
-  if (!row_needed(p, b, r)) return;
-  const RowStat st = p.stat[static_cast<int64_t>(b) * p.NRD + r];
-  const void* row = row_ptr(p, b, r);
-  const int64_t lo = static_cast<int64_t>(c) * p.chunk;
-  const int64_t hi = min(p.V, lo + p.chunk);
-  float* out = p.probs_out + (static_cast<int64_t>(b) * p.NR + r) * p.V;
-  for (int64_t i = lo + threadIdx.x; i < hi; i += kVocabThreads)
-    out[i] = prob_of(load_val(row, i, p.bf16), st, p.probs);
+  const int c = blockIdx.x % p.nch, r = blockIdx.x / p.nch;
+  for (int b = blockIdx.y; b < p.B; b += gridDim.y) {
+    if (!row_needed(p, b, r)) continue;
+    const RowStat st = p.stat[static_cast<int64_t>(b) * p.NRD + r];
+    const void* row = row_ptr(p, b, r);
+    const int64_t lo = static_cast<int64_t>(c) * p.chunk;
+    const int64_t hi = min(p.V, lo + p.chunk);
+    float* out = p.probs_out + (static_cast<int64_t>(b) * p.NR + r) * p.V;
+    for (int64_t i = lo + threadIdx.x; i < hi; i += kVocabThreads)
+      out[i] = prob_of(load_val(row, i, p.bf16), st, p.probs);
+  }
 }
 
 // ------------------------------------------------------------------ host
@@ -533,7 +550,8 @@ AcceptParams accept_params(const ssd_accept_args* a, const AcceptLayout& L, char
 }
 
 int accept_launch(const AcceptParams& p, cudaStream_t s) {
-  dim3 g1(p.nch, p.NRD, p.B);
+  const unsigned by = static_cast<unsigned>(p.B < 65535 ? p.B : 65535);
+  dim3 g1(static_cast<unsigned>(p.nch * p.NRD), by);
   {
     KernelTimer t(SSD_KERNEL_VOCAB_STATS, s);
     k_vocab_stats<<<g1, kVocabThreads, 0, s>>>(p);
@@ -544,13 +562,13 @@ int accept_launch(const AcceptParams& p, cudaStream_t s) {
   }
   int n = 2;
   if (p.sample) {
-    dim3 g3(p.nchs, p.B);
+    dim3 g3(static_cast<unsigned>(p.nchs), by);
     KernelTimer t(SSD_KERNEL_SAMPLE_FINAL, s);
     k_sample_final<<<g3, kVocabThreads, 0, s>>>(p);
     ++n;
   }
   if (p.probs_out != nullptr) {
-    dim3 g4(p.nch, p.NR, p.B);
+    dim3 g4(static_cast<unsigned>(p.nch * p.NR), by);
     k_probs_out<<<g4, kVocabThreads, 0, s>>>(p);
     ++n;
   }

@@ -48,7 +48,7 @@ __device__ __forceinline__ bool token_present(const int32_t* blk_len, int b, int
   return pos < blk_len[b * NB + k];
 }
 
-// grid (S, ceil(NT*G / 8), B*Hkv), block 128
+// grid (B*Hkv, ceil(NT*G / 8), S), block 128
 template <typename T, int DH>
 __global__ void __launch_bounds__(kSimtThreads)
 k_attn_prefix_simt(AttnParams p) {
@@ -57,8 +57,8 @@ k_attn_prefix_simt(AttnParams p) {
   __shared__ float k_s[kKeyTile][DH + 1];
   __shared__ float v_s[kKeyTile][DH];
 
-  const int split = blockIdx.x;
-  const int bk = blockIdx.z;
+  const int split = blockIdx.z;
+  const int bk = blockIdx.x;
   const int b = bk / p.Hkv, kvh = bk % p.Hkv;
   const int G = p.Hq / p.Hkv;
   const int NT = p.NB * p.Dmax;
@@ -240,7 +240,8 @@ static int validate(const ssd_attn_args* a) {
   if (a->B < 0 || a->NB < 1 || a->Dmax < 1 || a->Hq < 1 || a->Hkv < 1 || a->P_max < 0) return SSD_ERR_INVALID;
   if (a->dtype != SSD_F32 && a->dtype != SSD_BF16) return SSD_ERR_INVALID;
   if (a->Hq % a->Hkv != 0) return SSD_ERR_INVALID;
-  if (a->Dmax > 256) return SSD_ERR_UNSUPPORTED;
+  if (a->Dmax > 256 || a->NB * a->Dmax > 8192 || a->Hq / a->Hkv > 64) return SSD_ERR_UNSUPPORTED;
+  if (static_cast<long long>(a->B) * a->Hkv > 0x7fffffffLL) return SSD_ERR_UNSUPPORTED;
   if (a->dh != 64 && a->dh != 128) return SSD_ERR_UNSUPPORTED;
   if (a->P_max > (1LL << 30)) return SSD_ERR_UNSUPPORTED;
   if (a->B == 0) return SSD_OK;
@@ -301,26 +302,36 @@ extern "C" int ssd_verify_attn(const ssd_attn_args* a, void* ws, size_t ws_bytes
 
   const int NT = a->NB * a->Dmax;
   const int G = a->Hq / a->Hkv;
-  dim3 g1(L.S, (NT * G + kSimtRows - 1) / kSimtRows, a->B * a->Hkv);
-  const long long rows = static_cast<long long>(a->B) * NT * a->Hq;
-  dim3 g2(static_cast<unsigned>((rows + 3) / 4));
-  if (a->dtype == SSD_F32) {
-    if (a->dh == 64) {
-      { KernelTimer t(SSD_KERNEL_ATTN_PREFIX, s); k_attn_prefix_simt<float, 64><<<g1, kSimtThreads, 0, s>>>(p); }
-      { KernelTimer t(SSD_KERNEL_ATTN_COMBINE, s); k_attn_combine<float, 64><<<g2, 128, 0, s>>>(p); }
+  dim3 g1(a->B * a->Hkv, (NT * G + kSimtRows - 1) / kSimtRows, L.S);
+  {
+    KernelTimer t(SSD_KERNEL_ATTN_PREFIX, s);
+    if (a->dtype == SSD_F32) {
+      if (a->dh == 64) k_attn_prefix_simt<float, 64><<<g1, kSimtThreads, 0, s>>>(p);
+      else k_attn_prefix_simt<float, 128><<<g1, kSimtThreads, 0, s>>>(p);
     } else {
-      { KernelTimer t(SSD_KERNEL_ATTN_PREFIX, s); k_attn_prefix_simt<float, 128><<<g1, kSimtThreads, 0, s>>>(p); }
-      { KernelTimer t(SSD_KERNEL_ATTN_COMBINE, s); k_attn_combine<float, 128><<<g2, 128, 0, s>>>(p); }
-    }
-  } else {
-    if (a->dh == 64) {
-      { KernelTimer t(SSD_KERNEL_ATTN_PREFIX, s); k_attn_prefix_simt<uint16_t, 64><<<g1, kSimtThreads, 0, s>>>(p); }
-      { KernelTimer t(SSD_KERNEL_ATTN_COMBINE, s); k_attn_combine<uint16_t, 64><<<g2, 128, 0, s>>>(p); }
-    } else {
-      { KernelTimer t(SSD_KERNEL_ATTN_PREFIX, s); k_attn_prefix_simt<uint16_t, 128><<<g1, kSimtThreads, 0, s>>>(p); }
-      { KernelTimer t(SSD_KERNEL_ATTN_COMBINE, s); k_attn_combine<uint16_t, 128><<<g2, 128, 0, s>>>(p); }
+      if (a->dh == 64) k_attn_prefix_simt<uint16_t, 64><<<g1, kSimtThreads, 0, s>>>(p);
+      else k_attn_prefix_simt<uint16_t, 128><<<g1, kSimtThreads, 0, s>>>(p);
     }
   }
+  const int rc = check_launch();
+  if (rc != SSD_OK) return rc;
   count_launch(2);
+  return attn_combine_launch(p, a->dtype, a->dh, s);
+}
+
+namespace ssd {
+int attn_combine_launch(const AttnParams& p, int dtype, int dh, cudaStream_t s) {
+  const int NT = p.NB * p.Dmax;
+  const long long rows = static_cast<long long>(p.B) * NT * p.Hq;
+  dim3 g2(static_cast<unsigned>((rows + 3) / 4));
+  KernelTimer t(SSD_KERNEL_ATTN_COMBINE, s);
+  if (dtype == SSD_F32) {
+    if (dh == 64) k_attn_combine<float, 64><<<g2, 128, 0, s>>>(p);
+    else k_attn_combine<float, 128><<<g2, 128, 0, s>>>(p);
+  } else {
+    if (dh == 64) k_attn_combine<uint16_t, 64><<<g2, 128, 0, s>>>(p);
+    else k_attn_combine<uint16_t, 128><<<g2, 128, 0, s>>>(p);
+  }
   return check_launch();
 }
+}  // namespace ssd

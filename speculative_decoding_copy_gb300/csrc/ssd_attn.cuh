@@ -23,6 +23,9 @@ struct AttnParams {
   float* ws_o;           // [rows][S][dh] un-normalised output per split
 };
 
+// merge the splits, add the own-block keys, normalise (ssd_attn.cu)
+int attn_combine_launch(const AttnParams& p, int dtype, int dh, cudaStream_t s);
+
 // tcgen05 prefix path (ssd_attn_tc.cu)
 bool attn_tc_applies(const ssd_attn_args* a);
 size_t attn_tc_workspace_size(const ssd_attn_args* a);

@@ -1,10 +1,566 @@
-// tcgen05 prefix kernel for bf16 verification attention (not enabled yet).
+// tcgen05 prefix pass of the verification attention (bf16, head dim 128).
+//
+// Every candidate token of a sequence sees the same prefix keys (SwitchSD page,
+// "무엇과 다른가": each candidate attends to the whole prefix), so for one kv
+// head the G query heads of all NT candidate slots pack into NT*G rows of one
+// dense product with each prefix tile. A CTA owns 128 packed rows (the M of
+// the MMA) and one split of the prefix; it leaves the same per-split partial
+// (running max m, sum l, un-normalised o, log2 units) as the SIMT pass, and
+// the combine kernel adds the own-block keys and merges the splits.
+//
+// Per CTA (192 threads, one CTA per SM):
+//   warps 0-3  one thread per packed row: stage Q, online softmax from the S
+//              row in TMEM (tcgen05.ld), O rescale in TMEM, P as bf16 into
+//              shared memory, epilogue;
+//   warp 4     TMA producer: K and V tiles of 128 keys (two 64-wide halves,
+//              128-byte swizzle) into a 2-stage ring;
+//   warp 5     TMEM allocation and the single MMA-issuing thread:
+//              S = Q K^T (M128 N128 K16 x 8) and O += P V (M128 N128 K16 x 8),
+//              kind::f16 with bf16 operands and fp32 accumulators in TMEM.
+// Every mbarrier wait is bounded (about 2^32 clocks); on expiry the CTA
+// records SSD_ERR_TIMEOUT in the workspace header, skips the remaining waits,
+// frees its TMEM and exits.
+#include <cuda.h>
+#include <math.h>
+
+#include <mutex>
+
 #include "ssd_attn.cuh"
 
 namespace ssd {
+namespace tc {
 
-bool attn_tc_applies(const ssd_attn_args*) { return false; }
-size_t attn_tc_workspace_size(const ssd_attn_args*) { return 0; }
-int attn_tc_launch(const ssd_attn_args*, void*, cudaStream_t) { return SSD_ERR_UNSUPPORTED; }
+constexpr int DH = 128;
+constexpr int BM = 128;                   // packed rows per CTA
+constexpr int BN = 128;                   // keys per tile
+constexpr int STAGES = 2;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 256;       // S: cols 0-127, O: cols 128-255
+constexpr uint32_t kHalf = 128 * 128;     // one 64-wide half of a 128-row bf16 tile: 16 KB
+constexpr uint32_t OFF_Q = 0;
+constexpr uint32_t OFF_K = OFF_Q + 2 * kHalf;
+constexpr uint32_t OFF_V = OFF_K + STAGES * 2 * kHalf;
+constexpr uint32_t OFF_P = OFF_V + STAGES * 2 * kHalf;
+constexpr uint32_t OFF_BAR = OFF_P + 2 * kHalf;
+constexpr uint32_t kSmemBytes = OFF_BAR + 256 + 1024;   // + slack to align the base to 1024
+constexpr unsigned long long kWaitClocks = 1ull << 32;
+
+struct Bars {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t q_full, s_full, s_free, p_full, o_done;
+  uint32_t tmem_base;
+  int failed;
+};
+
+// ------------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait; false once this CTA has given up (then every later wait returns at once).
+__device__ __forceinline__ bool mbar_wait(Bars& bars, uint64_t* bar, uint32_t parity, WsHeader* hdr, int where) {
+  volatile int* failed = &bars.failed;
+  if (*failed) return false;
+  const unsigned long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*failed) return false;
+    if (clock64() - t0 > kWaitClocks) {
+      *failed = 1;
+      record_error(hdr, SSD_ERR_TIMEOUT, where);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// shared-memory matrix descriptor, 128-byte swizzle (sm_100 format)
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;            // descriptor version
+  d |= 2ull << 61;            // SWIZZLE_128B
+  return d;
+}
+
+// instruction descriptor, kind::f16: bf16 A and B, fp32 D, M = 128, N = 128
+__host__ __device__ constexpr uint32_t idesc_bf16(bool b_mn_major) {
+  return (1u << 4)            // D: f32
+         | (1u << 7)          // A: bf16
+         | (1u << 10)         // B: bf16
+         | ((b_mn_major ? 1u : 0u) << 16)
+         | ((128u >> 3) << 17)  // N
+         | ((128u >> 4) << 24); // M
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+      "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
+      "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// two fp32 -> packed bf16x2 (round to nearest even), low half = first
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  return static_cast<uint32_t>(f32_to_bf16(lo)) | (static_cast<uint32_t>(f32_to_bf16(hi)) << 16);
+}
+
+// offset of 16-byte chunk c (0..7) of row r inside a 128-byte-swizzled half
+__device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t c) { return r * 128u + ((c ^ (r & 7u)) << 4); }
+
+// ------------------------------------------------------------------ kernel
+__global__ void __launch_bounds__(kThreads, 1)
+k_attn_prefix_tc(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                 AttnParams p, int mtiles) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  Bars& bars = *reinterpret_cast<Bars*>(smem + OFF_BAR);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int mt = blockIdx.x % mtiles;
+  const int bk = blockIdx.x / mtiles;
+  const int b = bk / p.Hkv, kvh = bk % p.Hkv;
+  const int split = blockIdx.y;
+  const int G = p.Hq / p.Hkv;
+  const int NT = p.NB * p.Dmax;
+  const int rows_total = NT * G;
+  const int r0 = mt * BM;
+  const int P = p.prefix_len[b];
+  const int k0 = split * p.chunk;
+  const int k1 = min(P, k0 + p.chunk);
+  const int nT = k1 > k0 ? (k1 - k0 + BN - 1) / BN : 0;
+
+  // this thread's packed row (softmax warps) and whether it is a present token
+  const int r = r0 + tid;
+  bool present = false;
+  int t = 0, h = 0;
+  if (tid < BM && r < rows_total) {
+    t = r / G;
+    h = kvh * G + r % G;
+    present = (t % p.Dmax) < p.blk_len[b * p.NB + t / p.Dmax];
+  }
+  if (!__syncthreads_or(present)) return;          // no present row in this tile
+  const int64_t R = (static_cast<int64_t>(b) * NT + t) * p.Hq + h;
+
+  if (nT == 0) {                                   // empty split: neutral partial
+    if (present) {
+      float* ml = p.ws_ml + (R * p.S + split) * 2;
+      ml[0] = -INFINITY;
+      ml[1] = 0.f;
+      float4* ow = reinterpret_cast<float4*>(p.ws_o + (R * p.S + split) * DH);
+      for (int e = 0; e < DH / 4; ++e) ow[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    return;
+  }
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&bars.full[s], 1);
+      mbar_init(&bars.empty[s], 1);
+    }
+    mbar_init(&bars.q_full, BM);
+    mbar_init(&bars.s_full, 1);
+    mbar_init(&bars.s_free, BM);
+    mbar_init(&bars.p_full, BM);
+    mbar_init(&bars.o_done, 1);
+    bars.failed = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 5) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&bars.tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  const uint32_t tmem_S = tmem;
+  const uint32_t tmem_O = tmem + 128;
+
+  if (warp < 4) {
+    // ---------------------------------------------------------- softmax rows
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    {
+      // stage Q row `tid` (zeros past the last packed row), 128-byte swizzle
+      const uint4* q4 = nullptr;
+      if (r < rows_total)
+        q4 = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
+                                            ((static_cast<int64_t>(b) * NT + t) * p.Hq + h) * DH);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const uint4 v = q4 ? __ldg(q4 + c) : make_uint4(0, 0, 0, 0);
+        st_shared_v4(sbase + OFF_Q + (c >> 3) * kHalf + sw128_off(tid, c & 7), v.x, v.y, v.z, v.w);
+      }
+      fence_async_smem();
+      mbar_arrive(&bars.q_full);
+    }
+    const float sl2 = p.scale_log2;
+    float m = -INFINITY, l = 0.f;
+    uint32_t sreg[BN];
+    for (int j = 0; j < nT; ++j) {
+      const bool ok_s = mbar_wait(bars, &bars.s_full, j & 1, p.hdr, 10);
+      tc_fence_after();
+#pragma unroll
+      for (int q = 0; q < BN / 32; ++q) tmem_ld32(tmem_S + lane_off + q * 32, sreg + q * 32);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&bars.s_free);
+      const int nvalid = min(BN, k1 - (k0 + j * BN));
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < BN; ++c) {
+        const float s = c < nvalid ? __uint_as_float(sreg[c]) * sl2 : -INFINITY;
+        sreg[c] = __float_as_uint(s);
+        mx = fmaxf(mx, s);
+      }
+      (void)ok_s;
+      // keep a stale reference max unless the row max grew by more than 2^8
+      const float m_new = fmaxf(m, mx);
+      const bool need = m_new > m + 8.f;
+      const float mref = need ? m_new : m;
+      const float alpha = need ? exp2f(m - m_new) : 1.f;
+      uint32_t pk[BN / 2];
+      float rs = 0.f;
+#pragma unroll
+      for (int c = 0; c < BN; c += 2) {
+        const float p0 = exp2f(__uint_as_float(sreg[c]) - mref);
+        const float p1 = exp2f(__uint_as_float(sreg[c + 1]) - mref);
+        const uint32_t w = pack_bf16(p0, p1);
+        pk[c / 2] = w;
+        rs += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+      }
+      if (j > 0) {
+        mbar_wait(bars, &bars.o_done, (j - 1) & 1, p.hdr, 11);
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, need)) {
+          uint32_t o[32];
+#pragma unroll
+          for (int q = 0; q < DH / 32; ++q) {
+            tmem_ld32(tmem_O + lane_off + q * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(tmem_O + lane_off + q * 32, o);
+          }
+          tmem_wait_st();
+        }
+      }
+      l = l * alpha + rs;
+      m = mref;
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        st_shared_v4(sbase + OFF_P + (c >> 3) * kHalf + sw128_off(tid, c & 7), pk[4 * c], pk[4 * c + 1],
+                     pk[4 * c + 2], pk[4 * c + 3]);
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars.p_full);
+    }
+    // epilogue: un-normalised o, running max and sum of this split
+    mbar_wait(bars, &bars.o_done, (nT - 1) & 1, p.hdr, 12);
+    tc_fence_after();
+    float* ow = p.ws_o + (R * p.S + split) * DH;
+#pragma unroll
+    for (int q = 0; q < DH / 32; ++q) {
+      uint32_t o[32];
+      tmem_ld32(tmem_O + lane_off + q * 32, o);
+      tmem_wait_ld();
+      if (present) {
+        float4* o4 = reinterpret_cast<float4*>(ow + q * 32);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          o4[e] = make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
+                              __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+      }
+    }
+    if (present) {
+      float* ml = p.ws_ml + (R * p.S + split) * 2;
+      ml[0] = m;
+      ml[1] = l;
+    }
+  } else if (warp == 4) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      const int y0 = (b * p.Hkv + kvh) * static_cast<int>(p.P_max) + k0;
+      for (int j = 0; j < nT; ++j) {
+        const int s = j % STAGES;
+        if (j >= STAGES) mbar_wait(bars, &bars.empty[s], ((j / STAGES) - 1) & 1, p.hdr, 20);
+        if (bars.failed) break;
+        mbar_expect_tx(&bars.full[s], 4 * kHalf);
+        const int y = y0 + j * BN;
+        const uint32_t kd = sbase + OFF_K + s * 2 * kHalf, vd = sbase + OFF_V + s * 2 * kHalf;
+        tma_load_2d(kd, &tmap_k, 0, y, &bars.full[s]);
+        tma_load_2d(kd + kHalf, &tmap_k, 64, y, &bars.full[s]);
+        tma_load_2d(vd, &tmap_v, 0, y, &bars.full[s]);
+        tma_load_2d(vd + kHalf, &tmap_v, 64, y, &bars.full[s]);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(false), idPV = idesc_bf16(true);
+      mbar_wait(bars, &bars.q_full, 0, p.hdr, 30);
+      tc_fence_after();
+      auto issue_S = [&](int s) {
+        const uint32_t kb = sbase + OFF_K + s * 2 * kHalf;
+#pragma unroll
+        for (int ks = 0; ks < DH / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
+          mma_bf16(tmem_S, sw128_desc(sbase + OFF_Q + off, 16, 1024), sw128_desc(kb + off, 16, 1024), idS,
+                   ks > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars.s_full);
+      };
+      mbar_wait(bars, &bars.full[0], 0, p.hdr, 31);
+      tc_fence_after();
+      issue_S(0);
+      for (int j = 0; j < nT; ++j) {
+        const int s = j % STAGES;
+        if (j + 1 < nT) {
+          const int s1 = (j + 1) % STAGES;
+          mbar_wait(bars, &bars.full[s1], ((j + 1) / STAGES) & 1, p.hdr, 32);
+          mbar_wait(bars, &bars.s_free, j & 1, p.hdr, 33);
+          tc_fence_after();
+          issue_S(s1);
+        }
+        mbar_wait(bars, &bars.p_full, j & 1, p.hdr, 34);
+        tc_fence_after();
+        const uint32_t vb = sbase + OFF_V + s * 2 * kHalf;
+#pragma unroll
+        for (int ks = 0; ks < BN / 16; ++ks) {
+          const uint64_t a = sw128_desc(sbase + OFF_P + (ks >> 2) * kHalf + (ks & 3) * 32, 16, 1024);
+          const uint64_t bdesc = sw128_desc(vb + ks * 16 * 128, kHalf, 1024);
+          mma_bf16(tmem_O, a, bdesc, idPV, (j > 0 || ks > 0) ? 1u : 0u);
+        }
+        mma_commit(&bars.o_done);
+        mma_commit(&bars.empty[s]);
+      }
+    }
+  }
+
+  // teardown: every role is done with TMEM
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+// ------------------------------------------------------------------ host
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+static bool make_kv_map(CUtensorMap* map, const void* base, uint64_t rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(DH), rows};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(DH) * 2};
+  const cuuint32_t box[2] = {64, BN};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// splits: minimise (waves of CTAs) x (key tiles per split)
+static void choose_split(const ssd_attn_args* a, int mtiles, int* S_out, int* chunk_out) {
+  const long long per_split = static_cast<long long>(a->B) * a->Hkv * mtiles;
+  const long long nkt = a->P_max > 0 ? (a->P_max + BN - 1) / BN : 1;
+  int sms = 152;
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) sms = v;
+  }
+  long long best_cost = -1;
+  int best_S = 1;
+  for (int S = 1; S <= 64 && S <= nkt; ++S) {
+    const long long tiles = (nkt + S - 1) / S;
+    const long long waves = (per_split * S + sms - 1) / sms;
+    const long long cost = waves * tiles * 8 + S;   // small penalty per split for the combine
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_S = S;
+    }
+  }
+  const long long tiles = (nkt + best_S - 1) / best_S;
+  *chunk_out = static_cast<int>(tiles * BN);
+  *S_out = static_cast<int>((nkt + tiles - 1) / tiles);
+}
+
+}  // namespace tc
+
+static bool tc_disabled_by_env() {
+  const char* e = getenv("SSD_ATTN_KERNEL");
+  return e != nullptr && e[0] == 's';   // "simt" forces the SIMT prefix pass
+}
+
+bool attn_tc_applies(const ssd_attn_args* a) {
+  if (tc_disabled_by_env()) return false;
+  if (a->dtype != SSD_BF16 || a->dh != tc::DH || a->P_max < 1) return false;
+  if (!aligned(a->k_cache, 16) || !aligned(a->v_cache, 16) || !aligned(a->q, 16)) return false;
+  if (static_cast<long long>(a->B) * a->Hkv * a->P_max >= (1LL << 31)) return false;
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  return major == 10 && minor == 3 && tc::encode_fn() != nullptr;
+}
+
+struct TcLayout {
+  int mtiles, S, chunk;
+  size_t ml_off, o_off, total;
+};
+
+static TcLayout tc_layout(const ssd_attn_args* a) {
+  TcLayout L{};
+  const int NT = a->NB * a->Dmax;
+  const int G = a->Hq / a->Hkv;
+  L.mtiles = (NT * G + tc::BM - 1) / tc::BM;
+  tc::choose_split(a, L.mtiles, &L.S, &L.chunk);
+  const size_t R = static_cast<size_t>(a->B) * NT * a->Hq;
+  L.ml_off = sizeof(WsHeader);
+  L.o_off = round_up(L.ml_off + R * L.S * 2 * sizeof(float), 256);
+  L.total = round_up(L.o_off + R * L.S * tc::DH * sizeof(float), 256);
+  return L;
+}
+
+size_t attn_tc_workspace_size(const ssd_attn_args* a) {
+  if (a->dtype != SSD_BF16 || a->dh != tc::DH || a->P_max < 1) return 0;
+  return tc_layout(a).total;
+}
+
+int attn_tc_launch(const ssd_attn_args* a, void* ws, cudaStream_t s) {
+  const TcLayout L = tc_layout(a);
+  CUtensorMap mk, mv;
+  const uint64_t rows = static_cast<uint64_t>(a->B) * a->Hkv * a->P_max;
+  if (!tc::make_kv_map(&mk, a->k_cache, rows) || !tc::make_kv_map(&mv, a->v_cache, rows)) return SSD_ERR_CUDA;
+
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(tc::k_attn_prefix_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(tc::kSmemBytes));
+  });
+  if (attr_err != cudaSuccess) return SSD_ERR_CUDA;
+
+  AttnParams p{};
+  p.q = a->q; p.k_cache = a->k_cache; p.v_cache = a->v_cache; p.k_cand = a->k_cand; p.v_cand = a->v_cand;
+  p.out = a->out; p.prefix_len = a->prefix_len; p.blk_len = a->blk_len;
+  p.B = a->B; p.NB = a->NB; p.Dmax = a->Dmax; p.Hq = a->Hq; p.Hkv = a->Hkv; p.P_max = a->P_max;
+  const float scale = a->scale != 0.f ? a->scale : 1.f / sqrtf(static_cast<float>(a->dh));
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.S = L.S;
+  p.chunk = L.chunk;
+  char* base = static_cast<char*>(ws);
+  p.hdr = reinterpret_cast<WsHeader*>(base);
+  p.ws_ml = reinterpret_cast<float*>(base + L.ml_off);
+  p.ws_o = reinterpret_cast<float*>(base + L.o_off);
+
+  dim3 grid(static_cast<unsigned>(a->B * a->Hkv * L.mtiles), static_cast<unsigned>(L.S));
+  {
+    KernelTimer timer(SSD_KERNEL_ATTN_PREFIX, s);
+    tc::k_attn_prefix_tc<<<grid, tc::kThreads, tc::kSmemBytes, s>>>(mk, mv, p, L.mtiles);
+  }
+  int rc = check_launch();
+  if (rc != SSD_OK) return rc;
+  rc = attn_combine_launch(p, a->dtype, a->dh, s);
+  count_launch(2);
+  return rc;
+}
 
 }  // namespace ssd
