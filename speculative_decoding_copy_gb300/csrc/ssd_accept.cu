@@ -10,17 +10,19 @@
 // a match is accepted, the first mismatch truncates.
 //
 // Kernels (one stream, in order):
-//   k_vocab_stats   grid (chunks, rows, B): per needed row and vocabulary chunk,
-//                   max, sum of exp(l - max) and argmax (lowest index on ties);
-//                   a single streaming pass over the logits (HBM-bound);
-//   k_accept_select grid B: merges the chunks of each needed row, runs the
-//                   acceptance scan of every block (one warp per block, one
-//                   lane per token, ballot for the leading run), picks the
-//                   longest block and writes the accepted tokens;
+//   k_vocab_stats   grid (chunks x rows, B): one 16-byte-vector pass over the
+//                   logits; each CTA holds a whole 32 KB chunk in registers
+//                   (one memory latency), then max, argmax (lowest index on
+//                   ties) and sum of 2^((l - max) log2 e) for the chunk;
+//   k_accept_select grid B: merges the chunks of every needed row, runs the
+//                   acceptance test of every candidate token (one thread per
+//                   token slot, loads issued together), picks the longest
+//                   accepted block and writes the accepted tokens;
 //   k_sample_final  grid (chunks, B), sample mode only: integer weights of the
-//                   stop row per chunk, then the last CTA of each sequence
-//                   finds the chunk and the index where the prefix sum crosses
-//                   the threshold (no spin-wait: a completion counter);
+//                   stop row per chunk; the last CTA of each sequence (a
+//                   completion counter, no spin-wait) finds the chunk and the
+//                   index where the prefix sum crosses the threshold with
+//                   block-wide scans;
 //   k_probs_out     optional diagnostic copy of p for every needed row.
 #include <math.h>
 
@@ -29,8 +31,13 @@
 namespace ssd {
 
 constexpr int kVocabThreads = 256;
+constexpr int kVec = 8;                 // 16-byte vectors per thread per stats chunk
 constexpr int kSelectThreads = 256;
-constexpr int kMaxRows = 2048;          // 1 + NB*Dmax + K
+constexpr int kMaxRows = 1024;          // 1 + NB*Dmax + K
+constexpr int kMaxSlots = 1024;         // NB*Dmax
+constexpr int kStage = 1024;            // chunk partials staged per pass in select
+constexpr int kSampleChunk = 2048;      // vocabulary entries per sampler CTA
+constexpr int kSamplePer = kSampleChunk / kVocabThreads;
 constexpr long long kOneWeight = 1LL << 40;
 
 __device__ __forceinline__ float load_val(const void* base, int64_t i, int bf16) {
@@ -38,20 +45,27 @@ __device__ __forceinline__ float load_val(const void* base, int64_t i, int bf16)
               : __ldg(static_cast<const float*>(base) + i);
 }
 
-// p of one entry: exp(l - max) / Z in fp32, or the value itself for probabilities
+// p of one entry: 2^((l - max) log2 e) / Z in fp32, or the value itself for probabilities
 __device__ __forceinline__ float prob_of(float v, const RowStat& st, int probs) {
-  return probs ? v : expf(v - st.m) / st.s;
+  return probs ? v : ex2_approx(fmaf(v, kLog2e, -st.m * kLog2e)) / st.s;
 }
 
-// P = floor(p * 2^40): exact for fp32 p in [0, 1]
+// P = floor(p * 2^40) for fp32 p in [0, 1], exactly, from the bits of p
 __device__ __forceinline__ long long weight_of(float p) {
-  return __double2ll_rd(static_cast<double>(p) * 1099511627776.0);
+  const uint32_t u = __float_as_uint(p);
+  if (static_cast<int32_t>(u) <= 0) return 0;            // +0 or negative
+  const int e = static_cast<int>(u >> 23);                // biased exponent (0: subnormal, < 2^-126)
+  if (e == 0) return 0;
+  const long long mant = static_cast<long long>((u & 0x7fffffu) | 0x800000u);
+  const int sh = e - 110;                                 // p * 2^40 = mant * 2^(e - 127 - 23 + 40)
+  if (sh >= 0) return mant << min(sh, 30);
+  return sh <= -24 ? 0 : (mant >> (-sh));
 }
 
 __device__ __forceinline__ void stat_merge(float& m, float& s, float m2, float s2) {
   const float M = fmaxf(m, m2);
   if (M == -INFINITY) return;
-  s = s * expf(m - M) + s2 * expf(m2 - M);
+  s = s * ex2_approx((m - M) * kLog2e) + s2 * ex2_approx((m2 - M) * kLog2e);
   m = M;
 }
 
@@ -79,138 +93,116 @@ __device__ __forceinline__ const void* row_ptr(const AcceptParams& p, int b, int
   return static_cast<const char*>(p.drf) + (static_cast<int64_t>(b) * p.K + (r - p.NR)) * p.V * es;
 }
 
-// ------------------------------------------------------------------ stats
-__device__ void vocab_stats_one(const AcceptParams& p, int b, int r, int c);
+// block-wide exclusive prefix sum over the 256 threads; *total gets the sum
+__device__ __forceinline__ long long block_excl_scan(long long v, long long* warp_tot, long long* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  long long incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  __syncthreads();
+  if (lane == 31) warp_tot[wid] = incl;
+  __syncthreads();
+  long long before = 0, all = 0;
+#pragma unroll
+  for (int w = 0; w < kVocabThreads / 32; ++w) {
+    const long long t = warp_tot[w];
+    if (w < wid) before += t;
+    all += t;
+  }
+  *total = all;
+  return before + incl - v;
+}
 
-__global__ void __launch_bounds__(kVocabThreads)
+// ------------------------------------------------------------------ stats
+// element e (0..EPV-1) of a 16-byte vector
+template <bool BF16>
+__device__ __forceinline__ float vec_elem(const uint4& u, int e) {
+  const uint32_t w = e < (BF16 ? 2 : 1) ? u.x : e < (BF16 ? 4 : 2) ? u.y : e < (BF16 ? 6 : 3) ? u.z : u.w;
+  if (BF16) return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
+  return __uint_as_float(w);
+}
+
+// One chunk of one row: every 16-byte load is issued before any use and the raw
+// vectors stay in registers (32 per thread) for the two passes.
+template <bool BF16>
+__device__ __forceinline__ void stats_chunk(const void* row, int64_t lo, int64_t hi, bool vec_ok, bool probs,
+                                            float& m, float& s, float& av, int& ai) {
+  constexpr int EPV = BF16 ? 8 : 4;    // elements per 16-byte vector
+  uint4 raw[kVec];
+  bool full[kVec];
+#pragma unroll
+  for (int v = 0; v < kVec; ++v) {
+    const int64_t i0 = lo + static_cast<int64_t>(v * kVocabThreads + threadIdx.x) * EPV;
+    full[v] = vec_ok && i0 + EPV <= hi;
+    if (full[v]) {
+      raw[v] = __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(row) + i0 * (BF16 ? 2 : 4)));
+    } else {
+      // ragged tail or unaligned row: gather the elements that exist, -inf elsewhere
+      uint32_t w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) w[q] = BF16 ? 0xff80ff80u : 0xff800000u;
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        if (i0 + e < hi) {
+          if (BF16) {
+            const uint32_t h = __ldg(static_cast<const uint16_t*>(row) + i0 + e);
+            w[e >> 1] = (e & 1) ? ((w[e >> 1] & 0xffffu) | (h << 16)) : ((w[e >> 1] & 0xffff0000u) | h);
+          } else {
+            w[e] = __float_as_uint(__ldg(static_cast<const float*>(row) + i0 + e));
+          }
+        }
+      }
+      raw[v] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+  av = -INFINITY;
+  ai = 0x7fffffff;
+#pragma unroll
+  for (int v = 0; v < kVec; ++v) {
+    const int i0 = static_cast<int>(lo + static_cast<int64_t>(v * kVocabThreads + threadIdx.x) * EPV);
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) {
+      const float x = vec_elem<BF16>(raw[v], e);
+      if (x > av) {                      // indices increase: strict > keeps the lowest on ties
+        av = x;
+        ai = i0 + e;
+      }
+    }
+  }
+  m = av;
+  s = 0.f;
+  if (!probs && m > -INFINITY) {
+    const float c = -m * kLog2e;
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int v = 0; v < kVec; ++v) {
+#pragma unroll
+      for (int e = 0; e < EPV; e += 2) {
+        s0 += ex2_approx(fmaf(vec_elem<BF16>(raw[v], e), kLog2e, c));
+        s1 += ex2_approx(fmaf(vec_elem<BF16>(raw[v], e + 1), kLog2e, c));
+      }
+    }
+    s = s0 + s1;
+  }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kVocabThreads, 3)
 k_vocab_stats(AcceptParams p) {
   const int c = blockIdx.x % p.nch, r = blockIdx.x / p.nch;
-  for (int b = blockIdx.y; b < p.B; b += gridDim.y) vocab_stats_one(p, b, r, c);
-}
-
-__device__ void vocab_stats_one(const AcceptParams& p, int b, int r, int c) {
-  if (!row_needed(p, b, r)) return;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int64_t lo = static_cast<int64_t>(c) * p.chunk;
-  const int64_t hi = min(p.V, lo + p.chunk);
-  const void* row = row_ptr(p, b, r);
-
-  float m = -INFINITY, s = 0.f, av = -INFINITY;
-  int ai = 0x7fffffff;
-  if (lo < hi) {
-    const bool vec_ok = aligned_dev(row, 16);
-    const int64_t n = hi - lo;
-    if (!p.bf16) {
-      const float* f = static_cast<const float*>(row);
-      int64_t nv = vec_ok ? n / 4 : 0;
-      const float4* f4 = reinterpret_cast<const float4*>(f + lo);
-      for (int64_t v = tid; v < nv; v += kVocabThreads) {
-        const float4 x = __ldg(f4 + v);
-        const int i0 = static_cast<int>(lo + v * 4);
-        if (x.x > av) { av = x.x; ai = i0; }
-        if (x.y > av) { av = x.y; ai = i0 + 1; }
-        if (x.z > av) { av = x.z; ai = i0 + 2; }
-        if (x.w > av) { av = x.w; ai = i0 + 3; }
-        if (!p.probs) {
-          const float mx = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
-          if (mx > m) { s *= expf(m - mx); m = mx; }
-          s += expf(x.x - m) + expf(x.y - m) + expf(x.z - m) + expf(x.w - m);
-        }
-      }
-      for (int64_t i = lo + nv * 4 + tid; i < hi; i += kVocabThreads) {
-        const float x = __ldg(f + i);
-        if (x > av) { av = x; ai = static_cast<int>(i); }
-        if (!p.probs) {
-          if (x > m) { s *= expf(m - x); m = x; }
-          s += expf(x - m);
-        }
-      }
-    } else {
-      const uint16_t* hb = static_cast<const uint16_t*>(row);
-      int64_t nv = vec_ok ? n / 8 : 0;
-      const uint4* h8 = reinterpret_cast<const uint4*>(hb + lo);
-      for (int64_t v = tid; v < nv; v += kVocabThreads) {
-        const uint4 u = __ldg(h8 + v);
-        const int i0 = static_cast<int>(lo + v * 8);
-        float x[8];
-        x[0] = __uint_as_float(u.x << 16); x[1] = __uint_as_float(u.x & 0xffff0000u);
-        x[2] = __uint_as_float(u.y << 16); x[3] = __uint_as_float(u.y & 0xffff0000u);
-        x[4] = __uint_as_float(u.z << 16); x[5] = __uint_as_float(u.z & 0xffff0000u);
-        x[6] = __uint_as_float(u.w << 16); x[7] = __uint_as_float(u.w & 0xffff0000u);
-        float mx = x[0];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          if (x[q] > av) { av = x[q]; ai = i0 + q; }
-          mx = fmaxf(mx, x[q]);
-        }
-        if (mx > m) { s *= expf(m - mx); m = mx; }
-        float acc = 0.f;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) acc += expf(x[q] - m);
-        s += acc;
-      }
-      for (int64_t i = lo + nv * 8 + tid; i < hi; i += kVocabThreads) {
-        const float x = bf16_to_f32(__ldg(hb + i));
-        if (x > av) { av = x; ai = static_cast<int>(i); }
-        if (x > m) { s *= expf(m - x); m = x; }
-        s += expf(x - m);
-      }
-    }
-  }
-  // block reduction
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    const float v2 = __shfl_xor_sync(0xffffffffu, av, o);
-    const int i2 = __shfl_xor_sync(0xffffffffu, ai, o);
-    stat_merge(m, s, m2, s2);
-    amax_merge(av, ai, v2, i2);
-  }
   __shared__ RowStat red[kVocabThreads / 32];
-  if (lane == 0) red[wid] = RowStat{m, s, av, ai};
-  __syncthreads();
-  if (tid == 0) {
-    for (int w = 1; w < kVocabThreads / 32; ++w) {
-      stat_merge(m, s, red[w].m, red[w].s);
-      amax_merge(av, ai, red[w].amax_v, red[w].amax_i);
-    }
-    p.part[(static_cast<int64_t>(b) * p.NRD + r) * p.nch + c] = RowStat{m, s, av, ai};
-  }
-  __syncthreads();   // red[] is reused by the next sequence of this CTA
-}
-
-// ------------------------------------------------------------------ select
-__global__ void __launch_bounds__(kSelectThreads)
-k_accept_select(AcceptParams p) {
-  __shared__ RowStat st[kMaxRows];
-  __shared__ int acc_s[256];
-  __shared__ int len_s[256];
-  __shared__ int sel[4];   // best block, a, len, final (greedy)
-  const int b = blockIdx.x;
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  constexpr int nw = kSelectThreads / 32;
-
-  // block lengths, clamped to the slots that exist (a chain block to K draft rows)
-  for (int k = tid; k < p.NB; k += kSelectThreads) {
-    const int raw = p.blk_len[b * p.NB + k];
-    const int cap = (k == p.chain_blk) ? min(p.Dmax, p.K) : p.Dmax;
-    const int L = min(max(raw, 0), cap);
-    if (L != raw) record_error(p.hdr, SSD_ERR_DEVICE, 101);
-    len_s[k] = L;
-  }
-
-  // 1. merge the chunks of every needed row
-  for (int r = wid; r < p.NRD; r += nw) {
+  for (int b = blockIdx.y; b < p.B; b += gridDim.y) {
     if (!row_needed(p, b, r)) continue;
-    float m = -INFINITY, s = 0.f, av = -INFINITY;
-    int ai = 0x7fffffff;
-    const RowStat* pr = p.part + (static_cast<int64_t>(b) * p.NRD + r) * p.nch;
-    for (int c = lane; c < p.nch; c += 32) {
-      const RowStat x = pr[c];
-      stat_merge(m, s, x.m, x.s);
-      amax_merge(av, ai, x.amax_v, x.amax_i);
-    }
+    const int64_t lo = static_cast<int64_t>(c) * p.chunk;
+    const int64_t hi = min(p.V, lo + p.chunk);
+    const void* row = row_ptr(p, b, r);
+    float m, s, av;
+    int ai;
+    stats_chunk<BF16>(row, lo, hi, aligned_dev(row, 16), p.probs, m, s, av, ai);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
@@ -220,55 +212,156 @@ k_accept_select(AcceptParams p) {
       stat_merge(m, s, m2, s2);
       amax_merge(av, ai, v2, i2);
     }
-    if (lane == 0) {
-      const RowStat x{m, s, av, ai};
-      st[r] = x;
-      p.stat[static_cast<int64_t>(b) * p.NRD + r] = x;
+    if (lane == 0) red[wid] = RowStat{m, s, av, ai};
+    __syncthreads();
+    if (tid == 0) {
+      for (int w = 1; w < kVocabThreads / 32; ++w) {
+        stat_merge(m, s, red[w].m, red[w].s);
+        amax_merge(av, ai, red[w].amax_v, red[w].amax_i);
+      }
+      p.part[(static_cast<int64_t>(b) * p.NRD + r) * p.nch + c] = RowStat{m, s, av, ai};
     }
+    __syncthreads();   // red[] is reused by the next sequence of this CTA
   }
-  __syncthreads();
+}
 
-  // 2. acceptance scan: one warp per block, one lane per token
-  for (int k = wid; k < p.NB; k += nw) {
-    const int L = len_s[k];
-    const bool chain = (k == p.chain_blk);
-    int a = 0;
-    for (int d0 = 0; d0 < L; d0 += 32) {
-      const int d = d0 + lane;
-      bool ok = false;
+// ------------------------------------------------------------------ select
+constexpr int kSlotsPer = kMaxSlots / kSelectThreads;
+
+__global__ void __launch_bounds__(kSelectThreads)
+k_accept_select(AcceptParams p) {
+  __shared__ RowStat st[kMaxRows];
+  __shared__ RowStat stage[kStage];
+  __shared__ int len_s[256];
+  __shared__ int acc_s[256];
+  __shared__ unsigned char ok_s[kMaxSlots];
+  __shared__ int sel[4];   // best block, a, len, final (greedy)
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  constexpr int nw = kSelectThreads / 32;
+  const int nslots = p.NB * p.Dmax;
+
+  // 1. per token slot: its token, its block's length, its uniform and the logits
+  //    the acceptance test needs; every load is issued before the row merge
+  int x_[kSlotsPer], row_[kSlotsPer];
+  bool live_[kSlotsPer];
+  float lp_[kSlotsPer], lq_[kSlotsPer], u_[kSlotsPer];
+#pragma unroll
+  for (int k = 0; k < kSlotsPer; ++k) {
+    const int sl = tid + k * kSelectThreads;
+    live_[k] = false;
+    x_[k] = 0;
+    row_[k] = 0;
+    lp_[k] = 0.f;
+    lq_[k] = 0.f;
+    u_[k] = 0.f;
+    if (sl < nslots) {
+      const int blk = sl / p.Dmax, d = sl % p.Dmax;
+      const int raw = p.blk_len[b * p.NB + blk];
+      const int cap = (blk == p.chain_blk) ? min(p.Dmax, p.K) : p.Dmax;
+      const int L = min(max(raw, 0), cap);
       if (d < L) {
-        const int x = p.blk_tok[(static_cast<int64_t>(b) * p.NB + k) * p.Dmax + d];
-        const int r = d == 0 ? 0 : 1 + k * p.Dmax + d - 1;
+        const int x = p.blk_tok[static_cast<int64_t>(b) * nslots + sl];
         if (x < 0 || x >= p.V) {
           record_error(p.hdr, SSD_ERR_DEVICE, 100);
-        } else if (!p.sample) {
-          ok = (x == st[r].amax_i);
         } else {
-          const float px = prob_of(load_val(row_ptr(p, b, r), x, p.bf16), st[r], p.probs);
-          float qx = 1.f;
-          if (chain) qx = prob_of(load_val(row_ptr(p, b, p.NR + d), x, p.bf16), st[p.NR + d], p.probs);
-          const float u = p.u_acc[(static_cast<int64_t>(b) * p.NB + k) * p.Dmax + d];
-          ok = __dmul_rn(static_cast<double>(u), static_cast<double>(qx)) < static_cast<double>(px);
+          live_[k] = true;
+          x_[k] = x;
+          row_[k] = d == 0 ? 0 : 1 + blk * p.Dmax + d - 1;
+          if (p.sample) {
+            lp_[k] = load_val(row_ptr(p, b, row_[k]), x, p.bf16);
+            if (blk == p.chain_blk) lq_[k] = load_val(row_ptr(p, b, p.NR + d), x, p.bf16);
+            u_[k] = p.u_acc[static_cast<int64_t>(b) * nslots + sl];
+          }
         }
       }
-      const unsigned bal = __ballot_sync(0xffffffffu, ok);
-      const int run = __ffs(~bal) - 1;          // leading accepted lanes (-1 if all 32)
-      if (run < 0) {
-        a += min(32, L - d0);
-        if (L - d0 <= 32) break;
-      } else {
-        a += min(run, L - d0);
-        break;
+    }
+  }
+  for (int k = tid; k < p.NB; k += kSelectThreads) {
+    const int raw = p.blk_len[b * p.NB + k];
+    const int cap = (k == p.chain_blk) ? min(p.Dmax, p.K) : p.Dmax;
+    const int L = min(max(raw, 0), cap);
+    if (L != raw) record_error(p.hdr, SSD_ERR_DEVICE, 101);
+    len_s[k] = L;
+  }
+
+  // 2. merge the vocabulary chunks of every needed row (partials staged in passes)
+  const int rows_pass = max(1, kStage / p.nch);
+  for (int r0 = 0; r0 < p.NRD; r0 += rows_pass) {
+    const int nr = min(rows_pass, p.NRD - r0);
+    const int ne = nr * p.nch;
+    const RowStat* src = p.part + (static_cast<int64_t>(b) * p.NRD + r0) * p.nch;
+    RowStat tmp[kStage / kSelectThreads];
+#pragma unroll
+    for (int k = 0; k < kStage / kSelectThreads; ++k) {
+      const int e = tid + k * kSelectThreads;
+      if (e < ne) tmp[k] = src[e];
+    }
+#pragma unroll
+    for (int k = 0; k < kStage / kSelectThreads; ++k) {
+      const int e = tid + k * kSelectThreads;
+      if (e < ne) stage[e] = tmp[k];
+    }
+    __syncthreads();
+    for (int rr = wid; rr < nr; rr += nw) {
+      const int r = r0 + rr;
+      if (!row_needed(p, b, r)) continue;
+      float m = -INFINITY, s = 0.f, av = -INFINITY;
+      int ai = 0x7fffffff;
+      for (int c = lane; c < p.nch; c += 32) {
+        const RowStat x = stage[rr * p.nch + c];
+        stat_merge(m, s, x.m, x.s);
+        amax_merge(av, ai, x.amax_v, x.amax_i);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        const float v2 = __shfl_xor_sync(0xffffffffu, av, o);
+        const int i2 = __shfl_xor_sync(0xffffffffu, ai, o);
+        stat_merge(m, s, m2, s2);
+        amax_merge(av, ai, v2, i2);
+      }
+      if (lane == 0) {
+        const RowStat x{m, s, av, ai};
+        st[r] = x;
+        p.stat[static_cast<int64_t>(b) * p.NRD + r] = x;
       }
     }
-    if (lane == 0) {
-      acc_s[k] = a;
-      p.acc_len[b * p.NB + k] = a;
+    __syncthreads();
+  }
+
+  // 3. acceptance test of every present token
+#pragma unroll
+  for (int k = 0; k < kSlotsPer; ++k) {
+    const int sl = tid + k * kSelectThreads;
+    if (sl >= nslots) continue;
+    bool ok = false;
+    if (live_[k]) {
+      const int blk = sl / p.Dmax, d = sl % p.Dmax;
+      if (!p.sample) {
+        ok = (x_[k] == st[row_[k]].amax_i);
+      } else {
+        const float px = prob_of(lp_[k], st[row_[k]], p.probs);
+        const float qx = (blk == p.chain_blk) ? prob_of(lq_[k], st[p.NR + d], p.probs) : 1.f;
+        ok = __dmul_rn(static_cast<double>(u_[k]), static_cast<double>(qx)) < static_cast<double>(px);
+      }
     }
+    ok_s[sl] = ok ? 1 : 0;
   }
   __syncthreads();
 
-  // 3. longest accepted run, lowest block index on ties
+  // 4. leading accepted run of every block
+  for (int k = tid; k < p.NB; k += kSelectThreads) {
+    const int L = len_s[k];
+    int a = 0;
+    while (a < L && ok_s[k * p.Dmax + a]) ++a;
+    acc_s[k] = a;
+    p.acc_len[b * p.NB + k] = a;
+  }
+  __syncthreads();
+
+  // 5. longest accepted run, lowest block index on ties
   if (tid == 0) {
     int best = -1, ba = -1;
     for (int k = 0; k < p.NB; ++k) {
@@ -295,7 +388,7 @@ k_accept_select(AcceptParams p) {
       si.bonus = (a >= L) ? 1 : 0;
       if (a < L) {
         if (best == p.chain_blk) si.drf_row = a;
-        else si.excl = p.blk_tok[(static_cast<int64_t>(b) * p.NB + best) * p.Dmax + a];
+        else si.excl = p.blk_tok[static_cast<int64_t>(b) * nslots + best * p.Dmax + a];
       }
       p.stop[b] = si;
       p.cnt[b] = 0u;
@@ -303,72 +396,77 @@ k_accept_select(AcceptParams p) {
   }
   __syncthreads();
 
-  // 4. emitted tokens (the sampler fills the final one in sample mode)
+  // 6. emitted tokens (the sampler fills the final one in sample mode)
   const int best = sel[0], a = sel[1];
   for (int i = tid; i <= p.Dmax; i += kSelectThreads) {
     int v = -1;
-    if (i < a) v = p.blk_tok[(static_cast<int64_t>(b) * p.NB + best) * p.Dmax + i];
+    if (i < a) v = p.blk_tok[static_cast<int64_t>(b) * nslots + best * p.Dmax + i];
     else if (i == a && !p.sample) v = sel[3];
     p.out_tok[static_cast<int64_t>(b) * (p.Dmax + 1) + i] = v;
   }
 }
 
 // ------------------------------------------------------------------ final draw
-__device__ __forceinline__ void weights_at(const AcceptParams& p, const void* prow, const RowStat& ps,
-                                           const void* qrow, const RowStat& qs, int excl, int bonus,
-                                           int64_t i, long long& W, long long& P) {
-  P = weight_of(prob_of(load_val(prow, i, p.bf16), ps, p.probs));
+// residual (or bonus) weight of entry i given its p and q values
+__device__ __forceinline__ void weights_of(const AcceptParams& p, float pv, const RowStat& ps, bool has_q, float qv,
+                                           const RowStat& qs, int excl, int bonus, int64_t i, long long& W,
+                                           long long& P) {
+  P = weight_of(prob_of(pv, ps, p.probs));
   if (bonus) {
     W = P;
     return;
   }
-  long long Q;
-  if (qrow != nullptr) Q = weight_of(prob_of(load_val(qrow, i, p.bf16), qs, p.probs));
-  else Q = (i == excl) ? kOneWeight : 0LL;
+  const long long Q = has_q ? weight_of(prob_of(qv, qs, p.probs)) : ((i == excl) ? kOneWeight : 0LL);
   W = P > Q ? P - Q : 0LL;
-}
-
-__device__ void sample_final_one(const AcceptParams& p, int b, int c);
-
-__global__ void __launch_bounds__(kVocabThreads)
-k_sample_final(AcceptParams p) {
-  for (int b = blockIdx.y; b < p.B; b += gridDim.y) {
-    sample_final_one(p, b, blockIdx.x);
-    __syncthreads();   // shared state is reused by the next sequence of this CTA
-  }
 }
 
 __device__ void sample_final_one(const AcceptParams& p, int b, int c) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   constexpr int nw = kVocabThreads / 32;
   __shared__ long long red_w[nw], red_p[nw];
-  __shared__ int is_last;
+  __shared__ int is_last, c_star, use_bonus;
   __shared__ long long t_rem;
-  __shared__ int c_star, use_bonus;
 
   const StopInfo si = p.stop[b];
   const void* prow = row_ptr(p, b, si.row);
   const RowStat ps = p.stat[static_cast<int64_t>(b) * p.NRD + si.row];
-  const void* qrow = si.drf_row >= 0 ? row_ptr(p, b, p.NR + si.drf_row) : nullptr;
-  const RowStat qs = si.drf_row >= 0 ? p.stat[static_cast<int64_t>(b) * p.NRD + p.NR + si.drf_row] : ps;
+  const bool has_q = si.drf_row >= 0;
+  const void* qrow = has_q ? row_ptr(p, b, p.NR + si.drf_row) : prow;
+  const RowStat qs = has_q ? p.stat[static_cast<int64_t>(b) * p.NRD + p.NR + si.drf_row] : ps;
 
-  // phase 1: this chunk's residual and bonus weight sums
-  const int64_t lo = static_cast<int64_t>(c) * p.schunk;
-  const int64_t hi = min(p.V, lo + p.schunk);
+  // phase 1: this chunk's residual and bonus weight sums (all loads first)
+  const int64_t lo = static_cast<int64_t>(c) * kSampleChunk;
+  float pv[kSamplePer], qv[kSamplePer];
+#pragma unroll
+  for (int k = 0; k < kSamplePer; ++k) {
+    const int64_t i = lo + k * kVocabThreads + tid;
+    pv[k] = i < p.V ? load_val(prow, i, p.bf16) : 0.f;
+    qv[k] = (has_q && i < p.V) ? load_val(qrow, i, p.bf16) : 0.f;
+  }
   long long sw = 0, sp = 0;
-  for (int64_t i = lo + tid; i < hi; i += kVocabThreads) {
-    long long W, P;
-    weights_at(p, prow, ps, qrow, qs, si.excl, si.bonus, i, W, P);
-    sw += W;
-    sp += P;
+#pragma unroll
+  for (int k = 0; k < kSamplePer; ++k) {
+    const int64_t i = lo + k * kVocabThreads + tid;
+    if (i < p.V) {
+      long long W, P;
+      weights_of(p, pv[k], ps, has_q, qv[k], qs, si.excl, si.bonus, i, W, P);
+      sw += W;
+      sp += P;
+    }
   }
   sw = warp_sum(sw);
   sp = warp_sum(sp);
-  if (lane == 0) { red_w[wid] = sw; red_p[wid] = sp; }
+  if (lane == 0) {
+    red_w[wid] = sw;
+    red_p[wid] = sp;
+  }
   __syncthreads();
   if (tid == 0) {
     long long tw = 0, tp = 0;
-    for (int w = 0; w < nw; ++w) { tw += red_w[w]; tp += red_p[w]; }
+    for (int w = 0; w < nw; ++w) {
+      tw += red_w[w];
+      tp += red_p[w];
+    }
     p.csum[(static_cast<int64_t>(b) * p.nchs + c) * 2 + 0] = tw;
     p.csum[(static_cast<int64_t>(b) * p.nchs + c) * 2 + 1] = tp;
     __threadfence();
@@ -379,66 +477,90 @@ __device__ void sample_final_one(const AcceptParams& p, int b, int c) {
   if (!is_last) return;
   __threadfence();
 
-  // phase 2 (last CTA of this sequence): threshold, chunk, index
-  if (tid == 0) {
-    const volatile long long* cs = p.csum + static_cast<int64_t>(b) * p.nchs * 2;
-    long long SW = 0, SP = 0;
-    for (int k = 0; k < p.nchs; ++k) { SW += cs[2 * k]; SP += cs[2 * k + 1]; }
-    const int ub = (si.bonus || SW == 0) ? 1 : 0;
-    const unsigned long long S = static_cast<unsigned long long>(ub ? SP : SW);
-    const float u = fminf(fmaxf(p.u_fin[b], 0.f), 0.99999994f);   // contract: u in [0, 1)
-    const unsigned long long U = static_cast<unsigned long long>(u * 16777216.0f);   // floor(u 2^24), exact
-    const unsigned long long lo64 = U * S;
-    const unsigned long long hi64 = __umul64hi(U, S);
-    const long long T = static_cast<long long>((hi64 << 40) | (lo64 >> 24));
-    long long acc = 0;
-    int cs_i = p.nchs - 1;
-    for (int k = 0; k < p.nchs; ++k) {
-      const long long wk = cs[2 * k + (ub ? 1 : 0)];
-      if (acc + wk > T) { cs_i = k; break; }
+  // phase 2 (last CTA of this sequence): totals, threshold, chunk
+  // each thread owns a contiguous run of chunks
+  const int cpt = (p.nchs + kVocabThreads - 1) / kVocabThreads;
+  const int c_lo = min(p.nchs, tid * cpt), c_hi = min(p.nchs, c_lo + cpt);
+  const volatile long long* cs = p.csum + static_cast<int64_t>(b) * p.nchs * 2;
+  if (tid == 0) {            // defaults if no weight is positive (degenerate rows)
+    c_star = 0;
+    t_rem = 0;
+    use_bonus = 1;
+  }
+  long long mw = 0, mp = 0;
+  for (int k = c_lo; k < c_hi; ++k) {
+    mw += cs[2 * k];
+    mp += cs[2 * k + 1];
+  }
+  long long SW, SP;
+  const long long ew = block_excl_scan(mw, red_w, &SW);
+  const long long ep = block_excl_scan(mp, red_p, &SP);
+  const int ub = (si.bonus || SW == 0) ? 1 : 0;
+  const unsigned long long S = static_cast<unsigned long long>(ub ? SP : SW);
+  const float u = fminf(fmaxf(p.u_fin[b], 0.f), 0.99999994f);               // contract: u in [0, 1)
+  const unsigned long long U = static_cast<unsigned long long>(u * 16777216.0f);   // floor(u 2^24), exact
+  const long long T = static_cast<long long>((__umul64hi(U, S) << 40) | ((U * S) >> 24));
+  const long long mine = ub ? mp : mw, excl = ub ? ep : ew;
+  if (mine > 0 && excl <= T && T < excl + mine) {
+    long long acc = excl;
+    int cst = c_hi - 1;
+    for (int k = c_lo; k < c_hi; ++k) {
+      const long long wk = cs[2 * k + ub];
+      if (acc + wk > T) {
+        cst = k;
+        break;
+      }
       acc += wk;
     }
-    c_star = cs_i;
+    c_star = cst;
     t_rem = T - acc;
     use_bonus = ub;
-    p.cnt[b] = 0u;
   }
+  if (tid == 0) p.cnt[b] = 0u;
   __syncthreads();
-  const int64_t lo2 = static_cast<int64_t>(c_star) * p.schunk;
-  const int64_t hi2 = min(p.V, lo2 + p.schunk);
-  const int64_t per = (hi2 - lo2 + kVocabThreads - 1) / kVocabThreads;
-  const int64_t my_lo = min(hi2, lo2 + tid * per), my_hi = min(hi2, my_lo + per);
-  const int ub = use_bonus;
-  long long mine = 0;
-  for (int64_t i = my_lo; i < my_hi; ++i) {
-    long long W, P;
-    weights_at(p, prow, ps, qrow, qs, si.excl, si.bonus, i, W, P);
-    mine += ub ? P : W;
-  }
-  // exclusive block scan of `mine`
-  long long incl = mine;
+
+  // phase 3: the index inside chunk c_star; each thread owns kSamplePer contiguous entries
+  const int64_t lo2 = static_cast<int64_t>(c_star) * kSampleChunk + tid * kSamplePer;
+  const int ub2 = use_bonus;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const long long y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
+  for (int k = 0; k < kSamplePer; ++k) {
+    const int64_t i = lo2 + k;
+    pv[k] = i < p.V ? load_val(prow, i, p.bf16) : 0.f;
+    qv[k] = (has_q && i < p.V) ? load_val(qrow, i, p.bf16) : 0.f;
   }
-  __syncthreads();
-  if (lane == 31) red_w[wid] = incl;
-  __syncthreads();
-  long long wofs = 0;
-  for (int w = 0; w < wid; ++w) wofs += red_w[w];
-  const long long excl = wofs + incl - mine;
+  long long wv[kSamplePer];
+  long long my = 0;
+#pragma unroll
+  for (int k = 0; k < kSamplePer; ++k) {
+    const int64_t i = lo2 + k;
+    long long W = 0, P = 0;
+    if (i < p.V) weights_of(p, pv[k], ps, has_q, qv[k], qs, si.excl, si.bonus, i, W, P);
+    wv[k] = ub2 ? P : W;
+    my += wv[k];
+  }
+  long long tot;
+  const long long ex = block_excl_scan(my, red_w, &tot);
   const long long Tr = t_rem;
-  if (mine > 0 && excl <= Tr && Tr < excl + mine) {
-    long long acc = excl;
-    int64_t tok = my_hi - 1;
-    for (int64_t i = my_lo; i < my_hi; ++i) {
-      long long W, P;
-      weights_at(p, prow, ps, qrow, qs, si.excl, si.bonus, i, W, P);
-      acc += ub ? P : W;
-      if (acc > Tr) { tok = i; break; }
+  if (my > 0 && ex <= Tr && Tr < ex + my) {
+    long long acc = ex;
+    int64_t tok = lo2 + kSamplePer - 1;
+#pragma unroll
+    for (int k = 0; k < kSamplePer; ++k) {
+      acc += wv[k];
+      if (acc > Tr) {
+        tok = lo2 + k;
+        break;
+      }
     }
     p.out_tok[static_cast<int64_t>(b) * (p.Dmax + 1) + si.a] = static_cast<int>(tok);
+  }
+}
+
+__global__ void __launch_bounds__(kVocabThreads)
+k_sample_final(AcceptParams p) {
+  for (int b = blockIdx.y; b < p.B; b += gridDim.y) {
+    sample_final_one(p, b, blockIdx.x);
+    __syncthreads();   // shared state is reused by the next sequence of this CTA
   }
 }
 
@@ -465,29 +587,12 @@ AcceptLayout accept_layout(const ssd_accept_args* a) {
   const int NRD = NR + (a->chain_blk >= 0 ? a->K : 0);
   L.NR = NR;
   L.NRD = NRD;
-  // vocabulary chunks per row: about 8 CTAs per SM in total, multiples of 8 elements
-  const long long rows = static_cast<long long>(a->B) * NRD;
-  long long nch = (8LL * 152 + rows - 1) / (rows > 0 ? rows : 1);
-  const long long max_nch = (a->V + 2047) / 2048;            // at least 2048 elements per chunk
-  if (nch > max_nch) nch = max_nch;
-  if (nch > 64) nch = 64;
-  if (nch < 1) nch = 1;
-  long long chunk = (a->V + nch - 1) / nch;
-  chunk = (chunk + 7) / 8 * 8;
-  nch = (a->V + chunk - 1) / chunk;
-  L.nch = static_cast<int>(nch);
-  L.chunk = chunk;
-  // sampler chunks: about 2 CTAs per SM over the batch
-  long long nchs = (2LL * 152 + a->B - 1) / (a->B > 0 ? a->B : 1);
-  const long long max_nchs = (a->V + 1023) / 1024;
-  if (nchs > max_nchs) nchs = max_nchs;
-  if (nchs > 128) nchs = 128;
-  if (nchs < 1) nchs = 1;
-  long long schunk = (a->V + nchs - 1) / nchs;
-  schunk = (schunk + 7) / 8 * 8;
-  nchs = (a->V + schunk - 1) / schunk;
-  L.nchs = static_cast<int>(nchs);
-  L.schunk = schunk;
+  // a stats chunk is one 16-byte vector per thread per step: 8 x 256 vectors
+  const int64_t epv = (a->kind == SSD_LOGITS_BF16) ? 8 : 4;
+  L.chunk = static_cast<int64_t>(kVec) * kVocabThreads * epv;
+  L.nch = static_cast<int>((a->V + L.chunk - 1) / L.chunk);
+  L.schunk = kSampleChunk;
+  L.nchs = static_cast<int>((a->V + kSampleChunk - 1) / kSampleChunk);
 
   size_t off = sizeof(WsHeader);
   L.part_off = off;
@@ -510,9 +615,9 @@ int accept_validate(const ssd_accept_args* a) {
   if (a->kind != SSD_LOGITS_F32 && a->kind != SSD_LOGITS_BF16 && a->kind != SSD_PROBS_F32) return SSD_ERR_INVALID;
   if (a->B < 0 || a->NB < 1 || a->Dmax < 1 || a->K < 0 || a->V < 2) return SSD_ERR_INVALID;
   if (a->V >= (1LL << 31)) return SSD_ERR_UNSUPPORTED;
-  if (a->Dmax > 256) return SSD_ERR_UNSUPPORTED;
+  if (a->Dmax > 256 || a->NB > 256) return SSD_ERR_UNSUPPORTED;
   if (a->chain_blk < -1 || a->chain_blk >= a->NB) return SSD_ERR_INVALID;
-  if (a->NB > 256) return SSD_ERR_UNSUPPORTED;
+  if (static_cast<long long>(a->NB) * a->Dmax > kMaxSlots) return SSD_ERR_UNSUPPORTED;
   const long long nrd = 1LL + static_cast<long long>(a->NB) * a->Dmax + (a->chain_blk >= 0 ? a->K : 0);
   if (nrd > kMaxRows) return SSD_ERR_UNSUPPORTED;
   if (a->chain_blk >= 0 && (a->K < 1 || a->K > a->Dmax)) return SSD_ERR_INVALID;
@@ -554,7 +659,8 @@ int accept_launch(const AcceptParams& p, cudaStream_t s) {
   dim3 g1(static_cast<unsigned>(p.nch * p.NRD), by);
   {
     KernelTimer t(SSD_KERNEL_VOCAB_STATS, s);
-    k_vocab_stats<<<g1, kVocabThreads, 0, s>>>(p);
+    if (p.bf16) k_vocab_stats<true><<<g1, kVocabThreads, 0, s>>>(p);
+    else k_vocab_stats<false><<<g1, kVocabThreads, 0, s>>>(p);
   }
   {
     KernelTimer t(SSD_KERNEL_ACCEPT_SELECT, s);

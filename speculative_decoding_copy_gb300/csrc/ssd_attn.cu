@@ -168,46 +168,96 @@ k_attn_combine(AttnParams p) {
   const int kvh = h / G;
   const int k = t / p.Dmax, pos = t % p.Dmax;
 
+  constexpr int KG = 8;          // own-block keys whose loads are issued together
   const T* q = static_cast<const T*>(p.q) + R * DH;
+  const T* kd = static_cast<const T*>(p.k_cand);
+  const T* vd = static_cast<const T*>(p.v_cand);
+  const int64_t kv_row0 = (static_cast<int64_t>(b) * NT + k * p.Dmax) * p.Hkv + kvh;   // slot k*Dmax, head kvh
+  const int64_t kv_step = static_cast<int64_t>(p.Hkv) * DH;                            // next slot
   float qv[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) qv[e] = ld_elem(q, lane + 32 * e) * p.scale_log2;
 
-  // own-block keys: slots k*Dmax .. t
-  const T* kd = static_cast<const T*>(p.k_cand);
-  const T* vd = static_cast<const T*>(p.v_cand);
-  float M = -INFINITY;
-  for (int c = 0; c <= pos; ++c) {
-    const int64_t base = ((static_cast<int64_t>(b) * NT + k * p.Dmax + c) * p.Hkv + kvh) * DH;
-    float s = 0.f;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) s = fmaf(qv[e], ld_elem(kd, base + lane + 32 * e), s);
-    s = warp_sum(s);
-    if (lane == 0) sc_s[wid][c] = s;
-    M = fmaxf(M, s);
-  }
+  // per-split running max: lane s holds split s
   const float* ml = p.ws_ml + R * p.S * 2;
-  for (int s = 0; s < p.S; ++s) M = fmaxf(M, ml[2 * s]);
+  float M = -INFINITY;
+  for (int s = lane; s < p.S; s += 32) M = fmaxf(M, ml[2 * s]);
+  M = warp_max(M);
+
+  // own-block keys: slots k*Dmax .. t, scores in groups of KG
+  for (int c0 = 0; c0 <= pos; c0 += KG) {
+    float kk[KG][EPL];
+#pragma unroll
+    for (int g = 0; g < KG; ++g) {
+      const int c = c0 + g;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e)
+        kk[g][e] = c <= pos ? ld_elem(kd, (kv_row0 + c * (p.Hkv)) * DH + lane + 32 * e) : 0.f;
+    }
+    float sc[KG];
+#pragma unroll
+    for (int g = 0; g < KG; ++g) {
+      float s = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) s = fmaf(qv[e], kk[g][e], s);
+      sc[g] = s;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int g = 0; g < KG; ++g) sc[g] += __shfl_xor_sync(0xffffffffu, sc[g], o);
+#pragma unroll
+    for (int g = 0; g < KG; ++g) {
+      if (c0 + g <= pos) {
+        if (lane == 0) sc_s[wid][c0 + g] = sc[g];
+        M = fmaxf(M, sc[g]);
+      }
+    }
+  }
   __syncwarp();
+  (void)kv_step;
 
   float L = 0.f, O[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) O[e] = 0.f;
+  // splits: loads of four splits in flight at a time
   const float* ow = p.ws_o + R * p.S * DH;
-  for (int s = 0; s < p.S; ++s) {
-    const float ms = ml[2 * s];
-    if (ms == -INFINITY) continue;
-    const float f = exp2f(ms - M);
-    L += ml[2 * s + 1] * f;
+  for (int s0 = 0; s0 < p.S; s0 += 4) {
+    float ms[4], ls[4], ov[4][EPL];
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) O[e] = fmaf(f, ow[s * DH + lane + 32 * e], O[e]);
+    for (int g = 0; g < 4; ++g) {
+      const int s = s0 + g;
+      ms[g] = s < p.S ? ml[2 * s] : -INFINITY;
+      ls[g] = s < p.S ? ml[2 * s + 1] : 0.f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) ov[g][e] = s < p.S ? ow[s * DH + lane + 32 * e] : 0.f;
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      if (ms[g] == -INFINITY) continue;
+      const float f = exp2f(ms[g] - M);
+      L += ls[g] * f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) O[e] = fmaf(f, ov[g][e], O[e]);
+    }
   }
-  for (int c = 0; c <= pos; ++c) {
-    const float f = exp2f(sc_s[wid][c] - M);
-    L += f;
-    const int64_t base = ((static_cast<int64_t>(b) * NT + k * p.Dmax + c) * p.Hkv + kvh) * DH;
+  for (int c0 = 0; c0 <= pos; c0 += KG) {
+    float vv[KG][EPL];
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) O[e] = fmaf(f, ld_elem(vd, base + lane + 32 * e), O[e]);
+    for (int g = 0; g < KG; ++g) {
+      const int c = c0 + g;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e)
+        vv[g][e] = c <= pos ? ld_elem(vd, (kv_row0 + c * (p.Hkv)) * DH + lane + 32 * e) : 0.f;
+    }
+#pragma unroll
+    for (int g = 0; g < KG; ++g) {
+      if (c0 + g > pos) continue;
+      const float f = exp2f(sc_s[wid][c0 + g] - M);
+      L += f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) O[e] = fmaf(f, vv[g][e], O[e]);
+    }
   }
   const float inv = 1.f / L;
   T* out = static_cast<T*>(p.out) + R * DH;

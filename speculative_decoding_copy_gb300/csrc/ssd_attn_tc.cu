@@ -12,11 +12,14 @@
 //   warps 0-3  one thread per packed row: stage Q, online softmax from the S
 //              row in TMEM (tcgen05.ld), O rescale in TMEM, P as bf16 into
 //              shared memory, epilogue;
-//   warp 4     TMA producer: K and V tiles of 128 keys (two 64-wide halves,
-//              128-byte swizzle) into a 2-stage ring;
+//   warp 4     TMA producer: K and V tiles of 64 keys (two 64-wide halves of
+//              the head dim, 128-byte swizzle) into a 4-stage ring;
 //   warp 5     TMEM allocation and the single MMA-issuing thread:
-//              S = Q K^T (M128 N128 K16 x 8) and O += P V (M128 N128 K16 x 8),
-//              kind::f16 with bf16 operands and fp32 accumulators in TMEM.
+//              S = Q K^T (M128 N64, K16 x 8) into one of two TMEM buffers and
+//              O += P V (M128 N128, K16 x 4), kind::f16 with bf16 operands and
+//              fp32 accumulators in TMEM. S of tile j+1 is issued before P V of
+//              tile j so the tensor core works while the rows run the softmax;
+//              P is double-buffered in shared memory.
 // Every mbarrier wait is bounded (about 2^32 clocks); on expiry the CTA
 // records SSD_ERR_TIMEOUT in the workspace header, skips the remaining waits,
 // frees its TMEM and exits.
@@ -32,23 +35,25 @@ namespace tc {
 
 constexpr int DH = 128;
 constexpr int BM = 128;                   // packed rows per CTA
-constexpr int BN = 128;                   // keys per tile
-constexpr int STAGES = 2;
+constexpr int BN = 64;                    // keys per tile
+constexpr int STAGES = 4;                 // K/V ring depth
 constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 256;       // S: cols 0-127, O: cols 128-255
-constexpr uint32_t kHalf = 128 * 128;     // one 64-wide half of a 128-row bf16 tile: 16 KB
+constexpr uint32_t kTmemCols = 256;       // S buffers: cols 0-63 and 64-127, O: cols 128-255
+constexpr uint32_t kQHalf = BM * 128;     // 128 rows x 64 bf16 (one 128-byte-swizzled half): 16 KB
+constexpr uint32_t kKVHalf = BN * 128;    // 64 keys x 64 bf16: 8 KB
+constexpr uint32_t kPBuf = BM * 128;      // 128 rows x 64 keys bf16: 16 KB
 constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_K = OFF_Q + 2 * kHalf;
-constexpr uint32_t OFF_V = OFF_K + STAGES * 2 * kHalf;
-constexpr uint32_t OFF_P = OFF_V + STAGES * 2 * kHalf;
-constexpr uint32_t OFF_BAR = OFF_P + 2 * kHalf;
+constexpr uint32_t OFF_K = OFF_Q + 2 * kQHalf;
+constexpr uint32_t OFF_V = OFF_K + STAGES * 2 * kKVHalf;
+constexpr uint32_t OFF_P = OFF_V + STAGES * 2 * kKVHalf;
+constexpr uint32_t OFF_BAR = OFF_P + 2 * kPBuf;
 constexpr uint32_t kSmemBytes = OFF_BAR + 256 + 1024;   // + slack to align the base to 1024
 constexpr unsigned long long kWaitClocks = 1ull << 32;
-
 struct Bars {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
-  uint64_t q_full, s_full, s_free, p_full, o_done;
+  uint64_t q_full;
+  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
   uint32_t tmem_base;
   int failed;
 };
@@ -122,13 +127,13 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
   return d;
 }
 
-// instruction descriptor, kind::f16: bf16 A and B, fp32 D, M = 128, N = 128
-__host__ __device__ constexpr uint32_t idesc_bf16(bool b_mn_major) {
+// instruction descriptor, kind::f16: bf16 A and B, fp32 D, M = 128, N = n
+__host__ __device__ constexpr uint32_t idesc_bf16(bool b_mn_major, uint32_t n) {
   return (1u << 4)            // D: f32
          | (1u << 7)          // A: bf16
          | (1u << 10)         // B: bf16
          | ((b_mn_major ? 1u : 0u) << 16)
-         | ((128u >> 3) << 17)  // N
+         | ((n >> 3) << 17)     // N
          | ((128u >> 4) << 24); // M
 }
 
@@ -179,7 +184,19 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 
 // two fp32 -> packed bf16x2 (round to nearest even), low half = first
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  return static_cast<uint32_t>(f32_to_bf16(lo)) | (static_cast<uint32_t>(f32_to_bf16(hi)) << 16);
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
 }
 
 // offset of 16-byte chunk c (0..7) of row r inside a 128-byte-swizzled half
@@ -237,10 +254,12 @@ k_attn_prefix_tc(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       mbar_init(&bars.empty[s], 1);
     }
     mbar_init(&bars.q_full, BM);
-    mbar_init(&bars.s_full, 1);
-    mbar_init(&bars.s_free, BM);
-    mbar_init(&bars.p_full, BM);
-    mbar_init(&bars.o_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.s_full[i], 1);
+      mbar_init(&bars.s_free[i], BM);
+      mbar_init(&bars.p_full[i], BM);
+      mbar_init(&bars.pv_done[i], 1);
+    }
     bars.failed = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -254,7 +273,6 @@ k_attn_prefix_tc(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
-  const uint32_t tmem_S = tmem;
   const uint32_t tmem_O = tmem + 128;
 
   if (warp < 4) {
@@ -266,77 +284,85 @@ k_attn_prefix_tc(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       if (r < rows_total)
         q4 = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
                                             ((static_cast<int64_t>(b) * NT + t) * p.Hq + h) * DH);
+      uint4 qv[16];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const uint4 v = q4 ? __ldg(q4 + c) : make_uint4(0, 0, 0, 0);
-        st_shared_v4(sbase + OFF_Q + (c >> 3) * kHalf + sw128_off(tid, c & 7), v.x, v.y, v.z, v.w);
-      }
+      for (int c = 0; c < 16; ++c) qv[c] = q4 ? __ldg(q4 + c) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        st_shared_v4(sbase + OFF_Q + (c >> 3) * kQHalf + sw128_off(tid, c & 7), qv[c].x, qv[c].y, qv[c].z, qv[c].w);
       fence_async_smem();
       mbar_arrive(&bars.q_full);
     }
     const float sl2 = p.scale_log2;
-    float m = -INFINITY, l = 0.f;
-    uint32_t sreg[BN];
+    float m = -INFINITY, l = 0.f;        // running reference max (log2 units) and sum
     for (int j = 0; j < nT; ++j) {
-      const bool ok_s = mbar_wait(bars, &bars.s_full, j & 1, p.hdr, 10);
+      const int sb = j & 1;
+      mbar_wait(bars, &bars.s_full[sb], (j >> 1) & 1, p.hdr, 10);
       tc_fence_after();
+      uint32_t sreg[BN];
 #pragma unroll
-      for (int q = 0; q < BN / 32; ++q) tmem_ld32(tmem_S + lane_off + q * 32, sreg + q * 32);
+      for (int q = 0; q < BN / 32; ++q) tmem_ld32(tmem + sb * BN + lane_off + q * 32, sreg + q * 32);
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(&bars.s_free);
-      const int nvalid = min(BN, k1 - (k0 + j * BN));
+      mbar_arrive(&bars.s_free[sb]);
       float mx = -INFINITY;
+      const int nvalid = k1 - (k0 + j * BN);
+      if (nvalid >= BN) {
 #pragma unroll
-      for (int c = 0; c < BN; ++c) {
-        const float s = c < nvalid ? __uint_as_float(sreg[c]) * sl2 : -INFINITY;
-        sreg[c] = __float_as_uint(s);
-        mx = fmaxf(mx, s);
-      }
-      (void)ok_s;
-      // keep a stale reference max unless the row max grew by more than 2^8
-      const float m_new = fmaxf(m, mx);
-      const bool need = m_new > m + 8.f;
-      const float mref = need ? m_new : m;
-      const float alpha = need ? exp2f(m - m_new) : 1.f;
-      uint32_t pk[BN / 2];
-      float rs = 0.f;
+        for (int c = 0; c < BN; ++c) mx = fmaxf(mx, __uint_as_float(sreg[c]));
+      } else {
 #pragma unroll
-      for (int c = 0; c < BN; c += 2) {
-        const float p0 = exp2f(__uint_as_float(sreg[c]) - mref);
-        const float p1 = exp2f(__uint_as_float(sreg[c + 1]) - mref);
-        const uint32_t w = pack_bf16(p0, p1);
-        pk[c / 2] = w;
-        rs += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
-      }
-      if (j > 0) {
-        mbar_wait(bars, &bars.o_done, (j - 1) & 1, p.hdr, 11);
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, need)) {
-          uint32_t o[32];
-#pragma unroll
-          for (int q = 0; q < DH / 32; ++q) {
-            tmem_ld32(tmem_O + lane_off + q * 32, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(tmem_O + lane_off + q * 32, o);
-          }
-          tmem_wait_st();
+        for (int c = 0; c < BN; ++c) {
+          if (c >= nvalid) sreg[c] = __float_as_uint(-INFINITY);
+          mx = fmaxf(mx, __uint_as_float(sreg[c]));
         }
       }
-      l = l * alpha + rs;
-      m = mref;
+      // reference max only moves when the row max grows by more than 2^8
+      const float m_new = fmaxf(m, mx * sl2);
+      const bool need = m_new > m + 8.f;
+      const float mref = need ? m_new : m;
+      const float alpha = need ? ex2_approx(m - m_new) : 1.f;
+      uint32_t pk[BN / 2];
+      float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
-        st_shared_v4(sbase + OFF_P + (c >> 3) * kHalf + sw128_off(tid, c & 7), pk[4 * c], pk[4 * c + 1],
-                     pk[4 * c + 2], pk[4 * c + 3]);
+      for (int c = 0; c < BN; c += 2) {
+        const float p0 = ex2_approx(fmaf(__uint_as_float(sreg[c]), sl2, -mref));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(sreg[c + 1]), sl2, -mref));
+        const uint32_t w = pack_bf16(p0, p1);
+        pk[c / 2] = w;
+        // sum the rounded values the MMA uses, so numerator and denominator agree
+        rs0 += __uint_as_float(w << 16);
+        rs1 += __uint_as_float(w & 0xffff0000u);
+      }
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        // O holds the sum up to tile j-1: wait for its last MMA, then rescale
+        mbar_wait(bars, &bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, p.hdr, 11);
+        tc_fence_after();
+        uint32_t o[32];
+#pragma unroll
+        for (int q = 0; q < DH / 32; ++q) {
+          tmem_ld32(tmem_O + lane_off + q * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(tmem_O + lane_off + q * 32, o);
+        }
+        tmem_wait_st();
+      }
+      l = l * alpha + (rs0 + rs1);
+      m = mref;
+      // P buffer sb was last read by the MMA of tile j-2
+      if (j >= 2) mbar_wait(bars, &bars.pv_done[sb], ((j - 2) >> 1) & 1, p.hdr, 12);
+#pragma unroll
+      for (int c = 0; c < BN / 8; ++c)
+        st_shared_v4(sbase + OFF_P + sb * kPBuf + sw128_off(tid, c), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                     pk[4 * c + 3]);
       fence_async_smem();
       tc_fence_before();
-      mbar_arrive(&bars.p_full);
+      mbar_arrive(&bars.p_full[sb]);
     }
-    // epilogue: un-normalised o, running max and sum of this split
-    mbar_wait(bars, &bars.o_done, (nT - 1) & 1, p.hdr, 12);
+    // epilogue: un-normalised o, reference max and sum of this split
+    mbar_wait(bars, &bars.pv_done[(nT - 1) & 1], ((nT - 1) >> 1) & 1, p.hdr, 13);
     tc_fence_after();
     float* ow = p.ws_o + (R * p.S + split) * DH;
 #pragma unroll
@@ -365,54 +391,57 @@ k_attn_prefix_tc(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         const int s = j % STAGES;
         if (j >= STAGES) mbar_wait(bars, &bars.empty[s], ((j / STAGES) - 1) & 1, p.hdr, 20);
         if (bars.failed) break;
-        mbar_expect_tx(&bars.full[s], 4 * kHalf);
+        mbar_expect_tx(&bars.full[s], 4 * kKVHalf);
         const int y = y0 + j * BN;
-        const uint32_t kd = sbase + OFF_K + s * 2 * kHalf, vd = sbase + OFF_V + s * 2 * kHalf;
+        const uint32_t kd = sbase + OFF_K + s * 2 * kKVHalf, vd = sbase + OFF_V + s * 2 * kKVHalf;
         tma_load_2d(kd, &tmap_k, 0, y, &bars.full[s]);
-        tma_load_2d(kd + kHalf, &tmap_k, 64, y, &bars.full[s]);
+        tma_load_2d(kd + kKVHalf, &tmap_k, 64, y, &bars.full[s]);
         tma_load_2d(vd, &tmap_v, 0, y, &bars.full[s]);
-        tma_load_2d(vd + kHalf, &tmap_v, 64, y, &bars.full[s]);
+        tma_load_2d(vd + kKVHalf, &tmap_v, 64, y, &bars.full[s]);
       }
     }
   } else {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16(false), idPV = idesc_bf16(true);
+      constexpr uint32_t idS = idesc_bf16(false, BN), idPV = idesc_bf16(true, DH);
       mbar_wait(bars, &bars.q_full, 0, p.hdr, 30);
       tc_fence_after();
-      auto issue_S = [&](int s) {
-        const uint32_t kb = sbase + OFF_K + s * 2 * kHalf;
+      // S[j&1] = Q K_j^T : M128 N64, eight K16 steps over the head dim
+      auto issue_S = [&](int j) {
+        const int s = j % STAGES;
+        const uint32_t kb = sbase + OFF_K + s * 2 * kKVHalf;
 #pragma unroll
         for (int ks = 0; ks < DH / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
-          mma_bf16(tmem_S, sw128_desc(sbase + OFF_Q + off, 16, 1024), sw128_desc(kb + off, 16, 1024), idS,
-                   ks > 0 ? 1u : 0u);
+          const uint64_t a = sw128_desc(sbase + OFF_Q + (ks >> 2) * kQHalf + (ks & 3) * 32, 16, 1024);
+          const uint64_t bd = sw128_desc(kb + (ks >> 2) * kKVHalf + (ks & 3) * 32, 16, 1024);
+          mma_bf16(tmem + (j & 1) * BN, a, bd, idS, ks > 0 ? 1u : 0u);
         }
-        mma_commit(&bars.s_full);
+        mma_commit(&bars.s_full[j & 1]);
       };
       mbar_wait(bars, &bars.full[0], 0, p.hdr, 31);
       tc_fence_after();
       issue_S(0);
       for (int j = 0; j < nT; ++j) {
-        const int s = j % STAGES;
         if (j + 1 < nT) {
-          const int s1 = (j + 1) % STAGES;
-          mbar_wait(bars, &bars.full[s1], ((j + 1) / STAGES) & 1, p.hdr, 32);
-          mbar_wait(bars, &bars.s_free, j & 1, p.hdr, 33);
+          // S of the next tile into the other buffer, once its previous reader is done
+          mbar_wait(bars, &bars.full[(j + 1) % STAGES], ((j + 1) / STAGES) & 1, p.hdr, 32);
+          if (j >= 1) mbar_wait(bars, &bars.s_free[(j + 1) & 1], ((j - 1) >> 1) & 1, p.hdr, 33);
           tc_fence_after();
-          issue_S(s1);
+          issue_S(j + 1);
         }
-        mbar_wait(bars, &bars.p_full, j & 1, p.hdr, 34);
+        // O += P_j V_j : M128 N128 (head dim), four K16 steps over the tile's keys
+        mbar_wait(bars, &bars.p_full[j & 1], (j >> 1) & 1, p.hdr, 34);
         tc_fence_after();
-        const uint32_t vb = sbase + OFF_V + s * 2 * kHalf;
+        const uint32_t vb = sbase + OFF_V + (j % STAGES) * 2 * kKVHalf;
+        const uint32_t pb = sbase + OFF_P + (j & 1) * kPBuf;
 #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks) {
-          const uint64_t a = sw128_desc(sbase + OFF_P + (ks >> 2) * kHalf + (ks & 3) * 32, 16, 1024);
-          const uint64_t bdesc = sw128_desc(vb + ks * 16 * 128, kHalf, 1024);
-          mma_bf16(tmem_O, a, bdesc, idPV, (j > 0 || ks > 0) ? 1u : 0u);
+          const uint64_t a = sw128_desc(pb + ks * 32, 16, 1024);
+          const uint64_t bd = sw128_desc(vb + ks * 16 * 128, kKVHalf, 1024);
+          mma_bf16(tmem_O, a, bd, idPV, (j > 0 || ks > 0) ? 1u : 0u);
         }
-        mma_commit(&bars.o_done);
-        mma_commit(&bars.empty[s]);
+        mma_commit(&bars.pv_done[j & 1]);
+        mma_commit(&bars.empty[j % STAGES]);
       }
     }
   }

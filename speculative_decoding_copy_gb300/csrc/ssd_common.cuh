@@ -78,6 +78,15 @@ __device__ __forceinline__ void record_error(WsHeader* h, int code, int where) {
   if (h != nullptr && atomicCAS(&h->err, 0, code) == 0) h->where = where;
 }
 
+constexpr float kLog2e = 1.4426950408889634f;
+
+// 2^x, hardware approximation (MUFU), flush-to-zero
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <typename T>
 __device__ __forceinline__ T warp_sum(T v) {
 #pragma unroll

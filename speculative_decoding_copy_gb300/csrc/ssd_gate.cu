@@ -21,20 +21,35 @@ constexpr int kChunk = 4096;     // match ends examined per staged chunk
 constexpr int kMaxKappa = 64;
 constexpr int kMaxW = 64;
 
+constexpr int kPerThread = 16;           // positions examined per thread per chunk (kChunk / kGateThreads)
+constexpr int kStageLoads = (kChunk + kMaxKappa + kGateThreads - 1) / kGateThreads;
+
 struct ScanSmem {
   int tile[kChunk + kMaxKappa];
   int g[kMaxKappa];
   int warp_val[kGateThreads / 32];
+  int cnt[kPerThread][kGateThreads / 32];  // matches per (round, warp) of one chunk
   int ends[kMaxW];
   int nfound;
   long long warp_sum[kGateThreads / 32];
 };
 
-// Stage ctx[j_lo-kappa+1 .. j_hi] into shared memory.
+// Stage ctx[j_lo-kappa+1 .. j_hi] into shared memory: every load of the chunk is
+// issued before the first store, so the chunk costs one memory latency.
 __device__ __forceinline__ void stage_chunk(ScanSmem& s, const int32_t* row, int j_lo, int j_hi, int kappa) {
   const int base = j_lo - kappa + 1;
   const int cnt = j_hi - base + 1;
-  for (int i = threadIdx.x; i < cnt; i += blockDim.x) s.tile[i] = __ldg(row + base + i);
+  int v[kStageLoads];
+#pragma unroll
+  for (int u = 0; u < kStageLoads; ++u) {
+    const int i = threadIdx.x + u * kGateThreads;
+    v[u] = i < cnt ? __ldg(row + base + i) : 0;
+  }
+#pragma unroll
+  for (int u = 0; u < kStageLoads; ++u) {
+    const int i = threadIdx.x + u * kGateThreads;
+    if (i < cnt) s.tile[i] = v[u];
+  }
 }
 
 __device__ __forceinline__ bool match_at(const ScanSmem& s, int j, int j_lo, int kappa) {
@@ -43,6 +58,17 @@ __device__ __forceinline__ bool match_at(const ScanSmem& s, int j, int j_lo, int
   bool ok = true;
   for (int i = 0; i < kappa; ++i) ok &= (t[i] == s.g[i]);
   return ok;
+}
+
+// Bit u of the result: position j_hi - (u * kGateThreads + threadIdx.x) is a match end.
+__device__ __forceinline__ unsigned match_mask(const ScanSmem& s, int j_lo, int j_hi, int kappa) {
+  unsigned mask = 0;
+#pragma unroll
+  for (int u = 0; u < kPerThread; ++u) {
+    const int j = j_hi - (u * kGateThreads + static_cast<int>(threadIdx.x));
+    if (j >= j_lo && match_at(s, j, j_lo, kappa)) mask |= 1u << u;
+  }
+  return mask;
 }
 
 __global__ void __launch_bounds__(kGateThreads)
@@ -55,18 +81,25 @@ k_gate_match(const int32_t* __restrict__ ctx, int64_t stride, const int32_t* __r
   const int b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
 
-  // ---- probe: exact products, fixed point 2^-32, integer sum
+  // ---- probe: exact products, fixed point 2^-32, integer sum (8 loads in flight per thread)
   long long acc = 0;
-  if (h_bf16) {
-    const uint16_t* hb = static_cast<const uint16_t*>(h) + b * h_stride;
-    for (int i = tid; i < d; i += kGateThreads) {
-      const double p = static_cast<double>(bf16_to_f32(hb[i])) * static_cast<double>(__ldg(w + i));
-      acc += __double2ll_rz(p * 4294967296.0);
+  const uint16_t* hb = static_cast<const uint16_t*>(h) + b * h_stride;
+  const float* hf = static_cast<const float*>(h) + b * h_stride;
+  for (int base = 0; base < d; base += kGateThreads * 8) {
+    float hv[8], wv[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int i = base + k * kGateThreads + tid;
+      hv[k] = 0.f;
+      wv[k] = 0.f;
+      if (i < d) {
+        hv[k] = h_bf16 ? bf16_to_f32(__ldg(hb + i)) : __ldg(hf + i);
+        wv[k] = __ldg(w + i);
+      }
     }
-  } else {
-    const float* hf = static_cast<const float*>(h) + b * h_stride;
-    for (int i = tid; i < d; i += kGateThreads) {
-      const double p = static_cast<double>(__ldg(hf + i)) * static_cast<double>(__ldg(w + i));
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const double p = static_cast<double>(hv[k]) * static_cast<double>(wv[k]);
       acc += __double2ll_rz(p * 4294967296.0);
     }
   }
@@ -86,10 +119,9 @@ k_gate_match(const int32_t* __restrict__ ctx, int64_t stride, const int32_t* __r
       const int j_lo = max(j_min, j_hi - kChunk + 1);
       stage_chunk(s, row, j_lo, j_hi, kappa);
       __syncthreads();
-      int best = -1;
-      for (int j = j_hi - tid; j >= j_lo; j -= kGateThreads) {
-        if (match_at(s, j, j_lo, kappa)) { best = j; break; }   // descending: first hit is this thread's max
-      }
+      const unsigned mask = match_mask(s, j_lo, j_hi, kappa);
+      // lowest set bit = largest j of this thread
+      int best = mask ? j_hi - ((__ffs(mask) - 1) * kGateThreads + tid) : -1;
       best = __reduce_max_sync(0xffffffffu, best);
       if (lane == 0) s.warp_val[wid] = best;
       __syncthreads();
@@ -139,30 +171,58 @@ k_retrieve(const int32_t* __restrict__ ctx, int64_t stride, const int32_t* __res
       const int j_lo = max(j_min, j_hi - kChunk + 1);
       stage_chunk(s, row, j_lo, j_hi, kappa);
       __syncthreads();
-      bool done = false;
-      for (int j0 = j_hi; j0 >= j_lo; j0 -= kGateThreads) {
-        const int j = j0 - tid;                       // descending with the thread index
-        const bool m = (j >= j_lo) && match_at(s, j, j_lo, kappa);
-        const unsigned bal = __ballot_sync(0xffffffffu, m);
-        if (lane == 0) s.warp_val[wid] = __popc(bal);
-        __syncthreads();
-        int off = s.nfound, total = 0;
+      // rank every match of the chunk in descending j order: position
+      // j_hi - (u * 256 + tid) precedes every (u', tid') with a larger u'*256+tid'
+      const unsigned mask = match_mask(s, j_lo, j_hi, kappa);
 #pragma unroll
-        for (int i = 0; i < kGateThreads / 32; ++i) {
-          const int c = s.warp_val[i];
-          if (i < wid) off += c;
-          total += c;
-        }
-        if (m) {
-          const int rank = off + __popc(bal & ((1u << lane) - 1u));
-          if (rank < W) s.ends[rank] = j;
-        }
-        __syncthreads();
-        if (tid == 0) s.nfound += total;
-        __syncthreads();
-        if (s.nfound >= W) { done = true; break; }
+      for (int u = 0; u < kPerThread; ++u) {
+        const unsigned bal = __ballot_sync(0xffffffffu, (mask >> u) & 1u);
+        if (lane == 0) s.cnt[u][wid] = __popc(bal);
       }
-      if (done) break;
+      __syncthreads();
+      if (wid == 0) {
+        // exclusive prefix over the 128 (round, warp) counts, round-major, offset by
+        // the matches of earlier chunks
+        constexpr int nc = kPerThread * (kGateThreads / 32);
+        constexpr int per = nc / 32;
+        int* flat = &s.cnt[0][0];
+        int v[per];
+        int local = 0;
+#pragma unroll
+        for (int q = 0; q < per; ++q) {
+          v[q] = flat[lane * per + q];
+          local += v[q];
+        }
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const int before = s.nfound;
+        int run = before + incl - local;
+#pragma unroll
+        for (int q = 0; q < per; ++q) {
+          flat[lane * per + q] = run;
+          run += v[q];
+        }
+        __syncwarp();
+        if (lane == 31) s.warp_val[0] = before + incl;   // matches found so far
+      }
+      __syncthreads();
+#pragma unroll
+      for (int u = 0; u < kPerThread; ++u) {
+        const bool m = (mask >> u) & 1u;
+        const unsigned bal = __ballot_sync(0xffffffffu, m);
+        if (m) {
+          const int rank = s.cnt[u][wid] + __popc(bal & ((1u << lane) - 1u));
+          if (rank < W) s.ends[rank] = j_hi - (u * kGateThreads + tid);
+        }
+      }
+      __syncthreads();
+      if (tid == 0) s.nfound = s.warp_val[0];
+      __syncthreads();
+      if (s.nfound >= W) break;
       j_hi = j_lo - 1;
     }
   }
