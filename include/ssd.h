@@ -228,6 +228,31 @@ size_t ssd_accept_workspace_size(const ssd_accept_args* a);
 int ssd_accept(const ssd_accept_args* a, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * ssd_accept_static — ssd_accept without a caller-provided workspace.
+ *
+ * The pages have no counterpart for this call; it exists for callers that
+ * cannot allocate device memory at the point where they run the step: code
+ * that runs inside a stream capture or a real-time serving loop where every
+ * allocation is forbidden, hosts whose device memory is owned by a separate
+ * pool the library cannot draw from, or bindings with no allocator at all.
+ * Arguments, outputs and results are those of ssd_accept.
+ * Scratch: a fixed 4 MiB array inside the library's device code, present on
+ * every GPU that loads the library and held until the process exits. A call
+ * whose scratch need (ssd_accept_workspace_size) exceeds 4 MiB returns
+ * SSD_ERR_WORKSPACE and launches nothing.
+ * The first call on a device looks up the array's device address (and loads
+ * the library's device code there); make that first call before any stream
+ * capture. The call allocates nothing: no cudaMalloc, cudaFree or other
+ * allocating routine.
+ * Every call on a device shares the one array and it keeps the previous call's
+ * contents (nothing in it needs to start at zero), so calls that overlap on
+ * the GPU — on different streams or from different threads — race; serialise
+ * them. Device-side errors are recorded in the array's header and cannot be
+ * read back through ssd_read_device_error.
+ */
+int ssd_accept_static(const ssd_accept_args* a, void* stream);
+
+/*
  * ssd_read_device_error — SYNCHRONOUS: waits for `stream`, then reads and
  * clears the device error word at the head of a workspace used by
  * ssd_verify_attn or ssd_accept. *out receives SSD_OK, SSD_ERR_TIMEOUT or

@@ -25,7 +25,7 @@ SSD_CHAIN_NONE, SSD_CHAIN_WHEN_GATE_OFF, SSD_CHAIN_ALWAYS = 0, 1, 2
 
 EXPORTED = ["ssd_status_string", "ssd_version", "ssd_launch_count", "ssd_gate_match", "ssd_retrieve",
             "ssd_verify_attn_workspace_size", "ssd_verify_attn", "ssd_accept_workspace_size", "ssd_accept",
-            "ssd_read_device_error", "ssd_profile_kernel"]
+            "ssd_read_device_error", "ssd_profile_kernel", "ssd_accept_static"]
 SSD_KERNEL = dict(vocab_stats=1, attn_prefix=2, attn_combine=3, accept_select=4, sample_final=5, gate_match=6,
                   retrieve=7)
 
@@ -81,6 +81,8 @@ def lib() -> ctypes.CDLL:
         L.ssd_accept.argtypes = [POINTER(AcceptArgs), c_void_p, c_size_t, c_void_p]
         L.ssd_read_device_error.restype = c_int
         L.ssd_read_device_error.argtypes = [c_void_p, c_void_p, POINTER(c_int32)]
+        L.ssd_accept_static.restype = c_int
+        L.ssd_accept_static.argtypes = [POINTER(AcceptArgs), c_void_p]
         L.ssd_profile_kernel.restype = c_int
         L.ssd_profile_kernel.argtypes = [c_int, c_void_p, c_void_p]
         _lib = L
@@ -262,3 +264,19 @@ def ssd_profile_kernel(kernel: str | None, start=None, end=None):
             ev.record()
     rc = lib().ssd_profile_kernel(SSD_KERNEL[kernel], ctypes.c_void_p(start.cuda_event), ctypes.c_void_p(end.cuda_event))
     _check("ssd_profile_kernel", rc)
+
+
+def ssd_accept_static(tgt, drf, blk_tok, blk_len, u_acc, u_fin, *, mode, kind, K=0, chain_blk=-1, out=None,
+                      stream=None):
+    """ssd_accept with the library's fixed internal scratch instead of a workspace
+    (for callers that cannot allocate); calls must not overlap on the GPU."""
+    _need(tgt, "tgt", (torch.float32,) + _HALF, 3)
+    _need(blk_tok, "blk_tok", (torch.int32,), 3)
+    _need(blk_len, "blk_len", (torch.int32,), 2)
+    B, NR, V = tgt.shape
+    _, NB, Dmax = blk_tok.shape
+    outs = out or alloc_accept_outputs(B, NB, Dmax, tgt.device)
+    args = accept_args(mode, kind, tgt, drf, blk_tok, blk_len, K, chain_blk, u_acc, u_fin, outs, None)
+    rc = lib().ssd_accept_static(ctypes.byref(args), _stream(stream))
+    _check("ssd_accept_static", rc)
+    return outs

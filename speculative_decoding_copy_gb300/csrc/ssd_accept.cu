@@ -26,6 +26,8 @@
 //   k_probs_out     optional diagnostic copy of p for every needed row.
 #include <math.h>
 
+#include <mutex>
+
 #include "ssd_accept.cuh"
 
 namespace ssd {
@@ -698,6 +700,52 @@ extern "C" int ssd_accept(const ssd_accept_args* a, void* ws, size_t ws_bytes, v
   if (ws == nullptr || !aligned(ws, 256)) return SSD_ERR_WORKSPACE;
   const AcceptLayout L = accept_layout(a);
   if (ws_bytes < L.total) return SSD_ERR_WORKSPACE;
+  const AcceptParams p = accept_params(a, L, static_cast<char*>(ws));
+  return accept_launch(p, static_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------------------------ no-allocation variant
+// Scratch for ssd_accept_static: a fixed array in device memory that exists on
+// every GPU where this library's device code is loaded, for the life of the
+// process. Host code must not use the symbol itself as a device address (it is
+// a host-side stand-in); the real address is fetched once per device below.
+namespace ssd {
+
+constexpr size_t kStaticScratchBytes = size_t(4) << 20;   // 4 MiB
+static __device__ __align__(256) unsigned char g_accept_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+static std::mutex g_scratch_mu;
+static void* g_scratch_addr[kMaxDevices];
+
+// Device address of the scratch array on the current device, looked up on the
+// first call for that device (the lookup loads the module there if needed).
+static int static_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SSD_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_accept_scratch) != cudaSuccess || p == nullptr) return SSD_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return SSD_OK;
+}
+
+}  // namespace ssd
+
+extern "C" int ssd_accept_static(const ssd_accept_args* a, void* stream) {
+  const int st = accept_validate(a);
+  if (st != SSD_OK) return st;
+  if (a->B == 0) return SSD_OK;
+  const AcceptLayout L = accept_layout(a);
+  if (L.total > kStaticScratchBytes) return SSD_ERR_WORKSPACE;   // batch too large for the fixed scratch
+  void* ws = nullptr;
+  const int rc = static_scratch(&ws);
+  if (rc != SSD_OK) return rc;
+  // Nothing in the scratch has to start at zero: the select kernel sets every
+  // sampler completion counter before the sampler reads it.
   const AcceptParams p = accept_params(a, L, static_cast<char*>(ws));
   return accept_launch(p, static_cast<cudaStream_t>(stream));
 }
