@@ -201,7 +201,7 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-KERNELS = ["gate_match", "retrieve", "attn_prefix", "attn_combine", "vocab_stats", "accept_select", "sample_final"]
+KERNELS = ["gate_match", "attn_prefix", "attn_combine", "vocab_stats", "sample_final"]
 
 
 def source_sha(*names):
@@ -265,32 +265,54 @@ def run_ours(args):
     steps = [probe] + [VerifyStep(wl, inp, device=dev) for _ in range(R - 1)]
     tokens = ab["tokens"]
 
-    # per-kernel events, one pair per kernel per copy
-    ev = [{k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for k in KERNELS}
-          for _ in range(R)]
-    for d in ev:
-        for s, e in d.values():
-            s.record(main)
-            e.record(main)
-    torch.cuda.synchronize()
+    def capture(hooked):
+        """One graph per input copy; `hooked` kernels are bracketed by event nodes."""
+        evs = [{k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for k in hooked}
+               for _ in range(R)]
+        for d in evs:
+            for a, b2 in d.values():
+                a.record(main)
+                b2.record(main)
+        torch.cuda.synchronize()
+        gs = []
+        for i in range(R):
+            g = torch.cuda.CUDAGraph()
+            for k in hooked:
+                ssd.ssd_profile_kernel(k, *evs[i][k])
+            with torch.cuda.graph(g, stream=main):
+                steps[i].run(main, aux)
+            ssd.ssd_profile_kernel(None)
+            gs.append(g)
+        torch.cuda.synchronize()
+        return gs, evs
 
-    # warm-up (eager) then capture one graph per copy
+    def mean_us(evs, k):
+        v = [evs[i][k][0].elapsed_time(evs[i][k][1]) * 1000.0 for i in range(R)]
+        v = [x for x in v if x > 0]
+        return statistics.mean(v) if v else None
+
+    # warm-up (eager)
     with torch.cuda.stream(main):
         for i in range(max(3, args.warmup // 10)):
             steps[i % R].run(main, aux)
     torch.cuda.synchronize()
-    n0 = ssd.launch_count()
-    graphs = []
-    for i in range(R):
-        g = torch.cuda.CUDAGraph()
-        for k in KERNELS:
-            ssd.ssd_profile_kernel(k, *ev[i][k])
-        with torch.cuda.graph(g, stream=main):
-            steps[i].run(main, aux)
-        ssd.ssd_profile_kernel(None)
-        graphs.append(g)
-    launches_per_step = (ssd.launch_count() - n0) // R
+
+    # diagnostic pass (untimed): every kernel hooked, per-kernel durations
+    diag_graphs, diag_ev = capture(KERNELS)
+    with torch.cuda.stream(main):
+        for i in range(max(3 * R, 60)):
+            diag_graphs[i % R].replay()
     torch.cuda.synchronize()
+    kern_us = {k: mean_us(diag_ev, k) for k in KERNELS}
+    kern_us = {k: v for k, v in kern_us.items() if v is not None}
+    del diag_graphs
+    streaming = [k for k in ("vocab_stats", "attn_prefix") if k in kern_us]
+    dom = max(streaming, key=lambda k: kern_us[k])
+
+    # timed graphs: only the dominant kernel is bracketed by events
+    n0 = ssd.launch_count()
+    graphs, ev = capture([dom])
+    launches_per_step = (ssd.launch_count() - n0) // R
 
     with torch.cuda.stream(main):
         for i in range(args.warmup):
@@ -323,25 +345,18 @@ def run_ours(args):
         ms = float(t.item())
     ms_per_step = ms / K
     value = world * K / (ms / 1000.0)
-
-    # per-kernel durations over the last replay of each copy's graph
-    kern_us = {}
-    for k in KERNELS:
-        v = [ev[i][k][0].elapsed_time(ev[i][k][1]) * 1000.0 for i in range(R)]
-        v = [x for x in v if x > 0]
-        if v:
-            kern_us[k] = statistics.mean(v)
+    dom_us = mean_us(ev, dom)
 
     # end to end through the public API with host buffers
     e2e = run_e2e(args, wl, inp, steps[0], main, aux, dev)
 
     hbm, peak_kind = measured_peaks()
     kb = {"vocab_stats": ab["logits"], "attn_prefix": ab["kv"] + (ab["q_o"] // 2)}
-    dom = max(kb, key=lambda k: kern_us.get(k, 0.0))
-    achieved = kb[dom] / (kern_us[dom] * 1e-6) / 1e9 if kern_us.get(dom) else None
+    achieved = kb[dom] / (dom_us * 1e-6) / 1e9 if dom_us else None
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
                 "frac": (achieved / hbm) if achieved else None, "traffic": dram_traffic(dom, wl.name),
-                "algorithmic_bytes_per_launch": kb[dom], "peak_source": f"{peak_kind} hbm_gbs"}
+                "algorithmic_bytes_per_launch": kb[dom], "launch_us": dom_us,
+                "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth, burst)"}
     step_bytes = ab["total"]
     step_roof = {"algorithmic_bytes_per_step": step_bytes,
                  "achieved_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
@@ -367,7 +382,7 @@ def run_ours(args):
                 "candidate_tokens_per_s": value * tokens,
                 "hbm_roofline_step": step_roof,
                 "roofline": roofline,
-                "kernels_us": kern_us,
+                "kernels_us_diagnostic": kern_us,
                 "e2e": e2e,
                 "gpu_launches": launches_per_step * K,
                 "clocks": clk,

@@ -121,8 +121,9 @@ int ssd_gate_match(const int32_t* ctx, int64_t ctx_stride, const int32_t* ctx_le
  * Arguments
  *   ctx, ctx_stride, ctx_len, B, kappa: as for ssd_gate_match
  *   gate [B] int32 (from ssd_gate_match)
- *   last_match_end [B] int32 or NULL: when given (from ssd_gate_match on the
- *     same context) the scan starts there instead of at the end
+ *   last_match_end [B] int32 or NULL: accepted for symmetry with
+ *     ssd_gate_match and not read (the scan starts at the current token; the
+ *     most recent matches lie in its first staged chunk)
  *   1 <= W <= 64, 1 <= D <= 256, 0 <= K <= 256 (K >= 1 if chain_policy != 0)
  *   chain_tok [B][K] int32, may be NULL when chain_policy == SSD_CHAIN_NONE
  *   blk_tok [B][NB][Dmax], blk_len [B][NB], n_cand [B]: int32 outputs
@@ -131,6 +132,18 @@ int ssd_retrieve(const int32_t* ctx, int64_t ctx_stride, const int32_t* ctx_len,
                  const int32_t* gate, const int32_t* last_match_end,
                  int kappa, int W, int D, int K, int chain_policy, const int32_t* chain_tok,
                  int32_t* blk_tok, int32_t* blk_len, int32_t* n_cand, void* stream);
+
+/*
+ * ssd_gate_retrieve — ssd_gate_match and ssd_retrieve fused into one launch
+ * (one pass over the context per sequence); same definitions, arguments and
+ * outputs as the two calls made in sequence. probe_on may be NULL.
+ */
+int ssd_gate_retrieve(const int32_t* ctx, int64_t ctx_stride, const int32_t* ctx_len, int B,
+                      const void* h, int h_dtype, int64_t h_stride, const float* w, int d,
+                      float tau, int kappa, int W, int D, int K, int chain_policy,
+                      const int32_t* chain_tok,
+                      float* score, int32_t* gate, int32_t* last_match_end, int32_t* probe_on,
+                      int32_t* blk_tok, int32_t* blk_len, int32_t* n_cand, void* stream);
 
 /*
  * ssd_verify_attn — attention of every candidate token over its allowed keys.

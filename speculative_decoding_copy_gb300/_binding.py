@@ -25,7 +25,7 @@ SSD_CHAIN_NONE, SSD_CHAIN_WHEN_GATE_OFF, SSD_CHAIN_ALWAYS = 0, 1, 2
 
 EXPORTED = ["ssd_status_string", "ssd_version", "ssd_launch_count", "ssd_gate_match", "ssd_retrieve",
             "ssd_verify_attn_workspace_size", "ssd_verify_attn", "ssd_accept_workspace_size", "ssd_accept",
-            "ssd_read_device_error", "ssd_profile_kernel", "ssd_accept_static"]
+            "ssd_read_device_error", "ssd_profile_kernel", "ssd_accept_static", "ssd_gate_retrieve"]
 SSD_KERNEL = dict(vocab_stats=1, attn_prefix=2, attn_combine=3, accept_select=4, sample_final=5, gate_match=6,
                   retrieve=7)
 
@@ -71,6 +71,10 @@ def lib() -> ctypes.CDLL:
         L.ssd_retrieve.restype = c_int
         L.ssd_retrieve.argtypes = [c_void_p, c_int64, c_void_p, c_int, c_void_p, c_void_p, c_int, c_int, c_int,
                                    c_int, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
+        L.ssd_gate_retrieve.restype = c_int
+        L.ssd_gate_retrieve.argtypes = [c_void_p, c_int64, c_void_p, c_int, c_void_p, c_int, c_int64, c_void_p,
+                                        c_int, c_float, c_int, c_int, c_int, c_int, c_int, c_void_p, c_void_p,
+                                        c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
         L.ssd_verify_attn_workspace_size.restype = c_size_t
         L.ssd_verify_attn_workspace_size.argtypes = [POINTER(AttnArgs)]
         L.ssd_verify_attn.restype = c_int
@@ -175,6 +179,34 @@ def ssd_retrieve(ctx, ctx_len, gate, last_match_end, kappa, W, D, K, chain_polic
     return dict(blk_tok=blk_tok, blk_len=blk_len, n_cand=n_cand)
 
 
+def ssd_gate_retrieve(ctx, ctx_len, h, w, tau, kappa, W, D, K, chain_policy, chain_tok=None, *, out=None,
+                      stream=None):
+    """Gate and retrieval in one launch; returns the outputs of both calls."""
+    _need(ctx, "ctx", (torch.int32,), 2)
+    _need(ctx_len, "ctx_len", (torch.int32,), 1)
+    _need(h, "h", (torch.float32,) + _HALF, 2)
+    _need(w, "w", (torch.float32,), 1)
+    B = ctx.shape[0]
+    NB = W + (1 if chain_policy else 0)
+    Dmax = max(D, K) if chain_policy else D
+    o = dict(out or {})
+    need = dict(score=((B,), torch.float32), gate=((B,), torch.int32), last_match_end=((B,), torch.int32),
+                probe_on=((B,), torch.int32), blk_tok=((B, NB, Dmax), torch.int32), blk_len=((B, NB), torch.int32),
+                n_cand=((B,), torch.int32))
+    for k, (shape, dt) in need.items():
+        if o.get(k) is None:
+            o[k] = torch.empty(shape, dtype=dt, device=ctx.device)
+    if chain_tok is not None:
+        _need(chain_tok, "chain_tok", (torch.int32,), 2)
+    rc = lib().ssd_gate_retrieve(_ptr(ctx), ctx.shape[1], _ptr(ctx_len), B, _ptr(h), _elem_type(h), h.shape[1],
+                                 _ptr(w), w.shape[0], float(tau), int(kappa), int(W), int(D), int(K),
+                                 int(chain_policy), _ptr(chain_tok), _ptr(o["score"]), _ptr(o["gate"]),
+                                 _ptr(o["last_match_end"]), _ptr(o["probe_on"]), _ptr(o["blk_tok"]),
+                                 _ptr(o["blk_len"]), _ptr(o["n_cand"]), _stream(stream))
+    _check("ssd_gate_retrieve", rc)
+    return o
+
+
 def attn_args(q, k_cache, v_cache, k_cand, v_cand, prefix_len, blk_len, Dmax, out, scale=0.0) -> AttnArgs:
     B, NT, Hq, dh = q.shape
     Hkv = k_cache.shape[1]
@@ -240,7 +272,7 @@ def ssd_accept(tgt, drf, blk_tok, blk_len, u_acc, u_fin, *, mode, kind, K=0, cha
     args = accept_args(mode, kind, tgt, drf, blk_tok, blk_len, K, chain_blk, u_acc, u_fin, outs, probs_out)
     need = ssd_accept_workspace_size(args)
     if ws is None:
-        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=tgt.device)
+        ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=tgt.device)
     rc = lib().ssd_accept(ctypes.byref(args), _ptr(ws), ws.numel(), _stream(stream))
     _check("ssd_accept", rc)
     return outs

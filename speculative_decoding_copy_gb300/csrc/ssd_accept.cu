@@ -9,11 +9,13 @@
 // continuation is adopted. 추측 디코딩은 왜… page, "2단계 · 일괄 검증" — greedy:
 // a match is accepted, the first mismatch truncates.
 //
-// Kernels (one stream, in order):
-//   k_vocab_stats   grid (chunks x rows, B): one 16-byte-vector pass over the
-//                   logits; each CTA holds a whole 32 KB chunk in registers
-//                   (one memory latency), then max, argmax (lowest index on
-//                   ties) and sum of 2^((l - max) log2 e) for the chunk;
+// Kernels (one stream, in order; each later kernel is launched with
+// programmatic dependent launch and waits for its predecessor's results):
+//   k_vocab_stats   persistent CTAs over (sequence, row, chunk) tasks: one
+//                   16-byte-vector pass over the logits, a whole 32 KB chunk
+//                   in registers per task and the next task's loads in flight
+//                   while the current one is reduced to max, argmax (lowest
+//                   index on ties) and sum of 2^((l - max) log2 e);
 //   k_accept_select grid B: merges the chunks of every needed row, runs the
 //                   acceptance test of every candidate token (one thread per
 //                   token slot, loads issued together), picks the longest
@@ -37,7 +39,6 @@ constexpr int kVec = 8;                 // 16-byte vectors per thread per stats 
 constexpr int kSelectThreads = 256;
 constexpr int kMaxRows = 1024;          // 1 + NB*Dmax + K
 constexpr int kMaxSlots = 1024;         // NB*Dmax
-constexpr int kStage = 1024;            // chunk partials staged per pass in select
 constexpr int kSampleChunk = 2048;      // vocabulary entries per sampler CTA
 constexpr int kSamplePer = kSampleChunk / kVocabThreads;
 constexpr long long kOneWeight = 1LL << 40;
@@ -49,7 +50,7 @@ __device__ __forceinline__ float load_val(const void* base, int64_t i, int bf16)
 
 // p of one entry: 2^((l - max) log2 e) / Z in fp32, or the value itself for probabilities
 __device__ __forceinline__ float prob_of(float v, const RowStat& st, int probs) {
-  return probs ? v : ex2_approx(fmaf(v, kLog2e, -st.m * kLog2e)) / st.s;
+  return probs ? v : ex2_approx(fmaf(v, kLog2e, -st.m * kLog2e)) * __frcp_rn(st.s);
 }
 
 // P = floor(p * 2^40) for fp32 p in [0, 1], exactly, from the bits of p
@@ -127,22 +128,18 @@ __device__ __forceinline__ float vec_elem(const uint4& u, int e) {
   return __uint_as_float(w);
 }
 
-// One chunk of one row: every 16-byte load is issued before any use and the raw
-// vectors stay in registers (32 per thread) for the two passes.
+// One chunk of one row as 16-byte vectors held in registers (32 per thread).
+// Elements past the row end (or an unaligned row) are gathered one by one; the
+// padding is -inf.
 template <bool BF16>
-__device__ __forceinline__ void stats_chunk(const void* row, int64_t lo, int64_t hi, bool vec_ok, bool probs,
-                                            float& m, float& s, float& av, int& ai) {
+__device__ __forceinline__ void load_chunk(const void* row, int64_t lo, int64_t hi, bool vec_ok, uint4* raw) {
   constexpr int EPV = BF16 ? 8 : 4;    // elements per 16-byte vector
-  uint4 raw[kVec];
-  bool full[kVec];
 #pragma unroll
   for (int v = 0; v < kVec; ++v) {
     const int64_t i0 = lo + static_cast<int64_t>(v * kVocabThreads + threadIdx.x) * EPV;
-    full[v] = vec_ok && i0 + EPV <= hi;
-    if (full[v]) {
+    if (vec_ok && i0 + EPV <= hi) {
       raw[v] = __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(row) + i0 * (BF16 ? 2 : 4)));
     } else {
-      // ragged tail or unaligned row: gather the elements that exist, -inf elsewhere
       uint32_t w[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) w[q] = BF16 ? 0xff80ff80u : 0xff800000u;
@@ -160,6 +157,13 @@ __device__ __forceinline__ void stats_chunk(const void* row, int64_t lo, int64_t
       raw[v] = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
+}
+
+// max, argmax (lowest index on ties) and sum of 2^((x - max) log2 e) of this thread's elements
+template <bool BF16>
+__device__ __forceinline__ void reduce_chunk(const uint4* raw, int64_t lo, bool probs, float& m, float& s, float& av,
+                                             int& ai) {
+  constexpr int EPV = BF16 ? 8 : 4;
   av = -INFINITY;
   ai = 0x7fffffff;
 #pragma unroll
@@ -191,54 +195,25 @@ __device__ __forceinline__ void stats_chunk(const void* row, int64_t lo, int64_t
   }
 }
 
-template <bool BF16>
-__global__ void __launch_bounds__(kVocabThreads, 3)
-k_vocab_stats(AcceptParams p) {
-  const int c = blockIdx.x % p.nch, r = blockIdx.x / p.nch;
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  __shared__ RowStat red[kVocabThreads / 32];
-  for (int b = blockIdx.y; b < p.B; b += gridDim.y) {
-    if (!row_needed(p, b, r)) continue;
-    const int64_t lo = static_cast<int64_t>(c) * p.chunk;
-    const int64_t hi = min(p.V, lo + p.chunk);
-    const void* row = row_ptr(p, b, r);
-    float m, s, av;
-    int ai;
-    stats_chunk<BF16>(row, lo, hi, aligned_dev(row, 16), p.probs, m, s, av, ai);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-      const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-      const float v2 = __shfl_xor_sync(0xffffffffu, av, o);
-      const int i2 = __shfl_xor_sync(0xffffffffu, ai, o);
-      stat_merge(m, s, m2, s2);
-      amax_merge(av, ai, v2, i2);
-    }
-    if (lane == 0) red[wid] = RowStat{m, s, av, ai};
-    __syncthreads();
-    if (tid == 0) {
-      for (int w = 1; w < kVocabThreads / 32; ++w) {
-        stat_merge(m, s, red[w].m, red[w].s);
-        amax_merge(av, ai, red[w].amax_v, red[w].amax_i);
-      }
-      p.part[(static_cast<int64_t>(b) * p.NRD + r) * p.nch + c] = RowStat{m, s, av, ai};
-    }
-    __syncthreads();   // red[] is reused by the next sequence of this CTA
-  }
-}
-
 // ------------------------------------------------------------------ select
 constexpr int kSlotsPer = kMaxSlots / kSelectThreads;
 
-__global__ void __launch_bounds__(kSelectThreads)
-k_accept_select(AcceptParams p) {
-  __shared__ RowStat st[kMaxRows];
-  __shared__ RowStat stage[kStage];
-  __shared__ int len_s[256];
-  __shared__ int acc_s[256];
-  __shared__ unsigned char ok_s[kMaxSlots];
-  __shared__ int sel[4];   // best block, a, len, final (greedy)
-  const int b = blockIdx.x;
+struct SelectSmem {
+  RowStat st[kMaxRows];
+  int len_s[256];
+  int acc_s[256];
+  unsigned char ok_s[kMaxSlots];
+  int sel[4];   // best block, a, len, final (greedy)
+};
+
+// Acceptance and choice of block for sequence b, by one CTA of 256 threads,
+// once every needed row's chunk statistics are in p.part.
+__device__ void select_one(const AcceptParams& p, int b, SelectSmem& sm) {
+  RowStat* st = sm.st;
+  int* len_s = sm.len_s;
+  int* acc_s = sm.acc_s;
+  unsigned char* ok_s = sm.ok_s;
+  int* sel = sm.sel;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   constexpr int nw = kSelectThreads / 32;
   const int nslots = p.NB * p.Dmax;
@@ -287,51 +262,44 @@ k_accept_select(AcceptParams p) {
     len_s[k] = L;
   }
 
-  // 2. merge the vocabulary chunks of every needed row (partials staged in passes)
-  const int rows_pass = max(1, kStage / p.nch);
-  for (int r0 = 0; r0 < p.NRD; r0 += rows_pass) {
-    const int nr = min(rows_pass, p.NRD - r0);
-    const int ne = nr * p.nch;
-    const RowStat* src = p.part + (static_cast<int64_t>(b) * p.NRD + r0) * p.nch;
-    RowStat tmp[kStage / kSelectThreads];
+  __syncthreads();   // len_s
+  // 2. merge the vocabulary chunks of every needed row: one thread per row, its
+  //    chunk partials loaded together, max first, then one scaled sum
+  for (int r = tid; r < p.NRD; r += kSelectThreads) {
+    bool needed = r == 0;
+    if (r > 0 && r < p.NR) needed = ((r - 1) % p.Dmax) < len_s[(r - 1) / p.Dmax];
+    else if (r >= p.NR) needed = p.chain_blk >= 0 && (r - p.NR) < len_s[p.chain_blk];
+    if (!needed) continue;
+    const RowStat* src = p.part + (static_cast<int64_t>(b) * p.NRD + r) * p.nch;
+    float M = -INFINITY, S = 0.f, av = -INFINITY;
+    int ai = 0x7fffffff;
+    for (int c0 = 0; c0 < p.nch; c0 += 16) {
+      float4 v[16];
 #pragma unroll
-    for (int k = 0; k < kStage / kSelectThreads; ++k) {
-      const int e = tid + k * kSelectThreads;
-      if (e < ne) tmp[k] = src[e];
-    }
+      for (int q = 0; q < 16; ++q)
+        v[q] = (c0 + q < p.nch) ? __ldcg(reinterpret_cast<const float4*>(src + c0 + q))
+                                : make_float4(-INFINITY, 0.f, -INFINITY, __int_as_float(0x7fffffff));
+      float Mb = -INFINITY;
 #pragma unroll
-    for (int k = 0; k < kStage / kSelectThreads; ++k) {
-      const int e = tid + k * kSelectThreads;
-      if (e < ne) stage[e] = tmp[k];
-    }
-    __syncthreads();
-    for (int rr = wid; rr < nr; rr += nw) {
-      const int r = r0 + rr;
-      if (!row_needed(p, b, r)) continue;
-      float m = -INFINITY, s = 0.f, av = -INFINITY;
-      int ai = 0x7fffffff;
-      for (int c = lane; c < p.nch; c += 32) {
-        const RowStat x = stage[rr * p.nch + c];
-        stat_merge(m, s, x.m, x.s);
-        amax_merge(av, ai, x.amax_v, x.amax_i);
+      for (int q = 0; q < 16; ++q) {
+        Mb = fmaxf(Mb, v[q].x);
+        amax_merge(av, ai, v[q].z, __float_as_int(v[q].w));
       }
+      const float Mn = fmaxf(M, Mb);
+      if (Mn > -INFINITY) {
+        float acc = (M > -INFINITY) ? S * ex2_approx((M - Mn) * kLog2e) : 0.f;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-        const float v2 = __shfl_xor_sync(0xffffffffu, av, o);
-        const int i2 = __shfl_xor_sync(0xffffffffu, ai, o);
-        stat_merge(m, s, m2, s2);
-        amax_merge(av, ai, v2, i2);
-      }
-      if (lane == 0) {
-        const RowStat x{m, s, av, ai};
-        st[r] = x;
-        p.stat[static_cast<int64_t>(b) * p.NRD + r] = x;
+        for (int q = 0; q < 16; ++q)
+          if (v[q].x > -INFINITY) acc += v[q].y * ex2_approx((v[q].x - Mn) * kLog2e);
+        S = acc;
+        M = Mn;
       }
     }
-    __syncthreads();
+    const RowStat x{M, S, av, ai};
+    st[r] = x;
+    p.stat[static_cast<int64_t>(b) * p.NRD + r] = x;
   }
+  __syncthreads();
 
   // 3. acceptance test of every present token
 #pragma unroll
@@ -384,13 +352,20 @@ k_accept_select(AcceptParams p) {
     if (p.sample) {
       StopInfo si;
       si.row = stop;
+      si.ps = st[stop];
       si.a = a;
       si.drf_row = -1;
       si.excl = -1;
       si.bonus = (a >= L) ? 1 : 0;
+      si.qs = si.ps;
       if (a < L) {
-        if (best == p.chain_blk) si.drf_row = a;
-        else si.excl = p.blk_tok[static_cast<int64_t>(b) * nslots + best * p.Dmax + a];
+        if (best == p.chain_blk) {
+          si.drf_row = a;
+          si.qs = st[p.NR + a];
+        }
+        else {
+          si.excl = p.blk_tok[static_cast<int64_t>(b) * nslots + best * p.Dmax + a];
+        }
       }
       p.stop[b] = si;
       p.cnt[b] = 0u;
@@ -406,6 +381,89 @@ k_accept_select(AcceptParams p) {
     else if (i == a && !p.sample) v = sel[3];
     p.out_tok[static_cast<int64_t>(b) * (p.Dmax + 1) + i] = v;
   }
+  __syncthreads();
+}
+
+// next task (sequence, row, chunk) of this CTA whose row some token needs, or
+// ntask; tasks are numbered ((b * NRD) + r) * nch + c (fits in 32 bits)
+__device__ __forceinline__ int next_task(const AcceptParams& p, int t, int ntask) {
+  for (; t < ntask; t += gridDim.x) {
+    const int br = t / p.nch;
+    const int b = br / p.NRD, r = br - b * p.NRD;
+    if (row_needed(p, b, r)) break;
+  }
+  return t;
+}
+
+// Persistent CTAs walk the (sequence, row, chunk) tasks; the loads of the next
+// task are in flight while the current one is reduced.
+template <bool BF16>
+__global__ void __launch_bounds__(kVocabThreads, 2)
+k_vocab_stats(AcceptParams p) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  __shared__ RowStat red[kVocabThreads / 32];
+  // let the next kernel of the stream start its launch while this one runs
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // blk_len comes from the previous kernel of the stream
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int ntask = p.nch * p.NRD * p.B;
+  uint4 cur[kVec], nxt[kVec];
+  int t = next_task(p, blockIdx.x, ntask);
+  if (t < ntask) {
+    const int br = t / p.nch, c = t - br * p.nch;
+    const int b = br / p.NRD, r = br - b * p.NRD;
+    const int64_t lo = static_cast<int64_t>(c) * p.chunk;
+    const void* row = row_ptr(p, b, r);
+    load_chunk<BF16>(row, lo, min(p.V, lo + p.chunk), aligned_dev(row, 16), cur);
+  }
+  while (t < ntask) {
+    const int br = t / p.nch, c = t - br * p.nch;
+    const int b = br / p.NRD, r = br - b * p.NRD;
+    const int64_t lo = static_cast<int64_t>(c) * p.chunk;
+    // prefetch the next task
+    const int t2 = next_task(p, t + gridDim.x, ntask);
+    if (t2 < ntask) {
+      const int br2 = t2 / p.nch, c2 = t2 - br2 * p.nch;
+      const int b2 = br2 / p.NRD, r2 = br2 - b2 * p.NRD;
+      const int64_t lo2 = static_cast<int64_t>(c2) * p.chunk;
+      const void* row2 = row_ptr(p, b2, r2);
+      load_chunk<BF16>(row2, lo2, min(p.V, lo2 + p.chunk), aligned_dev(row2, 16), nxt);
+    }
+    float m, s, av;
+    int ai;
+    reduce_chunk<BF16>(cur, lo, p.probs, m, s, av, ai);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+      const float v2 = __shfl_xor_sync(0xffffffffu, av, o);
+      const int i2 = __shfl_xor_sync(0xffffffffu, ai, o);
+      stat_merge(m, s, m2, s2);
+      amax_merge(av, ai, v2, i2);
+    }
+    if (lane == 0) red[wid] = RowStat{m, s, av, ai};
+    __syncthreads();
+    if (tid == 0) {
+      for (int w = 1; w < kVocabThreads / 32; ++w) {
+        stat_merge(m, s, red[w].m, red[w].s);
+        amax_merge(av, ai, red[w].amax_v, red[w].amax_i);
+      }
+      p.part[(static_cast<int64_t>(b) * p.NRD + r) * p.nch + c] = RowStat{m, s, av, ai};
+    }
+    __syncthreads();   // red[] is reused by the next task of this CTA
+#pragma unroll
+    for (int v = 0; v < kVec; ++v) cur[v] = nxt[v];
+    t = t2;
+  }
+}
+
+// one CTA per sequence, once every chunk statistic is in
+__global__ void __launch_bounds__(kSelectThreads)
+k_accept_select(AcceptParams p) {
+  __shared__ SelectSmem sm;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");     // partials come from the stats kernel
+  for (int b = blockIdx.x; b < p.B; b += gridDim.x) select_one(p, b, sm);
 }
 
 // ------------------------------------------------------------------ final draw
@@ -431,10 +489,10 @@ __device__ void sample_final_one(const AcceptParams& p, int b, int c) {
 
   const StopInfo si = p.stop[b];
   const void* prow = row_ptr(p, b, si.row);
-  const RowStat ps = p.stat[static_cast<int64_t>(b) * p.NRD + si.row];
+  const RowStat ps = si.ps;
   const bool has_q = si.drf_row >= 0;
   const void* qrow = has_q ? row_ptr(p, b, p.NR + si.drf_row) : prow;
-  const RowStat qs = has_q ? p.stat[static_cast<int64_t>(b) * p.NRD + p.NR + si.drf_row] : ps;
+  const RowStat qs = si.qs;
 
   // phase 1: this chunk's residual and bonus weight sums (all loads first)
   const int64_t lo = static_cast<int64_t>(c) * kSampleChunk;
@@ -560,6 +618,8 @@ __device__ void sample_final_one(const AcceptParams& p, int b, int c) {
 
 __global__ void __launch_bounds__(kVocabThreads)
 k_sample_final(AcceptParams p) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");     // stop rows come from the previous kernel
   for (int b = blockIdx.y; b < p.B; b += gridDim.y) {
     sample_final_one(p, b, blockIdx.x);
     __syncthreads();   // shared state is reused by the next sequence of this CTA
@@ -569,6 +629,7 @@ k_sample_final(AcceptParams p) {
 // ------------------------------------------------------------------ diagnostics
 __global__ void __launch_bounds__(kVocabThreads)
 k_probs_out(AcceptParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int c = blockIdx.x % p.nch, r = blockIdx.x / p.nch;
   for (int b = blockIdx.y; b < p.B; b += gridDim.y) {
     if (!row_needed(p, b, r)) continue;
@@ -622,6 +683,10 @@ int accept_validate(const ssd_accept_args* a) {
   if (static_cast<long long>(a->NB) * a->Dmax > kMaxSlots) return SSD_ERR_UNSUPPORTED;
   const long long nrd = 1LL + static_cast<long long>(a->NB) * a->Dmax + (a->chain_blk >= 0 ? a->K : 0);
   if (nrd > kMaxRows) return SSD_ERR_UNSUPPORTED;
+  {
+    const long long chunk = static_cast<long long>(kVec) * kVocabThreads * (a->kind == SSD_LOGITS_BF16 ? 8 : 4);
+    if (((a->V + chunk - 1) / chunk) * nrd * a->B >= (1LL << 31)) return SSD_ERR_UNSUPPORTED;
+  }
   if (a->chain_blk >= 0 && (a->K < 1 || a->K > a->Dmax)) return SSD_ERR_INVALID;
   if (a->B == 0) return SSD_OK;
   if (!a->tgt || !a->blk_tok || !a->blk_len || !a->acc_len || !a->best_blk || !a->n_out || !a->out_tok)
@@ -656,28 +721,53 @@ AcceptParams accept_params(const ssd_accept_args* a, const AcceptLayout& L, char
   return p;
 }
 
+// resident CTAs of the stats kernel on the whole device (persistent grid)
+static long long stats_grid_cap(bool bf16) {
+  static long long cap[2] = {0, 0};
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  long long& c = cap[bf16 ? 1 : 0];
+  if (c == 0) {
+    int dev = 0, sms = 152, per = 1;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (bf16) cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, k_vocab_stats<true>, kVocabThreads, 0);
+    else cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, k_vocab_stats<false>, kVocabThreads, 0);
+    c = static_cast<long long>(sms) * (per > 0 ? per : 1);
+  }
+  return c;
+}
+
 int accept_launch(const AcceptParams& p, cudaStream_t s) {
   const unsigned by = static_cast<unsigned>(p.B < 65535 ? p.B : 65535);
-  dim3 g1(static_cast<unsigned>(p.nch * p.NRD), by);
+  cudaError_t e;
   {
+    // statistics of every needed row; the last CTA of each sequence runs the select
+    const long long ntask = static_cast<long long>(p.nch) * p.NRD * p.B;
+    const long long cap = stats_grid_cap(p.bf16 != 0);
+    const dim3 g1(static_cast<unsigned>(ntask < cap ? ntask : cap));
     KernelTimer t(SSD_KERNEL_VOCAB_STATS, s);
-    if (p.bf16) k_vocab_stats<true><<<g1, kVocabThreads, 0, s>>>(p);
-    else k_vocab_stats<false><<<g1, kVocabThreads, 0, s>>>(p);
+    e = p.bf16 ? launch_pdl(k_vocab_stats<true>, g1, dim3(kVocabThreads), 0, s, p)
+               : launch_pdl(k_vocab_stats<false>, g1, dim3(kVocabThreads), 0, s, p);
+    if (e != cudaSuccess) return SSD_ERR_CUDA;
   }
   {
     KernelTimer t(SSD_KERNEL_ACCEPT_SELECT, s);
-    k_accept_select<<<p.B, kSelectThreads, 0, s>>>(p);
+    const unsigned gb = static_cast<unsigned>(p.B < 1048576 ? p.B : 1048576);
+    e = launch_pdl(k_accept_select, dim3(gb), dim3(kSelectThreads), 0, s, p);
+    if (e != cudaSuccess) return SSD_ERR_CUDA;
   }
   int n = 2;
   if (p.sample) {
-    dim3 g3(static_cast<unsigned>(p.nchs), by);
+    const dim3 g3(static_cast<unsigned>(p.nchs), by);
     KernelTimer t(SSD_KERNEL_SAMPLE_FINAL, s);
-    k_sample_final<<<g3, kVocabThreads, 0, s>>>(p);
+    e = launch_pdl(k_sample_final, g3, dim3(kVocabThreads), 0, s, p);
+    if (e != cudaSuccess) return SSD_ERR_CUDA;
     ++n;
   }
   if (p.probs_out != nullptr) {
-    dim3 g4(static_cast<unsigned>(p.nch * p.NR), by);
-    k_probs_out<<<g4, kVocabThreads, 0, s>>>(p);
+    const dim3 g4(static_cast<unsigned>(p.nch * p.NR), by);
+    e = launch_pdl(k_probs_out, g4, dim3(kVocabThreads), 0, s, p);
+    if (e != cudaSuccess) return SSD_ERR_CUDA;
     ++n;
   }
   count_launch(n);

@@ -22,6 +22,8 @@ struct StopInfo {
   int excl;      // one-hot q of a rejected copy token, or -1
   int bonus;     // 1: every token was accepted, draw from p
   int pad[3];
+  RowStat ps;    // statistics of the target row
+  RowStat qs;    // statistics of the draft row (= ps when there is none)
 };
 
 struct AcceptParams {
@@ -46,7 +48,7 @@ struct AcceptParams {
   RowStat* stat;      // [B][NRD]
   StopInfo* stop;     // [B]
   long long* csum;    // [B][nchs][2]
-  unsigned* cnt;      // [B]
+  unsigned* cnt;      // [B] sampler completion counters (set by the select)
 };
 
 struct AcceptLayout {

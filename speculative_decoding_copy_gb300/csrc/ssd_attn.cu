@@ -54,6 +54,7 @@ __global__ void __launch_bounds__(kSimtThreads)
 k_attn_prefix_simt(AttnParams p) {
   constexpr int EPL = DH / 32;   // output dims per lane
   __shared__ float q_s[kSimtRows][DH];
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ float k_s[kKeyTile][DH + 1];
   __shared__ float v_s[kKeyTile][DH];
 
@@ -156,6 +157,7 @@ __global__ void __launch_bounds__(128)
 k_attn_combine(AttnParams p) {
   constexpr int EPL = DH / 32;
   __shared__ float sc_s[4][256];
+  asm volatile("griddepcontrol.wait;" ::: "memory");     // partials come from the prefix pass
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int NT = p.NB * p.Dmax;
   const int64_t R = static_cast<int64_t>(blockIdx.x) * 4 + wid;
@@ -375,13 +377,15 @@ int attn_combine_launch(const AttnParams& p, int dtype, int dh, cudaStream_t s) 
   const long long rows = static_cast<long long>(p.B) * NT * p.Hq;
   dim3 g2(static_cast<unsigned>((rows + 3) / 4));
   KernelTimer t(SSD_KERNEL_ATTN_COMBINE, s);
+  cudaError_t e;
   if (dtype == SSD_F32) {
-    if (dh == 64) k_attn_combine<float, 64><<<g2, 128, 0, s>>>(p);
-    else k_attn_combine<float, 128><<<g2, 128, 0, s>>>(p);
+    if (dh == 64) e = launch_pdl(k_attn_combine<float, 64>, g2, dim3(128), 0, s, p);
+    else e = launch_pdl(k_attn_combine<float, 128>, g2, dim3(128), 0, s, p);
   } else {
-    if (dh == 64) k_attn_combine<uint16_t, 64><<<g2, 128, 0, s>>>(p);
-    else k_attn_combine<uint16_t, 128><<<g2, 128, 0, s>>>(p);
+    if (dh == 64) e = launch_pdl(k_attn_combine<uint16_t, 64>, g2, dim3(128), 0, s, p);
+    else e = launch_pdl(k_attn_combine<uint16_t, 128>, g2, dim3(128), 0, s, p);
   }
+  if (e != cudaSuccess) return SSD_ERR_CUDA;
   return check_launch();
 }
 }  // namespace ssd

@@ -210,6 +210,7 @@ k_attn_prefix_tc(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   Bars& bars = *reinterpret_cast<Bars*>(smem + OFF_BAR);
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // the combine may start its launch
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int mt = blockIdx.x % mtiles;

@@ -1,7 +1,7 @@
 """One speculate-and-verify step on the GPU: device buffers for a batch and the
 launch order of the four C-ABI calls.
 
-    gate_match -> retrieve -> { verify_attn (aux stream) || accept (main stream) }
+    gate_retrieve -> { verify_attn (aux stream) || accept (main stream) }
 
 Verification attention and acceptance both depend only on the retrieval
 output, so with an auxiliary stream they run concurrently. The step issues
@@ -60,7 +60,7 @@ class VerifyStep:
             a = ssd.accept_args(self.mode, self.kind, self.x["tgt"], self.x.get("drf"), self.ret_out["blk_tok"],
                                 self.ret_out["blk_len"], wl.K, self.chain_blk, self.x["u_acc"], self.x["u_fin"],
                                 self.acc_out, self.probs)
-            self.acc_ws = torch.empty(max(256, ssd.ssd_accept_workspace_size(a)), dtype=torch.uint8,
+            self.acc_ws = torch.zeros(max(256, ssd.ssd_accept_workspace_size(a)), dtype=torch.uint8,
                                       device=self.device)
         if self.with_attention:
             self.attn_out = torch.empty_like(self.x["q"])
@@ -82,6 +82,13 @@ class VerifyStep:
         return ssd.ssd_retrieve(x["ctx"], x["ctx_len"], self.gate_out["gate"], self.gate_out["last_match_end"],
                                 wl.kappa, wl.W, wl.D, wl.K, wl.chain_policy, ct, out=self.ret_out, stream=stream)
 
+    def gate_retrieve(self, stream=None):
+        """Gate and retrieval fused into one launch (same outputs as gate() then retrieve())."""
+        wl, x = self.wl, self.x
+        ct = x.get("chain_tok") if wl.chain_policy else None
+        return ssd.ssd_gate_retrieve(x["ctx"], x["ctx_len"], x["h"], x["w"], wl.tau, wl.kappa, wl.W, wl.D, wl.K,
+                                     wl.chain_policy, ct, out={**self.gate_out, **self.ret_out}, stream=stream)
+
     def attention(self, stream=None):
         x = self.x
         return ssd.ssd_verify_attn(x["q"], x["k_cache"], x["v_cache"], x["k_cand"], x["v_cand"], x["prefix_len"],
@@ -98,8 +105,7 @@ class VerifyStep:
     def run(self, stream=None, aux: torch.cuda.Stream | None = None):
         """Issue the whole step on `stream` (default: current), attention on `aux` if given."""
         main = stream or torch.cuda.current_stream()
-        self.gate(main)
-        self.retrieve(main)
+        self.gate_retrieve(main)
         if self.with_attention and aux is not None:
             ev = torch.cuda.Event()
             ev.record(main)

@@ -22,8 +22,23 @@ def _run(ctx, ctx_len, h, h_dtype, w, tau, kappa, W, D, K, policy, chain_tok):
     return {k: v.cpu().numpy() for k, v in {**g, **r}.items()}
 
 
+def _run_fused(ctx, ctx_len, h, h_dtype, w, tau, kappa, W, D, K, policy, chain_tok):
+    dev = "cuda"
+    tc, tl, th, tw = (to_device(np.asarray(a), dev) for a in (ctx, ctx_len, h, w))
+    ct = to_device(np.asarray(chain_tok), dev) if policy else None
+    r = S.ssd_gate_retrieve(tc, tl, th, tw, tau, kappa, W, D, K, policy, ct)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in r.items()}
+
+
 def _compare(ctx, ctx_len, h, h_dtype, w, tau, kappa, W, D, K, policy, chain_tok):
     got = _run(ctx, ctx_len, h, h_dtype, w, tau, kappa, W, D, K, policy, chain_tok)
+    fused = _run_fused(ctx, ctx_len, h, h_dtype, w, tau, kappa, W, D, K, policy, chain_tok)
+    for k in got:
+        if k == "score":
+            np.testing.assert_allclose(fused[k], got[k], atol=1e-6)
+        else:
+            np.testing.assert_array_equal(fused[k], got[k], err_msg=f"fused {k}")
     score, on, gate, last = O.gate_match(ctx, ctx_len, h, h_dtype, w, tau, kappa)
     bt, bl, nc = O.retrieve(ctx, ctx_len, gate, kappa, W, D, K, policy, chain_tok)
     np.testing.assert_array_equal(got["probe_on"], on.astype(np.int32))
