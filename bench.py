@@ -201,7 +201,7 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-KERNELS = ["gate_match", "attn_prefix", "attn_combine", "vocab_stats", "sample_final"]
+KERNELS = ["gate_match", "verify_attn", "vocab_stats", "accept_select", "sample_final"]
 
 
 def source_sha(*names):
@@ -213,7 +213,7 @@ def source_sha(*names):
 
 
 KERNEL_SOURCES = {"vocab_stats": ("ssd_accept.cu", "ssd_accept.cuh", "ssd_common.cuh"),
-                  "attn_prefix": ("ssd_attn.cu", "ssd_attn_tc.cu", "ssd_attn.cuh", "ssd_common.cuh")}
+                  "verify_attn": ("ssd_attn.cu", "ssd_attn_tc.cu", "ssd_attn.cuh", "ssd_common.cuh")}
 
 
 def dram_traffic(kernel, workload):
@@ -306,7 +306,7 @@ def run_ours(args):
     kern_us = {k: mean_us(diag_ev, k) for k in KERNELS}
     kern_us = {k: v for k, v in kern_us.items() if v is not None}
     del diag_graphs
-    streaming = [k for k in ("vocab_stats", "attn_prefix") if k in kern_us]
+    streaming = [k for k in ("vocab_stats", "verify_attn") if k in kern_us]
     dom = max(streaming, key=lambda k: kern_us[k])
 
     # timed graphs: only the dominant kernel is bracketed by events
@@ -351,7 +351,7 @@ def run_ours(args):
     e2e = run_e2e(args, wl, inp, steps[0], main, aux, dev)
 
     hbm, peak_kind = measured_peaks()
-    kb = {"vocab_stats": ab["logits"], "attn_prefix": ab["kv"] + (ab["q_o"] // 2)}
+    kb = {"vocab_stats": ab["logits"], "verify_attn": ab["kv"] + (ab["q_o"] // 2)}
     achieved = kb[dom] / (dom_us * 1e-6) / 1e9 if dom_us else None
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
                 "frac": (achieved / hbm) if achieved else None, "traffic": dram_traffic(dom, wl.name),

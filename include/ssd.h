@@ -161,6 +161,7 @@ int ssd_gate_retrieve(const int32_t* ctx, int64_t ctx_stride, const int32_t* ctx
  *   prefix_len [B] int32, blk_len [B][NB] int32
  * Supported: dh in {64, 128}; Hq % Hkv == 0; 1 <= Dmax <= 256.
  * scale == 0 selects 1/sqrt(dh). Accumulation is fp32 whatever `dtype`.
+ * out_dtype is `dtype` or SSD_F32 (an fp32 output for bf16 inputs).
  * Workspace: ssd_verify_attn_workspace_size(a) bytes, 256-byte aligned; its
  * contents need no initialisation. Device-side errors are recorded in it.
  */
@@ -177,6 +178,7 @@ typedef struct {
   int B, NB, Dmax, Hq, Hkv, dh;
   int64_t P_max;
   float scale;
+  int out_dtype;
 } ssd_attn_args;
 
 size_t ssd_verify_attn_workspace_size(const ssd_attn_args* a);
@@ -286,7 +288,7 @@ int ssd_read_device_error(void* ws, void* stream, int32_t* out);
 enum {
   SSD_KERNEL_NONE = 0,
   SSD_KERNEL_VOCAB_STATS = 1,
-  SSD_KERNEL_ATTN_PREFIX = 2,
+  SSD_KERNEL_VERIFY_ATTN = 2,        /* the tensor-core attention kernel, or the SIMT prefix pass */
   SSD_KERNEL_ATTN_COMBINE = 3,
   SSD_KERNEL_ACCEPT_SELECT = 4,
   SSD_KERNEL_SAMPLE_FINAL = 5,

@@ -26,7 +26,7 @@ SSD_CHAIN_NONE, SSD_CHAIN_WHEN_GATE_OFF, SSD_CHAIN_ALWAYS = 0, 1, 2
 EXPORTED = ["ssd_status_string", "ssd_version", "ssd_launch_count", "ssd_gate_match", "ssd_retrieve",
             "ssd_verify_attn_workspace_size", "ssd_verify_attn", "ssd_accept_workspace_size", "ssd_accept",
             "ssd_read_device_error", "ssd_profile_kernel", "ssd_accept_static", "ssd_gate_retrieve"]
-SSD_KERNEL = dict(vocab_stats=1, attn_prefix=2, attn_combine=3, accept_select=4, sample_final=5, gate_match=6,
+SSD_KERNEL = dict(vocab_stats=1, verify_attn=2, attn_combine=3, accept_select=4, sample_final=5, gate_match=6,
                   retrieve=7)
 
 
@@ -40,7 +40,7 @@ class AttnArgs(ctypes.Structure):
     _fields_ = [("q", c_void_p), ("k_cache", c_void_p), ("v_cache", c_void_p), ("k_cand", c_void_p),
                 ("v_cand", c_void_p), ("out", c_void_p), ("prefix_len", c_void_p), ("blk_len", c_void_p),
                 ("dtype", c_int), ("B", c_int), ("NB", c_int), ("Dmax", c_int), ("Hq", c_int), ("Hkv", c_int),
-                ("dh", c_int), ("P_max", c_int64), ("scale", c_float)]
+                ("dh", c_int), ("P_max", c_int64), ("scale", c_float), ("out_dtype", c_int)]
 
 
 class AcceptArgs(ctypes.Structure):
@@ -213,7 +213,7 @@ def attn_args(q, k_cache, v_cache, k_cand, v_cand, prefix_len, blk_len, Dmax, ou
     NB = blk_len.shape[1]
     return AttnArgs(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_cand), _ptr(v_cand), _ptr(out),
                     _ptr(prefix_len), _ptr(blk_len), _elem_type(q), B, NB, int(Dmax), Hq, Hkv, dh,
-                    k_cache.shape[2], float(scale))
+                    k_cache.shape[2], float(scale), _elem_type(out))
 
 
 def ssd_verify_attn_workspace_size(args: AttnArgs) -> int:
@@ -221,8 +221,9 @@ def ssd_verify_attn_workspace_size(args: AttnArgs) -> int:
 
 
 def ssd_verify_attn(q, k_cache, v_cache, k_cand, v_cand, prefix_len, blk_len, Dmax, *, out=None, ws=None,
-                    scale=0.0, stream=None):
-    """Block-triangular verification attention; returns the output tensor [B][NT][Hq][dh]."""
+                    scale=0.0, stream=None, out_f32=False):
+    """Block-triangular verification attention; returns the output tensor [B][NT][Hq][dh]
+    (the inputs' dtype, or fp32 with out_f32)."""
     types = (torch.float32,) + _HALF
     for n, t in [("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("k_cand", k_cand), ("v_cand", v_cand)]:
         _need(t, n, types, 4)
@@ -231,7 +232,7 @@ def ssd_verify_attn(q, k_cache, v_cache, k_cand, v_cand, prefix_len, blk_len, Dm
     _need(prefix_len, "prefix_len", (torch.int32,), 1)
     _need(blk_len, "blk_len", (torch.int32,), 2)
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device) if out_f32 else torch.empty_like(q)
     args = attn_args(q, k_cache, v_cache, k_cand, v_cand, prefix_len, blk_len, Dmax, out, scale)
     need = ssd_verify_attn_workspace_size(args)
     if ws is None:

@@ -14,8 +14,9 @@
 //                   (log2 units) in the workspace;
 //   combine:        one warp per row merges the splits, adds the row's own
 //                   block keys, normalises and stores the output.
-// bf16 inputs use the tcgen05 prefix kernel (ssd_attn_tc.cu) when it applies;
-// the SIMT prefix kernel below serves fp32 and every other shape.
+// bf16 inputs with head dim 128 use the fused tcgen05 kernel (ssd_attn_tc.cu),
+// which covers both parts in one launch; the SIMT pair below serves fp32, head
+// dim 64 and every other shape.
 #include <math.h>
 
 #include "ssd_attn.cuh"
@@ -262,9 +263,15 @@ k_attn_combine(AttnParams p) {
     }
   }
   const float inv = 1.f / L;
-  T* out = static_cast<T*>(p.out) + R * DH;
+  if (p.out_f32) {
+    float* out = static_cast<float*>(p.out) + R * DH;
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) st_elem(out, lane + 32 * e, O[e] * inv);
+    for (int e = 0; e < EPL; ++e) out[lane + 32 * e] = O[e] * inv;
+  } else {
+    T* out = static_cast<T*>(p.out) + R * DH;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) st_elem(out, lane + 32 * e, O[e] * inv);
+  }
 }
 
 // ---------------------------------------------------------------- host
@@ -291,6 +298,7 @@ static int validate(const ssd_attn_args* a) {
   if (a == nullptr) return SSD_ERR_INVALID;
   if (a->B < 0 || a->NB < 1 || a->Dmax < 1 || a->Hq < 1 || a->Hkv < 1 || a->P_max < 0) return SSD_ERR_INVALID;
   if (a->dtype != SSD_F32 && a->dtype != SSD_BF16) return SSD_ERR_INVALID;
+  if (a->out_dtype != a->dtype && a->out_dtype != SSD_F32) return SSD_ERR_INVALID;
   if (a->Hq % a->Hkv != 0) return SSD_ERR_INVALID;
   if (a->Dmax > 256 || a->NB * a->Dmax > 8192 || a->Hq / a->Hkv > 64) return SSD_ERR_UNSUPPORTED;
   if (static_cast<long long>(a->B) * a->Hkv > 0x7fffffffLL) return SSD_ERR_UNSUPPORTED;
@@ -347,6 +355,7 @@ extern "C" int ssd_verify_attn(const ssd_attn_args* a, void* ws, size_t ws_bytes
   const float scale = a->scale != 0.f ? a->scale : 1.f / sqrtf(static_cast<float>(a->dh));
   p.scale_log2 = scale * 1.4426950408889634f;
   p.S = L.S; p.chunk = L.chunk;
+  p.out_f32 = (a->out_dtype == SSD_F32) ? 1 : 0;
   char* base = static_cast<char*>(ws);
   p.hdr = reinterpret_cast<WsHeader*>(base);
   p.ws_ml = reinterpret_cast<float*>(base + L.ml_off);
@@ -356,7 +365,7 @@ extern "C" int ssd_verify_attn(const ssd_attn_args* a, void* ws, size_t ws_bytes
   const int G = a->Hq / a->Hkv;
   dim3 g1(a->B * a->Hkv, (NT * G + kSimtRows - 1) / kSimtRows, L.S);
   {
-    KernelTimer t(SSD_KERNEL_ATTN_PREFIX, s);
+    KernelTimer t(SSD_KERNEL_VERIFY_ATTN, s);
     if (a->dtype == SSD_F32) {
       if (a->dh == 64) k_attn_prefix_simt<float, 64><<<g1, kSimtThreads, 0, s>>>(p);
       else k_attn_prefix_simt<float, 128><<<g1, kSimtThreads, 0, s>>>(p);

@@ -17,6 +17,7 @@ struct AttnParams {
   int B, NB, Dmax, Hq, Hkv;
   int64_t P_max;
   float scale_log2;      // softmax scale times log2(e): scores are kept in log2 units
+  int out_f32;           // 1: fp32 output whatever the input type
   int S, chunk;          // KV splits and keys per split
   WsHeader* hdr;
   float* ws_ml;          // [rows][S][2]  running max and sum per split

@@ -1,28 +1,38 @@
-// tcgen05 prefix pass of the verification attention (bf16, head dim 128).
+// Verification attention for bf16, head dim 128, on the tensor cores.
 //
-// Every candidate token of a sequence sees the same prefix keys (SwitchSD page,
-// "무엇과 다른가": each candidate attends to the whole prefix), so for one kv
+// SwitchSD page, "무엇과 다른가": a candidate token attends to the whole prefix
+// and to the earlier tokens of its own candidate, never to another candidate.
+// Every candidate token of a sequence sees the same prefix keys, so for one kv
 // head the G query heads of all NT candidate slots pack into NT*G rows of one
-// dense product with each prefix tile. A CTA owns 128 packed rows (the M of
-// the MMA) and one split of the prefix; it leaves the same per-split partial
-// (running max m, sum l, un-normalised o, log2 units) as the SIMT pass, and
-// the combine kernel adds the own-block keys and merges the splits.
+// dense product with each key tile. A CTA owns 128 packed rows (the M of the
+// MMA) and one split of the prefix; the S CTAs of a row tile form a thread-block
+// cluster, rank 0 also takes the own-block keys as masked tiles, and the splits
+// are merged on chip through distributed shared memory: no partial results go
+// to HBM and no second kernel runs.
 //
 // Per CTA (192 threads, one CTA per SM):
 //   warps 0-3  one thread per packed row: stage Q, online softmax from the S
-//              row in TMEM (tcgen05.ld), O rescale in TMEM, P as bf16 into
-//              shared memory, epilogue;
+//              row in TMEM (tcgen05.ld) with the row's key mask (a contiguous
+//              range per tile), O rescale in TMEM, P as bf16 into shared
+//              memory; after the loop the O row, max and sum are staged in
+//              shared memory for the cluster merge;
 //   warp 4     TMA producer: K and V tiles of 64 keys (two 64-wide halves of
-//              the head dim, 128-byte swizzle) into a 4-stage ring;
+//              the head dim, 128-byte swizzle) into a 4-stage ring, from the
+//              prefix cache (2-D map) or the candidate keys (3-D map);
 //   warp 5     TMEM allocation and the single MMA-issuing thread:
 //              S = Q K^T (M128 N64, K16 x 8) into one of two TMEM buffers and
 //              O += P V (M128 N128, K16 x 4), kind::f16 with bf16 operands and
 //              fp32 accumulators in TMEM. S of tile j+1 is issued before P V of
 //              tile j so the tensor core works while the rows run the softmax;
 //              P is double-buffered in shared memory.
+// Merge: each CTA of the cluster normalises 128/S rows, reading every split's
+// O, max and sum from its peers' shared memory, and writes the bf16 output of
+// the tokens that exist. The kernel may be launched before the retrieval that
+// decides which tokens exist has finished (programmatic dependent launch): it
+// reads the block lengths only after griddepcontrol.wait, just before writing.
 // Every mbarrier wait is bounded (about 2^32 clocks); on expiry the CTA
 // records SSD_ERR_TIMEOUT in the workspace header, skips the remaining waits,
-// frees its TMEM and exits.
+// frees its TMEM and exits through the cluster barriers.
 #include <cuda.h>
 #include <math.h>
 
@@ -110,6 +120,45 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
           "r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// whole-cluster barrier: arrive (release) + wait (acquire); every thread of every CTA
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// shared-memory address of the same location in the CTA of cluster rank `rank`
+__device__ __forceinline__ uint32_t map_peer(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float ld_peer_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float4 ld_peer_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
 }
 
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -203,20 +252,25 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
 __device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t c) { return r * 128u + ((c ^ (r & 7u)) << 4); }
 
 // ------------------------------------------------------------------ kernel
+constexpr int kMaxSplit = 8;              // cluster size limit (portable)
+constexpr int kOStride = 132;             // fp32 per staged O row (padding against bank conflicts)
+constexpr int kMergeItems = BM + kMaxSplit;   // bound on (rows merged by one CTA) x S
+
+// grid (S, row tiles, B*Hkv), cluster (S, 1, 1): the S CTAs of one row tile split
+// the prefix; cluster rank 0 also takes the own-block (candidate) keys.
 __global__ void __launch_bounds__(kThreads, 1)
-k_attn_prefix_tc(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                 AttnParams p, int mtiles) {
+k_attn_tc(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+          const __grid_constant__ CUtensorMap tmap_kc, const __grid_constant__ CUtensorMap tmap_vc, AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   Bars& bars = *reinterpret_cast<Bars*>(smem + OFF_BAR);
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // the combine may start its launch
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int mt = blockIdx.x % mtiles;
-  const int bk = blockIdx.x / mtiles;
-  const int b = bk / p.Hkv, kvh = bk % p.Hkv;
-  const int split = blockIdx.y;
+  const int split = static_cast<int>(cluster_rank());
+  const int S = static_cast<int>(gridDim.x);
+  const int mt = blockIdx.y;
+  const int b = blockIdx.z / p.Hkv, kvh = blockIdx.z % p.Hkv;
   const int G = p.Hq / p.Hkv;
   const int NT = p.NB * p.Dmax;
   const int rows_total = NT * G;
@@ -224,31 +278,22 @@ k_attn_prefix_tc(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   const int P = p.prefix_len[b];
   const int k0 = split * p.chunk;
   const int k1 = min(P, k0 + p.chunk);
-  const int nT = k1 > k0 ? (k1 - k0 + BN - 1) / BN : 0;
+  const int nP = k1 > k0 ? (k1 - k0 + BN - 1) / BN : 0;
+  // candidate slots of this row tile: from the start of its first token's block to its last token
+  const int t_first = r0 / G;
+  const int t_last = min(NT - 1, (r0 + BM - 1) / G);
+  const int s_base = (t_first / p.Dmax) * p.Dmax;
+  const int nC = (split == 0 && t_first < NT) ? (t_last + 1 - s_base + BN - 1) / BN : 0;
+  const int nT = nC + nP;
 
-  // this thread's packed row (softmax warps) and whether it is a present token
+  // this thread's packed row: token t, q-head h, allowed own-block slots [c_lo, t]
   const int r = r0 + tid;
-  bool present = false;
-  int t = 0, h = 0;
-  if (tid < BM && r < rows_total) {
-    t = r / G;
-    h = kvh * G + r % G;
-    present = (t % p.Dmax) < p.blk_len[b * p.NB + t / p.Dmax];
-  }
-  if (!__syncthreads_or(present)) return;          // no present row in this tile
-  const int64_t R = (static_cast<int64_t>(b) * NT + t) * p.Hq + h;
+  const bool row_ok = tid < BM && r < rows_total;
+  const int t = row_ok ? r / G : 0;
+  const int h = row_ok ? kvh * G + r % G : 0;
+  const int c_lo = (t / p.Dmax) * p.Dmax;
 
-  if (nT == 0) {                                   // empty split: neutral partial
-    if (present) {
-      float* ml = p.ws_ml + (R * p.S + split) * 2;
-      ml[0] = -INFINITY;
-      ml[1] = 0.f;
-      float4* ow = reinterpret_cast<float4*>(p.ws_o + (R * p.S + split) * DH);
-      for (int e = 0; e < DH / 4; ++e) ow[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    return;
-  }
-
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&bars.full[s], 1);
@@ -275,142 +320,165 @@ k_attn_prefix_tc(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
   const uint32_t tmem_O = tmem + 128;
+  float* ostage = reinterpret_cast<float*>(smem + OFF_K);          // [128][kOStride] after the main loop
+  float* ml_s = reinterpret_cast<float*>(smem + OFF_P);            // [2][128] after the main loop
 
   if (warp < 4) {
     // ---------------------------------------------------------- softmax rows
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    {
-      // stage Q row `tid` (zeros past the last packed row), 128-byte swizzle
-      const uint4* q4 = nullptr;
-      if (r < rows_total)
-        q4 = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
-                                            ((static_cast<int64_t>(b) * NT + t) * p.Hq + h) * DH);
-      uint4 qv[16];
+    float m = -INFINITY, l = 0.f;        // reference max (log2 units) and sum
+    if (nT > 0) {
+      {
+        // stage Q row `tid` (zeros past the last packed row), 128-byte swizzle
+        const uint4* q4 = row_ok ? reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
+                                                                   ((static_cast<int64_t>(b) * NT + t) * p.Hq + h) * DH)
+                                 : nullptr;
+        uint4 qv[16];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) qv[c] = q4 ? __ldg(q4 + c) : make_uint4(0, 0, 0, 0);
+        for (int c = 0; c < 16; ++c) qv[c] = q4 ? __ldg(q4 + c) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
-        st_shared_v4(sbase + OFF_Q + (c >> 3) * kQHalf + sw128_off(tid, c & 7), qv[c].x, qv[c].y, qv[c].z, qv[c].w);
-      fence_async_smem();
-      mbar_arrive(&bars.q_full);
-    }
-    const float sl2 = p.scale_log2;
-    float m = -INFINITY, l = 0.f;        // running reference max (log2 units) and sum
-    for (int j = 0; j < nT; ++j) {
-      const int sb = j & 1;
-      mbar_wait(bars, &bars.s_full[sb], (j >> 1) & 1, p.hdr, 10);
-      tc_fence_after();
-      uint32_t sreg[BN];
-#pragma unroll
-      for (int q = 0; q < BN / 32; ++q) tmem_ld32(tmem + sb * BN + lane_off + q * 32, sreg + q * 32);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&bars.s_free[sb]);
-      float mx = -INFINITY;
-      const int nvalid = k1 - (k0 + j * BN);
-      if (nvalid >= BN) {
-#pragma unroll
-        for (int c = 0; c < BN; ++c) mx = fmaxf(mx, __uint_as_float(sreg[c]));
-      } else {
-#pragma unroll
-        for (int c = 0; c < BN; ++c) {
-          if (c >= nvalid) sreg[c] = __float_as_uint(-INFINITY);
-          mx = fmaxf(mx, __uint_as_float(sreg[c]));
-        }
+        for (int c = 0; c < 16; ++c)
+          st_shared_v4(sbase + OFF_Q + (c >> 3) * kQHalf + sw128_off(tid, c & 7), qv[c].x, qv[c].y, qv[c].z,
+                       qv[c].w);
+        fence_async_smem();
+        mbar_arrive(&bars.q_full);
       }
-      // reference max only moves when the row max grows by more than 2^8
-      const float m_new = fmaxf(m, mx * sl2);
-      const bool need = m_new > m + 8.f;
-      const float mref = need ? m_new : m;
-      const float alpha = need ? ex2_approx(m - m_new) : 1.f;
-      uint32_t pk[BN / 2];
-      float rs0 = 0.f, rs1 = 0.f;
-#pragma unroll
-      for (int c = 0; c < BN; c += 2) {
-        const float p0 = ex2_approx(fmaf(__uint_as_float(sreg[c]), sl2, -mref));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(sreg[c + 1]), sl2, -mref));
-        const uint32_t w = pack_bf16(p0, p1);
-        pk[c / 2] = w;
-        // sum the rounded values the MMA uses, so numerator and denominator agree
-        rs0 += __uint_as_float(w << 16);
-        rs1 += __uint_as_float(w & 0xffff0000u);
-      }
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // O holds the sum up to tile j-1: wait for its last MMA, then rescale
-        mbar_wait(bars, &bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, p.hdr, 11);
+      const float sl2 = p.scale_log2;
+      for (int j = 0; j < nT; ++j) {
+        const int sb = j & 1;
+        mbar_wait(bars, &bars.s_full[sb], (j >> 1) & 1, p.hdr, 10);
         tc_fence_after();
-        uint32_t o[32];
+        uint32_t sreg[BN];
 #pragma unroll
-        for (int q = 0; q < DH / 32; ++q) {
-          tmem_ld32(tmem_O + lane_off + q * 32, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(tmem_O + lane_off + q * 32, o);
+        for (int q = 0; q < BN / 32; ++q) tmem_ld32(tmem + sb * BN + lane_off + q * 32, sreg + q * 32);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&bars.s_free[sb]);
+        // valid columns: a contiguous range [v_lo, v_hi) of this tile
+        int v_lo, v_hi;
+        if (j < nC) {                                   // own-block keys: slots c_lo .. t
+          const int s0 = s_base + j * BN;
+          v_lo = row_ok ? c_lo - s0 : BN;
+          v_hi = row_ok ? t + 1 - s0 : 0;
+        } else {                                        // prefix keys below k1
+          v_lo = 0;
+          v_hi = k1 - (k0 + (j - nC) * BN);
         }
-        tmem_wait_st();
-      }
-      l = l * alpha + (rs0 + rs1);
-      m = mref;
-      // P buffer sb was last read by the MMA of tile j-2
-      if (j >= 2) mbar_wait(bars, &bars.pv_done[sb], ((j - 2) >> 1) & 1, p.hdr, 12);
+        if (v_lo > 0 || v_hi < BN) {
 #pragma unroll
-      for (int c = 0; c < BN / 8; ++c)
-        st_shared_v4(sbase + OFF_P + sb * kPBuf + sw128_off(tid, c), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
-                     pk[4 * c + 3]);
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(&bars.p_full[sb]);
+          for (int c = 0; c < BN; ++c)
+            if (c < v_lo || c >= v_hi) sreg[c] = __float_as_uint(-INFINITY);
+        }
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < BN; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], __uint_as_float(sreg[c]));
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        // reference max only moves when the row max grows by more than 2^8
+        const float m_new = fmaxf(m, mx * sl2);
+        const bool need = m_new > m + 8.f;
+        const float mref = need ? m_new : m;
+        const float alpha = need ? ex2_approx(m - m_new) : 1.f;
+        uint32_t pk[BN / 2];
+        float rs[4] = {0.f, 0.f, 0.f, 0.f};
+        if (mref > -INFINITY) {
+#pragma unroll
+          for (int c = 0; c < BN; c += 2) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(sreg[c]), sl2, -mref));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(sreg[c + 1]), sl2, -mref));
+            const uint32_t w = pack_bf16(p0, p1);
+            pk[c / 2] = w;
+            // sum the rounded values the MMA uses, so numerator and denominator agree
+            rs[(c >> 1) & 1] += __uint_as_float(w << 16);
+            rs[2 + ((c >> 1) & 1)] += __uint_as_float(w & 0xffff0000u);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < BN / 2; ++c) pk[c] = 0u;   // no allowed key yet in this row
+        }
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          // O holds the sum up to tile j-1: wait for its last MMA, then rescale
+          mbar_wait(bars, &bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, p.hdr, 11);
+          tc_fence_after();
+          uint32_t o[32];
+#pragma unroll
+          for (int q = 0; q < DH / 32; ++q) {
+            tmem_ld32(tmem_O + lane_off + q * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(tmem_O + lane_off + q * 32, o);
+          }
+          tmem_wait_st();
+        }
+        l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+        m = mref;
+        // P buffer sb was last read by the MMA of tile j-2
+        if (j >= 2) mbar_wait(bars, &bars.pv_done[sb], ((j - 2) >> 1) & 1, p.hdr, 12);
+#pragma unroll
+        for (int c = 0; c < BN / 8; ++c)
+          st_shared_v4(sbase + OFF_P + sb * kPBuf + sw128_off(tid, c), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                       pk[4 * c + 3]);
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bars.p_full[sb]);
+      }
+      mbar_wait(bars, &bars.pv_done[(nT - 1) & 1], ((nT - 1) >> 1) & 1, p.hdr, 13);
+      tc_fence_after();
     }
-    // epilogue: un-normalised o, reference max and sum of this split
-    mbar_wait(bars, &bars.pv_done[(nT - 1) & 1], ((nT - 1) >> 1) & 1, p.hdr, 13);
-    tc_fence_after();
-    float* ow = p.ws_o + (R * p.S + split) * DH;
+    // stage this CTA's un-normalised O row, reference max and sum for the cluster merge
+    float* orow = ostage + tid * kOStride;
 #pragma unroll
     for (int q = 0; q < DH / 32; ++q) {
       uint32_t o[32];
-      tmem_ld32(tmem_O + lane_off + q * 32, o);
-      tmem_wait_ld();
-      if (present) {
-        float4* o4 = reinterpret_cast<float4*>(ow + q * 32);
+      if (nT > 0) {
+        tmem_ld32(tmem_O + lane_off + q * 32, o);
+        tmem_wait_ld();
+      } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          o4[e] = make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
-                              __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+        for (int e = 0; e < 32; ++e) o[e] = 0u;
       }
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        reinterpret_cast<float4*>(orow + q * 32)[e] =
+            make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]), __uint_as_float(o[4 * e + 2]),
+                        __uint_as_float(o[4 * e + 3]));
     }
-    if (present) {
-      float* ml = p.ws_ml + (R * p.S + split) * 2;
-      ml[0] = m;
-      ml[1] = l;
-    }
+    ml_s[tid] = m;
+    ml_s[BM + tid] = l;
   } else if (warp == 4) {
     // ---------------------------------------------------------- TMA producer
-    if (lane == 0) {
+    if (lane == 0 && nT > 0) {
       const int y0 = (b * p.Hkv + kvh) * static_cast<int>(p.P_max) + k0;
       for (int j = 0; j < nT; ++j) {
         const int s = j % STAGES;
         if (j >= STAGES) mbar_wait(bars, &bars.empty[s], ((j / STAGES) - 1) & 1, p.hdr, 20);
         if (bars.failed) break;
         mbar_expect_tx(&bars.full[s], 4 * kKVHalf);
-        const int y = y0 + j * BN;
         const uint32_t kd = sbase + OFF_K + s * 2 * kKVHalf, vd = sbase + OFF_V + s * 2 * kKVHalf;
-        tma_load_2d(kd, &tmap_k, 0, y, &bars.full[s]);
-        tma_load_2d(kd + kKVHalf, &tmap_k, 64, y, &bars.full[s]);
-        tma_load_2d(vd, &tmap_v, 0, y, &bars.full[s]);
-        tma_load_2d(vd + kKVHalf, &tmap_v, 64, y, &bars.full[s]);
+        if (j < nC) {
+          const int z = b * NT + s_base + j * BN;          // candidate slot (rows past NT are masked)
+          tma_load_3d(kd, &tmap_kc, 0, kvh, z, &bars.full[s]);
+          tma_load_3d(kd + kKVHalf, &tmap_kc, 64, kvh, z, &bars.full[s]);
+          tma_load_3d(vd, &tmap_vc, 0, kvh, z, &bars.full[s]);
+          tma_load_3d(vd + kKVHalf, &tmap_vc, 64, kvh, z, &bars.full[s]);
+        } else {
+          const int y = y0 + (j - nC) * BN;
+          tma_load_2d(kd, &tmap_k, 0, y, &bars.full[s]);
+          tma_load_2d(kd + kKVHalf, &tmap_k, 64, y, &bars.full[s]);
+          tma_load_2d(vd, &tmap_v, 0, y, &bars.full[s]);
+          tma_load_2d(vd + kKVHalf, &tmap_v, 64, y, &bars.full[s]);
+        }
       }
     }
   } else {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && nT > 0) {
       constexpr uint32_t idS = idesc_bf16(false, BN), idPV = idesc_bf16(true, DH);
       mbar_wait(bars, &bars.q_full, 0, p.hdr, 30);
       tc_fence_after();
       // S[j&1] = Q K_j^T : M128 N64, eight K16 steps over the head dim
       auto issue_S = [&](int j) {
-        const int s = j % STAGES;
-        const uint32_t kb = sbase + OFF_K + s * 2 * kKVHalf;
+        const uint32_t kb = sbase + OFF_K + (j % STAGES) * 2 * kKVHalf;
 #pragma unroll
         for (int ks = 0; ks < DH / 16; ++ks) {
           const uint64_t a = sw128_desc(sbase + OFF_Q + (ks >> 2) * kQHalf + (ks & 3) * 32, 16, 1024);
@@ -446,6 +514,78 @@ k_attn_prefix_tc(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       }
     }
   }
+
+  // ---- merge the S splits across the cluster through distributed shared memory
+  __syncwarp();
+  cluster_sync();                                   // every CTA's O, m, l are staged
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // blk_len (which rows exist) is final
+  const int rpc = (BM + S - 1) / S;                 // rows merged by each CTA of the cluster
+  const int rb = split * rpc, nr = max(0, min(BM, rb + rpc) - rb);
+  // scratch after the staged m, l: per (row, split) max and sum, then weights; per-row presence
+  float* mm = ml_s + 2 * BM;                        // [nr][S]
+  float* ll = mm + kMergeItems;                     // [nr][S]
+  float* fac = ll + kMergeItems;                    // [nr][S]: exp2(m_c - M) / L
+  int* live = reinterpret_cast<int*>(fac + kMergeItems);   // [nr]
+  if (tid < nr * S) {                               // (a) gather every split's max and sum of these rows
+    const int i = tid / S, c = tid % S;
+    mm[tid] = ld_peer_f32(map_peer(smem_u32(ml_s + rb + i), c));
+    ll[tid] = ld_peer_f32(map_peer(smem_u32(ml_s + BM + rb + i), c));
+  }
+  if (tid < nr) {                                   // presence of the row's token
+    const int gr = r0 + rb + tid;
+    int ok = 0;
+    if (gr < rows_total) {
+      const int tt = gr / G;
+      ok = (tt % p.Dmax) < p.blk_len[b * p.NB + tt / p.Dmax];
+    }
+    live[tid] = ok;
+  }
+  __syncthreads();
+  if (tid < nr) {                                   // (b) merged max, sum and per-split weights
+    float M = -INFINITY;
+    for (int c = 0; c < S; ++c) M = fmaxf(M, mm[tid * S + c]);
+    float L = 0.f;
+    for (int c = 0; c < S; ++c) {
+      const float mc = mm[tid * S + c];
+      const float f = mc > -INFINITY ? ex2_approx(mc - M) : 0.f;
+      fac[tid * S + c] = f;
+      L = fmaf(ll[tid * S + c], f, L);
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    for (int c = 0; c < S; ++c) fac[tid * S + c] *= inv;
+    if (!(L > 0.f)) live[tid] = 0;
+  }
+  __syncthreads();
+  // (c) one float4 of one row per item; a warp covers one row, its S peer loads in flight together
+  for (int it = tid; it < nr * (DH / 4); it += kThreads) {
+    const int i = it / (DH / 4), q4 = it % (DH / 4);
+    if (!live[i]) continue;
+    const uint32_t src = smem_u32(ostage + (rb + i) * kOStride + q4 * 4);
+    float4 o[kMaxSplit];
+#pragma unroll
+    for (int c = 0; c < kMaxSplit; ++c)
+      if (c < S) o[c] = ld_peer_f32x4(map_peer(src, c));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int c = 0; c < kMaxSplit; ++c)
+      if (c < S) {
+        const float f = fac[i * S + c];
+        acc.x = fmaf(f, o[c].x, acc.x);
+        acc.y = fmaf(f, o[c].y, acc.y);
+        acc.z = fmaf(f, o[c].z, acc.z);
+        acc.w = fmaf(f, o[c].w, acc.w);
+      }
+    const int gr = r0 + rb + i;
+    const int tt = gr / G, hh = kvh * G + gr % G;
+    const int64_t o_off = ((static_cast<int64_t>(b) * NT + tt) * p.Hq + hh) * DH + q4 * 4;
+    if (p.out_f32) {
+      *reinterpret_cast<float4*>(static_cast<float*>(p.out) + o_off) = acc;
+    } else {
+      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + o_off) =
+          make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
+    }
+  }
+  cluster_sync();                                   // peers are done reading this CTA's staging
 
   // teardown: every role is done with TMEM
   tc_fence_before();
@@ -486,22 +626,63 @@ static bool make_kv_map(CUtensorMap* map, const void* base, uint64_t rows) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// splits: minimise (waves of CTAs) x (key tiles per split)
-static void choose_split(const ssd_attn_args* a, int mtiles, int* S_out, int* chunk_out) {
-  const long long per_split = static_cast<long long>(a->B) * a->Hkv * mtiles;
-  const long long nkt = a->P_max > 0 ? (a->P_max + BN - 1) / BN : 1;
-  int sms = 152;
+// candidate K or V [B*NT][Hkv][dh] as a 3-D tensor (dh, kv head, slot): a box of
+// 64 slots of one kv head lands as a [64][64] tile like a prefix tile
+static bool make_cand_map(CUtensorMap* map, const void* base, uint64_t slots, int Hkv) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(DH), static_cast<cuuint64_t>(Hkv), slots};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(DH) * 2, static_cast<cuuint64_t>(Hkv) * DH * 2};
+  const cuuint32_t box[3] = {64, 1, BN};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// How many clusters of S CTAs can be resident at once (0 if the query fails).
+static int max_active_clusters(int S) {
+  static int cache[kMaxSplit + 1][64];
+  static bool done[kMaxSplit + 1][64];
+  static std::mutex mu;
   int dev = 0;
-  if (cudaGetDevice(&dev) == cudaSuccess) {
-    int v = 0;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) sms = v;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!done[S][dev]) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(S), 1, 1);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k_attn_tc, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    cache[S][dev] = n;
+    done[S][dev] = true;
   }
+  return cache[S][dev];
+}
+
+// splits (cluster size <= 8): minimise (waves of clusters) x (key tiles per split + fixed cost)
+static void choose_split(const ssd_attn_args* a, int mtiles, int* S_out, int* chunk_out) {
+  const long long groups = static_cast<long long>(a->B) * a->Hkv * mtiles;   // clusters in the grid
+  const long long nkt = a->P_max > 0 ? (a->P_max + BN - 1) / BN : 1;
   long long best_cost = -1;
   int best_S = 1;
-  for (int S = 1; S <= 64 && S <= nkt; ++S) {
+  for (int S = 1; S <= kMaxSplit && S <= nkt; ++S) {
+    const int active = max_active_clusters(S);
+    if (active <= 0) continue;
     const long long tiles = (nkt + S - 1) / S;
-    const long long waves = (per_split * S + sms - 1) / sms;
-    const long long cost = waves * tiles * 8 + S;   // small penalty per split for the combine
+    const long long waves = (groups + active - 1) / active;
+    const long long cost = waves * (tiles + 3) * 16 + S;   // +3 tiles: prologue, candidate tile, merge
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best_S = S;
@@ -509,7 +690,7 @@ static void choose_split(const ssd_attn_args* a, int mtiles, int* S_out, int* ch
   }
   const long long tiles = (nkt + best_S - 1) / best_S;
   *chunk_out = static_cast<int>(tiles * BN);
-  *S_out = static_cast<int>((nkt + tiles - 1) / tiles);
+  *S_out = best_S;
 }
 
 }  // namespace tc
@@ -523,7 +704,10 @@ bool attn_tc_applies(const ssd_attn_args* a) {
   if (tc_disabled_by_env()) return false;
   if (a->dtype != SSD_BF16 || a->dh != tc::DH || a->P_max < 1) return false;
   if (!aligned(a->k_cache, 16) || !aligned(a->v_cache, 16) || !aligned(a->q, 16)) return false;
+  if (!aligned(a->k_cand, 16) || !aligned(a->v_cand, 16) || !aligned(a->out, 16)) return false;
   if (static_cast<long long>(a->B) * a->Hkv * a->P_max >= (1LL << 31)) return false;
+  if (static_cast<long long>(a->B) * a->NB * a->Dmax >= (1LL << 31)) return false;
+  if (a->B * a->Hkv > 65535) return false;
   int dev = 0, major = 0, minor = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
@@ -531,42 +715,27 @@ bool attn_tc_applies(const ssd_attn_args* a) {
   return major == 10 && minor == 3 && tc::encode_fn() != nullptr;
 }
 
-struct TcLayout {
-  int mtiles, S, chunk;
-  size_t ml_off, o_off, total;
-};
-
-static TcLayout tc_layout(const ssd_attn_args* a) {
-  TcLayout L{};
-  const int NT = a->NB * a->Dmax;
-  const int G = a->Hq / a->Hkv;
-  L.mtiles = (NT * G + tc::BM - 1) / tc::BM;
-  tc::choose_split(a, L.mtiles, &L.S, &L.chunk);
-  const size_t R = static_cast<size_t>(a->B) * NT * a->Hq;
-  L.ml_off = sizeof(WsHeader);
-  L.o_off = round_up(L.ml_off + R * L.S * 2 * sizeof(float), 256);
-  L.total = round_up(L.o_off + R * L.S * tc::DH * sizeof(float), 256);
-  return L;
-}
-
-size_t attn_tc_workspace_size(const ssd_attn_args* a) {
-  if (a->dtype != SSD_BF16 || a->dh != tc::DH || a->P_max < 1) return 0;
-  return tc_layout(a).total;
-}
+size_t attn_tc_workspace_size(const ssd_attn_args*) { return sizeof(WsHeader); }
 
 int attn_tc_launch(const ssd_attn_args* a, void* ws, cudaStream_t s) {
-  const TcLayout L = tc_layout(a);
-  CUtensorMap mk, mv;
-  const uint64_t rows = static_cast<uint64_t>(a->B) * a->Hkv * a->P_max;
-  if (!tc::make_kv_map(&mk, a->k_cache, rows) || !tc::make_kv_map(&mv, a->v_cache, rows)) return SSD_ERR_CUDA;
-
+  const int NT = a->NB * a->Dmax;
+  const int G = a->Hq / a->Hkv;
+  const int mtiles = (NT * G + tc::BM - 1) / tc::BM;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(tc::k_attn_prefix_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(tc::k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(tc::kSmemBytes));
   });
   if (attr_err != cudaSuccess) return SSD_ERR_CUDA;
+  int S = 1, chunk = tc::BN;
+  tc::choose_split(a, mtiles, &S, &chunk);
+  CUtensorMap mk, mv, mkc, mvc;
+  const uint64_t rows = static_cast<uint64_t>(a->B) * a->Hkv * a->P_max;
+  const uint64_t slots = static_cast<uint64_t>(a->B) * NT;
+  if (!tc::make_kv_map(&mk, a->k_cache, rows) || !tc::make_kv_map(&mv, a->v_cache, rows) ||
+      !tc::make_cand_map(&mkc, a->k_cand, slots, a->Hkv) || !tc::make_cand_map(&mvc, a->v_cand, slots, a->Hkv))
+    return SSD_ERR_CUDA;
 
   AttnParams p{};
   p.q = a->q; p.k_cache = a->k_cache; p.v_cache = a->v_cache; p.k_cand = a->k_cand; p.v_cand = a->v_cand;
@@ -574,23 +743,31 @@ int attn_tc_launch(const ssd_attn_args* a, void* ws, cudaStream_t s) {
   p.B = a->B; p.NB = a->NB; p.Dmax = a->Dmax; p.Hq = a->Hq; p.Hkv = a->Hkv; p.P_max = a->P_max;
   const float scale = a->scale != 0.f ? a->scale : 1.f / sqrtf(static_cast<float>(a->dh));
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.S = L.S;
-  p.chunk = L.chunk;
-  char* base = static_cast<char*>(ws);
-  p.hdr = reinterpret_cast<WsHeader*>(base);
-  p.ws_ml = reinterpret_cast<float*>(base + L.ml_off);
-  p.ws_o = reinterpret_cast<float*>(base + L.o_off);
+  p.S = S;
+  p.chunk = chunk;
+  p.out_f32 = (a->out_dtype == SSD_F32) ? 1 : 0;
+  p.hdr = reinterpret_cast<WsHeader*>(ws);
 
-  dim3 grid(static_cast<unsigned>(a->B * a->Hkv * L.mtiles), static_cast<unsigned>(L.S));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(S), static_cast<unsigned>(mtiles), static_cast<unsigned>(a->B * a->Hkv));
+  cfg.blockDim = dim3(tc::kThreads);
+  cfg.dynamicSmemBytes = tc::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
   {
-    KernelTimer timer(SSD_KERNEL_ATTN_PREFIX, s);
-    tc::k_attn_prefix_tc<<<grid, tc::kThreads, tc::kSmemBytes, s>>>(mk, mv, p, L.mtiles);
+    KernelTimer timer(SSD_KERNEL_VERIFY_ATTN, s);
+    if (cudaLaunchKernelEx(&cfg, tc::k_attn_tc, mk, mv, mkc, mvc, p) != cudaSuccess) return SSD_ERR_CUDA;
   }
-  int rc = check_launch();
-  if (rc != SSD_OK) return rc;
-  rc = attn_combine_launch(p, a->dtype, a->dh, s);
-  count_launch(2);
-  return rc;
+  count_launch(1);
+  return check_launch();
 }
 
 }  // namespace ssd
