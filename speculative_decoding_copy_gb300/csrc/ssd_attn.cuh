@@ -19,6 +19,7 @@ struct AttnParams {
   float scale_log2;      // softmax scale times log2(e): scores are kept in log2 units
   int out_f32;           // 1: fp32 output whatever the input type
   int S, chunk;          // KV splits and keys per split
+  int chunk0;            // keys of split 0 (tensor-core path: it also takes the own-block tiles)
   WsHeader* hdr;
   float* ws_ml;          // [rows][S][2]  running max and sum per split
   float* ws_o;           // [rows][S][dh] un-normalised output per split

@@ -7,29 +7,32 @@
 // dense product with each key tile. A CTA owns 128 packed rows (the M of the
 // MMA) and one split of the prefix; the S CTAs of a row tile form a thread-block
 // cluster, rank 0 also takes the own-block keys as masked tiles, and the splits
-// are merged on chip through distributed shared memory: no partial results go
-// to HBM and no second kernel runs.
+// are merged on chip through distributed shared memory.
 //
-// Per CTA (192 threads, one CTA per SM):
-//   warps 0-3  one thread per packed row: stage Q, online softmax from the S
-//              row in TMEM (tcgen05.ld) with the row's key mask (a contiguous
-//              range per tile), O rescale in TMEM, P as bf16 into shared
-//              memory; after the loop the O row, max and sum are staged in
-//              shared memory for the cluster merge;
-//   warp 4     TMA producer: K and V tiles of 64 keys (two 64-wide halves of
-//              the head dim, 128-byte swizzle) into a 4-stage ring, from the
-//              prefix cache (2-D map) or the candidate keys (3-D map);
-//   warp 5     TMEM allocation and the single MMA-issuing thread:
-//              S = Q K^T (M128 N64, K16 x 8) into one of two TMEM buffers and
-//              O += P V (M128 N128, K16 x 4), kind::f16 with bf16 operands and
-//              fp32 accumulators in TMEM. S of tile j+1 is issued before P V of
-//              tile j so the tensor core works while the rows run the softmax;
-//              P is double-buffered in shared memory.
-// Merge: each CTA of the cluster normalises 128/S rows, reading every split's
-// O, max and sum from its peers' shared memory, and writes the bf16 output of
-// the tokens that exist. The kernel may be launched before the retrieval that
-// decides which tokens exist has finished (programmatic dependent launch): it
-// reads the block lengths only after griddepcontrol.wait, just before writing.
+// Per CTA (192 threads, one CTA per SM, all 512 TMEM columns):
+//   warps 0-3  one thread per packed row: online softmax of a 128-key tile read
+//              from TMEM (tcgen05.ld), masked to a contiguous key range; O is
+//              rescaled in TMEM when the row max grows; P goes back to TMEM as
+//              bf16 pairs (tcgen05.st), where the P V product reads it as its
+//              A operand;
+//   warp 4     TMEM allocation, then the TMA producer: Q (a 4-D map lays the G
+//              heads of 128/G tokens out as 128 rows) and a 3-stage ring of K
+//              and V tiles of 128 keys (two 64-wide halves of the head dim,
+//              128-byte swizzle), from the prefix cache (2-D map) or the
+//              candidate keys (3-D map); after its last load it waits for the
+//              retrieval (griddepcontrol.wait) and fetches which of the rows
+//              this CTA merges belong to tokens that exist;
+//   warp 5     the single MMA-issuing thread: S = Q K^T (M128 N128, eight K16
+//              steps, both operands in shared memory) into one of two TMEM
+//              buffers, two tiles ahead of the softmax, and O += P V (M128
+//              N128, eight K16 steps, A from TMEM, V MN-major in shared memory).
+// TMEM columns: S buffers 0-127 and 128-255, O 256-383, P buffers 384-447 and
+// 448-511.
+// Merge: after a cluster barrier (every CTA is past its main loop, so the K/V
+// rings are idle) each CTA stores every row's un-normalised O, max and sum
+// into the ring of the CTA that owns the row (remote shared-memory stores);
+// after a second barrier each CTA combines its 128/S rows locally and writes
+// the output of the tokens that exist.
 // Every mbarrier wait is bounded (about 2^32 clocks); on expiry the CTA
 // records SSD_ERR_TIMEOUT in the workspace header, skips the remaining waits,
 // frees its TMEM and exits through the cluster barriers.
@@ -45,28 +48,33 @@ namespace tc {
 
 constexpr int DH = 128;
 constexpr int BM = 128;                   // packed rows per CTA
-constexpr int BN = 64;                    // keys per tile
-constexpr int STAGES = 4;                 // K/V ring depth
+constexpr int BN = 128;                   // keys per tile
+constexpr int STAGES = 3;                 // K/V ring depth
 constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 256;       // S buffers: cols 0-63 and 64-127, O: cols 128-255
-constexpr uint32_t kQHalf = BM * 128;     // 128 rows x 64 bf16 (one 128-byte-swizzled half): 16 KB
-constexpr uint32_t kKVHalf = BN * 128;    // 64 keys x 64 bf16: 8 KB
-constexpr uint32_t kPBuf = BM * 128;      // 128 rows x 64 keys bf16: 16 KB
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t TM_S = 0;              // two S buffers of BN columns
+constexpr uint32_t TM_O = 2 * BN;         // O: DH columns
+constexpr uint32_t TM_P = TM_O + DH;      // two P buffers of BN/2 columns (bf16 pairs)
+static_assert(TM_P + BN <= kTmemCols, "TMEM budget");
+constexpr uint32_t kHalf = 128 * 128;     // 128 rows x 64 bf16, one 128-byte-swizzled half: 16 KB
+constexpr uint32_t kStage = 4 * kHalf;    // K and V tiles, two halves each: 64 KB
 constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_K = OFF_Q + 2 * kQHalf;
-constexpr uint32_t OFF_V = OFF_K + STAGES * 2 * kKVHalf;
-constexpr uint32_t OFF_P = OFF_V + STAGES * 2 * kKVHalf;
-constexpr uint32_t OFF_BAR = OFF_P + 2 * kPBuf;
-constexpr uint32_t kSmemBytes = OFF_BAR + 256 + 1024;   // + slack to align the base to 1024
+constexpr uint32_t OFF_RING = OFF_Q + 2 * kHalf;
+constexpr uint32_t OFF_BAR = OFF_RING + STAGES * kStage;
+constexpr uint32_t kBarBytes = 1024;
+constexpr uint32_t kSmemBytes = OFF_BAR + kBarBytes + 1024;   // + slack to align the base to 1024
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 constexpr unsigned long long kWaitClocks = 1ull << 32;
 struct Bars {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full_k[STAGES], full_v[STAGES], empty[STAGES];
   uint64_t q_full;
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
+  uint64_t recv_full;                     // every split's rows owned by this CTA have arrived
   uint32_t tmem_base;
   int failed;
+  int live[BM];                           // merged row belongs to a token that exists
 };
+static_assert(sizeof(Bars) <= kBarBytes, "barrier block");
 
 // ------------------------------------------------------------------ PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -100,6 +108,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Bounded wait; false once this CTA has given up (then every later wait returns at once).
 __device__ __forceinline__ bool mbar_wait(Bars& bars, uint64_t* bar, uint32_t parity, WsHeader* hdr, int where) {
+  if (mbar_try_wait(bar, parity)) return true;      // the common case: one probe, no bookkeeping
   volatile int* failed = &bars.failed;
   if (*failed) return false;
   const unsigned long long t0 = clock64();
@@ -130,6 +139,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, int w,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // whole-cluster barrier: arrive (release) + wait (acquire); every thread of every CTA
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
@@ -153,6 +171,14 @@ __device__ __forceinline__ float4 ld_peer_f32x4(uint32_t addr) {
   asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                : "r"(addr) : "memory");
   return v;
+}
+
+// shared memory of this CTA -> shared memory of a CTA of the cluster, completing on that CTA's mbarrier
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "r"(src), "r"(bytes), "r"(bar)
+      : "memory");
 }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -195,6 +221,16 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b
       : "memory");
 }
 
+// the same with the A operand in TMEM (M rows on the lanes, K/2 columns of bf16 pairs)
+__device__ __forceinline__ void mma_bf16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
@@ -227,10 +263,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-
 // two fp32 -> packed bf16x2 (round to nearest even), low half = first
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
@@ -238,29 +270,18 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return r;
 }
 
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-}
-
-// offset of 16-byte chunk c (0..7) of row r inside a 128-byte-swizzled half
-__device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t c) { return r * 128u + ((c ^ (r & 7u)) << 4); }
-
 // ------------------------------------------------------------------ kernel
 constexpr int kMaxSplit = 8;              // cluster size limit (portable)
-constexpr int kOStride = 132;             // fp32 per staged O row (padding against bank conflicts)
-constexpr int kMergeItems = BM + kMaxSplit;   // bound on (rows merged by one CTA) x S
+constexpr int kRowF = 132;                // fp32 per merged row: O (128), max, sum, padding to 16 bytes
+constexpr int kMergeItems = BM + kMaxSplit;   // bound on (rows owned by one CTA) x S
+static_assert((BM + kMergeItems) * kRowF * 4 + BM * kMaxSplit * 4 <= STAGES * kStage, "merge buffers fit in the ring");
 
 // grid (S, row tiles, B*Hkv), cluster (S, 1, 1): the S CTAs of one row tile split
 // the prefix; cluster rank 0 also takes the own-block (candidate) keys.
 __global__ void __launch_bounds__(kThreads, 1)
-k_attn_tc(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-          const __grid_constant__ CUtensorMap tmap_kc, const __grid_constant__ CUtensorMap tmap_vc, AttnParams p) {
+k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+          const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_kc,
+          const __grid_constant__ CUtensorMap tmap_vc, AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -276,8 +297,9 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CU
   const int rows_total = NT * G;
   const int r0 = mt * BM;
   const int P = p.prefix_len[b];
-  const int k0 = split * p.chunk;
-  const int k1 = min(P, k0 + p.chunk);
+  // split 0 also takes the own-block tiles, so its share of the prefix is shorter
+  const int k0 = split == 0 ? 0 : p.chunk0 + (split - 1) * p.chunk;
+  const int k1 = min(P, k0 + (split == 0 ? p.chunk0 : p.chunk));
   const int nP = k1 > k0 ? (k1 - k0 + BN - 1) / BN : 0;
   // candidate slots of this row tile: from the start of its first token's block to its last token
   const int t_first = r0 / G;
@@ -285,21 +307,19 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CU
   const int s_base = (t_first / p.Dmax) * p.Dmax;
   const int nC = (split == 0 && t_first < NT) ? (t_last + 1 - s_base + BN - 1) / BN : 0;
   const int nT = nC + nP;
-
-  // this thread's packed row: token t, q-head h, allowed own-block slots [c_lo, t]
-  const int r = r0 + tid;
-  const bool row_ok = tid < BM && r < rows_total;
-  const int t = row_ok ? r / G : 0;
-  const int h = row_ok ? kvh * G + r % G : 0;
-  const int c_lo = (t / p.Dmax) * p.Dmax;
+  // rows of this tile merged by this CTA: [rb, rb + nr)
+  const int rpc = (BM + S - 1) / S;
+  const int rb = split * rpc, nr = max(0, min(BM, rb + rpc) - rb);
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&bars.full[s], 1);
+      mbar_init(&bars.full_k[s], 1);
+      mbar_init(&bars.full_v[s], 1);
       mbar_init(&bars.empty[s], 1);
     }
-    mbar_init(&bars.q_full, BM);
+    mbar_init(&bars.q_full, 1);
+    mbar_init(&bars.recv_full, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.s_full[i], 1);
       mbar_init(&bars.s_free[i], BM);
@@ -309,7 +329,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CU
     bars.failed = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 5) {
+  if (warp == 4) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&bars.tmem_base)),
                  "r"(kTmemCols)
                  : "memory");
@@ -319,262 +339,264 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CU
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
-  const uint32_t tmem_O = tmem + 128;
-  float* ostage = reinterpret_cast<float*>(smem + OFF_K);          // [128][kOStride] after the main loop
-  float* ml_s = reinterpret_cast<float*>(smem + OFF_P);            // [2][128] after the main loop
+  const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  float m = -INFINITY, l = 0.f;            // softmax rows: reference max (log2 units) and sum
 
   if (warp < 4) {
     // ---------------------------------------------------------- softmax rows
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    float m = -INFINITY, l = 0.f;        // reference max (log2 units) and sum
-    if (nT > 0) {
-      {
-        // stage Q row `tid` (zeros past the last packed row), 128-byte swizzle
-        const uint4* q4 = row_ok ? reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
-                                                                   ((static_cast<int64_t>(b) * NT + t) * p.Hq + h) * DH)
-                                 : nullptr;
-        uint4 qv[16];
+    // this thread's packed row: token t, allowed own-block slots [c_lo, t]
+    const int r = r0 + tid;
+    const bool row_ok = r < rows_total;
+    const int t = row_ok ? r / G : 0;
+    const int c_lo = (t / p.Dmax) * p.Dmax;
+    const float sl2 = p.scale_log2;
+    for (int j = 0; j < nT; ++j) {
+      const int sb = j & 1;
+      mbar_wait(bars, &bars.s_full[sb], (j >> 1) & 1, p.hdr, 10);
+      tc_fence_after();
+      uint32_t sreg[BN];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) qv[c] = q4 ? __ldg(q4 + c) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          st_shared_v4(sbase + OFF_Q + (c >> 3) * kQHalf + sw128_off(tid, c & 7), qv[c].x, qv[c].y, qv[c].z,
-                       qv[c].w);
-        fence_async_smem();
-        mbar_arrive(&bars.q_full);
+      for (int q = 0; q < BN / 32; ++q) tmem_ld32(tmem + TM_S + sb * BN + lane_off + q * 32, sreg + q * 32);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&bars.s_free[sb]);
+      // valid columns: a contiguous range [v_lo, v_hi) of this tile
+      int v_lo, v_hi;
+      if (j < nC) {                                   // own-block keys: slots c_lo .. t
+        const int s0 = s_base + j * BN;
+        v_lo = row_ok ? c_lo - s0 : BN;
+        v_hi = row_ok ? t + 1 - s0 : 0;
+      } else {                                        // prefix keys below k1
+        v_lo = 0;
+        v_hi = k1 - (k0 + (j - nC) * BN);
       }
-      const float sl2 = p.scale_log2;
-      for (int j = 0; j < nT; ++j) {
-        const int sb = j & 1;
-        mbar_wait(bars, &bars.s_full[sb], (j >> 1) & 1, p.hdr, 10);
+      if (v_lo > 0 || v_hi < BN) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (c < v_lo || c >= v_hi) sreg[c] = __float_as_uint(-INFINITY);
+      }
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < BN; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], __uint_as_float(sreg[c]));
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      // reference max only moves when the row max grows by more than 2^8
+      const float m_new = fmaxf(m, mx * sl2);
+      const bool need = m_new > m + 8.f;
+      const float mref = need ? m_new : m;
+      const float alpha = need ? ex2_approx(m - m_new) : 1.f;
+      uint32_t pk[BN / 2];
+      float rs[4] = {0.f, 0.f, 0.f, 0.f};
+      if (mref > -INFINITY) {
+#pragma unroll
+        for (int c = 0; c < BN; c += 2) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sreg[c]), sl2, -mref));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sreg[c + 1]), sl2, -mref));
+          const uint32_t w = pack_bf16(p0, p1);
+          pk[c / 2] = w;
+          // sum the rounded values the MMA uses, so numerator and denominator agree
+          rs[(c >> 1) & 1] += __uint_as_float(w << 16);
+          rs[2 + ((c >> 1) & 1)] += __uint_as_float(w & 0xffff0000u);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < BN / 2; ++c) pk[c] = 0u;   // no allowed key yet in this row
+      }
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        // O holds the sum up to tile j-1: wait for its last MMA, then rescale
+        mbar_wait(bars, &bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, p.hdr, 11);
         tc_fence_after();
-        uint32_t sreg[BN];
+        uint32_t o[32];
 #pragma unroll
-        for (int q = 0; q < BN / 32; ++q) tmem_ld32(tmem + sb * BN + lane_off + q * 32, sreg + q * 32);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&bars.s_free[sb]);
-        // valid columns: a contiguous range [v_lo, v_hi) of this tile
-        int v_lo, v_hi;
-        if (j < nC) {                                   // own-block keys: slots c_lo .. t
-          const int s0 = s_base + j * BN;
-          v_lo = row_ok ? c_lo - s0 : BN;
-          v_hi = row_ok ? t + 1 - s0 : 0;
-        } else {                                        // prefix keys below k1
-          v_lo = 0;
-          v_hi = k1 - (k0 + (j - nC) * BN);
+        for (int q = 0; q < DH / 32; ++q) {
+          tmem_ld32(tmem + TM_O + lane_off + q * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(tmem + TM_O + lane_off + q * 32, o);
         }
-        if (v_lo > 0 || v_hi < BN) {
-#pragma unroll
-          for (int c = 0; c < BN; ++c)
-            if (c < v_lo || c >= v_hi) sreg[c] = __float_as_uint(-INFINITY);
-        }
-        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int c = 0; c < BN; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], __uint_as_float(sreg[c]));
-        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-        // reference max only moves when the row max grows by more than 2^8
-        const float m_new = fmaxf(m, mx * sl2);
-        const bool need = m_new > m + 8.f;
-        const float mref = need ? m_new : m;
-        const float alpha = need ? ex2_approx(m - m_new) : 1.f;
-        uint32_t pk[BN / 2];
-        float rs[4] = {0.f, 0.f, 0.f, 0.f};
-        if (mref > -INFINITY) {
-#pragma unroll
-          for (int c = 0; c < BN; c += 2) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(sreg[c]), sl2, -mref));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(sreg[c + 1]), sl2, -mref));
-            const uint32_t w = pack_bf16(p0, p1);
-            pk[c / 2] = w;
-            // sum the rounded values the MMA uses, so numerator and denominator agree
-            rs[(c >> 1) & 1] += __uint_as_float(w << 16);
-            rs[2 + ((c >> 1) & 1)] += __uint_as_float(w & 0xffff0000u);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < BN / 2; ++c) pk[c] = 0u;   // no allowed key yet in this row
-        }
-        if (j > 0 && __any_sync(0xffffffffu, need)) {
-          // O holds the sum up to tile j-1: wait for its last MMA, then rescale
-          mbar_wait(bars, &bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, p.hdr, 11);
-          tc_fence_after();
-          uint32_t o[32];
-#pragma unroll
-          for (int q = 0; q < DH / 32; ++q) {
-            tmem_ld32(tmem_O + lane_off + q * 32, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(tmem_O + lane_off + q * 32, o);
-          }
-          tmem_wait_st();
-        }
-        l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
-        m = mref;
-        // P buffer sb was last read by the MMA of tile j-2
-        if (j >= 2) mbar_wait(bars, &bars.pv_done[sb], ((j - 2) >> 1) & 1, p.hdr, 12);
-#pragma unroll
-        for (int c = 0; c < BN / 8; ++c)
-          st_shared_v4(sbase + OFF_P + sb * kPBuf + sw128_off(tid, c), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
-                       pk[4 * c + 3]);
-        fence_async_smem();
-        tc_fence_before();
-        mbar_arrive(&bars.p_full[sb]);
       }
+      l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+      m = mref;
+      // P buffer sb was last read by the P V product of tile j-2
+      if (j >= 2) {
+        mbar_wait(bars, &bars.pv_done[sb], ((j - 2) >> 1) & 1, p.hdr, 12);
+        tc_fence_after();
+      }
+      tmem_st32(tmem + TM_P + sb * (BN / 2) + lane_off, pk);
+      tmem_st32(tmem + TM_P + sb * (BN / 2) + lane_off + 32, pk + 32);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars.p_full[sb]);
+    }
+    if (nT > 0) {
       mbar_wait(bars, &bars.pv_done[(nT - 1) & 1], ((nT - 1) >> 1) & 1, p.hdr, 13);
       tc_fence_after();
     }
-    // stage this CTA's un-normalised O row, reference max and sum for the cluster merge
-    float* orow = ostage + tid * kOStride;
-#pragma unroll
-    for (int q = 0; q < DH / 32; ++q) {
-      uint32_t o[32];
-      if (nT > 0) {
-        tmem_ld32(tmem_O + lane_off + q * 32, o);
-        tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = 0u;
-      }
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        reinterpret_cast<float4*>(orow + q * 32)[e] =
-            make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]), __uint_as_float(o[4 * e + 2]),
-                        __uint_as_float(o[4 * e + 3]));
-    }
-    ml_s[tid] = m;
-    ml_s[BM + tid] = l;
   } else if (warp == 4) {
     // ---------------------------------------------------------- TMA producer
     if (lane == 0 && nT > 0) {
+      mbar_expect_tx(&bars.q_full, 2 * kHalf);
+      const int qz = b * NT + t_first;                     // rows past the sequence are masked or zero
+      tma_load_4d(sbase + OFF_Q, &tmap_q, 0, 0, kvh, qz, &bars.q_full);
+      tma_load_4d(sbase + OFF_Q + kHalf, &tmap_q, 64, 0, kvh, qz, &bars.q_full);
       const int y0 = (b * p.Hkv + kvh) * static_cast<int>(p.P_max) + k0;
       for (int j = 0; j < nT; ++j) {
         const int s = j % STAGES;
         if (j >= STAGES) mbar_wait(bars, &bars.empty[s], ((j / STAGES) - 1) & 1, p.hdr, 20);
         if (bars.failed) break;
-        mbar_expect_tx(&bars.full[s], 4 * kKVHalf);
-        const uint32_t kd = sbase + OFF_K + s * 2 * kKVHalf, vd = sbase + OFF_V + s * 2 * kKVHalf;
+        const uint32_t kd = sbase + OFF_RING + s * kStage, vd = kd + 2 * kHalf;
+        mbar_expect_tx(&bars.full_k[s], 2 * kHalf);
         if (j < nC) {
           const int z = b * NT + s_base + j * BN;          // candidate slot (rows past NT are masked)
-          tma_load_3d(kd, &tmap_kc, 0, kvh, z, &bars.full[s]);
-          tma_load_3d(kd + kKVHalf, &tmap_kc, 64, kvh, z, &bars.full[s]);
-          tma_load_3d(vd, &tmap_vc, 0, kvh, z, &bars.full[s]);
-          tma_load_3d(vd + kKVHalf, &tmap_vc, 64, kvh, z, &bars.full[s]);
+          tma_load_3d(kd, &tmap_kc, 0, kvh, z, &bars.full_k[s]);
+          tma_load_3d(kd + kHalf, &tmap_kc, 64, kvh, z, &bars.full_k[s]);
+          mbar_expect_tx(&bars.full_v[s], 2 * kHalf);
+          tma_load_3d(vd, &tmap_vc, 0, kvh, z, &bars.full_v[s]);
+          tma_load_3d(vd + kHalf, &tmap_vc, 64, kvh, z, &bars.full_v[s]);
         } else {
           const int y = y0 + (j - nC) * BN;
-          tma_load_2d(kd, &tmap_k, 0, y, &bars.full[s]);
-          tma_load_2d(kd + kKVHalf, &tmap_k, 64, y, &bars.full[s]);
-          tma_load_2d(vd, &tmap_v, 0, y, &bars.full[s]);
-          tma_load_2d(vd + kKVHalf, &tmap_v, 64, y, &bars.full[s]);
+          tma_load_2d(kd, &tmap_k, 0, y, &bars.full_k[s]);
+          tma_load_2d(kd + kHalf, &tmap_k, 64, y, &bars.full_k[s]);
+          mbar_expect_tx(&bars.full_v[s], 2 * kHalf);
+          tma_load_2d(vd, &tmap_v, 0, y, &bars.full_v[s]);
+          tma_load_2d(vd + kHalf, &tmap_v, 64, y, &bars.full_v[s]);
         }
       }
+    }
+    __syncwarp();
+    // which merged rows belong to tokens that exist: blk_len comes from the retrieval
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (int i = lane; i < nr; i += 32) {
+      const int gr = r0 + rb + i;
+      int ok = 0;
+      if (gr < rows_total) {
+        const int tt = gr / G;
+        ok = (tt % p.Dmax) < p.blk_len[b * p.NB + tt / p.Dmax];
+      }
+      bars.live[i] = ok;
     }
   } else {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0 && nT > 0) {
       constexpr uint32_t idS = idesc_bf16(false, BN), idPV = idesc_bf16(true, DH);
-      mbar_wait(bars, &bars.q_full, 0, p.hdr, 30);
-      tc_fence_after();
-      // S[j&1] = Q K_j^T : M128 N64, eight K16 steps over the head dim
-      auto issue_S = [&](int j) {
-        const uint32_t kb = sbase + OFF_K + (j % STAGES) * 2 * kKVHalf;
+      // S[jj & 1] = Q K_jj^T : M128 N128, eight K16 steps over the head dim
+      auto issue_S = [&](int jj) {
+        const int s = jj % STAGES;
+        mbar_wait(bars, &bars.full_k[s], (jj / STAGES) & 1, p.hdr, 31);
+        tc_fence_after();
+        const uint32_t kb = sbase + OFF_RING + s * kStage;
 #pragma unroll
         for (int ks = 0; ks < DH / 16; ++ks) {
-          const uint64_t a = sw128_desc(sbase + OFF_Q + (ks >> 2) * kQHalf + (ks & 3) * 32, 16, 1024);
-          const uint64_t bd = sw128_desc(kb + (ks >> 2) * kKVHalf + (ks & 3) * 32, 16, 1024);
-          mma_bf16(tmem + (j & 1) * BN, a, bd, idS, ks > 0 ? 1u : 0u);
+          const uint64_t a = sw128_desc(sbase + OFF_Q + (ks >> 2) * kHalf + (ks & 3) * 32, 16, 1024);
+          const uint64_t bd = sw128_desc(kb + (ks >> 2) * kHalf + (ks & 3) * 32, 16, 1024);
+          mma_bf16(tmem + TM_S + (jj & 1) * BN, a, bd, idS, ks > 0 ? 1u : 0u);
         }
-        mma_commit(&bars.s_full[j & 1]);
+        mma_commit(&bars.s_full[jj & 1]);
       };
-      mbar_wait(bars, &bars.full[0], 0, p.hdr, 31);
-      tc_fence_after();
+      mbar_wait(bars, &bars.q_full, 0, p.hdr, 30);
       issue_S(0);
+      if (nT > 1) issue_S(1);
       for (int j = 0; j < nT; ++j) {
-        if (j + 1 < nT) {
-          // S of the next tile into the other buffer, once its previous reader is done
-          mbar_wait(bars, &bars.full[(j + 1) % STAGES], ((j + 1) / STAGES) & 1, p.hdr, 32);
-          if (j >= 1) mbar_wait(bars, &bars.s_free[(j + 1) & 1], ((j - 1) >> 1) & 1, p.hdr, 33);
-          tc_fence_after();
-          issue_S(j + 1);
-        }
-        // O += P_j V_j : M128 N128 (head dim), four K16 steps over the tile's keys
+        // O += P_j V_j : M128 N128 (head dim), eight K16 steps over the tile's keys, P from TMEM
+        const int s = j % STAGES;
         mbar_wait(bars, &bars.p_full[j & 1], (j >> 1) & 1, p.hdr, 34);
+        mbar_wait(bars, &bars.full_v[s], (j / STAGES) & 1, p.hdr, 35);
         tc_fence_after();
-        const uint32_t vb = sbase + OFF_V + (j % STAGES) * 2 * kKVHalf;
-        const uint32_t pb = sbase + OFF_P + (j & 1) * kPBuf;
+        const uint32_t vb = sbase + OFF_RING + s * kStage + 2 * kHalf;
+        const uint32_t pa = tmem + TM_P + (j & 1) * (BN / 2);
 #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks) {
-          const uint64_t a = sw128_desc(pb + ks * 32, 16, 1024);
-          const uint64_t bd = sw128_desc(vb + ks * 16 * 128, kKVHalf, 1024);
-          mma_bf16(tmem_O, a, bd, idPV, (j > 0 || ks > 0) ? 1u : 0u);
+          const uint64_t bd = sw128_desc(vb + ks * 16 * 128, kHalf, 1024);
+          mma_bf16_ts(tmem + TM_O, pa + ks * 8, bd, idPV, (j > 0 || ks > 0) ? 1u : 0u);
         }
         mma_commit(&bars.pv_done[j & 1]);
-        mma_commit(&bars.empty[j % STAGES]);
+        mma_commit(&bars.empty[s]);
+        // S of tile j+2 into the buffer the softmax of tile j has read
+        if (j + 2 < nT) {
+          mbar_wait(bars, &bars.s_free[j & 1], (j >> 1) & 1, p.hdr, 33);
+          issue_S(j + 2);
+        }
       }
     }
   }
 
-  // ---- merge the S splits across the cluster through distributed shared memory
-  __syncwarp();
-  cluster_sync();                                   // every CTA's O, m, l are staged
-  asm volatile("griddepcontrol.wait;" ::: "memory");   // blk_len (which rows exist) is final
-  const int rpc = (BM + S - 1) / S;                 // rows merged by each CTA of the cluster
-  const int rb = split * rpc, nr = max(0, min(BM, rb + rpc) - rb);
-  // scratch after the staged m, l: per (row, split) max and sum, then weights; per-row presence
-  float* mm = ml_s + 2 * BM;                        // [nr][S]
-  float* ll = mm + kMergeItems;                     // [nr][S]
-  float* fac = ll + kMergeItems;                    // [nr][S]: exp2(m_c - M) / L
-  int* live = reinterpret_cast<int*>(fac + kMergeItems);   // [nr]
-  if (tid < nr * S) {                               // (a) gather every split's max and sum of these rows
-    const int i = tid / S, c = tid % S;
-    mm[tid] = ld_peer_f32(map_peer(smem_u32(ml_s + rb + i), c));
-    ll[tid] = ld_peer_f32(map_peer(smem_u32(ml_s + BM + rb + i), c));
-  }
-  if (tid < nr) {                                   // presence of the row's token
-    const int gr = r0 + rb + tid;
-    int ok = 0;
-    if (gr < rows_total) {
-      const int tt = gr / G;
-      ok = (tt % p.Dmax) < p.blk_len[b * p.NB + tt / p.Dmax];
+  // ---- merge the S splits of every row in the CTA that owns it
+  // Layout in the (now idle) K/V ring: this CTA's rows as sent [BM][kRowF] (O, then max
+  // and sum), the rows it owns as received [S][rpc][kRowF], then their weights [rpc][S].
+  float* stage = reinterpret_cast<float*>(smem + OFF_RING);
+  float* recv = stage + BM * kRowF;
+  float* fac = recv + kMergeItems * kRowF;
+  if (warp < 4) {
+#pragma unroll
+    for (int q = 0; q < DH / 32; ++q) {
+      uint32_t o[32];
+      if (nT > 0) {
+        tmem_ld32(tmem + TM_O + lane_off + q * 32, o);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = 0u;
+      }
+      float4* dst = reinterpret_cast<float4*>(stage + tid * kRowF + q * 32);
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        dst[e] = make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]), __uint_as_float(o[4 * e + 2]),
+                             __uint_as_float(o[4 * e + 3]));
     }
-    live[tid] = ok;
+    stage[tid * kRowF + DH] = m;
+    stage[tid * kRowF + DH + 1] = l;
+    fence_async_smem();                              // the bulk copies read what the threads wrote
   }
-  __syncthreads();
-  if (tid < nr) {                                   // (b) merged max, sum and per-split weights
+  if (tid == 0) mbar_expect_tx(&bars.recv_full, static_cast<uint32_t>(S * nr * kRowF * 4));
+  tc_fence_before();
+  __syncwarp();
+  cluster_sync();                                   // every CTA is past its main loop: the rings are idle
+  tc_fence_after();
+  if (tid == 0) {
+    // rows [c*rpc, c*rpc + n_c) go to cluster rank c, into its slot for this split
+    for (int c = 0; c < S; ++c) {
+      const int n_c = min(BM, (c + 1) * rpc) - c * rpc;
+      if (n_c <= 0) continue;
+      const uint32_t dst = map_peer(smem_u32(recv + split * rpc * kRowF), static_cast<uint32_t>(c));
+      const uint32_t bar = map_peer(smem_u32(&bars.recv_full), static_cast<uint32_t>(c));
+      bulk_copy_to_peer(dst, smem_u32(stage + c * rpc * kRowF), static_cast<uint32_t>(n_c * kRowF * 4), bar);
+    }
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  }
+  // weights of the owned rows once every split has arrived
+  if (tid < nr) {
+    const bool ok = mbar_wait(bars, &bars.recv_full, 0, p.hdr, 40) && bars.live[tid];
     float M = -INFINITY;
-    for (int c = 0; c < S; ++c) M = fmaxf(M, mm[tid * S + c]);
+    for (int c = 0; c < S; ++c) M = fmaxf(M, recv[(c * rpc + tid) * kRowF + DH]);
     float L = 0.f;
     for (int c = 0; c < S; ++c) {
-      const float mc = mm[tid * S + c];
+      const float mc = recv[(c * rpc + tid) * kRowF + DH];
       const float f = mc > -INFINITY ? ex2_approx(mc - M) : 0.f;
-      fac[tid * S + c] = f;
-      L = fmaf(ll[tid * S + c], f, L);
+      fac[tid * kMaxSplit + c] = f;
+      L = fmaf(recv[(c * rpc + tid) * kRowF + DH + 1], f, L);
     }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    for (int c = 0; c < S; ++c) fac[tid * S + c] *= inv;
-    if (!(L > 0.f)) live[tid] = 0;
+    // a row with no allowed key is not a present token: weights 0, row skipped
+    const float inv = (ok && L > 0.f) ? 1.f / L : 0.f;
+    for (int c = 0; c < S; ++c) fac[tid * kMaxSplit + c] *= inv;
+    bars.live[tid] = (ok && L > 0.f) ? 1 : 0;
   }
   __syncthreads();
-  // (c) one float4 of one row per item; a warp covers one row, its S peer loads in flight together
+  // one float4 of one owned row per item, the S partial loads in flight together
   for (int it = tid; it < nr * (DH / 4); it += kThreads) {
     const int i = it / (DH / 4), q4 = it % (DH / 4);
-    if (!live[i]) continue;
-    const uint32_t src = smem_u32(ostage + (rb + i) * kOStride + q4 * 4);
-    float4 o[kMaxSplit];
-#pragma unroll
-    for (int c = 0; c < kMaxSplit; ++c)
-      if (c < S) o[c] = ld_peer_f32x4(map_peer(src, c));
+    if (!bars.live[i]) continue;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int c = 0; c < kMaxSplit; ++c)
+    for (int c = 0; c < kMaxSplit; ++c) {
       if (c < S) {
-        const float f = fac[i * S + c];
-        acc.x = fmaf(f, o[c].x, acc.x);
-        acc.y = fmaf(f, o[c].y, acc.y);
-        acc.z = fmaf(f, o[c].z, acc.z);
-        acc.w = fmaf(f, o[c].w, acc.w);
+        const float f = fac[i * kMaxSplit + c];
+        const float4 o = *reinterpret_cast<const float4*>(recv + (c * rpc + i) * kRowF + q4 * 4);
+        acc.x = fmaf(f, o.x, acc.x);
+        acc.y = fmaf(f, o.y, acc.y);
+        acc.z = fmaf(f, o.z, acc.z);
+        acc.w = fmaf(f, o.w, acc.w);
       }
+    }
     const int gr = r0 + rb + i;
     const int tt = gr / G, hh = kvh * G + gr % G;
     const int64_t o_off = ((static_cast<int64_t>(b) * NT + tt) * p.Hq + hh) * DH + q4 * 4;
@@ -585,12 +607,13 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CU
           make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
     }
   }
-  cluster_sync();                                   // peers are done reading this CTA's staging
+  // this CTA's outgoing copies have finished reading its rows before it exits
+  if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 
   // teardown: every role is done with TMEM
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 4) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
@@ -619,21 +642,37 @@ static bool make_kv_map(CUtensorMap* map, const void* base, uint64_t rows) {
   if (enc == nullptr) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(DH), rows};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(DH) * 2};
-  const cuuint32_t box[2] = {64, BN};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(BN)};
   const cuuint32_t estr[2] = {1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Q [B*NT][Hq][dh] as a 4-D tensor (dh, head in group, kv head, token): a box of
+// 128/G tokens of one kv head's G heads lands as the 128 packed rows of a row tile
+static bool make_q_map(CUtensorMap* map, const void* base, uint64_t tokens, int G, int Hkv) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(DH), static_cast<cuuint64_t>(G), static_cast<cuuint64_t>(Hkv),
+                              tokens};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(DH) * 2, static_cast<cuuint64_t>(G) * DH * 2,
+                                 static_cast<cuuint64_t>(G) * Hkv * DH * 2};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(G), 1, static_cast<cuuint32_t>(BM / G)};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // candidate K or V [B*NT][Hkv][dh] as a 3-D tensor (dh, kv head, slot): a box of
-// 64 slots of one kv head lands as a [64][64] tile like a prefix tile
+// BN slots of one kv head lands as a [BN][64] tile like a prefix tile
 static bool make_cand_map(CUtensorMap* map, const void* base, uint64_t slots, int Hkv) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(DH), static_cast<cuuint64_t>(Hkv), slots};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(DH) * 2, static_cast<cuuint64_t>(Hkv) * DH * 2};
-  const cuuint32_t box[3] = {64, 1, BN};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(BN)};
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -671,26 +710,32 @@ static int max_active_clusters(int S) {
   return cache[S][dev];
 }
 
-// splits (cluster size <= 8): minimise (waves of clusters) x (key tiles per split + fixed cost)
-static void choose_split(const ssd_attn_args* a, int mtiles, int* S_out, int* chunk_out) {
+// Splits (cluster size <= 8): minimise (waves of clusters) x (tiles per split + fixed
+// cost). Split 0 also takes the own-block tiles of its row tile (at most nc of them),
+// so it gets nc fewer prefix tiles than the others.
+static void choose_split(const ssd_attn_args* a, int mtiles, int* S_out, int* chunk_out, int* chunk0_out) {
   const long long groups = static_cast<long long>(a->B) * a->Hkv * mtiles;   // clusters in the grid
   const long long nkt = a->P_max > 0 ? (a->P_max + BN - 1) / BN : 1;
+  const int G = a->Hq / a->Hkv;
+  // a row tile spans BM/G tokens; with the start of the first one's block, at most this many slots
+  const long long nc = (BM / G + a->Dmax - 1 + BN - 1) / BN;
   long long best_cost = -1;
   int best_S = 1;
   for (int S = 1; S <= kMaxSplit && S <= nkt; ++S) {
     const int active = max_active_clusters(S);
     if (active <= 0) continue;
-    const long long tiles = (nkt + S - 1) / S;
+    const long long tiles = (nkt + nc + S - 1) / S;
     const long long waves = (groups + active - 1) / active;
-    const long long cost = waves * (tiles + 3) * 16 + S;   // +3 tiles: prologue, candidate tile, merge
+    const long long cost = waves * (tiles + 2) * 16 + S;   // +2 tiles: prologue and merge
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best_S = S;
     }
   }
-  const long long tiles = (nkt + best_S - 1) / best_S;
-  *chunk_out = static_cast<int>(tiles * BN);
+  const long long tiles = (nkt + nc + best_S - 1) / best_S;
   *S_out = best_S;
+  *chunk_out = static_cast<int>(tiles * BN);
+  *chunk0_out = static_cast<int>((tiles > nc ? tiles - nc : 0) * BN);
 }
 
 }  // namespace tc
@@ -708,6 +753,9 @@ bool attn_tc_applies(const ssd_attn_args* a) {
   if (static_cast<long long>(a->B) * a->Hkv * a->P_max >= (1LL << 31)) return false;
   if (static_cast<long long>(a->B) * a->NB * a->Dmax >= (1LL << 31)) return false;
   if (a->B * a->Hkv > 65535) return false;
+  // Q rows arrive by TMA as whole tokens: G must divide the 128 rows of a tile
+  const int G = a->Hq / a->Hkv;
+  if (G < 1 || G > 64 || (tc::BM % G) != 0) return false;
   int dev = 0, major = 0, minor = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
@@ -728,12 +776,12 @@ int attn_tc_launch(const ssd_attn_args* a, void* ws, cudaStream_t s) {
                                     static_cast<int>(tc::kSmemBytes));
   });
   if (attr_err != cudaSuccess) return SSD_ERR_CUDA;
-  int S = 1, chunk = tc::BN;
-  tc::choose_split(a, mtiles, &S, &chunk);
-  CUtensorMap mk, mv, mkc, mvc;
+  int S = 1, chunk = tc::BN, chunk0 = tc::BN;
+  tc::choose_split(a, mtiles, &S, &chunk, &chunk0);
+  CUtensorMap mq, mk, mv, mkc, mvc;
   const uint64_t rows = static_cast<uint64_t>(a->B) * a->Hkv * a->P_max;
   const uint64_t slots = static_cast<uint64_t>(a->B) * NT;
-  if (!tc::make_kv_map(&mk, a->k_cache, rows) || !tc::make_kv_map(&mv, a->v_cache, rows) ||
+  if (!tc::make_q_map(&mq, a->q, slots, G, a->Hkv) || !tc::make_kv_map(&mk, a->k_cache, rows) || !tc::make_kv_map(&mv, a->v_cache, rows) ||
       !tc::make_cand_map(&mkc, a->k_cand, slots, a->Hkv) || !tc::make_cand_map(&mvc, a->v_cand, slots, a->Hkv))
     return SSD_ERR_CUDA;
 
@@ -745,6 +793,7 @@ int attn_tc_launch(const ssd_attn_args* a, void* ws, cudaStream_t s) {
   p.scale_log2 = scale * 1.4426950408889634f;
   p.S = S;
   p.chunk = chunk;
+  p.chunk0 = chunk0;
   p.out_f32 = (a->out_dtype == SSD_F32) ? 1 : 0;
   p.hdr = reinterpret_cast<WsHeader*>(ws);
 
@@ -764,7 +813,7 @@ int attn_tc_launch(const ssd_attn_args* a, void* ws, cudaStream_t s) {
   cfg.numAttrs = 2;
   {
     KernelTimer timer(SSD_KERNEL_VERIFY_ATTN, s);
-    if (cudaLaunchKernelEx(&cfg, tc::k_attn_tc, mk, mv, mkc, mvc, p) != cudaSuccess) return SSD_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, tc::k_attn_tc, mq, mk, mv, mkc, mvc, p) != cudaSuccess) return SSD_ERR_CUDA;
   }
   count_launch(1);
   return check_launch();
