@@ -6,41 +6,45 @@
 // ending at the current token occurred earlier in the context; then up to W
 // continuations of length D are taken, most recent first.
 //
-// One kernel, k_front<GATE, RETRIEVE>, one CTA per sequence, serves the three
-// entry points (gate only, retrieval only, both fused). Every global load of a
-// phase is issued before its first use:
-//   1. ctx_len and the probe operands (h, w) together;
-//   2. one staged chunk of the context ending at the current token, extended
-//      by D positions so that continuations can be copied from shared memory;
+// One kernel, k_front<GATE, RETRIEVE>, one CTA of 512 threads per sequence,
+// serves the three entry points (gate only, retrieval only, both fused):
+//   1. ctx_len and the first pass of the probe operands (h, w) are loaded;
+//   2. the loads of the first context chunk (ending at the current token,
+//      extended by D positions so that continuations come from shared memory)
+//      are issued as soon as ctx_len is in, before the probe arithmetic;
 //   3. the probe sum in exact integer arithmetic (no fp64: the product of two
 //      fp32 significands is formed as a 64-bit integer and shifted into the
 //      2^-32 fixed point, identical to the exact real product truncated);
-//   4. match ends ranked in descending order with per-warp ballots and one
-//      prefix over the (round, warp) counts; the scan stops once W are known.
+//   4. each thread tests 8 consecutive match ends; one block scan of the
+//      per-thread counts ranks the matches in descending order; the
+//      continuations of the W most recent are copied from the tile by all
+//      threads; further chunks are staged only if fewer than W were found;
+//   5. one warp sums the probe partials and takes the gate decision.
 #include <math.h>
 
 #include "ssd_common.cuh"
 
 namespace ssd {
 
-constexpr int kGateThreads = 1024;
-constexpr int kChunk = 8192;                 // match ends examined per staged chunk
-constexpr int kPerThread = kChunk / kGateThreads;
+constexpr int kFrontThreads = 512;
+constexpr int kWarps = kFrontThreads / 32;
+constexpr int kPer = 8;                      // match ends per thread per chunk (contiguous, descending)
+constexpr int kChunk = kFrontThreads * kPer; // match ends examined per staged chunk
 constexpr int kMaxKappa = 64;
 constexpr int kMaxW = 64;
 constexpr int kMaxD = 256;
 constexpr int kTile = kChunk + kMaxKappa + kMaxD;
-constexpr int kStageLoads = (kTile + kGateThreads - 1) / kGateThreads;
-constexpr int kProbeBatch = 8;               // probe elements per thread in flight
+constexpr int kStageLoads = (kTile + kFrontThreads - 1) / kFrontThreads;
+constexpr int kProbePer = 8;                 // probe elements per thread per pass
 
 struct FrontSmem {
   int tile[kTile];                           // ctx[base .. base + cnt)
-  int cnt[kPerThread][kGateThreads / 32];    // matches per (round, warp), then their prefix
   int g[kMaxKappa];                          // the final kappa-gram
-  int ends[kMaxW];
+  int ends[kMaxW];                           // match ends, most recent first
+  int warp_cnt[kWarps];                      // matches per warp in the current chunk
+  long long warp_sum[kWarps];                // probe partial sums
   int nfound;
-  int total;
-  long long warp_sum[kGateThreads / 32];
+  int on;
 };
 
 // trunc(a * b * 2^32) for finite fp32 a, b with |a*b| < 2^31, exactly
@@ -61,7 +65,7 @@ __device__ __forceinline__ long long fixed_prod32(float a, float b) {
 }
 
 template <bool GATE, bool RETRIEVE>
-__global__ void __launch_bounds__(kGateThreads, 1)
+__global__ void __launch_bounds__(kFrontThreads, 1)
 k_front(const int32_t* __restrict__ ctx, int64_t stride, const int32_t* __restrict__ ctx_len,
         const void* __restrict__ h, int h_bf16, int64_t h_stride, const float* __restrict__ w, int d,
         int thr_mode, long long thr, int kappa, int W, int D, int K, int chain_policy,
@@ -74,76 +78,86 @@ k_front(const int32_t* __restrict__ ctx, int64_t stride, const int32_t* __restri
   const int b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int32_t* row = ctx + b * stride;
+  const uint16_t* hb = static_cast<const uint16_t*>(h) + b * h_stride;
+  const float* hf = static_cast<const float*>(h) + b * h_stride;
 
-  // ---- 1. context length and the probe operands, all loads in flight together
+  // ---- 1. loads that do not depend on the context length: ctx_len, the first probe pass
   const int n = __ldg(ctx_len + b);
-  long long acc = 0;
+  float hv[kProbePer], wv[kProbePer];
   if (GATE) {
-    const uint16_t* hb = static_cast<const uint16_t*>(h) + b * h_stride;
-    const float* hf = static_cast<const float*>(h) + b * h_stride;
-    for (int base = 0; base < d; base += kGateThreads * kProbeBatch) {
-      float hv[kProbeBatch], wv[kProbeBatch];
 #pragma unroll
-      for (int k = 0; k < kProbeBatch; ++k) {
-        const int i = base + k * kGateThreads + tid;
-        hv[k] = 0.f;
-        wv[k] = 0.f;
-        if (i < d) {
-          hv[k] = h_bf16 ? bf16_to_f32(__ldg(hb + i)) : __ldg(hf + i);
-          wv[k] = __ldg(w + i);
-        }
+    for (int k = 0; k < kProbePer; ++k) {
+      const int i = tid * kProbePer + k;
+      hv[k] = 0.f;
+      wv[k] = 0.f;
+      if (i < d) {
+        hv[k] = h_bf16 ? bf16_to_f32(__ldg(hb + i)) : __ldg(hf + i);
+        wv[k] = __ldg(w + i);
       }
+    }
+  }
+  bool on = true;
+  if (RETRIEVE && !GATE) on = __ldg(gate + b) != 0;
+  const int want = RETRIEVE ? W : 1;
+  bool scan = n >= kappa + 1;
+  if (RETRIEVE && !GATE) scan = scan && on;
+
+  // ---- 2. the first chunk of the context (ending at the current token): its loads
+  // are in flight while the probe sum is formed. A chunk covers match ends
+  // [j_lo, j_hi]; its tile adds the kappa-1 tokens before j_lo and, for
+  // retrieval, the D tokens after j_hi, so continuations come from shared memory.
+  const int j_min = kappa - 1;
+  int j_hi = n - 2, j_lo = 0, base = 0, cnt = 0;
+  int v[kStageLoads];
+  auto stage_loads = [&]() {
+    j_lo = max(j_min, j_hi - kChunk + 1);
+    base = j_lo - kappa + 1;
+    const int top = min(n - 1, j_hi + (RETRIEVE ? D : 0) + 1);
+    cnt = top - base + 1;
 #pragma unroll
-      for (int k = 0; k < kProbeBatch; ++k) acc += fixed_prod32(hv[k], wv[k]);
+    for (int u = 0; u < kStageLoads; ++u) {
+      const int i = tid + u * kFrontThreads;
+      v[u] = i < cnt ? __ldg(row + base + i) : 0;
+    }
+  };
+  if (scan) stage_loads();
+
+  // ---- 3. the probe sum in exact integer fixed point (2^-32)
+  if (GATE) {
+    long long acc = 0;
+#pragma unroll
+    for (int k = 0; k < kProbePer; ++k) acc += fixed_prod32(hv[k], wv[k]);
+    for (int i0 = kFrontThreads * kProbePer; i0 < d; i0 += kFrontThreads * kProbePer) {
+#pragma unroll
+      for (int k = 0; k < kProbePer; ++k) {
+        const int i = i0 + tid * kProbePer + k;
+        if (i < d) acc += fixed_prod32(h_bf16 ? bf16_to_f32(__ldg(hb + i)) : __ldg(hf + i), __ldg(w + i));
+      }
     }
     acc = warp_sum(acc);
     if (lane == 0) s.warp_sum[wid] = acc;
   }
-  bool on = true;
-  if (RETRIEVE && !GATE) on = __ldg(gate + b) != 0;
   if (tid == 0) s.nfound = 0;
-  __syncthreads();
 
-  // ---- 2..4. scan for earlier occurrences of the final kappa-gram
-  // GATE needs the largest end; RETRIEVE the W largest (only when the gate is on,
-  // which for the fused kernel is known once the probe sum is in).
-  const int want = RETRIEVE ? W : 1;
-  bool scan = n >= kappa + 1;
-  if (RETRIEVE && !GATE) scan = scan && on;
-  int first = -1;
+  // ---- 4. scan chunks from the end until `want` match ends are known
   if (scan) {
-    const int j_min = kappa - 1;
-    for (int j_hi = n - 2; j_hi >= j_min;) {
-      const int j_lo = max(j_min, j_hi - kChunk + 1);
-      // stage ctx[j_lo-kappa+1 .. min(n-1, j_hi+D)] (the final kappa-gram and every
-      // continuation of a match in this chunk lie inside)
-      const int base = j_lo - kappa + 1;
-      const int top = min(n - 1, j_hi + (RETRIEVE ? D : 0) + 1);
-      const int cnt = top - base + 1;
-      {
-        int v[kStageLoads];
+    for (;;) {
 #pragma unroll
-        for (int u = 0; u < kStageLoads; ++u) {
-          const int i = tid + u * kGateThreads;
-          v[u] = i < cnt ? __ldg(row + base + i) : 0;
-        }
-        __syncthreads();   // the previous chunk's tile is no longer read
-#pragma unroll
-        for (int u = 0; u < kStageLoads; ++u) {
-          const int i = tid + u * kGateThreads;
-          if (i < cnt) s.tile[i] = v[u];
-        }
+      for (int u = 0; u < kStageLoads; ++u) {
+        const int i = tid + u * kFrontThreads;
+        if (i < cnt) s.tile[i] = v[u];
       }
       __syncthreads();
-      // the final kappa-gram ctx[n-kappa .. n-1] lies in the first chunk's tile
-      if (j_hi == n - 2) {
+      if (j_hi == n - 2) {   // the final kappa-gram ctx[n-kappa .. n-1] lies in the first chunk's tile
         if (tid < kappa) s.g[tid] = s.tile[n - kappa + tid - base];
         __syncthreads();
       }
+      const int before = s.nfound;
+      // this thread's match ends j = j_hi - (tid*kPer + u), u = 0.. (descending)
       unsigned mask = 0;
 #pragma unroll
-      for (int u = 0; u < kPerThread; ++u) {
-        const int j = j_hi - (u * kGateThreads + tid);
+      for (int u = 0; u < kPer; ++u) {
+        const int j = j_hi - (tid * kPer + u);
         if (j >= j_lo) {
           const int* t = s.tile + (j - kappa + 1 - base);
           bool ok = true;
@@ -151,100 +165,89 @@ k_front(const int32_t* __restrict__ ctx, int64_t stride, const int32_t* __restri
           if (ok) mask |= 1u << u;
         }
       }
-      // rank: position j_hi - (u*256 + tid) precedes every (u', tid') with a larger u'*256+tid'
+      // rank of a match = matches at larger j: in earlier threads, then at lower u here
+      const int c = __popc(mask);
+      int incl = c;
 #pragma unroll
-      for (int u = 0; u < kPerThread; ++u) {
-        const unsigned bal = __ballot_sync(0xffffffffu, (mask >> u) & 1u);
-        if (lane == 0) s.cnt[u][wid] = __popc(bal);
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
       }
+      if (lane == 31) s.warp_cnt[wid] = incl;
       __syncthreads();
-      if (wid == 0) {
-        constexpr int nc = kPerThread * (kGateThreads / 32);
-        constexpr int per = nc / 32;
-        int* flat = &s.cnt[0][0];
-        int v[per];
-        int local = 0;
+      int woff = 0, total = 0;
 #pragma unroll
-        for (int q = 0; q < per; ++q) {
-          v[q] = flat[lane * per + q];
-          local += v[q];
-        }
-        int incl = local;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        const int before = s.nfound;
-        int run = before + incl - local;
-#pragma unroll
-        for (int q = 0; q < per; ++q) {
-          flat[lane * per + q] = run;
-          run += v[q];
-        }
-        if (lane == 31) s.total = before + incl;
+      for (int q = 0; q < kWarps; ++q) {
+        const int x = s.warp_cnt[q];
+        woff += q < wid ? x : 0;
+        total += x;
       }
-      __syncthreads();
+      int rank = before + woff + incl - c;
 #pragma unroll
-      for (int u = 0; u < kPerThread; ++u) {
-        const bool m = (mask >> u) & 1u;
-        const unsigned bal = __ballot_sync(0xffffffffu, m);
-        if (m) {
-          const int rank = s.cnt[u][wid] + __popc(bal & ((1u << lane) - 1u));
-          const int j = j_hi - (u * kGateThreads + tid);
-          if (rank < want) {
-            s.ends[rank] = j;
-            if (RETRIEVE && blk_tok != nullptr) {
-              // continuation tokens straight from the tile into block `rank`
-              const int len = min(D, n - 1 - j);
-              int32_t* bt = blk_tok + (static_cast<int64_t>(b) * NB + rank) * Dmax;
-              for (int q = 0; q < len; ++q) bt[q] = s.tile[j + 1 + q - base];
-            }
-          }
+      for (int u = 0; u < kPer; ++u) {
+        if ((mask >> u) & 1u) {
+          if (rank < want) s.ends[rank] = j_hi - (tid * kPer + u);
+          ++rank;
         }
       }
       __syncthreads();
-      if (tid == 0) s.nfound = s.total;
-      __syncthreads();
-      if (s.nfound >= want) break;
+      // continuation tokens of the ends found in this chunk, straight from the tile
+      const int r_lo = before, r_hi = min(want, before + total);
+      if (RETRIEVE && blk_tok != nullptr && r_hi > r_lo) {
+        for (int idx = tid; idx < (r_hi - r_lo) * D; idx += kFrontThreads) {
+          const int rr = r_lo + idx / D, q = idx - (idx / D) * D;
+          const int j = s.ends[rr];
+          if (q < min(D, n - 1 - j))
+            blk_tok[(static_cast<int64_t>(b) * NB + rr) * Dmax + q] = s.tile[j + 1 + q - base];
+        }
+      }
+      const bool done = before + total >= want || j_lo == j_min;
+      __syncthreads();                               // the tile, ends and count are no longer read
+      if (tid == 0) s.nfound = before + total;
+      if (done) break;
       j_hi = j_lo - 1;
+      stage_loads();
     }
-    first = s.nfound > 0 ? s.ends[0] : -1;
   }
+  __syncthreads();
+  const int nfound = s.nfound;
+  const int first = nfound > 0 ? s.ends[0] : -1;
 
-  // ---- gate decision
+  // ---- 5. gate decision: one warp sums the probe partials
   if (GATE) {
-    __syncthreads();
-    long long S = 0;
-#pragma unroll
-    for (int i = 0; i < kGateThreads / 32; ++i) S += s.warp_sum[i];
-    on = thr_mode == 1 ? true : thr_mode == 2 ? false : (S >= thr);
-    if (tid == 0) {
-      const float x = static_cast<float>(S) * 2.3283064365386962890625e-10f;   // 2^-32
-      score[b] = 1.f / (1.f + expf(-x));
-      last[b] = first;
-      gate[b] = (on && first >= 0) ? 1 : 0;
-      if (probe_on != nullptr) probe_on[b] = on ? 1 : 0;
+    if (wid == 0) {
+      long long S = lane < kWarps ? s.warp_sum[lane] : 0;
+      S = warp_sum(S);
+      if (lane == 0) {
+        const bool pon = thr_mode == 1 ? true : thr_mode == 2 ? false : (S >= thr);
+        const float x = static_cast<float>(S) * 2.3283064365386962890625e-10f;   // 2^-32
+        score[b] = 1.f / (1.f + expf(-x));
+        last[b] = first;
+        gate[b] = (pon && first >= 0) ? 1 : 0;
+        if (probe_on != nullptr) probe_on[b] = pon ? 1 : 0;
+        s.on = (pon && first >= 0) ? 1 : 0;
+      }
     }
-    on = on && first >= 0;
+    __syncthreads();
+    on = s.on != 0;
   }
 
-  // ---- retrieval outputs: lengths, padding, chain block
+  // ---- 6. retrieval outputs: lengths, padding, chain block
   if (RETRIEVE) {
-    const int nf = on ? min(s.nfound, W) : 0;
+    const int nf = on ? min(nfound, W) : 0;
     const bool chain_on = chain_policy == SSD_CHAIN_ALWAYS || (chain_policy == SSD_CHAIN_WHEN_GATE_OFF && !on);
     int32_t* bt = blk_tok + static_cast<int64_t>(b) * NB * Dmax;
-    for (int i = tid; i < NB * Dmax; i += kGateThreads) {
-      const int k = i / Dmax, pos = i % Dmax;
+    for (int i = tid; i < NB * Dmax; i += kFrontThreads) {
+      const int k = i / Dmax, pos = i - (i / Dmax) * Dmax;
       if (k < W) {
         // copy blocks were written during the scan (only when the gate is on)
         const int len = k < nf ? min(D, n - 1 - s.ends[k]) : 0;
-        if (pos >= len || k >= nf) bt[i] = -1;
+        if (pos >= len) bt[i] = -1;
       } else {
         bt[i] = (chain_on && pos < K) ? __ldg(chain_tok + static_cast<int64_t>(b) * K + pos) : -1;
       }
     }
-    for (int k = tid; k < NB; k += kGateThreads) {
+    for (int k = tid; k < NB; k += kFrontThreads) {
       int len = 0;
       if (k < W) {
         if (k < nf) len = min(D, n - 1 - s.ends[k]);
@@ -305,7 +308,7 @@ extern "C" int ssd_gate_match(const int32_t* ctx, int64_t ctx_stride, const int3
   const Threshold t = probe_threshold(tau);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   KernelTimer timer(SSD_KERNEL_GATE_MATCH, s);
-  k_front<true, false><<<B, kGateThreads, 0, s>>>(ctx, ctx_stride, ctx_len, h, h_dtype == SSD_BF16, h_stride, w, d,
+  k_front<true, false><<<B, kFrontThreads, 0, s>>>(ctx, ctx_stride, ctx_len, h, h_dtype == SSD_BF16, h_stride, w, d,
                                                   t.mode, t.thr, kappa, 1, 1, 0, 0, nullptr, 1, 1, score, gate,
                                                   last_match_end, probe_on, nullptr, nullptr, nullptr);
   count_launch();
@@ -327,7 +330,7 @@ extern "C" int ssd_retrieve(const int32_t* ctx, int64_t ctx_stride, const int32_
   const int Dmax = chain_policy != SSD_CHAIN_NONE ? (D > K ? D : K) : D;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   KernelTimer timer(SSD_KERNEL_RETRIEVE, s);
-  k_front<false, true><<<B, kGateThreads, 0, s>>>(ctx, ctx_stride, ctx_len, nullptr, 0, 0, nullptr, 0, 0, 0, kappa, W,
+  k_front<false, true><<<B, kFrontThreads, 0, s>>>(ctx, ctx_stride, ctx_len, nullptr, 0, 0, nullptr, 0, 0, 0, kappa, W,
                                                   D, K, chain_policy, chain_tok, NB, Dmax, nullptr,
                                                   const_cast<int32_t*>(gate), nullptr, nullptr, blk_tok, blk_len,
                                                   n_cand);
@@ -350,7 +353,7 @@ extern "C" int ssd_gate_retrieve(const int32_t* ctx, int64_t ctx_stride, const i
   const int Dmax = chain_policy != SSD_CHAIN_NONE ? (D > K ? D : K) : D;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   KernelTimer timer(SSD_KERNEL_GATE_MATCH, s);
-  k_front<true, true><<<B, kGateThreads, 0, s>>>(ctx, ctx_stride, ctx_len, h, h_dtype == SSD_BF16, h_stride, w, d,
+  k_front<true, true><<<B, kFrontThreads, 0, s>>>(ctx, ctx_stride, ctx_len, h, h_dtype == SSD_BF16, h_stride, w, d,
                                                  t.mode, t.thr, kappa, W, D, K, chain_policy, chain_tok, NB, Dmax,
                                                  score, gate, last_match_end, probe_on, blk_tok, blk_len, n_cand);
   count_launch();
