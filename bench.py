@@ -201,7 +201,7 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-KERNELS = ["gate_match", "verify_attn", "vocab_stats", "accept_select", "sample_final"]
+KERNELS = ["gate_match", "verify_attn", "vocab_stats", "accept_finish"]
 
 
 def source_sha(*names):

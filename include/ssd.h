@@ -290,8 +290,8 @@ enum {
   SSD_KERNEL_VOCAB_STATS = 1,
   SSD_KERNEL_VERIFY_ATTN = 2,        /* the tensor-core attention kernel, or the SIMT prefix pass */
   SSD_KERNEL_ATTN_COMBINE = 3,
-  SSD_KERNEL_ACCEPT_SELECT = 4,
-  SSD_KERNEL_SAMPLE_FINAL = 5,
+  SSD_KERNEL_ACCEPT_FINISH = 4,      /* merge, acceptance, choice and final draw */
+  SSD_KERNEL_RESERVED_5 = 5,         /* unused */
   SSD_KERNEL_GATE_MATCH = 6,
   SSD_KERNEL_RETRIEVE = 7
 };

@@ -26,7 +26,7 @@ SSD_CHAIN_NONE, SSD_CHAIN_WHEN_GATE_OFF, SSD_CHAIN_ALWAYS = 0, 1, 2
 EXPORTED = ["ssd_status_string", "ssd_version", "ssd_launch_count", "ssd_gate_match", "ssd_retrieve",
             "ssd_verify_attn_workspace_size", "ssd_verify_attn", "ssd_accept_workspace_size", "ssd_accept",
             "ssd_read_device_error", "ssd_profile_kernel", "ssd_accept_static", "ssd_gate_retrieve"]
-SSD_KERNEL = dict(vocab_stats=1, verify_attn=2, attn_combine=3, accept_select=4, sample_final=5, gate_match=6,
+SSD_KERNEL = dict(vocab_stats=1, verify_attn=2, attn_combine=3, accept_finish=4, gate_match=6,
                   retrieve=7)
 
 

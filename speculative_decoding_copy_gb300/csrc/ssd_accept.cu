@@ -11,20 +11,17 @@
 //
 // Kernels (one stream, in order; each later kernel is launched with
 // programmatic dependent launch and waits for its predecessor's results):
-//   k_vocab_stats   persistent CTAs over (sequence, row, chunk) tasks: one
-//                   16-byte-vector pass over the logits, a whole 32 KB chunk
-//                   in registers per task and the next task's loads in flight
-//                   while the current one is reduced to max, argmax (lowest
-//                   index on ties) and sum of 2^((l - max) log2 e);
-//   k_accept_select grid B: merges the chunks of every needed row, runs the
-//                   acceptance test of every candidate token (one thread per
-//                   token slot, loads issued together), picks the longest
-//                   accepted block and writes the accepted tokens;
-//   k_sample_final  grid (chunks, B), sample mode only: integer weights of the
-//                   stop row per chunk; the last CTA of each sequence (a
-//                   completion counter, no spin-wait) finds the chunk and the
-//                   index where the prefix sum crosses the threshold with
-//                   block-wide scans;
+//   k_vocab_stats   every warp streams whole pieces of 2048 entries of the rows
+//                   some token needs (16-byte loads, all in flight together) and
+//                   reduces each to max, argmax (greedy only; lowest index on
+//                   ties) and sum of 2^((l - max) log2 e) with warp shuffles;
+//   k_accept_finish one cluster of 8 CTAs per sequence: merges the pieces of
+//                   every needed row (one warp per row), runs the acceptance test
+//                   of every candidate token and picks the longest accepted block
+//                   (rank 0), and in sample mode draws the final token from the
+//                   integer weights of the stop row (chunk sums exchanged through
+//                   distributed shared memory, then one block scan in the chunk
+//                   that holds the threshold);
 //   k_probs_out     optional diagnostic copy of p for every needed row.
 #include <math.h>
 
@@ -35,12 +32,9 @@
 namespace ssd {
 
 constexpr int kVocabThreads = 256;
-constexpr int kVec = 8;                 // 16-byte vectors per thread per stats chunk
-constexpr int kSelectThreads = 256;
 constexpr int kMaxRows = 1024;          // 1 + NB*Dmax + K
 constexpr int kMaxSlots = 1024;         // NB*Dmax
-constexpr int kSampleChunk = 2048;      // vocabulary entries per sampler CTA
-constexpr int kSamplePer = kSampleChunk / kVocabThreads;
+constexpr int kSampleChunk = 512;       // stop-row entries per warp of the final draw
 constexpr long long kOneWeight = 1LL << 40;
 
 __device__ __forceinline__ float load_val(const void* base, int64_t i, int bf16) {
@@ -120,6 +114,19 @@ __device__ __forceinline__ long long block_excl_scan(long long v, long long* war
 }
 
 // ------------------------------------------------------------------ stats
+// k_vocab_stats: every warp streams whole pieces of 2048 entries of the rows
+// some token needs (8 KB of fp32 or 4 KB of bf16: 16 or 8 16-byte loads per
+// lane, all in flight together) and reduces each piece alone with warp
+// shuffles; two CTAs of 8 warps per SM keep up to 128 KB of loads in flight per SM.
+constexpr int kStatsWarps = 8;
+constexpr int kStatsThreads = 32 * kStatsWarps;
+constexpr int kPieceElems = 2048;
+template <bool BF16>
+struct Piece {
+  static constexpr int kEPV = BF16 ? 8 : 4;                 // entries per 16-byte vector
+  static constexpr int kVec = kPieceElems / kEPV / 32;     // 16-byte loads per lane
+};
+
 // element e (0..EPV-1) of a 16-byte vector
 template <bool BF16>
 __device__ __forceinline__ float vec_elem(const uint4& u, int e) {
@@ -128,266 +135,92 @@ __device__ __forceinline__ float vec_elem(const uint4& u, int e) {
   return __uint_as_float(w);
 }
 
-// One chunk of one row as 16-byte vectors held in registers (32 per thread).
-// Elements past the row end (or an unaligned row) are gathered one by one; the
-// padding is -inf.
-template <bool BF16>
-__device__ __forceinline__ void load_chunk(const void* row, int64_t lo, int64_t hi, bool vec_ok, uint4* raw) {
-  constexpr int EPV = BF16 ? 8 : 4;    // elements per 16-byte vector
+// One warp's statistics of the piece of n elements starting at element e0 of `row`:
+// max, sum of 2^((x - max) log2 e) (not for probabilities) and, with AMAX, the argmax
+// (lowest index on ties). VEC: the row is 16-byte aligned with a whole number of
+// vectors, so every lane reads 16-byte vectors; missing elements count as -inf.
+// FULL: a whole piece (n = kPieceElems), no bounds checks.
+template <bool BF16, bool AMAX, bool VEC, bool FULL>
+__device__ __forceinline__ RowStat reduce_piece(const void* row, int n, int e0, int probs) {
+  constexpr int EPV = Piece<BF16>::kEPV;
+  constexpr int kPieceVec = Piece<BF16>::kVec;
+  const int lane = threadIdx.x & 31;
+  uint4 v[kPieceVec];
+  // lane's elements: vector j covers [e0 + (j*32 + lane)*EPV, +EPV)
+  if (VEC) {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const char*>(row) + static_cast<int64_t>(e0) * (BF16 ? 2 : 4));
+    const int nv = n / EPV;                 // whole vectors (the row length is a multiple of EPV)
 #pragma unroll
-  for (int v = 0; v < kVec; ++v) {
-    const int64_t i0 = lo + static_cast<int64_t>(v * kVocabThreads + threadIdx.x) * EPV;
-    if (vec_ok && i0 + EPV <= hi) {
-      raw[v] = __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(row) + i0 * (BF16 ? 2 : 4)));
-    } else {
-      uint32_t w[4];
+    for (int j = 0; j < kPieceVec; ++j) {
+      const int vi = j * 32 + lane;
+      v[j] = (FULL || vi < nv) ? __ldg(src + vi) : make_uint4(0, 0, 0, 0);
+    }
+  } else {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) w[q] = BF16 ? 0xff80ff80u : 0xff800000u;
+    for (int j = 0; j < kPieceVec; ++j) {
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
       for (int e = 0; e < EPV; ++e) {
-        if (i0 + e < hi) {
+        const int i = (j * 32 + lane) * EPV + e;
+        if (i < n) {
           if (BF16) {
-            const uint32_t h = __ldg(static_cast<const uint16_t*>(row) + i0 + e);
-            w[e >> 1] = (e & 1) ? ((w[e >> 1] & 0xffffu) | (h << 16)) : ((w[e >> 1] & 0xffff0000u) | h);
+            const uint32_t hbits = __ldg(static_cast<const uint16_t*>(row) + e0 + i);
+            w[e >> 1] |= (e & 1) ? (hbits << 16) : hbits;
           } else {
-            w[e] = __float_as_uint(__ldg(static_cast<const float*>(row) + i0 + e));
+            w[e] = __float_as_uint(__ldg(static_cast<const float*>(row) + e0 + i));
           }
         }
       }
-      raw[v] = make_uint4(w[0], w[1], w[2], w[3]);
+      v[j] = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
-}
-
-// max, argmax (lowest index on ties) and sum of 2^((x - max) log2 e) of this thread's elements
-template <bool BF16>
-__device__ __forceinline__ void reduce_chunk(const uint4* raw, int64_t lo, bool probs, float& m, float& s, float& av,
-                                             int& ai) {
-  constexpr int EPV = BF16 ? 8 : 4;
-  av = -INFINITY;
-  ai = 0x7fffffff;
+  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  float av = -INFINITY;
+  int ai = 0x7fffffff;
 #pragma unroll
-  for (int v = 0; v < kVec; ++v) {
-    const int i0 = static_cast<int>(lo + static_cast<int64_t>(v * kVocabThreads + threadIdx.x) * EPV);
+  for (int j = 0; j < kPieceVec; ++j) {
 #pragma unroll
     for (int e = 0; e < EPV; ++e) {
-      const float x = vec_elem<BF16>(raw[v], e);
-      if (x > av) {                      // indices increase: strict > keeps the lowest on ties
-        av = x;
-        ai = i0 + e;
-      }
-    }
-  }
-  m = av;
-  s = 0.f;
-  if (!probs && m > -INFINITY) {
-    const float c = -m * kLog2e;
-    float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-    for (int v = 0; v < kVec; ++v) {
-#pragma unroll
-      for (int e = 0; e < EPV; e += 2) {
-        s0 += ex2_approx(fmaf(vec_elem<BF16>(raw[v], e), kLog2e, c));
-        s1 += ex2_approx(fmaf(vec_elem<BF16>(raw[v], e + 1), kLog2e, c));
-      }
-    }
-    s = s0 + s1;
-  }
-}
-
-// ------------------------------------------------------------------ select
-constexpr int kSlotsPer = kMaxSlots / kSelectThreads;
-
-struct SelectSmem {
-  RowStat st[kMaxRows];
-  int len_s[256];
-  int acc_s[256];
-  unsigned char ok_s[kMaxSlots];
-  int sel[4];   // best block, a, len, final (greedy)
-};
-
-// Acceptance and choice of block for sequence b, by one CTA of 256 threads,
-// once every needed row's chunk statistics are in p.part.
-__device__ void select_one(const AcceptParams& p, int b, SelectSmem& sm) {
-  RowStat* st = sm.st;
-  int* len_s = sm.len_s;
-  int* acc_s = sm.acc_s;
-  unsigned char* ok_s = sm.ok_s;
-  int* sel = sm.sel;
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  constexpr int nw = kSelectThreads / 32;
-  const int nslots = p.NB * p.Dmax;
-
-  // 1. per token slot: its token, its block's length, its uniform and the logits
-  //    the acceptance test needs; every load is issued before the row merge
-  int x_[kSlotsPer], row_[kSlotsPer];
-  bool live_[kSlotsPer];
-  float lp_[kSlotsPer], lq_[kSlotsPer], u_[kSlotsPer];
-#pragma unroll
-  for (int k = 0; k < kSlotsPer; ++k) {
-    const int sl = tid + k * kSelectThreads;
-    live_[k] = false;
-    x_[k] = 0;
-    row_[k] = 0;
-    lp_[k] = 0.f;
-    lq_[k] = 0.f;
-    u_[k] = 0.f;
-    if (sl < nslots) {
-      const int blk = sl / p.Dmax, d = sl % p.Dmax;
-      const int raw = p.blk_len[b * p.NB + blk];
-      const int cap = (blk == p.chain_blk) ? min(p.Dmax, p.K) : p.Dmax;
-      const int L = min(max(raw, 0), cap);
-      if (d < L) {
-        const int x = p.blk_tok[static_cast<int64_t>(b) * nslots + sl];
-        if (x < 0 || x >= p.V) {
-          record_error(p.hdr, SSD_ERR_DEVICE, 100);
-        } else {
-          live_[k] = true;
-          x_[k] = x;
-          row_[k] = d == 0 ? 0 : 1 + blk * p.Dmax + d - 1;
-          if (p.sample) {
-            lp_[k] = load_val(row_ptr(p, b, row_[k]), x, p.bf16);
-            if (blk == p.chain_blk) lq_[k] = load_val(row_ptr(p, b, p.NR + d), x, p.bf16);
-            u_[k] = p.u_acc[static_cast<int64_t>(b) * nslots + sl];
-          }
+      const int i = (j * 32 + lane) * EPV + e;
+      const float x = (FULL || i < n) ? vec_elem<BF16>(v[j], e) : -INFINITY;
+      if (AMAX) {
+        if (x > av) {                       // indices increase along the lane: strict > keeps the lowest
+          av = x;
+          ai = e0 + i;
         }
-      }
-    }
-  }
-  for (int k = tid; k < p.NB; k += kSelectThreads) {
-    const int raw = p.blk_len[b * p.NB + k];
-    const int cap = (k == p.chain_blk) ? min(p.Dmax, p.K) : p.Dmax;
-    const int L = min(max(raw, 0), cap);
-    if (L != raw) record_error(p.hdr, SSD_ERR_DEVICE, 101);
-    len_s[k] = L;
-  }
-
-  __syncthreads();   // len_s
-  // 2. merge the vocabulary chunks of every needed row: one thread per row, its
-  //    chunk partials loaded together, max first, then one scaled sum
-  for (int r = tid; r < p.NRD; r += kSelectThreads) {
-    bool needed = r == 0;
-    if (r > 0 && r < p.NR) needed = ((r - 1) % p.Dmax) < len_s[(r - 1) / p.Dmax];
-    else if (r >= p.NR) needed = p.chain_blk >= 0 && (r - p.NR) < len_s[p.chain_blk];
-    if (!needed) continue;
-    const RowStat* src = p.part + (static_cast<int64_t>(b) * p.NRD + r) * p.nch;
-    float M = -INFINITY, S = 0.f, av = -INFINITY;
-    int ai = 0x7fffffff;
-    for (int c0 = 0; c0 < p.nch; c0 += 16) {
-      float4 v[16];
-#pragma unroll
-      for (int q = 0; q < 16; ++q)
-        v[q] = (c0 + q < p.nch) ? __ldcg(reinterpret_cast<const float4*>(src + c0 + q))
-                                : make_float4(-INFINITY, 0.f, -INFINITY, __int_as_float(0x7fffffff));
-      float Mb = -INFINITY;
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        Mb = fmaxf(Mb, v[q].x);
-        amax_merge(av, ai, v[q].z, __float_as_int(v[q].w));
-      }
-      const float Mn = fmaxf(M, Mb);
-      if (Mn > -INFINITY) {
-        float acc = (M > -INFINITY) ? S * ex2_approx((M - Mn) * kLog2e) : 0.f;
-#pragma unroll
-        for (int q = 0; q < 16; ++q)
-          if (v[q].x > -INFINITY) acc += v[q].y * ex2_approx((v[q].x - Mn) * kLog2e);
-        S = acc;
-        M = Mn;
-      }
-    }
-    const RowStat x{M, S, av, ai};
-    st[r] = x;
-    p.stat[static_cast<int64_t>(b) * p.NRD + r] = x;
-  }
-  __syncthreads();
-
-  // 3. acceptance test of every present token
-#pragma unroll
-  for (int k = 0; k < kSlotsPer; ++k) {
-    const int sl = tid + k * kSelectThreads;
-    if (sl >= nslots) continue;
-    bool ok = false;
-    if (live_[k]) {
-      const int blk = sl / p.Dmax, d = sl % p.Dmax;
-      if (!p.sample) {
-        ok = (x_[k] == st[row_[k]].amax_i);
       } else {
-        const float px = prob_of(lp_[k], st[row_[k]], p.probs);
-        const float qx = (blk == p.chain_blk) ? prob_of(lq_[k], st[p.NR + d], p.probs) : 1.f;
-        ok = __dmul_rn(static_cast<double>(u_[k]), static_cast<double>(qx)) < static_cast<double>(px);
+        m4[e & 3] = fmaxf(m4[e & 3], x);
       }
     }
-    ok_s[sl] = ok ? 1 : 0;
   }
-  __syncthreads();
-
-  // 4. leading accepted run of every block
-  for (int k = tid; k < p.NB; k += kSelectThreads) {
-    const int L = len_s[k];
-    int a = 0;
-    while (a < L && ok_s[k * p.Dmax + a]) ++a;
-    acc_s[k] = a;
-    p.acc_len[b * p.NB + k] = a;
-  }
-  __syncthreads();
-
-  // 5. longest accepted run, lowest block index on ties
-  if (tid == 0) {
-    int best = -1, ba = -1;
-    for (int k = 0; k < p.NB; ++k) {
-      if (len_s[k] > 0 && acc_s[k] > ba) {
-        ba = acc_s[k];
-        best = k;
-      }
-    }
-    const int a = best >= 0 ? ba : 0;
-    const int L = best >= 0 ? len_s[best] : 0;
-    const int stop = a == 0 ? 0 : 1 + best * p.Dmax + a - 1;
-    sel[0] = best;
-    sel[1] = a;
-    sel[2] = L;
-    sel[3] = st[stop].amax_i;
-    p.best_blk[b] = best;
-    p.n_out[b] = a + 1;
-    if (p.sample) {
-      StopInfo si;
-      si.row = stop;
-      si.ps = st[stop];
-      si.a = a;
-      si.drf_row = -1;
-      si.excl = -1;
-      si.bonus = (a >= L) ? 1 : 0;
-      si.qs = si.ps;
-      if (a < L) {
-        if (best == p.chain_blk) {
-          si.drf_row = a;
-          si.qs = st[p.NR + a];
-        }
-        else {
-          si.excl = p.blk_tok[static_cast<int64_t>(b) * nslots + best * p.Dmax + a];
-        }
-      }
-      p.stop[b] = si;
-      p.cnt[b] = 0u;
+  float M = AMAX ? av : fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if (AMAX) {
+      const float v2 = __shfl_xor_sync(0xffffffffu, av, o);
+      const int i2 = __shfl_xor_sync(0xffffffffu, ai, o);
+      amax_merge(av, ai, v2, i2);
     }
   }
-  __syncthreads();
-
-  // 6. emitted tokens (the sampler fills the final one in sample mode)
-  const int best = sel[0], a = sel[1];
-  for (int i = tid; i <= p.Dmax; i += kSelectThreads) {
-    int v = -1;
-    if (i < a) v = p.blk_tok[static_cast<int64_t>(b) * nslots + best * p.Dmax + i];
-    else if (i == a && !p.sample) v = sel[3];
-    p.out_tok[static_cast<int64_t>(b) * (p.Dmax + 1) + i] = v;
+  float S = 0.f;
+  if (!probs && M > -INFINITY) {
+    const float c = -M * kLog2e;
+    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < kPieceVec; ++j)
+#pragma unroll
+      for (int e = 0; e < EPV; ++e)
+        if (FULL || (j * 32 + lane) * EPV + e < n) s4[e & 3] += ex2_approx(fmaf(vec_elem<BF16>(v[j], e), kLog2e, c));
+    S = warp_sum((s4[0] + s4[1]) + (s4[2] + s4[3]));
   }
-  __syncthreads();
+  return RowStat{M, S, av, ai};
 }
 
-// next task (sequence, row, chunk) of this CTA whose row some token needs, or
-// ntask; tasks are numbered ((b * NRD) + r) * nch + c (fits in 32 bits)
-__device__ __forceinline__ int next_task(const AcceptParams& p, int t, int ntask) {
-  for (; t < ntask; t += gridDim.x) {
+// next task (sequence, row, piece) at or after t, in steps of `step`, whose row
+// some token needs, or ntask; tasks are numbered ((b * NRD) + r) * nch + c
+__device__ __forceinline__ int next_task(const AcceptParams& p, int t, int step, int ntask) {
+  for (; t < ntask; t += step) {
     const int br = t / p.nch;
     const int b = br / p.NRD, r = br - b * p.NRD;
     if (row_needed(p, b, r)) break;
@@ -395,235 +228,544 @@ __device__ __forceinline__ int next_task(const AcceptParams& p, int t, int ntask
   return t;
 }
 
-// Persistent CTAs walk the (sequence, row, chunk) tasks; the loads of the next
-// task are in flight while the current one is reduced.
-template <bool BF16>
-__global__ void __launch_bounds__(kVocabThreads, 2)
+// Every warp of the grid takes the tasks gw, gw + (warps in the grid), ...
+template <bool BF16, bool AMAX>
+__global__ void __launch_bounds__(kStatsThreads, 2)
 k_vocab_stats(AcceptParams p) {
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  __shared__ RowStat red[kVocabThreads / 32];
-  // let the next kernel of the stream start its launch while this one runs
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  // blk_len comes from the previous kernel of the stream
+  // blk_len comes from the retrieval; once it is in, the next kernel of the stream may
+  // start (its prologue reads the retrieval's outputs, never this kernel's)
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int ntask = p.nch * p.NRD * p.B;
-  uint4 cur[kVec], nxt[kVec];
-  int t = next_task(p, blockIdx.x, ntask);
-  if (t < ntask) {
-    const int br = t / p.nch, c = t - br * p.nch;
-    const int b = br / p.NRD, r = br - b * p.NRD;
-    const int64_t lo = static_cast<int64_t>(c) * p.chunk;
-    const void* row = row_ptr(p, b, r);
-    load_chunk<BF16>(row, lo, min(p.V, lo + p.chunk), aligned_dev(row, 16), cur);
-  }
-  while (t < ntask) {
-    const int br = t / p.nch, c = t - br * p.nch;
-    const int b = br / p.NRD, r = br - b * p.NRD;
-    const int64_t lo = static_cast<int64_t>(c) * p.chunk;
-    // prefetch the next task
-    const int t2 = next_task(p, t + gridDim.x, ntask);
-    if (t2 < ntask) {
-      const int br2 = t2 / p.nch, c2 = t2 - br2 * p.nch;
-      const int b2 = br2 / p.NRD, r2 = br2 - b2 * p.NRD;
-      const int64_t lo2 = static_cast<int64_t>(c2) * p.chunk;
-      const void* row2 = row_ptr(p, b2, r2);
-      load_chunk<BF16>(row2, lo2, min(p.V, lo2 + p.chunk), aligned_dev(row2, 16), nxt);
-    }
-    float m, s, av;
-    int ai;
-    reduce_chunk<BF16>(cur, lo, p.probs, m, s, av, ai);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-      const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-      const float v2 = __shfl_xor_sync(0xffffffffu, av, o);
-      const int i2 = __shfl_xor_sync(0xffffffffu, ai, o);
-      stat_merge(m, s, m2, s2);
-      amax_merge(av, ai, v2, i2);
-    }
-    if (lane == 0) red[wid] = RowStat{m, s, av, ai};
-    __syncthreads();
-    if (tid == 0) {
-      for (int w = 1; w < kVocabThreads / 32; ++w) {
-        stat_merge(m, s, red[w].m, red[w].s);
-        amax_merge(av, ai, red[w].amax_v, red[w].amax_i);
-      }
-      p.part[(static_cast<int64_t>(b) * p.NRD + r) * p.nch + c] = RowStat{m, s, av, ai};
-    }
-    __syncthreads();   // red[] is reused by the next task of this CTA
-#pragma unroll
-    for (int v = 0; v < kVec; ++v) cur[v] = nxt[v];
-    t = t2;
-  }
-}
-
-// one CTA per sequence, once every chunk statistic is in
-__global__ void __launch_bounds__(kSelectThreads)
-k_accept_select(AcceptParams p) {
-  __shared__ SelectSmem sm;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");     // partials come from the stats kernel
-  for (int b = blockIdx.x; b < p.B; b += gridDim.x) select_one(p, b, sm);
+  constexpr int es = BF16 ? 2 : 4;
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * kStatsWarps + (threadIdx.x >> 5);
+  const int TW = gridDim.x * kStatsWarps;
+  const int ntask = p.nch * p.NRD * p.B;
+  const int per = kPieceElems;
+  const bool vec_rows = ((p.V * es) & 15) == 0;
+  for (int t = next_task(p, gw, TW, ntask); t < ntask; t = next_task(p, t + TW, TW, ntask)) {
+    const int br = t / p.nch, c = t - br * p.nch;
+    const int b = br / p.NRD, r = br - b * p.NRD;
+    const void* row = row_ptr(p, b, r);
+    const int e0 = c * per;
+    const int n = static_cast<int>(min(static_cast<int64_t>(per), p.V - e0));
+    RowStat st;
+    if (!vec_rows || !aligned_dev(row, 16)) st = reduce_piece<BF16, AMAX, false, false>(row, n, e0, p.probs);
+    else if (n == per) st = reduce_piece<BF16, AMAX, true, true>(row, n, e0, p.probs);
+    else st = reduce_piece<BF16, AMAX, true, false>(row, n, e0, p.probs);
+    if (lane == 0) p.part[static_cast<int64_t>(br) * p.nch + c] = st;
+  }
 }
 
-// ------------------------------------------------------------------ final draw
-// residual (or bonus) weight of entry i given its p and q values
-__device__ __forceinline__ void weights_of(const AcceptParams& p, float pv, const RowStat& ps, bool has_q, float qv,
-                                           const RowStat& qs, int excl, int bonus, int64_t i, long long& W,
-                                           long long& P) {
-  P = weight_of(prob_of(pv, ps, p.probs));
+// ------------------------------------------------------------------ finish
+// k_accept_finish: one cluster of kFinCTAs CTAs per sequence does the rest of the
+// step after the row pass: merging every needed row's piece statistics (all
+// warps of the cluster, one row per warp), the acceptance tests and the choice
+// of block (cluster rank 0), and in sample mode the final draw from the stop
+// row (every CTA sums the integer weights of its chunks; the sums go to every
+// CTA through distributed shared memory; the CTA holding the threshold finds
+// the index). What needs only the retrieval's outputs and the inputs (token
+// slots, their logits and uniforms) is loaded before griddepcontrol.wait, while
+// the row pass still runs.
+constexpr int kFinCTAs = 8;                 // cluster size when the stop row has at most 256 chunks
+constexpr int kMaxFinCTAs = 16;             // ... and up to 512 chunks (a non-portable cluster size)
+constexpr int kFinThreads = 1024;
+constexpr int kFinWarps = kFinThreads / 32;
+constexpr int kSlotsPer = kMaxSlots / kFinThreads;
+constexpr int kMaxSampleChunks = kMaxFinCTAs * kFinWarps;   // one chunk per warp of the cluster
+constexpr int kChunkVec = kSampleChunk / 4 / 32;            // float4 per lane per chunk
+constexpr size_t kFinDynSmem = 2ull * kFinWarps * kSampleChunk * sizeof(float);
+
+struct __align__(16) FinishSmem {
+  RowStat st[kMaxRows];                     // merged rows (rank 0 receives them)
+  long long csum[kMaxSampleChunks][2];      // chunk sums of the residual and bonus weights (every rank)
+  StopInfo si;                              // the stop row (rank 0 sends it to every rank)
+  int tok_s[kMaxSlots];                     // candidate tokens (rank 0)
+  int len_s[256];
+  int acc_s[256];
+  unsigned char ok_s[kMaxSlots];
+  long long red_w[kFinWarps], red_p[kFinWarps];
+  int sel[4];
+  int c_star, use_bonus;
+  long long t_rem;
+};
+
+__device__ __forceinline__ uint32_t smem_addr(const void* ptr) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
+}
+__device__ __forceinline__ uint32_t cl_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// every thread of every CTA of the cluster; orders shared-memory accesses across the cluster
+__device__ __forceinline__ void cl_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cl_map(const void* local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(local)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ RowStat warp_merge_stat(float M, float S, float av, int ai) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, M, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
+    const float v2 = __shfl_xor_sync(0xffffffffu, av, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, ai, o);
+    stat_merge(M, S, m2, s2);
+    amax_merge(av, ai, v2, i2);
+  }
+  return RowStat{M, S, av, ai};
+}
+
+// statistics of rows ra and rb of sequence b (rb < 0: none) merged from their pieces,
+// by one warp; the loads of both rows are in flight together
+__device__ __forceinline__ void merge_rows(const AcceptParams& p, int b, int ra, int rb, RowStat& xa, RowStat& xb) {
+  const int lane = threadIdx.x & 31;
+  const float4 none = make_float4(-INFINITY, 0.f, -INFINITY, __int_as_float(0x7fffffff));
+  const RowStat* sa = p.part + (static_cast<int64_t>(b) * p.NRD + ra) * p.nch;
+  const RowStat* sb = p.part + (static_cast<int64_t>(b) * p.NRD + (rb >= 0 ? rb : ra)) * p.nch;
+  float Ma = -INFINITY, Sa = 0.f, ava = -INFINITY, Mb = -INFINITY, Sb = 0.f, avb = -INFINITY;
+  int aia = 0x7fffffff, aib = 0x7fffffff;
+  for (int c0 = 0; c0 < p.nch; c0 += 64) {
+    const bool k0 = c0 + lane < p.nch, k1 = c0 + 32 + lane < p.nch;
+    const float4 a0 = k0 ? __ldcg(reinterpret_cast<const float4*>(sa + c0 + lane)) : none;
+    const float4 a1 = k1 ? __ldcg(reinterpret_cast<const float4*>(sa + c0 + 32 + lane)) : none;
+    const float4 b0 = (rb >= 0 && k0) ? __ldcg(reinterpret_cast<const float4*>(sb + c0 + lane)) : none;
+    const float4 b1 = (rb >= 0 && k1) ? __ldcg(reinterpret_cast<const float4*>(sb + c0 + 32 + lane)) : none;
+    stat_merge(Ma, Sa, a0.x, a0.y);
+    stat_merge(Ma, Sa, a1.x, a1.y);
+    amax_merge(ava, aia, a0.z, __float_as_int(a0.w));
+    amax_merge(ava, aia, a1.z, __float_as_int(a1.w));
+    stat_merge(Mb, Sb, b0.x, b0.y);
+    stat_merge(Mb, Sb, b1.x, b1.y);
+    amax_merge(avb, aib, b0.z, __float_as_int(b0.w));
+    amax_merge(avb, aib, b1.z, __float_as_int(b1.w));
+  }
+  xa = warp_merge_stat(Ma, Sa, ava, aia);
+  xb = warp_merge_stat(Mb, Sb, avb, aib);
+}
+
+
+// The weights with the row statistics folded in once: p = 2^(v log2 e - m log2 e) * (1/Z)
+// exactly as prob_of forms it, then P = floor(p 2^40) from the bits of p (weight_of).
+struct DrawRow {
+  float c;      // -m log2 e
+  float inv;    // 1/Z (round to nearest)
+  int probs;
+};
+__device__ __forceinline__ DrawRow draw_row(const RowStat& st, int probs) {
+  return DrawRow{-st.m * kLog2e, __frcp_rn(st.s), probs};
+}
+__device__ __forceinline__ long long weight_fast(float v, const DrawRow& r) {
+  return weight_of(r.probs ? v : ex2_approx(fmaf(v, kLog2e, r.c)) * r.inv);
+}
+// residual weight W = max(0, P - Q) (Q one-hot at excl for a copy block, from the draft
+// row for the chain block) and bonus weight P of entry i
+__device__ __forceinline__ void draw_weights(float pv, const DrawRow& pr, bool has_q, float qv, const DrawRow& qr,
+                                             int excl, int bonus, int64_t i, long long& W, long long& P) {
+  P = weight_fast(pv, pr);
   if (bonus) {
     W = P;
-    return;
-  }
-  const long long Q = has_q ? weight_of(prob_of(qv, qs, p.probs)) : ((i == excl) ? kOneWeight : 0LL);
-  W = P > Q ? P - Q : 0LL;
-}
-
-__device__ void sample_final_one(const AcceptParams& p, int b, int c) {
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  constexpr int nw = kVocabThreads / 32;
-  __shared__ long long red_w[nw], red_p[nw];
-  __shared__ int is_last, c_star, use_bonus;
-  __shared__ long long t_rem;
-
-  const StopInfo si = p.stop[b];
-  const void* prow = row_ptr(p, b, si.row);
-  const RowStat ps = si.ps;
-  const bool has_q = si.drf_row >= 0;
-  const void* qrow = has_q ? row_ptr(p, b, p.NR + si.drf_row) : prow;
-  const RowStat qs = si.qs;
-
-  // phase 1: this chunk's residual and bonus weight sums (all loads first)
-  const int64_t lo = static_cast<int64_t>(c) * kSampleChunk;
-  float pv[kSamplePer], qv[kSamplePer];
-#pragma unroll
-  for (int k = 0; k < kSamplePer; ++k) {
-    const int64_t i = lo + k * kVocabThreads + tid;
-    pv[k] = i < p.V ? load_val(prow, i, p.bf16) : 0.f;
-    qv[k] = (has_q && i < p.V) ? load_val(qrow, i, p.bf16) : 0.f;
-  }
-  long long sw = 0, sp = 0;
-#pragma unroll
-  for (int k = 0; k < kSamplePer; ++k) {
-    const int64_t i = lo + k * kVocabThreads + tid;
-    if (i < p.V) {
-      long long W, P;
-      weights_of(p, pv[k], ps, has_q, qv[k], qs, si.excl, si.bonus, i, W, P);
-      sw += W;
-      sp += P;
-    }
-  }
-  sw = warp_sum(sw);
-  sp = warp_sum(sp);
-  if (lane == 0) {
-    red_w[wid] = sw;
-    red_p[wid] = sp;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    long long tw = 0, tp = 0;
-    for (int w = 0; w < nw; ++w) {
-      tw += red_w[w];
-      tp += red_p[w];
-    }
-    p.csum[(static_cast<int64_t>(b) * p.nchs + c) * 2 + 0] = tw;
-    p.csum[(static_cast<int64_t>(b) * p.nchs + c) * 2 + 1] = tp;
-    __threadfence();
-    const unsigned ticket = atomicAdd(p.cnt + b, 1u);
-    is_last = (ticket == static_cast<unsigned>(p.nchs - 1)) ? 1 : 0;
-  }
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-
-  // phase 2 (last CTA of this sequence): totals, threshold, chunk
-  // each thread owns a contiguous run of chunks
-  const int cpt = (p.nchs + kVocabThreads - 1) / kVocabThreads;
-  const int c_lo = min(p.nchs, tid * cpt), c_hi = min(p.nchs, c_lo + cpt);
-  const volatile long long* cs = p.csum + static_cast<int64_t>(b) * p.nchs * 2;
-  if (tid == 0) {            // defaults if no weight is positive (degenerate rows)
-    c_star = 0;
-    t_rem = 0;
-    use_bonus = 1;
-  }
-  long long mw = 0, mp = 0;
-  for (int k = c_lo; k < c_hi; ++k) {
-    mw += cs[2 * k];
-    mp += cs[2 * k + 1];
-  }
-  long long SW, SP;
-  const long long ew = block_excl_scan(mw, red_w, &SW);
-  const long long ep = block_excl_scan(mp, red_p, &SP);
-  const int ub = (si.bonus || SW == 0) ? 1 : 0;
-  const unsigned long long S = static_cast<unsigned long long>(ub ? SP : SW);
-  const float u = fminf(fmaxf(p.u_fin[b], 0.f), 0.99999994f);               // contract: u in [0, 1)
-  const unsigned long long U = static_cast<unsigned long long>(u * 16777216.0f);   // floor(u 2^24), exact
-  const long long T = static_cast<long long>((__umul64hi(U, S) << 40) | ((U * S) >> 24));
-  const long long mine = ub ? mp : mw, excl = ub ? ep : ew;
-  if (mine > 0 && excl <= T && T < excl + mine) {
-    long long acc = excl;
-    int cst = c_hi - 1;
-    for (int k = c_lo; k < c_hi; ++k) {
-      const long long wk = cs[2 * k + ub];
-      if (acc + wk > T) {
-        cst = k;
-        break;
-      }
-      acc += wk;
-    }
-    c_star = cst;
-    t_rem = T - acc;
-    use_bonus = ub;
-  }
-  if (tid == 0) p.cnt[b] = 0u;
-  __syncthreads();
-
-  // phase 3: the index inside chunk c_star; each thread owns kSamplePer contiguous entries
-  const int64_t lo2 = static_cast<int64_t>(c_star) * kSampleChunk + tid * kSamplePer;
-  const int ub2 = use_bonus;
-#pragma unroll
-  for (int k = 0; k < kSamplePer; ++k) {
-    const int64_t i = lo2 + k;
-    pv[k] = i < p.V ? load_val(prow, i, p.bf16) : 0.f;
-    qv[k] = (has_q && i < p.V) ? load_val(qrow, i, p.bf16) : 0.f;
-  }
-  long long wv[kSamplePer];
-  long long my = 0;
-#pragma unroll
-  for (int k = 0; k < kSamplePer; ++k) {
-    const int64_t i = lo2 + k;
-    long long W = 0, P = 0;
-    if (i < p.V) weights_of(p, pv[k], ps, has_q, qv[k], qs, si.excl, si.bonus, i, W, P);
-    wv[k] = ub2 ? P : W;
-    my += wv[k];
-  }
-  long long tot;
-  const long long ex = block_excl_scan(my, red_w, &tot);
-  const long long Tr = t_rem;
-  if (my > 0 && ex <= Tr && Tr < ex + my) {
-    long long acc = ex;
-    int64_t tok = lo2 + kSamplePer - 1;
-#pragma unroll
-    for (int k = 0; k < kSamplePer; ++k) {
-      acc += wv[k];
-      if (acc > Tr) {
-        tok = lo2 + k;
-        break;
-      }
-    }
-    p.out_tok[static_cast<int64_t>(b) * (p.Dmax + 1) + si.a] = static_cast<int>(tok);
+  } else if (has_q) {
+    const long long Q = weight_fast(qv, qr);
+    W = P > Q ? P - Q : 0LL;
+  } else {
+    W = (i == excl) ? (P > kOneWeight ? P - kOneWeight : 0LL) : P;
   }
 }
 
-__global__ void __launch_bounds__(kVocabThreads)
-k_sample_final(AcceptParams p) {
+__device__ __forceinline__ float f4(const float4& v, int e) { return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w; }
+
+// chunk [lo, lo + kSampleChunk) of a row as this lane's kChunkVec groups of 4 entries
+// (entry lo + (j*32 + lane)*4 + e); entries past the row end are -inf (weight 0)
+template <int NJ = kChunkVec>
+__device__ __forceinline__ void load_chunk4(const AcceptParams& p, const void* row, int64_t lo, float4* v, int j0 = 0) {
+  const int lane = threadIdx.x & 31;
+  const bool full = lo + kSampleChunk <= p.V;
+  if (!p.bf16 && full && ((p.V * 4) & 15) == 0 && aligned_dev(row, 16)) {
+    const float4* r4 = reinterpret_cast<const float4*>(static_cast<const float*>(row) + lo);
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) v[j] = __ldg(r4 + (j0 + j) * 32 + lane);
+  } else if (p.bf16 && full && ((p.V * 2) & 7) == 0 && aligned_dev(row, 8)) {
+    const uint2* r2 = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(row) + lo);
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      const uint2 w = __ldg(r2 + (j0 + j) * 32 + lane);
+      v[j] = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u), __uint_as_float(w.y << 16),
+                         __uint_as_float(w.y & 0xffff0000u));
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      float x[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int64_t i = lo + static_cast<int64_t>((j0 + j) * 32 + lane) * 4 + e;
+        x[e] = i < p.V ? load_val(row, i, p.bf16) : -INFINITY;
+      }
+      v[j] = make_float4(x[0], x[1], x[2], x[3]);
+    }
+  }
+}
+
+// chunk [lo, lo + kSampleChunk) of a row into shared memory as fp32, entry lo + k at dst[k]
+__device__ __forceinline__ void stage_chunk(const AcceptParams& p, const void* row, int64_t lo, float4* dst) {
+  const int lane = threadIdx.x & 31;
+  constexpr int H = kChunkVec / 2;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float4 v[H];
+    load_chunk4<H>(p, row, lo, v, h * H);
+#pragma unroll
+    for (int j = 0; j < H; ++j) dst[(h * H + j) * 32 + lane] = v[j];
+  }
+}
+
+__global__ void __launch_bounds__(kFinThreads, 1)
+k_accept_finish(AcceptParams p) {
+  __shared__ FinishSmem sm;
+  extern __shared__ float4 fin_chunk[];             // [2][kFinWarps][kSampleChunk] fp32 chunks of p and q
+  const uint32_t rank = cl_rank();
+  const int C = static_cast<int>(gridDim.x);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nslots = p.NB * p.Dmax;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");     // stop rows come from the previous kernel
   for (int b = blockIdx.y; b < p.B; b += gridDim.y) {
-    sample_final_one(p, b, blockIdx.x);
-    __syncthreads();   // shared state is reused by the next sequence of this CTA
+    // ---- 1. (rank 0) per token slot: token, block length, uniform and the logits the
+    //         test needs; none of it comes from the row pass, so it is loaded before
+    //         griddepcontrol.wait
+    int x_[kSlotsPer], row_[kSlotsPer];
+    bool live_[kSlotsPer];
+    float lp_[kSlotsPer], lq_[kSlotsPer], u_[kSlotsPer];
+#pragma unroll
+    for (int k = 0; k < kSlotsPer; ++k) {
+      live_[k] = false;
+      x_[k] = 0;
+      row_[k] = 0;
+      lp_[k] = 0.f;
+      lq_[k] = 0.f;
+      u_[k] = 0.f;
+    }
+    if (rank == 0) {
+#pragma unroll
+      for (int k = 0; k < kSlotsPer; ++k) {
+        const int sl = tid + k * kFinThreads;
+        if (sl < nslots) {
+          const int blk = sl / p.Dmax, d = sl % p.Dmax;
+          sm.tok_s[sl] = p.blk_tok[static_cast<int64_t>(b) * nslots + sl];
+          const int raw = p.blk_len[b * p.NB + blk];
+          const int cap = (blk == p.chain_blk) ? min(p.Dmax, p.K) : p.Dmax;
+          const int L = min(max(raw, 0), cap);
+          if (d < L) {
+            const int x = sm.tok_s[sl];
+            if (x < 0 || x >= p.V) {
+              record_error(p.hdr, SSD_ERR_DEVICE, 100);
+            } else {
+              live_[k] = true;
+              x_[k] = x;
+              row_[k] = d == 0 ? 0 : 1 + blk * p.Dmax + d - 1;
+              if (p.sample) {
+                lp_[k] = load_val(row_ptr(p, b, row_[k]), x, p.bf16);
+                if (blk == p.chain_blk) lq_[k] = load_val(row_ptr(p, b, p.NR + d), x, p.bf16);
+                u_[k] = p.u_acc[static_cast<int64_t>(b) * nslots + sl];
+              }
+            }
+          }
+        }
+      }
+      for (int k = tid; k < p.NB; k += kFinThreads) {
+        const int raw = p.blk_len[b * p.NB + k];
+        const int cap = (k == p.chain_blk) ? min(p.Dmax, p.K) : p.Dmax;
+        const int L = min(max(raw, 0), cap);
+        if (L != raw) record_error(p.hdr, SSD_ERR_DEVICE, 101);
+        sm.len_s[k] = L;
+      }
+    }
+    cl_sync();                                        // every CTA runs: peers' shared memory may be written
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // the piece statistics are complete
+
+    // ---- 2. merge every needed row, one warp per row over the cluster; to rank 0
+    {
+      const int gw = static_cast<int>(rank) * kFinWarps + warp, nw = C * kFinWarps;
+      for (int r = gw; r < p.NRD; r += 2 * nw) {
+        const int r2 = r + nw;
+        const bool na = row_needed(p, b, r), nb = r2 < p.NRD && row_needed(p, b, r2);
+        if (!na && !nb) continue;
+        RowStat xa, xb;
+        merge_rows(p, b, na ? r : r2, (na && nb) ? r2 : -1, xa, xb);
+        if (lane == 0) {
+          const int rows[2] = {na ? r : r2, r2};
+          const RowStat xs[2] = {xa, xb};
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            if (k == 1 && !(na && nb)) break;
+            const RowStat x = xs[k];
+            p.stat[static_cast<int64_t>(b) * p.NRD + rows[k]] = x;
+            st_cluster_v4(cl_map(&sm.st[rows[k]], 0),
+                          make_uint4(__float_as_uint(x.m), __float_as_uint(x.s), __float_as_uint(x.amax_v),
+                                     static_cast<uint32_t>(x.amax_i)));
+          }
+        }
+      }
+    }
+    cl_sync();
+
+    // ---- 3. (rank 0) acceptance, leading runs, longest block, stop row
+    if (rank == 0) {
+#pragma unroll
+      for (int k = 0; k < kSlotsPer; ++k) {
+        const int sl = tid + k * kFinThreads;
+        if (sl >= nslots) continue;
+        bool ok = false;
+        if (live_[k]) {
+          const int blk = sl / p.Dmax, d = sl % p.Dmax;
+          if (!p.sample) {
+            ok = (x_[k] == sm.st[row_[k]].amax_i);
+          } else {
+            const float px = prob_of(lp_[k], sm.st[row_[k]], p.probs);
+            const float qx = (blk == p.chain_blk) ? prob_of(lq_[k], sm.st[p.NR + d], p.probs) : 1.f;
+            ok = __dmul_rn(static_cast<double>(u_[k]), static_cast<double>(qx)) < static_cast<double>(px);
+          }
+        }
+        sm.ok_s[sl] = ok ? 1 : 0;
+      }
+      __syncthreads();
+      // leading accepted run of every block: one warp per block, the first rejection by ballot
+      for (int k = warp; k < p.NB; k += kFinWarps) {
+        const int L = sm.len_s[k];
+        int a = L;
+        for (int d0 = 0; d0 < L; d0 += 32) {
+          const int d = d0 + lane;
+          const unsigned rej = __ballot_sync(0xffffffffu, d < L && !sm.ok_s[k * p.Dmax + d]);
+          if (rej != 0u) {
+            a = d0 + __ffs(rej) - 1;
+            break;
+          }
+        }
+        if (lane == 0) {
+          sm.acc_s[k] = a;
+          p.acc_len[b * p.NB + k] = a;
+        }
+      }
+      __syncthreads();
+      if (tid == 0) {
+        // longest accepted run, lowest block index on ties
+        int best = -1, ba = -1;
+        for (int k = 0; k < p.NB; ++k) {
+          if (sm.len_s[k] > 0 && sm.acc_s[k] > ba) {
+            ba = sm.acc_s[k];
+            best = k;
+          }
+        }
+        const int a = best >= 0 ? ba : 0;
+        const int L = best >= 0 ? sm.len_s[best] : 0;
+        const int stop = a == 0 ? 0 : 1 + best * p.Dmax + a - 1;
+        sm.sel[0] = best;
+        sm.sel[1] = a;
+        sm.sel[3] = sm.st[stop].amax_i;
+        p.best_blk[b] = best;
+        p.n_out[b] = a + 1;
+        StopInfo si;
+        si.row = stop;
+        si.ps = sm.st[stop];
+        si.a = a;
+        si.drf_row = -1;
+        si.excl = -1;
+        si.bonus = (a >= L) ? 1 : 0;
+        si.pad[0] = si.pad[1] = si.pad[2] = 0;
+        si.qs = si.ps;
+        if (a < L) {
+          if (best == p.chain_blk) {
+            si.drf_row = a;
+            si.qs = sm.st[p.NR + a];
+          } else {
+            si.excl = sm.tok_s[best * p.Dmax + a];
+          }
+        }
+        sm.si = si;
+      }
+      __syncthreads();
+      // emitted tokens (the draw below fills the final one in sample mode)
+      const int best = sm.sel[0], a = sm.sel[1];
+      for (int i = tid; i <= p.Dmax; i += kFinThreads) {
+        int v = -1;
+        if (i < a) v = sm.tok_s[best * p.Dmax + i];
+        else if (i == a && !p.sample) v = sm.sel[3];
+        p.out_tok[static_cast<int64_t>(b) * (p.Dmax + 1) + i] = v;
+      }
+      // the stop row to every rank
+      if (p.sample && tid < C * 4) {
+        const uint4* src = reinterpret_cast<const uint4*>(&sm.si);
+        st_cluster_v4(cl_map(reinterpret_cast<const uint4*>(&sm.si) + (tid & 3), static_cast<uint32_t>(tid >> 2)),
+                      src[tid & 3]);
+      }
+    }
+    cl_sync();
+    if (!p.sample) continue;
+
+    // ---- 4. warp gw holds chunk gw of the stop row in registers (entry lo + (j*32 + lane)*4 + e)
+    //         and sends its residual and bonus weight sums to every rank
+    const StopInfo si = sm.si;
+    const void* prow = row_ptr(p, b, si.row);
+    const bool has_q = si.drf_row >= 0;
+    const void* qrow = has_q ? row_ptr(p, b, p.NR + si.drf_row) : prow;
+    const DrawRow pr = draw_row(si.ps, p.probs), qr = draw_row(si.qs, p.probs);
+    const int gw = static_cast<int>(rank) * kFinWarps + warp;
+    const int64_t lo = static_cast<int64_t>(gw) * kSampleChunk;
+    float4* pch = fin_chunk + warp * (kSampleChunk / 4);                   // this warp's chunk of p
+    float4* qch = fin_chunk + (kFinWarps + warp) * (kSampleChunk / 4);     // ... and of q
+    if (gw < p.nchs) {
+      stage_chunk(p, prow, lo, pch);
+      if (has_q) stage_chunk(p, qrow, lo, qch);
+      __syncwarp();
+      long long sw = 0, sp = 0;
+#pragma unroll 2
+      for (int j = 0; j < kChunkVec; ++j) {
+        const int64_t i0 = lo + static_cast<int64_t>(j * 32 + lane) * 4;
+        const float4 a = pch[j * 32 + lane];
+        const float4 q = has_q ? qch[j * 32 + lane] : a;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          long long W, P;
+          draw_weights(f4(a, e), pr, has_q, f4(q, e), qr, si.excl, si.bonus, i0 + e, W, P);
+          sw += W;
+          sp += P;
+        }
+      }
+      sw = warp_sum(sw);
+      sp = warp_sum(sp);
+      if (lane < C) {
+        const uint32_t dst = cl_map(&sm.csum[gw][0], static_cast<uint32_t>(lane));
+        asm volatile("st.shared::cluster.v2.b64 [%0], {%1, %2};" ::"r"(dst), "l"(sw), "l"(sp) : "memory");
+      }
+    }
+    cl_sync();
+
+    // ---- 5. (warp 0 of every rank) S, the threshold T = floor(U S / 2^24) and the chunk holding it
+    if (warp == 0) {
+      constexpr int kPerLane = kMaxSampleChunks / 32;
+      long long aw = 0, ap = 0;
+#pragma unroll
+      for (int k = 0; k < kPerLane; ++k) {
+        const int c = lane * kPerLane + k;
+        if (c < p.nchs) {
+          aw += sm.csum[c][0];
+          ap += sm.csum[c][1];
+        }
+      }
+      long long iw = aw, ip = ap;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long yw = __shfl_up_sync(0xffffffffu, iw, o);
+        const long long yp = __shfl_up_sync(0xffffffffu, ip, o);
+        if (lane >= o) {
+          iw += yw;
+          ip += yp;
+        }
+      }
+      const long long SW = __shfl_sync(0xffffffffu, iw, 31), SP = __shfl_sync(0xffffffffu, ip, 31);
+      const int ub = (si.bonus || SW == 0) ? 1 : 0;
+      const unsigned long long S = static_cast<unsigned long long>(ub ? SP : SW);
+      const float u = fminf(fmaxf(p.u_fin[b], 0.f), 0.99999994f);               // contract: u in [0, 1)
+      const unsigned long long U = static_cast<unsigned long long>(u * 16777216.0f);   // floor(u 2^24), exact
+      const long long T = static_cast<long long>((__umul64hi(U, S) << 40) | ((U * S) >> 24));
+      const long long mine = ub ? ap : aw, ex = (ub ? ip : iw) - mine;
+      if (lane == 0) {            // defaults if no weight is positive (degenerate rows)
+        sm.c_star = 0;
+        sm.t_rem = 0;
+        sm.use_bonus = 1;
+      }
+      __syncwarp();
+      if (mine > 0 && ex <= T && T < ex + mine) {
+        long long acc = ex;
+        int cst = min(p.nchs, (lane + 1) * kPerLane) - 1;
+        for (int k = 0; k < kPerLane; ++k) {
+          const int c = lane * kPerLane + k;
+          if (c >= p.nchs) break;
+          const long long wk = sm.csum[c][ub];
+          if (acc + wk > T) {
+            cst = c;
+            break;
+          }
+          acc += wk;
+        }
+        sm.c_star = cst;
+        sm.t_rem = T - acc;
+        sm.use_bonus = ub;
+      }
+    }
+    __syncthreads();
+
+    // ---- 6. the warp that holds chunk c_star finds the index in its staged chunk
+    if (gw == sm.c_star && gw < p.nchs) {
+      const int ub = sm.use_bonus;
+      const long long Tr = sm.t_rem;
+      // group j covers entries [lo + 128 j, lo + 128 j + 128): find the group, then the lane, then the entry
+      long long before = 0, t_in = Tr, g = 0;
+      int jstar = -1;
+#pragma unroll 2
+      for (int j = 0; j < kChunkVec; ++j) {
+        const int64_t i0 = lo + static_cast<int64_t>(j * 32 + lane) * 4;
+        const float4 a = pch[j * 32 + lane];
+        const float4 q = has_q ? qch[j * 32 + lane] : a;
+        long long gl = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          long long W, P;
+          draw_weights(f4(a, e), pr, has_q, f4(q, e), qr, si.excl, si.bonus, i0 + e, W, P);
+          gl += ub ? P : W;
+        }
+        long long tj = gl;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tj += __shfl_xor_sync(0xffffffffu, tj, o);
+        if (jstar < 0) {
+          if (before + tj > Tr) {
+            jstar = j;
+            t_in = Tr - before;
+            g = gl;
+          } else {
+            before += tj;
+          }
+        }
+      }
+      long long incl = g;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const long long ex = incl - g;
+      if (jstar >= 0 && g > 0 && ex <= t_in && t_in < incl) {
+        long long acc = ex;
+        int e_hit = 3;
+        const int64_t i0 = lo + static_cast<int64_t>(jstar * 32 + lane) * 4;
+        const float4 a = pch[jstar * 32 + lane];
+        const float4 q = has_q ? qch[jstar * 32 + lane] : a;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          long long W, P;
+          draw_weights(f4(a, e), pr, has_q, f4(q, e), qr, si.excl, si.bonus, i0 + e, W, P);
+          acc += ub ? P : W;
+          if (acc > t_in) {
+            e_hit = e;
+            break;
+          }
+        }
+        p.out_tok[static_cast<int64_t>(b) * (p.Dmax + 1) + si.a] = static_cast<int>(i0 + e_hit);
+      }
+    }
+    __syncthreads();
   }
+  cl_sync();                                        // no CTA leaves while a peer may still write to it
 }
 
 // ------------------------------------------------------------------ diagnostics
@@ -650,9 +792,8 @@ AcceptLayout accept_layout(const ssd_accept_args* a) {
   const int NRD = NR + (a->chain_blk >= 0 ? a->K : 0);
   L.NR = NR;
   L.NRD = NRD;
-  // a stats chunk is one 16-byte vector per thread per step: 8 x 256 vectors
-  const int64_t epv = (a->kind == SSD_LOGITS_BF16) ? 8 : 4;
-  L.chunk = static_cast<int64_t>(kVec) * kVocabThreads * epv;
+  // a stats piece is kPieceElems entries of one row
+  L.chunk = kPieceElems;
   L.nch = static_cast<int>((a->V + L.chunk - 1) / L.chunk);
   L.schunk = kSampleChunk;
   L.nchs = static_cast<int>((a->V + kSampleChunk - 1) / kSampleChunk);
@@ -662,12 +803,6 @@ AcceptLayout accept_layout(const ssd_accept_args* a) {
   off = round_up(off + static_cast<size_t>(a->B) * NRD * L.nch * sizeof(RowStat), 256);
   L.stat_off = off;
   off = round_up(off + static_cast<size_t>(a->B) * NRD * sizeof(RowStat), 256);
-  L.stop_off = off;
-  off = round_up(off + static_cast<size_t>(a->B) * sizeof(StopInfo), 256);
-  L.csum_off = off;
-  off = round_up(off + static_cast<size_t>(a->B) * L.nchs * 2 * sizeof(long long), 256);
-  L.cnt_off = off;
-  off = round_up(off + static_cast<size_t>(a->B) * sizeof(unsigned), 256);
   L.total = off;
   return L;
 }
@@ -684,10 +819,11 @@ int accept_validate(const ssd_accept_args* a) {
   const long long nrd = 1LL + static_cast<long long>(a->NB) * a->Dmax + (a->chain_blk >= 0 ? a->K : 0);
   if (nrd > kMaxRows) return SSD_ERR_UNSUPPORTED;
   {
-    const long long chunk = static_cast<long long>(kVec) * kVocabThreads * (a->kind == SSD_LOGITS_BF16 ? 8 : 4);
-    if (((a->V + chunk - 1) / chunk) * nrd * a->B >= (1LL << 31)) return SSD_ERR_UNSUPPORTED;
+    const long long chunk = kPieceElems;
+    if (((a->V + chunk - 1) / chunk) * nrd * a->B >= (1LL << 31) - (1LL << 20)) return SSD_ERR_UNSUPPORTED;
   }
   if (a->chain_blk >= 0 && (a->K < 1 || a->K > a->Dmax)) return SSD_ERR_INVALID;
+  if (a->mode == SSD_SAMPLE && (a->V + kSampleChunk - 1) / kSampleChunk > kMaxSampleChunks) return SSD_ERR_UNSUPPORTED;
   if (a->B == 0) return SSD_OK;
   if (!a->tgt || !a->blk_tok || !a->blk_len || !a->acc_len || !a->best_blk || !a->n_out || !a->out_tok)
     return SSD_ERR_INVALID;
@@ -715,55 +851,71 @@ AcceptParams accept_params(const ssd_accept_args* a, const AcceptLayout& L, char
   p.hdr = reinterpret_cast<WsHeader*>(base);
   p.part = reinterpret_cast<RowStat*>(base + L.part_off);
   p.stat = reinterpret_cast<RowStat*>(base + L.stat_off);
-  p.stop = reinterpret_cast<StopInfo*>(base + L.stop_off);
-  p.csum = reinterpret_cast<long long*>(base + L.csum_off);
-  p.cnt = reinterpret_cast<unsigned*>(base + L.cnt_off);
   return p;
 }
 
-// resident CTAs of the stats kernel on the whole device (persistent grid)
-static long long stats_grid_cap(bool bf16) {
-  static long long cap[2] = {0, 0};
-  static std::mutex mu;
-  std::lock_guard<std::mutex> lock(mu);
-  long long& c = cap[bf16 ? 1 : 0];
-  if (c == 0) {
+// the stats kernel: a grid of as many CTAs as are resident at once
+template <bool BF16, bool AMAX>
+static cudaError_t launch_stats(const AcceptParams& p, cudaStream_t s) {
+  static std::once_flag once;
+  static long long cap = 0;
+  std::call_once(once, [] {
     int dev = 0, sms = 152, per = 1;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (bf16) cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, k_vocab_stats<true>, kVocabThreads, 0);
-    else cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, k_vocab_stats<false>, kVocabThreads, 0);
-    c = static_cast<long long>(sms) * (per > 0 ? per : 1);
-  }
-  return c;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, k_vocab_stats<BF16, AMAX>, kStatsThreads, 0) !=
+        cudaSuccess)
+      per = 1;
+    cap = static_cast<long long>(sms) * (per > 0 ? per : 1);
+  });
+  const long long ntask = static_cast<long long>(p.nch) * p.NRD * p.B;
+  const long long want = (ntask + kStatsWarps - 1) / kStatsWarps;
+  const dim3 g1(static_cast<unsigned>(want < cap ? want : cap));
+  return launch_pdl(k_vocab_stats<BF16, AMAX>, g1, dim3(kStatsThreads), 0, s, p);
 }
 
 int accept_launch(const AcceptParams& p, cudaStream_t s) {
   const unsigned by = static_cast<unsigned>(p.B < 65535 ? p.B : 65535);
   cudaError_t e;
   {
-    // statistics of every needed row; the last CTA of each sequence runs the select
-    const long long ntask = static_cast<long long>(p.nch) * p.NRD * p.B;
-    const long long cap = stats_grid_cap(p.bf16 != 0);
-    const dim3 g1(static_cast<unsigned>(ntask < cap ? ntask : cap));
+    // statistics of every needed row (the argmax only where greedy decisions need it)
     KernelTimer t(SSD_KERNEL_VOCAB_STATS, s);
-    e = p.bf16 ? launch_pdl(k_vocab_stats<true>, g1, dim3(kVocabThreads), 0, s, p)
-               : launch_pdl(k_vocab_stats<false>, g1, dim3(kVocabThreads), 0, s, p);
+    const bool amax = !p.sample;
+    e = p.bf16 ? (amax ? launch_stats<true, true>(p, s) : launch_stats<true, false>(p, s))
+               : (amax ? launch_stats<false, true>(p, s) : launch_stats<false, false>(p, s));
     if (e != cudaSuccess) return SSD_ERR_CUDA;
   }
   {
-    KernelTimer t(SSD_KERNEL_ACCEPT_SELECT, s);
-    const unsigned gb = static_cast<unsigned>(p.B < 1048576 ? p.B : 1048576);
-    e = launch_pdl(k_accept_select, dim3(gb), dim3(kSelectThreads), 0, s, p);
+    // merge, acceptance, choice and final draw: one cluster per sequence, with a warp
+    // for every chunk of the stop row (8 CTAs up to 64 chunks, else 16)
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+      attr_err = cudaFuncSetAttribute(k_accept_finish, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(kFinDynSmem));
+      if (attr_err == cudaSuccess)
+        attr_err = cudaFuncSetAttribute(k_accept_finish, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    });
+    if (attr_err != cudaSuccess) return SSD_ERR_CUDA;
+    const unsigned C = (!p.sample || p.nchs <= kFinCTAs * kFinWarps) ? kFinCTAs : kMaxFinCTAs;
+    KernelTimer t(SSD_KERNEL_ACCEPT_FINISH, s);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C, by, 1);
+    cfg.blockDim = dim3(kFinThreads);
+    cfg.dynamicSmemBytes = kFinDynSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, k_accept_finish, p);
     if (e != cudaSuccess) return SSD_ERR_CUDA;
   }
   int n = 2;
-  if (p.sample) {
-    const dim3 g3(static_cast<unsigned>(p.nchs), by);
-    KernelTimer t(SSD_KERNEL_SAMPLE_FINAL, s);
-    e = launch_pdl(k_sample_final, g3, dim3(kVocabThreads), 0, s, p);
-    if (e != cudaSuccess) return SSD_ERR_CUDA;
-    ++n;
-  }
   if (p.probs_out != nullptr) {
     const dim3 g4(static_cast<unsigned>(p.nch * p.NR), by);
     e = launch_pdl(k_probs_out, g4, dim3(kVocabThreads), 0, s, p);

@@ -45,16 +45,13 @@ struct AcceptParams {
   int64_t chunk, schunk;
   WsHeader* hdr;
   RowStat* part;      // [B][NRD][nch]
-  RowStat* stat;      // [B][NRD]
-  StopInfo* stop;     // [B]
-  long long* csum;    // [B][nchs][2]
-  unsigned* cnt;      // [B] sampler completion counters (set by the select)
+  RowStat* stat;      // [B][NRD] merged rows (read by the diagnostic copy of p)
 };
 
 struct AcceptLayout {
   int NR, NRD, nch, nchs;
   int64_t chunk, schunk;
-  size_t part_off, stat_off, stop_off, csum_off, cnt_off, total;
+  size_t part_off, stat_off, total;
 };
 
 __device__ __forceinline__ bool aligned_dev(const void* p, unsigned a) {

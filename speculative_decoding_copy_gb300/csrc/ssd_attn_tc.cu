@@ -270,6 +270,55 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return r;
 }
 
+// Softmax pieces on 64 columns of one row's S in TMEM. MASK: only columns in
+// [lo, hi) (relative to the chunk) count; the others act as -inf.
+template <bool MASK>
+__device__ __forceinline__ float chunk_max(uint32_t taddr, int lo, int hi) {
+  uint32_t v[64];
+  tmem_ld32(taddr, v);
+  tmem_ld32(taddr + 32, v + 32);
+  tmem_wait_ld();
+  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int c = 0; c < 64; ++c) {
+    const float x = __uint_as_float(v[c]);
+    if (!MASK || (c >= lo && c < hi)) m4[c & 3] = fmaxf(m4[c & 3], x);
+  }
+  return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+}
+
+// p = 2^(s*sl2 - mref) rounded to bf16, stored as 32 bf16 pairs at `paddr`;
+// returns the sum of the rounded values (what the P V product multiplies).
+template <bool MASK>
+__device__ __forceinline__ float chunk_exp(uint32_t saddr, uint32_t paddr, int lo, int hi, float sl2, float mref) {
+  uint32_t v[64];
+  tmem_ld32(saddr, v);
+  tmem_ld32(saddr + 32, v + 32);
+  tmem_wait_ld();
+  uint32_t pk[32];
+  float rs[4] = {0.f, 0.f, 0.f, 0.f};
+  if (mref > -INFINITY) {
+#pragma unroll
+    for (int c = 0; c < 64; c += 2) {
+      float p0 = ex2_approx(fmaf(__uint_as_float(v[c]), sl2, -mref));
+      float p1 = ex2_approx(fmaf(__uint_as_float(v[c + 1]), sl2, -mref));
+      if (MASK) {
+        if (c < lo || c >= hi) p0 = 0.f;
+        if (c + 1 < lo || c + 1 >= hi) p1 = 0.f;
+      }
+      const uint32_t w = pack_bf16(p0, p1);
+      pk[c / 2] = w;
+      rs[(c >> 1) & 1] += __uint_as_float(w << 16);
+      rs[2 + ((c >> 1) & 1)] += __uint_as_float(w & 0xffff0000u);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 32; ++c) pk[c] = 0u;       // no allowed key yet in this row
+  }
+  tmem_st32(paddr, pk);
+  return (rs[0] + rs[1]) + (rs[2] + rs[3]);
+}
+
 // ------------------------------------------------------------------ kernel
 constexpr int kMaxSplit = 8;              // cluster size limit (portable)
 constexpr int kRowF = 132;                // fp32 per merged row: O (128), max, sum, padding to 16 bytes
@@ -354,12 +403,6 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
       const int sb = j & 1;
       mbar_wait(bars, &bars.s_full[sb], (j >> 1) & 1, p.hdr, 10);
       tc_fence_after();
-      uint32_t sreg[BN];
-#pragma unroll
-      for (int q = 0; q < BN / 32; ++q) tmem_ld32(tmem + TM_S + sb * BN + lane_off + q * 32, sreg + q * 32);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&bars.s_free[sb]);
       // valid columns: a contiguous range [v_lo, v_hi) of this tile
       int v_lo, v_hi;
       if (j < nC) {                                   // own-block keys: slots c_lo .. t
@@ -370,44 +413,39 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
         v_lo = 0;
         v_hi = k1 - (k0 + (j - nC) * BN);
       }
-      if (v_lo > 0 || v_hi < BN) {
-#pragma unroll
-        for (int c = 0; c < BN; ++c)
-          if (c < v_lo || c >= v_hi) sreg[c] = __float_as_uint(-INFINITY);
-      }
-      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int c = 0; c < BN; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], __uint_as_float(sreg[c]));
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      const bool full = v_lo <= 0 && v_hi >= BN;
+      const uint32_t sc = tmem + TM_S + sb * BN + lane_off;
+      // pass 1: row max over the allowed columns
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int h = 0; h < BN / 64; ++h)
+        mx = fmaxf(mx, full ? chunk_max<false>(sc + h * 64, 0, 0) : chunk_max<true>(sc + h * 64, v_lo - h * 64, v_hi - h * 64));
       // reference max only moves when the row max grows by more than 2^8
       const float m_new = fmaxf(m, mx * sl2);
       const bool need = m_new > m + 8.f;
       const float mref = need ? m_new : m;
       const float alpha = need ? ex2_approx(m - m_new) : 1.f;
-      uint32_t pk[BN / 2];
-      float rs[4] = {0.f, 0.f, 0.f, 0.f};
-      if (mref > -INFINITY) {
-#pragma unroll
-        for (int c = 0; c < BN; c += 2) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sreg[c]), sl2, -mref));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sreg[c + 1]), sl2, -mref));
-          const uint32_t w = pack_bf16(p0, p1);
-          pk[c / 2] = w;
-          // sum the rounded values the MMA uses, so numerator and denominator agree
-          rs[(c >> 1) & 1] += __uint_as_float(w << 16);
-          rs[2 + ((c >> 1) & 1)] += __uint_as_float(w & 0xffff0000u);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < BN / 2; ++c) pk[c] = 0u;   // no allowed key yet in this row
+      // P buffer sb was last read by the P V product of tile j-2
+      if (j >= 2) {
+        mbar_wait(bars, &bars.pv_done[sb], ((j - 2) >> 1) & 1, p.hdr, 12);
+        tc_fence_after();
       }
+      // pass 2: P = 2^(s*scale - mref) as bf16 pairs into TMEM, and its row sum
+      const uint32_t pc = tmem + TM_P + sb * (BN / 2) + lane_off;
+      float rs = 0.f;
+#pragma unroll 1
+      for (int h = 0; h < BN / 64; ++h)
+        rs += full ? chunk_exp<false>(sc + h * 64, pc + h * 32, 0, 0, sl2, mref)
+                   : chunk_exp<true>(sc + h * 64, pc + h * 32, v_lo - h * 64, v_hi - h * 64, sl2, mref);
+      tc_fence_before();
+      mbar_arrive(&bars.s_free[sb]);                 // S of this tile is no longer read
       if (j > 0 && __any_sync(0xffffffffu, need)) {
         // O holds the sum up to tile j-1: wait for its last MMA, then rescale
         mbar_wait(bars, &bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, p.hdr, 11);
         tc_fence_after();
-        uint32_t o[32];
-#pragma unroll
+#pragma unroll 1
         for (int q = 0; q < DH / 32; ++q) {
+          uint32_t o[32];
           tmem_ld32(tmem + TM_O + lane_off + q * 32, o);
           tmem_wait_ld();
 #pragma unroll
@@ -415,15 +453,8 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
           tmem_st32(tmem + TM_O + lane_off + q * 32, o);
         }
       }
-      l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+      l = l * alpha + rs;
       m = mref;
-      // P buffer sb was last read by the P V product of tile j-2
-      if (j >= 2) {
-        mbar_wait(bars, &bars.pv_done[sb], ((j - 2) >> 1) & 1, p.hdr, 12);
-        tc_fence_after();
-      }
-      tmem_st32(tmem + TM_P + sb * (BN / 2) + lane_off, pk);
-      tmem_st32(tmem + TM_P + sb * (BN / 2) + lane_off + 32, pk + 32);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars.p_full[sb]);
