@@ -273,12 +273,15 @@ constexpr int kFinThreads = 1024;
 constexpr int kFinWarps = kFinThreads / 32;
 constexpr int kSlotsPer = kMaxSlots / kFinThreads;
 constexpr int kMaxSampleChunks = kMaxFinCTAs * kFinWarps;   // one chunk per warp of the cluster
-constexpr int kChunkVec = kSampleChunk / 4 / 32;            // float4 per lane per chunk
+constexpr int kLaneEntries = kSampleChunk / 32;             // contiguous entries per lane per chunk
+constexpr int kChunkVec = kLaneEntries / 4;                  // float4 per lane per chunk
 constexpr size_t kFinDynSmem = 2ull * kFinWarps * kSampleChunk * sizeof(float);
 
 struct __align__(16) FinishSmem {
   RowStat st[kMaxRows];                     // merged rows (rank 0 receives them)
-  long long csum[kMaxSampleChunks][2];      // chunk sums of the residual and bonus weights (every rank)
+  long long wsum[kFinWarps][2];             // residual and bonus weight sums of this CTA's chunks
+  long long lsum[kFinWarps][32][2];         // ... of every lane's entries
+  long long ctasum[kMaxFinCTAs][2];         // ... of every rank's chunks
   StopInfo si;                              // the stop row (rank 0 sends it to every rank)
   int tok_s[kMaxSlots];                     // candidate tokens (rank 0)
   int len_s[256];
@@ -311,6 +314,16 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)
                : "memory");
+}
+
+// row_needed with the (clamped) block lengths in shared memory
+__device__ __forceinline__ bool row_needed_s(const AcceptParams& p, const int* len_s, int r) {
+  if (r == 0) return true;
+  if (r < p.NR) {
+    const int sl = r - 1, k = sl / p.Dmax;
+    return sl - k * p.Dmax < len_s[k];
+  }
+  return p.chain_blk >= 0 && (r - p.NR) < len_s[p.chain_blk];
 }
 
 __device__ __forceinline__ RowStat warp_merge_stat(float M, float S, float av, int ai) {
@@ -355,78 +368,76 @@ __device__ __forceinline__ void merge_rows(const AcceptParams& p, int b, int ra,
 }
 
 
-// The weights with the row statistics folded in once: p = 2^(v log2 e - m log2 e) * (1/Z)
-// exactly as prob_of forms it, then P = floor(p 2^40) from the bits of p (weight_of).
+// The weights of the final draw with the row statistics folded in once. p is formed
+// exactly as prob_of forms it (2^(v log2 e - m log2 e) * (1/Z)), with the power of two
+// 2^20 folded into 1/Z, which scales the rounded product exactly. P = floor(p 2^40) is
+// then built in fp32 as hi 2^20 + lo with hi = floor(y), lo = floor((y - hi) 2^20) for
+// y = p 2^20: each floor is the low bits of y + 2^23 added with rounding toward zero,
+// and every step is exact for 0 <= y < 2^23 (p < 8; a probability is at most 1).
 struct DrawRow {
   float c;      // -m log2 e
-  float inv;    // 1/Z (round to nearest)
+  float inv20;  // (1/Z rounded to nearest) * 2^20
   int probs;
 };
 __device__ __forceinline__ DrawRow draw_row(const RowStat& st, int probs) {
-  return DrawRow{-st.m * kLog2e, __frcp_rn(st.s), probs};
+  return DrawRow{-st.m * kLog2e, __frcp_rn(st.s) * 1048576.0f, probs};
 }
-__device__ __forceinline__ long long weight_fast(float v, const DrawRow& r) {
-  return weight_of(r.probs ? v : ex2_approx(fmaf(v, kLog2e, r.c)) * r.inv);
+struct Split {
+  uint32_t hi, lo;      // P = hi 2^20 + lo
+};
+__device__ __forceinline__ Split weight_split(float v, const DrawRow& r) {
+  float y = r.probs ? v * 1048576.0f : ex2_approx(fmaf(v, kLog2e, r.c)) * r.inv20;
+  y = fminf(fmaxf(y, 0.f), 8388607.0f);
+  const float t1 = __fadd_rz(y, 8388608.0f);           // 2^23 + floor(y)
+  const float f = y + (8388608.0f - t1);               // y - floor(y)
+  const float t2 = __fadd_rz(f * 1048576.0f, 8388608.0f);
+  return Split{__float_as_uint(t1) - 0x4B000000u, __float_as_uint(t2) - 0x4B000000u};
 }
-// residual weight W = max(0, P - Q) (Q one-hot at excl for a copy block, from the draft
-// row for the chain block) and bonus weight P of entry i
-__device__ __forceinline__ void draw_weights(float pv, const DrawRow& pr, bool has_q, float qv, const DrawRow& qr,
-                                             int excl, int bonus, int64_t i, long long& W, long long& P) {
-  P = weight_fast(pv, pr);
-  if (bonus) {
-    W = P;
-  } else if (has_q) {
-    const long long Q = weight_fast(qv, qr);
-    W = P > Q ? P - Q : 0LL;
-  } else {
-    W = (i == excl) ? (P > kOneWeight ? P - kOneWeight : 0LL) : P;
-  }
+__device__ __forceinline__ long long split64(const Split& w) {
+  return (static_cast<long long>(w.hi) << 20) + static_cast<long long>(w.lo);
+}
+// the weight the draw uses at entry i: P (bonus) or the residual max(0, P - Q), with Q
+// one-hot at excl for a copy block or from the draft row for the chain block
+__device__ __forceinline__ long long draw_weight(float pv, const DrawRow& pr, bool has_q, float qv,
+                                                 const DrawRow& qr, int excl, int ub, int64_t i) {
+  const long long P = split64(weight_split(pv, pr));
+  if (ub) return P;
+  const long long Q = has_q ? split64(weight_split(qv, qr)) : ((i == excl) ? kOneWeight : 0LL);
+  return P > Q ? P - Q : 0LL;
 }
 
 __device__ __forceinline__ float f4(const float4& v, int e) { return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w; }
 
-// chunk [lo, lo + kSampleChunk) of a row as this lane's kChunkVec groups of 4 entries
-// (entry lo + (j*32 + lane)*4 + e); entries past the row end are -inf (weight 0)
-template <int NJ = kChunkVec>
-__device__ __forceinline__ void load_chunk4(const AcceptParams& p, const void* row, int64_t lo, float4* v, int j0 = 0) {
+// this lane's entries [lo + lane*kLaneEntries, + kLaneEntries) of a row as kChunkVec float4
+// (entry k of the run is component k%4 of v[k/4]); entries past the row end are -inf
+__device__ __forceinline__ void load_lane_run(const AcceptParams& p, const void* row, int64_t lo, float4* v) {
   const int lane = threadIdx.x & 31;
-  const bool full = lo + kSampleChunk <= p.V;
-  if (!p.bf16 && full && ((p.V * 4) & 15) == 0 && aligned_dev(row, 16)) {
-    const float4* r4 = reinterpret_cast<const float4*>(static_cast<const float*>(row) + lo);
+  const int64_t l0 = lo + static_cast<int64_t>(lane) * kLaneEntries;
+  if (!p.bf16 && l0 + kLaneEntries <= p.V && ((p.V * 4) & 15) == 0 && aligned_dev(row, 16)) {
+    const float4* r4 = reinterpret_cast<const float4*>(static_cast<const float*>(row) + l0);
 #pragma unroll
-    for (int j = 0; j < NJ; ++j) v[j] = __ldg(r4 + (j0 + j) * 32 + lane);
-  } else if (p.bf16 && full && ((p.V * 2) & 7) == 0 && aligned_dev(row, 8)) {
-    const uint2* r2 = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(row) + lo);
+    for (int j = 0; j < kChunkVec; ++j) v[j] = __ldg(r4 + j);
+  } else if (p.bf16 && l0 + kLaneEntries <= p.V && ((p.V * 2) & 15) == 0 && aligned_dev(row, 16)) {
+    const uint4* r2 = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(row) + l0);
 #pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      const uint2 w = __ldg(r2 + (j0 + j) * 32 + lane);
-      v[j] = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u), __uint_as_float(w.y << 16),
-                         __uint_as_float(w.y & 0xffff0000u));
+    for (int j = 0; j < kChunkVec / 2; ++j) {
+      const uint4 w = __ldg(r2 + j);
+      v[2 * j] = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                             __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+      v[2 * j + 1] = make_float4(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u),
+                                 __uint_as_float(w.w << 16), __uint_as_float(w.w & 0xffff0000u));
     }
   } else {
 #pragma unroll
-    for (int j = 0; j < NJ; ++j) {
+    for (int j = 0; j < kChunkVec; ++j) {
       float x[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int64_t i = lo + static_cast<int64_t>((j0 + j) * 32 + lane) * 4 + e;
+        const int64_t i = l0 + j * 4 + e;
         x[e] = i < p.V ? load_val(row, i, p.bf16) : -INFINITY;
       }
       v[j] = make_float4(x[0], x[1], x[2], x[3]);
     }
-  }
-}
-
-// chunk [lo, lo + kSampleChunk) of a row into shared memory as fp32, entry lo + k at dst[k]
-__device__ __forceinline__ void stage_chunk(const AcceptParams& p, const void* row, int64_t lo, float4* dst) {
-  const int lane = threadIdx.x & 31;
-  constexpr int H = kChunkVec / 2;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    float4 v[H];
-    load_chunk4<H>(p, row, lo, v, h * H);
-#pragma unroll
-    for (int j = 0; j < H; ++j) dst[(h * H + j) * 32 + lane] = v[j];
   }
 }
 
@@ -482,13 +493,13 @@ k_accept_finish(AcceptParams p) {
           }
         }
       }
-      for (int k = tid; k < p.NB; k += kFinThreads) {
-        const int raw = p.blk_len[b * p.NB + k];
-        const int cap = (k == p.chain_blk) ? min(p.Dmax, p.K) : p.Dmax;
-        const int L = min(max(raw, 0), cap);
-        if (L != raw) record_error(p.hdr, SSD_ERR_DEVICE, 101);
-        sm.len_s[k] = L;
-      }
+    }
+    for (int k = tid; k < p.NB; k += kFinThreads) {     // every rank: the block lengths
+      const int raw = p.blk_len[b * p.NB + k];
+      const int cap = (k == p.chain_blk) ? min(p.Dmax, p.K) : p.Dmax;
+      const int L = min(max(raw, 0), cap);
+      if (rank == 0 && L != raw) record_error(p.hdr, SSD_ERR_DEVICE, 101);
+      sm.len_s[k] = L;
     }
     cl_sync();                                        // every CTA runs: peers' shared memory may be written
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the piece statistics are complete
@@ -498,7 +509,7 @@ k_accept_finish(AcceptParams p) {
       const int gw = static_cast<int>(rank) * kFinWarps + warp, nw = C * kFinWarps;
       for (int r = gw; r < p.NRD; r += 2 * nw) {
         const int r2 = r + nw;
-        const bool na = row_needed(p, b, r), nb = r2 < p.NRD && row_needed(p, b, r2);
+        const bool na = row_needed_s(p, sm.len_s, r), nb = r2 < p.NRD && row_needed_s(p, sm.len_s, r2);
         if (!na && !nb) continue;
         RowStat xa, xb;
         merge_rows(p, b, na ? r : r2, (na && nb) ? r2 : -1, xa, xb);
@@ -612,8 +623,9 @@ k_accept_finish(AcceptParams p) {
     cl_sync();
     if (!p.sample) continue;
 
-    // ---- 4. warp gw holds chunk gw of the stop row in registers (entry lo + (j*32 + lane)*4 + e)
-    //         and sends its residual and bonus weight sums to every rank
+    // ---- 4. warp gw stages chunk gw of the stop row in shared memory (lane l: entries
+    //         [16 l, 16 l + 16) of the chunk) and sums the bonus weights P and residual
+    //         weights W per lane and per warp; the CTA's totals go to every rank
     const StopInfo si = sm.si;
     const void* prow = row_ptr(p, b, si.row);
     const bool has_q = si.drf_row >= 0;
@@ -621,48 +633,76 @@ k_accept_finish(AcceptParams p) {
     const DrawRow pr = draw_row(si.ps, p.probs), qr = draw_row(si.qs, p.probs);
     const int gw = static_cast<int>(rank) * kFinWarps + warp;
     const int64_t lo = static_cast<int64_t>(gw) * kSampleChunk;
-    float4* pch = fin_chunk + warp * (kSampleChunk / 4);                   // this warp's chunk of p
-    float4* qch = fin_chunk + (kFinWarps + warp) * (kSampleChunk / 4);     // ... and of q
-    if (gw < p.nchs) {
-      stage_chunk(p, prow, lo, pch);
-      if (has_q) stage_chunk(p, qrow, lo, qch);
-      __syncwarp();
+    const int64_t l0 = lo + static_cast<int64_t>(lane) * kLaneEntries;   // this lane's first entry
+    float* pf = reinterpret_cast<float*>(fin_chunk + warp * (kSampleChunk / 4)) + lane * kLaneEntries;
+    float* qf = reinterpret_cast<float*>(fin_chunk + (kFinWarps + warp) * (kSampleChunk / 4)) + lane * kLaneEntries;
+    {
       long long sw = 0, sp = 0;
-#pragma unroll 2
-      for (int j = 0; j < kChunkVec; ++j) {
-        const int64_t i0 = lo + static_cast<int64_t>(j * 32 + lane) * 4;
-        const float4 a = pch[j * 32 + lane];
-        const float4 q = has_q ? qch[j * 32 + lane] : a;
+      if (gw < p.nchs) {
+        float4 a[kChunkVec];
+        load_lane_run(p, prow, lo, a);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          long long W, P;
-          draw_weights(f4(a, e), pr, has_q, f4(q, e), qr, si.excl, si.bonus, i0 + e, W, P);
-          sw += W;
-          sp += P;
+        for (int j = 0; j < kChunkVec; ++j) reinterpret_cast<float4*>(pf)[j] = a[j];
+        uint32_t shi = 0, slo = 0;
+#pragma unroll
+        for (int j = 0; j < kChunkVec; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const Split w = weight_split(f4(a[j], e), pr);
+            shi += w.hi;
+            slo += w.lo;
+          }
+        sp = (static_cast<long long>(shi) << 20) + static_cast<long long>(slo);
+        if (si.bonus) {
+          sw = sp;
+        } else if (has_q) {
+          float4 q[kChunkVec];
+          load_lane_run(p, qrow, lo, q);
+#pragma unroll
+          for (int j = 0; j < kChunkVec; ++j) {
+            reinterpret_cast<float4*>(qf)[j] = q[j];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const long long P = split64(weight_split(f4(a[j], e), pr));
+              const long long Q = split64(weight_split(f4(q[j], e), qr));
+              sw += P > Q ? P - Q : 0LL;
+            }
+          }
+        } else {
+          // a rejected copy token: W = P everywhere but there, where Q = 2^40
+          sw = sp;
+          const int64_t xl = static_cast<int64_t>(si.excl) - l0;
+          if (xl >= 0 && xl < kLaneEntries) {
+            const long long Pe = split64(weight_split(pf[xl], pr));
+            sw = sp - Pe + (Pe > kOneWeight ? Pe - kOneWeight : 0LL);
+          }
         }
       }
+      sm.lsum[warp][lane][0] = sw;
+      sm.lsum[warp][lane][1] = sp;
       sw = warp_sum(sw);
       sp = warp_sum(sp);
+      if (lane == 0) {
+        sm.wsum[warp][0] = sw;
+        sm.wsum[warp][1] = sp;
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      long long tw = sm.wsum[lane][0], tp = sm.wsum[lane][1];
+      tw = warp_sum(tw);
+      tp = warp_sum(tp);
       if (lane < C) {
-        const uint32_t dst = cl_map(&sm.csum[gw][0], static_cast<uint32_t>(lane));
-        asm volatile("st.shared::cluster.v2.b64 [%0], {%1, %2};" ::"r"(dst), "l"(sw), "l"(sp) : "memory");
+        const uint32_t dst = cl_map(&sm.ctasum[rank][0], static_cast<uint32_t>(lane));
+        asm volatile("st.shared::cluster.v2.b64 [%0], {%1, %2};" ::"r"(dst), "l"(tw), "l"(tp) : "memory");
       }
     }
     cl_sync();
 
-    // ---- 5. (warp 0 of every rank) S, the threshold T = floor(U S / 2^24) and the chunk holding it
+    // ---- 5. (warp 0) S, the threshold T = floor(U S / 2^24), the CTA and then the warp that hold it
     if (warp == 0) {
-      constexpr int kPerLane = kMaxSampleChunks / 32;
-      long long aw = 0, ap = 0;
-#pragma unroll
-      for (int k = 0; k < kPerLane; ++k) {
-        const int c = lane * kPerLane + k;
-        if (c < p.nchs) {
-          aw += sm.csum[c][0];
-          ap += sm.csum[c][1];
-        }
-      }
-      long long iw = aw, ip = ap;
+      const long long cw = lane < C ? sm.ctasum[lane][0] : 0, cp = lane < C ? sm.ctasum[lane][1] : 0;
+      long long iw = cw, ip = cp;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const long long yw = __shfl_up_sync(0xffffffffu, iw, o);
@@ -678,89 +718,59 @@ k_accept_finish(AcceptParams p) {
       const float u = fminf(fmaxf(p.u_fin[b], 0.f), 0.99999994f);               // contract: u in [0, 1)
       const unsigned long long U = static_cast<unsigned long long>(u * 16777216.0f);   // floor(u 2^24), exact
       const long long T = static_cast<long long>((__umul64hi(U, S) << 40) | ((U * S) >> 24));
-      const long long mine = ub ? ap : aw, ex = (ub ? ip : iw) - mine;
-      if (lane == 0) {            // defaults if no weight is positive (degenerate rows)
-        sm.c_star = 0;
-        sm.t_rem = 0;
-        sm.use_bonus = 1;
-      }
-      __syncwarp();
-      if (mine > 0 && ex <= T && T < ex + mine) {
-        long long acc = ex;
-        int cst = min(p.nchs, (lane + 1) * kPerLane) - 1;
-        for (int k = 0; k < kPerLane; ++k) {
-          const int c = lane * kPerLane + k;
-          if (c >= p.nchs) break;
-          const long long wk = sm.csum[c][ub];
-          if (acc + wk > T) {
-            cst = c;
-            break;
-          }
-          acc += wk;
+      const long long mc = ub ? cp : cw, ec = (ub ? ip : iw) - mc;
+      const unsigned hitc = __ballot_sync(0xffffffffu, mc > 0 && ec <= T && T < ec + mc);
+      int ow = -1;
+      long long t2 = 0;
+      if (hitc != 0u && static_cast<int>(rank) == __ffs(hitc) - 1) {
+        const long long t1 = T - __shfl_sync(0xffffffffu, ec, __ffs(hitc) - 1);
+        const long long mw = sm.wsum[lane][ub];
+        long long iw2 = mw;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const long long y = __shfl_up_sync(0xffffffffu, iw2, o);
+          if (lane >= o) iw2 += y;
         }
-        sm.c_star = cst;
-        sm.t_rem = T - acc;
+        const long long ew2 = iw2 - mw;
+        const unsigned hitw = __ballot_sync(0xffffffffu, mw > 0 && ew2 <= t1 && t1 < iw2);
+        if (hitw != 0u) {
+          ow = __ffs(hitw) - 1;
+          t2 = t1 - __shfl_sync(0xffffffffu, ew2, ow);
+        }
+      }
+      if (lane == 0) {
+        sm.c_star = ow;
+        sm.t_rem = t2;
         sm.use_bonus = ub;
       }
     }
     __syncthreads();
 
-    // ---- 6. the warp that holds chunk c_star finds the index in its staged chunk
-    if (gw == sm.c_star && gw < p.nchs) {
+    // ---- 6. the warp that holds the threshold: the lane by one scan of its lane sums,
+    //         then that lane walks its 16 staged entries
+    if (warp == sm.c_star && gw < p.nchs) {
       const int ub = sm.use_bonus;
       const long long Tr = sm.t_rem;
-      // group j covers entries [lo + 128 j, lo + 128 j + 128): find the group, then the lane, then the entry
-      long long before = 0, t_in = Tr, g = 0;
-      int jstar = -1;
-#pragma unroll 2
-      for (int j = 0; j < kChunkVec; ++j) {
-        const int64_t i0 = lo + static_cast<int64_t>(j * 32 + lane) * 4;
-        const float4 a = pch[j * 32 + lane];
-        const float4 q = has_q ? qch[j * 32 + lane] : a;
-        long long gl = 0;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          long long W, P;
-          draw_weights(f4(a, e), pr, has_q, f4(q, e), qr, si.excl, si.bonus, i0 + e, W, P);
-          gl += ub ? P : W;
-        }
-        long long tj = gl;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) tj += __shfl_xor_sync(0xffffffffu, tj, o);
-        if (jstar < 0) {
-          if (before + tj > Tr) {
-            jstar = j;
-            t_in = Tr - before;
-            g = gl;
-          } else {
-            before += tj;
-          }
-        }
-      }
-      long long incl = g;
+      const long long mine = sm.lsum[warp][lane][ub];
+      long long incl = mine;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const long long y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
       }
-      const long long ex = incl - g;
-      if (jstar >= 0 && g > 0 && ex <= t_in && t_in < incl) {
+      const long long ex = incl - mine;
+      const unsigned hit = __ballot_sync(0xffffffffu, mine > 0 && ex <= Tr && Tr < incl);
+      if (hit != 0u && lane == __ffs(hit) - 1) {
         long long acc = ex;
-        int e_hit = 3;
-        const int64_t i0 = lo + static_cast<int64_t>(jstar * 32 + lane) * 4;
-        const float4 a = pch[jstar * 32 + lane];
-        const float4 q = has_q ? qch[jstar * 32 + lane] : a;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          long long W, P;
-          draw_weights(f4(a, e), pr, has_q, f4(q, e), qr, si.excl, si.bonus, i0 + e, W, P);
-          acc += ub ? P : W;
-          if (acc > t_in) {
-            e_hit = e;
+        int k_hit = kLaneEntries - 1;
+        for (int k = 0; k < kLaneEntries; ++k) {
+          acc += draw_weight(pf[k], pr, has_q, has_q ? qf[k] : 0.f, qr, si.excl, ub, l0 + k);
+          if (acc > Tr) {
+            k_hit = k;
             break;
           }
         }
-        p.out_tok[static_cast<int64_t>(b) * (p.Dmax + 1) + si.a] = static_cast<int>(i0 + e_hit);
+        p.out_tok[static_cast<int64_t>(b) * (p.Dmax + 1) + si.a] = static_cast<int>(l0 + k_hit);
       }
     }
     __syncthreads();
