@@ -310,11 +310,6 @@ __device__ __forceinline__ uint32_t cl_map(const void* local, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(local)), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint4 v) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
-               : "memory");
-}
 
 // row_needed with the (clamped) block lengths in shared memory
 __device__ __forceinline__ bool row_needed_s(const AcceptParams& p, const int* len_s, int r) {
@@ -451,9 +446,11 @@ k_accept_finish(AcceptParams p) {
   const int nslots = p.NB * p.Dmax;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (int b = blockIdx.y; b < p.B; b += gridDim.y) {
-    // ---- 1. (rank 0) per token slot: token, block length, uniform and the logits the
-    //         test needs; none of it comes from the row pass, so it is loaded before
-    //         griddepcontrol.wait
+    // this CTA has started this sequence (its peers wait for that before writing to it)
+    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+    // ---- 1. per token slot: token, block length, uniform and the logits the test needs;
+    //         none of it comes from the row pass, so it is loaded before griddepcontrol.wait.
+    //         Every CTA of the cluster takes the same decisions from the same data.
     int x_[kSlotsPer], row_[kSlotsPer];
     bool live_[kSlotsPer];
     float lp_[kSlotsPer], lq_[kSlotsPer], u_[kSlotsPer];
@@ -465,146 +462,136 @@ k_accept_finish(AcceptParams p) {
       lp_[k] = 0.f;
       lq_[k] = 0.f;
       u_[k] = 0.f;
-    }
-    if (rank == 0) {
-#pragma unroll
-      for (int k = 0; k < kSlotsPer; ++k) {
-        const int sl = tid + k * kFinThreads;
-        if (sl < nslots) {
-          const int blk = sl / p.Dmax, d = sl % p.Dmax;
-          sm.tok_s[sl] = p.blk_tok[static_cast<int64_t>(b) * nslots + sl];
-          const int raw = p.blk_len[b * p.NB + blk];
-          const int cap = (blk == p.chain_blk) ? min(p.Dmax, p.K) : p.Dmax;
-          const int L = min(max(raw, 0), cap);
-          if (d < L) {
-            const int x = sm.tok_s[sl];
-            if (x < 0 || x >= p.V) {
-              record_error(p.hdr, SSD_ERR_DEVICE, 100);
-            } else {
-              live_[k] = true;
-              x_[k] = x;
-              row_[k] = d == 0 ? 0 : 1 + blk * p.Dmax + d - 1;
-              if (p.sample) {
-                lp_[k] = load_val(row_ptr(p, b, row_[k]), x, p.bf16);
-                if (blk == p.chain_blk) lq_[k] = load_val(row_ptr(p, b, p.NR + d), x, p.bf16);
-                u_[k] = p.u_acc[static_cast<int64_t>(b) * nslots + sl];
-              }
+      const int sl = tid + k * kFinThreads;
+      if (sl < nslots) {
+        const int blk = sl / p.Dmax, d = sl % p.Dmax;
+        sm.tok_s[sl] = p.blk_tok[static_cast<int64_t>(b) * nslots + sl];
+        const int raw = p.blk_len[b * p.NB + blk];
+        const int cap = (blk == p.chain_blk) ? min(p.Dmax, p.K) : p.Dmax;
+        const int L = min(max(raw, 0), cap);
+        if (d < L) {
+          const int x = sm.tok_s[sl];
+          if (x < 0 || x >= p.V) {
+            if (rank == 0) record_error(p.hdr, SSD_ERR_DEVICE, 100);
+          } else {
+            live_[k] = true;
+            x_[k] = x;
+            row_[k] = d == 0 ? 0 : 1 + blk * p.Dmax + d - 1;
+            if (p.sample) {
+              lp_[k] = load_val(row_ptr(p, b, row_[k]), x, p.bf16);
+              if (blk == p.chain_blk) lq_[k] = load_val(row_ptr(p, b, p.NR + d), x, p.bf16);
+              u_[k] = p.u_acc[static_cast<int64_t>(b) * nslots + sl];
             }
           }
         }
       }
     }
-    for (int k = tid; k < p.NB; k += kFinThreads) {     // every rank: the block lengths
+    for (int k = tid; k < p.NB; k += kFinThreads) {
       const int raw = p.blk_len[b * p.NB + k];
       const int cap = (k == p.chain_blk) ? min(p.Dmax, p.K) : p.Dmax;
       const int L = min(max(raw, 0), cap);
       if (rank == 0 && L != raw) record_error(p.hdr, SSD_ERR_DEVICE, 101);
       sm.len_s[k] = L;
     }
-    cl_sync();                                        // every CTA runs: peers' shared memory may be written
+    __syncthreads();
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the piece statistics are complete
 
-    // ---- 2. merge every needed row, one warp per row over the cluster; to rank 0
-    {
-      const int gw = static_cast<int>(rank) * kFinWarps + warp, nw = C * kFinWarps;
-      for (int r = gw; r < p.NRD; r += 2 * nw) {
-        const int r2 = r + nw;
-        const bool na = row_needed_s(p, sm.len_s, r), nb = r2 < p.NRD && row_needed_s(p, sm.len_s, r2);
-        if (!na && !nb) continue;
-        RowStat xa, xb;
-        merge_rows(p, b, na ? r : r2, (na && nb) ? r2 : -1, xa, xb);
-        if (lane == 0) {
-          const int rows[2] = {na ? r : r2, r2};
-          const RowStat xs[2] = {xa, xb};
-#pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            if (k == 1 && !(na && nb)) break;
-            const RowStat x = xs[k];
-            p.stat[static_cast<int64_t>(b) * p.NRD + rows[k]] = x;
-            st_cluster_v4(cl_map(&sm.st[rows[k]], 0),
-                          make_uint4(__float_as_uint(x.m), __float_as_uint(x.s), __float_as_uint(x.amax_v),
-                                     static_cast<uint32_t>(x.amax_i)));
-          }
+    // ---- 2. every needed row merged from its pieces, two rows per warp pass
+    for (int r = warp; r < p.NRD; r += 2 * kFinWarps) {
+      const int r2 = r + kFinWarps;
+      const bool na = row_needed_s(p, sm.len_s, r), nb = r2 < p.NRD && row_needed_s(p, sm.len_s, r2);
+      if (!na && !nb) continue;
+      RowStat xa, xb;
+      merge_rows(p, b, na ? r : r2, (na && nb) ? r2 : -1, xa, xb);
+      if (lane == 0) {
+        const int ra = na ? r : r2;
+        sm.st[ra] = xa;
+        if (rank == 0) p.stat[static_cast<int64_t>(b) * p.NRD + ra] = xa;
+        if (na && nb) {
+          sm.st[r2] = xb;
+          if (rank == 0) p.stat[static_cast<int64_t>(b) * p.NRD + r2] = xb;
         }
       }
     }
-    cl_sync();
+    __syncthreads();
 
-    // ---- 3. (rank 0) acceptance, leading runs, longest block, stop row
-    if (rank == 0) {
+    // ---- 3. acceptance, leading runs, longest block, stop row (outputs by rank 0)
 #pragma unroll
-      for (int k = 0; k < kSlotsPer; ++k) {
-        const int sl = tid + k * kFinThreads;
-        if (sl >= nslots) continue;
-        bool ok = false;
-        if (live_[k]) {
-          const int blk = sl / p.Dmax, d = sl % p.Dmax;
-          if (!p.sample) {
-            ok = (x_[k] == sm.st[row_[k]].amax_i);
-          } else {
-            const float px = prob_of(lp_[k], sm.st[row_[k]], p.probs);
-            const float qx = (blk == p.chain_blk) ? prob_of(lq_[k], sm.st[p.NR + d], p.probs) : 1.f;
-            ok = __dmul_rn(static_cast<double>(u_[k]), static_cast<double>(qx)) < static_cast<double>(px);
-          }
-        }
-        sm.ok_s[sl] = ok ? 1 : 0;
-      }
-      __syncthreads();
-      // leading accepted run of every block: one warp per block, the first rejection by ballot
-      for (int k = warp; k < p.NB; k += kFinWarps) {
-        const int L = sm.len_s[k];
-        int a = L;
-        for (int d0 = 0; d0 < L; d0 += 32) {
-          const int d = d0 + lane;
-          const unsigned rej = __ballot_sync(0xffffffffu, d < L && !sm.ok_s[k * p.Dmax + d]);
-          if (rej != 0u) {
-            a = d0 + __ffs(rej) - 1;
-            break;
-          }
-        }
-        if (lane == 0) {
-          sm.acc_s[k] = a;
-          p.acc_len[b * p.NB + k] = a;
+    for (int k = 0; k < kSlotsPer; ++k) {
+      const int sl = tid + k * kFinThreads;
+      if (sl >= nslots) continue;
+      bool ok = false;
+      if (live_[k]) {
+        const int blk = sl / p.Dmax, d = sl % p.Dmax;
+        if (!p.sample) {
+          ok = (x_[k] == sm.st[row_[k]].amax_i);
+        } else {
+          const float px = prob_of(lp_[k], sm.st[row_[k]], p.probs);
+          const float qx = (blk == p.chain_blk) ? prob_of(lq_[k], sm.st[p.NR + d], p.probs) : 1.f;
+          ok = __dmul_rn(static_cast<double>(u_[k]), static_cast<double>(qx)) < static_cast<double>(px);
         }
       }
-      __syncthreads();
-      if (tid == 0) {
-        // longest accepted run, lowest block index on ties
-        int best = -1, ba = -1;
-        for (int k = 0; k < p.NB; ++k) {
-          if (sm.len_s[k] > 0 && sm.acc_s[k] > ba) {
-            ba = sm.acc_s[k];
-            best = k;
-          }
+      sm.ok_s[sl] = ok ? 1 : 0;
+    }
+    __syncthreads();
+    // leading accepted run of every block: one warp per block, the first rejection by ballot
+    for (int k = warp; k < p.NB; k += kFinWarps) {
+      const int L = sm.len_s[k];
+      int a = L;
+      for (int d0 = 0; d0 < L; d0 += 32) {
+        const int d = d0 + lane;
+        const unsigned rej = __ballot_sync(0xffffffffu, d < L && !sm.ok_s[k * p.Dmax + d]);
+        if (rej != 0u) {
+          a = d0 + __ffs(rej) - 1;
+          break;
         }
-        const int a = best >= 0 ? ba : 0;
-        const int L = best >= 0 ? sm.len_s[best] : 0;
-        const int stop = a == 0 ? 0 : 1 + best * p.Dmax + a - 1;
-        sm.sel[0] = best;
-        sm.sel[1] = a;
-        sm.sel[3] = sm.st[stop].amax_i;
+      }
+      if (lane == 0) {
+        sm.acc_s[k] = a;
+        if (rank == 0) p.acc_len[b * p.NB + k] = a;
+      }
+    }
+    __syncthreads();
+    if (tid == 0) {
+      // longest accepted run, lowest block index on ties
+      int best = -1, ba = -1;
+      for (int k = 0; k < p.NB; ++k) {
+        if (sm.len_s[k] > 0 && sm.acc_s[k] > ba) {
+          ba = sm.acc_s[k];
+          best = k;
+        }
+      }
+      const int a = best >= 0 ? ba : 0;
+      const int L = best >= 0 ? sm.len_s[best] : 0;
+      const int stop = a == 0 ? 0 : 1 + best * p.Dmax + a - 1;
+      sm.sel[0] = best;
+      sm.sel[1] = a;
+      sm.sel[3] = sm.st[stop].amax_i;
+      if (rank == 0) {
         p.best_blk[b] = best;
         p.n_out[b] = a + 1;
-        StopInfo si;
-        si.row = stop;
-        si.ps = sm.st[stop];
-        si.a = a;
-        si.drf_row = -1;
-        si.excl = -1;
-        si.bonus = (a >= L) ? 1 : 0;
-        si.pad[0] = si.pad[1] = si.pad[2] = 0;
-        si.qs = si.ps;
-        if (a < L) {
-          if (best == p.chain_blk) {
-            si.drf_row = a;
-            si.qs = sm.st[p.NR + a];
-          } else {
-            si.excl = sm.tok_s[best * p.Dmax + a];
-          }
-        }
-        sm.si = si;
       }
-      __syncthreads();
+      StopInfo si;
+      si.row = stop;
+      si.ps = sm.st[stop];
+      si.a = a;
+      si.drf_row = -1;
+      si.excl = -1;
+      si.bonus = (a >= L) ? 1 : 0;
+      si.pad[0] = si.pad[1] = si.pad[2] = 0;
+      si.qs = si.ps;
+      if (a < L) {
+        if (best == p.chain_blk) {
+          si.drf_row = a;
+          si.qs = sm.st[p.NR + a];
+        } else {
+          si.excl = sm.tok_s[best * p.Dmax + a];
+        }
+      }
+      sm.si = si;
+    }
+    __syncthreads();
+    if (rank == 0) {
       // emitted tokens (the draw below fills the final one in sample mode)
       const int best = sm.sel[0], a = sm.sel[1];
       for (int i = tid; i <= p.Dmax; i += kFinThreads) {
@@ -613,15 +600,11 @@ k_accept_finish(AcceptParams p) {
         else if (i == a && !p.sample) v = sm.sel[3];
         p.out_tok[static_cast<int64_t>(b) * (p.Dmax + 1) + i] = v;
       }
-      // the stop row to every rank
-      if (p.sample && tid < C * 4) {
-        const uint4* src = reinterpret_cast<const uint4*>(&sm.si);
-        st_cluster_v4(cl_map(reinterpret_cast<const uint4*>(&sm.si) + (tid & 3), static_cast<uint32_t>(tid >> 2)),
-                      src[tid & 3]);
-      }
     }
-    cl_sync();
-    if (!p.sample) continue;
+    if (!p.sample) {
+      asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+      continue;
+    }
 
     // ---- 4. warp gw stages chunk gw of the stop row in shared memory (lane l: entries
     //         [16 l, 16 l + 16) of the chunk) and sums the bonus weights P and residual
@@ -688,6 +671,7 @@ k_accept_finish(AcceptParams p) {
       }
     }
     __syncthreads();
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");   // every peer has started: its memory may be written
     if (warp == 0) {
       long long tw = sm.wsum[lane][0], tp = sm.wsum[lane][1];
       tw = warp_sum(tw);
@@ -775,7 +759,7 @@ k_accept_finish(AcceptParams p) {
     }
     __syncthreads();
   }
-  cl_sync();                                        // no CTA leaves while a peer may still write to it
+  // no peer writes to this CTA after the last cluster barrier of its sequences
 }
 
 // ------------------------------------------------------------------ diagnostics
