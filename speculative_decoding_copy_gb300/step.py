@@ -1,11 +1,15 @@
 """One speculate-and-verify step on the GPU: device buffers for a batch and the
-launch order of the four C-ABI calls.
+launch order of the C-ABI calls.
 
-    gate_retrieve -> { verify_attn (aux stream) || accept (main stream) }
+    gate_retrieve -> accept (row pass, finish) -> verify_attn     (one stream)
+    gate_retrieve -> { verify_attn (aux stream) || accept }       (two streams)
 
-Verification attention and acceptance both depend only on the retrieval
-output, so with an auxiliary stream they run concurrently. The step issues
-only library calls; it computes nothing itself.
+Verification attention and acceptance both depend only on the retrieval output.
+On one stream the kernels are chained by programmatic dependent launch: the row
+pass streams the logits alone right after the retrieval, and the attention's main
+loop (which needs nothing from the acceptance) runs on the SMs the latency-bound
+finish kernel leaves free; it waits for its predecessors only before writing.
+The step issues only library calls; it computes nothing itself.
 """
 from __future__ import annotations
 
@@ -117,10 +121,12 @@ class VerifyStep:
             ev2.record(aux)
             main.wait_event(ev2)
         else:
-            if self.with_attention:
-                self.attention(main)
+            # one stream: the acceptance chain first (it needs only the retrieval's output),
+            # then the attention, whose main loop overlaps the latency-bound finish kernel
             if self.with_accept:
                 self.accept(main)
+            if self.with_attention:
+                self.attention(main)
 
     def results(self) -> dict:
         """Copy every output to host numpy arrays (synchronises)."""
