@@ -594,48 +594,67 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
     }
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
   }
-  // weights of the owned rows once every split has arrived
+  // weights of the owned rows once every split has arrived (one thread per row, the
+  // split loop unrolled so that every load is in flight together)
   if (tid < nr) {
     const bool ok = mbar_wait(bars, &bars.recv_full, 0, p.hdr, 40) && bars.live[tid];
-    float M = -INFINITY;
-    for (int c = 0; c < S; ++c) M = fmaxf(M, recv[(c * rpc + tid) * kRowF + DH]);
-    float L = 0.f;
-    for (int c = 0; c < S; ++c) {
-      const float mc = recv[(c * rpc + tid) * kRowF + DH];
-      const float f = mc > -INFINITY ? ex2_approx(mc - M) : 0.f;
-      fac[tid * kMaxSplit + c] = f;
-      L = fmaf(recv[(c * rpc + tid) * kRowF + DH + 1], f, L);
-    }
-    // a row with no allowed key is not a present token: weights 0, row skipped
-    const float inv = (ok && L > 0.f) ? 1.f / L : 0.f;
-    for (int c = 0; c < S; ++c) fac[tid * kMaxSplit + c] *= inv;
-    bars.live[tid] = (ok && L > 0.f) ? 1 : 0;
-  }
-  __syncthreads();
-  // one float4 of one owned row per item, the S partial loads in flight together
-  for (int it = tid; it < nr * (DH / 4); it += kThreads) {
-    const int i = it / (DH / 4), q4 = it % (DH / 4);
-    if (!bars.live[i]) continue;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float mc[kMaxSplit], lc[kMaxSplit];
 #pragma unroll
     for (int c = 0; c < kMaxSplit; ++c) {
-      if (c < S) {
-        const float f = fac[i * kMaxSplit + c];
-        const float4 o = *reinterpret_cast<const float4*>(recv + (c * rpc + i) * kRowF + q4 * 4);
-        acc.x = fmaf(f, o.x, acc.x);
-        acc.y = fmaf(f, o.y, acc.y);
-        acc.z = fmaf(f, o.z, acc.z);
-        acc.w = fmaf(f, o.w, acc.w);
+      mc[c] = c < S ? recv[(c * rpc + tid) * kRowF + DH] : -INFINITY;
+      lc[c] = c < S ? recv[(c * rpc + tid) * kRowF + DH + 1] : 0.f;
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < kMaxSplit; ++c) M = fmaxf(M, mc[c]);
+    float f[kMaxSplit], L = 0.f;
+#pragma unroll
+    for (int c = 0; c < kMaxSplit; ++c) {
+      f[c] = mc[c] > -INFINITY ? ex2_approx(mc[c] - M) : 0.f;
+      L = fmaf(lc[c], f[c], L);
+    }
+    // a row with no allowed key is not a present token: weights 0, row skipped
+    const bool live = ok && L > 0.f;
+    const float inv = live ? __frcp_rn(L) : 0.f;
+#pragma unroll
+    for (int c = 0; c < kMaxSplit; ++c) fac[tid * kMaxSplit + c] = f[c] * inv;
+    bars.live[tid] = live ? 1 : 0;
+  }
+  __syncthreads();
+  // one warp per owned row, lane = 16-byte column group; two rows in flight per pass
+  for (int i0 = warp; i0 < nr; i0 += 2 * (kThreads / 32)) {
+    int rows[2];
+    float4 acc[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int i = i0 + k * (kThreads / 32);
+      rows[k] = (i < nr && bars.live[i]) ? i : -1;
+      acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (rows[k] < 0) continue;
+#pragma unroll
+      for (int c = 0; c < kMaxSplit; ++c) {
+        if (c < S) {
+          const float fw = fac[i * kMaxSplit + c];
+          const float4 o = *reinterpret_cast<const float4*>(recv + (c * rpc + i) * kRowF + lane * 4);
+          acc[k].x = fmaf(fw, o.x, acc[k].x);
+          acc[k].y = fmaf(fw, o.y, acc[k].y);
+          acc[k].z = fmaf(fw, o.z, acc[k].z);
+          acc[k].w = fmaf(fw, o.w, acc[k].w);
+        }
       }
     }
-    const int gr = r0 + rb + i;
-    const int tt = gr / G, hh = kvh * G + gr % G;
-    const int64_t o_off = ((static_cast<int64_t>(b) * NT + tt) * p.Hq + hh) * DH + q4 * 4;
-    if (p.out_f32) {
-      *reinterpret_cast<float4*>(static_cast<float*>(p.out) + o_off) = acc;
-    } else {
-      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + o_off) =
-          make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      if (rows[k] < 0) continue;
+      const int gr = r0 + rb + rows[k];
+      const int tt = gr / G, hh = kvh * G + (gr - tt * G);
+      const int64_t o_off = ((static_cast<int64_t>(b) * NT + tt) * p.Hq + hh) * DH + lane * 4;
+      if (p.out_f32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(p.out) + o_off) = acc[k];
+      } else {
+        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + o_off) =
+            make_uint2(pack_bf16(acc[k].x, acc[k].y), pack_bf16(acc[k].z, acc[k].w));
+      }
     }
   }
   // this CTA's outgoing copies have finished reading its rows before it exits
