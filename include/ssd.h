@@ -214,7 +214,14 @@ int ssd_verify_attn(const ssd_attn_args* a, void* ws, size_t ws_bytes, void* str
  *   acc_len [B][NB], best_blk [B], n_out [B], out_tok [B][Dmax+1]: int32 outputs
  *   probs_out: optional fp32 [B][1 + NB*Dmax][V]; when given, p of every
  *     needed target row is written there (diagnostics; costs a full write)
- * Only the rows a present token needs are read. 2 <= V < 2^31; NB*Dmax < 4096;
+ *   early_rows: 0 — the row pass waits for the kernel before it on the stream
+ *     (the retrieval that wrote blk_len) and reads only the rows a present
+ *     token needs; 1 — it starts at once and reads every target row (and
+ *     every draft row when chain_blk >= 0), so that it overlaps a retrieval
+ *     launched just before it; blk_tok and blk_len are read only after that
+ *     kernel has completed. Results are identical; early_rows = 1 reads rows
+ *     of absent tokens too (their contents are never used).
+ * 2 <= V < 2^31; NB*Dmax < 4096;
  * Dmax <= 256; 0 <= chain_blk < NB or chain_blk == -1.
  * Workspace: ssd_accept_workspace_size(a) bytes, 256-byte aligned; its
  * contents need no initialisation. The call may not overlap on the GPU with
@@ -237,6 +244,7 @@ typedef struct {
   int32_t* n_out;
   int32_t* out_tok;
   float* probs_out;
+  int early_rows;
 } ssd_accept_args;
 
 size_t ssd_accept_workspace_size(const ssd_accept_args* a);

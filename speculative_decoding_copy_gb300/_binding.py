@@ -48,7 +48,7 @@ class AcceptArgs(ctypes.Structure):
                 ("blk_tok", c_void_p), ("blk_len", c_void_p), ("B", c_int), ("NB", c_int), ("Dmax", c_int),
                 ("K", c_int), ("chain_blk", c_int), ("u_acc", c_void_p), ("u_fin", c_void_p),
                 ("acc_len", c_void_p), ("best_blk", c_void_p), ("n_out", c_void_p), ("out_tok", c_void_p),
-                ("probs_out", c_void_p)]
+                ("probs_out", c_void_p), ("early_rows", c_int)]
 
 
 _lib = None
@@ -242,12 +242,14 @@ def ssd_verify_attn(q, k_cache, v_cache, k_cand, v_cand, prefix_len, blk_len, Dm
     return out
 
 
-def accept_args(mode, kind, tgt, drf, blk_tok, blk_len, K, chain_blk, u_acc, u_fin, outs, probs_out=None):
+def accept_args(mode, kind, tgt, drf, blk_tok, blk_len, K, chain_blk, u_acc, u_fin, outs, probs_out=None,
+                early_rows=False):
     B, NR, V = tgt.shape
     _, NB, Dmax = blk_tok.shape
     return AcceptArgs(int(mode), int(kind), _ptr(tgt), _ptr(drf), V, _ptr(blk_tok), _ptr(blk_len), B, NB, Dmax,
                       int(K), int(chain_blk), _ptr(u_acc), _ptr(u_fin), _ptr(outs["acc_len"]),
-                      _ptr(outs["best_blk"]), _ptr(outs["n_out"]), _ptr(outs["out_tok"]), _ptr(probs_out))
+                      _ptr(outs["best_blk"]), _ptr(outs["n_out"]), _ptr(outs["out_tok"]), _ptr(probs_out),
+                      int(bool(early_rows)))
 
 
 def ssd_accept_workspace_size(args: AcceptArgs) -> int:
@@ -260,8 +262,9 @@ def alloc_accept_outputs(B, NB, Dmax, device):
 
 
 def ssd_accept(tgt, drf, blk_tok, blk_len, u_acc, u_fin, *, mode, kind, K=0, chain_blk=-1, out=None, ws=None,
-               probs_out=None, stream=None):
-    """Acceptance, choice of block and final token; returns dict(acc_len, best_blk, n_out, out_tok)."""
+               probs_out=None, stream=None, early_rows=False):
+    """Acceptance, choice of block and final token; returns dict(acc_len, best_blk, n_out, out_tok).
+    early_rows: the row pass reads every row without first waiting for the kernel before it."""
     _need(tgt, "tgt", (torch.float32,) + _HALF, 3)
     if drf is not None:
         _need(drf, "drf", (tgt.dtype,), 3)
@@ -270,7 +273,8 @@ def ssd_accept(tgt, drf, blk_tok, blk_len, u_acc, u_fin, *, mode, kind, K=0, cha
     B, NR, V = tgt.shape
     _, NB, Dmax = blk_tok.shape
     outs = out or alloc_accept_outputs(B, NB, Dmax, tgt.device)
-    args = accept_args(mode, kind, tgt, drf, blk_tok, blk_len, K, chain_blk, u_acc, u_fin, outs, probs_out)
+    args = accept_args(mode, kind, tgt, drf, blk_tok, blk_len, K, chain_blk, u_acc, u_fin, outs, probs_out,
+                       early_rows)
     need = ssd_accept_workspace_size(args)
     if ws is None:
         ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=tgt.device)

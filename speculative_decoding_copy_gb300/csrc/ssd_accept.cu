@@ -14,7 +14,9 @@
 //   k_vocab_stats   every warp streams whole pieces of 2048 entries of the rows
 //                   some token needs (16-byte loads, all in flight together) and
 //                   reduces each to max, argmax (greedy only; lowest index on
-//                   ties) and sum of 2^((l - max) log2 e) with warp shuffles;
+//                   ties) and sum of 2^((l - max) log2 e) with warp shuffles; in
+//                   the early mode it streams every row before the retrieval has
+//                   finished and waits for it only at its end;
 //   k_accept_finish one cluster of 8 CTAs per sequence: merges the pieces of
 //                   every needed row (one warp per row), runs the acceptance test
 //                   of every candidate token and picks the longest accepted block
@@ -218,8 +220,10 @@ __device__ __forceinline__ RowStat reduce_piece(const void* row, int n, int e0, 
 }
 
 // next task (sequence, row, piece) at or after t, in steps of `step`, whose row
-// some token needs, or ntask; tasks are numbered ((b * NRD) + r) * nch + c
+// some token needs (every row in the early mode), or ntask; tasks are numbered
+// ((b * NRD) + r) * nch + c
 __device__ __forceinline__ int next_task(const AcceptParams& p, int t, int step, int ntask) {
+  if (p.early) return t < ntask ? t : ntask;
   for (; t < ntask; t += step) {
     const int br = t / p.nch;
     const int b = br / p.NRD, r = br - b * p.NRD;
@@ -233,9 +237,13 @@ template <bool BF16, bool AMAX>
 __global__ void __launch_bounds__(kStatsThreads, 2)
 k_vocab_stats(AcceptParams p) {
   // blk_len comes from the retrieval; once it is in, the next kernel of the stream may
-  // start (its prologue reads the retrieval's outputs, never this kernel's)
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // start (its prologue reads the retrieval's outputs, never this kernel's). The early
+  // mode reads no blk_len and waits at its end instead, so that this grid completes only
+  // after the retrieval has: the next kernel's wait then covers both.
+  if (!p.early) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  }
   constexpr int es = BF16 ? 2 : 4;
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * kStatsWarps + (threadIdx.x >> 5);
@@ -254,6 +262,10 @@ k_vocab_stats(AcceptParams p) {
     else if (n == per) st = reduce_piece<BF16, AMAX, true, true>(row, n, e0, p.probs);
     else st = reduce_piece<BF16, AMAX, true, false>(row, n, e0, p.probs);
     if (lane == 0) p.part[static_cast<int64_t>(br) * p.nch + c] = st;
+  }
+  if (p.early) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   }
 }
 
@@ -818,6 +830,7 @@ int accept_validate(const ssd_accept_args* a) {
   }
   if (a->chain_blk >= 0 && (a->K < 1 || a->K > a->Dmax)) return SSD_ERR_INVALID;
   if (a->mode == SSD_SAMPLE && (a->V + kSampleChunk - 1) / kSampleChunk > kMaxSampleChunks) return SSD_ERR_UNSUPPORTED;
+  if (a->early_rows != 0 && a->early_rows != 1) return SSD_ERR_INVALID;
   if (a->B == 0) return SSD_OK;
   if (!a->tgt || !a->blk_tok || !a->blk_len || !a->acc_len || !a->best_blk || !a->n_out || !a->out_tok)
     return SSD_ERR_INVALID;
@@ -841,6 +854,7 @@ AcceptParams accept_params(const ssd_accept_args* a, const AcceptLayout& L, char
   p.sample = a->mode == SSD_SAMPLE;
   p.bf16 = a->kind == SSD_LOGITS_BF16;
   p.probs = a->kind == SSD_PROBS_F32;
+  p.early = a->early_rows;
   p.nch = L.nch; p.chunk = L.chunk; p.nchs = L.nchs; p.schunk = L.schunk;
   p.hdr = reinterpret_cast<WsHeader*>(base);
   p.part = reinterpret_cast<RowStat*>(base + L.part_off);

@@ -41,6 +41,7 @@ struct AcceptParams {
   int32_t* out_tok;
   float* probs_out;
   int sample, bf16, probs;
+  int early;          // row pass reads every row without waiting for the retrieval
   int nch, nchs;
   int64_t chunk, schunk;
   WsHeader* hdr;

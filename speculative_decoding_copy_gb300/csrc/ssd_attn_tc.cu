@@ -9,7 +9,7 @@
 // cluster, rank 0 also takes the own-block keys as masked tiles, and the splits
 // are merged on chip through distributed shared memory.
 //
-// Per CTA (192 threads, one CTA per SM, all 512 TMEM columns):
+// Per CTA (384 threads, one CTA per SM, all 512 TMEM columns):
 //   warps 0-3  one thread per packed row: online softmax of a 128-key tile read
 //              from TMEM (tcgen05.ld), masked to a contiguous key range; O is
 //              rescaled in TMEM when the row max grows; P goes back to TMEM as
@@ -19,20 +19,21 @@
 //              heads of 128/G tokens out as 128 rows) and a 3-stage ring of K
 //              and V tiles of 128 keys (two 64-wide halves of the head dim,
 //              128-byte swizzle), from the prefix cache (2-D map) or the
-//              candidate keys (3-D map); after its last load it waits for the
-//              retrieval (griddepcontrol.wait) and fetches which of the rows
-//              this CTA merges belong to tokens that exist;
+//              candidate keys (3-D map);
 //   warp 5     the single MMA-issuing thread: S = Q K^T (M128 N128, eight K16
 //              steps, both operands in shared memory) into one of two TMEM
 //              buffers, two tiles ahead of the softmax, and O += P V (M128
-//              N128, eight K16 steps, A from TMEM, V MN-major in shared memory).
+//              N128, eight K16 steps, A from TMEM, V MN-major in shared memory);
+//   warps 6-11 wait at the first cluster barrier and add threads to the merge.
 // TMEM columns: S buffers 0-127 and 128-255, O 256-383, P buffers 384-447 and
 // 448-511.
-// Merge: after a cluster barrier (every CTA is past its main loop, so the K/V
-// rings are idle) each CTA stores every row's un-normalised O, max and sum
-// into the ring of the CTA that owns the row (remote shared-memory stores);
-// after a second barrier each CTA combines its 128/S rows locally and writes
-// the output of the tokens that exist.
+// Merge: each softmax thread stages its row's un-normalised O (16-bit integers
+// after a power-of-two scale), max and sum in the CTA's idle ring; after a
+// cluster barrier (every ring is idle) one thread sends each other CTA of the
+// cluster the rows it owns (128/S each) with one bulk copy completing on that
+// CTA's mbarrier, and the owner combines the S copies and writes the output of
+// the tokens that exist. Which tokens exist comes from the retrieval, so only
+// warp 4's read of it waits for the preceding kernel (griddepcontrol.wait).
 // Every mbarrier wait is bounded (about 2^32 clocks); on expiry the CTA
 // records SSD_ERR_TIMEOUT in the workspace header, skips the remaining waits,
 // frees its TMEM and exits through the cluster barriers.
@@ -50,7 +51,7 @@ constexpr int DH = 128;
 constexpr int BM = 128;                   // packed rows per CTA
 constexpr int BN = 128;                   // keys per tile
 constexpr int STAGES = 3;                 // K/V ring depth
-constexpr int kThreads = 192;
+constexpr int kThreads = 384;            // 6 role warps + 6 that join for the merge
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t TM_S = 0;              // two S buffers of BN columns
 constexpr uint32_t TM_O = 2 * BN;         // O: DH columns
@@ -69,10 +70,11 @@ struct Bars {
   uint64_t full_k[STAGES], full_v[STAGES], empty[STAGES];
   uint64_t q_full;
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
-  uint64_t recv_full;                     // every split's rows owned by this CTA have arrived
+  uint64_t recv_full;                     // every other split's copy of the owned rows has arrived
   uint32_t tmem_base;
   int failed;
-  int live[BM];                           // merged row belongs to a token that exists
+  uint8_t live[BM];                       // merged row has an allowed key and no wait of this CTA expired
+  uint8_t exists[BM];                     // merged row belongs to a token that exists
 };
 static_assert(sizeof(Bars) <= kBarBytes, "barrier block");
 
@@ -87,6 +89,10 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
 
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
@@ -160,19 +166,6 @@ __device__ __forceinline__ uint32_t map_peer(uint32_t saddr, uint32_t rank) {
   return r;
 }
 
-__device__ __forceinline__ float ld_peer_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ float4 ld_peer_f32x4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr) : "memory");
-  return v;
-}
-
 // shared memory of this CTA -> shared memory of a CTA of the cluster, completing on that CTA's mbarrier
 __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
   asm volatile(
@@ -181,13 +174,15 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, ui
       : "memory");
 }
 
+// this thread's shared-memory writes become visible to the copy engine
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
 
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -263,6 +258,22 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Merged rows travel as 16-bit integers (two per word, low half first) on the ALU pipes.
+// Encode: for |x| < 2^22, x + 1.5*2^23 rounded to fp32 is an integer whose low 16 bits are
+// round(x) in two's complement; one FFMA per value scales and rounds.
+__device__ __forceinline__ uint32_t pack_i16(float x0, float x1, float s) {
+  const uint32_t a = __float_as_uint(fmaf(x0, s, 12582912.f)), b = __float_as_uint(fmaf(x1, s, 12582912.f));
+  return __byte_perm(a, b, 0x5410);
+}
+
+// Decode: flipping the sign bit maps n to n + 2^15 in [0, 2^16); under the exponent of 2^23
+// that is the fp32 2^23 + 2^15 + n, from which one FADD recovers n exactly.
+__device__ __forceinline__ float2 unpack_i16(uint32_t w) {
+  const uint32_t f = w ^ 0x80008000u;
+  return make_float2(__uint_as_float(__byte_perm(f, 0x4B000000u, 0x7610)) - 8421376.f,
+                     __uint_as_float(__byte_perm(f, 0x4B000000u, 0x7632)) - 8421376.f);
+}
+
 // two fp32 -> packed bf16x2 (round to nearest even), low half = first
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
@@ -321,9 +332,11 @@ __device__ __forceinline__ float chunk_exp(uint32_t saddr, uint32_t paddr, int l
 
 // ------------------------------------------------------------------ kernel
 constexpr int kMaxSplit = 8;              // cluster size limit (portable)
-constexpr int kRowF = 132;                // fp32 per merged row: O (128), max, sum, padding to 16 bytes
-constexpr int kMergeItems = BM + kMaxSplit;   // bound on (rows owned by one CTA) x S
-static_assert((BM + kMergeItems) * kRowF * 4 + BM * kMaxSplit * 4 <= STAGES * kStage, "merge buffers fit in the ring");
+// one split's partial row as sent to its owner: O as 128 16-bit integers, round(O 2^(14-e)) with
+// max |O| in [2^(e-1), 2^e), then max, sum and 2^(e-14) as fp32 (16-byte units)
+constexpr int kRowB = 2 * DH + 16;
+static_assert((2 * BM + kMaxSplit) * kRowB + BM * kMaxSplit * 4 <= static_cast<int>(STAGES * kStage),
+              "merge buffers fit in the ring");
 
 // grid (S, row tiles, B*Hkv), cluster (S, 1, 1): the S CTAs of one row tile split
 // the prefix; cluster rank 0 also takes the own-block (candidate) keys.
@@ -356,11 +369,24 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
   const int s_base = (t_first / p.Dmax) * p.Dmax;
   const int nC = (split == 0 && t_first < NT) ? (t_last + 1 - s_base + BN - 1) / BN : 0;
   const int nT = nC + nP;
-  // rows of this tile merged by this CTA: [rb, rb + nr)
-  const int rpc = (BM + S - 1) / S;
-  const int rb = split * rpc, nr = max(0, min(BM, rb + rpc) - rb);
+  // rows of this tile that exist (rv) and those merged by this CTA: [rb, rb + nr)
+  const int rv = min(BM, rows_total - r0);
+  const int rpc = (rv + S - 1) / S;
+  const int rb = split * rpc, nr = max(0, min(rv, rb + rpc) - rb);
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (warp == 4 && lane == 0) {
+    // the descriptors are fetched on first use: start those fetches before the first copy
+    prefetch_tmap(&tmap_q);
+    if (nP > 0) {
+      prefetch_tmap(&tmap_k);
+      prefetch_tmap(&tmap_v);
+    }
+    if (nC > 0) {
+      prefetch_tmap(&tmap_kc);
+      prefetch_tmap(&tmap_vc);
+    }
+  }
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&bars.full_k[s], 1);
@@ -494,19 +520,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
         }
       }
     }
-    __syncwarp();
-    // which merged rows belong to tokens that exist: blk_len comes from the retrieval
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    for (int i = lane; i < nr; i += 32) {
-      const int gr = r0 + rb + i;
-      int ok = 0;
-      if (gr < rows_total) {
-        const int tt = gr / G;
-        ok = (tt % p.Dmax) < p.blk_len[b * p.NB + tt / p.Dmax];
-      }
-      bars.live[i] = ok;
-    }
-  } else {
+  } else if (warp == 5) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0 && nT > 0) {
       constexpr uint32_t idS = idesc_bf16(false, BN), idPV = idesc_bf16(true, DH);
@@ -552,12 +566,39 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
   }
 
   // ---- merge the S splits of every row in the CTA that owns it
-  // Layout in the (now idle) K/V ring: this CTA's rows as sent [BM][kRowF] (O, then max
-  // and sum), the rows it owns as received [S][rpc][kRowF], then their weights [rpc][S].
-  float* stage = reinterpret_cast<float*>(smem + OFF_RING);
-  float* recv = stage + BM * kRowF;
-  float* fac = recv + kMergeItems * kRowF;
+  // Each softmax thread stages its row's partial O (16-bit integers, scaled by a power of two
+  // so that max |O| maps into [2^13, 2^14)), max, sum and inverse scale in this CTA's idle
+  // ring; after a cluster barrier
+  // (every ring is idle) one thread sends each other CTA the rows it owns with one bulk copy,
+  // completing on that CTA's mbarrier. The owner combines the S copies (its own split's rows
+  // where they were staged) and writes the rows of the tokens that exist.
+  // Ring layout (bytes): staged rows [BM][kRowB], received rows [sender split][rpc][kRowB],
+  // weights [rpc][kMaxSplit] fp32.
+  uint8_t* stage = smem + OFF_RING;
+  uint8_t* recv = stage + BM * kRowB;
+  float* fac = reinterpret_cast<float*>(recv + (BM + kMaxSplit) * kRowB);
+  auto part = [&](int c, int i) -> const uint8_t* {
+    return c == split ? stage + (rb + i) * kRowB : recv + (c * rpc + i) * kRowB;
+  };
   if (warp < 4) {
+    // max |O| of the row, then round(O 2^(14-e)) as 16-bit pairs
+    float amax = 0.f;
+    if (nT > 0) {
+#pragma unroll
+      for (int q = 0; q < DH / 32; ++q) {
+        uint32_t o[32];
+        tmem_ld32(tmem + TM_O + lane_off + q * 32, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(__uint_as_float(o[e])));
+      }
+    }
+    // amax in [2^k, 2^(k+1)): e = k + 1; rows below 2^-100 keep e = 0 (they round to zero)
+    const int k = (amax >= 0x1p-100f) ? static_cast<int>((__float_as_uint(amax) >> 23) & 0xff) - 127 : -1;
+    const int ex = min(k, 125) + 1;
+    const float scale = __uint_as_float(static_cast<uint32_t>(127 + 14 - ex) << 23);
+    const float inv_scale = __uint_as_float(static_cast<uint32_t>(127 - 14 + ex) << 23);
+    uint4* dst = reinterpret_cast<uint4*>(stage + tid * kRowB);
 #pragma unroll
     for (int q = 0; q < DH / 32; ++q) {
       uint32_t o[32];
@@ -568,41 +609,55 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
 #pragma unroll
         for (int e = 0; e < 32; ++e) o[e] = 0u;
       }
-      float4* dst = reinterpret_cast<float4*>(stage + tid * kRowF + q * 32);
+      uint32_t pk[16];
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
-        dst[e] = make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]), __uint_as_float(o[4 * e + 2]),
-                             __uint_as_float(o[4 * e + 3]));
+      for (int e = 0; e < 16; ++e)
+        pk[e] = pack_i16(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1]), scale);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) dst[q * 4 + u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
     }
-    stage[tid * kRowF + DH] = m;
-    stage[tid * kRowF + DH + 1] = l;
+    dst[DH / 8] = make_uint4(__float_as_uint(m), __float_as_uint(l), __float_as_uint(inv_scale), 0u);
     fence_async_smem();                              // the bulk copies read what the threads wrote
   }
-  if (tid == 0) mbar_expect_tx(&bars.recv_full, static_cast<uint32_t>(S * nr * kRowF * 4));
+  if (tid == 0) mbar_expect_tx(&bars.recv_full, static_cast<uint32_t>((S - 1) * nr * kRowB));
   tc_fence_before();
   __syncwarp();
   cluster_sync();                                   // every CTA is past its main loop: the rings are idle
   tc_fence_after();
   if (tid == 0) {
-    // rows [c*rpc, c*rpc + n_c) go to cluster rank c, into its slot for this split
-    for (int c = 0; c < S; ++c) {
-      const int n_c = min(BM, (c + 1) * rpc) - c * rpc;
+    // rows [c*rpc, c*rpc + n_c) go to cluster rank c, into its slot for this split; each
+    // rank starts with a different destination, so that no CTA receives from all at once
+    for (int i = 1; i < S; ++i) {
+      const int c = (split + i) % S;
+      const int n_c = min(rv, (c + 1) * rpc) - c * rpc;
       if (n_c <= 0) continue;
-      const uint32_t dst = map_peer(smem_u32(recv + split * rpc * kRowF), static_cast<uint32_t>(c));
+      const uint32_t dst = map_peer(smem_u32(recv + split * rpc * kRowB), static_cast<uint32_t>(c));
       const uint32_t bar = map_peer(smem_u32(&bars.recv_full), static_cast<uint32_t>(c));
-      bulk_copy_to_peer(dst, smem_u32(stage + c * rpc * kRowF), static_cast<uint32_t>(n_c * kRowF * 4), bar);
+      bulk_copy_to_peer(dst, smem_u32(stage + c * rpc * kRowB), static_cast<uint32_t>(n_c * kRowB), bar);
     }
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
   }
-  // weights of the owned rows once every split has arrived (one thread per row, the
-  // split loop unrolled so that every load is in flight together)
+  if (warp == 4) {
+    // which owned rows belong to tokens that exist: blk_len comes from the retrieval, which
+    // precedes this kernel in the stream
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (int i = lane; i < nr; i += 32) {
+      const int gr = r0 + rb + i;
+      const int tt = gr / G;
+      bars.exists[i] = (tt % p.Dmax) < __ldcg(p.blk_len + b * p.NB + tt / p.Dmax) ? 1 : 0;
+    }
+  }
+  // weights of the owned rows once every split has arrived (one thread per row)
   if (tid < nr) {
-    const bool ok = mbar_wait(bars, &bars.recv_full, 0, p.hdr, 40) && bars.live[tid];
-    float mc[kMaxSplit], lc[kMaxSplit];
+    const bool ok = mbar_wait(bars, &bars.recv_full, 0, p.hdr, 40);
+    float mc[kMaxSplit], lc[kMaxSplit], sc[kMaxSplit];
 #pragma unroll
     for (int c = 0; c < kMaxSplit; ++c) {
-      mc[c] = c < S ? recv[(c * rpc + tid) * kRowF + DH] : -INFINITY;
-      lc[c] = c < S ? recv[(c * rpc + tid) * kRowF + DH + 1] : 0.f;
+      float4 v = make_float4(-INFINITY, 0.f, 0.f, 0.f);
+      if (c < S) v = *reinterpret_cast<const float4*>(part(c, tid) + 2 * DH);
+      mc[c] = v.x;
+      lc[c] = v.y;
+      sc[c] = v.z;
     }
     float M = -INFINITY;
 #pragma unroll
@@ -614,50 +669,59 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
       L = fmaf(lc[c], f[c], L);
     }
     // a row with no allowed key is not a present token: weights 0, row skipped
-    const bool live = ok && L > 0.f;
+    const bool live = ok && !bars.failed && L > 0.f;
     const float inv = live ? __frcp_rn(L) : 0.f;
 #pragma unroll
-    for (int c = 0; c < kMaxSplit; ++c) fac[tid * kMaxSplit + c] = f[c] * inv;
+    for (int c = 0; c < kMaxSplit; ++c) fac[tid * kMaxSplit + c] = f[c] * inv * sc[c];
     bars.live[tid] = live ? 1 : 0;
   }
   __syncthreads();
-  // one warp per owned row, lane = 16-byte column group; two rows in flight per pass
-  for (int i0 = warp; i0 < nr; i0 += 2 * (kThreads / 32)) {
-    int rows[2];
-    float4 acc[2];
+  // one thread per (owned row, 16-column group): every split's 32 bytes of it loaded together
+  for (int it = tid; it < nr * (DH / 16); it += kThreads) {
+    const int i = it / (DH / 16), cg = it % (DH / 16);
+    if (!bars.live[i] || !bars.exists[i]) continue;
+    uint4 h[kMaxSplit][2];
+    float fw[kMaxSplit];
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int i = i0 + k * (kThreads / 32);
-      rows[k] = (i < nr && bars.live[i]) ? i : -1;
-      acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (rows[k] < 0) continue;
+    for (int c = 0; c < kMaxSplit; ++c) {
+      if (c < S) {
+        fw[c] = fac[i * kMaxSplit + c];
+        const uint4* src = reinterpret_cast<const uint4*>(part(c, i) + cg * 32);
+        h[c][0] = src[0];
+        h[c][1] = src[1];
+      }
+    }
+    float acc[16];
 #pragma unroll
-      for (int c = 0; c < kMaxSplit; ++c) {
-        if (c < S) {
-          const float fw = fac[i * kMaxSplit + c];
-          const float4 o = *reinterpret_cast<const float4*>(recv + (c * rpc + i) * kRowF + lane * 4);
-          acc[k].x = fmaf(fw, o.x, acc[k].x);
-          acc[k].y = fmaf(fw, o.y, acc[k].y);
-          acc[k].z = fmaf(fw, o.z, acc[k].z);
-          acc[k].w = fmaf(fw, o.w, acc[k].w);
+    for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+#pragma unroll
+    for (int c = 0; c < kMaxSplit; ++c) {
+      if (c < S) {
+        const uint32_t w[8] = {h[c][0].x, h[c][0].y, h[c][0].z, h[c][0].w, h[c][1].x, h[c][1].y, h[c][1].z, h[c][1].w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float2 v = unpack_i16(w[e]);
+          acc[2 * e] = fmaf(fw[c], v.x, acc[2 * e]);
+          acc[2 * e + 1] = fmaf(fw[c], v.y, acc[2 * e + 1]);
         }
       }
     }
+    const int gr = r0 + rb + i;
+    const int tt = gr / G, hh = kvh * G + (gr - tt * G);
+    const int64_t o_off = ((static_cast<int64_t>(b) * NT + tt) * p.Hq + hh) * DH + cg * 16;
+    if (p.out_f32) {
+      float4* o = reinterpret_cast<float4*>(static_cast<float*>(p.out) + o_off);
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      if (rows[k] < 0) continue;
-      const int gr = r0 + rb + rows[k];
-      const int tt = gr / G, hh = kvh * G + (gr - tt * G);
-      const int64_t o_off = ((static_cast<int64_t>(b) * NT + tt) * p.Hq + hh) * DH + lane * 4;
-      if (p.out_f32) {
-        *reinterpret_cast<float4*>(static_cast<float*>(p.out) + o_off) = acc[k];
-      } else {
-        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + o_off) =
-            make_uint2(pack_bf16(acc[k].x, acc[k].y), pack_bf16(acc[k].z, acc[k].w));
-      }
+      for (int u = 0; u < 4; ++u) o[u] = make_float4(acc[4 * u], acc[4 * u + 1], acc[4 * u + 2], acc[4 * u + 3]);
+    } else {
+      uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + o_off);
+      o[0] = make_uint4(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]), pack_bf16(acc[4], acc[5]),
+                        pack_bf16(acc[6], acc[7]));
+      o[1] = make_uint4(pack_bf16(acc[8], acc[9]), pack_bf16(acc[10], acc[11]), pack_bf16(acc[12], acc[13]),
+                        pack_bf16(acc[14], acc[15]));
     }
   }
-  // this CTA's outgoing copies have finished reading its rows before it exits
+  // this CTA's outgoing copies have finished reading its staged rows before it exits
   if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 
   // teardown: every role is done with TMEM
@@ -774,7 +838,7 @@ static void choose_split(const ssd_attn_args* a, int mtiles, int* S_out, int* ch
   for (int S = 1; S <= kMaxSplit && S <= nkt; ++S) {
     const int active = max_active_clusters(S);
     if (active <= 0) continue;
-    const long long tiles = (nkt + nc + S - 1) / S;
+    const long long tiles = (nkt + 2 * nc + S - 1) / S;
     const long long waves = (groups + active - 1) / active;
     const long long cost = waves * (tiles + 2) * 16 + S;   // +2 tiles: prologue and merge
     if (best_cost < 0 || cost < best_cost) {
@@ -782,10 +846,11 @@ static void choose_split(const ssd_attn_args* a, int mtiles, int* S_out, int* ch
       best_S = S;
     }
   }
-  const long long tiles = (nkt + nc + best_S - 1) / best_S;
+  // a masked candidate tile costs about two prefix tiles (per-element masks in both passes)
+  const long long tiles = (nkt + 2 * nc + best_S - 1) / best_S;
   *S_out = best_S;
   *chunk_out = static_cast<int>(tiles * BN);
-  *chunk0_out = static_cast<int>((tiles > nc ? tiles - nc : 0) * BN);
+  *chunk0_out = static_cast<int>((tiles > 2 * nc ? tiles - 2 * nc : 0) * BN);
 }
 
 }  // namespace tc

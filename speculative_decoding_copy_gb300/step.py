@@ -6,9 +6,12 @@ launch order of the C-ABI calls.
 
 Verification attention and acceptance both depend only on the retrieval output.
 On one stream the kernels are chained by programmatic dependent launch: the row
-pass streams the logits alone right after the retrieval, and the attention's main
-loop (which needs nothing from the acceptance) runs on the SMs the latency-bound
-finish kernel leaves free; it waits for its predecessors only before writing.
+pass streams the needed logit rows right after the retrieval, and the attention's
+main loop (which needs nothing from the acceptance) runs on the SMs the
+latency-bound finish kernel leaves free; it waits for its predecessors only before
+writing. early_rows=True lets the row pass stream every row while the retrieval
+still runs: a step without attention is faster that way, but with attention on
+the same stream the attention then starts no earlier and the step is slower.
 The step issues only library calls; it computes nothing itself.
 """
 from __future__ import annotations
@@ -34,8 +37,9 @@ class VerifyStep:
     """Holds the inputs, outputs and workspaces of one batch of workload `wl`."""
 
     def __init__(self, wl, inp: dict, device="cuda", mode=None, kind=None, with_attention=True,
-                 with_probs=False):
+                 with_probs=False, early_rows=False):
         self.wl = wl
+        self.early_rows = early_rows
         self.mode = ssd.SSD_SAMPLE if (mode or wl.mode) == "sample" else ssd.SSD_GREEDY
         if kind is None:
             kind = ssd.SSD_LOGITS_BF16 if wl.logit_dtype == "bf16" else ssd.SSD_LOGITS_F32
@@ -104,7 +108,7 @@ class VerifyStep:
         return ssd.ssd_accept(x["tgt"], x.get("drf") if wl.chain_policy else None, self.ret_out["blk_tok"],
                               self.ret_out["blk_len"], x["u_acc"], x["u_fin"], mode=self.mode, kind=self.kind,
                               K=wl.K, chain_blk=self.chain_blk, out=self.acc_out, ws=self.acc_ws,
-                              probs_out=self.probs, stream=stream)
+                              probs_out=self.probs, stream=stream, early_rows=self.early_rows)
 
     def run(self, stream=None, aux: torch.cuda.Stream | None = None):
         """Issue the whole step on `stream` (default: current), attention on `aux` if given."""

@@ -52,13 +52,13 @@ def _boost_probs(tgt, blk_tok, blk_len, Dmax, rng):
     return t
 
 
-def _gpu_accept(mode, kind, tgt, drf, blk_tok, blk_len, K, chain_blk, u_acc, u_fin, probs=False):
+def _gpu_accept(mode, kind, tgt, drf, blk_tok, blk_len, K, chain_blk, u_acc, u_fin, probs=False, early=False):
     dev = "cuda"
     T = lambda a: to_device(np.asarray(a), dev) if a is not None else None
     tt = T(tgt)
     po = torch.empty(tgt.shape, dtype=torch.float32, device=dev) if probs else None
     r = S.ssd_accept(tt, T(drf), T(blk_tok), T(blk_len), T(u_acc), T(u_fin), mode=MODE[mode], kind=KIND[kind], K=K,
-                     chain_blk=chain_blk, probs_out=po)
+                     chain_blk=chain_blk, probs_out=po, early_rows=early)
     torch.cuda.synchronize()
     out = {k: v.cpu().numpy() for k, v in r.items()}
     if probs:
@@ -96,6 +96,40 @@ def test_accept_probs_bit_exact(mode, V, B, W, Dmax, K, policy):
     ref = _oracle(mode, "probs_f32", tgt, drf, blk_tok, blk_len, W, policy, u_acc, u_fin)
     _assert_same(got, ref)
     assert ref["acc_len"].max() > 0          # the boost produced accepted runs
+
+
+@pytest.mark.parametrize("mode", ["sample", "greedy"])
+@pytest.mark.parametrize("V,B,W,Dmax,K,policy", [(17, 64, 3, 6, 4, 1), (4099, 16, 8, 16, 7, 1),
+                                                  (128256, 3, 4, 20, 0, 0)])
+def test_accept_early_rows(mode, V, B, W, Dmax, K, policy):
+    """The early row pass reads every row, rows of absent tokens included: filled with
+    NaN here, they must change nothing. Bit-exact against the oracle and against the
+    row pass that reads only the needed rows."""
+    rng = np.random.default_rng(3 * V + B)
+    blk_tok, blk_len = _blocks(rng, B, W, Dmax, K, V, policy)
+    NB = blk_tok.shape[1]
+    tgt = _boost_probs(_rows_probs(rng, (B, 1 + NB * Dmax, V)), blk_tok, blk_len, Dmax, rng)
+    drf = _rows_probs(rng, (B, K, V)) if policy else None
+    if policy:
+        for b in range(B):
+            for d in range(blk_len[b, W]):
+                blk_tok[b, W, d] = int(np.argmax(drf[b, d] * rng.random(V)))
+    u_acc = WL.uniforms24(rng, (B, NB, Dmax))
+    u_fin = WL.uniforms24(rng, (B,))
+    chain_blk = W if policy else -1
+    ref = _oracle(mode, "probs_f32", tgt, drf, blk_tok, blk_len, W, policy, u_acc, u_fin)
+    poisoned = tgt.copy()
+    for b in range(B):
+        for k in range(NB):
+            poisoned[b, 1 + k * Dmax + blk_len[b, k]:1 + (k + 1) * Dmax] = np.nan   # rows no token reads
+    if policy:
+        drf = drf.copy()
+        for b in range(B):
+            drf[b, blk_len[b, W]:] = np.nan
+    early = _gpu_accept(mode, "probs_f32", poisoned, drf, blk_tok, blk_len, K, chain_blk, u_acc, u_fin, early=True)
+    late = _gpu_accept(mode, "probs_f32", poisoned, drf, blk_tok, blk_len, K, chain_blk, u_acc, u_fin, early=False)
+    _assert_same(early, ref)
+    _assert_same(late, ref)
 
 
 def _margins_explain(kind, tgt, drf, blk_tok, blk_len, W, policy, u_acc, u_fin, got, ref, b):
@@ -171,14 +205,16 @@ def test_accept_logits_probs_and_decisions(kind, V):
     _assert_same(gg, _oracle("greedy", kind, lg, dl, blk_tok, blk_len, W, policy, u_acc, u_fin))
 
 
-@pytest.mark.parametrize("name", WL.WORKLOAD_ORDER)
-def test_whole_step_workloads(name):
-    """gate -> retrieve -> attention || accept through the step's own launch path,
-    compared with the oracle step on the same inputs (sampled rows for attention)."""
+@pytest.mark.parametrize("name,two_streams", [(n, True) for n in WL.WORKLOAD_ORDER] +
+                         [("tiny", False), ("llama8b", False), ("batched", False)])
+def test_whole_step_workloads(name, two_streams):
+    """gate -> retrieve -> accept -> attention through the step's own launch path (one
+    stream, or attention on a second stream), compared with the oracle step on the same
+    inputs (sampled rows for attention)."""
     wl = WL.WORKLOADS[name]
     inp = WL.make_inputs(wl, 77 + len(name), full_width=False)
     st = VerifyStep(wl, inp, with_attention=(name in ("tiny", "llama8b")))
-    st.run(aux=torch.cuda.Stream())
+    st.run(aux=torch.cuda.Stream() if two_streams else None)
     got = st.results()
     ref = O.verify_step(inp, wl, attention_slots=None)
     for k in ("gate", "last_match_end", "blk_tok", "blk_len", "n_cand"):
