@@ -73,7 +73,6 @@ struct Bars {
   uint64_t recv_full;                     // every other split's copy of the owned rows has arrived
   uint32_t tmem_base;
   int failed;
-  uint8_t live[BM];                       // merged row has an allowed key and no wait of this CTA expired
   uint8_t exists[BM];                     // merged row belongs to a token that exists
 };
 static_assert(sizeof(Bars) <= kBarBytes, "barrier block");
@@ -333,7 +332,8 @@ __device__ __forceinline__ float chunk_exp(uint32_t saddr, uint32_t paddr, int l
 // ------------------------------------------------------------------ kernel
 constexpr int kMaxSplit = 8;              // cluster size limit (portable)
 // one split's partial row as sent to its owner: O as 128 16-bit integers, round(O 2^(14-e)) with
-// max |O| in [2^(e-1), 2^e), then max, sum and 2^(e-14) as fp32 (16-byte units)
+// e per 64-column half such that its max |O| lies in [2^(e-1), 2^e), then the row's max and
+// sum and the two halves' 2^(e-14) as fp32 (16-byte units)
 constexpr int kRowB = 2 * DH + 16;
 static_assert((2 * BM + kMaxSplit) * kRowB + BM * kMaxSplit * 4 <= static_cast<int>(STAGES * kStage),
               "merge buffers fit in the ring");
@@ -566,57 +566,60 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
   }
 
   // ---- merge the S splits of every row in the CTA that owns it
-  // Each softmax thread stages its row's partial O (16-bit integers, scaled by a power of two
-  // so that max |O| maps into [2^13, 2^14)), max, sum and inverse scale in this CTA's idle
-  // ring; after a cluster barrier
-  // (every ring is idle) one thread sends each other CTA the rows it owns with one bulk copy,
-  // completing on that CTA's mbarrier. The owner combines the S copies (its own split's rows
-  // where they were staged) and writes the rows of the tokens that exist.
-  // Ring layout (bytes): staged rows [BM][kRowB], received rows [sender split][rpc][kRowB],
-  // weights [rpc][kMaxSplit] fp32.
+  // Each row's partial O is staged in this CTA's idle ring as 16-bit integers, each 64-column
+  // half scaled by its own power of two (so that its max |O| maps into [2^13, 2^14)), with
+  // the row's max, sum and the two inverse scales; warps 0-3 stage columns 0-63 and warps 6-9
+  // (which share the TMEM lane quarters) columns 64-127. After a cluster barrier (every ring
+  // is idle) S-1 threads each send one other CTA the rows it owns with one bulk copy,
+  // completing on that CTA's mbarrier. Every owner thread then weights and sums the S copies
+  // (its own split's rows where they were staged) and writes the rows of tokens that exist.
+  // Ring layout (bytes): staged rows [BM][kRowB], received rows [sender split][rpc][kRowB].
   uint8_t* stage = smem + OFF_RING;
   uint8_t* recv = stage + BM * kRowB;
-  float* fac = reinterpret_cast<float*>(recv + (BM + kMaxSplit) * kRowB);
   auto part = [&](int c, int i) -> const uint8_t* {
     return c == split ? stage + (rb + i) * kRowB : recv + (c * rpc + i) * kRowB;
   };
-  if (warp < 4) {
-    // max |O| of the row, then round(O 2^(14-e)) as 16-bit pairs
-    float amax = 0.f;
+  if (warp < 4 || (warp >= 6 && warp < 10)) {
+    const int half = warp < 4 ? 0 : 1;
+    const int row = (warp & 3) * 32 + lane;          // this warp's TMEM lane quarter
+    const uint32_t oa = tmem + TM_O + (static_cast<uint32_t>((warp & 3) * 32) << 16) + half * 64;
+    // warps 6-9 read O once warps 0-3 have seen the last P V product complete (a parity
+    // wait on pv_done is only valid for a waiter at most one phase behind, as those are)
+    tc_fence_before();
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    tc_fence_after();
+    // max |O| of this half row, then round(O 2^(14-e)) as 16-bit pairs
+    uint32_t o[64];
     if (nT > 0) {
+      tmem_ld32(oa, o);
+      tmem_ld32(oa + 32, o + 32);
+      tmem_wait_ld();
+    } else {
 #pragma unroll
-      for (int q = 0; q < DH / 32; ++q) {
-        uint32_t o[32];
-        tmem_ld32(tmem + TM_O + lane_off + q * 32, o);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(__uint_as_float(o[e])));
-      }
+      for (int e = 0; e < 64; ++e) o[e] = 0u;
     }
-    // amax in [2^k, 2^(k+1)): e = k + 1; rows below 2^-100 keep e = 0 (they round to zero)
+    float amax = 0.f;
+#pragma unroll
+    for (int e = 0; e < 64; ++e) amax = fmaxf(amax, fabsf(__uint_as_float(o[e])));
+    // amax in [2^k, 2^(k+1)): e = k + 1; halves below 2^-100 keep e = 0 (they round to zero)
     const int k = (amax >= 0x1p-100f) ? static_cast<int>((__float_as_uint(amax) >> 23) & 0xff) - 127 : -1;
     const int ex = min(k, 125) + 1;
     const float scale = __uint_as_float(static_cast<uint32_t>(127 + 14 - ex) << 23);
     const float inv_scale = __uint_as_float(static_cast<uint32_t>(127 - 14 + ex) << 23);
-    uint4* dst = reinterpret_cast<uint4*>(stage + tid * kRowB);
+    uint4* dst = reinterpret_cast<uint4*>(stage + row * kRowB + half * DH);
 #pragma unroll
-    for (int q = 0; q < DH / 32; ++q) {
-      uint32_t o[32];
-      if (nT > 0) {
-        tmem_ld32(tmem + TM_O + lane_off + q * 32, o);
-        tmem_wait_ld();
-      } else {
+    for (int u = 0; u < 8; ++u) {
+      uint32_t pk[4];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = 0u;
-      }
-      uint32_t pk[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e)
-        pk[e] = pack_i16(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1]), scale);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) dst[q * 4 + u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      for (int e = 0; e < 4; ++e) pk[e] = pack_i16(__uint_as_float(o[8 * u + 2 * e]), __uint_as_float(o[8 * u + 2 * e + 1]), scale);
+      dst[u] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
-    dst[DH / 8] = make_uint4(__float_as_uint(m), __float_as_uint(l), __float_as_uint(inv_scale), 0u);
+    float* tail = reinterpret_cast<float*>(stage + row * kRowB + 2 * DH);
+    if (half == 0) {
+      tail[0] = m;
+      tail[1] = l;
+    }
+    tail[2 + half] = inv_scale;
     fence_async_smem();                              // the bulk copies read what the threads wrote
   }
   if (tid == 0) mbar_expect_tx(&bars.recv_full, static_cast<uint32_t>((S - 1) * nr * kRowB));
@@ -624,13 +627,12 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
   __syncwarp();
   cluster_sync();                                   // every CTA is past its main loop: the rings are idle
   tc_fence_after();
-  if (tid == 0) {
+  if (tid < S - 1) {
     // rows [c*rpc, c*rpc + n_c) go to cluster rank c, into its slot for this split; each
     // rank starts with a different destination, so that no CTA receives from all at once
-    for (int i = 1; i < S; ++i) {
-      const int c = (split + i) % S;
-      const int n_c = min(rv, (c + 1) * rpc) - c * rpc;
-      if (n_c <= 0) continue;
+    const int c = (split + 1 + tid) % S;
+    const int n_c = min(rv, (c + 1) * rpc) - c * rpc;
+    if (n_c > 0) {
       const uint32_t dst = map_peer(smem_u32(recv + split * rpc * kRowB), static_cast<uint32_t>(c));
       const uint32_t bar = map_peer(smem_u32(&bars.recv_full), static_cast<uint32_t>(c));
       bulk_copy_to_peer(dst, smem_u32(stage + c * rpc * kRowB), static_cast<uint32_t>(n_c * kRowB), bar);
@@ -647,62 +649,51 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
       bars.exists[i] = (tt % p.Dmax) < __ldcg(p.blk_len + b * p.NB + tt / p.Dmax) ? 1 : 0;
     }
   }
-  // weights of the owned rows once every split has arrived (one thread per row)
-  if (tid < nr) {
-    const bool ok = mbar_wait(bars, &bars.recv_full, 0, p.hdr, 40);
-    float mc[kMaxSplit], lc[kMaxSplit], sc[kMaxSplit];
-#pragma unroll
-    for (int c = 0; c < kMaxSplit; ++c) {
-      float4 v = make_float4(-INFINITY, 0.f, 0.f, 0.f);
-      if (c < S) v = *reinterpret_cast<const float4*>(part(c, tid) + 2 * DH);
-      mc[c] = v.x;
-      lc[c] = v.y;
-      sc[c] = v.z;
-    }
-    float M = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < kMaxSplit; ++c) M = fmaxf(M, mc[c]);
-    float f[kMaxSplit], L = 0.f;
-#pragma unroll
-    for (int c = 0; c < kMaxSplit; ++c) {
-      f[c] = mc[c] > -INFINITY ? ex2_approx(mc[c] - M) : 0.f;
-      L = fmaf(lc[c], f[c], L);
-    }
-    // a row with no allowed key is not a present token: weights 0, row skipped
-    const bool live = ok && !bars.failed && L > 0.f;
-    const float inv = live ? __frcp_rn(L) : 0.f;
-#pragma unroll
-    for (int c = 0; c < kMaxSplit; ++c) fac[tid * kMaxSplit + c] = f[c] * inv * sc[c];
-    bars.live[tid] = live ? 1 : 0;
-  }
   __syncthreads();
-  // one thread per (owned row, 16-column group): every split's 32 bytes of it loaded together
+  // one thread per (owned row, 16-column group): every split's max, sum, scale and 32 bytes
+  // of the row loaded together, the weights 2^(m_c - M) / sum_c l_c 2^(m_c - M) computed here
   for (int it = tid; it < nr * (DH / 16); it += kThreads) {
     const int i = it / (DH / 16), cg = it % (DH / 16);
-    if (!bars.live[i] || !bars.exists[i]) continue;
+    if (!bars.exists[i]) continue;
+    if (!mbar_wait(bars, &bars.recv_full, 0, p.hdr, 40)) continue;
+    float4 tl[kMaxSplit];
     uint4 h[kMaxSplit][2];
-    float fw[kMaxSplit];
 #pragma unroll
     for (int c = 0; c < kMaxSplit; ++c) {
+      tl[c] = make_float4(-INFINITY, 0.f, 0.f, 0.f);
       if (c < S) {
-        fw[c] = fac[i * kMaxSplit + c];
-        const uint4* src = reinterpret_cast<const uint4*>(part(c, i) + cg * 32);
+        const uint8_t* pr = part(c, i);
+        tl[c] = *reinterpret_cast<const float4*>(pr + 2 * DH);
+        const uint4* src = reinterpret_cast<const uint4*>(pr + cg * 32);
         h[c][0] = src[0];
         h[c][1] = src[1];
       }
     }
+    float M = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < kMaxSplit; ++c) M = fmaxf(M, tl[c].x);
+    float fw[kMaxSplit], L = 0.f;
+#pragma unroll
+    for (int c = 0; c < kMaxSplit; ++c) {
+      fw[c] = tl[c].x > -INFINITY ? ex2_approx(tl[c].x - M) : 0.f;
+      L = fmaf(tl[c].y, fw[c], L);
+    }
+    // a row with no allowed key is not a present token: nothing written
+    if (bars.failed || !(L > 0.f)) continue;
+    const float inv = __frcp_rn(L);
     float acc[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) acc[e] = 0.f;
 #pragma unroll
     for (int c = 0; c < kMaxSplit; ++c) {
       if (c < S) {
+        const float f = fw[c] * inv * (cg < 4 ? tl[c].z : tl[c].w);
         const uint32_t w[8] = {h[c][0].x, h[c][0].y, h[c][0].z, h[c][0].w, h[c][1].x, h[c][1].y, h[c][1].z, h[c][1].w};
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float2 v = unpack_i16(w[e]);
-          acc[2 * e] = fmaf(fw[c], v.x, acc[2 * e]);
-          acc[2 * e + 1] = fmaf(fw[c], v.y, acc[2 * e + 1]);
+          acc[2 * e] = fmaf(f, v.x, acc[2 * e]);
+          acc[2 * e + 1] = fmaf(f, v.y, acc[2 * e + 1]);
         }
       }
     }
@@ -722,7 +713,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
     }
   }
   // this CTA's outgoing copies have finished reading its staged rows before it exits
-  if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+  if (tid < S - 1) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 
   // teardown: every role is done with TMEM
   tc_fence_before();
