@@ -426,43 +426,6 @@ def run_e2e(args, wl, inp, st, main, aux, dev):
     h2d = sum(h.numel() * h.element_size() for h in host.values())
     d2h = out_h.numel() * 4 + nout_h.numel() * 4
     E = args.e2e_steps
-    # the host->device copies are spread over several streams (several copy engines), in
-    # pieces of at most 8 MiB, each stream waiting for the previous step's kernels and the
-    # step waiting for every copy
-    NC = 4
-    cstreams = [torch.cuda.Stream(dev) for _ in range(NC)]
-    pieces = []
-    for k, h in host.items():
-        src, dst = h.view(-1), st.x[k].view(-1)
-        step = max(1, (8 << 20) // h.element_size())
-        for o in range(0, src.numel(), step):
-            pieces.append((dst[o:o + step], src[o:o + step]))
-    pieces.sort(key=lambda p: -p[1].numel())
-    lanes = [[] for _ in range(NC)]
-    load = [0] * NC
-    for d_, s_ in pieces:
-        i = load.index(min(load))
-        lanes[i].append((d_, s_))
-        load[i] += s_.numel() * s_.element_size()
-
-    def one_step():
-        ready = torch.cuda.Event()
-        ready.record(main)
-        done = []
-        for cs, lane in zip(cstreams, lanes):
-            cs.wait_event(ready)
-            with torch.cuda.stream(cs):
-                for d_, s_ in lane:
-                    d_.copy_(s_, non_blocking=True)
-            ev = torch.cuda.Event()
-            ev.record(cs)
-            done.append(ev)
-        for ev in done:
-            main.wait_event(ev)
-        st.run(main, aux)
-        out_h.copy_(st.acc_out["out_tok"], non_blocking=True)
-        nout_h.copy_(st.acc_out["n_out"], non_blocking=True)
-
     s0 = torch.cuda.Event(enable_timing=True)
     s1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(main):
@@ -471,7 +434,11 @@ def run_e2e(args, wl, inp, st, main, aux, dev):
                 torch.cuda.synchronize()
                 s0.record(main)
             for _ in range(E if rep == 1 else 3):
-                one_step()
+                for k, h in host.items():
+                    st.x[k].copy_(h, non_blocking=True)
+                st.run(main, aux)
+                out_h.copy_(st.acc_out["out_tok"], non_blocking=True)
+                nout_h.copy_(st.acc_out["n_out"], non_blocking=True)
             if rep == 1:
                 s1.record(main)
     torch.cuda.synchronize()
