@@ -27,13 +27,15 @@
 //   warps 6-11 wait at the first cluster barrier and add threads to the merge.
 // TMEM columns: S buffers 0-127 and 128-255, O 256-383, P buffers 384-447 and
 // 448-511.
-// Merge: each softmax thread stages its row's un-normalised O (16-bit integers
-// after a power-of-two scale), max and sum in the CTA's idle ring; after a
-// cluster barrier (every ring is idle) one thread sends each other CTA of the
+// Merge: each row's un-normalised O is staged in the CTA's idle ring as 16-bit
+// integers, one power-of-two scale per 64-column half (warps 0-3 stage columns
+// 0-63, warps 6-9 columns 64-127), with the row's max and sum; after a cluster
+// barrier (every ring is idle) S-1 threads each send one other CTA of the
 // cluster the rows it owns (128/S each) with one bulk copy completing on that
-// CTA's mbarrier, and the owner combines the S copies and writes the output of
-// the tokens that exist. Which tokens exist comes from the retrieval, so only
-// warp 4's read of it waits for the preceding kernel (griddepcontrol.wait).
+// CTA's mbarrier, and every owner thread weights and sums the S copies of one
+// row's 16 columns and writes them for tokens that exist. Which tokens exist
+// comes from the retrieval, so only warp 4's read of it waits for the preceding
+// kernel (griddepcontrol.wait).
 // Every mbarrier wait is bounded (about 2^32 clocks); on expiry the CTA
 // records SSD_ERR_TIMEOUT in the workspace header, skips the remaining waits,
 // frees its TMEM and exits through the cluster barriers.
