@@ -205,6 +205,26 @@ class ClockSampler:
 KERNELS = ["gate_match", "verify_attn", "vocab_stats", "accept_finish"]
 
 
+def rank_seed(rank):
+    """Each rank verifies its own batch: independent synthetic inputs per rank."""
+    from speculative_decoding_copy_gb300 import workloads as WL
+    return WL.SEED_BASE + 1 + 1000 * rank
+
+
+def max_over_ranks(ms, device):
+    """The slowest rank's time (all ranks end the timed region behind a barrier)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(world, steps, ms):
+    """Steps of all ranks per second of the slowest rank (weak scaling: a batch per rank)."""
+    return world * steps / (ms / 1000.0)
+
+
 def source_sha(*names):
     h = hashlib.sha256()
     for n in names:
@@ -249,7 +269,7 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=dev)
 
     wl = WL.WORKLOADS[args.workload]
-    inp = WL.make_inputs(wl, WL.SEED_BASE + 1 + 1000 * rank)
+    inp = WL.make_inputs(wl, rank_seed(rank))
     ssd.lib()
 
     # rotating copies: total bytes above twice the L2
@@ -356,11 +376,9 @@ def run_ours(args):
         dist.barrier()
     ms = t_start.elapsed_time(t_end)
     if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = max_over_ranks(ms, dev)
     ms_per_step = ms / K
-    value = world * K / (ms / 1000.0)
+    value = whole_job_value(world, K, ms)
     dom_us = mean_us(ev_h, dom)
 
     # end to end through the public API with host buffers
