@@ -79,6 +79,23 @@ int ssd_version(void);
 uint64_t ssd_launch_count(void);
 
 /*
+ * ssd_selftest_wait — exercise the device-side failure detection.
+ *
+ * The pages have no counterpart; this tests the library's bounded waits without
+ * faulting or hanging the GPU. One CTA initialises an mbarrier in shared memory
+ * and waits on it with the same bounded wait the kernels use. With arrive != 0
+ * it arrives first and the wait completes; with arrive == 0 nothing arrives, so
+ * the wait gives up after limit_clocks SM clocks, records SSD_ERR_TIMEOUT in the
+ * header of `ws` (read back by ssd_read_device_error) and the kernel returns
+ * normally, leaving the context usable.
+ *   ws: device workspace of at least 256 bytes, 256-byte aligned (its header
+ *       must hold SSD_OK beforehand for the error to be recorded);
+ *   1 <= limit_clocks <= 2^32.
+ * Errors: SSD_ERR_INVALID, SSD_ERR_WORKSPACE, SSD_ERR_CUDA (launch failure).
+ */
+int ssd_selftest_wait(void* ws, int arrive, uint64_t limit_clocks, void* stream);
+
+/*
  * ssd_gate_match — probe gate and kappa-gram check.
  *
  * For each sequence b (n = ctx_len[b], the current token is ctx[b][n-1]):

@@ -25,7 +25,8 @@ SSD_CHAIN_NONE, SSD_CHAIN_WHEN_GATE_OFF, SSD_CHAIN_ALWAYS = 0, 1, 2
 
 EXPORTED = ["ssd_status_string", "ssd_version", "ssd_launch_count", "ssd_gate_match", "ssd_retrieve",
             "ssd_verify_attn_workspace_size", "ssd_verify_attn", "ssd_accept_workspace_size", "ssd_accept",
-            "ssd_read_device_error", "ssd_profile_kernel", "ssd_accept_static", "ssd_gate_retrieve"]
+            "ssd_read_device_error", "ssd_profile_kernel", "ssd_accept_static", "ssd_gate_retrieve",
+            "ssd_selftest_wait"]
 SSD_KERNEL = dict(vocab_stats=1, verify_attn=2, attn_combine=3, accept_finish=4, gate_match=6,
                   retrieve=7)
 
@@ -65,6 +66,8 @@ def lib() -> ctypes.CDLL:
         L.ssd_status_string.argtypes = [c_int]
         L.ssd_version.restype = c_int
         L.ssd_launch_count.restype = c_uint64
+        L.ssd_selftest_wait.restype = c_int
+        L.ssd_selftest_wait.argtypes = [c_void_p, c_int, ctypes.c_uint64, c_void_p]
         L.ssd_gate_match.restype = c_int
         L.ssd_gate_match.argtypes = [c_void_p, c_int64, c_void_p, c_int, c_void_p, c_int, c_int64, c_void_p, c_int,
                                      c_float, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
@@ -281,6 +284,11 @@ def ssd_accept(tgt, drf, blk_tok, blk_len, u_acc, u_fin, *, mode, kind, K=0, cha
     rc = lib().ssd_accept(ctypes.byref(args), _ptr(ws), ws.numel(), _stream(stream))
     _check("ssd_accept", rc)
     return outs
+
+
+def ssd_selftest_wait(ws, arrive, limit_clocks, stream=None):
+    """One CTA waits on an mbarrier with the library's bounded wait (arrived on, or never)."""
+    _check("ssd_selftest_wait", lib().ssd_selftest_wait(_ptr(ws), int(arrive), int(limit_clocks), _stream(stream)))
 
 
 def ssd_read_device_error(ws, stream=None) -> int:

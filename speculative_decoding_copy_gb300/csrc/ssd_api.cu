@@ -1,5 +1,5 @@
-// Library-wide entry points: status strings, version, launch counter and the
-// device error word.
+// Library-wide entry points: status strings, version, launch counter, the device
+// error word and the self-test of the bounded waits.
 #include "ssd_common.cuh"
 
 extern "C" const char* ssd_status_string(int status) {
@@ -51,4 +51,33 @@ extern "C" int ssd_read_device_error(void* ws, void* stream, int32_t* out) {
   }
   *out = host[0];
   return SSD_OK;
+}
+
+namespace ssd {
+// one CTA: an mbarrier that is arrived on (arrive != 0) or never, waited on with the
+// library's bounded wait
+__global__ void k_selftest_wait(WsHeader* hdr, int arrive, unsigned long long limit) {
+  __shared__ uint64_t bar;
+  __shared__ int failed;
+  if (threadIdx.x == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(&bar)))
+                 : "memory");
+    failed = 0;
+  }
+  __syncthreads();
+  if (arrive && threadIdx.x == 0)
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(&bar)))
+                 : "memory");
+  mbar_wait_bounded(&bar, 0, &failed, hdr, 99, limit);
+  __syncthreads();
+}
+}  // namespace ssd
+
+extern "C" int ssd_selftest_wait(void* ws, int arrive, uint64_t limit_clocks, void* stream) {
+  if (limit_clocks < 1 || limit_clocks > (1ull << 32)) return SSD_ERR_INVALID;
+  if (ws == nullptr || !ssd::aligned(ws, 256)) return SSD_ERR_WORKSPACE;
+  ssd::k_selftest_wait<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<ssd::WsHeader*>(ws), arrive,
+                                                                         static_cast<unsigned long long>(limit_clocks));
+  ssd::count_launch();
+  return ssd::check_launch();
 }

@@ -101,33 +101,10 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
                : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
 
 // Bounded wait; false once this CTA has given up (then every later wait returns at once).
 __device__ __forceinline__ bool mbar_wait(Bars& bars, uint64_t* bar, uint32_t parity, WsHeader* hdr, int where) {
-  if (mbar_try_wait(bar, parity)) return true;      // the common case: one probe, no bookkeeping
-  volatile int* failed = &bars.failed;
-  if (*failed) return false;
-  const unsigned long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (*failed) return false;
-    if (clock64() - t0 > kWaitClocks) {
-      *failed = 1;
-      record_error(hdr, SSD_ERR_TIMEOUT, where);
-      return false;
-    }
-  }
-  return true;
+  return mbar_wait_bounded(bar, parity, &bars.failed, hdr, where, kWaitClocks);
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {

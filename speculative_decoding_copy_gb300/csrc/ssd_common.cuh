@@ -97,6 +97,39 @@ __device__ __forceinline__ void record_error(WsHeader* h, int code, int where) {
   if (h != nullptr && atomicCAS(&h->err, 0, code) == 0) h->where = where;
 }
 
+// One probe of an mbarrier phase (shared memory of this CTA): true once the phase of the
+// given parity has completed.
+__device__ __forceinline__ bool mbar_probe(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(bar))), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// The library's bounded wait: after `limit` clocks without the phase completing it sets
+// *failed (so that the CTA's other waits return at once), records SSD_ERR_TIMEOUT with
+// `where` in the workspace header and returns false; it never traps.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* failed, WsHeader* hdr,
+                                                  int where, unsigned long long limit) {
+  if (mbar_probe(bar, parity)) return true;      // the common case: one probe, no bookkeeping
+  if (*failed) return false;
+  const unsigned long long t0 = clock64();
+  while (!mbar_probe(bar, parity)) {
+    if (*failed) return false;
+    if (clock64() - t0 > limit) {
+      *failed = 1;
+      record_error(hdr, SSD_ERR_TIMEOUT, where);
+      return false;
+    }
+  }
+  return true;
+}
+
 constexpr float kLog2e = 1.4426950408889634f;
 
 // 2^x, hardware approximation (MUFU), flush-to-zero
