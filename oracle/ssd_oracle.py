@@ -408,3 +408,42 @@ def verify_step(inp: dict, wl, mode=None, kind=None, attention_slots="all"):
         res.update(verify_step_accept(mode, kind, inp["tgt"], inp.get("drf"), blk_tok, blk_len,
                                       wl.W, wl.chain_policy, inp["u_acc"], inp["u_fin"]))
     return res
+
+
+# ---------------------------------------------------------------------------
+# after the step: committing the accepted candidates' keys and values
+#     [SD-anatomy §6, "KV 캐시 롤백(Rollback) 및 페이징 메모리 오버헤드 관리": the
+#     target holds the candidates' K/V to verify them, and what follows the first
+#     rejection must be released.] Here the candidates' K/V sit beside the cache, so
+#     the accepted ones are appended to it and the rejected ones never enter it.
+# ---------------------------------------------------------------------------
+def commit_kv(k_cache, v_cache, k_cand, v_cand, prefix_len, best_blk, n_out, Dmax):
+    """Append the accepted tokens' keys and values to the prefix cache.
+
+    For sequence b with chosen block k = best_blk[b] >= 0, the a = n_out[b] - 1
+    accepted tokens (the emitted tokens minus the final one, whose K/V the next
+    step computes) occupy candidate slots k*Dmax .. k*Dmax + a - 1; their rows of
+    every kv head become cache rows P_b .. P_b + a - 1 and prefix_len[b] grows by a.
+    A sequence whose cache has no room (P_b + a > P_max) is left unchanged and
+    flagged. Layouts as in verify_attention. Returns (k_cache', v_cache',
+    prefix_len', ok[B])."""
+    kc = np.array(k_cache, copy=True)
+    vc = np.array(v_cache, copy=True)
+    pl = np.array(prefix_len, dtype=np.int32, copy=True)
+    B, Hkv, P_max = kc.shape[:3]
+    ok = np.ones(B, dtype=bool)
+    for b in range(B):
+        k = int(best_blk[b])
+        a = int(n_out[b]) - 1 if k >= 0 else 0
+        if a <= 0:
+            continue
+        P = int(pl[b])
+        if P + a > P_max:
+            ok[b] = False
+            continue
+        for i in range(a):
+            slot = k * Dmax + i
+            kc[b, :, P + i, :] = k_cand[b, slot, :, :]
+            vc[b, :, P + i, :] = v_cand[b, slot, :, :]
+        pl[b] = P + a
+    return kc, vc, pl, ok
