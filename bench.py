@@ -396,6 +396,7 @@ def run_ours(args):
 
     # end to end through the public API with host buffers
     e2e = run_e2e(args, wl, inp, steps[0], main, aux, dev)
+    nxt = {"commit_kv": measure_commit(wl, main, dev)}
 
     hbm, peak_kind = measured_peaks()
     tflops_sus, tflops_kind = measured_tensor_peak()
@@ -452,12 +453,59 @@ def run_ours(args):
                 "roofline": roofline,
                 "kernels_us_diagnostic": kern_us,
                 "e2e": e2e,
+                "next": nxt,
                 "gpu_launches": launches_per_step * K,
                 "clocks": clk,
                 "cpu_baseline": cpu}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def measure_commit(wl, main, dev, calls=200):
+    """The commit of accepted keys/values (the step after the hot path) on the workload's
+    shapes with every token of a full block accepted: mean time per call over `calls`
+    graph-replayed calls, each preceded by a reset of prefix_len (a 4-byte copy per
+    sequence, included in the time)."""
+    import torch
+    from speculative_decoding_copy_gb300 import _binding as ssd
+    B, Hkv, dh, NT, D = wl.B, wl.Hkv, wl.dh, wl.NB * wl.Dmax, wl.D
+    P = 4096
+    es = 4 if wl.kv_dtype == "f32" else 2
+    dt = torch.float32 if es == 4 else torch.int16
+    kc = torch.zeros((B, Hkv, P + NT, dh), dtype=dt, device=dev)
+    vc = torch.zeros_like(kc)
+    kd = torch.ones((B, NT, Hkv, dh), dtype=dt, device=dev)
+    vd = torch.ones_like(kd)
+    p0 = torch.full((B,), P, dtype=torch.int32, device=dev)
+    pl = p0.clone()
+    best = torch.zeros(B, dtype=torch.int32, device=dev)
+    n_out = torch.full((B,), D + 1, dtype=torch.int32, device=dev)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(main):
+        for _ in range(3):
+            pl.copy_(p0)
+            ssd.ssd_commit_kv(kc, vc, kd, vd, pl, best, n_out, wl.Dmax, ws=ws, stream=main)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=main):
+        for _ in range(calls):
+            pl.copy_(p0)
+            ssd.ssd_commit_kv(kc, vc, kd, vd, pl, best, n_out, wl.Dmax, ws=ws, stream=main)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(main):
+        g.replay()
+        a.record(main)
+        g.replay()
+        b.record(main)
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) * 1000.0 / calls
+    nbytes = 2 * 2 * B * D * Hkv * dh * es            # K and V rows, read once and written once
+    return {"us_per_call": us, "bytes_per_call": nbytes, "achieved_gbs": nbytes / (us * 1e-6) / 1e9,
+            "bound": "latency (one CTA per sequence copying a few rows)",
+            "case": f"B={B}, {D} accepted tokens of block 0, {Hkv} kv heads, dh {dh}, prefix {P}",
+            "device_error": ssd.ssd_read_device_error(ws, main)}
 
 
 def run_e2e(args, wl, inp, st, main, aux, dev):

@@ -268,6 +268,42 @@ size_t ssd_accept_workspace_size(const ssd_accept_args* a);
 int ssd_accept(const ssd_accept_args* a, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * ssd_commit_kv — append the accepted tokens' keys and values to the prefix cache.
+ *
+ * Speculative Decoding 해부 page, §6 "KV 캐시 롤백(Rollback) 및 페이징 메모리
+ * 오버헤드 관리": the target holds the candidates' K/V to verify them and what
+ * follows the first rejection must be released. Here the candidates' K/V sit
+ * beside the cache (k_cand, v_cand), so after ssd_accept the accepted ones are
+ * appended and the rejected ones never enter it. For sequence b with chosen block
+ * k = best_blk[b] >= 0, the a = n_out[b] - 1 accepted tokens (all emitted tokens
+ * but the final one, whose K/V the next step computes) occupy candidate slots
+ * k*Dmax .. k*Dmax + a - 1; their rows of every kv head become cache rows
+ * prefix_len[b] .. prefix_len[b] + a - 1 and prefix_len[b] grows by a.
+ * Layouts (elements of `dtype`, SSD_F32 or SSD_BF16):
+ *   k_cache, v_cache [B][Hkv][P_max][dh]   (updated in place)
+ *   k_cand, v_cand   [B][NB*Dmax][Hkv][dh]
+ *   prefix_len [B] int32 (updated in place); best_blk [B], n_out [B] int32 (from
+ *   ssd_accept; read after the kernel before this one on the stream completes)
+ * A sequence whose cache has no room (prefix_len + a > P_max) is left unchanged and
+ * SSD_ERR_DEVICE is recorded in the workspace header. The regions must not overlap.
+ * Workspace: at least 256 bytes, 256-byte aligned (the status header).
+ */
+typedef struct {
+  void* k_cache;
+  void* v_cache;
+  const void* k_cand;
+  const void* v_cand;
+  int32_t* prefix_len;
+  const int32_t* best_blk;
+  const int32_t* n_out;
+  int dtype;
+  int B, NB, Dmax, Hkv, dh;
+  int64_t P_max;
+} ssd_commit_args;
+
+int ssd_commit_kv(const ssd_commit_args* a, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * ssd_accept_static — ssd_accept without a caller-provided workspace.
  *
  * The pages have no counterpart for this call; it exists for callers that

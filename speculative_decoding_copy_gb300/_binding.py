@@ -26,7 +26,7 @@ SSD_CHAIN_NONE, SSD_CHAIN_WHEN_GATE_OFF, SSD_CHAIN_ALWAYS = 0, 1, 2
 EXPORTED = ["ssd_status_string", "ssd_version", "ssd_launch_count", "ssd_gate_match", "ssd_retrieve",
             "ssd_verify_attn_workspace_size", "ssd_verify_attn", "ssd_accept_workspace_size", "ssd_accept",
             "ssd_read_device_error", "ssd_profile_kernel", "ssd_accept_static", "ssd_gate_retrieve",
-            "ssd_selftest_wait"]
+            "ssd_selftest_wait", "ssd_commit_kv"]
 SSD_KERNEL = dict(vocab_stats=1, verify_attn=2, attn_combine=3, accept_finish=4, gate_match=6,
                   retrieve=7)
 
@@ -42,6 +42,12 @@ class AttnArgs(ctypes.Structure):
                 ("v_cand", c_void_p), ("out", c_void_p), ("prefix_len", c_void_p), ("blk_len", c_void_p),
                 ("dtype", c_int), ("B", c_int), ("NB", c_int), ("Dmax", c_int), ("Hq", c_int), ("Hkv", c_int),
                 ("dh", c_int), ("P_max", c_int64), ("scale", c_float), ("out_dtype", c_int)]
+
+
+class CommitArgs(ctypes.Structure):
+    _fields_ = [("k_cache", c_void_p), ("v_cache", c_void_p), ("k_cand", c_void_p), ("v_cand", c_void_p),
+                ("prefix_len", c_void_p), ("best_blk", c_void_p), ("n_out", c_void_p), ("dtype", c_int),
+                ("B", c_int), ("NB", c_int), ("Dmax", c_int), ("Hkv", c_int), ("dh", c_int), ("P_max", c_int64)]
 
 
 class AcceptArgs(ctypes.Structure):
@@ -68,6 +74,8 @@ def lib() -> ctypes.CDLL:
         L.ssd_launch_count.restype = c_uint64
         L.ssd_selftest_wait.restype = c_int
         L.ssd_selftest_wait.argtypes = [c_void_p, c_int, ctypes.c_uint64, c_void_p]
+        L.ssd_commit_kv.restype = c_int
+        L.ssd_commit_kv.argtypes = [c_void_p, c_void_p, ctypes.c_size_t, c_void_p]
         L.ssd_gate_match.restype = c_int
         L.ssd_gate_match.argtypes = [c_void_p, c_int64, c_void_p, c_int, c_void_p, c_int, c_int64, c_void_p, c_int,
                                      c_float, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
@@ -289,6 +297,22 @@ def ssd_accept(tgt, drf, blk_tok, blk_len, u_acc, u_fin, *, mode, kind, K=0, cha
 def ssd_selftest_wait(ws, arrive, limit_clocks, stream=None):
     """One CTA waits on an mbarrier with the library's bounded wait (arrived on, or never)."""
     _check("ssd_selftest_wait", lib().ssd_selftest_wait(_ptr(ws), int(arrive), int(limit_clocks), _stream(stream)))
+
+
+def ssd_commit_kv(k_cache, v_cache, k_cand, v_cand, prefix_len, best_blk, n_out, Dmax, ws=None, stream=None):
+    """Append the accepted tokens' K/V rows (from ssd_accept's best_blk, n_out) to the prefix
+    cache in place and advance prefix_len. Returns the workspace (its header holds any
+    device-side error)."""
+    _need(k_cache, "k_cache", (torch.float32,) + _HALF, 4)
+    B, Hkv, P_max, dh = k_cache.shape
+    NT = k_cand.shape[1]
+    dt = SSD_F32 if k_cache.dtype == torch.float32 else SSD_BF16
+    args = CommitArgs(_ptr(k_cache), _ptr(v_cache), _ptr(k_cand), _ptr(v_cand), _ptr(prefix_len), _ptr(best_blk),
+                      _ptr(n_out), dt, B, NT // Dmax, Dmax, Hkv, dh, P_max)
+    if ws is None:
+        ws = torch.zeros(256, dtype=torch.uint8, device=k_cache.device)
+    _check("ssd_commit_kv", lib().ssd_commit_kv(ctypes.byref(args), _ptr(ws), ws.numel(), _stream(stream)))
+    return ws
 
 
 def ssd_read_device_error(ws, stream=None) -> int:
