@@ -179,6 +179,14 @@ int ssd_gate_retrieve(const int32_t* ctx, int64_t ctx_stride, const int32_t* ctx
  * Supported: dh in {64, 128}; Hq % Hkv == 0; 1 <= Dmax <= 256.
  * scale == 0 selects 1/sqrt(dh). Accumulation is fp32 whatever `dtype`.
  * out_dtype is `dtype` or SSD_F32 (an fp32 output for bf16 inputs).
+ * Paged prefix cache (block_table != NULL; bf16, dh 128 only, else
+ * SSD_ERR_UNSUPPORTED): the Speculative Decoding 해부 page's §6 names a
+ * PagedAttention pool for the cache. k_cache, v_cache are then pages of 128
+ * tokens, [num_pages][Hkv][128][dh], and key position p of sequence b is row
+ * p % 128 of page block_table[b][p / 128] (block_table [B][pages_per_seq] int32,
+ * prefix_len[b] <= 128 * pages_per_seq; pages may be shared by sequences). A page
+ * index outside [0, num_pages) records SSD_ERR_DEVICE and reads page 0. P_max is
+ * then unused.
  * Workspace: ssd_verify_attn_workspace_size(a) bytes, 256-byte aligned; its
  * contents need no initialisation. Device-side errors are recorded in it.
  */
@@ -196,6 +204,9 @@ typedef struct {
   int64_t P_max;
   float scale;
   int out_dtype;
+  const int32_t* block_table;
+  int pages_per_seq;
+  int64_t num_pages;
 } ssd_attn_args;
 
 size_t ssd_verify_attn_workspace_size(const ssd_attn_args* a);

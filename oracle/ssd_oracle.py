@@ -232,6 +232,33 @@ def verify_attention(q, k_cache, v_cache, k_cand, v_cand, prefix_len, blk_len,
     return out
 
 
+PAGE = 128              # tokens per page of a paged prefix cache
+
+
+def gather_pages(pages, block_table, P_max):
+    """The contiguous cache [B][Hkv][P_max][dh] that a paged one stands for: key
+    position p of sequence b is row p % PAGE of page block_table[b][p // PAGE]
+    (pages [num_pages][Hkv][PAGE][dh]; SD-anatomy §6 names a PagedAttention pool)."""
+    B = block_table.shape[0]
+    num_pages, Hkv, page, dh = pages.shape
+    assert page == PAGE
+    out = np.zeros((B, Hkv, P_max, dh), dtype=pages.dtype)
+    for b in range(B):
+        for p in range(P_max):
+            pg = int(block_table[b, p // PAGE])
+            if 0 <= pg < num_pages:
+                out[b, :, p, :] = pages[pg, :, p % PAGE, :]
+    return out
+
+
+def verify_attention_paged(q, k_pages, v_pages, block_table, k_cand, v_cand, prefix_len, blk_len,
+                           Dmax, dtype, slots=None):
+    """verify_attention over a paged prefix cache (see gather_pages)."""
+    P_max = PAGE * block_table.shape[1]
+    return verify_attention(q, gather_pages(k_pages, block_table, P_max), gather_pages(v_pages, block_table, P_max),
+                            k_cand, v_cand, prefix_len, blk_len, Dmax, dtype, slots)
+
+
 # ---------------------------------------------------------------------------
 # a6: vocabulary rows  [SD-anatomy §2 Phase 2: the target yields a next-token
 #     distribution at every verified position; §3: p and q are full-vocab

@@ -304,6 +304,12 @@ static int validate(const ssd_attn_args* a) {
   if (static_cast<long long>(a->B) * a->Hkv > 0x7fffffffLL) return SSD_ERR_UNSUPPORTED;
   if (a->dh != 64 && a->dh != 128) return SSD_ERR_UNSUPPORTED;
   if (a->P_max > (1LL << 30)) return SSD_ERR_UNSUPPORTED;
+  if (a->block_table != nullptr) {
+    if (a->dtype != SSD_BF16 || a->dh != 128) return SSD_ERR_UNSUPPORTED;
+    if (a->pages_per_seq < 1 || a->num_pages < 1) return SSD_ERR_INVALID;
+    if (a->num_pages * a->Hkv * 128LL >= (1LL << 31)) return SSD_ERR_UNSUPPORTED;
+    if (a->P_max > 128LL * a->pages_per_seq) return SSD_ERR_INVALID;
+  }
   if (a->B == 0) return SSD_OK;
   if (!a->q || !a->k_cand || !a->v_cand || !a->out || !a->prefix_len || !a->blk_len) return SSD_ERR_INVALID;
   if (a->P_max > 0 && (!a->k_cache || !a->v_cache)) return SSD_ERR_INVALID;
@@ -346,6 +352,7 @@ extern "C" int ssd_verify_attn(const ssd_attn_args* a, void* ws, size_t ws_bytes
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   if (attn_tc_applies(a)) return attn_tc_launch(a, ws, s);
+  if (a->block_table != nullptr) return SSD_ERR_UNSUPPORTED;   // paged caches: tensor-core path only
 
   const AttnLayout L = attn_layout(a);
   AttnParams p{};
