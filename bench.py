@@ -396,7 +396,7 @@ def run_ours(args):
 
     # end to end through the public API with host buffers
     e2e = run_e2e(args, wl, inp, steps[0], main, aux, dev)
-    nxt = {"commit_kv": measure_commit(wl, main, dev)}
+    nxt = {"commit_kv": measure_commit(wl, main, dev), "paged_attn": measure_paged(wl, steps[0], main, dev)}
 
     hbm, peak_kind = measured_peaks()
     tflops_sus, tflops_kind = measured_tensor_peak()
@@ -506,6 +506,53 @@ def measure_commit(wl, main, dev, calls=200):
             "bound": "latency (one CTA per sequence copying a few rows)",
             "case": f"B={B}, {D} accepted tokens of block 0, {Hkv} kv heads, dh {dh}, prefix {P}",
             "device_error": ssd.ssd_read_device_error(ws, main)}
+
+
+def measure_paged(wl, st, main, dev, calls=100):
+    """The verification attention alone on the workload's tensors, contiguous cache against
+    the same cache scattered into 128-token pages in reverse order (block table), each the
+    mean over `calls` graph-replayed launches."""
+    import torch
+    from speculative_decoding_copy_gb300 import _binding as ssd
+    x = st.x
+    B, Hkv, P_max, dh = x["k_cache"].shape
+    pps = -(-P_max // 128)
+    n = B * pps
+    kp = torch.zeros((n, Hkv, 128, dh), dtype=x["k_cache"].dtype, device=dev)
+    vp = torch.zeros_like(kp)
+    table = torch.arange(n - 1, -1, -1, dtype=torch.int32, device=dev).view(B, pps)
+    for b in range(B):
+        for j in range(pps):
+            r0, r1 = j * 128, min(P_max, (j + 1) * 128)
+            kp[int(table[b, j]), :, :r1 - r0] = x["k_cache"][b, :, r0:r1]
+            vp[int(table[b, j]), :, :r1 - r0] = x["v_cache"][b, :, r0:r1]
+    out = torch.empty_like(x["q"])
+    res = {}
+    for name, kc, vc, bt in (("contiguous", x["k_cache"], x["v_cache"], None), ("paged", kp, vp, table)):
+        a = ssd.attn_args(x["q"], kc, vc, x["k_cand"], x["v_cand"], x["prefix_len"], st.ret_out["blk_len"], wl.Dmax,
+                          out, block_table=bt)
+        ws = torch.zeros(max(256, ssd.ssd_verify_attn_workspace_size(a)), dtype=torch.uint8, device=dev)
+        run = lambda: ssd.ssd_verify_attn(x["q"], kc, vc, x["k_cand"], x["v_cand"], x["prefix_len"],
+                                          st.ret_out["blk_len"], wl.Dmax, out=out, ws=ws, stream=main, block_table=bt)
+        with torch.cuda.stream(main):
+            for _ in range(3):
+                run()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=main):
+            for _ in range(calls):
+                run()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(main):
+            g.replay()
+            e0.record(main)
+            g.replay()
+            e1.record(main)
+        torch.cuda.synchronize()
+        res[name + "_us"] = e0.elapsed_time(e1) * 1000.0 / calls
+        res[name + "_device_error"] = ssd.ssd_read_device_error(ws, main)
+    res["case"] = f"{wl.name} attention alone, back to back (L2 holds the {P_max}-key cache between launches)"
+    return res
 
 
 def run_e2e(args, wl, inp, st, main, aux, dev):

@@ -20,6 +20,9 @@ struct AttnParams {
   int out_f32;           // 1: fp32 output whatever the input type
   int S, chunk;          // KV splits and keys per split
   int chunk0;            // keys of split 0 (tensor-core path: it also takes the own-block tiles)
+  const int32_t* block_table;   // tensor-core path: paged cache [B][pages_per_seq], or null
+  int pages_per_seq;
+  int64_t num_pages;
   WsHeader* hdr;
   float* ws_ml;          // [rows][S][2]  running max and sum per split
   float* ws_o;           // [rows][S][dh] un-normalised output per split

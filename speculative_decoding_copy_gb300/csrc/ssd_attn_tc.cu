@@ -475,7 +475,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
       const int qz = b * NT + t_first;                     // rows past the sequence are masked or zero
       tma_load_4d(sbase + OFF_Q, &tmap_q, 0, 0, kvh, qz, &bars.q_full);
       tma_load_4d(sbase + OFF_Q + kHalf, &tmap_q, 64, 0, kvh, qz, &bars.q_full);
-      const int y0 = (b * p.Hkv + kvh) * static_cast<int>(p.P_max) + k0;
+      const int y0 = p.block_table != nullptr ? 0 : (b * p.Hkv + kvh) * static_cast<int>(p.P_max) + k0;
       for (int j = 0; j < nT; ++j) {
         const int s = j % STAGES;
         if (j >= STAGES) mbar_wait(bars, &bars.empty[s], ((j / STAGES) - 1) & 1, p.hdr, 20);
@@ -490,7 +490,16 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
           tma_load_3d(vd, &tmap_vc, 0, kvh, z, &bars.full_v[s]);
           tma_load_3d(vd + kHalf, &tmap_vc, 64, kvh, z, &bars.full_v[s]);
         } else {
-          const int y = y0 + (j - nC) * BN;
+          int y = y0 + (j - nC) * BN;
+          if (p.block_table != nullptr) {
+            // paged cache: this tile of 128 keys is one page; rows (page, kv head, 0..127)
+            int pg = __ldg(p.block_table + static_cast<int64_t>(b) * p.pages_per_seq + (k0 + (j - nC) * BN) / BN);
+            if (pg < 0 || pg >= p.num_pages) {
+              record_error(p.hdr, SSD_ERR_DEVICE, 26);
+              pg = 0;
+            }
+            y = (pg * p.Hkv + kvh) * BN;
+          }
           tma_load_2d(kd, &tmap_k, 0, y, &bars.full_k[s]);
           tma_load_2d(kd + kHalf, &tmap_k, 64, y, &bars.full_k[s]);
           mbar_expect_tx(&bars.full_v[s], 2 * kHalf);
@@ -835,7 +844,7 @@ bool attn_tc_applies(const ssd_attn_args* a) {
   if (a->dtype != SSD_BF16 || a->dh != tc::DH || a->P_max < 1) return false;
   if (!aligned(a->k_cache, 16) || !aligned(a->v_cache, 16) || !aligned(a->q, 16)) return false;
   if (!aligned(a->k_cand, 16) || !aligned(a->v_cand, 16) || !aligned(a->out, 16)) return false;
-  if (static_cast<long long>(a->B) * a->Hkv * a->P_max >= (1LL << 31)) return false;
+  if (a->block_table == nullptr && static_cast<long long>(a->B) * a->Hkv * a->P_max >= (1LL << 31)) return false;
   if (static_cast<long long>(a->B) * a->NB * a->Dmax >= (1LL << 31)) return false;
   if (a->B * a->Hkv > 65535) return false;
   // Q rows arrive by TMA as whole tokens: G must divide the 128 rows of a tile
@@ -864,7 +873,9 @@ int attn_tc_launch(const ssd_attn_args* a, void* ws, cudaStream_t s) {
   int S = 1, chunk = tc::BN, chunk0 = tc::BN;
   tc::choose_split(a, mtiles, &S, &chunk, &chunk0);
   CUtensorMap mq, mk, mv, mkc, mvc;
-  const uint64_t rows = static_cast<uint64_t>(a->B) * a->Hkv * a->P_max;
+  // K/V rows of the 2-D maps: [B][Hkv][P_max] contiguous, or [num_pages][Hkv][128] pages
+  const uint64_t rows = a->block_table != nullptr ? static_cast<uint64_t>(a->num_pages) * a->Hkv * tc::BN
+                                                  : static_cast<uint64_t>(a->B) * a->Hkv * a->P_max;
   const uint64_t slots = static_cast<uint64_t>(a->B) * NT;
   if (!tc::make_q_map(&mq, a->q, slots, G, a->Hkv) || !tc::make_kv_map(&mk, a->k_cache, rows) || !tc::make_kv_map(&mv, a->v_cache, rows) ||
       !tc::make_cand_map(&mkc, a->k_cand, slots, a->Hkv) || !tc::make_cand_map(&mvc, a->v_cand, slots, a->Hkv))
@@ -880,6 +891,9 @@ int attn_tc_launch(const ssd_attn_args* a, void* ws, cudaStream_t s) {
   p.chunk = chunk;
   p.chunk0 = chunk0;
   p.out_f32 = (a->out_dtype == SSD_F32) ? 1 : 0;
+  p.block_table = a->block_table;
+  p.pages_per_seq = a->pages_per_seq;
+  p.num_pages = a->num_pages;
   p.hdr = reinterpret_cast<WsHeader*>(ws);
 
   cudaLaunchConfig_t cfg = {};

@@ -126,3 +126,62 @@ def test_attention_tcgen05_and_simt_paths(prefix, G, monkeypatch):
             monkeypatch.delenv("SSD_ATTN_KERNEL", raising=False)
         errs[path] = _check_all(case, blk_len, Dmax, "bf16", out_f32=True)
     assert errs["tc"] <= TOL and errs["simt"] <= TOL
+
+
+def _paged(rng, cache_bits, spare=5):
+    """A contiguous cache [B][Hkv][P_max][dh] (bf16 bits) scattered into 128-token pages in
+    a random order, with unused pages of noise; returns (pages, block_table)."""
+    B, Hkv, P_max, dh = cache_bits.shape
+    pps = -(-P_max // 128)
+    n = B * pps + spare
+    order = rng.permutation(n)
+    pages = WL.f32_to_bf16_bits(rng.standard_normal((n, Hkv, 128, dh)).astype(np.float32))
+    table = np.zeros((B, pps), np.int32)
+    for b in range(B):
+        for j in range(pps):
+            pg = int(order[b * pps + j])
+            table[b, j] = pg
+            rows = cache_bits[b, :, j * 128:min(P_max, (j + 1) * 128)]
+            pages[pg, :, :rows.shape[1]] = rows
+    return pages, table
+
+
+@pytest.mark.parametrize("G,prefix", [(4, [0, 37, 300]), (1, [129, 256, 500]), (8, [4096, 1000, 2049])])
+def test_attention_paged_cache(G, prefix):
+    """The tensor-core pass reading its prefix through a block table of 128-token pages
+    (random page order, pages shared by two sequences) against the oracle."""
+    rng = np.random.default_rng(G + len(prefix) + prefix[0])
+    Hkv, B, NB, Dmax = 2, 3, 3, 5
+    case = _case(rng, B, NB, Dmax, Hkv * G, Hkv, 128, prefix, "bf16", q_scale=2.0)
+    blk_len = np.array([[5, 0, 3], [1, 5, 5], [2, 4, 0]], np.int32)
+    kp, table = _paged(rng, case["k_cache"])
+    vp = np.zeros_like(kp)
+    for b in range(B):
+        for j in range(table.shape[1]):
+            rows = case["v_cache"][b, :, j * 128:min(case["v_cache"].shape[2], (j + 1) * 128)]
+            vp[table[b, j], :, :rows.shape[1]] = rows
+    table[2, 0] = table[0, 0]                          # sequence 2 reads sequence 0's first page (a shared prompt)
+    dev = "cuda"
+    t = {k: to_device(np.asarray(v), dev) for k, v in case.items()}
+    out = S.ssd_verify_attn(t["q"], to_device(kp, dev), to_device(vp, dev), t["k_cand"], t["v_cand"], t["prefix_len"],
+                            to_device(blk_len, dev), Dmax, out_f32=True, block_table=to_device(table, dev))
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    ref = O.verify_attention_paged(case["q"], kp, vp, table, case["k_cand"], case["v_cand"], case["prefix_len"],
+                                   blk_len, Dmax, "bf16")
+    err = max(float(np.max(np.abs(got[b, t_] - o))) for (b, t_), o in ref.items())
+    assert err <= TOL, err
+
+
+def test_attention_paged_bad_page_is_reported():
+    rng = np.random.default_rng(77)
+    case = _case(rng, 1, 1, 4, 4, 1, 128, [300], "bf16")
+    kp, table = _paged(rng, case["k_cache"])
+    vp = kp.copy()
+    table[0, 1] = kp.shape[0] + 3                      # a page that does not exist
+    dev = "cuda"
+    t = {k: to_device(np.asarray(v), dev) for k, v in case.items()}
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device=dev)
+    S.ssd_verify_attn(t["q"], to_device(kp, dev), to_device(vp, dev), t["k_cand"], t["v_cand"], t["prefix_len"],
+                      to_device(np.array([[4]], np.int32), dev), 4, ws=ws, block_table=to_device(table, dev))
+    assert S.ssd_read_device_error(ws) == S.SSD_ERR_DEVICE
