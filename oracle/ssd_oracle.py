@@ -474,3 +474,24 @@ def commit_kv(k_cache, v_cache, k_cand, v_cand, prefix_len, best_blk, n_out, Dma
             vc[b, :, P + i, :] = v_cand[b, slot, :, :]
         pl[b] = P + a
     return kc, vc, pl, ok
+
+
+# ---------------------------------------------------------------------------
+# speculation tax  [SwitchSD "무엇인가": a copy draft opened by an accidental surface
+#     repetition is verified and accepted for 0 tokens, so the step pays the
+#     verification for nothing; "어떻게 쓰나" reports how often copying fires and the
+#     accepted length it gets]
+# ---------------------------------------------------------------------------
+def copy_stats(gate, n_cand, acc_len, W):
+    """Counts over a batch: copy attempts (gate on and at least one copy candidate), taxed
+    attempts (no copy block accepted a token), accepted copy tokens (over attempts, the
+    longest accepted run among the W copy blocks), sequences. Returns int64 [4]."""
+    attempts = taxed = tokens = 0
+    for b in range(len(gate)):
+        if not (int(gate[b]) != 0 and int(n_cand[b]) > 0):
+            continue
+        run = int(np.max(acc_len[b, :W])) if W > 0 else 0
+        attempts += 1
+        taxed += 1 if run == 0 else 0
+        tokens += run
+    return np.array([attempts, taxed, tokens, len(gate)], dtype=np.int64)
