@@ -396,7 +396,8 @@ def run_ours(args):
 
     # end to end through the public API with host buffers
     e2e = run_e2e(args, wl, inp, steps[0], main, aux, dev)
-    nxt = {"commit_kv": measure_commit(wl, main, dev), "paged_attn": measure_paged(wl, steps[0], main, dev)}
+    nxt = {"commit_kv": measure_commit(wl, main, dev), "paged_attn": measure_paged(wl, steps[0], main, dev),
+           "spec_tax": measure_tax(main, dev)}
 
     hbm, peak_kind = measured_peaks()
     tflops_sus, tflops_kind = measured_tensor_peak()
@@ -552,6 +553,63 @@ def measure_paged(wl, st, main, dev, calls=100):
         res[name + "_us"] = e0.elapsed_time(e1) * 1000.0 / calls
         res[name + "_device_error"] = ssd.ssd_read_device_error(ws, main)
     res["case"] = f"{wl.name} attention alone, back to back (L2 holds the {P_max}-key cache between launches)"
+    return res
+
+
+def measure_tax(main, dev, steps=50):
+    """The speculation-tax experiment: a batch in which every sequence ends in a repeated
+    5-gram, half copy-intended (probe high, the target follows the copy), half accidental
+    (probe low). For the surface gate (tau = 0) and the probe gate (tau = 0.4): copy
+    attempts, taxed attempts, mean accepted copy run per attempt (ssd_copy_stats), and the
+    step time (graphs of `steps` steps)."""
+    import dataclasses
+    import numpy as np
+    import torch
+    from speculative_decoding_copy_gb300 import _binding as ssd
+    from speculative_decoding_copy_gb300 import workloads as WL
+    from speculative_decoding_copy_gb300.step import VerifyStep
+    wl0 = WL.TAX_WORKLOAD
+    B = wl0.B
+    intended = np.zeros(B, bool)
+    intended[::2] = True
+    inp = WL.make_inputs(wl0, WL.SEED_BASE + 77, with_attention=False, gate_on=np.ones(B, bool), probe_on=intended)
+    # the candidates the surface gate retrieves (on the GPU), so that the target can follow
+    # the copy of the intended sequences
+    probe = VerifyStep(dataclasses.replace(wl0, tau=0.0), inp, device=dev, with_attention=False)
+    probe.gate_retrieve(main)
+    torch.cuda.synchronize()
+    bt, bl = probe.ret_out["blk_tok"].cpu().numpy(), probe.ret_out["blk_len"].cpu().numpy()
+    rows = {}
+    for b in np.flatnonzero(intended):
+        for k in range(wl0.NB):
+            for d in range(int(bl[b, k])):
+                rows[(int(b), 0 if d == 0 else 1 + k * wl0.Dmax + d - 1)] = int(bt[b, k, d])
+    inp["tgt"] = WL.boost_accepts(inp["tgt"], wl0.logit_dtype, rows)
+    res = {"case": wl0.description}
+    for tau in (0.0, 0.4):
+        wl = dataclasses.replace(wl0, tau=tau)
+        st = VerifyStep(wl, inp, device=dev, with_attention=False)
+        counts = torch.zeros(4, dtype=torch.int64, device=dev)
+        with torch.cuda.stream(main):
+            st.run(main)
+            ssd.ssd_copy_stats(st.gate_out["gate"], st.ret_out["n_cand"], st.acc_out["acc_len"], wl.W, counts,
+                               stream=main)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=main):
+            for _ in range(steps):
+                st.run(main)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(main):
+            g.replay()
+            e0.record(main)
+            g.replay()
+            e1.record(main)
+        torch.cuda.synchronize()
+        a, t, tok, n = (int(v) for v in counts.cpu().numpy())
+        res[f"tau_{tau}"] = {"copy_attempts": a, "taxed_attempts": t, "taxed_fraction": t / a if a else None,
+                             "mean_accepted_copy_run": tok / a if a else None, "sequences": n,
+                             "step_us": e0.elapsed_time(e1) * 1000.0 / steps}
     return res
 
 

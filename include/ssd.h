@@ -315,6 +315,26 @@ typedef struct {
 int ssd_commit_kv(const ssd_commit_args* a, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * ssd_copy_stats — count copy attempts and the speculation tax over a batch.
+ *
+ * SwitchSD page, "무엇인가": a copy draft opened by an accidental surface repetition
+ * is verified and accepted for 0 tokens, so the step pays the verification for
+ * nothing (the speculation tax); "어떻게 쓰나" reports how often copying fires and
+ * the accepted length it gets. Adds to counts[4] (int64, device memory, running
+ * totals across calls):
+ *   counts[0] += sequences with gate[b] != 0 and n_cand[b] > 0 (copy attempts)
+ *   counts[1] += those whose W copy blocks all accepted 0 tokens (taxed attempts)
+ *   counts[2] += over attempts, the longest accepted run among the copy blocks
+ *   counts[3] += B
+ * gate, n_cand [B] int32 (from ssd_gate_retrieve / ssd_retrieve); acc_len [B][NB]
+ * int32 (from ssd_accept; copy blocks are 0 .. W-1, NB >= W). Read after the
+ * kernel before this one on the stream completes. B == 0 launches nothing.
+ * Errors: SSD_ERR_INVALID (NULL pointer, W < 0 or NB < W).
+ */
+int ssd_copy_stats(const int32_t* gate, const int32_t* n_cand, const int32_t* acc_len, int B, int NB, int W,
+                   int64_t* counts, void* stream);
+
+/*
  * ssd_accept_static — ssd_accept without a caller-provided workspace.
  *
  * The pages have no counterpart for this call; it exists for callers that

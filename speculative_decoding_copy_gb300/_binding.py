@@ -26,7 +26,8 @@ SSD_CHAIN_NONE, SSD_CHAIN_WHEN_GATE_OFF, SSD_CHAIN_ALWAYS = 0, 1, 2
 EXPORTED = ["ssd_status_string", "ssd_version", "ssd_launch_count", "ssd_gate_match", "ssd_retrieve",
             "ssd_verify_attn_workspace_size", "ssd_verify_attn", "ssd_accept_workspace_size", "ssd_accept",
             "ssd_read_device_error", "ssd_profile_kernel", "ssd_accept_static", "ssd_gate_retrieve",
-            "ssd_selftest_wait", "ssd_commit_kv"]
+            "ssd_selftest_wait", "ssd_commit_kv",
+            "ssd_copy_stats"]
 SSD_KERNEL = dict(vocab_stats=1, verify_attn=2, attn_combine=3, accept_finish=4, gate_match=6,
                   retrieve=7)
 
@@ -77,6 +78,8 @@ def lib() -> ctypes.CDLL:
         L.ssd_selftest_wait.argtypes = [c_void_p, c_int, ctypes.c_uint64, c_void_p]
         L.ssd_commit_kv.restype = c_int
         L.ssd_commit_kv.argtypes = [c_void_p, c_void_p, ctypes.c_size_t, c_void_p]
+        L.ssd_copy_stats.restype = c_int
+        L.ssd_copy_stats.argtypes = [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p]
         L.ssd_gate_match.restype = c_int
         L.ssd_gate_match.argtypes = [c_void_p, c_int64, c_void_p, c_int, c_void_p, c_int, c_int64, c_void_p, c_int,
                                      c_float, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
@@ -325,6 +328,18 @@ def ssd_commit_kv(k_cache, v_cache, k_cand, v_cand, prefix_len, best_blk, n_out,
         ws = torch.zeros(256, dtype=torch.uint8, device=k_cache.device)
     _check("ssd_commit_kv", lib().ssd_commit_kv(ctypes.byref(args), _ptr(ws), ws.numel(), _stream(stream)))
     return ws
+
+
+def ssd_copy_stats(gate, n_cand, acc_len, W, counts, stream=None):
+    """Add this batch's copy attempts, taxed attempts, accepted copy tokens and sequences
+    to counts (int64 [4] on the device)."""
+    _need(acc_len, "acc_len", (torch.int32,), 2)
+    B, NB = acc_len.shape
+    if counts.dtype != torch.int64 or counts.numel() < 4 or not counts.is_cuda:
+        raise ValueError("counts: int64 device tensor of 4")
+    _check("ssd_copy_stats", lib().ssd_copy_stats(_ptr(gate), _ptr(n_cand), _ptr(acc_len), B, NB, int(W), _ptr(counts),
+                                                  _stream(stream)))
+    return counts
 
 
 def ssd_read_device_error(ws, stream=None) -> int:

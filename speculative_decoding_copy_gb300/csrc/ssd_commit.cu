@@ -1,4 +1,5 @@
-// Commit of the accepted candidates' keys and values to the prefix cache.
+// After the step: commit of the accepted candidates' keys and values to the prefix
+// cache, and the copy-attempt / speculation-tax counts.
 //
 // Speculative Decoding 해부 page, §6 "KV 캐시 롤백(Rollback) 및 페이징 메모리 오버헤드
 // 관리": the target holds the candidates' K/V to verify them, and what follows the first
@@ -91,6 +92,54 @@ extern "C" int ssd_commit_kv(const ssd_commit_args* a, void* ws, size_t ws_bytes
   const cudaError_t e = vec ? launch_pdl(k_commit_kv<true>, dim3(a->B), dim3(kCommitThreads), 0, s, *a, hdr)
                             : launch_pdl(k_commit_kv<false>, dim3(a->B), dim3(kCommitThreads), 0, s, *a, hdr);
   if (e != cudaSuccess) return SSD_ERR_CUDA;
+  count_launch();
+  return check_launch();
+}
+
+namespace ssd {
+constexpr int kStatThreads = 256;
+
+// one CTA: block sums of the four counts, added to the running totals
+__global__ void __launch_bounds__(kStatThreads)
+k_copy_stats(const int32_t* __restrict__ gate, const int32_t* __restrict__ n_cand, const int32_t* __restrict__ acc_len,
+             int B, int NB, int W, unsigned long long* counts) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __shared__ unsigned long long part[3][kStatThreads / 32];
+  unsigned long long c[3] = {0, 0, 0};
+  for (int b = threadIdx.x; b < B; b += kStatThreads) {
+    if (gate[b] == 0 || n_cand[b] <= 0) continue;
+    int run = 0;
+    for (int k = 0; k < W; ++k) run = max(run, acc_len[static_cast<int64_t>(b) * NB + k]);
+    c[0] += 1;
+    c[1] += run == 0 ? 1 : 0;
+    c[2] += static_cast<unsigned long long>(run);
+  }
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int i = 0; i < 3; ++i) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c[i] += __shfl_xor_sync(0xffffffffu, c[i], o);
+    if (lane == 0) part[i][wid] = c[i];
+  }
+  __syncthreads();
+  if (threadIdx.x < 3) {
+    unsigned long long t = 0;
+    for (int w = 0; w < kStatThreads / 32; ++w) t += part[threadIdx.x][w];
+    atomicAdd(counts + threadIdx.x, t);
+  }
+  if (threadIdx.x == 3) atomicAdd(counts + 3, static_cast<unsigned long long>(B));
+}
+}  // namespace ssd
+
+extern "C" int ssd_copy_stats(const int32_t* gate, const int32_t* n_cand, const int32_t* acc_len, int B, int NB, int W,
+                              int64_t* counts, void* stream) {
+  using namespace ssd;
+  if (B < 0 || W < 0 || NB < W || NB < 1) return SSD_ERR_INVALID;
+  if (B == 0) return SSD_OK;
+  if (!gate || !n_cand || !acc_len || !counts || !aligned(counts, 8)) return SSD_ERR_INVALID;
+  if (launch_pdl(k_copy_stats, dim3(1), dim3(kStatThreads), 0, static_cast<cudaStream_t>(stream), gate, n_cand, acc_len,
+                 B, NB, W, reinterpret_cast<unsigned long long*>(counts)) != cudaSuccess)
+    return SSD_ERR_CUDA;
   count_launch();
   return check_launch();
 }

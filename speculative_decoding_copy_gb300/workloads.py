@@ -143,6 +143,19 @@ WORKLOADS = {
 # order of the five workloads (small case first)
 WORKLOAD_ORDER = ["tiny", "llama8b", "batched", "llama70b", "qwen8b_mixed"]
 
+# the speculation-tax experiment: every sequence ends in a repeated kappa-gram, half of
+# them copy-intended (probe high, target follows the copy), half accidental (probe low,
+# target unrelated to the copy)
+TAX_WORKLOAD = Workload(
+    name="tax64", B=64, ctx_len=(1024, 1024), V=32000, zipf_s=1.1,
+    repeat_density=(0.1, 0.1), span_len=(20, 60), n_spans=0,
+    kappa=5, W=4, D=8, K=0, chain_policy=0,
+    d_probe=1024, h_dtype="bf16", tau=0.4,
+    Hq=8, Hkv=2, dh=128, kv_dtype="bf16", logit_dtype="f32", logit_var=3.0,
+    gate_on_frac=1.0,
+    description="speculation tax: B=64, ctx 1024, every sequence ends in a repeated 5-gram, "
+                "half copy-intended, half accidental; W=4 D=8, fp32 logits V=32000")
+
 
 # ---------------------------------------------------------------------------
 # helpers (sampling and bit layout only)
@@ -252,13 +265,15 @@ def logit_of(p: float) -> float:
 # ---------------------------------------------------------------------------
 def make_inputs(wl: Workload, seed: int | None = None, *, full_width: bool = True,
                 with_attention: bool = True, with_logits: bool = True,
-                ctx_lens=None, gate_on=None, q_scale: float = 1.0) -> dict:
+                ctx_lens=None, gate_on=None, q_scale: float = 1.0, probe_on=None) -> dict:
     """Draw one batch of inputs for workload `wl`.
 
     full_width: gate-on sequences get W extra copies of the tail's source span, so
         retrieval finds >= W candidates of full length D (measurement runs).
         False draws the number of extra copies from U{0..2W-1} (correctness runs).
-    ctx_lens / gate_on: optional per-sequence overrides.
+    ctx_lens / gate_on: optional per-sequence overrides (gate_on plants the copy tail and,
+        unless probe_on is given, sets the probe score high).
+    probe_on: optional per-sequence probe target (score 0.9 or 0.1) independent of the tail.
     q_scale: multiplies Q (sharper attention for tests).
     """
     if seed is None:
@@ -294,7 +309,8 @@ def make_inputs(wl: Workload, seed: int | None = None, *, full_width: bool = Tru
             _plant_copy_tail(rng, row, n, wl.kappa, wl.D, reps)
         ctx[b, :n] = row
 
-    alphas = np.where(gate_on, logit_of(0.9), logit_of(0.1))
+    probe_on = gate_on if probe_on is None else np.asarray(probe_on, dtype=bool)
+    alphas = np.where(probe_on, logit_of(0.9), logit_of(0.1))
     h, w = _probe_pair(rng, wl.d_probe, alphas, wl.h_dtype)
 
     out = dict(ctx=ctx, ctx_len=ctx_lens, h=h, w=w, gate_on_target=gate_on)
