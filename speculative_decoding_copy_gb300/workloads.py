@@ -391,3 +391,44 @@ def algorithmic_bytes(wl: Workload, prefix_len: np.ndarray, blk_len: np.ndarray)
     other = int(prefix_len.sum()) * 4 + blk_len.shape[0] * wl.d_probe * h_es + wl.d_probe * 4
     return dict(kv=kv, q_o=qo, kv_cand=kvc, logits=logits, other=other,
                 attn=kv + qo + kvc, total=kv + qo + kvc + logits + other, tokens=T)
+
+
+# ---------------------------------------------------------------------------
+# the SlimSpec low-rank draft head (a second workload; SlimSpec page,
+# "방법론: SlimSpec" / "아키텍처": r = d/8, evaluated on Llama-3.1-8B drafters at
+# batch 1 and 64)
+# ---------------------------------------------------------------------------
+@dataclass(frozen=True)
+class HeadWorkload:
+    name: str
+    M: int                    # rows of h (draft positions of a batch)
+    d: int                    # hidden size
+    r: int                    # rank
+    V: int                    # vocabulary
+    z_std: float              # standard deviation of the logits the weights produce
+    description: str = ""
+
+
+HEAD_WORKLOADS = {
+    # small: several 128-row vocabulary tiles and a ragged tail (V % 128 != 0), a
+    # rank that is not a multiple of 64, a batch that is not a multiple of 16
+    "head_small": HeadWorkload("head_small", M=5, d=512, r=72, V=1000, z_std=3.0,
+                               description="low-rank head d=512 r=72 V=1000, 5 rows"),
+    "head_llama8b_b1": HeadWorkload("head_llama8b_b1", M=1, d=4096, r=512, V=128256, z_std=3.0,
+                                    description="low-rank head d=4096 r=512 V=128256, batch 1"),
+    "head_llama8b_b64": HeadWorkload("head_llama8b_b64", M=64, d=4096, r=512, V=128256, z_std=3.0,
+                                     description="low-rank head d=4096 r=512 V=128256, batch 64"),
+}
+
+
+def make_head_inputs(hw: HeadWorkload, seed: int | None = None) -> dict:
+    """bf16 bit patterns: h [M][d] ~ N(0, 1), W_down [r][d] ~ N(0, 1/d),
+    W_up [V][r] ~ N(0, z_std^2 / r), so that W_down h has unit-variance entries
+    and the logits have standard deviation about z_std."""
+    if seed is None:
+        seed = SEED_BASE + 0x5E
+    rng = np.random.Generator(np.random.PCG64(seed))
+    h = rng.standard_normal((hw.M, hw.d), dtype=np.float32)
+    w_down = rng.standard_normal((hw.r, hw.d), dtype=np.float32) * np.float32(1.0 / math.sqrt(hw.d))
+    w_up = rng.standard_normal((hw.V, hw.r), dtype=np.float32) * np.float32(hw.z_std / math.sqrt(hw.r))
+    return {"h": f32_to_bf16_bits(h), "w_down": f32_to_bf16_bits(w_down), "w_up": f32_to_bf16_bits(w_up)}
