@@ -247,7 +247,7 @@ def source_sha(*names):
 
 
 KERNEL_SOURCES = {"vocab_stats": ("ssd_accept.cu", "ssd_accept.cuh", "ssd_common.cuh"),
-                  "verify_attn": ("ssd_attn.cu", "ssd_attn_tc.cu", "ssd_attn.cuh", "ssd_common.cuh")}
+                  "verify_attn": ("ssd_attn.cu", "ssd_attn_tc.cu", "ssd_attn.cuh", "ssd_tc.cuh", "ssd_common.cuh")}
 
 
 def dram_traffic(kernel, workload):

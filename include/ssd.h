@@ -335,6 +335,47 @@ int ssd_copy_stats(const int32_t* gate, const int32_t* n_cand, const int32_t* ac
                    int64_t* counts, void* stream);
 
 /*
+ * ssd_lowrank_head — the SlimSpec low-rank draft LM head with its softmax statistics.
+ *
+ * SlimSpec page ("SlimSpec: Low-Rank Draft LM-Head for Accelerated Speculative
+ * Decoding"), "방법론: SlimSpec" / "아키텍처": the drafter's logits are
+ * z = W_up (W_down h), W_down [r][d] compressing the hidden state to rank r (such
+ * as d/8) and W_up [V][r] projecting it to the whole vocabulary, in place of the
+ * full-rank z = W_full h. The draft distribution is q = softmax(z) (Speculative
+ * Decoding 해부 page, §3). For each of the M rows of h:
+ *   u = W_down h       fp32 accumulation, rounded to bf16 (the operand of the
+ *                      second product)
+ *   z = W_up u         fp32 accumulation
+ *   row_max[m] = max_v z_v;  lse[m] = log sum_v exp(z_v) (natural log), so that
+ *   q_v = exp(z_v - lse[m]);  argmax[m] = the lowest v with z_v = row_max[m]
+ *   (the greedy draft token);  logits [M][V] (when not NULL) receive z as fp32
+ *   (logits_dtype SSD_F32) or bf16 rounded to nearest even (SSD_BF16).
+ * Layouts: h [M][d], w_down [r][d], w_up [V][r], bf16, dense row-major, 16-byte
+ * aligned. row_max, lse [M] fp32; argmax [M] int32.
+ * Limits: 1 <= M <= 64 (larger batches: several calls), d and r multiples of 8,
+ * 8 <= r <= 1024, 1 <= V < 2^31 - 128; SSD_ERR_UNSUPPORTED otherwise (or off sm_103).
+ * Workspace: ssd_lowrank_head_workspace_size(a) bytes (0 for invalid arguments),
+ * 256-byte aligned: the status header, u, and per-CTA partial statistics. Three
+ * kernels run on `stream` (down projection, up projection with the statistics,
+ * per-row merge); outputs are complete when the last one finishes. A device-side
+ * wait that gives up records SSD_ERR_TIMEOUT in the header (ssd_read_device_error).
+ */
+typedef struct {
+  const void* h;
+  const void* w_down;
+  const void* w_up;
+  void* logits;           /* optional [M][V] */
+  int logits_dtype;       /* SSD_F32 or SSD_BF16 */
+  float* row_max;
+  float* lse;
+  int32_t* argmax;
+  int M, d, r, V;
+} ssd_head_args;
+
+size_t ssd_lowrank_head_workspace_size(const ssd_head_args* a);
+int ssd_lowrank_head(const ssd_head_args* a, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * ssd_accept_static — ssd_accept without a caller-provided workspace.
  *
  * The pages have no counterpart for this call; it exists for callers that
@@ -385,7 +426,10 @@ enum {
   SSD_KERNEL_ACCEPT_FINISH = 4,      /* merge, acceptance, choice and final draw */
   SSD_KERNEL_RESERVED_5 = 5,         /* unused */
   SSD_KERNEL_GATE_MATCH = 6,
-  SSD_KERNEL_RETRIEVE = 7
+  SSD_KERNEL_RETRIEVE = 7,
+  SSD_KERNEL_HEAD_DOWN = 8,          /* ssd_lowrank_head: u = W_down h */
+  SSD_KERNEL_HEAD_UP = 9,            /* ssd_lowrank_head: z = W_up u and its statistics */
+  SSD_KERNEL_HEAD_COMBINE = 10       /* ssd_lowrank_head: per-row merge */
 };
 int ssd_profile_kernel(int kernel_id, void* start_event, void* end_event);
 

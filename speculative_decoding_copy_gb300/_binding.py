@@ -27,9 +27,9 @@ EXPORTED = ["ssd_status_string", "ssd_version", "ssd_launch_count", "ssd_gate_ma
             "ssd_verify_attn_workspace_size", "ssd_verify_attn", "ssd_accept_workspace_size", "ssd_accept",
             "ssd_read_device_error", "ssd_profile_kernel", "ssd_accept_static", "ssd_gate_retrieve",
             "ssd_selftest_wait", "ssd_commit_kv",
-            "ssd_copy_stats"]
+            "ssd_copy_stats", "ssd_lowrank_head_workspace_size", "ssd_lowrank_head"]
 SSD_KERNEL = dict(vocab_stats=1, verify_attn=2, attn_combine=3, accept_finish=4, gate_match=6,
-                  retrieve=7)
+                  retrieve=7, head_down=8, head_up=9, head_combine=10)
 
 
 class SsdError(RuntimeError):
@@ -50,6 +50,12 @@ class CommitArgs(ctypes.Structure):
     _fields_ = [("k_cache", c_void_p), ("v_cache", c_void_p), ("k_cand", c_void_p), ("v_cand", c_void_p),
                 ("prefix_len", c_void_p), ("best_blk", c_void_p), ("n_out", c_void_p), ("dtype", c_int),
                 ("B", c_int), ("NB", c_int), ("Dmax", c_int), ("Hkv", c_int), ("dh", c_int), ("P_max", c_int64)]
+
+
+class HeadArgs(ctypes.Structure):
+    _fields_ = [("h", c_void_p), ("w_down", c_void_p), ("w_up", c_void_p), ("logits", c_void_p),
+                ("logits_dtype", c_int), ("row_max", c_void_p), ("lse", c_void_p), ("argmax", c_void_p),
+                ("M", c_int), ("d", c_int), ("r", c_int), ("V", c_int)]
 
 
 class AcceptArgs(ctypes.Structure):
@@ -80,6 +86,10 @@ def lib() -> ctypes.CDLL:
         L.ssd_commit_kv.argtypes = [c_void_p, c_void_p, ctypes.c_size_t, c_void_p]
         L.ssd_copy_stats.restype = c_int
         L.ssd_copy_stats.argtypes = [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p]
+        L.ssd_lowrank_head_workspace_size.restype = c_size_t
+        L.ssd_lowrank_head_workspace_size.argtypes = [POINTER(HeadArgs)]
+        L.ssd_lowrank_head.restype = c_int
+        L.ssd_lowrank_head.argtypes = [POINTER(HeadArgs), c_void_p, c_size_t, c_void_p]
         L.ssd_gate_match.restype = c_int
         L.ssd_gate_match.argtypes = [c_void_p, c_int64, c_void_p, c_int, c_void_p, c_int, c_int64, c_void_p, c_int,
                                      c_float, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
@@ -340,6 +350,59 @@ def ssd_copy_stats(gate, n_cand, acc_len, W, counts, stream=None):
     _check("ssd_copy_stats", lib().ssd_copy_stats(_ptr(gate), _ptr(n_cand), _ptr(acc_len), B, NB, int(W), _ptr(counts),
                                                   _stream(stream)))
     return counts
+
+
+def head_args(h, w_down, w_up, row_max, lse, argmax, logits=None) -> HeadArgs:
+    """Marshal the low-rank head's arguments (shapes and dtypes checked)."""
+    _need(h, "h", (torch.bfloat16,), 2)
+    _need(w_down, "w_down", (torch.bfloat16,), 2)
+    _need(w_up, "w_up", (torch.bfloat16,), 2)
+    M, d = h.shape
+    r, V = w_down.shape[0], w_up.shape[0]
+    if w_down.shape[1] != d or w_up.shape[1] != r:
+        raise ValueError("shapes: h [M][d], w_down [r][d], w_up [V][r]")
+    for t, n, dt in ((row_max, "row_max", torch.float32), (lse, "lse", torch.float32), (argmax, "argmax", torch.int32)):
+        _need(t, n, (dt,), 1)
+        if t.numel() != M:
+            raise ValueError(f"{n} must hold M = {M} values")
+    ldt = SSD_F32
+    if logits is not None:
+        _need(logits, "logits", (torch.float32, torch.bfloat16), 2)
+        if tuple(logits.shape) != (M, V):
+            raise ValueError(f"logits must be [{M}][{V}]")
+        ldt = SSD_F32 if logits.dtype == torch.float32 else SSD_BF16
+    return HeadArgs(_ptr(h), _ptr(w_down), _ptr(w_up), _ptr(logits), ldt, _ptr(row_max), _ptr(lse), _ptr(argmax),
+                    M, d, r, V)
+
+
+def ssd_lowrank_head_workspace_size(args: HeadArgs) -> int:
+    return int(lib().ssd_lowrank_head_workspace_size(ctypes.byref(args)))
+
+
+def ssd_lowrank_head(h, w_down, w_up, logits=None, logits_dtype=None, out=None, ws=None, stream=None):
+    """The low-rank draft head z = W_up (W_down h) with per-row max, log-sum-exp and first
+    argmax. h [M][d], w_down [r][d], w_up [V][r] bf16 on the device. logits_dtype
+    (torch.float32 / torch.bfloat16) asks for the logits [M][V]; out = (row_max, lse,
+    argmax[, logits]) reuses buffers. Returns (row_max, lse, argmax, logits or None, ws)."""
+    M, V = h.shape[0], w_up.shape[0]
+    dev = h.device
+    if out is not None:
+        row_max, lse, argmax = out[:3]
+        logits = out[3] if len(out) > 3 else None
+    else:
+        row_max = torch.empty(M, dtype=torch.float32, device=dev)
+        lse = torch.empty(M, dtype=torch.float32, device=dev)
+        argmax = torch.empty(M, dtype=torch.int32, device=dev)
+        logits = torch.empty(M, V, dtype=logits_dtype, device=dev) if logits_dtype is not None else None
+    args = head_args(h, w_down, w_up, row_max, lse, argmax, logits)
+    need = ssd_lowrank_head_workspace_size(args)
+    if need == 0:   # invalid or unsupported arguments: the call itself reports which
+        _check("ssd_lowrank_head", lib().ssd_lowrank_head(ctypes.byref(args), None, 0, _stream(stream)))
+        raise SsdError("ssd_lowrank_head_workspace_size", SSD_ERR_INVALID)
+    if ws is None or ws.numel() < need:
+        ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+    _check("ssd_lowrank_head", lib().ssd_lowrank_head(ctypes.byref(args), _ptr(ws), ws.numel(), _stream(stream)))
+    return row_max, lse, argmax, logits, ws
 
 
 def ssd_read_device_error(ws, stream=None) -> int:

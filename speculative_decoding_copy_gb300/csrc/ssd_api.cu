@@ -23,7 +23,7 @@ ProfileHook g_profile;
 
 extern "C" int ssd_profile_kernel(int kernel_id, void* start_event, void* end_event) {
   using ssd::g_profile;
-  if (kernel_id < SSD_KERNEL_NONE || kernel_id > SSD_KERNEL_RETRIEVE) return SSD_ERR_INVALID;
+  if (kernel_id < SSD_KERNEL_NONE || kernel_id > SSD_KERNEL_HEAD_COMBINE) return SSD_ERR_INVALID;
   if (kernel_id == SSD_KERNEL_NONE) {
     for (int i = 0; i < ssd::kProfileSlots; ++i) g_profile.on[i].store(0);
     return SSD_OK;

@@ -21,7 +21,7 @@ inline int check_launch() {
 }
 
 // measurement hook: events recorded around chosen kernels (ssd_profile_kernel)
-constexpr int kProfileSlots = 8;
+constexpr int kProfileSlots = 16;
 struct ProfileHook {
   std::atomic<int> on[kProfileSlots];
   cudaEvent_t start[kProfileSlots];
