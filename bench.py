@@ -49,6 +49,8 @@ def parse_args(argv=None):
     ap.add_argument("--two-streams", action="store_true",
                     help="run attention on a second stream beside the acceptance chain (default: one stream, "
                          "acceptance first, attention overlapping the finish kernel)")
+    ap.add_argument("--section", choices=["head"], default=None,
+                    help="run one extra measurement alone and print its JSON (head: the low-rank draft head)")
     ap.add_argument("--oracle-worker", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--oracle-seconds", type=float, default=20.0, help=argparse.SUPPRESS)
     return ap.parse_args(argv)
@@ -397,7 +399,7 @@ def run_ours(args):
     # end to end through the public API with host buffers
     e2e = run_e2e(args, wl, inp, steps[0], main, aux, dev)
     nxt = {"commit_kv": measure_commit(wl, main, dev), "paged_attn": measure_paged(wl, steps[0], main, dev),
-           "spec_tax": measure_tax(main, dev)}
+           "spec_tax": measure_tax(main, dev), "slimspec_head": measure_head(main, dev)}
 
     hbm, peak_kind = measured_peaks()
     tflops_sus, tflops_kind = measured_tensor_peak()
@@ -613,6 +615,108 @@ def measure_tax(main, dev, steps=50):
     return res
 
 
+def measure_head(main, dev, iters=20):
+    """The SlimSpec low-rank draft head on Llama-3.1-8B sizes (d 4096, r 512, V 128256) at
+    batch 64 and batch 1. Each call is timed alone with CUDA events after a 256 MiB write
+    that flushes L2, mean over `iters` calls after 3 warm-up calls:
+      ours_logits   ssd_lowrank_head writing fp32 logits and the statistics
+      ours_stats    ssd_lowrank_head, statistics only (max, log-sum-exp, argmax)
+      cublas_lowrank  the same product by cuBLAS (u = h W_down^T, z = u W_up^T) with torch
+                    logsumexp / max / argmax
+      cublas_fullrank the full-rank head the method replaces, z = h W_full^T, W_full [V][d]
+    k_head_up's own time comes from the profiling hook in a separate pass. Inputs are the
+    seeded synthetic weights of the head workloads; W_full is random bf16 on the device."""
+    import numpy as np
+    import torch
+    from speculative_decoding_copy_gb300 import _binding as ssd
+    from speculative_decoding_copy_gb300 import workloads as WL
+    hbm, peak_kind = measured_peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(WL.SEED_BASE + 0xF0)
+
+    def timed(fn):
+        with torch.cuda.stream(main):
+            for _ in range(3):
+                fn()
+            ts = []
+            for _ in range(iters):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(main)
+                fn()
+                e1.record(main)
+                ts.append((e0, e1))
+        torch.cuda.synchronize()
+        return float(np.mean([a.elapsed_time(b) * 1000.0 for a, b in ts]))
+
+    res = {"peak_gbs": hbm, "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth, burst)",
+           "l2": "256 MiB write before every timed call"}
+    w_full = None
+    for name in ("head_llama8b_b64", "head_llama8b_b1"):
+        hw = WL.HEAD_WORKLOADS[name]
+        x = WL.make_head_inputs(hw)
+        dv = lambda b: torch.from_numpy(b.view(np.int16).copy()).to(dev).view(torch.bfloat16)
+        h, wd, wu = dv(x["h"]), dv(x["w_down"]), dv(x["w_up"])
+        M, V, d, r = hw.M, hw.V, hw.d, hw.r
+        rm = torch.empty(M, dtype=torch.float32, device=dev)
+        ls = torch.empty(M, dtype=torch.float32, device=dev)
+        am = torch.empty(M, dtype=torch.int32, device=dev)
+        lg = torch.empty(M, V, dtype=torch.float32, device=dev)
+        ws = torch.zeros(ssd.ssd_lowrank_head_workspace_size(ssd.head_args(h, wd, wu, rm, ls, am, lg)),
+                         dtype=torch.uint8, device=dev)
+        ours_l = lambda: ssd.ssd_lowrank_head(h, wd, wu, out=(rm, ls, am, lg), ws=ws, stream=main)
+        ours_s = lambda: ssd.ssd_lowrank_head(h, wd, wu, out=(rm, ls, am), ws=ws, stream=main)
+
+        def cublas_low():
+            z = (h @ wd.t()) @ wu.t()
+            zf = z.float()
+            return torch.logsumexp(zf, dim=1), zf.max(dim=1)
+
+        if w_full is None:
+            w_full = torch.randn(V, d, generator=gen, device=dev, dtype=torch.float32).mul_(
+                hw.z_std / d ** 0.5).to(torch.bfloat16)
+
+        def cublas_full():
+            zf = (h @ w_full.t()).float()
+            return torch.logsumexp(zf, dim=1), zf.max(dim=1)
+
+        t = {"ours_logits_us": timed(ours_l), "ours_stats_us": timed(ours_s),
+             "cublas_lowrank_us": timed(cublas_low), "cublas_fullrank_us": timed(cublas_full)}
+        # k_head_up alone (the hook's event nodes sit between the three kernels)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ssd.ssd_profile_kernel("head_up", e0, e1)
+        up = []
+        with torch.cuda.stream(main):
+            for _ in range(iters):
+                flush.zero_()
+                ours_s()
+                torch.cuda.synchronize()
+                up.append(e0.elapsed_time(e1) * 1000.0)
+        ssd.ssd_profile_kernel(None)
+        t["head_up_us"] = float(np.mean(up))
+        w_bytes = V * r * 2 + r * d * 2
+        io = M * d * 2 + 2 * M * r * 2
+        b_stats = w_bytes + io
+        b_logits = b_stats + M * V * 4
+        t["bytes_stats"] = b_stats
+        t["bytes_logits"] = b_logits
+        t["achieved_gbs_stats"] = b_stats / (t["ours_stats_us"] * 1e-6) / 1e9
+        t["achieved_gbs_logits"] = b_logits / (t["ours_logits_us"] * 1e-6) / 1e9
+        t["frac_stats"] = t["achieved_gbs_stats"] / hbm
+        t["frac_logits"] = t["achieved_gbs_logits"] / hbm
+        t["head_up_bytes"] = V * r * 2 + M * r * 2
+        t["head_up_frac"] = t["head_up_bytes"] / (t["head_up_us"] * 1e-6) / 1e9 / hbm
+        t["speedup_vs_fullrank"] = t["cublas_fullrank_us"] / t["ours_stats_us"]
+        t["speedup_vs_cublas_lowrank"] = t["cublas_lowrank_us"] / t["ours_stats_us"]
+        torch.cuda.synchronize()
+        t["device_error"] = ssd.ssd_read_device_error(ws, main)
+        res[name] = t
+    del w_full, flush
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_e2e(args, wl, inp, st, main, aux, dev):
     """Same step through the public API with host inputs: every step copies its
     inputs host->device (pinned) and reads the emitted tokens back."""
@@ -657,6 +761,14 @@ def main():
         return
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.section == "head":
+        import torch
+        from speculative_decoding_copy_gb300 import _binding as ssd
+        ssd.lib()
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        print(json.dumps({"slimspec_head": measure_head(torch.cuda.Stream(dev), dev)}), flush=True)
         return
     run_ours(args)
 

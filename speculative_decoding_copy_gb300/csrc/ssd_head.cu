@@ -8,24 +8,30 @@
 // the caller asks for them.
 //
 // Three kernels, chained by programmatic dependent launch:
-//  k_head_down     u = W_down h. Grid (8, ceil(r/128)), clusters of 8 along d:
-//                  a CTA multiplies a 128-row tile of W_down (the M of the MMA)
-//                  by h (the N, the batch rows padded to 16) over its eighth of
-//                  d, in TMEM; the eight partial tiles meet in distributed shared
-//                  memory, where each CTA adds 16 of the rows in rank order and
+//  k_head_down     u = W_down h. Grid (CS, ceil(r/128)), clusters of CS = 16 CTAs
+//                  along d (8 where a 16-CTA cluster cannot be scheduled): a CTA
+//                  multiplies a 128-row tile of W_down (the M of the MMA) by h
+//                  (the N, the batch rows padded to 16) over its 1/CS of d, in
+//                  TMEM; the partial tiles meet in distributed shared memory,
+//                  where each CTA adds 128/CS of the rows in rank order and
 //                  writes them as bf16 (the second product's operand).
 //  k_head_up       z = W_up u and its statistics. One CTA per SM, a contiguous
 //                  range of 128-row vocabulary tiles each. u stays in shared
 //                  memory; W_up streams through a TMA ring whose first loads go
 //                  out before the wait for k_head_down (the weights do not
 //                  depend on it). The MMA thread fills one of two TMEM
-//                  accumulators while four epilogue warps reduce the other: per
-//                  batch column, the max, sum of exp and first argmax over the
-//                  tile's rows by warp reductions that transpose as they go.
+//                  accumulators while eight epilogue warps (a TMEM lane quarter
+//                  and 32 batch columns each) empty the other and fold it into
+//                  per-lane running statistics: for each batch column, the max,
+//                  the sum of exp(z - max) (one exponential per logit) and the
+//                  first row at the max. At the end of its range a warp merges
+//                  its 32 lanes per column with shuffles that transpose as they
+//                  go, and the four lane quarters are merged in order.
 //  k_head_combine  one CTA per batch row merges the per-CTA statistics in CTA
 //                  order.
-// Warp roles in the first two: warps 0-3 epilogue (one TMEM lane each), warp 4
-// TMEM allocation and TMA producer, warp 5 the single MMA-issuing thread.
+// Warp roles: in k_head_down warps 0-3 epilogue (one TMEM lane each), warp 4 TMEM
+// allocation and TMA producer, warp 5 the single MMA-issuing thread; in k_head_up
+// warps 0-7 epilogue, warp 8 TMEM allocation and producer, warp 9 MMA.
 // Every mbarrier wait is bounded; on expiry SSD_ERR_TIMEOUT is recorded in the
 // workspace header, the remaining waits return at once and the kernel exits
 // through its barriers after its copies in flight have landed.
@@ -43,7 +49,7 @@ constexpr int KAT = 64;                    // K elements per 128-byte swizzle at
 constexpr uint32_t kATile = BM * 128;      // one atom of a 128-row tile: 16 KB
 constexpr int kMaxRows = 64;               // rows of h per call
 constexpr int kMaxRank = 1024;
-constexpr int kCluster = 8;                // split of d in k_head_down
+constexpr int kClusterMax = 16;            // split of d in k_head_down (16, else 8 where 16 cannot be scheduled)
 constexpr int kThreads = 192;
 constexpr int kDownStages = 6;
 constexpr int kMaxUpStages = 16;
@@ -103,7 +109,7 @@ __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
 }
 
 // ------------------------------------------------------------------ k_head_down
-// grid (8, ceil(r/128)), cluster (8, 1, 1)
+// grid (CS, ceil(r/128)), cluster (CS, 1, 1)
 __global__ void __launch_bounds__(kThreads, 1)
 k_head_down(const __grid_constant__ CUtensorMap map_wd, const __grid_constant__ CUtensorMap map_h, HeadParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -115,9 +121,10 @@ k_head_down(const __grid_constant__ CUtensorMap map_wd, const __grid_constant__ 
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int q = static_cast<int>(cluster_rank());
+  const int CS = gridDim.x;                  // cluster size: the grid is one cluster wide
   const int rt = blockIdx.y;
   const int natoms = (p.d + KAT - 1) / KAT;
-  const int a0 = q * natoms / kCluster, n_at = (q + 1) * natoms / kCluster - a0;
+  const int a0 = q * natoms / CS, n_at = (q + 1) * natoms / CS - a0;
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
@@ -200,16 +207,17 @@ k_head_down(const __grid_constant__ CUtensorMap map_wd, const __grid_constant__ 
   tc_fence_before();
   cluster_sync();   // every CTA's partial tile is in its shared memory
 
-  // this CTA adds rows [16q, 16q + 16) of the tile over the 8 ranks, in rank order
-  if (tid < 128) {
-    const int row = q * (BM / kCluster) + (tid >> 3);
+  // this CTA adds rows [q RP, (q + 1) RP) of the tile over the CS ranks, in rank order
+  const int RP = BM / CS, nq = p.N / 4;
+  for (int it = tid; it < RP * nq; it += kThreads) {
+    const int row = q * RP + it / nq, c4 = it % nq;
     const int rg = rt * BM + row;
-    const uint32_t raddr = smem_u32(part + row * kPartStride);
-    for (int c4 = tid & 7; c4 < p.N / 4; c4 += 8) {
+    const uint32_t addr = smem_u32(part + row * kPartStride + c4 * 4);
+    {
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int pr = 0; pr < kCluster; ++pr) {
-        const float4 x = ld_dsmem_f4(map_peer(raddr + c4 * 16, static_cast<uint32_t>(pr)));
+#pragma unroll 4
+      for (int pr = 0; pr < CS; ++pr) {
+        const float4 x = ld_dsmem_f4(map_peer(addr, static_cast<uint32_t>(pr)));
         acc.x += x.x;
         acc.y += x.y;
         acc.z += x.z;
@@ -233,50 +241,8 @@ k_head_down(const __grid_constant__ CUtensorMap map_wd, const __grid_constant__ 
 }
 
 // ------------------------------------------------------------------ k_head_up
-// Warp-wide reduction of 32 columns (one value per lane and column) that
-// transposes as it goes: at each step a lane keeps half of its columns and
-// trades the other half with its partner, so after five steps lane L holds
-// column L reduced over all 32 lanes, for 31 shuffles instead of 160.
-template <int S, typename Op>
-__device__ __forceinline__ void transpose_step(float* t, int lane, Op op) {
-  const bool up = (lane & S) != 0;
-#pragma unroll
-  for (int i = 0; i < S; ++i) {
-    const float send = up ? t[i] : t[i + S];
-    const float keep = up ? t[i + S] : t[i];
-    t[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, S));
-  }
-}
-
-template <typename Op>
-__device__ __forceinline__ float transpose_reduce(float* t, int lane, Op op) {
-  transpose_step<16>(t, lane, op);
-  transpose_step<8>(t, lane, op);
-  transpose_step<4>(t, lane, op);
-  transpose_step<2>(t, lane, op);
-  transpose_step<1>(t, lane, op);
-  return t[0];
-}
-
-// Statistics of 32 batch columns over the warp's 32 rows (lane = row, z[j] =
-// column j): lane L receives column L's max, sum of exp(z - max) and the first
-// lane holding the max (-1 if no row is valid).
-__device__ __forceinline__ void column_stats(const float* z, bool valid, int lane, float& cmax, float& csum,
-                                             int& crow) {
-  float t[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) t[j] = valid ? z[j] : -INFINITY;
-  cmax = transpose_reduce(t, lane, [](float a, float b) { return fmaxf(a, b); });
-  crow = -1;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const float mj = __shfl_sync(0xffffffffu, cmax, j);
-    const unsigned hit = __ballot_sync(0xffffffffu, valid && z[j] == mj);
-    if (lane == j) crow = hit != 0u ? __ffs(static_cast<int>(hit)) - 1 : -1;
-    t[j] = valid ? ex2_approx((z[j] - mj) * kLog2e) : 0.f;
-  }
-  csum = transpose_reduce(t, lane, [](float a, float b) { return a + b; });
-}
+constexpr int kUpEpiWarps = 8;                        // TMEM lane quarter w % 4, column group w / 4
+constexpr int kUpThreads = 32 * (kUpEpiWarps + 2);    // + warp 8 producer, warp 9 MMA
 
 // (m, s, a) <- (m, s, a) merged with (m2, s2, a2); s is a sum of exp(z - m); the
 // argmax is the lowest index among equal maxima.
@@ -291,7 +257,30 @@ __device__ __forceinline__ void merge_stats(float& m, float& s, int& a, float m2
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// One step of a warp-wide merge of 32 column states (one per lane and column) that
+// transposes as it goes: a lane keeps half of its columns and trades the other half
+// with its partner, so after the five steps S = 16 .. 1 lane L holds column L merged
+// over all 32 lanes, for 31 exchanges per lane.
+template <int S>
+__device__ __forceinline__ void transpose_merge_step(float* m, float* s, int* a, int lane) {
+  const bool up = (lane & S) != 0;
+#pragma unroll
+  for (int i = 0; i < S; ++i) {
+    const float send_m = up ? m[i] : m[i + S], send_s = up ? s[i] : s[i + S];
+    const int send_a = up ? a[i] : a[i + S];
+    float km = up ? m[i + S] : m[i], ks = up ? s[i + S] : s[i];
+    int ka = up ? a[i + S] : a[i];
+    const float rm = __shfl_xor_sync(0xffffffffu, send_m, S);
+    const float rs = __shfl_xor_sync(0xffffffffu, send_s, S);
+    const int ra = __shfl_xor_sync(0xffffffffu, send_a, S);
+    merge_stats(km, ks, ka, rm, rs, ra);
+    m[i] = km;
+    s[i] = ks;
+    a[i] = ka;
+  }
+}
+
+__global__ void __launch_bounds__(kUpThreads, 1)
 k_head_up(const __grid_constant__ CUtensorMap map_wu, const __grid_constant__ CUtensorMap map_u, HeadParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -308,6 +297,7 @@ k_head_up(const __grid_constant__ CUtensorMap map_wu, const __grid_constant__ CU
   const int base = p.tiles / G, rem = p.tiles % G;
   const int t0 = c * base + min(c, rem), nt = base + (c < rem ? 1 : 0);
   const int total = nt * KA;   // ring loads of this CTA
+  const int ng = (p.M + 31) / 32;
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
@@ -318,12 +308,12 @@ k_head_up(const __grid_constant__ CUtensorMap map_wu, const __grid_constant__ CU
     mbar_init(&bars.u_full, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.acc_full[i], 1);
-      mbar_init(&bars.acc_empty[i], 4);
+      mbar_init(&bars.acc_empty[i], 4 * ng);   // one arrival per epilogue warp with columns
     }
     bars.failed = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 4) {
+  if (warp == kUpEpiWarps) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&bars.tmem_base)),
                  "r"(128)
                  : "memory");
@@ -337,7 +327,7 @@ k_head_up(const __grid_constant__ CUtensorMap map_wu, const __grid_constant__ CU
     return mbar_wait_bounded(bar, parity, &bars.failed, p.hdr, where, kWaitClocks);
   };
 
-  if (warp == 4 && lane == 0) {
+  if (warp == kUpEpiWarps && lane == 0) {
     prefetch_tmap(&map_wu);
     prefetch_tmap(&map_u);
     // ring load i: vocabulary tile t0 + i / KA, K atom i % KA
@@ -361,7 +351,7 @@ k_head_up(const __grid_constant__ CUtensorMap map_wu, const __grid_constant__ CU
       const int n_s = (i - 1 - s) / p.up_stages + 1;
       drain_wait(&bars.full[s], (n_s - 1) & 1);
     }
-  } else if (warp == 5 && lane == 0) {
+  } else if (warp == kUpEpiWarps + 1 && lane == 0) {
     const uint32_t idesc = idesc_bf16(false, static_cast<uint32_t>(p.N));
     bool ok = wait(&bars.u_full, 0, 71);
     int i = 0;
@@ -385,72 +375,89 @@ k_head_up(const __grid_constant__ CUtensorMap map_wu, const __grid_constant__ CU
       }
       mma_commit(&bars.acc_full[a]);
     }
-  } else if (warp < 4) {
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const int ng = (p.M + 31) / 32;
-    float rm[2] = {-INFINITY, -INFINITY}, rs[2] = {0.f, 0.f};
-    int ra[2] = {INT_MAX, INT_MAX};
-    for (int t = 0; t < nt; ++t) {
-      const int a = t & 1;
-      int ok = 0;
-      if (lane == 0) ok = wait(&bars.acc_full[a], (t >> 1) & 1, 74);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      tc_fence_after();
-      const int row0 = (t0 + t) * BM + warp * 32;
-      const int v = row0 + lane;
-      const bool valid = v < p.V;
+  } else if (warp < kUpEpiWarps) {
+    // rows 32*q4 .. +31 of each tile (this warp's TMEM lanes), columns 32*g .. 32*g + jn - 1
+    const int q4 = warp & 3, g = warp >> 2;
+    const int jn = min(32, p.M - 32 * g);
+    if (jn > 0) {
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + g * 32;
+      // per lane and column: running max, sum of exp(z - max), first row at the max
+      float m[32], s[32];
+      int a[32];
 #pragma unroll
-      for (int g = 0; g < 2; ++g) {
-        if (g >= ng) break;
+      for (int j = 0; j < 32; ++j) {
+        m[j] = -INFINITY;
+        s[j] = 0.f;
+        a[j] = INT_MAX;
+      }
+      for (int t = 0; t < nt; ++t) {
+        const int b = t & 1;
+        int ok = 0;
+        if (lane == 0) ok = wait(&bars.acc_full[b], (t >> 1) & 1, 74);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        tc_fence_after();
         uint32_t raw[32];
-        tmem_ld32(tmem + lane_off + a * 64 + g * 32, raw);
+        tmem_ld32(taddr + b * 64, raw);
         tmem_wait_ld();
-        float z[32];
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.acc_empty[b]);   // the accumulator is in registers
+        const int v = (t0 + t) * BM + q4 * 32 + lane;
+        if (v < p.V) {
+          if (p.logits != nullptr) {
+            if (p.logits_bf16) {
+              uint16_t* L = static_cast<uint16_t*>(p.logits) + static_cast<size_t>(g * 32) * p.V + v;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) z[j] = __uint_as_float(raw[j]);
-        if (p.logits != nullptr && valid) {
-          const int mend = min(32, p.M - g * 32);
-          if (p.logits_bf16) {
-            uint16_t* L = static_cast<uint16_t*>(p.logits) + static_cast<size_t>(g * 32) * p.V + v;
+              for (int j = 0; j < 32; ++j)
+                if (j < jn) L[static_cast<size_t>(j) * p.V] = f32_to_bf16(__uint_as_float(raw[j]));
+            } else {
+              float* L = static_cast<float*>(p.logits) + static_cast<size_t>(g * 32) * p.V + v;
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j < mend) L[static_cast<size_t>(j) * p.V] = f32_to_bf16(z[j]);
-          } else {
-            float* L = static_cast<float*>(p.logits) + static_cast<size_t>(g * 32) * p.V + v;
+              for (int j = 0; j < 32; ++j)
+                if (j < jn) L[static_cast<size_t>(j) * p.V] = __uint_as_float(raw[j]);
+            }
+          }
+          // online update: of exp(m - x) and exp(x - m) one factor is 1, so one exponential
+          // of -|x - m| serves both the rescale (new max) and the new term
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j < mend) L[static_cast<size_t>(j) * p.V] = z[j];
+          for (int j = 0; j < 32; ++j) {
+            if (j < jn) {
+              const float x = __uint_as_float(raw[j]);
+              const float mn = fmaxf(m[j], x);
+              const float e = ex2_approx((fminf(m[j], x) - mn) * kLog2e);
+              const bool grows = x > m[j];
+              s[j] = grows ? fmaf(s[j], e, 1.f) : s[j] + e;
+              a[j] = grows ? v : a[j];
+              m[j] = mn;
+            }
           }
         }
-        float cmax, csum;
-        int crow;
-        column_stats(z, valid, lane, cmax, csum, crow);
-        merge_stats(rm[g], rs[g], ra[g], cmax, csum, crow >= 0 ? row0 + crow : INT_MAX);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.acc_empty[a]);
+      // the warp's 32 rows merged per column: lane L ends with column 32*g + L
+      transpose_merge_step<16>(m, s, a, lane);
+      transpose_merge_step<8>(m, s, a, lane);
+      transpose_merge_step<4>(m, s, a, lane);
+      transpose_merge_step<2>(m, s, a, lane);
+      transpose_merge_step<1>(m, s, a, lane);
+      scratch[q4 * kMaxRows + g * 32 + lane] = make_float4(m[0], s[0], __int_as_float(a[0]), 0.f);
     }
-    // the four warps' statistics, merged in warp order per column
-#pragma unroll
-    for (int g = 0; g < 2; ++g)
-      scratch[warp * kMaxRows + g * 32 + lane] = make_float4(rm[g], rs[g], __int_as_float(ra[g]), 0.f);
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+    // the four lane quarters merged in order, one thread per column
+    asm volatile("bar.sync 1, %0;" ::"r"(kUpEpiWarps * 32) : "memory");
     if (tid < p.M) {
-      float4 s0 = scratch[tid];
-      float m = s0.x, s = s0.y;
+      const float4 s0 = scratch[tid];
+      float mm = s0.x, ss = s0.y;
       int am = __float_as_int(s0.z);
       for (int w = 1; w < 4; ++w) {
         const float4 x = scratch[w * kMaxRows + tid];
-        merge_stats(m, s, am, x.x, x.y, __float_as_int(x.z));
+        merge_stats(mm, ss, am, x.x, x.y, __float_as_int(x.z));
       }
-      p.parts[c * kMaxRows + tid] = make_float4(m, s, __int_as_float(am), 0.f);
+      p.parts[c * kMaxRows + tid] = make_float4(mm, ss, __int_as_float(am), 0.f);
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == kUpEpiWarps) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(128) : "memory");
   }
@@ -509,6 +516,41 @@ static int up_grid(const ssd_head_args* a) {
   const int tiles = (a->V + BM - 1) / BM;
   const int n = num_sms();
   return n > 0 ? min(n, tiles) : 0;
+}
+
+static size_t down_smem_bytes(int N) {
+  return 1024 + kDownStages * (kATile + static_cast<size_t>(N) * 128) + BM * kPartStride * 4 + sizeof(DownBars);
+}
+
+// 16 CTAs per cluster where the device can hold such a cluster of k_head_down at its
+// largest shared-memory size, else the portable 8 (per device, decided once)
+static int down_cluster_size() {
+  static int cache[64];
+  static std::once_flag once[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
+  std::call_once(once[dev], [dev] {
+    int cs = 8;
+    if (cudaFuncSetAttribute(k_head_down, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+        cudaFuncSetAttribute(k_head_down, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(kClusterMax, 1, 1);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = down_smem_bytes(kMaxRows);
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = kClusterMax;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, k_head_down, &cfg) == cudaSuccess && n >= 1) cs = kClusterMax;
+    }
+    cudaGetLastError();
+    cache[dev] = cs;
+  });
+  return cache[dev];
 }
 
 static size_t u_bytes(const ssd_head_args* a) { return round_up(static_cast<size_t>(a->M) * a->r * 2, 256); }
@@ -586,9 +628,9 @@ extern "C" int ssd_lowrank_head(const ssd_head_args* a, void* ws, size_t ws_byte
   p.up_stages = min(kMaxUpStages, static_cast<int>((kSmemLimit - up_fixed) / kATile));
   if (p.up_stages < 2) return SSD_ERR_UNSUPPORTED;
   const size_t up_smem = up_fixed + static_cast<size_t>(p.up_stages) * kATile;
-  const size_t down_smem =
-      1024 + kDownStages * (kATile + static_cast<size_t>(p.N) * 128) + BM * kPartStride * 4 + sizeof(DownBars);
+  const size_t down_smem = down_smem_bytes(p.N);
   if (down_smem > static_cast<size_t>(kSmemLimit)) return SSD_ERR_UNSUPPORTED;
+  const int CS = down_cluster_size();
 
   CUtensorMap m_wd, m_h, m_wu, m_u;
   if (!make_map(&m_wd, a->w_down, a->d, a->r, BM) || !make_map(&m_h, a->h, a->d, a->M, p.N) ||
@@ -599,12 +641,12 @@ extern "C" int ssd_lowrank_head(const ssd_head_args* a, void* ws, size_t ws_byte
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = kCluster;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(CS);
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kCluster, static_cast<unsigned>((a->r + BM - 1) / BM), 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(CS), static_cast<unsigned>((a->r + BM - 1) / BM), 1);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = down_smem;
     cfg.stream = s;
@@ -616,7 +658,7 @@ extern "C" int ssd_lowrank_head(const ssd_head_args* a, void* ws, size_t ws_byte
   {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(G));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kUpThreads);
     cfg.dynamicSmemBytes = up_smem;
     cfg.stream = s;
     cfg.attrs = attr;
