@@ -717,19 +717,60 @@ def measure_head(main, dev, iters=20):
     return res
 
 
+def _cpulist(text):
+    cpus = set()
+    for part in text.strip().split(","):
+        if "-" in part:
+            a, b = part.split("-")
+            cpus.update(range(int(a), int(b) + 1))
+        elif part:
+            cpus.add(int(part))
+    return cpus
+
+
+def gpu_local_cpus(dev):
+    """(NUMA node, CPUs of that node this process may run on) for the host node the GPU
+    hangs off, read from sysfs; (None, None) when the topology cannot be read."""
+    import torch
+    try:
+        pr = torch.cuda.get_device_properties(dev)
+        addr = "%04x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+        base = os.path.join("/sys/bus/pci/devices", addr)
+        node = int(open(os.path.join(base, "numa_node")).read())
+        cpus = _cpulist(open(os.path.join(base, "local_cpulist")).read()) & os.sched_getaffinity(0)
+        return (node, cpus) if node >= 0 and cpus else (None, None)
+    except (AttributeError, OSError, ValueError):
+        return None, None
+
+
+def pinned_like(tensors, dev):
+    """Pinned host copies of `tensors`, allocated while this thread runs on the GPU's own
+    host node, so that the pages (placed by first touch) sit next to the GPU and the copy
+    engines do not cross the CPU-to-CPU link. Returns (copies, node used or None)."""
+    import torch
+    node, cpus = gpu_local_cpus(dev)
+    before = os.sched_getaffinity(0)
+    if cpus:
+        os.sched_setaffinity(0, cpus)
+    try:
+        out = {}
+        for k, t in tensors.items():
+            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            h.copy_(t.cpu())
+            out[k] = h
+    finally:
+        if cpus:
+            os.sched_setaffinity(0, before)
+    return out, node
+
+
 def run_e2e(args, wl, inp, st, main, aux, dev):
     """Same step through the public API with host inputs: every step copies its
     inputs host->device (pinned) and reads the emitted tokens back."""
     import torch
-    from speculative_decoding_copy_gb300.step import to_device  # noqa: F401
 
-    host = {}
-    for k, t in st.x.items():
-        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-        h.copy_(t.cpu())
-        host[k] = h
-    out_h = torch.empty(st.acc_out["out_tok"].shape, dtype=torch.int32, pin_memory=True)
-    nout_h = torch.empty(st.acc_out["n_out"].shape, dtype=torch.int32, pin_memory=True)
+    host, node = pinned_like(dict(st.x, out_tok=st.acc_out["out_tok"], n_out=st.acc_out["n_out"]), dev)
+    out_h, nout_h = host.pop("out_tok"), host.pop("n_out")
     h2d = sum(h.numel() * h.element_size() for h in host.values())
     d2h = out_h.numel() * 4 + nout_h.numel() * 4
     E = args.e2e_steps
@@ -751,7 +792,7 @@ def run_e2e(args, wl, inp, st, main, aux, dev):
     torch.cuda.synchronize()
     ms = s0.elapsed_time(s1)
     return {"value": E / (ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": E}
+            "steps": E, "host_buffers_numa_node": node}
 
 
 def main():

@@ -994,8 +994,9 @@ extern "C" int ssd_accept_static(const ssd_accept_args* a, void* stream) {
   void* ws = nullptr;
   const int rc = static_scratch(&ws);
   if (rc != SSD_OK) return rc;
-  // Nothing in the scratch has to start at zero: the select kernel sets every
-  // sampler completion counter before the sampler reads it.
+  // Nothing in the scratch has to start at zero: the row pass writes every
+  // partial row statistic and the finish kernel every merged one before either
+  // is read, and the error header is only ever written here, never read back.
   const AcceptParams p = accept_params(a, L, static_cast<char*>(ws));
   return accept_launch(p, static_cast<cudaStream_t>(stream));
 }
