@@ -193,3 +193,52 @@ def test_chi_square_first_token_distribution_equals_p(V):
     expected = p.astype(np.float64) / p.sum() * N
     chi2, pval = scipy.stats.chisquare(counts, expected)
     assert pval > 0.01, (chi2, pval)
+
+
+# ---- several copy blocks: the choice of the longest (sample mode) ---------------
+def _two_block_categories(p, p1row, p2row, x1, x2):
+    """Joint law of (chosen block, tokens emitted) for two one-token copy blocks with
+    candidates x1 (block 0) and x2 (block 1), derived by hand from the rules: block k
+    accepts with probability p(x_k) (one-hot q); the longer run wins, ties go to block 0;
+    an accepted block adds a bonus token from the row after its token; when both reject,
+    block 0 is chosen and its residual is p without x1."""
+    V = len(p)
+    pa, pb = float(p[x1]), float(p[x2])
+    cats = {}
+    for y in range(V):
+        cats[(0, 2, x1, y)] = pa * float(p1row[y])
+        cats[(1, 2, x2, y)] = (1.0 - pa) * pb * float(p2row[y])
+        if y != x1:
+            cats[(0, 1, y, -1)] = (1.0 - pb) * float(p[y])
+    return cats
+
+
+def test_two_copy_blocks_follow_their_closed_form_and_are_not_lossless():
+    """Pins the selection across blocks in sample mode (the pages make no losslessness
+    claim for it): longest run, lowest block on ties, residual of the chosen block."""
+    rng = np.random.default_rng(2024)
+    V, x1, x2 = 6, 1, 4
+    p, p1row, p2row = (rng.dirichlet(np.full(V, 2.0)).astype(np.float32) for _ in range(3))
+    N = 200_000
+    tgt = np.broadcast_to(np.stack([p, p1row, p2row])[None], (N, 3, V))
+    blk_tok = np.broadcast_to(np.array([[[x1], [x2]]], np.int32), (N, 2, 1))
+    u_acc = (rng.integers(0, 1 << 24, size=(N, 2, 1)) * 2.0 ** -24).astype(np.float32)
+    u_fin = (rng.integers(0, 1 << 24, size=N) * 2.0 ** -24).astype(np.float32)
+    r = O.verify_step_accept("sample", "probs_f32", tgt, None, blk_tok, np.ones((N, 2), np.int32), 2, 0,
+                             u_acc, u_fin)
+    cats = _two_block_categories(p.astype(np.float64), p1row, p2row, x1, x2)
+    assert abs(sum(cats.values()) - 1.0) < 1e-6
+    keys = list(cats)
+    index = {k: i for i, k in enumerate(keys)}
+    counts = np.zeros(len(keys), np.int64)
+    for b in range(N):
+        n = int(r["n_out"][b])
+        key = (int(r["best_blk"][b]), n, int(r["out_tok"][b, 0]), int(r["out_tok"][b, 1]) if n == 2 else -1)
+        counts[index[key]] += 1          # a KeyError is an outcome the rules cannot produce
+    expected = np.array([cats[k] for k in keys]) * N
+    chi2, pval = scipy.stats.chisquare(counts, expected / expected.sum() * N)
+    assert pval > 0.01, (chi2, pval)
+    # the first emitted token does not follow p: x2 is favoured (p2 (2 - p1 - p2) > p2)
+    first = np.bincount(r["out_tok"][:, 0], minlength=V)
+    _, pval_p = scipy.stats.chisquare(first, p.astype(np.float64) / p.sum() * N)
+    assert pval_p < 1e-6
