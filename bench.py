@@ -49,6 +49,9 @@ def parse_args(argv=None):
     ap.add_argument("--two-streams", action="store_true",
                     help="run attention on a second stream beside the acceptance chain (default: one stream, "
                          "acceptance first, attention overlapping the finish kernel)")
+    ap.add_argument("--order", choices=["rows_first", "attn_first"], default="rows_first",
+                    help="one-stream kernel order: rows_first = retrieval, row pass, finish, attention; "
+                         "attn_first = retrieval, attention, row pass (early mode) beside it, finish")
     ap.add_argument("--section", choices=["head"], default=None,
                     help="run one extra measurement alone and print its JSON (head: the low-rank draft head)")
     ap.add_argument("--oracle-worker", action="store_true", help=argparse.SUPPRESS)
@@ -288,7 +291,7 @@ def run_ours(args):
     ssd.lib()
 
     # rotating copies: total bytes above twice the L2
-    probe = VerifyStep(wl, inp, device=dev)
+    probe = VerifyStep(wl, inp, device=dev, order=args.order)
     main = torch.cuda.Stream(dev)
     aux = torch.cuda.Stream(dev) if args.two_streams else None
     with torch.cuda.stream(main):
@@ -298,7 +301,7 @@ def run_ours(args):
     prefix = inp["prefix_len"]
     ab = WL.algorithmic_bytes(wl, prefix, blk_len)
     R = max(3, min(16, math.ceil(2 * L2_BYTES / max(ab["total"], 1)) + 1))
-    steps = [probe] + [VerifyStep(wl, inp, device=dev) for _ in range(R - 1)]
+    steps = [probe] + [VerifyStep(wl, inp, device=dev, order=args.order) for _ in range(R - 1)]
     tokens = ab["tokens"]
 
     def capture(idx, hooked):
@@ -450,7 +453,8 @@ def run_ours(args):
                 "dtype": "bf16/f32", "data": "synthetic",
                 "config": workload_config(wl, tokens, {
                     "l2": f"{R} rotating input copies ({R * step_bytes / 2**20:.0f} MiB > 2x L2); no flush",
-                    "parallelism": f"replicas x{world} (independent batches per GPU)"}),
+                    "parallelism": f"replicas x{world} (independent batches per GPU)",
+                    "step_order": "two streams" if args.two_streams else args.order}),
                 "candidate_tokens_per_s": value * tokens,
                 "hbm_roofline_step": step_roof,
                 "roofline": roofline,
@@ -765,34 +769,61 @@ def pinned_like(tensors, dev):
 
 
 def run_e2e(args, wl, inp, st, main, aux, dev):
-    """Same step through the public API with host inputs: every step copies its
-    inputs host->device (pinned) and reads the emitted tokens back."""
+    """Same step through the public API with host inputs. Every step copies all of its
+    inputs host->device from one pinned buffer (one copy into the step's input arena)
+    and reads the emitted tokens back. Two input arenas alternate: the copy of step i+1
+    runs on a copy stream while step i computes, and a copy into an arena waits until
+    the step that last read it has finished."""
     import torch
+    from speculative_decoding_copy_gb300.step import VerifyStep, arena_bytes
 
-    host, node = pinned_like(dict(st.x, out_tok=st.acc_out["out_tok"], n_out=st.acc_out["n_out"]), dev)
-    out_h, nout_h = host.pop("out_tok"), host.pop("n_out")
-    h2d = sum(h.numel() * h.element_size() for h in host.values())
-    d2h = out_h.numel() * 4 + nout_h.numel() * 4
+    nbytes = arena_bytes(inp, True)
+    slots = [VerifyStep(wl, inp, device=dev, order=st.order,
+                        arena=torch.empty(nbytes, dtype=torch.uint8, device=dev)) for _ in range(2)]
+    bufs = {"arena": slots[0].arena}
+    for j, s in enumerate(slots):
+        bufs[f"out_tok{j}"] = s.acc_out["out_tok"]
+        bufs[f"n_out{j}"] = s.acc_out["n_out"]
+    host, node = pinned_like(bufs, dev)
+    h2d = host["arena"].numel()
+    d2h = host["out_tok0"].numel() * 4 + host["n_out0"].numel() * 4
+    copy = torch.cuda.Stream(dev)
     E = args.e2e_steps
+
+    def run(n, t0=None, t1=None):
+        copied = [torch.cuda.Event() for _ in range(2)]
+        freed = [torch.cuda.Event() for _ in range(2)]
+        if t0 is not None:
+            t0.record(main)
+        for j in range(2):
+            freed[j].record(main)
+        for i in range(n):
+            j = i % 2
+            s = slots[j]
+            copy.wait_event(freed[j])
+            with torch.cuda.stream(copy):
+                s.arena.copy_(host["arena"], non_blocking=True)
+            copied[j].record(copy)
+            main.wait_event(copied[j])
+            with torch.cuda.stream(main):
+                s.run(main, aux)
+                host[f"out_tok{j}"].copy_(s.acc_out["out_tok"], non_blocking=True)
+                host[f"n_out{j}"].copy_(s.acc_out["n_out"], non_blocking=True)
+            freed[j].record(main)
+        if t1 is not None:
+            t1.record(main)
+
+    run(4)
+    torch.cuda.synchronize()
     s0 = torch.cuda.Event(enable_timing=True)
     s1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(main):
-        for rep in range(2):
-            if rep == 1:
-                torch.cuda.synchronize()
-                s0.record(main)
-            for _ in range(E if rep == 1 else 3):
-                for k, h in host.items():
-                    st.x[k].copy_(h, non_blocking=True)
-                st.run(main, aux)
-                out_h.copy_(st.acc_out["out_tok"], non_blocking=True)
-                nout_h.copy_(st.acc_out["n_out"], non_blocking=True)
-            if rep == 1:
-                s1.record(main)
+    run(E, s0, s1)
     torch.cuda.synchronize()
     ms = s0.elapsed_time(s1)
     return {"value": E / (ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": E, "host_buffers_numa_node": node}
+            "steps": E, "host_buffers_numa_node": node,
+            "copies": "one host-to-device copy of a pinned input arena per step; two arenas alternate so "
+                      "that step i+1's copy overlaps step i"}
 
 
 def main():

@@ -245,10 +245,12 @@ int ssd_verify_attn(const ssd_attn_args* a, void* ws, size_t ws_bytes, void* str
  *   early_rows: 0 — the row pass waits for the kernel before it on the stream
  *     (the retrieval that wrote blk_len) and reads only the rows a present
  *     token needs; 1 — it starts at once and reads every target row (and
- *     every draft row when chain_blk >= 0), so that it overlaps a retrieval
- *     launched just before it; blk_tok and blk_len are read only after that
- *     kernel has completed. Results are identical; early_rows = 1 reads rows
- *     of absent tokens too (their contents are never used).
+ *     every draft row when chain_blk >= 0), so that it overlaps the kernel
+ *     launched just before it (the retrieval, or an attention launched after
+ *     the retrieval); blk_tok and blk_len are read only after that kernel has
+ *     completed, and the call's last kernel starts only then. Results are
+ *     identical; early_rows = 1 reads rows of absent tokens too (their
+ *     contents are never used).
  * 2 <= V < 2^31; NB*Dmax < 4096;
  * Dmax <= 256; 0 <= chain_blk < NB or chain_blk == -1.
  * Workspace: ssd_accept_workspace_size(a) bytes, 256-byte aligned; its

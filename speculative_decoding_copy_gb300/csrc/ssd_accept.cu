@@ -15,8 +15,11 @@
 //                   some token needs (16-byte loads, all in flight together) and
 //                   reduces each to max, argmax (greedy only; lowest index on
 //                   ties) and sum of 2^((l - max) log2 e) with warp shuffles; in
-//                   the early mode it streams every row before the retrieval has
-//                   finished and waits for it only at its end;
+//                   the early mode it streams every row without waiting for the
+//                   kernel before it, and only its last CTA waits for that kernel
+//                   before exiting (the others leave as soon as their pieces are
+//                   done, so their SMs take further CTAs while, say, an attention
+//                   launched just before still runs);
 //   k_accept_finish one cluster of 8 CTAs per sequence: merges the pieces of
 //                   every needed row (one warp per row), runs the acceptance test
 //                   of every candidate token and picks the longest accepted block
@@ -238,8 +241,10 @@ __global__ void __launch_bounds__(kStatsThreads, 2)
 k_vocab_stats(AcceptParams p) {
   // blk_len comes from the retrieval; once it is in, the next kernel of the stream may
   // start (its prologue reads the retrieval's outputs, never this kernel's). The early
-  // mode reads no blk_len and waits at its end instead, so that this grid completes only
-  // after the retrieval has: the next kernel's wait then covers both.
+  // mode reads no blk_len; its last CTA waits for the preceding kernel at its end, so
+  // that this grid completes only after that kernel (and what it waited for) has: the
+  // next kernel's wait then covers them all. One waiting CTA is enough for that, and the
+  // others do not hold their SMs while they would only wait.
   if (!p.early) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -263,7 +268,7 @@ k_vocab_stats(AcceptParams p) {
     else st = reduce_piece<BF16, AMAX, true, false>(row, n, e0, p.probs);
     if (lane == 0) p.part[static_cast<int64_t>(br) * p.nch + c] = st;
   }
-  if (p.early) {
+  if (p.early && blockIdx.x == gridDim.x - 1) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   }

@@ -1,7 +1,8 @@
 """One speculate-and-verify step on the GPU: device buffers for a batch and the
 launch order of the C-ABI calls.
 
-    gate_retrieve -> accept (row pass, finish) -> verify_attn     (one stream)
+    gate_retrieve -> accept (row pass, finish) -> verify_attn     (one stream, "rows_first")
+    gate_retrieve -> verify_attn -> accept (early rows)            (one stream, "attn_first")
     gate_retrieve -> { verify_attn (aux stream) || accept }       (two streams)
 
 Verification attention and acceptance both depend only on the retrieval output.
@@ -11,7 +12,11 @@ main loop (which needs nothing from the acceptance) runs on the SMs the
 latency-bound finish kernel leaves free; it waits for its predecessors only before
 writing. early_rows=True lets the row pass stream every row while the retrieval
 still runs: a step without attention is faster that way, but with attention on
-the same stream the attention then starts no earlier and the step is slower.
+the same stream after the acceptance the attention then starts no earlier and the
+step is slower. In the "attn_first" order the attention's main loop starts while
+the retrieval still runs (it waits for blk_len only before its merge), and the row
+pass, in its early mode, streams every row on the SMs the attention leaves free;
+the finish kernel starts once both are done.
 The step issues only library calls; it computes nothing itself.
 """
 from __future__ import annotations
@@ -31,28 +36,65 @@ def to_device(a: np.ndarray, device) -> torch.Tensor:
 
 INPUT_KEYS = ["ctx", "ctx_len", "h", "w", "q", "k_cache", "v_cache", "k_cand", "v_cand", "prefix_len", "tgt", "drf",
               "chain_tok", "u_acc", "u_fin"]
+ATTN_KEYS = ("q", "k_cache", "v_cache", "k_cand", "v_cand")
+ARENA_ALIGN = 256
+
+
+def _step_inputs(inp: dict, with_attention: bool):
+    """(key, contiguous numpy array) for every input a step reads, in INPUT_KEYS order."""
+    out = []
+    for k in INPUT_KEYS:
+        v = inp.get(k)
+        if v is None or (not with_attention and k in ATTN_KEYS):
+            continue
+        a = np.ascontiguousarray(v)
+        out.append((k, a.view(np.int16) if a.dtype == np.uint16 else a))
+    return out
+
+
+def arena_bytes(inp: dict, with_attention=True) -> int:
+    """Bytes of one arena that holds every input of a step, each at a 256-byte boundary."""
+    n = 0
+    for _, a in _step_inputs(inp, with_attention):
+        n = -(-n // ARENA_ALIGN) * ARENA_ALIGN + a.nbytes
+    return max(n, ARENA_ALIGN)
 
 
 class VerifyStep:
     """Holds the inputs, outputs and workspaces of one batch of workload `wl`."""
 
     def __init__(self, wl, inp: dict, device="cuda", mode=None, kind=None, with_attention=True,
-                 with_probs=False, early_rows=False):
+                 with_probs=False, early_rows=False, order="rows_first", arena: torch.Tensor | None = None):
+        """`arena`: optional uint8 device tensor of at least arena_bytes(inp, with_attention)
+        bytes; the inputs are then placed in it (256-byte aligned views), so that a caller
+        can refresh all of them with one host-to-device copy of a same-layout host buffer."""
+        if order not in ("rows_first", "attn_first"):
+            raise ValueError(f"unknown step order {order!r}")
         self.wl = wl
         self.early_rows = early_rows
+        self.order = order
         self.mode = ssd.SSD_SAMPLE if (mode or wl.mode) == "sample" else ssd.SSD_GREEDY
         if kind is None:
             kind = ssd.SSD_LOGITS_BF16 if wl.logit_dtype == "bf16" else ssd.SSD_LOGITS_F32
         self.kind = kind
         self.device = torch.device(device)
         self.x = {}
-        for k in INPUT_KEYS:
-            v = inp.get(k)
-            if v is None:
-                continue
-            if not with_attention and k in ("q", "k_cache", "v_cache", "k_cand", "v_cand"):
-                continue
-            self.x[k] = to_device(np.asarray(v), self.device)
+        self.arena = arena
+        if arena is not None:
+            same_dev = arena.device.type == self.device.type and (self.device.index is None or
+                                                                  arena.device.index == self.device.index)
+            if arena.dtype != torch.uint8 or not same_dev or arena.numel() < arena_bytes(inp, with_attention):
+                raise ValueError("arena must be a uint8 tensor on the step's device of at least arena_bytes() bytes")
+            off = 0
+            for k, a in _step_inputs(inp, with_attention):
+                off = -(-off // ARENA_ALIGN) * ARENA_ALIGN
+                t = arena[off:off + a.nbytes].view(torch.from_numpy(a[:0].reshape(-1)).dtype).view(a.shape)
+                t.copy_(torch.from_numpy(a))
+                self.x[k] = t
+                off += a.nbytes
+        else:
+            for k, a in _step_inputs(inp, with_attention):
+                self.x[k] = to_device(a, self.device)
         B = wl.B
         self.with_attention = with_attention and "q" in self.x
         i32 = lambda *s: torch.empty(s, dtype=torch.int32, device=self.device)
@@ -103,12 +145,13 @@ class VerifyStep:
                                    self.ret_out["blk_len"], self.wl.Dmax, out=self.attn_out, ws=self.attn_ws,
                                    stream=stream)
 
-    def accept(self, stream=None):
+    def accept(self, stream=None, early_rows=None):
         wl, x = self.wl, self.x
+        early = self.early_rows if early_rows is None else early_rows
         return ssd.ssd_accept(x["tgt"], x.get("drf") if wl.chain_policy else None, self.ret_out["blk_tok"],
                               self.ret_out["blk_len"], x["u_acc"], x["u_fin"], mode=self.mode, kind=self.kind,
                               K=wl.K, chain_blk=self.chain_blk, out=self.acc_out, ws=self.acc_ws,
-                              probs_out=self.probs, stream=stream, early_rows=self.early_rows)
+                              probs_out=self.probs, stream=stream, early_rows=early)
 
     def run(self, stream=None, aux: torch.cuda.Stream | None = None):
         """Issue the whole step on `stream` (default: current), attention on `aux` if given."""
@@ -124,6 +167,12 @@ class VerifyStep:
             ev2 = torch.cuda.Event()
             ev2.record(aux)
             main.wait_event(ev2)
+        elif self.order == "attn_first" and self.with_attention:
+            # one stream: the attention right behind the retrieval, then the row pass in its
+            # early mode beside the attention, then the finish kernel
+            self.attention(main)
+            if self.with_accept:
+                self.accept(main, early_rows=True)
         else:
             # one stream: the acceptance chain first (it needs only the retrieval's output),
             # then the attention, whose main loop overlaps the latency-bound finish kernel
