@@ -1,8 +1,8 @@
 #!/usr/bin/env python
 """Benchmark of the speculate-and-verify step on GB300.
 
-One step = gate -> retrieval -> verification attention || acceptance for one
-batch of the chosen workload (default: the Llama-3.1-8B-shaped verify, batch 1,
+One step = retrieval (gate + kappa-gram + continuations) || row pass, then the
+finish kernel || verification attention, for one batch of the chosen workload (default: the Llama-3.1-8B-shaped verify, batch 1,
 prefix 4096, W=4 D=20, V=128256). Prints ONE JSON line on rank 0.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -52,6 +52,9 @@ def parse_args(argv=None):
     ap.add_argument("--order", choices=["rows_first", "attn_first"], default="rows_first",
                     help="one-stream kernel order: rows_first = retrieval, row pass, finish, attention; "
                          "attn_first = retrieval, attention, row pass (early mode) beside it, finish")
+    ap.add_argument("--early-rows", action=argparse.BooleanOptionalAction, default=True,
+                    help="row pass in its early mode: it streams every row while the retrieval runs and "
+                         "lets the finish kernel launch once the retrieval is done (default: on)")
     ap.add_argument("--section", choices=["head"], default=None,
                     help="run one extra measurement alone and print its JSON (head: the low-rank draft head)")
     ap.add_argument("--oracle-worker", action="store_true", help=argparse.SUPPRESS)
@@ -291,7 +294,7 @@ def run_ours(args):
     ssd.lib()
 
     # rotating copies: total bytes above twice the L2
-    probe = VerifyStep(wl, inp, device=dev, order=args.order)
+    probe = VerifyStep(wl, inp, device=dev, order=args.order, early_rows=args.early_rows)
     main = torch.cuda.Stream(dev)
     aux = torch.cuda.Stream(dev) if args.two_streams else None
     with torch.cuda.stream(main):
@@ -301,7 +304,8 @@ def run_ours(args):
     prefix = inp["prefix_len"]
     ab = WL.algorithmic_bytes(wl, prefix, blk_len)
     R = max(3, min(16, math.ceil(2 * L2_BYTES / max(ab["total"], 1)) + 1))
-    steps = [probe] + [VerifyStep(wl, inp, device=dev, order=args.order) for _ in range(R - 1)]
+    steps = [probe] + [VerifyStep(wl, inp, device=dev, order=args.order, early_rows=args.early_rows)
+                       for _ in range(R - 1)]
     tokens = ab["tokens"]
 
     def capture(idx, hooked):
@@ -454,7 +458,8 @@ def run_ours(args):
                 "config": workload_config(wl, tokens, {
                     "l2": f"{R} rotating input copies ({R * step_bytes / 2**20:.0f} MiB > 2x L2); no flush",
                     "parallelism": f"replicas x{world} (independent batches per GPU)",
-                    "step_order": "two streams" if args.two_streams else args.order}),
+                    "step_order": "two streams" if args.two_streams else args.order,
+                    "early_rows": bool(args.early_rows)}),
                 "candidate_tokens_per_s": value * tokens,
                 "hbm_roofline_step": step_roof,
                 "roofline": roofline,
@@ -778,7 +783,7 @@ def run_e2e(args, wl, inp, st, main, aux, dev):
     from speculative_decoding_copy_gb300.step import VerifyStep, arena_bytes
 
     nbytes = arena_bytes(inp, True)
-    slots = [VerifyStep(wl, inp, device=dev, order=st.order,
+    slots = [VerifyStep(wl, inp, device=dev, order=st.order, early_rows=st.early_rows,
                         arena=torch.empty(nbytes, dtype=torch.uint8, device=dev)) for _ in range(2)]
     bufs = {"arena": slots[0].arena}
     for j, s in enumerate(slots):

@@ -16,10 +16,8 @@
 //                   reduces each to max, argmax (greedy only; lowest index on
 //                   ties) and sum of 2^((l - max) log2 e) with warp shuffles; in
 //                   the early mode it streams every row without waiting for the
-//                   kernel before it, and only its last CTA waits for that kernel
-//                   before exiting (the others leave as soon as their pieces are
-//                   done, so their SMs take further CTAs while, say, an attention
-//                   launched just before still runs);
+//                   kernel before it: only its last CTA waits for that kernel
+//                   (then lets the next kernel launch), the others never wait;
 //   k_accept_finish one cluster of 8 CTAs per sequence: merges the pieces of
 //                   every needed row (one warp per row), runs the acceptance test
 //                   of every candidate token and picks the longest accepted block
@@ -241,14 +239,12 @@ __global__ void __launch_bounds__(kStatsThreads, 2)
 k_vocab_stats(AcceptParams p) {
   // blk_len comes from the retrieval; once it is in, the next kernel of the stream may
   // start (its prologue reads the retrieval's outputs, never this kernel's). The early
-  // mode reads no blk_len; its last CTA waits for the preceding kernel at its end, so
-  // that this grid completes only after that kernel (and what it waited for) has: the
-  // next kernel's wait then covers them all. One waiting CTA is enough for that, and the
-  // others do not hold their SMs while they would only wait.
-  if (!p.early) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  }
+  // mode reads no blk_len: every CTA but the last lets the next kernel start at once and
+  // never waits; the last CTA first waits for the preceding kernel. So the next kernel
+  // starts only once that kernel (and what it waited for) has completed, and this grid
+  // completes only after it: the next kernel's wait then covers them all.
+  if (!p.early || blockIdx.x == gridDim.x - 1) asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int es = BF16 ? 2 : 4;
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * kStatsWarps + (threadIdx.x >> 5);
@@ -267,10 +263,6 @@ k_vocab_stats(AcceptParams p) {
     else if (n == per) st = reduce_piece<BF16, AMAX, true, true>(row, n, e0, p.probs);
     else st = reduce_piece<BF16, AMAX, true, false>(row, n, e0, p.probs);
     if (lane == 0) p.part[static_cast<int64_t>(br) * p.nch + c] = st;
-  }
-  if (p.early && blockIdx.x == gridDim.x - 1) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   }
 }
 

@@ -11,9 +11,10 @@ pass streams the needed logit rows right after the retrieval, and the attention'
 main loop (which needs nothing from the acceptance) runs on the SMs the
 latency-bound finish kernel leaves free; it waits for its predecessors only before
 writing. early_rows=True lets the row pass stream every row while the retrieval
-still runs: a step without attention is faster that way, but with attention on
-the same stream after the acceptance the attention then starts no earlier and the
-step is slower. In the "attn_first" order the attention's main loop starts while
+still runs; all its CTAs but the last let the finish kernel launch at once, and the
+last waits for the retrieval first, so the finish (and the attention after it) are
+launched as soon as the retrieval is done. On the Llama-3.1-8B-shaped step every row
+is needed anyway and this is the faster mode. In the "attn_first" order the attention's main loop starts while
 the retrieval still runs (it waits for blk_len only before its merge), and the row
 pass, in its early mode, streams every row on the SMs the attention leaves free;
 the finish kernel starts once both are done.
