@@ -207,7 +207,8 @@ def test_accept_logits_probs_and_decisions(kind, V):
 
 @pytest.mark.parametrize("name,order", [(n, "two_streams") for n in WL.WORKLOAD_ORDER] +
                          [("tiny", "rows_first"), ("llama8b", "rows_first"), ("batched", "rows_first"),
-                          ("tiny", "attn_first"), ("llama8b", "attn_first")])
+                          ("tiny", "attn_first"), ("llama8b", "attn_first"),
+                          ("tiny", "bench"), ("llama8b", "bench")])
 def test_whole_step_workloads(name, order):
     """gate -> retrieve -> accept and attention through the step's own launch path (one
     stream in either order, or attention on a second stream), compared with the oracle
@@ -216,7 +217,9 @@ def test_whole_step_workloads(name, order):
     wl = WL.WORKLOADS[name]
     inp = WL.make_inputs(wl, 77 + len(name), full_width=False)
     two = order == "two_streams"
-    st = VerifyStep(wl, inp, with_attention=(name in ("tiny", "llama8b")), order="rows_first" if two else order)
+    # "bench": the launch configuration the benchmark times (one stream, early row pass)
+    st = VerifyStep(wl, inp, with_attention=(name in ("tiny", "llama8b")),
+                    order=order if order.endswith("_first") else "rows_first", early_rows=order == "bench")
     for _ in range(1 if two else 2):
         st.run(aux=torch.cuda.Stream() if two else None)
     got = st.results()
