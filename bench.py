@@ -46,6 +46,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="llama8b")
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-next", action="store_true",
+                    help="skip the measurements of the rows after the step (commit, paged cache, tax, head)")
     ap.add_argument("--two-streams", action="store_true",
                     help="run attention on a second stream beside the acceptance chain (default: one stream, "
                          "acceptance first, attention overlapping the finish kernel)")
@@ -405,7 +407,8 @@ def run_ours(args):
 
     # end to end through the public API with host buffers
     e2e = run_e2e(args, wl, inp, steps[0], main, aux, dev)
-    nxt = {"commit_kv": measure_commit(wl, main, dev), "paged_attn": measure_paged(wl, steps[0], main, dev),
+    nxt = None if args.no_next else {
+           "commit_kv": measure_commit(wl, main, dev), "paged_attn": measure_paged(wl, steps[0], main, dev),
            "spec_tax": measure_tax(main, dev), "slimspec_head": measure_head(main, dev)}
 
     hbm, peak_kind = measured_peaks()

@@ -187,6 +187,14 @@ int ssd_gate_retrieve(const int32_t* ctx, int64_t ctx_stride, const int32_t* ctx
  * prefix_len[b] <= 128 * pages_per_seq; pages may be shared by sequences). A page
  * index outside [0, num_pages) records SSD_ERR_DEVICE and reads page 0. P_max is
  * then unused.
+ * skip_absent (0 or 1; tensor-core path only, ignored by the fp32 / head-dim-64
+ * pass): 1 makes every CTA first wait for the kernel before it on the stream
+ * (the one whose outputs include blk_len, or a later one) and then skip a tile
+ * of 128 packed rows in which no token is present, e.g. the copy-block rows of
+ * a sequence whose gate is off. Outputs are identical; the attention then no
+ * longer overlaps the tail of that preceding kernel, so it pays off only when
+ * many candidate slots are empty. 0: every tile is computed, blk_len is read
+ * only before the merge.
  * Workspace: ssd_verify_attn_workspace_size(a) bytes, 256-byte aligned; its
  * contents need no initialisation. Device-side errors are recorded in it.
  */
@@ -207,6 +215,7 @@ typedef struct {
   const int32_t* block_table;
   int pages_per_seq;
   int64_t num_pages;
+  int skip_absent;
 } ssd_attn_args;
 
 size_t ssd_verify_attn_workspace_size(const ssd_attn_args* a);

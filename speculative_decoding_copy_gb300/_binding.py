@@ -43,7 +43,8 @@ class AttnArgs(ctypes.Structure):
                 ("v_cand", c_void_p), ("out", c_void_p), ("prefix_len", c_void_p), ("blk_len", c_void_p),
                 ("dtype", c_int), ("B", c_int), ("NB", c_int), ("Dmax", c_int), ("Hq", c_int), ("Hkv", c_int),
                 ("dh", c_int), ("P_max", c_int64), ("scale", c_float), ("out_dtype", c_int),
-                ("block_table", c_void_p), ("pages_per_seq", c_int), ("num_pages", c_int64)]
+                ("block_table", c_void_p), ("pages_per_seq", c_int), ("num_pages", c_int64),
+                ("skip_absent", c_int)]
 
 
 class CommitArgs(ctypes.Structure):
@@ -233,7 +234,7 @@ def ssd_gate_retrieve(ctx, ctx_len, h, w, tau, kappa, W, D, K, chain_policy, cha
 
 
 def attn_args(q, k_cache, v_cache, k_cand, v_cand, prefix_len, blk_len, Dmax, out, scale=0.0,
-              block_table=None) -> AttnArgs:
+              block_table=None, skip_absent=False) -> AttnArgs:
     """k_cache/v_cache: [B][Hkv][P_max][dh], or with block_table [B][pages_per_seq] pages of 128
     tokens [num_pages][Hkv][128][dh]."""
     B, NT, Hq, dh = q.shape
@@ -242,11 +243,12 @@ def attn_args(q, k_cache, v_cache, k_cand, v_cand, prefix_len, blk_len, Dmax, ou
     if block_table is None:
         return AttnArgs(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_cand), _ptr(v_cand), _ptr(out),
                         _ptr(prefix_len), _ptr(blk_len), _elem_type(q), B, NB, int(Dmax), Hq, Hkv, dh,
-                        k_cache.shape[2], float(scale), _elem_type(out), None, 0, 0)
+                        k_cache.shape[2], float(scale), _elem_type(out), None, 0, 0, int(bool(skip_absent)))
     pps = block_table.shape[1]
     return AttnArgs(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_cand), _ptr(v_cand), _ptr(out),
                     _ptr(prefix_len), _ptr(blk_len), _elem_type(q), B, NB, int(Dmax), Hq, Hkv, dh,
-                    128 * pps, float(scale), _elem_type(out), _ptr(block_table), pps, k_cache.shape[0])
+                    128 * pps, float(scale), _elem_type(out), _ptr(block_table), pps, k_cache.shape[0],
+                    int(bool(skip_absent)))
 
 
 def ssd_verify_attn_workspace_size(args: AttnArgs) -> int:
@@ -254,7 +256,7 @@ def ssd_verify_attn_workspace_size(args: AttnArgs) -> int:
 
 
 def ssd_verify_attn(q, k_cache, v_cache, k_cand, v_cand, prefix_len, blk_len, Dmax, *, out=None, ws=None,
-                    scale=0.0, stream=None, out_f32=False, block_table=None):
+                    scale=0.0, stream=None, out_f32=False, block_table=None, skip_absent=False):
     """Block-triangular verification attention; returns the output tensor [B][NT][Hq][dh]
     (the inputs' dtype, or fp32 with out_f32). With block_table [B][pages_per_seq] int32 the
     caches are pages of 128 tokens [num_pages][Hkv][128][dh]."""
@@ -269,7 +271,8 @@ def ssd_verify_attn(q, k_cache, v_cache, k_cand, v_cand, prefix_len, blk_len, Dm
         out = torch.empty(q.shape, dtype=torch.float32, device=q.device) if out_f32 else torch.empty_like(q)
     if block_table is not None:
         _need(block_table, "block_table", (torch.int32,), 2)
-    args = attn_args(q, k_cache, v_cache, k_cand, v_cand, prefix_len, blk_len, Dmax, out, scale, block_table)
+    args = attn_args(q, k_cache, v_cache, k_cand, v_cand, prefix_len, blk_len, Dmax, out, scale, block_table,
+                     skip_absent)
     need = ssd_verify_attn_workspace_size(args)
     if ws is None:
         ws = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)

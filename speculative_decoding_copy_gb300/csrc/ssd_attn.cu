@@ -300,6 +300,7 @@ static int validate(const ssd_attn_args* a) {
   if (a->dtype != SSD_F32 && a->dtype != SSD_BF16) return SSD_ERR_INVALID;
   if (a->out_dtype != a->dtype && a->out_dtype != SSD_F32) return SSD_ERR_INVALID;
   if (a->Hq % a->Hkv != 0) return SSD_ERR_INVALID;
+  if (a->skip_absent != 0 && a->skip_absent != 1) return SSD_ERR_INVALID;
   if (a->Dmax > 256 || a->NB * a->Dmax > 8192 || a->Hq / a->Hkv > 64) return SSD_ERR_UNSUPPORTED;
   if (static_cast<long long>(a->B) * a->Hkv > 0x7fffffffLL) return SSD_ERR_UNSUPPORTED;
   if (a->dh != 64 && a->dh != 128) return SSD_ERR_UNSUPPORTED;

@@ -23,6 +23,7 @@ struct AttnParams {
   const int32_t* block_table;   // tensor-core path: paged cache [B][pages_per_seq], or null
   int pages_per_seq;
   int64_t num_pages;
+  int skip_absent;       // tensor-core path: wait for the predecessor first, skip tiles without a present token
   WsHeader* hdr;
   float* ws_ml;          // [rows][S][2]  running max and sum per split
   float* ws_o;           // [rows][S][dh] un-normalised output per split

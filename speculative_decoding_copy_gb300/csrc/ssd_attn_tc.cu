@@ -198,6 +198,17 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
   const int rb = split * rpc, nr = max(0, min(rv, rb + rpc) - rb);
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (p.skip_absent) {
+    // a tile none of whose rows belongs to a present token is skipped; the S CTAs of a
+    // cluster hold the same rows, so they all leave here together, before any barrier
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    int any = 0;
+    for (int i = tid; i < rv; i += kThreads) {
+      const int tt = (r0 + i) / G;
+      any |= (tt % p.Dmax) < __ldcg(p.blk_len + b * p.NB + tt / p.Dmax) ? 1 : 0;
+    }
+    if (!__syncthreads_or(any)) return;
+  }
   if (warp == 4 && lane == 0) {
     // the descriptors are fetched on first use: start those fetches before the first copy
     prefetch_tmap(&tmap_q);
@@ -721,6 +732,7 @@ int attn_tc_launch(const ssd_attn_args* a, void* ws, cudaStream_t s) {
   p.block_table = a->block_table;
   p.pages_per_seq = a->pages_per_seq;
   p.num_pages = a->num_pages;
+  p.skip_absent = a->skip_absent;
   p.hdr = reinterpret_cast<WsHeader*>(ws);
 
   cudaLaunchConfig_t cfg = {};

@@ -65,15 +65,20 @@ class VerifyStep:
     """Holds the inputs, outputs and workspaces of one batch of workload `wl`."""
 
     def __init__(self, wl, inp: dict, device="cuda", mode=None, kind=None, with_attention=True,
-                 with_probs=False, early_rows=False, order="rows_first", arena: torch.Tensor | None = None):
+                 with_probs=False, early_rows=False, order="rows_first", arena: torch.Tensor | None = None,
+                 skip_absent=None):
         """`arena`: optional uint8 device tensor of at least arena_bytes(inp, with_attention)
         bytes; the inputs are then placed in it (256-byte aligned views), so that a caller
-        can refresh all of them with one host-to-device copy of a same-layout host buffer."""
+        can refresh all of them with one host-to-device copy of a same-layout host buffer.
+        `skip_absent`: the attention skips 128-row tiles without a present token (after
+        waiting for its predecessor); None turns it on for batches whose gate can send
+        sequences to the chain draft, where the copy-block rows of those sequences are empty."""
         if order not in ("rows_first", "attn_first"):
             raise ValueError(f"unknown step order {order!r}")
         self.wl = wl
         self.early_rows = early_rows
         self.order = order
+        self.skip_absent = (wl.chain_policy == 1 and wl.B > 1) if skip_absent is None else bool(skip_absent)
         self.mode = ssd.SSD_SAMPLE if (mode or wl.mode) == "sample" else ssd.SSD_GREEDY
         if kind is None:
             kind = ssd.SSD_LOGITS_BF16 if wl.logit_dtype == "bf16" else ssd.SSD_LOGITS_F32
@@ -117,7 +122,7 @@ class VerifyStep:
             self.attn_out = torch.empty_like(self.x["q"])
             a = ssd.attn_args(self.x["q"], self.x["k_cache"], self.x["v_cache"], self.x["k_cand"],
                               self.x["v_cand"], self.x["prefix_len"], self.ret_out["blk_len"], wl.Dmax,
-                              self.attn_out)
+                              self.attn_out, skip_absent=self.skip_absent)
             self.attn_ws = torch.empty(max(256, ssd.ssd_verify_attn_workspace_size(a)), dtype=torch.uint8,
                                        device=self.device)
 
@@ -144,7 +149,7 @@ class VerifyStep:
         x = self.x
         return ssd.ssd_verify_attn(x["q"], x["k_cache"], x["v_cache"], x["k_cand"], x["v_cand"], x["prefix_len"],
                                    self.ret_out["blk_len"], self.wl.Dmax, out=self.attn_out, ws=self.attn_ws,
-                                   stream=stream)
+                                   stream=stream, skip_absent=self.skip_absent)
 
     def accept(self, stream=None, early_rows=None):
         wl, x = self.wl, self.x

@@ -185,3 +185,36 @@ def test_attention_paged_bad_page_is_reported():
     S.ssd_verify_attn(t["q"], to_device(kp, dev), to_device(vp, dev), t["k_cand"], t["v_cand"], t["prefix_len"],
                       to_device(np.array([[4]], np.int32), dev), 4, ws=ws, block_table=to_device(table, dev))
     assert S.ssd_read_device_error(ws) == S.SSD_ERR_DEVICE
+
+
+@pytest.mark.parametrize("G", [4, 8])
+def test_attention_skip_absent_tiles(G):
+    """skip_absent: 128-row tiles in which no token is present are skipped. Present rows
+    equal the full computation bit for bit and the oracle within the bound; absent rows
+    are written by neither."""
+    rng = np.random.default_rng(50 + G)
+    Hkv, B, NB, Dmax = 2, 4, 3, 20
+    prefix = [300, 0, 4100, 129]
+    case = _case(rng, B, NB, Dmax, Hkv * G, Hkv, 128, prefix, "bf16", q_scale=2.0)
+    # tile 0 empty / tile 1 empty / everything empty / everything present
+    blk_len = np.array([[0, 0, 5], [3, 0, 0], [0, 0, 0], [20, 20, 20]], np.int32)
+    dev = "cuda"
+    t = {k: to_device(np.asarray(v), dev) for k, v in case.items()}
+    bl = to_device(blk_len, dev)
+    outs = []
+    for skip in (False, True):
+        out = torch.full(t["q"].shape, 7.0, dtype=torch.float32, device=dev)
+        S.ssd_verify_attn(t["q"], t["k_cache"], t["v_cache"], t["k_cand"], t["v_cand"], t["prefix_len"], bl, Dmax,
+                          out=out, skip_absent=skip)
+        torch.cuda.synchronize()
+        outs.append(out.cpu().numpy())
+    present = np.zeros((B, NB * Dmax), bool)
+    for b in range(B):
+        for k in range(NB):
+            present[b, k * Dmax:k * Dmax + blk_len[b, k]] = True
+    np.testing.assert_array_equal(outs[1][present], outs[0][present])
+    assert np.all(outs[1][~present] == 7.0) and np.all(outs[0][~present] == 7.0)
+    ref = O.verify_attention(case["q"], case["k_cache"], case["v_cache"], case["k_cand"], case["v_cand"],
+                             case["prefix_len"], blk_len, Dmax, "bf16", None)
+    err = max(float(np.max(np.abs(outs[1][b, t_] - o))) for (b, t_), o in ref.items())
+    assert err <= TOL, err
