@@ -54,9 +54,11 @@ def parse_args(argv=None):
     ap.add_argument("--order", choices=["rows_first", "attn_first"], default="rows_first",
                     help="one-stream kernel order: rows_first = retrieval, row pass, finish, attention; "
                          "attn_first = retrieval, attention, row pass (early mode) beside it, finish")
-    ap.add_argument("--early-rows", action=argparse.BooleanOptionalAction, default=True,
-                    help="row pass in its early mode: it streams every row while the retrieval runs and "
-                         "lets the finish kernel launch once the retrieval is done (default: on)")
+    ap.add_argument("--early-rows", choices=["auto", "on", "off"], default="auto",
+                    help="row pass in its early mode (it streams every row while the retrieval runs and "
+                         "lets the finish kernel launch once the retrieval is done); auto: on unless the "
+                         "gate can send sequences to the chain draft, whose unused copy-block rows the "
+                         "early mode would read too")
     ap.add_argument("--section", choices=["head"], default=None,
                     help="run one extra measurement alone and print its JSON (head: the low-rank draft head)")
     ap.add_argument("--oracle-worker", action="store_true", help=argparse.SUPPRESS)
@@ -294,9 +296,10 @@ def run_ours(args):
     wl = WL.WORKLOADS[args.workload]
     inp = WL.make_inputs(wl, rank_seed(rank))
     ssd.lib()
+    early = args.early_rows == "on" or (args.early_rows == "auto" and wl.chain_policy != 1)
 
     # rotating copies: total bytes above twice the L2
-    probe = VerifyStep(wl, inp, device=dev, order=args.order, early_rows=args.early_rows)
+    probe = VerifyStep(wl, inp, device=dev, order=args.order, early_rows=early)
     main = torch.cuda.Stream(dev)
     aux = torch.cuda.Stream(dev) if args.two_streams else None
     with torch.cuda.stream(main):
@@ -306,7 +309,7 @@ def run_ours(args):
     prefix = inp["prefix_len"]
     ab = WL.algorithmic_bytes(wl, prefix, blk_len)
     R = max(3, min(16, math.ceil(2 * L2_BYTES / max(ab["total"], 1)) + 1))
-    steps = [probe] + [VerifyStep(wl, inp, device=dev, order=args.order, early_rows=args.early_rows)
+    steps = [probe] + [VerifyStep(wl, inp, device=dev, order=args.order, early_rows=early)
                        for _ in range(R - 1)]
     tokens = ab["tokens"]
 
@@ -462,7 +465,7 @@ def run_ours(args):
                     "l2": f"{R} rotating input copies ({R * step_bytes / 2**20:.0f} MiB > 2x L2); no flush",
                     "parallelism": f"replicas x{world} (independent batches per GPU)",
                     "step_order": "two streams" if args.two_streams else args.order,
-                    "early_rows": bool(args.early_rows)}),
+                    "early_rows": early}),
                 "candidate_tokens_per_s": value * tokens,
                 "hbm_roofline_step": step_roof,
                 "roofline": roofline,
