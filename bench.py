@@ -283,7 +283,7 @@ def run_ours(args):
 
     from speculative_decoding_copy_gb300 import _binding as ssd
     from speculative_decoding_copy_gb300 import workloads as WL
-    from speculative_decoding_copy_gb300.step import VerifyStep
+    from speculative_decoding_copy_gb300.step import VerifyStep, default_early_rows
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -296,7 +296,7 @@ def run_ours(args):
     wl = WL.WORKLOADS[args.workload]
     inp = WL.make_inputs(wl, rank_seed(rank))
     ssd.lib()
-    early = args.early_rows == "on" or (args.early_rows == "auto" and wl.chain_policy != 1)
+    early = args.early_rows == "on" or (args.early_rows == "auto" and default_early_rows(wl))
 
     # rotating copies: total bytes above twice the L2
     probe = VerifyStep(wl, inp, device=dev, order=args.order, early_rows=early)

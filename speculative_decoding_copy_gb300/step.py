@@ -61,6 +61,13 @@ def arena_bytes(inp: dict, with_attention=True) -> int:
     return max(n, ARENA_ALIGN)
 
 
+def default_early_rows(wl) -> bool:
+    """The row-pass mode measured faster for a workload: early (every row streamed while the
+    retrieval runs) unless the gate can send sequences to the chain draft, whose unused
+    copy-block rows the early mode would read as well."""
+    return wl.chain_policy != 1
+
+
 class VerifyStep:
     """Holds the inputs, outputs and workspaces of one batch of workload `wl`."""
 

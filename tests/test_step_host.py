@@ -5,7 +5,7 @@ import pytest
 import torch
 
 from speculative_decoding_copy_gb300 import workloads as WL
-from speculative_decoding_copy_gb300.step import ARENA_ALIGN, VerifyStep, arena_bytes
+from speculative_decoding_copy_gb300.step import ARENA_ALIGN, VerifyStep, arena_bytes, default_early_rows
 
 
 @pytest.mark.parametrize("with_attention", [True, False])
@@ -44,3 +44,14 @@ def test_arena_too_small_is_rejected():
         VerifyStep(wl, inp, device="cpu", arena=torch.zeros(arena_bytes(inp) - 1, dtype=torch.uint8))
     with pytest.raises(ValueError):
         VerifyStep(wl, inp, device="cpu", order="sideways")
+
+
+def test_step_defaults_per_workload():
+    """Early row pass where every row is needed anyway; tile skipping in the attention only
+    for batches whose gate can send sequences to the chain draft."""
+    W = WL.WORKLOADS
+    assert default_early_rows(W["llama8b"]) and default_early_rows(W["llama70b"])
+    assert not default_early_rows(W["batched"]) and not default_early_rows(W["qwen8b_mixed"])
+    inp = WL.make_inputs(W["tiny"], 5, full_width=False)
+    assert VerifyStep(W["tiny"], inp, device="cpu").skip_absent is False          # a single sequence
+    assert VerifyStep(W["tiny"], inp, device="cpu", skip_absent=True).skip_absent is True
