@@ -413,7 +413,7 @@ def run_ours(args):
     dom_us = mean_us(ev_h, dom)
 
     # end to end through the public API with host buffers
-    e2e = run_e2e(args, wl, inp, steps[0], main, aux, dev)
+    e2e = run_e2e(args, wl, inp, steps[0], main, aux, dev, world)
     nxt = None if args.no_next else {
            "commit_kv": measure_commit(wl, main, dev), "paged_attn": measure_paged(wl, steps[0], main, dev),
            "spec_tax": measure_tax(main, dev), "slimspec_head": measure_head(main, dev)}
@@ -783,7 +783,7 @@ def pinned_like(tensors, dev):
     return out, node
 
 
-def run_e2e(args, wl, inp, st, main, aux, dev):
+def run_e2e(args, wl, inp, st, main, aux, dev, world=1):
     """Same step through the public API with host inputs. Every step copies all of its
     inputs host->device from one pinned buffer (one copy into the step's input arena)
     and reads the emitted tokens back. Two input arenas alternate: the copy of step i+1
@@ -832,10 +832,16 @@ def run_e2e(args, wl, inp, st, main, aux, dev):
     torch.cuda.synchronize()
     s0 = torch.cuda.Event(enable_timing=True)
     s1 = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
     run(E, s0, s1)
     torch.cuda.synchronize()
     ms = s0.elapsed_time(s1)
-    return {"value": E / (ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+    if world > 1:
+        ms = max_over_ranks(ms, dev)
+    # whole job, like `value`: every rank's steps over the slowest rank's time
+    return {"value": whole_job_value(world, E, ms), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": E, "host_buffers_numa_node": node,
             "copies": "one host-to-device copy of a pinned input arena per step; two arenas alternate so "
                       "that step i+1's copy overlaps step i"}
