@@ -10,15 +10,21 @@ On one stream the kernels are chained by programmatic dependent launch: the row
 pass streams the needed logit rows right after the retrieval, and the attention's
 main loop (which needs nothing from the acceptance) runs on the SMs the
 latency-bound finish kernel leaves free; it waits for its predecessors only before
-writing. early_rows=True lets the row pass stream every row while the retrieval
-still runs; all its CTAs but the last let the finish kernel launch at once, and the
-last waits for the retrieval first, so the finish (and the attention after it) are
-launched as soon as the retrieval is done. On the Llama-3.1-8B-shaped step every row
-is needed anyway and this is the faster mode. In the "attn_first" order the attention's main loop starts while
-the retrieval still runs (it waits for blk_len only before its merge), and the row
-pass, in its early mode, streams every row on the SMs the attention leaves free;
-the finish kernel starts once both are done.
-The step issues only library calls; it computes nothing itself.
+writing.
+
+early_rows=True lets the row pass stream every row while the retrieval still runs;
+all its CTAs but the last let the finish kernel launch at once, and the last waits
+for the retrieval first, so the finish (and the attention after it) are launched as
+soon as the retrieval is done. Where every row is needed anyway (default_early_rows)
+this is the faster mode. skip_absent makes the attention skip 128-row tiles without a
+present token, at the price of waiting for its predecessor first; it pays off in
+batches whose gate sends sequences to the chain draft. In the "attn_first" order the
+attention's main loop starts while the retrieval still runs and the row pass, in its
+early mode, streams beside it (measured slower; kept as an option).
+
+Inputs may sit in one device arena (arena_bytes), so that a caller refreshes all of
+them with a single host-to-device copy. The step issues only library calls; it
+computes nothing itself.
 """
 from __future__ import annotations
 
