@@ -242,3 +242,27 @@ def test_two_copy_blocks_follow_their_closed_form_and_are_not_lossless():
     first = np.bincount(r["out_tok"][:, 0], minlength=V)
     _, pval_p = scipy.stats.chisquare(first, p.astype(np.float64) / p.sum() * N)
     assert pval_p < 1e-6
+
+
+def test_copy_and_chain_blocks_in_one_step_ties_go_to_the_copy_block():
+    """Copy blocks and the chain block verified in one pass (chain block always present):
+    the longest run wins and, on a tie, the copy block (the chain block comes last)."""
+    V, W, Dmax, K = 8, 2, 3, 3
+    NB = W + 1
+    eye = np.eye(V, dtype=np.float32)
+    tgt = np.tile(eye[1], (1, 1 + NB * Dmax, 1))                    # the target always wants token 1
+    drf = np.tile(eye[1], (1, K, 1))
+    z = np.zeros((1, NB, Dmax), np.float32)
+
+    def run(copy0, copy1, chain):
+        bt = np.array([[copy0, copy1, chain]], np.int32)
+        bl = np.array([[3, 3, 3]], np.int32)
+        return O.verify_step_accept("greedy", "probs_f32", tgt, drf, bt, bl, W, 2, z, np.zeros(1, np.float32))
+
+    r = run([1, 2, 2], [3, 3, 3], [1, 5, 5])       # copy 0 and chain both accept one token
+    assert list(r["acc_len"][0]) == [1, 0, 1] and r["best_blk"][0] == 0
+    r = run([1, 2, 2], [3, 3, 3], [1, 1, 1])       # the chain block is longer: it wins
+    assert list(r["acc_len"][0]) == [1, 0, 3] and r["best_blk"][0] == 2
+    assert r["n_out"][0] == 4 and list(r["out_tok"][0]) == [1, 1, 1, 1]
+    r = run([1, 1, 1], [3, 3, 3], [1, 1, 1])       # a full copy block ties the full chain block
+    assert r["best_blk"][0] == 0 and list(r["out_tok"][0]) == [1, 1, 1, 1]
