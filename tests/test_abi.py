@@ -67,3 +67,48 @@ def test_host_validation_without_gpu(libpath):
     assert L.ssd_accept(ctypes.byref(c), null, 0, null) == b.SSD_ERR_INVALID
     c.chain_blk, c.B = -1, 0
     assert L.ssd_accept(ctypes.byref(c), null, 0, null) == b.SSD_OK
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "ssd.h"
+
+int main(void) {
+  ssd_attn_args a;
+  ssd_accept_args c;
+  memset(&a, 0, sizeof a);
+  memset(&c, 0, sizeof c);
+  if (ssd_version() < 100) return 1;
+  if (strcmp(ssd_status_string(SSD_OK), "ok") != 0) return 2;
+  /* argument errors come back from host-side validation, before any device work */
+  a.B = 1; a.NB = 1; a.Dmax = 4; a.Hq = 4; a.Hkv = 2; a.dh = 96; a.dtype = SSD_BF16;
+  if (ssd_verify_attn(&a, NULL, 0, NULL) != SSD_ERR_UNSUPPORTED) return 3;
+  c.mode = 7; c.V = 100; c.B = 1; c.NB = 1; c.Dmax = 4; c.chain_blk = -1;
+  if (ssd_accept(&c, NULL, 0, NULL) != SSD_ERR_INVALID) return 4;
+  c.mode = SSD_GREEDY; c.B = 0;
+  if (ssd_accept(&c, NULL, 0, NULL) != SSD_OK) return 5;
+  printf("c-abi ok\n");
+  return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_links(libpath, tmp_path):
+    """A C99 program includes ssd.h with every warning an error, links libssd.so and runs
+    host-side calls: the boundary needs no C++ and no torch."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "abi.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "abi"
+    libdir = os.path.dirname(libpath)
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                        str(src), "-o", str(exe), "-L", libdir, "-lssd", "-Wl,-rpath," + libdir],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and "c-abi ok" in r.stdout, (r.returncode, r.stdout, r.stderr)
