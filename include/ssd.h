@@ -22,10 +22,20 @@
  *                     SwitchSD page, "무엇과 다른가" (longest verified
  *                     continuation); 추측 디코딩은 왜… page, "2단계 · 일괄 검증"]
  *
+ * Around the step: ssd_gate_retrieve (gate and retrieval in one launch),
+ * ssd_commit_kv (append the accepted candidates' keys and values to the cache),
+ * ssd_copy_stats (copy attempts and speculation tax), ssd_lowrank_head (the
+ * SlimSpec low-rank draft LM head), ssd_accept_static (ssd_accept without a
+ * caller workspace), and the diagnostics ssd_read_device_error,
+ * ssd_status_string, ssd_version, ssd_launch_count, ssd_profile_kernel,
+ * ssd_selftest_wait.
+ *
  * Conventions for every entry point
  *   - Pointers are DEVICE pointers unless a comment says otherwise. The caller
  *     owns every buffer; the library allocates nothing and keeps no state
- *     between calls (beyond per-process kernel attributes set on first use).
+ *     between calls beyond per-process caches filled on first use (kernel
+ *     attributes, occupancy queries), the launch counter and profiling hook,
+ *     and the fixed scratch array of ssd_accept_static (described there).
  *   - `stream` is a cudaStream_t (NULL = legacy default stream). Every call is
  *     asynchronous on that stream and never synchronises, except
  *     ssd_read_device_error, which is documented as synchronous.
