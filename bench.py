@@ -60,8 +60,9 @@ def parse_args(argv=None):
                          "lets the finish kernel launch once the retrieval is done); auto: on unless the "
                          "gate can send sequences to the chain draft, whose unused copy-block rows the "
                          "early mode would read too")
-    ap.add_argument("--section", choices=["head"], default=None,
-                    help="run one extra measurement alone and print its JSON (head: the low-rank draft head)")
+    ap.add_argument("--section", choices=["head", "burst"], default=None,
+                    help="run one extra measurement alone and print its JSON (head: the low-rank draft head; "
+                         "burst: read bandwidth against burst size)")
     ap.add_argument("--oracle-worker", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--oracle-seconds", type=float, default=20.0, help=argparse.SUPPRESS)
     ap.add_argument("--oracle-warmup", type=int, default=0, help=argparse.SUPPRESS)
@@ -739,6 +740,55 @@ def measure_head(main, dev, iters=20):
     return res
 
 
+def measure_burst_curve(main, dev, sizes_mb=(8, 16, 32, 42, 64, 128, 256, 1024), reps=24, pool_mb=1024):
+    """Read bandwidth against burst size: ssd_read_probe (plain 16-byte loads, 8 in flight per
+    thread) reads X MB once per launch. Rotating buffers whose total is at least `pool_mb`
+    (> 7x L2), so every launch reads from DRAM. For each size and grid (2 or 4 CTAs of 256
+    threads per SM): `single` = median of the per-launch times between event pairs placed
+    around each of `reps` launches issued back to back (first 4 dropped); `stream` = the same
+    launches between one pair of events, mean per launch."""
+    import torch
+    from speculative_decoding_copy_gb300 import _binding as ssd
+    hbm, peak_kind = measured_peaks()
+    sink = torch.zeros(16, dtype=torch.uint8, device=dev)
+    pool = torch.empty(pool_mb << 20, dtype=torch.uint8, device=dev)
+    pool.fill_(1)
+    rows = []
+    for mb in sizes_mb:
+        nb = mb << 20
+        R = max(2, (pool_mb << 20) // nb)
+        bufs = [pool[i * nb:(i + 1) * nb] for i in range(R)]
+        for cps in (2, 4):
+            with torch.cuda.stream(main):
+                for j in range(3):
+                    ssd.ssd_read_probe(bufs[j % R], nb, sink, cps, stream=main)
+                evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+                for j in range(reps):
+                    evs[j].record(main)
+                    ssd.ssd_read_probe(bufs[j % R], nb, sink, cps, stream=main)
+                evs[reps].record(main)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(main)
+                for j in range(reps):
+                    ssd.ssd_read_probe(bufs[(j + 1) % R], nb, sink, cps, stream=main)
+                b.record(main)
+            torch.cuda.synchronize()
+            per = sorted(evs[j].elapsed_time(evs[j + 1]) * 1000.0 for j in range(4, reps))
+            single = statistics.median(per)
+            stream_us = a.elapsed_time(b) * 1000.0 / reps
+            rows.append({"mb": mb, "ctas_per_sm": cps, "buffers": R, "single_us": single,
+                         "single_gbs": nb / (single * 1e-6) / 1e9, "single_us_min": per[0], "single_us_max": per[-1],
+                         "stream_us": stream_us, "stream_gbs": nb / (stream_us * 1e-6) / 1e9})
+    del pool
+    torch.cuda.empty_cache()
+    for r in rows:
+        r["single_frac"] = r["single_gbs"] / hbm
+    return {"peak_gbs": hbm, "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth, burst)",
+            "kernel": "ssd_read_probe: grid-stride 16-byte loads, 8 in flight per thread, 256-thread CTAs",
+            "l2": f"rotating buffers over {pool_mb} MiB, each launch reads data last touched >= 1 GiB earlier",
+            "rows": rows}
+
+
 def _cpulist(text):
     cpus = set()
     for part in text.strip().split(","):
@@ -858,13 +908,16 @@ def main():
     if args.impl == "reference":
         run_reference(args)
         return
-    if args.section == "head":
+    if args.section is not None:
         import torch
         from speculative_decoding_copy_gb300 import _binding as ssd
         ssd.lib()
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)
-        print(json.dumps({"slimspec_head": measure_head(torch.cuda.Stream(dev), dev)}), flush=True)
+        if args.section == "head":
+            print(json.dumps({"slimspec_head": measure_head(torch.cuda.Stream(dev), dev)}), flush=True)
+        else:
+            print(json.dumps({"burst_curve": measure_burst_curve(torch.cuda.Stream(dev), dev)}), flush=True)
         return
     run_ours(args)
 

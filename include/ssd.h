@@ -26,9 +26,9 @@
  * ssd_commit_kv (append the accepted candidates' keys and values to the cache),
  * ssd_copy_stats (copy attempts and speculation tax), ssd_lowrank_head (the
  * SlimSpec low-rank draft LM head), ssd_accept_static (ssd_accept without a
- * caller workspace), and the diagnostics ssd_read_device_error,
- * ssd_status_string, ssd_version, ssd_launch_count, ssd_profile_kernel,
- * ssd_selftest_wait.
+ * caller workspace) with ssd_read_static_error, and the diagnostics
+ * ssd_read_device_error, ssd_status_string, ssd_version, ssd_launch_count,
+ * ssd_profile_kernel, ssd_selftest_wait, and the measurement tool ssd_read_probe.
  *
  * Conventions for every entry point
  *   - Pointers are DEVICE pointers unless a comment says otherwise. The caller
@@ -38,7 +38,8 @@
  *     and the fixed scratch array of ssd_accept_static (described there).
  *   - `stream` is a cudaStream_t (NULL = legacy default stream). Every call is
  *     asynchronous on that stream and never synchronises, except
- *     ssd_read_device_error, which is documented as synchronous.
+ *     ssd_read_device_error and ssd_read_static_error, which are documented
+ *     as synchronous.
  *   - Return value: SSD_OK or a negative ssd_status. Arguments are validated on
  *     the host before any launch; on an error nothing is launched and no output
  *     is written. SSD_ERR_CUDA means a launch failed (cudaGetLastError).
@@ -269,12 +270,17 @@ int ssd_verify_attn(const ssd_attn_args* a, void* ws, size_t ws_bytes, void* str
  *     the retrieval); blk_tok and blk_len are read only after that kernel has
  *     completed, and the call's last kernel starts only then. Results are
  *     identical; early_rows = 1 reads rows of absent tokens too (their
- *     contents are never used).
+ *     contents are never used). With early_rows = 1 the caller guarantees
+ *     that tgt and drf are complete before the call is issued (they are read
+ *     while the kernel before it on the stream may still run); only blk_tok
+ *     and blk_len may come from that kernel. In both modes the workspace is
+ *     written only after the kernel before the call on the stream has
+ *     completed, so consecutive calls on one stream may share a workspace.
  * 2 <= V < 2^31; NB*Dmax < 4096;
  * Dmax <= 256; 0 <= chain_blk < NB or chain_blk == -1.
  * Workspace: ssd_accept_workspace_size(a) bytes, 256-byte aligned; its
- * contents need no initialisation. The call may not overlap on the GPU with
- * another call that uses the same workspace.
+ * contents need no initialisation. Calls issued one after another on one
+ * stream may share it; calls that overlap on the GPU (other streams) may not.
  */
 typedef struct {
   int mode;
@@ -416,10 +422,35 @@ int ssd_lowrank_head(const ssd_head_args* a, void* ws, size_t ws_bytes, void* st
  * Every call on a device shares the one array and it keeps the previous call's
  * contents (nothing in it needs to start at zero), so calls that overlap on
  * the GPU — on different streams or from different threads — race; serialise
- * them. Device-side errors are recorded in the array's header and cannot be
- * read back through ssd_read_device_error.
+ * them. Calls issued one after another on one stream are serialised (in both
+ * early_rows modes). Device-side errors (a candidate token outside [0, V), a
+ * block longer than its slots) are recorded in the array's header; read and
+ * clear them with ssd_read_static_error.
  */
 int ssd_accept_static(const ssd_accept_args* a, void* stream);
+
+/*
+ * ssd_read_static_error — SYNCHRONOUS: waits for `stream`, then reads and
+ * clears the device error word of ssd_accept_static's fixed scratch on the
+ * current device. *out receives SSD_OK or the first error recorded since the
+ * last read (SSD_ERR_DEVICE, SSD_ERR_TIMEOUT). Like ssd_accept_static it
+ * allocates nothing (one small copy to the host, one to the device when the
+ * word was set) and has no counterpart on the pages. `out` is a host pointer.
+ * Errors: SSD_ERR_INVALID (out NULL), SSD_ERR_CUDA.
+ */
+int ssd_read_static_error(void* stream, int32_t* out);
+
+/*
+ * ssd_read_probe — measurement tool (no counterpart on the pages): reads `bytes`
+ * bytes of device memory at `buf` once with plain 16-byte loads (eight in flight
+ * per thread, a grid of ctas_per_sm x 256-thread CTAs per SM) and discards them,
+ * so that CUDA events around it give the device's read bandwidth for a burst of
+ * that size. Writes at most 16 bytes at `sink` (and in practice nothing).
+ *   buf, sink: device pointers, 16-byte aligned; bytes a multiple of 16, >= 16;
+ *   1 <= ctas_per_sm <= 8.
+ * Errors: SSD_ERR_INVALID, SSD_ERR_CUDA.
+ */
+int ssd_read_probe(const void* buf, size_t bytes, int ctas_per_sm, void* sink, void* stream);
 
 /*
  * ssd_read_device_error — SYNCHRONOUS: waits for `stream`, then reads and

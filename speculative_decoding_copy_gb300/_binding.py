@@ -27,7 +27,8 @@ EXPORTED = ["ssd_status_string", "ssd_version", "ssd_launch_count", "ssd_gate_ma
             "ssd_verify_attn_workspace_size", "ssd_verify_attn", "ssd_accept_workspace_size", "ssd_accept",
             "ssd_read_device_error", "ssd_profile_kernel", "ssd_accept_static", "ssd_gate_retrieve",
             "ssd_selftest_wait", "ssd_commit_kv",
-            "ssd_copy_stats", "ssd_lowrank_head_workspace_size", "ssd_lowrank_head"]
+            "ssd_copy_stats", "ssd_lowrank_head_workspace_size", "ssd_lowrank_head", "ssd_read_static_error",
+            "ssd_read_probe"]
 SSD_KERNEL = dict(vocab_stats=1, verify_attn=2, attn_combine=3, accept_finish=4, gate_match=6,
                   retrieve=7, head_down=8, head_up=9, head_combine=10)
 
@@ -113,6 +114,10 @@ def lib() -> ctypes.CDLL:
         L.ssd_read_device_error.argtypes = [c_void_p, c_void_p, POINTER(c_int32)]
         L.ssd_accept_static.restype = c_int
         L.ssd_accept_static.argtypes = [POINTER(AcceptArgs), c_void_p]
+        L.ssd_read_probe.restype = c_int
+        L.ssd_read_probe.argtypes = [c_void_p, c_size_t, c_int, c_void_p, c_void_p]
+        L.ssd_read_static_error.restype = c_int
+        L.ssd_read_static_error.argtypes = [c_void_p, POINTER(c_int32)]
         L.ssd_profile_kernel.restype = c_int
         L.ssd_profile_kernel.argtypes = [c_int, c_void_p, c_void_p]
         _lib = L
@@ -408,6 +413,16 @@ def ssd_lowrank_head(h, w_down, w_up, logits=None, logits_dtype=None, out=None, 
     return row_max, lse, argmax, logits, ws
 
 
+def ssd_read_probe(buf, nbytes, sink, ctas_per_sm=2, stream=None):
+    """Read `nbytes` of the device tensor `buf` once (measurement tool for read bandwidth)."""
+    if not buf.is_cuda or not sink.is_cuda or sink.numel() * sink.element_size() < 16:
+        raise ValueError("buf and sink (>= 16 bytes) must be CUDA tensors")
+    if nbytes > buf.numel() * buf.element_size():
+        raise ValueError("nbytes exceeds the buffer")
+    _check("ssd_read_probe", lib().ssd_read_probe(_ptr(buf), int(nbytes), int(ctas_per_sm), _ptr(sink),
+                                                  _stream(stream)))
+
+
 def ssd_read_device_error(ws, stream=None) -> int:
     v = c_int32(0)
     rc = lib().ssd_read_device_error(_ptr(ws), _stream(stream), ctypes.byref(v))
@@ -429,7 +444,7 @@ def ssd_profile_kernel(kernel: str | None, start=None, end=None):
 
 
 def ssd_accept_static(tgt, drf, blk_tok, blk_len, u_acc, u_fin, *, mode, kind, K=0, chain_blk=-1, out=None,
-                      stream=None):
+                      stream=None, early_rows=False):
     """ssd_accept with the library's fixed internal scratch instead of a workspace
     (for callers that cannot allocate); calls must not overlap on the GPU."""
     _need(tgt, "tgt", (torch.float32,) + _HALF, 3)
@@ -438,7 +453,15 @@ def ssd_accept_static(tgt, drf, blk_tok, blk_len, u_acc, u_fin, *, mode, kind, K
     B, NR, V = tgt.shape
     _, NB, Dmax = blk_tok.shape
     outs = out or alloc_accept_outputs(B, NB, Dmax, tgt.device)
-    args = accept_args(mode, kind, tgt, drf, blk_tok, blk_len, K, chain_blk, u_acc, u_fin, outs, None)
+    args = accept_args(mode, kind, tgt, drf, blk_tok, blk_len, K, chain_blk, u_acc, u_fin, outs, None, early_rows)
     rc = lib().ssd_accept_static(ctypes.byref(args), _stream(stream))
     _check("ssd_accept_static", rc)
     return outs
+
+
+def ssd_read_static_error(stream=None) -> int:
+    """Read and clear the device error word of ssd_accept_static's fixed scratch on the
+    current device (synchronises the stream)."""
+    v = c_int32(0)
+    _check("ssd_read_static_error", lib().ssd_read_static_error(_stream(stream), ctypes.byref(v)))
+    return int(v.value)

@@ -239,11 +239,16 @@ __global__ void __launch_bounds__(kStatsThreads, 2)
 k_vocab_stats(AcceptParams p) {
   // blk_len comes from the retrieval; once it is in, the next kernel of the stream may
   // start (its prologue reads the retrieval's outputs, never this kernel's). The early
-  // mode reads no blk_len: every CTA but the last lets the next kernel start at once and
-  // never waits; the last CTA first waits for the preceding kernel. So the next kernel
-  // starts only once that kernel (and what it waited for) has completed, and this grid
-  // completes only after it: the next kernel's wait then covers them all.
-  if (!p.early || blockIdx.x == gridDim.x - 1) asm volatile("griddepcontrol.wait;" ::: "memory");
+  // mode reads no blk_len: every CTA but the last lets the next kernel start at once;
+  // the last CTA first waits for the preceding kernel. So the next kernel starts only
+  // once that kernel (and what it waited for) has completed, and this grid completes
+  // only after it: the next kernel's wait then covers them all.
+  // The workspace may still be read by the kernel before this one (the finish kernel of
+  // an earlier call on the same workspace, which lets this grid launch at its start), so
+  // no CTA writes it before griddepcontrol.wait: in the early mode each warp keeps up to
+  // 32 piece results in its lanes and waits only before its first store.
+  bool waited = !p.early || blockIdx.x == gridDim.x - 1;
+  if (waited) asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int es = BF16 ? 2 : 4;
   const int lane = threadIdx.x & 31;
@@ -252,6 +257,9 @@ k_vocab_stats(AcceptParams p) {
   const int ntask = p.nch * p.NRD * p.B;
   const int per = kPieceElems;
   const bool vec_rows = ((p.V * es) & 15) == 0;
+  RowStat held{};                     // lane i: the i-th result of this warp, not yet stored
+  int64_t held_at = -1;
+  int nheld = 0;
   for (int t = next_task(p, gw, TW, ntask); t < ntask; t = next_task(p, t + TW, TW, ntask)) {
     const int br = t / p.nch, c = t - br * p.nch;
     const int b = br / p.NRD, r = br - b * p.NRD;
@@ -262,7 +270,26 @@ k_vocab_stats(AcceptParams p) {
     if (!vec_rows || !aligned_dev(row, 16)) st = reduce_piece<BF16, AMAX, false, false>(row, n, e0, p.probs);
     else if (n == per) st = reduce_piece<BF16, AMAX, true, true>(row, n, e0, p.probs);
     else st = reduce_piece<BF16, AMAX, true, false>(row, n, e0, p.probs);
-    if (lane == 0) p.part[static_cast<int64_t>(br) * p.nch + c] = st;
+    const int64_t at = static_cast<int64_t>(br) * p.nch + c;
+    if (!waited && nheld < 32) {      // every lane holds the same st after the warp reduction
+      if (lane == nheld) {
+        held = st;
+        held_at = at;
+      }
+      ++nheld;
+      continue;
+    }
+    if (!waited) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      waited = true;
+      if (held_at >= 0) p.part[held_at] = held;
+      held_at = -1;
+    }
+    if (lane == 0) p.part[at] = st;
+  }
+  if (!waited && nheld > 0) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (held_at >= 0) p.part[held_at] = held;
   }
 }
 
@@ -862,19 +889,21 @@ AcceptParams accept_params(const ssd_accept_args* a, const AcceptLayout& L, char
 // the stats kernel: a grid of as many CTAs as are resident at once
 template <bool BF16, bool AMAX>
 static cudaError_t launch_stats(const AcceptParams& p, cudaStream_t s) {
-  static std::once_flag once;
-  static long long cap = 0;
-  std::call_once(once, [] {
-    int dev = 0, sms = 152, per = 1;
-    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  static std::once_flag once[kMaxDevices];
+  static long long cap[kMaxDevices];
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  std::call_once(once[dev], [dev] {
+    int sms = 152, per = 1;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, k_vocab_stats<BF16, AMAX>, kStatsThreads, 0) !=
         cudaSuccess)
       per = 1;
-    cap = static_cast<long long>(sms) * (per > 0 ? per : 1);
+    cap[dev] = static_cast<long long>(sms) * (per > 0 ? per : 1);
   });
   const long long ntask = static_cast<long long>(p.nch) * p.NRD * p.B;
   const long long want = (ntask + kStatsWarps - 1) / kStatsWarps;
-  const dim3 g1(static_cast<unsigned>(want < cap ? want : cap));
+  const dim3 g1(static_cast<unsigned>(want < cap[dev] ? want : cap[dev]));
   return launch_pdl(k_vocab_stats<BF16, AMAX>, g1, dim3(kStatsThreads), 0, s, p);
 }
 
@@ -892,15 +921,17 @@ int accept_launch(const AcceptParams& p, cudaStream_t s) {
   {
     // merge, acceptance, choice and final draw: one cluster per sequence, with a warp
     // for every chunk of the stop row (8 CTAs up to 64 chunks, else 16)
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-      attr_err = cudaFuncSetAttribute(k_accept_finish, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      static_cast<int>(kFinDynSmem));
-      if (attr_err == cudaSuccess)
-        attr_err = cudaFuncSetAttribute(k_accept_finish, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    static std::once_flag once[kMaxDevices];
+    static cudaError_t attr_err[kMaxDevices];
+    const int dev = current_device();
+    if (dev < 0) return SSD_ERR_CUDA;
+    std::call_once(once[dev], [dev] {
+      attr_err[dev] = cudaFuncSetAttribute(k_accept_finish, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(kFinDynSmem));
+      if (attr_err[dev] == cudaSuccess)
+        attr_err[dev] = cudaFuncSetAttribute(k_accept_finish, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     });
-    if (attr_err != cudaSuccess) return SSD_ERR_CUDA;
+    if (attr_err[dev] != cudaSuccess) return SSD_ERR_CUDA;
     const unsigned C = (!p.sample || p.nchs <= kFinCTAs * kFinWarps) ? kFinCTAs : kMaxFinCTAs;
     KernelTimer t(SSD_KERNEL_ACCEPT_FINISH, s);
     cudaLaunchConfig_t cfg = {};
@@ -961,15 +992,14 @@ namespace ssd {
 constexpr size_t kStaticScratchBytes = size_t(4) << 20;   // 4 MiB
 static __device__ __align__(256) unsigned char g_accept_scratch[kStaticScratchBytes];
 
-constexpr int kMaxDevices = 64;
 static std::mutex g_scratch_mu;
 static void* g_scratch_addr[kMaxDevices];
 
 // Device address of the scratch array on the current device, looked up on the
 // first call for that device (the lookup loads the module there if needed).
 static int static_scratch(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SSD_ERR_CUDA;
+  const int dev = current_device();
+  if (dev < 0) return SSD_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
   if (g_scratch_addr[dev] == nullptr) {
     void* p = nullptr;
@@ -991,9 +1021,19 @@ extern "C" int ssd_accept_static(const ssd_accept_args* a, void* stream) {
   void* ws = nullptr;
   const int rc = static_scratch(&ws);
   if (rc != SSD_OK) return rc;
-  // Nothing in the scratch has to start at zero: the row pass writes every
-  // partial row statistic and the finish kernel every merged one before either
-  // is read, and the error header is only ever written here, never read back.
+  // Nothing in the scratch has to start at zero: the row pass writes every partial
+  // row statistic and the finish kernel every merged one before either is read. The
+  // error header at its start keeps the first device-side error until
+  // ssd_read_static_error reads and clears it (the array starts zeroed at load).
   const AcceptParams p = accept_params(a, L, static_cast<char*>(ws));
   return accept_launch(p, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int ssd_read_static_error(void* stream, int32_t* out) {
+  if (out == nullptr) return SSD_ERR_INVALID;
+  void* ws = nullptr;
+  const int rc = static_scratch(&ws);
+  if (rc != SSD_OK) return rc;
+  // the same read-and-clear as for a caller's workspace: a copy to the host, no allocation
+  return ssd_read_device_error(ws, stream, out);
 }

@@ -81,3 +81,50 @@ extern "C" int ssd_selftest_wait(void* ws, int arrive, uint64_t limit_clocks, vo
   ssd::count_launch();
   return ssd::check_launch();
 }
+
+// ------------------------------------------------------------------ read-bandwidth probe
+namespace ssd {
+// Every thread keeps 8 independent 16-byte loads in flight per pass of a grid-stride
+// loop over the buffer and folds them into an XOR; the fold is stored only if it equals
+// a value the caller passes (never, for a buffer that does not hold it), so the loads
+// cannot be dropped and nothing but `sink` is ever written.
+__global__ void __launch_bounds__(256) k_read_probe(const uint4* __restrict__ buf, size_t nvec, uint4* sink,
+                                                    uint32_t magic) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  uint4 acc = make_uint4(0u, 0u, 0u, 0u);
+  for (; i + 7 * stride < nvec; i += 8 * stride) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = __ldg(buf + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      acc.x ^= v[u].x;
+      acc.y ^= v[u].y;
+      acc.z ^= v[u].z;
+      acc.w ^= v[u].w;
+    }
+  }
+  for (; i < nvec; i += stride) {
+    const uint4 v = __ldg(buf + i);
+    acc.x ^= v.x;
+    acc.y ^= v.y;
+    acc.z ^= v.z;
+    acc.w ^= v.w;
+  }
+  if ((acc.x ^ acc.y ^ acc.z ^ acc.w) == magic) *sink = acc;
+}
+}  // namespace ssd
+
+extern "C" int ssd_read_probe(const void* buf, size_t bytes, int ctas_per_sm, void* sink, void* stream) {
+  if (buf == nullptr || sink == nullptr || bytes < 16 || (bytes % 16) != 0) return SSD_ERR_INVALID;
+  if (!ssd::aligned(buf, 16) || !ssd::aligned(sink, 16) || ctas_per_sm < 1 || ctas_per_sm > 8) return SSD_ERR_INVALID;
+  const int dev = ssd::current_device();
+  int sms = 0;
+  if (dev < 0 || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    return SSD_ERR_CUDA;
+  ssd::k_read_probe<<<sms * ctas_per_sm, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(buf), bytes / 16, static_cast<uint4*>(sink), 0x9E3779B9u);
+  ssd::count_launch();
+  return ssd::check_launch();
+}

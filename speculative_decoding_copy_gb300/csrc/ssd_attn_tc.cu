@@ -612,11 +612,11 @@ static bool make_cand_map(CUtensorMap* map, const void* base, uint64_t slots, in
 
 // How many clusters of S CTAs can be resident at once (0 if the query fails).
 static int max_active_clusters(int S) {
-  static int cache[kMaxSplit + 1][64];
-  static bool done[kMaxSplit + 1][64];
+  static int cache[kMaxSplit + 1][kMaxDevices];
+  static bool done[kMaxSplit + 1][kMaxDevices];
   static std::mutex mu;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  const int dev = current_device();
+  if (dev < 0) return 0;
   std::lock_guard<std::mutex> lock(mu);
   if (!done[S][dev]) {
     cudaLaunchConfig_t cfg = {};
@@ -701,13 +701,15 @@ int attn_tc_launch(const ssd_attn_args* a, void* ws, cudaStream_t s) {
   const int NT = a->NB * a->Dmax;
   const int G = a->Hq / a->Hkv;
   const int mtiles = (NT * G + tc::BM - 1) / tc::BM;
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(tc::k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(tc::kSmemBytes));
+  static std::once_flag attr_once[kMaxDevices];
+  static cudaError_t attr_err[kMaxDevices];
+  const int dev = current_device();
+  if (dev < 0) return SSD_ERR_CUDA;
+  std::call_once(attr_once[dev], [dev] {
+    attr_err[dev] = cudaFuncSetAttribute(tc::k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(tc::kSmemBytes));
   });
-  if (attr_err != cudaSuccess) return SSD_ERR_CUDA;
+  if (attr_err[dev] != cudaSuccess) return SSD_ERR_CUDA;
   int S = 1, chunk = tc::BN, chunk0 = tc::BN;
   tc::choose_split(a, mtiles, &S, &chunk, &chunk0);
   CUtensorMap mq, mk, mv, mkc, mvc;

@@ -71,6 +71,17 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Kernel attributes, occupancy figures and the static scratch address are per device:
+// host-side caches of them are arrays indexed by the current device.
+constexpr int kMaxDevices = 64;
+
+// the current device as an index into such a cache, or -1
+inline int current_device() {
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return -1;
+  return d;
+}
+
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Every workspace starts with this header. err is the device error word.

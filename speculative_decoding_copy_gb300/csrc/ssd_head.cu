@@ -525,10 +525,10 @@ static size_t down_smem_bytes(int N) {
 // 16 CTAs per cluster where the device can hold such a cluster of k_head_down at its
 // largest shared-memory size, else the portable 8 (per device, decided once)
 static int down_cluster_size() {
-  static int cache[64];
-  static std::once_flag once[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
+  static int cache[kMaxDevices];
+  static std::once_flag once[kMaxDevices];
+  const int dev = current_device();
+  if (dev < 0) return 8;
   std::call_once(once[dev], [dev] {
     int cs = 8;
     if (cudaFuncSetAttribute(k_head_down, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
@@ -596,14 +596,16 @@ extern "C" int ssd_lowrank_head(const ssd_head_args* a, void* ws, size_t ws_byte
   if (ws == nullptr || !aligned(ws, 256) || ws_bytes < need) return SSD_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(k_head_down, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(k_head_up, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+  static std::once_flag attr_once[kMaxDevices];
+  static cudaError_t attr_err[kMaxDevices];
+  const int dev = current_device();
+  if (dev < 0) return SSD_ERR_CUDA;
+  std::call_once(attr_once[dev], [dev] {
+    attr_err[dev] = cudaFuncSetAttribute(k_head_down, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    if (attr_err[dev] == cudaSuccess)
+      attr_err[dev] = cudaFuncSetAttribute(k_head_up, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
   });
-  if (attr_err != cudaSuccess) return SSD_ERR_CUDA;
+  if (attr_err[dev] != cudaSuccess) return SSD_ERR_CUDA;
 
   HeadParams p{};
   uint8_t* wsb = static_cast<uint8_t*>(ws);

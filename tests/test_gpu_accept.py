@@ -132,6 +132,44 @@ def test_accept_early_rows(mode, V, B, W, Dmax, K, policy):
     _assert_same(late, ref)
 
 
+@pytest.mark.parametrize("early", [True, False])
+def test_accept_back_to_back_calls_share_a_workspace(early):
+    """Calls issued one after another on one stream may share a workspace: each call's
+    row pass writes the workspace only after the previous call's finish kernel (which
+    reads it) has completed, in the early mode too. Pairs of calls with different rows
+    on one workspace, each pair's results bit-exact against the oracle."""
+    rng = np.random.default_rng(808 + early)
+    V, B, W, Dmax, K, policy = 128256, 3, 4, 20, 5, 2
+    dev = "cuda"
+    T = lambda a: to_device(np.asarray(a), dev) if a is not None else None
+    calls = []
+    for _ in range(2):
+        blk_tok, blk_len = _blocks(rng, B, W, Dmax, K, V, policy)
+        NB = blk_tok.shape[1]
+        tgt = _boost_probs(_rows_probs(rng, (B, 1 + NB * Dmax, V)), blk_tok, blk_len, Dmax, rng)
+        drf = _rows_probs(rng, (B, K, V))
+        for b in range(B):
+            for d in range(blk_len[b, W]):
+                blk_tok[b, W, d] = int(np.argmax(drf[b, d] * rng.random(V)))
+        u_acc = WL.uniforms24(rng, (B, NB, Dmax))
+        u_fin = WL.uniforms24(rng, (B,))
+        calls.append((tgt, drf, blk_tok, blk_len, u_acc, u_fin))
+    dv = [tuple(T(a) for a in c) for c in calls]
+    args = S.accept_args(S.SSD_SAMPLE, S.SSD_PROBS_F32, *dv[0][:4], K, W, *dv[0][4:],
+                         S.alloc_accept_outputs(B, W + 1, Dmax, dev))
+    ws = torch.zeros(S.ssd_accept_workspace_size(args), dtype=torch.uint8, device=dev)
+    refs = [_oracle("sample", "probs_f32", *c[:4], W, policy, *c[4:]) for c in calls]
+    for rep in range(20):
+        outs = []
+        for c in dv:
+            outs.append(S.ssd_accept(c[0], c[1], c[2], c[3], c[4], c[5], mode=S.SSD_SAMPLE, kind=S.SSD_PROBS_F32,
+                                     K=K, chain_blk=W, ws=ws, early_rows=early))
+        torch.cuda.synchronize()
+        for ref, o in zip(refs, outs):
+            _assert_same({k: v.cpu().numpy() for k, v in o.items()}, ref)
+    assert S.ssd_read_device_error(ws) == S.SSD_OK
+
+
 def _margins_explain(kind, tgt, drf, blk_tok, blk_len, W, policy, u_acc, u_fin, got, ref, b):
     """True if sequence b's disagreement sits within fp32 precision of one of the
     oracle's decision boundaries: an acceptance test u*q vs p, or the inverse-CDF
