@@ -35,7 +35,7 @@ UNIT = "verify steps/s"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0          # the "about 8 TB/s" the step's roofline is also quoted against
-FALLBACK_TFLOPS_SUSTAINED = 1700.0
+FALLBACK_TFLOPS_BURST = 1900.0
 
 
 def parse_args(argv=None):
@@ -48,7 +48,10 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-next", action="store_true",
-                    help="skip the measurements of the rows after the step (commit, paged cache, tax, head)")
+                    help="skip the measurements of the rows after the step (commit, paged cache, tax, head) "
+                         "and the burst curve")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the step measurements of the other workload shapes")
     ap.add_argument("--two-streams", action="store_true",
                     help="run attention on a second stream beside the acceptance chain (default: one stream, "
                          "acceptance first, attention overlapping the finish kernel)")
@@ -66,6 +69,8 @@ def parse_args(argv=None):
     ap.add_argument("--oracle-worker", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--oracle-seconds", type=float, default=20.0, help=argparse.SUPPRESS)
     ap.add_argument("--oracle-warmup", type=int, default=0, help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-procs", type=int, default=1, help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-sample-seqs", type=int, default=0, help=argparse.SUPPRESS)
     return ap.parse_args(argv)
 
 
@@ -83,15 +88,16 @@ def workload_config(wl, tokens_per_step, extra=None):
 
 
 def measured_tensor_peak():
-    """Sustained dense bf16 TFLOP/s measured on this machine (a cuBLAS GEMM looped under the power
-    cap), else the recipe's fallback."""
+    """Burst dense bf16 TFLOP/s measured on this machine (a cuBLAS GEMM timed alone): the
+    kernels here run in sub-millisecond regions, not under a seconds-long power cap.
+    Else the recipe's fallback."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        if d.get("bf16_tflops_sustained"):
-            return float(d["bf16_tflops_sustained"]), "measured"
-    return FALLBACK_TFLOPS_SUSTAINED, "fallback"
+        if d.get("bf16_tflops"):
+            return float(d["bf16_tflops"]), "measured"
+    return FALLBACK_TFLOPS_BURST, "fallback"
 
 
 def measured_peaks():
@@ -103,40 +109,101 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+_ORACLE = {}          # inputs and workload of the oracle worker's parallel step (inherited by forked workers)
+
+
+def _oracle_attn_chunk(task):
+    """One worker's share of the oracle attention: its slots of the batch (the inputs are
+    inherited from the parent at the fork; the block lengths come with the task)."""
+    from oracle import ssd_oracle as O
+    slots, bl = task
+    inp, wl = _ORACLE["inp"], _ORACLE["wl"]
+    return O.verify_attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["k_cand"], inp["v_cand"],
+                              inp["prefix_len"], bl, wl.Dmax, wl.kv_dtype, slots)
+
+
+def oracle_parallel_step(inp, wl, pool, procs):
+    """One oracle step with the attention's present slots dealt round-robin to `procs`
+    worker processes while the parent runs gate, retrieval and acceptance (the oracle's
+    own functions, unchanged; only the slots are split)."""
+    from oracle import ssd_oracle as O
+    r = O.verify_step(inp, wl, attention_slots=None)
+    bl = r["blk_len"]
+    slots = [(b, k * wl.Dmax + d) for b in range(wl.B) for k in range(wl.NB) for d in range(int(bl[b, k]))]
+    parts = pool.map(_oracle_attn_chunk, [(slots[i::procs], bl) for i in range(procs)])
+    r["attn"] = {k: v for part in parts for k, v in part.items()}
+    return r
+
+
 def oracle_worker(args):
-    """Time the CPU oracle on full steps of the workload (runs in a child process
-    pinned to one BLAS thread). Prints a JSON dict."""
+    """Time the CPU oracle on full steps of the workload (runs in a child process that
+    never touches the GPU). One process: one BLAS thread. --oracle-procs N > 1: the
+    attention is split over N forked worker processes (one BLAS thread each).
+    --oracle-sample-seqs S > 0: a batch of S sequences drawn with the workload's recipe
+    stands in for the full batch (the step rate is scaled by S / B). Prints a JSON dict."""
     import numpy as np  # noqa: F401
     from oracle import ssd_oracle as O
     from speculative_decoding_copy_gb300 import workloads as WL
-    wl = WL.WORKLOADS[args.workload]
-    inp = WL.make_inputs(wl)
+    wl_full = WL.WORKLOADS[args.workload]
+    S = args.oracle_sample_seqs
+    wl = wl_full.replace(B=S) if 0 < S < wl_full.B else wl_full
+    inp = WL.make_inputs(wl, WL.default_seed(wl_full.name))
+    procs = max(1, args.oracle_procs)
+    pool = None
+    if procs > 1:
+        import multiprocessing as mp
+        _ORACLE["inp"], _ORACLE["wl"] = inp, wl
+        pool = mp.get_context("fork").Pool(procs)    # this process has no CUDA context
+    step = (lambda: oracle_parallel_step(inp, wl, pool, procs)) if pool else (lambda: O.verify_step(inp, wl))
     for _ in range(args.oracle_warmup):          # untimed
-        O.verify_step(inp, wl)
+        step()
     budget = args.oracle_seconds
     n, t0 = 0, time.perf_counter()
     while True:
-        r = O.verify_step(inp, wl)
+        r = step()
         n += 1
         if time.perf_counter() - t0 >= budget or n >= 1000:
             break
     dt = time.perf_counter() - t0
+    if pool:
+        pool.close()
+        pool.join()
     tokens = int(r["blk_len"].sum())
-    print(json.dumps({"steps": n, "seconds": dt, "tokens_per_step": tokens}))
+    print(json.dumps({"steps": n, "seconds": dt, "tokens_per_step": tokens, "procs": procs, "sample_seqs": wl.B,
+                      "batch": wl_full.B}))
 
 
-def run_oracle_subprocess(workload, seconds, warmup=0):
+def run_oracle_subprocess(workload, seconds, warmup=0, procs=1, sample_seqs=0, timeout=900):
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
         env[k] = "1"
     env.pop("RANK", None)
     env.pop("WORLD_SIZE", None)
     cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--oracle-worker", "--workload", workload,
-           "--oracle-seconds", str(seconds), "--oracle-warmup", str(warmup)]
-    r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=900)
+           "--oracle-seconds", str(seconds), "--oracle-warmup", str(warmup), "--oracle-procs", str(procs),
+           "--oracle-sample-seqs", str(sample_seqs)]
+    r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=timeout)
     if r.returncode != 0:
         raise RuntimeError(f"oracle worker failed: {r.stderr[-2000:]}")
     return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def oracle_baseline(workload, seconds, procs=1, sample_seqs=0):
+    """The cpu_baseline record of one oracle run (steps/s of the full batch; a sample of
+    sequences is scaled to it)."""
+    try:
+        res = run_oracle_subprocess(workload, seconds, 0, procs, sample_seqs)
+    except Exception as e:  # report, do not hide
+        return {"value": None, "unit": UNIT, "cores": procs, "kind": "oracle", "sample": f"failed: {e}"}
+    scale = res["sample_seqs"] / res["batch"]
+    value = res["steps"] / res["seconds"] * scale
+    how = "one BLAS thread" if procs == 1 else f"attention split over {procs} processes, one BLAS thread each"
+    part = ("full batches" if res["sample_seqs"] == res["batch"] else
+            f"batches of {res['sample_seqs']} of the {res['batch']} sequences (same recipe), rate scaled by "
+            f"{res['sample_seqs']}/{res['batch']}")
+    return {"value": value, "unit": UNIT, "cores": procs, "kind": "oracle",
+            "sample": f"{res['steps']} oracle steps on {part} in {res['seconds']:.1f} s ({how})",
+            "cpu": cpu_model(), "nproc": os.cpu_count()}
 
 
 def cpu_model():
@@ -282,8 +349,134 @@ def dram_traffic(kernel, workload):
     return e.get("dram_bytes_per_launch")
 
 
+REPEATS = 7          # timed repeats of the K-step region; the reported step time is their median
+
+
+class StepTimer:
+    """CUDA graphs of consecutive steps over R input copies (one step per copy, in order)
+    and timed replays of exactly K steps."""
+
+    def __init__(self, steps, main, aux, world=1, dev=None):
+        self.steps, self.main, self.aux, self.world, self.dev = steps, main, aux, world, dev
+        self.R = len(steps)
+
+    def capture(self, idx, hooked):
+        """One graph running the steps of copies `idx` in order; `hooked` kernels are
+        bracketed by event nodes (one pair per step and kernel)."""
+        import torch
+        from speculative_decoding_copy_gb300 import _binding as ssd
+        main = self.main
+        evs = [{k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for k in hooked}
+               for _ in idx]
+        for d in evs:
+            for a, b2 in d.values():
+                a.record(main)
+                b2.record(main)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=main):
+            for j, i in enumerate(idx):
+                for k in hooked:
+                    ssd.ssd_profile_kernel(k, *evs[j][k])
+                self.steps[i].run(main, self.aux)
+                ssd.ssd_profile_kernel(None)
+        torch.cuda.synchronize()
+        return g, evs
+
+    def plan(self, K, hooked):
+        """Graphs that run exactly K steps: K // R replays of the R-step graph and one
+        replay of a graph of the first K % R steps."""
+        R = self.R
+        full, ev_full = self.capture(list(range(R)), hooked)
+        tail, ev_tail = (self.capture(list(range(K % R)), hooked) if K % R else (None, []))
+        seq = [full] * (K // R) + ([tail] if tail is not None else [])
+        return full, seq, ev_full + ev_tail
+
+    def warm(self, n):
+        import torch
+        with torch.cuda.stream(self.main):
+            for i in range(n):
+                self.steps[i % self.R].run(self.main, self.aux)
+        torch.cuda.synchronize()
+
+    @staticmethod
+    def mean_us(evs, k):
+        v = [d[k][0].elapsed_time(d[k][1]) * 1000.0 for d in evs]
+        v = [x for x in v if x > 0]
+        return statistics.mean(v) if v else None
+
+    def kernel_us(self, kernels, replays):
+        """Per-kernel durations (µs, mean) with every kernel of `kernels` bracketed (untimed pass)."""
+        import torch
+        g, ev = self.capture(list(range(self.R)), kernels)
+        with torch.cuda.stream(self.main):
+            for _ in range(replays):
+                g.replay()
+        torch.cuda.synchronize()
+        out = {k: self.mean_us(ev, k) for k in kernels}
+        del g
+        return {k: v for k, v in out.items() if v is not None}
+
+    def timed(self, seq, repeats):
+        """Replay `seq` (exactly K steps) `repeats` times, each bracketed by a barrier, a
+        synchronize and CUDA events on the launching stream; ms per repeat (max over ranks)."""
+        import torch
+        import torch.distributed as dist
+        out = []
+        for _ in range(repeats):
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            if self.world > 1:
+                dist.barrier()
+            torch.cuda.synchronize()
+            with torch.cuda.stream(self.main):
+                t0.record(self.main)
+                for g in seq:
+                    g.replay()
+                t1.record(self.main)
+            torch.cuda.synchronize()
+            ms = t0.elapsed_time(t1)
+            out.append(max_over_ranks(ms, self.dev) if self.world > 1 else ms)
+        return out
+
+
+def kernel_roofline(dom, dom_us, wl, ab, blk_len, prefix, hbm, peak_kind, tf_burst, tf_kind):
+    """The dominant kernel against its bound: the attention against the burst bf16 tensor
+    rate when its flops take longer there than its bytes at the copy bandwidth, else
+    against HBM; the row pass against HBM."""
+    kb = {"vocab_stats": ab["logits"], "verify_attn": ab["kv"] + (ab["q_o"] // 2)}
+    kf = {"vocab_stats": 0.0,
+          "verify_attn": float(sum(4.0 * int(blk_len[b].sum()) * wl.Hq * wl.dh * int(prefix[b])
+                                   for b in range(wl.B)))}
+    t_hbm = kb[dom] / (hbm * 1e9)
+    t_tc = kf[dom] / (tf_burst * 1e12) if kf[dom] else 0.0
+    hbm_view = {"bound": "hbm", "achieved": kb[dom] / (dom_us * 1e-6) / 1e9 if dom_us else None, "peak": hbm,
+                "unit": "GB/s", "algorithmic_bytes_per_launch": kb[dom],
+                "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth, burst)"}
+    hbm_view["frac"] = hbm_view["achieved"] / hbm if hbm_view["achieved"] else None
+    timing = ("CUDA events around the kernel inside the graphs of a second timed region of the same "
+              "K steps (event nodes break the kernel chaining, so the step time is taken without them)")
+    if t_tc > t_hbm:
+        ach = kf[dom] / (dom_us * 1e-6) / 1e12 if dom_us else None
+        return {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": tf_burst, "unit": "TFLOP/s",
+                "frac": (ach / tf_burst) if ach else None, "traffic": dram_traffic(dom, wl.name),
+                "algorithmic_flops_per_launch": kf[dom], "algorithmic_bytes_per_launch": kb[dom],
+                "launch_us": dom_us, "timing": timing,
+                "peak_source": f"{tf_kind} bf16_tflops (cuBLAS bf16 GEMM, burst: the kernel runs in "
+                               f"sub-millisecond regions)",
+                "hbm_view": hbm_view}
+    return dict(hbm_view, kernel=dom, traffic=dram_traffic(dom, wl.name), launch_us=dom_us, timing=timing)
+
+
+def step_record(wl, ab, ms_list, K, world, hbm):
+    ms_per_step = statistics.median(ms_list) / K
+    step_bytes = ab["total"]
+    step_gbs = step_bytes / (ms_per_step * 1e-3) / 1e9
+    return ms_per_step, {"algorithmic_bytes_per_step": step_bytes, "achieved_gbs": step_gbs,
+                         "frac_of_measured_hbm": step_gbs / hbm, "frac_of_nominal_hbm": step_gbs / NOMINAL_HBM_GBS}
+
+
 def run_ours(args):
-    import numpy as np
+    import numpy as np  # noqa: F401
     import torch
     import torch.distributed as dist
 
@@ -318,66 +511,21 @@ def run_ours(args):
     steps = [probe] + [VerifyStep(wl, inp, device=dev, order=args.order, early_rows=early)
                        for _ in range(R - 1)]
     tokens = ab["tokens"]
-
-    def capture(idx, hooked):
-        """One graph that runs the steps of input copies `idx` in order; `hooked` kernels
-        are bracketed by event nodes (one pair per step and kernel)."""
-        evs = [{k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for k in hooked}
-               for _ in idx]
-        for d in evs:
-            for a, b2 in d.values():
-                a.record(main)
-                b2.record(main)
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=main):
-            for j, i in enumerate(idx):
-                for k in hooked:
-                    ssd.ssd_profile_kernel(k, *evs[j][k])
-                steps[i].run(main, aux)
-                ssd.ssd_profile_kernel(None)
-        torch.cuda.synchronize()
-        return g, evs
-
-    def mean_us(evs, k):
-        v = [d[k][0].elapsed_time(d[k][1]) * 1000.0 for d in evs]
-        v = [x for x in v if x > 0]
-        return statistics.mean(v) if v else None
-
     K = args.steps
-
-    def plan(hooked):
-        """Graphs that run exactly K steps: K // R replays of the R-step graph and one
-        replay of a graph of the first K % R steps."""
-        full, ev_full = capture(list(range(R)), hooked)
-        tail, ev_tail = (capture(list(range(K % R)), hooked) if K % R else (None, []))
-        seq = [full] * (K // R) + ([tail] if tail is not None else [])
-        return full, seq, ev_full + ev_tail
-
-    # warm-up (eager)
-    with torch.cuda.stream(main):
-        for i in range(max(3, args.warmup // 10)):
-            steps[i % R].run(main, aux)
-    torch.cuda.synchronize()
+    timer = StepTimer(steps, main, aux, world, dev)
+    timer.warm(max(3, args.warmup // 10))
 
     # diagnostic pass (untimed): every kernel hooked, per-kernel durations
-    diag, diag_ev = capture(list(range(R)), KERNELS)
-    with torch.cuda.stream(main):
-        for i in range(max(3, 60 // R)):
-            diag.replay()
-    torch.cuda.synchronize()
-    kern_us = {k: mean_us(diag_ev, k) for k in KERNELS}
-    kern_us = {k: v for k, v in kern_us.items() if v is not None}
-    del diag
+    kern_us = timer.kernel_us(KERNELS, max(3, 60 // R))
     streaming = [k for k in ("vocab_stats", "verify_attn") if k in kern_us]
     dom = max(streaming, key=lambda k: kern_us[k])
 
     # timed region 1: the step, no event nodes inside the graphs
     n0 = ssd.launch_count()
-    full, seq, _ = plan([])
+    full, seq, _ = timer.plan(K, [])
     launches_per_step = (ssd.launch_count() - n0) // (R + K % R)
     # timed region 2: the same K steps with the dominant kernel bracketed by event nodes
-    full_h, seq_h, ev_h = plan([dom])
+    full_h, seq_h, ev_h = timer.plan(K, [dom])
 
     with torch.cuda.stream(main):
         for _ in range(max(1, -(-args.warmup // R))):
@@ -385,107 +533,128 @@ def run_ours(args):
             full_h.replay()
     torch.cuda.synchronize()
 
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
-    with torch.cuda.stream(main):
-        t_start.record(main)
-        for g in seq:
-            g.replay()
-        t_end.record(main)
-    torch.cuda.synchronize()
+    ms_list = timer.timed(seq, REPEATS)
     with torch.cuda.stream(main):
         for g in seq_h:
             g.replay()
     torch.cuda.synchronize()
     time.sleep(0.2)
     clk = clocks.stop()
-    if world > 1:
-        dist.barrier()
-    ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        ms = max_over_ranks(ms, dev)
-    ms_per_step = ms / K
-    value = whole_job_value(world, K, ms)
-    dom_us = mean_us(ev_h, dom)
+    hbm, peak_kind = measured_peaks()
+    tf_burst, tf_kind = measured_tensor_peak()
+    ms_per_step, step_roof = step_record(wl, ab, ms_list, K, world, hbm)
+    value = whole_job_value(world, K, ms_per_step * K)
+    dom_us = StepTimer.mean_us(ev_h, dom)
+    roofline = kernel_roofline(dom, dom_us, wl, ab, blk_len, prefix, hbm, peak_kind, tf_burst, tf_kind)
+    del full, seq, full_h, seq_h
 
     # end to end through the public API with host buffers
     e2e = run_e2e(args, wl, inp, steps[0], main, aux, dev, world)
     nxt = None if args.no_next else {
            "commit_kv": measure_commit(wl, main, dev), "paged_attn": measure_paged(wl, steps[0], main, dev),
            "spec_tax": measure_tax(main, dev), "slimspec_head": measure_head(main, dev)}
+    del steps, probe, timer
+    torch.cuda.empty_cache()
+    do_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    others = None if args.no_workloads else measure_workloads(args, main, dev, world, rank, do_cpu)
+    burst = None if args.no_next else measure_burst_curve(main, dev)
 
-    hbm, peak_kind = measured_peaks()
-    tflops_sus, tflops_kind = measured_tensor_peak()
-    kb = {"vocab_stats": ab["logits"], "verify_attn": ab["kv"] + (ab["q_o"] // 2)}
-    # algorithmic flops: Q K^T and P V over the prefix for every verified token and q head
-    # (the own-block part is negligible); the row pass has no contraction
-    kf = {"vocab_stats": 0.0,
-          "verify_attn": float(sum(4.0 * int(blk_len[b].sum()) * wl.Hq * wl.dh * int(prefix[b])
-                                   for b in range(wl.B)))}
-    t_hbm = kb[dom] / (hbm * 1e9)
-    t_tc = kf[dom] / (tflops_sus * 1e12) if kf[dom] else 0.0
-    timing = ("CUDA events around the kernel inside the graphs of a second timed region of the same "
-              "K steps (event nodes break the kernel chaining, so the step time is taken without them)")
-    hbm_view = {"bound": "hbm", "achieved": kb[dom] / (dom_us * 1e-6) / 1e9 if dom_us else None, "peak": hbm,
-                "unit": "GB/s", "algorithmic_bytes_per_launch": kb[dom],
-                "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth, burst)"}
-    hbm_view["frac"] = hbm_view["achieved"] / hbm if hbm_view["achieved"] else None
-    if t_tc > t_hbm:
-        # the kernel's own roofline is its tensor time: report against the sustained bf16 peak
-        # (it is timed inside a long step), the HBM view beside it
-        ach = kf[dom] / (dom_us * 1e-6) / 1e12 if dom_us else None
-        roofline = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": tflops_sus, "unit": "TFLOP/s",
-                    "frac": (ach / tflops_sus) if ach else None, "traffic": dram_traffic(dom, wl.name),
-                    "algorithmic_flops_per_launch": kf[dom], "algorithmic_bytes_per_launch": kb[dom],
-                    "launch_us": dom_us, "timing": timing,
-                    "peak_source": f"{tflops_kind} bf16_tflops_sustained (cuBLAS bf16 GEMM under the power cap)",
-                    "hbm_view": hbm_view}
-    else:
-        roofline = dict(hbm_view, kernel=dom, traffic=dram_traffic(dom, wl.name), launch_us=dom_us, timing=timing)
-    step_bytes = ab["total"]
-    step_gbs = step_bytes / (ms_per_step * 1e-3) / 1e9
-    step_roof = {"algorithmic_bytes_per_step": step_bytes,
-                 "achieved_gbs": step_gbs,
-                 "frac_of_measured_hbm": step_gbs / hbm,
-                 "frac_of_nominal_hbm": step_gbs / NOMINAL_HBM_GBS}
-
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        try:
-            res = run_oracle_subprocess(args.workload, args.oracle_seconds)
-            cpu = {"value": res["steps"] / res["seconds"], "unit": UNIT, "cores": 1, "kind": "oracle",
-                   "sample": f"{res['steps']} full oracle steps (same workload, one BLAS thread) in "
-                             f"{res['seconds']:.1f} s", "cpu": cpu_model()}
-        except Exception as e:  # report, do not hide
-            cpu = {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": f"failed: {e}"}
+    cpu = cpu_par = None
+    if do_cpu:
+        cpu = oracle_baseline(args.workload, args.oracle_seconds, 1)
+        cpu_par = oracle_baseline(args.workload, min(args.oracle_seconds, 15.0), os.cpu_count() or 1)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
                 "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16/f32", "data": "synthetic",
                 "config": workload_config(wl, tokens, {
-                    "l2": f"{R} rotating input copies ({R * step_bytes / 2**20:.0f} MiB > 2x L2); no flush",
+                    "l2": f"{R} rotating input copies ({R * ab['total'] / 2**20:.0f} MiB > 2x L2); no flush",
+                    "timing": f"median of {REPEATS} timed repeats of the K-step region (each bracketed by a "
+                              f"barrier, a synchronize and CUDA events); value and ms_per_step from the median",
                     "parallelism": f"replicas x{world} (independent batches per GPU)",
                     "step_order": "two streams" if args.two_streams else args.order,
                     "early_rows": early}),
+                "ms_per_step_repeats": [m / K for m in ms_list],
+                "ms_per_step_spread": [min(ms_list) / K, max(ms_list) / K],
                 "candidate_tokens_per_s": value * tokens,
                 "hbm_roofline_step": step_roof,
                 "roofline": roofline,
                 "kernels_us_diagnostic": kern_us,
                 "e2e": e2e,
+                "workloads": others,
                 "next": nxt,
+                "burst_curve": burst,
                 "gpu_launches": launches_per_step * K,
                 "clocks": clk,
-                "cpu_baseline": cpu}
+                "cpu_baseline": cpu,
+                "cpu_baseline_parallel": cpu_par}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+OTHER_WORKLOADS = ["batched", "llama70b", "qwen8b_mixed", "qwen8b_mixed_act086"]
+
+
+def measure_workloads(args, main, dev, world, rank, do_cpu, steps=10):
+    """The other workload shapes: per workload its step time (median of REPEATS timed
+    repeats of `steps` graph-replayed steps), steps/s, candidate tokens/s, the step's
+    fraction of the HBM roofline and the dominant kernel against its bound. Inputs are
+    drawn on the device (workloads.make_inputs_device): one copy of 0.7-5 GB per workload,
+    far above the L2, so every step reads HBM. With do_cpu, the oracle on a sample of
+    sequences with the attention split over the host's cores (cpu_baseline)."""
+    import torch
+    from speculative_decoding_copy_gb300 import workloads as WL
+    from speculative_decoding_copy_gb300.step import VerifyStep, default_early_rows
+    hbm, peak_kind = measured_peaks()
+    tf_burst, tf_kind = measured_tensor_peak()
+    out = {}
+    for name in OTHER_WORKLOADS:
+        wl = WL.WORKLOADS[name]
+        inp = WL.make_inputs_device(wl, WL.default_seed(name) + 1000 * rank, dev)
+        early = default_early_rows(wl)
+        st = VerifyStep(wl, inp, device=dev, early_rows=early)
+        with torch.cuda.stream(main):
+            st.run(main)
+        torch.cuda.synchronize()
+        blk_len = st.ret_out["blk_len"].cpu().numpy()
+        prefix = inp["prefix_len"]
+        ab = WL.algorithmic_bytes(wl, prefix, blk_len)
+        timer = StepTimer([st], main, None, world, dev)
+        timer.warm(3)
+        kern_us = timer.kernel_us(KERNELS, 3)
+        dom = max([k for k in ("vocab_stats", "verify_attn") if k in kern_us], key=lambda k: kern_us[k])
+        full, seq, _ = timer.plan(steps, [])
+        _, seq_h, ev_h = timer.plan(steps, [dom])
+        with torch.cuda.stream(main):
+            full.replay()
+        torch.cuda.synchronize()
+        ms_list = timer.timed(seq, REPEATS)
+        with torch.cuda.stream(main):
+            for g in seq_h:
+                g.replay()
+        torch.cuda.synchronize()
+        ms_per_step, step_roof = step_record(wl, ab, ms_list, steps, world, hbm)
+        dom_us = StepTimer.mean_us(ev_h, dom)
+        value = whole_job_value(world, steps, ms_per_step * steps)
+        rec = {"workload": f"{wl.name}: {wl.description}, {wl.mode} mode", "batch": wl.B,
+               "steps": steps, "ms_per_step": ms_per_step, "us_per_step": ms_per_step * 1000.0,
+               "ms_per_step_spread": [min(ms_list) / steps, max(ms_list) / steps],
+               "steps_per_s": value, "candidate_tokens_per_step": ab["tokens"],
+               "candidate_tokens_per_s": value * ab["tokens"], "early_rows": early, "skip_absent": st.skip_absent,
+               "hbm_roofline_step": step_roof, "kernels_us_diagnostic": kern_us,
+               "roofline": kernel_roofline(dom, dom_us, wl, ab, blk_len, prefix, hbm, peak_kind, tf_burst, tf_kind),
+               "inputs": "drawn on the device (seeded torch generator), one copy above the L2; no flush"}
+        del full, seq, seq_h, timer, st, inp
+        torch.cuda.empty_cache()
+        if do_cpu:
+            rec["cpu_baseline"] = oracle_baseline(name, 8.0, os.cpu_count() or 1, sample_seqs=2 if wl.B > 4 else 1)
+        out[name] = rec
+    return out
 
 
 def measure_commit(wl, main, dev, calls=200):
@@ -740,10 +909,10 @@ def measure_head(main, dev, iters=20):
     return res
 
 
-def measure_burst_curve(main, dev, sizes_mb=(8, 16, 32, 42, 64, 128, 256, 1024), reps=24, pool_mb=1024):
+def measure_burst_curve(main, dev, sizes_mb=(8, 16, 32, 42, 64, 128, 256, 1024), reps=24, pool_mb=2048):
     """Read bandwidth against burst size: ssd_read_probe (plain 16-byte loads, 8 in flight per
     thread) reads X MB once per launch. Rotating buffers whose total is at least `pool_mb`
-    (> 7x L2), so every launch reads from DRAM. For each size and grid (2 or 4 CTAs of 256
+    (> 15x L2), so every launch reads from DRAM. For each size and grid (2 or 4 CTAs of 256
     threads per SM): `single` = median of the per-launch times between event pairs placed
     around each of `reps` launches issued back to back (first 4 dropped); `stream` = the same
     launches between one pair of events, mean per launch."""
@@ -756,7 +925,7 @@ def measure_burst_curve(main, dev, sizes_mb=(8, 16, 32, 42, 64, 128, 256, 1024),
     rows = []
     for mb in sizes_mb:
         nb = mb << 20
-        R = max(2, (pool_mb << 20) // nb)
+        R = (pool_mb << 20) // nb        # >= 2: the pool holds at least two buffers of the largest size
         bufs = [pool[i * nb:(i + 1) * nb] for i in range(R)]
         for cps in (2, 4):
             with torch.cuda.stream(main):
@@ -785,7 +954,8 @@ def measure_burst_curve(main, dev, sizes_mb=(8, 16, 32, 42, 64, 128, 256, 1024),
         r["single_frac"] = r["single_gbs"] / hbm
     return {"peak_gbs": hbm, "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth, burst)",
             "kernel": "ssd_read_probe: grid-stride 16-byte loads, 8 in flight per thread, 256-thread CTAs",
-            "l2": f"rotating buffers over {pool_mb} MiB, each launch reads data last touched >= 1 GiB earlier",
+            "l2": f"rotating buffers over {pool_mb} MiB: each launch reads data last touched at least one buffer "
+                  f"pool's worth of reads earlier (>= 1 GiB)",
             "rows": rows}
 
 
@@ -900,11 +1070,28 @@ def run_e2e(args, wl, inp, st, main, aux, dev, world=1):
                       "that step i+1's copy overlaps step i"}
 
 
+def free_port():
+    import socket
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as so:
+        so.bind(("127.0.0.1", 0))
+        return so.getsockname()[1]
+
+
+def relaunch_ranks(n):
+    """`--gpus N` outside torchrun: start N ranks of this same command under
+    torch.distributed.run (one per GPU, rendezvous on 127.0.0.1); rank 0 prints the line."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(free_port()), os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.run(cmd).returncode
+
+
 def main():
     args = parse_args()
     if args.oracle_worker:
         oracle_worker(args)
         return
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(relaunch_ranks(args.gpus))
     if args.impl == "reference":
         run_reference(args)
         return

@@ -48,11 +48,15 @@ ARENA_ALIGN = 256
 
 
 def _step_inputs(inp: dict, with_attention: bool):
-    """(key, contiguous numpy array) for every input a step reads, in INPUT_KEYS order."""
+    """(key, contiguous numpy array or device tensor) for every input a step reads, in
+    INPUT_KEYS order."""
     out = []
     for k in INPUT_KEYS:
         v = inp.get(k)
         if v is None or (not with_attention and k in ATTN_KEYS):
+            continue
+        if isinstance(v, torch.Tensor):
+            out.append((k, v))
             continue
         a = np.ascontiguousarray(v)
         out.append((k, a.view(np.int16) if a.dtype == np.uint16 else a))
@@ -113,7 +117,8 @@ class VerifyStep:
                 off += a.nbytes
         else:
             for k, a in _step_inputs(inp, with_attention):
-                self.x[k] = to_device(a, self.device)
+                # device tensors (inputs drawn on the GPU) are used in place
+                self.x[k] = a.contiguous() if isinstance(a, torch.Tensor) else to_device(a, self.device)
         B = wl.B
         self.with_attention = with_attention and "q" in self.x
         i32 = lambda *s: torch.empty(s, dtype=torch.int32, device=self.device)

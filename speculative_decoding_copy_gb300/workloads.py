@@ -140,8 +140,25 @@ WORKLOADS = {
                     "D=20) or chain (K=5) per sequence, bf16 logits V=151936"),
 }
 
-# order of the five workloads (small case first)
+# the Qwen3-8B-shaped batch at the copy-mode activation rate the SwitchSD page reports for
+# Qwen3-8B ("어떻게 쓰나": copying fires on 8.6% of steps): 6 of 64 sequences in copy mode
+WORKLOADS["qwen8b_mixed_act086"] = WORKLOADS["qwen8b_mixed"].replace(
+    name="qwen8b_mixed_act086", gate_on_frac=0.086,
+    description="Qwen3-8B-shaped mixed batch at 8.6% copy activation: B=64, prefix 2k-8k, copy (W=4 "
+                "D=20) for 6 sequences, chain (K=5) for the rest, bf16 logits V=151936")
+
+# order of the five workloads (small case first); variants take the seeds after them
 WORKLOAD_ORDER = ["tiny", "llama8b", "batched", "llama70b", "qwen8b_mixed"]
+VARIANT_ORDER = ["qwen8b_mixed_act086"]
+
+
+def default_seed(name: str) -> int:
+    """The seed a workload's inputs are drawn with unless one is given."""
+    if name in WORKLOAD_ORDER:
+        return SEED_BASE + WORKLOAD_ORDER.index(name)
+    if name in VARIANT_ORDER:
+        return SEED_BASE + len(WORKLOAD_ORDER) + VARIANT_ORDER.index(name)
+    return SEED_BASE
 
 # the speculation-tax experiment: every sequence ends in a repeated kappa-gram, half of
 # them copy-intended (probe high, target follows the copy), half accidental (probe low,
@@ -277,7 +294,7 @@ def make_inputs(wl: Workload, seed: int | None = None, *, full_width: bool = Tru
     q_scale: multiplies Q (sharper attention for tests).
     """
     if seed is None:
-        seed = SEED_BASE + WORKLOAD_ORDER.index(wl.name) if wl.name in WORKLOAD_ORDER else SEED_BASE
+        seed = default_seed(wl.name)
     rng = np.random.Generator(np.random.PCG64(seed))
     B = wl.B
     lo, hi = wl.ctx_len
@@ -354,6 +371,51 @@ def make_inputs(wl: Workload, seed: int | None = None, *, full_width: bool = Tru
         out["chain_tok"] = rng.integers(0, wl.V, size=(B, wl.K)).astype(np.int32)
     out["u_acc"] = uniforms24(rng, (B, NB, Dmax))
     out["u_fin"] = uniforms24(rng, (B,))
+    return out
+
+
+def make_inputs_device(wl: Workload, seed: int | None, device, *, full_width: bool = True) -> dict:
+    """The recipe of make_inputs with the large tensors drawn on `device` by torch's seeded
+    generator: Q, the prefix K/V cache and the candidate K/V ~ N(0, 1) and the target and
+    draft logits ~ N(0, logit_var), stored as bf16 (torch.bfloat16 viewed as int16) or fp32,
+    and the chain tokens drawn from softmax(draft logits) by the Gumbel-max construction.
+    The context, probe and uniforms come from make_inputs on the host. Host-side drawing of
+    the multi-GB batches takes minutes; the values differ from make_inputs' but follow the
+    same distributions (timing runs only: no oracle sees them)."""
+    import torch
+    if seed is None:
+        seed = default_seed(wl.name)
+    out = make_inputs(wl, seed, full_width=full_width, with_attention=False, with_logits=False)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed) + 0x7E57)
+    B, NT = wl.B, wl.NT
+    P_max = int(out["ctx"].shape[1])
+
+    def draw(shape, dtype, std=1.0):
+        x = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+        if std != 1.0:
+            x.mul_(std)
+        return x.to(torch.bfloat16).view(torch.int16) if dtype == "bf16" else x
+
+    out["q"] = draw((B, NT, wl.Hq, wl.dh), wl.kv_dtype)
+    out["k_cache"] = draw((B, wl.Hkv, P_max, wl.dh), wl.kv_dtype)
+    out["v_cache"] = draw((B, wl.Hkv, P_max, wl.dh), wl.kv_dtype)
+    out["k_cand"] = draw((B, NT, wl.Hkv, wl.dh), wl.kv_dtype)
+    out["v_cand"] = draw((B, NT, wl.Hkv, wl.dh), wl.kv_dtype)
+    out["prefix_len"] = out["ctx_len"].copy()
+    sd = math.sqrt(wl.logit_var)
+    out["tgt"] = draw((B, wl.NR, wl.V), wl.logit_dtype, sd)
+    if wl.K > 0:
+        drf = draw((B, wl.K, wl.V), wl.logit_dtype, sd)
+        vals = drf.view(torch.bfloat16).float() if wl.logit_dtype == "bf16" else drf
+        u = torch.rand((B, wl.K, wl.V), generator=gen, device=device, dtype=torch.float64)
+        g = -torch.log(-torch.log(u * (1 - 1e-12) + 1e-300))
+        out["chain_tok"] = torch.argmax(vals.double() + g, dim=2).to(torch.int32).cpu().numpy()
+        out["drf"] = drf
+        del u, g, vals
+    else:
+        out["chain_tok"] = np.zeros((B, 0), dtype=np.int32)
+        out["drf"] = None
     return out
 
 

@@ -98,6 +98,50 @@ def test_accept_probs_bit_exact(mode, V, B, W, Dmax, K, policy):
     assert ref["acc_len"].max() > 0          # the boost produced accepted runs
 
 
+@pytest.mark.parametrize("rows_kernel", ["stream", "ldg"])
+@pytest.mark.parametrize("early", [True, False])
+@pytest.mark.parametrize("V,B,W,Dmax,K,policy,kind", [(1000, 40, 4, 20, 5, 2, "probs_f32"),
+                                                       (128256, 3, 4, 20, 5, 1, "probs_f32"),
+                                                       (151936, 4, 4, 20, 5, 1, "logits_bf16")])
+def test_accept_row_pass_kernels(rows_kernel, early, V, B, W, Dmax, K, policy, kind, monkeypatch):
+    """The row pass fed by bulk copies into shared memory (rows 16-byte aligned with a whole
+    number of 16-byte units) and the register-fed one give the same statistics: every
+    decision and p of every needed row identical, bit-exact against the oracle where
+    probabilities are given."""
+    if rows_kernel == "stream":
+        monkeypatch.setenv("SSD_ROWS_KERNEL", "stream")
+    else:
+        monkeypatch.delenv("SSD_ROWS_KERNEL", raising=False)
+    rng = np.random.default_rng(V + B + 5)
+    blk_tok, blk_len = _blocks(rng, B, W, Dmax, K, V, policy)
+    NB = blk_tok.shape[1]
+    if kind == "probs_f32":
+        tgt = _boost_probs(_rows_probs(rng, (B, 1 + NB * Dmax, V)), blk_tok, blk_len, Dmax, rng)
+        drf = _rows_probs(rng, (B, K, V))
+    else:
+        lg = (rng.standard_normal((B, 1 + NB * Dmax, V)) * np.sqrt(3)).astype(np.float32)
+        tgt = WL.f32_to_bf16_bits(lg)
+        drf = WL.f32_to_bf16_bits((rng.standard_normal((B, K, V)) * np.sqrt(3)).astype(np.float32))
+    for b in range(B):
+        for d in range(blk_len[b, W]):
+            q = drf[b, d] if kind == "probs_f32" else np.exp(WL.bf16_bits_to_f32(drf[b, d]) - 10)
+            blk_tok[b, W, d] = int(np.argmax(q * rng.random(V)))
+    u_acc = WL.uniforms24(rng, (B, NB, Dmax))
+    u_fin = WL.uniforms24(rng, (B,))
+    got = _gpu_accept("sample", kind, tgt, drf, blk_tok, blk_len, K, W, u_acc, u_fin, probs=True, early=early)
+    ref = _oracle("sample", kind, tgt, drf, blk_tok, blk_len, W, policy, u_acc, u_fin)
+    if kind == "probs_f32":
+        _assert_same(got, ref)
+    else:
+        for b in range(B):
+            rows = [0] + [1 + k * Dmax + d for k in range(NB) for d in range(int(blk_len[b, k]))]
+            np.testing.assert_allclose(got["probs"][b, rows], O.softmax_f64(O.row_values(tgt[b, rows], kind)),
+                                       rtol=1e-5, atol=1e-30)
+            same = all(np.array_equal(got[k][b], ref[k][b]) for k in ("acc_len", "best_blk", "n_out", "out_tok"))
+            if not same:
+                assert _margins_explain(kind, tgt, drf, blk_tok, blk_len, W, policy, u_acc, u_fin, got, ref, b)
+
+
 @pytest.mark.parametrize("mode", ["sample", "greedy"])
 @pytest.mark.parametrize("V,B,W,Dmax,K,policy", [(17, 64, 3, 6, 4, 1), (4099, 16, 8, 16, 7, 1),
                                                   (128256, 3, 4, 20, 0, 0)])
