@@ -55,9 +55,13 @@ def parse_args(argv=None):
     ap.add_argument("--two-streams", action="store_true",
                     help="run attention on a second stream beside the acceptance chain (default: one stream, "
                          "acceptance first, attention overlapping the finish kernel)")
-    ap.add_argument("--order", choices=["rows_first", "attn_first"], default="rows_first",
-                    help="one-stream kernel order: rows_first = retrieval, row pass, finish, attention; "
-                         "attn_first = retrieval, attention, row pass (early mode) beside it, finish")
+    ap.add_argument("--order", choices=["rows_first", "attn_first", "split"], default="rows_first",
+                    help="kernel order: rows_first = retrieval, row pass, finish, attention (one stream); "
+                         "attn_first = retrieval, attention, row pass (early mode) beside it, finish (one "
+                         "stream); split = the attention (every row) on a second stream on --attn-ctas SMs "
+                         "beside retrieval, row pass (--rows-ctas SMs) and finish")
+    ap.add_argument("--attn-ctas", type=int, default=0, help="split order: SMs for the attention (0: all)")
+    ap.add_argument("--rows-ctas", type=int, default=0, help="split order: SMs for the row pass (0: all)")
     ap.add_argument("--early-rows", choices=["auto", "on", "off"], default="auto",
                     help="row pass in its early mode (it streams every row while the retrieval runs and "
                          "lets the finish kernel launch once the retrieval is done); auto: on unless the "
@@ -498,9 +502,10 @@ def run_ours(args):
     early = args.early_rows == "on" or (args.early_rows == "auto" and default_early_rows(wl))
 
     # rotating copies: total bytes above twice the L2
-    probe = VerifyStep(wl, inp, device=dev, order=args.order, early_rows=early)
+    kw = dict(order=args.order, early_rows=early, attn_ctas=args.attn_ctas, rows_ctas=args.rows_ctas)
+    probe = VerifyStep(wl, inp, device=dev, **kw)
     main = torch.cuda.Stream(dev)
-    aux = torch.cuda.Stream(dev) if args.two_streams else None
+    aux = torch.cuda.Stream(dev) if (args.two_streams or args.order == "split") else None
     with torch.cuda.stream(main):
         probe.run(main, aux)
     torch.cuda.synchronize()
@@ -508,8 +513,7 @@ def run_ours(args):
     prefix = inp["prefix_len"]
     ab = WL.algorithmic_bytes(wl, prefix, blk_len)
     R = max(3, min(16, math.ceil(2 * L2_BYTES / max(ab["total"], 1)) + 1))
-    steps = [probe] + [VerifyStep(wl, inp, device=dev, order=args.order, early_rows=early)
-                       for _ in range(R - 1)]
+    steps = [probe] + [VerifyStep(wl, inp, device=dev, **kw) for _ in range(R - 1)]
     tokens = ab["tokens"]
     K = args.steps
     timer = StepTimer(steps, main, aux, world, dev)
@@ -577,6 +581,7 @@ def run_ours(args):
                               f"barrier, a synchronize and CUDA events); value and ms_per_step from the median",
                     "parallelism": f"replicas x{world} (independent batches per GPU)",
                     "step_order": "two streams" if args.two_streams else args.order,
+                    "attn_ctas": args.attn_ctas, "rows_ctas": args.rows_ctas,
                     "early_rows": early}),
                 "ms_per_step_repeats": [m / K for m in ms_list],
                 "ms_per_step_spread": [min(ms_list) / K, max(ms_list) / K],
@@ -1016,8 +1021,9 @@ def run_e2e(args, wl, inp, st, main, aux, dev, world=1):
     from speculative_decoding_copy_gb300.step import VerifyStep, arena_bytes
 
     nbytes = arena_bytes(inp, True)
-    slots = [VerifyStep(wl, inp, device=dev, order=st.order, early_rows=st.early_rows,
-                        arena=torch.empty(nbytes, dtype=torch.uint8, device=dev)) for _ in range(2)]
+    slots = [VerifyStep(wl, inp, device=dev, order=st.order, early_rows=st.early_rows, attn_ctas=st.attn_ctas,
+                        rows_ctas=st.rows_ctas, arena=torch.empty(nbytes, dtype=torch.uint8, device=dev))
+             for _ in range(2)]
     bufs = {"arena": slots[0].arena}
     for j, s in enumerate(slots):
         bufs[f"out_tok{j}"] = s.acc_out["out_tok"]

@@ -206,6 +206,14 @@ int ssd_gate_retrieve(const int32_t* ctx, int64_t ctx_stride, const int32_t* ctx
  * longer overlaps the tail of that preceding kernel, so it pays off only when
  * many candidate slots are empty. 0: every tile is computed, blk_len is read
  * only before the merge.
+ * all_rows (0 or 1): 1 writes the row of every slot t, present or not, as the
+ * attention of its q over the prefix and the slots k*Dmax .. t of its block
+ * (what the row of a present token holds), and never reads blk_len (it may be
+ * NULL), so the call depends on no earlier kernel's output and may run on
+ * another stream beside the retrieval. Requires skip_absent == 0.
+ * max_ctas (>= 0): 0 lets the call use the whole GPU; n > 0 sizes the
+ * tensor-core grid to at most max(n, clusters of one CTA) CTAs, one per SM, so
+ * that a kernel on another stream can hold the remaining SMs at the same time.
  * Workspace: ssd_verify_attn_workspace_size(a) bytes, 256-byte aligned; its
  * contents need no initialisation. Device-side errors are recorded in it.
  */
@@ -227,6 +235,8 @@ typedef struct {
   int pages_per_seq;
   int64_t num_pages;
   int skip_absent;
+  int all_rows;
+  int max_ctas;
 } ssd_attn_args;
 
 size_t ssd_verify_attn_workspace_size(const ssd_attn_args* a);
@@ -276,6 +286,9 @@ int ssd_verify_attn(const ssd_attn_args* a, void* ws, size_t ws_bytes, void* str
  *     and blk_len may come from that kernel. In both modes the workspace is
  *     written only after the kernel before the call on the stream has
  *     completed, so consecutive calls on one stream may share a workspace.
+ *   max_ctas (>= 0): 0 sizes the row pass to the whole GPU; n > 0 runs it as at
+ *     most n CTAs of one SM each, so that a kernel on another stream can hold
+ *     the remaining SMs at the same time.
  * 2 <= V < 2^31; NB*Dmax < 4096;
  * Dmax <= 256; 0 <= chain_blk < NB or chain_blk == -1.
  * Workspace: ssd_accept_workspace_size(a) bytes, 256-byte aligned; its
@@ -300,6 +313,7 @@ typedef struct {
   int32_t* out_tok;
   float* probs_out;
   int early_rows;
+  int max_ctas;
 } ssd_accept_args;
 
 size_t ssd_accept_workspace_size(const ssd_accept_args* a);

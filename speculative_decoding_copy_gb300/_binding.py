@@ -45,7 +45,7 @@ class AttnArgs(ctypes.Structure):
                 ("dtype", c_int), ("B", c_int), ("NB", c_int), ("Dmax", c_int), ("Hq", c_int), ("Hkv", c_int),
                 ("dh", c_int), ("P_max", c_int64), ("scale", c_float), ("out_dtype", c_int),
                 ("block_table", c_void_p), ("pages_per_seq", c_int), ("num_pages", c_int64),
-                ("skip_absent", c_int)]
+                ("skip_absent", c_int), ("all_rows", c_int), ("max_ctas", c_int)]
 
 
 class CommitArgs(ctypes.Structure):
@@ -65,7 +65,7 @@ class AcceptArgs(ctypes.Structure):
                 ("blk_tok", c_void_p), ("blk_len", c_void_p), ("B", c_int), ("NB", c_int), ("Dmax", c_int),
                 ("K", c_int), ("chain_blk", c_int), ("u_acc", c_void_p), ("u_fin", c_void_p),
                 ("acc_len", c_void_p), ("best_blk", c_void_p), ("n_out", c_void_p), ("out_tok", c_void_p),
-                ("probs_out", c_void_p), ("early_rows", c_int)]
+                ("probs_out", c_void_p), ("early_rows", c_int), ("max_ctas", c_int)]
 
 
 _lib = None
@@ -239,21 +239,21 @@ def ssd_gate_retrieve(ctx, ctx_len, h, w, tau, kappa, W, D, K, chain_policy, cha
 
 
 def attn_args(q, k_cache, v_cache, k_cand, v_cand, prefix_len, blk_len, Dmax, out, scale=0.0,
-              block_table=None, skip_absent=False) -> AttnArgs:
+              block_table=None, skip_absent=False, all_rows=False, max_ctas=0, NB=None) -> AttnArgs:
     """k_cache/v_cache: [B][Hkv][P_max][dh], or with block_table [B][pages_per_seq] pages of 128
-    tokens [num_pages][Hkv][128][dh]."""
+    tokens [num_pages][Hkv][128][dh]. blk_len may be None with all_rows (NB then given)."""
     B, NT, Hq, dh = q.shape
     Hkv = k_cache.shape[1]
-    NB = blk_len.shape[1]
+    NB = blk_len.shape[1] if blk_len is not None else (NB if NB is not None else NT // int(Dmax))
+    tail = (int(bool(skip_absent)), int(bool(all_rows)), int(max_ctas))
     if block_table is None:
         return AttnArgs(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_cand), _ptr(v_cand), _ptr(out),
                         _ptr(prefix_len), _ptr(blk_len), _elem_type(q), B, NB, int(Dmax), Hq, Hkv, dh,
-                        k_cache.shape[2], float(scale), _elem_type(out), None, 0, 0, int(bool(skip_absent)))
+                        k_cache.shape[2], float(scale), _elem_type(out), None, 0, 0, *tail)
     pps = block_table.shape[1]
     return AttnArgs(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_cand), _ptr(v_cand), _ptr(out),
                     _ptr(prefix_len), _ptr(blk_len), _elem_type(q), B, NB, int(Dmax), Hq, Hkv, dh,
-                    128 * pps, float(scale), _elem_type(out), _ptr(block_table), pps, k_cache.shape[0],
-                    int(bool(skip_absent)))
+                    128 * pps, float(scale), _elem_type(out), _ptr(block_table), pps, k_cache.shape[0], *tail)
 
 
 def ssd_verify_attn_workspace_size(args: AttnArgs) -> int:
@@ -261,23 +261,26 @@ def ssd_verify_attn_workspace_size(args: AttnArgs) -> int:
 
 
 def ssd_verify_attn(q, k_cache, v_cache, k_cand, v_cand, prefix_len, blk_len, Dmax, *, out=None, ws=None,
-                    scale=0.0, stream=None, out_f32=False, block_table=None, skip_absent=False):
+                    scale=0.0, stream=None, out_f32=False, block_table=None, skip_absent=False, all_rows=False,
+                    max_ctas=0, NB=None):
     """Block-triangular verification attention; returns the output tensor [B][NT][Hq][dh]
     (the inputs' dtype, or fp32 with out_f32). With block_table [B][pages_per_seq] int32 the
-    caches are pages of 128 tokens [num_pages][Hkv][128][dh]."""
+    caches are pages of 128 tokens [num_pages][Hkv][128][dh]. all_rows: every slot's row is
+    written and blk_len is not read (it may be None, NB then given)."""
     types = (torch.float32,) + _HALF
     for n, t in [("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("k_cand", k_cand), ("v_cand", v_cand)]:
         _need(t, n, types, 4)
         if _elem_type(t) != _elem_type(q):
             raise ValueError("all attention tensors must share one dtype")
     _need(prefix_len, "prefix_len", (torch.int32,), 1)
-    _need(blk_len, "blk_len", (torch.int32,), 2)
+    if blk_len is not None or not all_rows:
+        _need(blk_len, "blk_len", (torch.int32,), 2)
     if out is None:
         out = torch.empty(q.shape, dtype=torch.float32, device=q.device) if out_f32 else torch.empty_like(q)
     if block_table is not None:
         _need(block_table, "block_table", (torch.int32,), 2)
     args = attn_args(q, k_cache, v_cache, k_cand, v_cand, prefix_len, blk_len, Dmax, out, scale, block_table,
-                     skip_absent)
+                     skip_absent, all_rows, max_ctas, NB)
     need = ssd_verify_attn_workspace_size(args)
     if ws is None:
         ws = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
@@ -287,13 +290,13 @@ def ssd_verify_attn(q, k_cache, v_cache, k_cand, v_cand, prefix_len, blk_len, Dm
 
 
 def accept_args(mode, kind, tgt, drf, blk_tok, blk_len, K, chain_blk, u_acc, u_fin, outs, probs_out=None,
-                early_rows=False):
+                early_rows=False, max_ctas=0):
     B, NR, V = tgt.shape
     _, NB, Dmax = blk_tok.shape
     return AcceptArgs(int(mode), int(kind), _ptr(tgt), _ptr(drf), V, _ptr(blk_tok), _ptr(blk_len), B, NB, Dmax,
                       int(K), int(chain_blk), _ptr(u_acc), _ptr(u_fin), _ptr(outs["acc_len"]),
                       _ptr(outs["best_blk"]), _ptr(outs["n_out"]), _ptr(outs["out_tok"]), _ptr(probs_out),
-                      int(bool(early_rows)))
+                      int(bool(early_rows)), int(max_ctas))
 
 
 def ssd_accept_workspace_size(args: AcceptArgs) -> int:
@@ -306,7 +309,7 @@ def alloc_accept_outputs(B, NB, Dmax, device):
 
 
 def ssd_accept(tgt, drf, blk_tok, blk_len, u_acc, u_fin, *, mode, kind, K=0, chain_blk=-1, out=None, ws=None,
-               probs_out=None, stream=None, early_rows=False):
+               probs_out=None, stream=None, early_rows=False, max_ctas=0):
     """Acceptance, choice of block and final token; returns dict(acc_len, best_blk, n_out, out_tok).
     early_rows: the row pass reads every row without first waiting for the kernel before it."""
     _need(tgt, "tgt", (torch.float32,) + _HALF, 3)
@@ -318,7 +321,7 @@ def ssd_accept(tgt, drf, blk_tok, blk_len, u_acc, u_fin, *, mode, kind, K=0, cha
     _, NB, Dmax = blk_tok.shape
     outs = out or alloc_accept_outputs(B, NB, Dmax, tgt.device)
     args = accept_args(mode, kind, tgt, drf, blk_tok, blk_len, K, chain_blk, u_acc, u_fin, outs, probs_out,
-                       early_rows)
+                       early_rows, max_ctas)
     need = ssd_accept_workspace_size(args)
     if ws is None:
         ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=tgt.device)

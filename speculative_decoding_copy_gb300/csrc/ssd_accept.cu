@@ -28,9 +28,12 @@
 //   k_probs_out     optional diagnostic copy of p for every needed row.
 #include <math.h>
 
+#include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "ssd_accept.cuh"
+#include "ssd_tc.cuh"
 
 namespace ssd {
 
@@ -121,8 +124,6 @@ __device__ __forceinline__ long long block_excl_scan(long long v, long long* war
 // some token needs (8 KB of fp32 or 4 KB of bf16: 16 or 8 16-byte loads per
 // lane, all in flight together) and reduces each piece alone with warp
 // shuffles; two CTAs of 8 warps per SM keep up to 128 KB of loads in flight per SM.
-constexpr int kStatsWarps = 8;
-constexpr int kStatsThreads = 32 * kStatsWarps;
 constexpr int kPieceElems = 2048;
 template <bool BF16>
 struct Piece {
@@ -137,6 +138,10 @@ __device__ __forceinline__ float vec_elem(const uint4& u, int e) {
   if (BF16) return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
   return __uint_as_float(w);
 }
+
+template <bool BF16, bool AMAX, bool FULL, typename Consumed>
+__device__ __forceinline__ RowStat reduce_vecs(const uint4 (&v)[Piece<BF16>::kVec], int n, int e0, int probs,
+                                               Consumed consumed);
 
 // One warp's statistics of the piece of n elements starting at element e0 of `row`:
 // max, sum of 2^((x - max) log2 e) (not for probabilities) and, with AMAX, the argmax
@@ -177,6 +182,19 @@ __device__ __forceinline__ RowStat reduce_piece(const void* row, int n, int e0, 
       v[j] = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
+  return reduce_vecs<BF16, AMAX, FULL>(v, n, e0, probs, nullptr);
+}
+
+// The reduction of reduce_piece on a piece already in registers: lane's vector j holds
+// elements [e0 + (j*32 + lane)*EPV, +EPV), those at or past n count as -inf. `consumed`
+// (optional) is called once every vector has been used (the max pass reads them all),
+// after which the registers alone carry the piece.
+template <bool BF16, bool AMAX, bool FULL, typename Consumed>
+__device__ __forceinline__ RowStat reduce_vecs(const uint4 (&v)[Piece<BF16>::kVec], int n, int e0, int probs,
+                                               Consumed consumed) {
+  constexpr int EPV = Piece<BF16>::kEPV;
+  constexpr int kPieceVec = Piece<BF16>::kVec;
+  const int lane = threadIdx.x & 31;
   float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
   float av = -INFINITY;
   int ai = 0x7fffffff;
@@ -197,6 +215,7 @@ __device__ __forceinline__ RowStat reduce_piece(const void* row, int n, int e0, 
     }
   }
   float M = AMAX ? av : fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+  if constexpr (!std::is_same<Consumed, decltype(nullptr)>::value) consumed(M);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
@@ -234,8 +253,10 @@ __device__ __forceinline__ int next_task(const AcceptParams& p, int t, int step,
 }
 
 // Every warp of the grid takes the tasks gw, gw + (warps in the grid), ...
-template <bool BF16, bool AMAX>
-__global__ void __launch_bounds__(kStatsThreads, 2)
+// WARPS = 8: two CTAs per SM (the whole-GPU grid); WARPS = 16: one CTA per SM (a grid
+// capped to part of the GPU, so that every CTA holds an SM of its own)
+template <bool BF16, bool AMAX, int WARPS>
+__global__ void __launch_bounds__(32 * WARPS, 16 / WARPS)
 k_vocab_stats(AcceptParams p) {
   // blk_len comes from the retrieval; once it is in, the next kernel of the stream may
   // start (its prologue reads the retrieval's outputs, never this kernel's). The early
@@ -252,8 +273,8 @@ k_vocab_stats(AcceptParams p) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int es = BF16 ? 2 : 4;
   const int lane = threadIdx.x & 31;
-  const int gw = blockIdx.x * kStatsWarps + (threadIdx.x >> 5);
-  const int TW = gridDim.x * kStatsWarps;
+  const int gw = blockIdx.x * WARPS + (threadIdx.x >> 5);
+  const int TW = gridDim.x * WARPS;
   const int ntask = p.nch * p.NRD * p.B;
   const int per = kPieceElems;
   const bool vec_rows = ((p.V * es) & 15) == 0;
@@ -293,37 +314,211 @@ k_vocab_stats(AcceptParams p) {
   }
 }
 
+// ------------------------------------------------------------------ stats, copy-engine fed
+// k_vocab_stream: the same statistics with the pieces brought into shared memory by
+// bulk copies (the copy engine), so that each SM keeps a whole ring of pieces in flight
+// from one thread instead of from its warps' registers. One CTA per SM; CTA c takes the
+// contiguous range [c T / C, (c+1) T / C) of the T tasks (those some token needs) in
+// order. A ring stage holds the next kStreamSlots pieces of the range (32 KB of fp32 or
+// bf16 entries), fetched by one bulk copy per run of pieces that are consecutive in
+// memory and in the stage (copies of 4 KB or 8 KB move data at about two thirds of the
+// rate of 32 KB ones); piece j of the range goes to slot j % kStreamSlots of stage
+// (j / kStreamSlots) % kStreamStages and to consumer warp j % kStreamWarps. Rows must
+// start on 16-byte boundaries and hold a multiple of 16 bytes (the host checks; other
+// rows take k_vocab_stats).
+constexpr int kStreamWarps = 8;
+constexpr int kStreamThreads = 32 * (kStreamWarps + 1);    // + one producer warp
+constexpr int kStreamStage = 32768;
+constexpr int kStreamStages = 6;
+struct StreamBars {
+  uint64_t full[kStreamStages], empty[kStreamStages];
+  int failed;
+  int issued;
+};
+constexpr size_t kStreamSmem = 128 + static_cast<size_t>(kStreamStages) * kStreamStage + sizeof(StreamBars);
+constexpr unsigned long long kStreamWaitClocks = 1ull << 32;
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(tc::smem_u32(bar))
+               : "memory");
+}
+
+// the first task at or after t (below t1) that some token needs, or t1
+__device__ __forceinline__ int next_task_in(const AcceptParams& p, int t, int t1) {
+  if (p.early) return t < t1 ? t : t1;
+  for (; t < t1; ++t) {
+    const int br = t / p.nch;
+    const int b = br / p.NRD, r = br - b * p.NRD;
+    if (row_needed(p, b, r)) break;
+  }
+  return t;
+}
+
+template <bool BF16, bool AMAX>
+__global__ void __launch_bounds__(kStreamThreads, 1)
+k_vocab_stream(AcceptParams p) {
+  constexpr int es = BF16 ? 2 : 4;
+  constexpr int kPieceBytes = kPieceElems * es;
+  constexpr int kSlots = kStreamStage / kPieceBytes;       // 4 fp32 or 8 bf16 pieces per stage
+  extern __shared__ uint8_t sraw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sraw) + 127) & ~uintptr_t(127));
+  StreamBars& sb = *reinterpret_cast<StreamBars*>(ring + kStreamStages * kStreamStage);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int i = 0; i < kStreamStages; ++i) {
+      tc::mbar_init(&sb.full[i], 1);
+      tc::mbar_init(&sb.empty[i], kSlots);
+    }
+    sb.failed = 0;
+    sb.issued = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  // the dependency rules of k_vocab_stats: in the early mode only the last CTA waits
+  // first, and nothing is written to the workspace before griddepcontrol.wait
+  bool waited = !p.early || blockIdx.x == gridDim.x - 1;
+  if (waited) asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const long long C = gridDim.x;
+  const long long ntask = static_cast<long long>(p.nch) * p.NRD * p.B;
+  const int t0 = static_cast<int>(blockIdx.x * ntask / C), t1 = static_cast<int>((blockIdx.x + 1) * ntask / C);
+  if (warp == kStreamWarps) {
+    // producer: a stage per kSlots pieces, one bulk copy per run of consecutive pieces
+    if (lane == 0) {
+      int j = 0, st = 0;                        // pieces issued, stages issued
+      int t = next_task_in(p, t0, t1);
+      while (t < t1) {
+        const int s = st % kStreamStages;
+        if (st >= kStreamStages &&
+            !mbar_wait_bounded(&sb.empty[s], ((st / kStreamStages) - 1) & 1, &sb.failed, p.hdr, 110,
+                               kStreamWaitClocks))
+          break;
+        // the stage's pieces and their runs
+        const char* run_src = nullptr;
+        uint32_t run_dst = 0, run_bytes = 0, stage_bytes = 0;
+        const uint32_t base = tc::smem_u32(ring + s * kStreamStage);
+        int k = 0;
+        // expect_tx first would need the byte count: count the stage's bytes in a first walk
+        {
+          int tt = t;
+          for (int kk = 0; kk < kSlots && tt < t1; ++kk, tt = next_task_in(p, tt + 1, t1)) {
+            const int c = tt % p.nch;
+            stage_bytes += static_cast<uint32_t>(min(static_cast<int64_t>(kPieceElems), p.V - c * kPieceElems) * es);
+          }
+        }
+        tc::mbar_expect_tx(&sb.full[s], stage_bytes);
+        for (; k < kSlots && t < t1; ++k, ++j, t = next_task_in(p, t + 1, t1)) {
+          const int br = t / p.nch, c = t - br * p.nch;
+          const int b = br / p.NRD, r = br - b * p.NRD;
+          const char* src = static_cast<const char*>(row_ptr(p, b, r)) + static_cast<int64_t>(c) * kPieceBytes;
+          const uint32_t n = static_cast<uint32_t>(min(static_cast<int64_t>(kPieceElems), p.V - c * kPieceElems) * es);
+          const uint32_t dst = base + k * kPieceBytes;
+          if (run_bytes > 0 && src == run_src + run_bytes && dst == run_dst + run_bytes &&
+              run_bytes % kPieceBytes == 0) {
+            run_bytes += n;                    // extends the run (every piece before it was whole)
+          } else {
+            if (run_bytes > 0) bulk_g2s(run_dst, run_src, run_bytes, &sb.full[s]);
+            run_src = src;
+            run_dst = dst;
+            run_bytes = n;
+          }
+        }
+        if (run_bytes > 0) bulk_g2s(run_dst, run_src, run_bytes, &sb.full[s]);
+        ++st;
+      }
+      sb.issued = st;
+    }
+  } else {
+    RowStat held{};
+    int64_t held_at = -1;
+    int nheld = 0;
+    int j = 0;
+    for (int t = next_task_in(p, t0, t1); t < t1; t = next_task_in(p, t + 1, t1), ++j) {
+      if (j % kStreamWarps != warp) continue;
+      const int st = j / kSlots, s = st % kStreamStages, k = j % kSlots;
+      if (!mbar_wait_bounded(&sb.full[s], (st / kStreamStages) & 1, &sb.failed, p.hdr, 111, kStreamWaitClocks)) break;
+      const int br = t / p.nch, c = t - br * p.nch;
+      const int e0 = c * kPieceElems;
+      const int n = static_cast<int>(min(static_cast<int64_t>(kPieceElems), p.V - e0));
+      constexpr int kPieceVec = Piece<BF16>::kVec;
+      const uint32_t src = tc::smem_u32(ring + s * kStreamStage + k * kPieceBytes) + lane * 16;
+      uint4 v[kPieceVec];
+#pragma unroll
+      for (int q = 0; q < kPieceVec; ++q)
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v[q].x), "=r"(v[q].y), "=r"(v[q].z), "=r"(v[q].w)
+                     : "r"(src + q * 512));
+      // the slot is released once the max pass has used every loaded vector
+      auto release = [&](float) {
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&sb.empty[s]);
+      };
+      const RowStat r = n == kPieceElems ? reduce_vecs<BF16, AMAX, true>(v, n, e0, p.probs, release)
+                                         : reduce_vecs<BF16, AMAX, false>(v, n, e0, p.probs, release);
+      const int64_t at = static_cast<int64_t>(br) * p.nch + c;
+      if (!waited && nheld < 32) {
+        if (lane == nheld) {
+          held = r;
+          held_at = at;
+        }
+        ++nheld;
+        continue;
+      }
+      if (!waited) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        waited = true;
+        if (held_at >= 0) p.part[held_at] = held;
+        held_at = -1;
+      }
+      if (lane == 0) p.part[at] = r;
+    }
+    if (!waited && nheld > 0) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      if (held_at >= 0) p.part[held_at] = held;
+    }
+  }
+  __syncthreads();
+  if (tid == 0 && sb.failed) {
+    // a wait gave up: let the copies still in flight land before the CTA exits (the
+    // last kStreamStages issued stages are distinct)
+    for (int q = max(0, sb.issued - kStreamStages); q < sb.issued; ++q) {
+      const unsigned long long c0 = clock64();
+      while (!mbar_probe(&sb.full[q % kStreamStages], (q / kStreamStages) & 1) && clock64() - c0 < kStreamWaitClocks) {
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ finish
-// k_accept_finish: one cluster of kFinCTAs CTAs per sequence does the rest of the
-// step after the row pass: merging every needed row's piece statistics (all
-// warps of the cluster, one row per warp), the acceptance tests and the choice
-// of block (cluster rank 0), and in sample mode the final draw from the stop
-// row (every CTA sums the integer weights of its chunks; the sums go to every
-// CTA through distributed shared memory; the CTA holding the threshold finds
-// the index). What needs only the retrieval's outputs and the inputs (token
-// slots, their logits and uniforms) is loaded before griddepcontrol.wait, while
-// the row pass still runs.
-constexpr int kFinCTAs = 8;                 // cluster size when the stop row has at most 256 chunks
-constexpr int kMaxFinCTAs = 16;             // ... and up to 512 chunks (a non-portable cluster size)
-constexpr int kFinThreads = 1024;
+// k_accept_finish_batch: one cluster of C CTAs (C = 1, 2 or 4; chosen so that the
+// clusters of the whole batch fit on the GPU at once) per sequence does the rest
+// of the step after the row pass: merging every needed row's piece statistics
+// (every CTA, one row per warp), the acceptance tests and the choice of block
+// (each CTA takes the same decisions from the same data; rank 0 writes them), and
+// in sample mode the final draw from the stop row: CTA r owns a contiguous range
+// of 512-entry chunks, its warps loop over them summing the exact integer weights
+// per chunk, the CTA totals go to every rank through distributed shared memory,
+// and the CTA holding the threshold finds the chunk, then the lane, then the
+// entry. What needs only the retrieval's outputs and the inputs (token slots,
+// their logits and uniforms) is loaded before griddepcontrol.wait, while the row
+// pass still runs.
+constexpr int kFinThreads = 512;
 constexpr int kFinWarps = kFinThreads / 32;
 constexpr int kSlotsPer = kMaxSlots / kFinThreads;
-constexpr int kMaxSampleChunks = kMaxFinCTAs * kFinWarps;   // one chunk per warp of the cluster
+constexpr int kMaxSampleChunks = 512;       // chunks of a stop row (V <= 262144)
 constexpr int kLaneEntries = kSampleChunk / 32;             // contiguous entries per lane per chunk
 constexpr int kChunkVec = kLaneEntries / 4;                  // float4 per lane per chunk
-constexpr size_t kFinDynSmem = 2ull * kFinWarps * kSampleChunk * sizeof(float);
 
 struct __align__(16) FinishSmem {
-  RowStat st[kMaxRows];                     // merged rows (rank 0 receives them)
-  long long wsum[kFinWarps][2];             // residual and bonus weight sums of this CTA's chunks
-  long long lsum[kFinWarps][32][2];         // ... of every lane's entries
-  long long ctasum[kMaxFinCTAs][2];         // ... of every rank's chunks
-  StopInfo si;                              // the stop row (rank 0 sends it to every rank)
-  int tok_s[kMaxSlots];                     // candidate tokens (rank 0)
+  RowStat st[kMaxRows];                     // merged rows
+  long long csum[kMaxSampleChunks][2];      // residual and bonus weight sums of this CTA's chunks
+  long long ctasum[4][2];                   // ... of every rank's chunks (clusters of up to 4)
+  StopInfo si;                              // the stop row
+  int tok_s[kMaxSlots];                     // candidate tokens
   int len_s[256];
   int acc_s[256];
   unsigned char ok_s[kMaxSlots];
-  long long red_w[kFinWarps], red_p[kFinWarps];
   int sel[4];
   int c_star, use_bonus;
   long long t_rem;
@@ -473,9 +668,8 @@ __device__ __forceinline__ void load_lane_run(const AcceptParams& p, const void*
 }
 
 __global__ void __launch_bounds__(kFinThreads, 1)
-k_accept_finish(AcceptParams p) {
+k_accept_finish_batch(AcceptParams p) {
   __shared__ FinishSmem sm;
-  extern __shared__ float4 fin_chunk[];             // [2][kFinWarps][kSampleChunk] fp32 chunks of p and q
   const uint32_t rank = cl_rank();
   const int C = static_cast<int>(gridDim.x);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -483,7 +677,7 @@ k_accept_finish(AcceptParams p) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (int b = blockIdx.y; b < p.B; b += gridDim.y) {
     // this CTA has started this sequence (its peers wait for that before writing to it)
-    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+    if (C > 1) asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
     // ---- 1. per token slot: token, block length, uniform and the logits the test needs;
     //         none of it comes from the row pass, so it is loaded before griddepcontrol.wait.
     //         Every CTA of the cluster takes the same decisions from the same data.
@@ -638,6 +832,418 @@ k_accept_finish(AcceptParams p) {
       }
     }
     if (!p.sample) {
+      if (C > 1) asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+      __syncthreads();                    // shared state is reused by the next sequence
+      continue;
+    }
+
+    // ---- 4. the bonus weights P and residual weights W of every chunk of this CTA's
+    //         range [c0, c1): warp w takes chunks c0 + w, c0 + w + 32, ...; lane l sums
+    //         entries [16 l, 16 l + 16) of a chunk
+    const StopInfo si = sm.si;
+    const void* prow = row_ptr(p, b, si.row);
+    const bool has_q = si.drf_row >= 0;
+    const void* qrow = has_q ? row_ptr(p, b, p.NR + si.drf_row) : prow;
+    const DrawRow pr = draw_row(si.ps, p.probs), qr = draw_row(si.qs, p.probs);
+    const int nper = (p.nchs + C - 1) / C;
+    const int c0 = min(p.nchs, static_cast<int>(rank) * nper), c1 = min(p.nchs, c0 + nper);
+    // this lane's weights W (residual or bonus) and P of chunk cc, summed, from its entries
+    // a (target row) and q (draft row, when there is one)
+    auto lane_load = [&](int cc, float4 (&a)[kChunkVec], float4 (&q)[kChunkVec]) {
+      const int64_t lo = static_cast<int64_t>(cc) * kSampleChunk;
+      load_lane_run(p, prow, lo, a);
+      if (has_q && !si.bonus) load_lane_run(p, qrow, lo, q);
+    };
+    auto lane_sums = [&](int cc, const float4 (&a)[kChunkVec], const float4 (&q)[kChunkVec], long long& sw,
+                         long long& sp) {
+      const int64_t l0 = static_cast<int64_t>(cc) * kSampleChunk + static_cast<int64_t>(lane) * kLaneEntries;
+      uint32_t shi = 0, slo = 0;
+#pragma unroll
+      for (int j = 0; j < kChunkVec; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const Split w = weight_split(f4(a[j], e), pr);
+          shi += w.hi;
+          slo += w.lo;
+        }
+      sp = (static_cast<long long>(shi) << 20) + static_cast<long long>(slo);
+      if (si.bonus) {
+        sw = sp;
+      } else if (has_q) {
+        sw = 0;
+#pragma unroll
+        for (int j = 0; j < kChunkVec; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const long long P = split64(weight_split(f4(a[j], e), pr));
+            const long long Q = split64(weight_split(f4(q[j], e), qr));
+            sw += P > Q ? P - Q : 0LL;
+          }
+      } else {
+        // a rejected copy token: W = P everywhere but there, where Q = 2^40
+        sw = sp;
+        const int64_t xl = static_cast<int64_t>(si.excl) - l0;
+        if (xl >= 0 && xl < kLaneEntries) {
+          float pe = 0.f;
+#pragma unroll
+          for (int j = 0; j < kChunkVec; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (4 * j + e == xl) pe = f4(a[j], e);
+          const long long Pe = split64(weight_split(pe, pr));
+          sw = sp - Pe + (Pe > kOneWeight ? Pe - kOneWeight : 0LL);
+        }
+      }
+    };
+    for (int cc = c0 + warp; cc < c1; cc += kFinWarps) {
+      long long sw, sp;
+      float4 a[kChunkVec], q[kChunkVec];
+      lane_load(cc, a, q);
+      lane_sums(cc, a, q, sw, sp);
+      sw = warp_sum(sw);
+      sp = warp_sum(sp);
+      if (lane == 0) {
+        sm.csum[cc - c0][0] = sw;
+        sm.csum[cc - c0][1] = sp;
+      }
+    }
+    __syncthreads();
+    // this CTA's totals go to every rank (after every peer has started this sequence)
+    if (C > 1) asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+    if (warp == 0) {
+      long long tw = 0, tp = 0;
+      for (int i = lane; i < c1 - c0; i += 32) {
+        tw += sm.csum[i][0];
+        tp += sm.csum[i][1];
+      }
+      tw = warp_sum(tw);
+      tp = warp_sum(tp);
+      if (C == 1) {
+        if (lane == 0) {
+          sm.ctasum[0][0] = tw;
+          sm.ctasum[0][1] = tp;
+        }
+      } else if (lane < C) {
+        const uint32_t dst = cl_map(&sm.ctasum[rank][0], static_cast<uint32_t>(lane));
+        asm volatile("st.shared::cluster.v2.b64 [%0], {%1, %2};" ::"r"(dst), "l"(tw), "l"(tp) : "memory");
+      }
+    }
+    if (C > 1) cl_sync();
+    else __syncthreads();
+
+    // ---- 5. (warp 0) S, the threshold T = floor(U S / 2^24), the CTA and then the chunk
+    //         that hold it
+    if (warp == 0) {
+      const long long cw = lane < C ? sm.ctasum[lane][0] : 0, cp = lane < C ? sm.ctasum[lane][1] : 0;
+      long long iw = cw, ip = cp;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long yw = __shfl_up_sync(0xffffffffu, iw, o);
+        const long long yp = __shfl_up_sync(0xffffffffu, ip, o);
+        if (lane >= o) {
+          iw += yw;
+          ip += yp;
+        }
+      }
+      const long long SW = __shfl_sync(0xffffffffu, iw, 31), SP = __shfl_sync(0xffffffffu, ip, 31);
+      const int ub = (si.bonus || SW == 0) ? 1 : 0;
+      const unsigned long long S = static_cast<unsigned long long>(ub ? SP : SW);
+      const float u = fminf(fmaxf(p.u_fin[b], 0.f), 0.99999994f);               // contract: u in [0, 1)
+      const unsigned long long U = static_cast<unsigned long long>(u * 16777216.0f);   // floor(u 2^24), exact
+      const long long T = static_cast<long long>((__umul64hi(U, S) << 40) | ((U * S) >> 24));
+      const long long mc = ub ? cp : cw, ec = (ub ? ip : iw) - mc;
+      const unsigned hitc = __ballot_sync(0xffffffffu, mc > 0 && ec <= T && T < ec + mc);
+      int oc = -1;
+      long long t2 = 0;
+      if (hitc != 0u && static_cast<int>(rank) == __ffs(hitc) - 1) {
+        // this CTA: the chunk, lane l scanning local chunks [16 l, 16 l + 16)
+        const long long t1 = T - __shfl_sync(0xffffffffu, ec, __ffs(hitc) - 1);
+        const int n = c1 - c0;
+        constexpr int kPerLane = kMaxSampleChunks / 32;
+        long long mine = 0;
+#pragma unroll
+        for (int k = 0; k < kPerLane; ++k) {
+          const int i = lane * kPerLane + k;
+          if (i < n) mine += sm.csum[i][ub];
+        }
+        long long incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const long long ex = incl - mine;
+        const unsigned hitl = __ballot_sync(0xffffffffu, mine > 0 && ex <= t1 && t1 < incl);
+        if (hitl != 0u && lane == __ffs(hitl) - 1) {
+          long long acc = ex;
+          for (int k = 0; k < kPerLane; ++k) {
+            const int i = lane * kPerLane + k;
+            if (i >= n) break;
+            const long long w = sm.csum[i][ub];
+            if (w > 0 && t1 < acc + w) {
+              oc = i;
+              t2 = t1 - acc;
+              break;
+            }
+            acc += w;
+          }
+        }
+        const unsigned got = __ballot_sync(0xffffffffu, oc >= 0);
+        if (got != 0u) {
+          const int src = __ffs(got) - 1;
+          oc = __shfl_sync(0xffffffffu, oc, src);
+          t2 = __shfl_sync(0xffffffffu, t2, src);
+        }
+      }
+      if (lane == 0) {
+        sm.c_star = oc;
+        sm.t_rem = t2;
+        sm.use_bonus = ub;
+      }
+    }
+    __syncthreads();
+
+    // ---- 6. (warp 0 of the CTA that holds it) the lane by one scan of the chunk's lane
+    //         sums, then that lane walks its 16 entries
+    if (warp == 0 && sm.c_star >= 0) {
+      const int ub = sm.use_bonus;
+      const long long Tr = sm.t_rem;
+      const int cc = c0 + sm.c_star;
+      long long mine;
+      {
+        long long sw, sp;
+        float4 a[kChunkVec], q[kChunkVec];
+        lane_load(cc, a, q);
+        lane_sums(cc, a, q, sw, sp);
+        mine = ub ? sp : sw;
+      }
+      long long incl = mine;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const long long ex = incl - mine;
+      const unsigned hit = __ballot_sync(0xffffffffu, mine > 0 && ex <= Tr && Tr < incl);
+      if (hit != 0u && lane == __ffs(hit) - 1) {
+        const int64_t l0 = static_cast<int64_t>(cc) * kSampleChunk + static_cast<int64_t>(lane) * kLaneEntries;
+        float4 a[kChunkVec], q[kChunkVec];
+        lane_load(cc, a, q);                  // again (cached): fewer live registers across the scan
+        // the first entry whose prefix sum exceeds the threshold (unrolled: the entries
+        // stay in registers)
+        long long acc = ex;
+        int k_hit = -1;
+#pragma unroll
+        for (int k = 0; k < kLaneEntries; ++k) {
+          acc += draw_weight(f4(a[k / 4], k % 4), pr, has_q, has_q ? f4(q[k / 4], k % 4) : 0.f, qr, si.excl, ub,
+                             l0 + k);
+          if (k_hit < 0 && acc > Tr) k_hit = k;
+        }
+        if (k_hit < 0) k_hit = kLaneEntries - 1;
+        p.out_tok[static_cast<int64_t>(b) * (p.Dmax + 1) + si.a] = static_cast<int>(l0 + k_hit);
+      }
+    }
+    __syncthreads();
+  }
+  // no peer writes to this CTA after the last cluster barrier of its sequences
+}
+
+// ------------------------------------------------------------------ finish, one warp per chunk
+// k_accept_finish_wide: for batches whose clusters of eight (or sixteen) 1024-thread CTAs
+// all fit on the GPU at once (B x 8 <= SMs): the same steps with one warp per 512-entry
+// chunk of the stop row, each warp staging its chunk in shared memory for the final walk
+// and keeping its lanes' sums there, so that the draw needs no second pass over the row.
+constexpr int kWideCTAs = 8;                 // cluster size when the stop row has at most 256 chunks
+constexpr int kWideMaxCTAs = 16;             // ... and up to 512 chunks (a non-portable cluster size)
+constexpr int kWideThreads = 1024;
+constexpr int kWideWarps = kWideThreads / 32;
+constexpr int kWideSlotsPer = kMaxSlots / kWideThreads;
+constexpr int kWideMaxChunks = kWideMaxCTAs * kWideWarps;   // one chunk per warp of the cluster
+constexpr size_t kWideDynSmem = 2ull * kWideWarps * kSampleChunk * sizeof(float);
+
+struct __align__(16) WideSmem {
+  RowStat st[kMaxRows];                     // merged rows (rank 0 receives them)
+  long long wsum[kWideWarps][2];             // residual and bonus weight sums of this CTA's chunks
+  long long lsum[kWideWarps][32][2];         // ... of every lane's entries
+  long long ctasum[kWideMaxCTAs][2];         // ... of every rank's chunks
+  StopInfo si;                              // the stop row (rank 0 sends it to every rank)
+  int tok_s[kMaxSlots];                     // candidate tokens (rank 0)
+  int len_s[256];
+  int acc_s[256];
+  unsigned char ok_s[kMaxSlots];
+  long long red_w[kWideWarps], red_p[kWideWarps];
+  int sel[4];
+  int c_star, use_bonus;
+  long long t_rem;
+};
+
+
+__global__ void __launch_bounds__(kWideThreads, 1)
+k_accept_finish_wide(AcceptParams p) {
+  __shared__ WideSmem sm;
+  extern __shared__ float4 wide_chunk[];             // [2][kWideWarps][kSampleChunk] fp32 chunks of p and q
+  const uint32_t rank = cl_rank();
+  const int C = static_cast<int>(gridDim.x);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nslots = p.NB * p.Dmax;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  for (int b = blockIdx.y; b < p.B; b += gridDim.y) {
+    // this CTA has started this sequence (its peers wait for that before writing to it)
+    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+    // ---- 1. per token slot: token, block length, uniform and the logits the test needs;
+    //         none of it comes from the row pass, so it is loaded before griddepcontrol.wait.
+    //         Every CTA of the cluster takes the same decisions from the same data.
+    int x_[kWideSlotsPer], row_[kWideSlotsPer];
+    bool live_[kWideSlotsPer];
+    float lp_[kWideSlotsPer], lq_[kWideSlotsPer], u_[kWideSlotsPer];
+#pragma unroll
+    for (int k = 0; k < kWideSlotsPer; ++k) {
+      live_[k] = false;
+      x_[k] = 0;
+      row_[k] = 0;
+      lp_[k] = 0.f;
+      lq_[k] = 0.f;
+      u_[k] = 0.f;
+      const int sl = tid + k * kWideThreads;
+      if (sl < nslots) {
+        const int blk = sl / p.Dmax, d = sl % p.Dmax;
+        sm.tok_s[sl] = p.blk_tok[static_cast<int64_t>(b) * nslots + sl];
+        const int raw = p.blk_len[b * p.NB + blk];
+        const int cap = (blk == p.chain_blk) ? min(p.Dmax, p.K) : p.Dmax;
+        const int L = min(max(raw, 0), cap);
+        if (d < L) {
+          const int x = sm.tok_s[sl];
+          if (x < 0 || x >= p.V) {
+            if (rank == 0) record_error(p.hdr, SSD_ERR_DEVICE, 100);
+          } else {
+            live_[k] = true;
+            x_[k] = x;
+            row_[k] = d == 0 ? 0 : 1 + blk * p.Dmax + d - 1;
+            if (p.sample) {
+              lp_[k] = load_val(row_ptr(p, b, row_[k]), x, p.bf16);
+              if (blk == p.chain_blk) lq_[k] = load_val(row_ptr(p, b, p.NR + d), x, p.bf16);
+              u_[k] = p.u_acc[static_cast<int64_t>(b) * nslots + sl];
+            }
+          }
+        }
+      }
+    }
+    for (int k = tid; k < p.NB; k += kWideThreads) {
+      const int raw = p.blk_len[b * p.NB + k];
+      const int cap = (k == p.chain_blk) ? min(p.Dmax, p.K) : p.Dmax;
+      const int L = min(max(raw, 0), cap);
+      if (rank == 0 && L != raw) record_error(p.hdr, SSD_ERR_DEVICE, 101);
+      sm.len_s[k] = L;
+    }
+    __syncthreads();
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // the piece statistics are complete
+
+    // ---- 2. every needed row merged from its pieces, two rows per warp pass
+    for (int r = warp; r < p.NRD; r += 2 * kWideWarps) {
+      const int r2 = r + kWideWarps;
+      const bool na = row_needed_s(p, sm.len_s, r), nb = r2 < p.NRD && row_needed_s(p, sm.len_s, r2);
+      if (!na && !nb) continue;
+      RowStat xa, xb;
+      merge_rows(p, b, na ? r : r2, (na && nb) ? r2 : -1, xa, xb);
+      if (lane == 0) {
+        const int ra = na ? r : r2;
+        sm.st[ra] = xa;
+        if (rank == 0) p.stat[static_cast<int64_t>(b) * p.NRD + ra] = xa;
+        if (na && nb) {
+          sm.st[r2] = xb;
+          if (rank == 0) p.stat[static_cast<int64_t>(b) * p.NRD + r2] = xb;
+        }
+      }
+    }
+    __syncthreads();
+
+    // ---- 3. acceptance, leading runs, longest block, stop row (outputs by rank 0)
+#pragma unroll
+    for (int k = 0; k < kWideSlotsPer; ++k) {
+      const int sl = tid + k * kWideThreads;
+      if (sl >= nslots) continue;
+      bool ok = false;
+      if (live_[k]) {
+        const int blk = sl / p.Dmax, d = sl % p.Dmax;
+        if (!p.sample) {
+          ok = (x_[k] == sm.st[row_[k]].amax_i);
+        } else {
+          const float px = prob_of(lp_[k], sm.st[row_[k]], p.probs);
+          const float qx = (blk == p.chain_blk) ? prob_of(lq_[k], sm.st[p.NR + d], p.probs) : 1.f;
+          ok = __dmul_rn(static_cast<double>(u_[k]), static_cast<double>(qx)) < static_cast<double>(px);
+        }
+      }
+      sm.ok_s[sl] = ok ? 1 : 0;
+    }
+    __syncthreads();
+    // leading accepted run of every block: one warp per block, the first rejection by ballot
+    for (int k = warp; k < p.NB; k += kWideWarps) {
+      const int L = sm.len_s[k];
+      int a = L;
+      for (int d0 = 0; d0 < L; d0 += 32) {
+        const int d = d0 + lane;
+        const unsigned rej = __ballot_sync(0xffffffffu, d < L && !sm.ok_s[k * p.Dmax + d]);
+        if (rej != 0u) {
+          a = d0 + __ffs(rej) - 1;
+          break;
+        }
+      }
+      if (lane == 0) {
+        sm.acc_s[k] = a;
+        if (rank == 0) p.acc_len[b * p.NB + k] = a;
+      }
+    }
+    __syncthreads();
+    if (tid == 0) {
+      // longest accepted run, lowest block index on ties
+      int best = -1, ba = -1;
+      for (int k = 0; k < p.NB; ++k) {
+        if (sm.len_s[k] > 0 && sm.acc_s[k] > ba) {
+          ba = sm.acc_s[k];
+          best = k;
+        }
+      }
+      const int a = best >= 0 ? ba : 0;
+      const int L = best >= 0 ? sm.len_s[best] : 0;
+      const int stop = a == 0 ? 0 : 1 + best * p.Dmax + a - 1;
+      sm.sel[0] = best;
+      sm.sel[1] = a;
+      sm.sel[3] = sm.st[stop].amax_i;
+      if (rank == 0) {
+        p.best_blk[b] = best;
+        p.n_out[b] = a + 1;
+      }
+      StopInfo si;
+      si.row = stop;
+      si.ps = sm.st[stop];
+      si.a = a;
+      si.drf_row = -1;
+      si.excl = -1;
+      si.bonus = (a >= L) ? 1 : 0;
+      si.pad[0] = si.pad[1] = si.pad[2] = 0;
+      si.qs = si.ps;
+      if (a < L) {
+        if (best == p.chain_blk) {
+          si.drf_row = a;
+          si.qs = sm.st[p.NR + a];
+        } else {
+          si.excl = sm.tok_s[best * p.Dmax + a];
+        }
+      }
+      sm.si = si;
+    }
+    __syncthreads();
+    if (rank == 0) {
+      // emitted tokens (the draw below fills the final one in sample mode)
+      const int best = sm.sel[0], a = sm.sel[1];
+      for (int i = tid; i <= p.Dmax; i += kWideThreads) {
+        int v = -1;
+        if (i < a) v = sm.tok_s[best * p.Dmax + i];
+        else if (i == a && !p.sample) v = sm.sel[3];
+        p.out_tok[static_cast<int64_t>(b) * (p.Dmax + 1) + i] = v;
+      }
+    }
+    if (!p.sample) {
       asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
       continue;
     }
@@ -650,11 +1256,11 @@ k_accept_finish(AcceptParams p) {
     const bool has_q = si.drf_row >= 0;
     const void* qrow = has_q ? row_ptr(p, b, p.NR + si.drf_row) : prow;
     const DrawRow pr = draw_row(si.ps, p.probs), qr = draw_row(si.qs, p.probs);
-    const int gw = static_cast<int>(rank) * kFinWarps + warp;
+    const int gw = static_cast<int>(rank) * kWideWarps + warp;
     const int64_t lo = static_cast<int64_t>(gw) * kSampleChunk;
     const int64_t l0 = lo + static_cast<int64_t>(lane) * kLaneEntries;   // this lane's first entry
-    float* pf = reinterpret_cast<float*>(fin_chunk + warp * (kSampleChunk / 4)) + lane * kLaneEntries;
-    float* qf = reinterpret_cast<float*>(fin_chunk + (kFinWarps + warp) * (kSampleChunk / 4)) + lane * kLaneEntries;
+    float* pf = reinterpret_cast<float*>(wide_chunk + warp * (kSampleChunk / 4)) + lane * kLaneEntries;
+    float* qf = reinterpret_cast<float*>(wide_chunk + (kWideWarps + warp) * (kSampleChunk / 4)) + lane * kLaneEntries;
     {
       long long sw = 0, sp = 0;
       if (gw < p.nchs) {
@@ -798,6 +1404,7 @@ k_accept_finish(AcceptParams p) {
   // no peer writes to this CTA after the last cluster barrier of its sequences
 }
 
+
 // ------------------------------------------------------------------ diagnostics
 __global__ void __launch_bounds__(kVocabThreads)
 k_probs_out(AcceptParams p) {
@@ -855,6 +1462,7 @@ int accept_validate(const ssd_accept_args* a) {
   if (a->chain_blk >= 0 && (a->K < 1 || a->K > a->Dmax)) return SSD_ERR_INVALID;
   if (a->mode == SSD_SAMPLE && (a->V + kSampleChunk - 1) / kSampleChunk > kMaxSampleChunks) return SSD_ERR_UNSUPPORTED;
   if (a->early_rows != 0 && a->early_rows != 1) return SSD_ERR_INVALID;
+  if (a->max_ctas < 0) return SSD_ERR_INVALID;
   if (a->B == 0) return SSD_OK;
   if (!a->tgt || !a->blk_tok || !a->blk_len || !a->acc_len || !a->best_blk || !a->n_out || !a->out_tok)
     return SSD_ERR_INVALID;
@@ -879,6 +1487,7 @@ AcceptParams accept_params(const ssd_accept_args* a, const AcceptLayout& L, char
   p.bf16 = a->kind == SSD_LOGITS_BF16;
   p.probs = a->kind == SSD_PROBS_F32;
   p.early = a->early_rows;
+  p.max_ctas = a->max_ctas;
   p.nch = L.nch; p.chunk = L.chunk; p.nchs = L.nchs; p.schunk = L.schunk;
   p.hdr = reinterpret_cast<WsHeader*>(base);
   p.part = reinterpret_cast<RowStat*>(base + L.part_off);
@@ -886,25 +1495,71 @@ AcceptParams accept_params(const ssd_accept_args* a, const AcceptLayout& L, char
   return p;
 }
 
-// the stats kernel: a grid of as many CTAs as are resident at once
+// SSD_ROWS_KERNEL=stream selects the copy-engine-fed row pass (measured slower than the
+// register-fed one on the 42 MB row pass of the Llama-3.1-8B-shaped step: 18.3 against
+// 14.3 µs per launch; kept as a tested alternative)
+static bool stream_enabled_by_env() {
+  const char* e = getenv("SSD_ROWS_KERNEL");
+  return e != nullptr && e[0] == 's';
+}
+
+// rows the copy engine can bring in: 16-byte aligned starts, whole 16-byte units
+static bool stream_rows_ok(const AcceptParams& p) {
+  const int64_t es = p.bf16 ? 2 : 4;
+  if (((p.V * es) & 15) != 0 || !aligned(p.tgt, 16)) return false;
+  return p.K == 0 || p.drf == nullptr || aligned(p.drf, 16);
+}
+
+// the copy-engine-fed stats kernel: one CTA per SM (or per task, if fewer)
 template <bool BF16, bool AMAX>
-static cudaError_t launch_stats(const AcceptParams& p, cudaStream_t s) {
+static cudaError_t launch_stream(const AcceptParams& p, cudaStream_t s) {
   static std::once_flag once[kMaxDevices];
-  static long long cap[kMaxDevices];
+  static int sms[kMaxDevices];
+  static cudaError_t err[kMaxDevices];
   const int dev = current_device();
   if (dev < 0) return cudaErrorInvalidDevice;
   std::call_once(once[dev], [dev] {
-    int sms = 152, per = 1;
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, k_vocab_stats<BF16, AMAX>, kStatsThreads, 0) !=
-        cudaSuccess)
+    sms[dev] = 0;
+    err[dev] = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (err[dev] == cudaSuccess)
+      err[dev] = cudaFuncSetAttribute(k_vocab_stream<BF16, AMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(kStreamSmem));
+  });
+  if (err[dev] != cudaSuccess) return err[dev];
+  const long long ntask = static_cast<long long>(p.nch) * p.NRD * p.B;
+  long long g = ntask < sms[dev] ? ntask : sms[dev];
+  if (p.max_ctas > 0 && g > p.max_ctas) g = p.max_ctas;
+  return launch_pdl(k_vocab_stream<BF16, AMAX>, dim3(static_cast<unsigned>(g > 0 ? g : 1)), dim3(kStreamThreads),
+                    kStreamSmem, s, p);
+}
+
+// the stats kernel: a grid of as many CTAs as are resident at once, or with max_ctas one
+// CTA of 16 warps per SM on at most max_ctas SMs
+template <bool BF16, bool AMAX>
+static cudaError_t launch_stats(const AcceptParams& p, cudaStream_t s) {
+  if (stream_rows_ok(p) && stream_enabled_by_env()) return launch_stream<BF16, AMAX>(p, s);
+  static std::once_flag once[kMaxDevices];
+  static long long cap[kMaxDevices];
+  static int sms[kMaxDevices];
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  std::call_once(once[dev], [dev] {
+    int n = 152, per = 1;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, k_vocab_stats<BF16, AMAX, 8>, 256, 0) != cudaSuccess)
       per = 1;
-    cap[dev] = static_cast<long long>(sms) * (per > 0 ? per : 1);
+    cap[dev] = static_cast<long long>(n) * (per > 0 ? per : 1);
+    sms[dev] = n;
   });
   const long long ntask = static_cast<long long>(p.nch) * p.NRD * p.B;
-  const long long want = (ntask + kStatsWarps - 1) / kStatsWarps;
+  if (p.max_ctas > 0) {
+    const long long want = (ntask + 15) / 16;
+    const long long g = std::min<long long>(want, std::min<long long>(p.max_ctas, sms[dev]));
+    return launch_pdl(k_vocab_stats<BF16, AMAX, 16>, dim3(static_cast<unsigned>(g > 0 ? g : 1)), dim3(512), 0, s, p);
+  }
+  const long long want = (ntask + 7) / 8;
   const dim3 g1(static_cast<unsigned>(want < cap[dev] ? want : cap[dev]));
-  return launch_pdl(k_vocab_stats<BF16, AMAX>, g1, dim3(kStatsThreads), 0, s, p);
+  return launch_pdl(k_vocab_stats<BF16, AMAX, 8>, g1, dim3(256), 0, s, p);
 }
 
 int accept_launch(const AcceptParams& p, cudaStream_t s) {
@@ -919,37 +1574,55 @@ int accept_launch(const AcceptParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return SSD_ERR_CUDA;
   }
   {
-    // merge, acceptance, choice and final draw: one cluster per sequence, with a warp
-    // for every chunk of the stop row (8 CTAs up to 64 chunks, else 16)
+    // merge, acceptance, choice and final draw. Sample mode with B x 8 <= SMs: a cluster of
+    // 8 (16 for stop rows of more than 256 chunks) 1024-thread CTAs per sequence, one warp
+    // per chunk (k_accept_finish_wide). Otherwise a cluster of C 512-thread CTAs, C the
+    // largest of 4, 2 with the whole batch's clusters resident at once, else 1 (and 1 in
+    // greedy mode, which has no draw), warps looping over chunks (k_accept_finish_batch).
     static std::once_flag once[kMaxDevices];
+    static int sms[kMaxDevices];
     static cudaError_t attr_err[kMaxDevices];
     const int dev = current_device();
     if (dev < 0) return SSD_ERR_CUDA;
     std::call_once(once[dev], [dev] {
-      attr_err[dev] = cudaFuncSetAttribute(k_accept_finish, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(kFinDynSmem));
+      sms[dev] = 0;
+      attr_err[dev] = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
       if (attr_err[dev] == cudaSuccess)
-        attr_err[dev] = cudaFuncSetAttribute(k_accept_finish, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        attr_err[dev] = cudaFuncSetAttribute(k_accept_finish_wide, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kWideDynSmem));
+      if (attr_err[dev] == cudaSuccess)
+        attr_err[dev] = cudaFuncSetAttribute(k_accept_finish_wide, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     });
     if (attr_err[dev] != cudaSuccess) return SSD_ERR_CUDA;
-    const unsigned C = (!p.sample || p.nchs <= kFinCTAs * kFinWarps) ? kFinCTAs : kMaxFinCTAs;
+    const bool wide = p.sample && 8LL * p.B <= sms[dev];
+    unsigned C = 1;
+    if (wide) {
+      C = p.nchs <= kWideCTAs * kWideWarps ? kWideCTAs : kWideMaxCTAs;
+    } else if (p.sample) {
+      while (C < 4u && 2LL * C * p.B <= sms[dev]) C *= 2;
+    }
     KernelTimer t(SSD_KERNEL_ACCEPT_FINISH, s);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(C, by, 1);
-    cfg.blockDim = dim3(kFinThreads);
-    cfg.dynamicSmemBytes = kFinDynSmem;
+    cfg.blockDim = dim3(wide ? kWideThreads : kFinThreads);
+    cfg.dynamicSmemBytes = wide ? kWideDynSmem : 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = C;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = C;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, k_accept_finish, p);
-    if (e != cudaSuccess) return SSD_ERR_CUDA;
+    cfg.numAttrs = C > 1 ? 2 : 1;
+    if (wide) {
+      e = cudaLaunchKernelEx(&cfg, k_accept_finish_wide, p);
+      if (e != cudaSuccess) return SSD_ERR_CUDA;
+    } else {
+      e = cudaLaunchKernelEx(&cfg, k_accept_finish_batch, p);
+      if (e != cudaSuccess) return SSD_ERR_CUDA;
+    }
   }
   int n = 2;
   if (p.probs_out != nullptr) {

@@ -42,6 +42,7 @@ struct AcceptParams {
   float* probs_out;
   int sample, bf16, probs;
   int early;          // row pass reads every row without waiting for the retrieval
+  int max_ctas;       // row pass on at most this many SMs (0: the whole GPU)
   int nch, nchs;
   int64_t chunk, schunk;
   WsHeader* hdr;

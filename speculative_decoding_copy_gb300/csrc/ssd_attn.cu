@@ -139,7 +139,7 @@ k_attn_prefix_simt(AttnParams p) {
     const int r = r_base + wid * kSimtRowsPerWarp + j;
     if (r >= rows_total) continue;
     const int t = r / G, h = kvh * G + r % G;
-    if (!token_present(p.blk_len, b, p.NB, p.Dmax, t)) continue;
+    if (!p.all_rows && !token_present(p.blk_len, b, p.NB, p.Dmax, t)) continue;
     const int64_t R = (static_cast<int64_t>(b) * NT + t) * p.Hq + h;
     float* ml = p.ws_ml + (R * p.S + split) * 2;
     float* ow = p.ws_o + (R * p.S + split) * DH;
@@ -166,7 +166,7 @@ k_attn_combine(AttnParams p) {
   const int h = static_cast<int>(R % p.Hq);
   const int t = static_cast<int>((R / p.Hq) % NT);
   const int b = static_cast<int>(R / (static_cast<int64_t>(p.Hq) * NT));
-  if (!token_present(p.blk_len, b, p.NB, p.Dmax, t)) return;
+  if (!p.all_rows && !token_present(p.blk_len, b, p.NB, p.Dmax, t)) return;
   const int G = p.Hq / p.Hkv;
   const int kvh = h / G;
   const int k = t / p.Dmax, pos = t % p.Dmax;
@@ -301,6 +301,9 @@ static int validate(const ssd_attn_args* a) {
   if (a->out_dtype != a->dtype && a->out_dtype != SSD_F32) return SSD_ERR_INVALID;
   if (a->Hq % a->Hkv != 0) return SSD_ERR_INVALID;
   if (a->skip_absent != 0 && a->skip_absent != 1) return SSD_ERR_INVALID;
+  if (a->all_rows != 0 && a->all_rows != 1) return SSD_ERR_INVALID;
+  if (a->all_rows && a->skip_absent) return SSD_ERR_INVALID;
+  if (a->max_ctas < 0) return SSD_ERR_INVALID;
   if (a->Dmax > 256 || a->NB * a->Dmax > 8192 || a->Hq / a->Hkv > 64) return SSD_ERR_UNSUPPORTED;
   if (static_cast<long long>(a->B) * a->Hkv > 0x7fffffffLL) return SSD_ERR_UNSUPPORTED;
   if (a->dh != 64 && a->dh != 128) return SSD_ERR_UNSUPPORTED;
@@ -312,7 +315,8 @@ static int validate(const ssd_attn_args* a) {
     if (a->P_max > 128LL * a->pages_per_seq) return SSD_ERR_INVALID;
   }
   if (a->B == 0) return SSD_OK;
-  if (!a->q || !a->k_cand || !a->v_cand || !a->out || !a->prefix_len || !a->blk_len) return SSD_ERR_INVALID;
+  if (!a->q || !a->k_cand || !a->v_cand || !a->out || !a->prefix_len) return SSD_ERR_INVALID;
+  if (!a->all_rows && !a->blk_len) return SSD_ERR_INVALID;
   if (a->P_max > 0 && (!a->k_cache || !a->v_cache)) return SSD_ERR_INVALID;
   return SSD_OK;
 }
@@ -364,6 +368,7 @@ extern "C" int ssd_verify_attn(const ssd_attn_args* a, void* ws, size_t ws_bytes
   p.scale_log2 = scale * 1.4426950408889634f;
   p.S = L.S; p.chunk = L.chunk;
   p.out_f32 = (a->out_dtype == SSD_F32) ? 1 : 0;
+  p.all_rows = a->all_rows;
   char* base = static_cast<char*>(ws);
   p.hdr = reinterpret_cast<WsHeader*>(base);
   p.ws_ml = reinterpret_cast<float*>(base + L.ml_off);

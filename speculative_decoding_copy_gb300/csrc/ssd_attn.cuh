@@ -24,6 +24,7 @@ struct AttnParams {
   int pages_per_seq;
   int64_t num_pages;
   int skip_absent;       // tensor-core path: wait for the predecessor first, skip tiles without a present token
+  int all_rows;          // write every slot's row; blk_len is never read
   WsHeader* hdr;
   float* ws_ml;          // [rows][S][2]  running max and sum per split
   float* ws_o;           // [rows][S][dh] un-normalised output per split

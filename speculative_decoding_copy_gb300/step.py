@@ -4,6 +4,8 @@ launch order of the C-ABI calls.
     gate_retrieve -> accept (row pass, finish) -> verify_attn     (one stream, "rows_first")
     gate_retrieve -> verify_attn -> accept (early rows)            (one stream, "attn_first")
     gate_retrieve -> { verify_attn (aux stream) || accept }       (two streams)
+    { gate_retrieve -> accept (early rows, part of the SMs) }
+      || verify_attn (every row, aux stream, the other SMs)       ("split")
 
 Verification attention and acceptance both depend only on the retrieval output.
 On one stream the kernels are chained by programmatic dependent launch: the row
@@ -21,6 +23,11 @@ present token, at the price of waiting for its predecessor first; it pays off in
 batches whose gate sends sequences to the chain draft. In the "attn_first" order the
 attention's main loop starts while the retrieval still runs and the row pass, in its
 early mode, streams beside it (measured slower; kept as an option).
+
+In the "split" order the attention writes every slot's row (all_rows), so it depends on
+no earlier kernel of the step: it starts on an auxiliary stream together with the
+retrieval, on at most attn_ctas SMs, while the retrieval, the row pass (early mode, at
+most rows_ctas SMs of one CTA each) and the finish kernel run on the main stream.
 
 Inputs may sit in one device arena (arena_bytes), so that a caller refreshes all of
 them with a single host-to-device copy. The step issues only library calls; it
@@ -83,19 +90,23 @@ class VerifyStep:
 
     def __init__(self, wl, inp: dict, device="cuda", mode=None, kind=None, with_attention=True,
                  with_probs=False, early_rows=False, order="rows_first", arena: torch.Tensor | None = None,
-                 skip_absent=None):
+                 skip_absent=None, attn_ctas=0, rows_ctas=0):
         """`arena`: optional uint8 device tensor of at least arena_bytes(inp, with_attention)
         bytes; the inputs are then placed in it (256-byte aligned views), so that a caller
         can refresh all of them with one host-to-device copy of a same-layout host buffer.
         `skip_absent`: the attention skips 128-row tiles without a present token (after
         waiting for its predecessor); None turns it on for batches whose gate can send
         sequences to the chain draft, where the copy-block rows of those sequences are empty."""
-        if order not in ("rows_first", "attn_first"):
+        if order not in ("rows_first", "attn_first", "split"):
             raise ValueError(f"unknown step order {order!r}")
         self.wl = wl
         self.early_rows = early_rows
         self.order = order
+        self.attn_ctas, self.rows_ctas = int(attn_ctas), int(rows_ctas)
         self.skip_absent = (wl.chain_policy == 1 and wl.B > 1) if skip_absent is None else bool(skip_absent)
+        if order == "split":
+            self.skip_absent = False          # the attention reads nothing from the retrieval
+        self.all_rows = order == "split"
         self.mode = ssd.SSD_SAMPLE if (mode or wl.mode) == "sample" else ssd.SSD_GREEDY
         if kind is None:
             kind = ssd.SSD_LOGITS_BF16 if wl.logit_dtype == "bf16" else ssd.SSD_LOGITS_F32
@@ -140,7 +151,8 @@ class VerifyStep:
             self.attn_out = torch.empty_like(self.x["q"])
             a = ssd.attn_args(self.x["q"], self.x["k_cache"], self.x["v_cache"], self.x["k_cand"],
                               self.x["v_cand"], self.x["prefix_len"], self.ret_out["blk_len"], wl.Dmax,
-                              self.attn_out, skip_absent=self.skip_absent)
+                              self.attn_out, skip_absent=self.skip_absent, all_rows=self.all_rows,
+                              max_ctas=self.attn_ctas)
             self.attn_ws = torch.empty(max(256, ssd.ssd_verify_attn_workspace_size(a)), dtype=torch.uint8,
                                        device=self.device)
 
@@ -167,7 +179,8 @@ class VerifyStep:
         x = self.x
         return ssd.ssd_verify_attn(x["q"], x["k_cache"], x["v_cache"], x["k_cand"], x["v_cand"], x["prefix_len"],
                                    self.ret_out["blk_len"], self.wl.Dmax, out=self.attn_out, ws=self.attn_ws,
-                                   stream=stream, skip_absent=self.skip_absent)
+                                   stream=stream, skip_absent=self.skip_absent, all_rows=self.all_rows,
+                                   max_ctas=self.attn_ctas)
 
     def accept(self, stream=None, early_rows=None):
         wl, x = self.wl, self.x
@@ -175,11 +188,27 @@ class VerifyStep:
         return ssd.ssd_accept(x["tgt"], x.get("drf") if wl.chain_policy else None, self.ret_out["blk_tok"],
                               self.ret_out["blk_len"], x["u_acc"], x["u_fin"], mode=self.mode, kind=self.kind,
                               K=wl.K, chain_blk=self.chain_blk, out=self.acc_out, ws=self.acc_ws,
-                              probs_out=self.probs, stream=stream, early_rows=early)
+                              probs_out=self.probs, stream=stream, early_rows=early,
+                              max_ctas=self.rows_ctas if self.order == "split" else 0)
 
     def run(self, stream=None, aux: torch.cuda.Stream | None = None):
-        """Issue the whole step on `stream` (default: current), attention on `aux` if given."""
+        """Issue the whole step on `stream` (default: current), attention on `aux` if given
+        (the "split" order needs `aux`)."""
         main = stream or torch.cuda.current_stream()
+        if self.order == "split" and self.with_attention:
+            if aux is None:
+                raise ValueError("the split order runs the attention on an auxiliary stream")
+            ev = torch.cuda.Event()
+            ev.record(main)
+            aux.wait_event(ev)
+            self.attention(aux)
+            self.gate_retrieve(main)
+            if self.with_accept:
+                self.accept(main)
+            ev2 = torch.cuda.Event()
+            ev2.record(aux)
+            main.wait_event(ev2)
+            return
         self.gate_retrieve(main)
         if self.with_attention and aux is not None:
             ev = torch.cuda.Event()

@@ -176,6 +176,31 @@ def test_accept_early_rows(mode, V, B, W, Dmax, K, policy):
     _assert_same(late, ref)
 
 
+@pytest.mark.parametrize("max_ctas", [1, 7, 52])
+def test_accept_row_pass_on_capped_grid(max_ctas):
+    """The row pass on at most max_ctas SMs (one 16-warp CTA each) gives the same statistics:
+    decisions bit-exact against the oracle given probabilities, early mode and not."""
+    rng = np.random.default_rng(900 + max_ctas)
+    V, B, W, Dmax, K, policy = 4000, 6, 4, 20, 5, 1
+    blk_tok, blk_len = _blocks(rng, B, W, Dmax, K, V, policy)
+    NB = blk_tok.shape[1]
+    tgt = _boost_probs(_rows_probs(rng, (B, 1 + NB * Dmax, V)), blk_tok, blk_len, Dmax, rng)
+    drf = _rows_probs(rng, (B, K, V))
+    for b in range(B):
+        for d in range(blk_len[b, W]):
+            blk_tok[b, W, d] = int(np.argmax(drf[b, d] * rng.random(V)))
+    u_acc = WL.uniforms24(rng, (B, NB, Dmax))
+    u_fin = WL.uniforms24(rng, (B,))
+    ref = _oracle("sample", "probs_f32", tgt, drf, blk_tok, blk_len, W, policy, u_acc, u_fin)
+    dev = "cuda"
+    T = lambda a: to_device(np.asarray(a), dev)
+    for early in (True, False):
+        r = S.ssd_accept(T(tgt), T(drf), T(blk_tok), T(blk_len), T(u_acc), T(u_fin), mode=S.SSD_SAMPLE,
+                         kind=S.SSD_PROBS_F32, K=K, chain_blk=W, early_rows=early, max_ctas=max_ctas)
+        torch.cuda.synchronize()
+        _assert_same({k: v.cpu().numpy() for k, v in r.items()}, ref)
+
+
 @pytest.mark.parametrize("early", [True, False])
 def test_accept_back_to_back_calls_share_a_workspace(early):
     """Calls issued one after another on one stream may share a workspace: each call's
@@ -290,7 +315,8 @@ def test_accept_logits_probs_and_decisions(kind, V):
 @pytest.mark.parametrize("name,order", [(n, "two_streams") for n in WL.WORKLOAD_ORDER] +
                          [("tiny", "rows_first"), ("llama8b", "rows_first"), ("batched", "rows_first"),
                           ("tiny", "attn_first"), ("llama8b", "attn_first"),
-                          ("tiny", "bench"), ("llama8b", "bench")])
+                          ("tiny", "bench"), ("llama8b", "bench"), ("tiny", "split"), ("llama8b", "split"),
+                          ("batched", "split")])
 def test_whole_step_workloads(name, order):
     """gate -> retrieve -> accept and attention through the step's own launch path (one
     stream in either order, or attention on a second stream), compared with the oracle
@@ -299,11 +325,15 @@ def test_whole_step_workloads(name, order):
     wl = WL.WORKLOADS[name]
     inp = WL.make_inputs(wl, 77 + len(name), full_width=False)
     two = order == "two_streams"
-    # "bench": the launch configuration the benchmark times (one stream, early row pass)
+    split = order == "split"
+    # "bench": the launch configuration the benchmark times (one stream, early row pass); "split":
+    # the attention on a second stream (every row) beside the acceptance chain on capped grids
     st = VerifyStep(wl, inp, with_attention=(name in ("tiny", "llama8b")),
-                    order=order if order.endswith("_first") else "rows_first", early_rows=order == "bench")
+                    order=order if (order.endswith("_first") or split) else "rows_first",
+                    early_rows=order == "bench" or (split and name != "batched"),
+                    attn_ctas=96 if split else 0, rows_ctas=52 if split else 0)
     for _ in range(1 if two else 2):
-        st.run(aux=torch.cuda.Stream() if two else None)
+        st.run(aux=torch.cuda.Stream() if (two or split) else None)
     got = st.results()
     ref = O.verify_step(inp, wl, attention_slots=None)
     for k in ("gate", "last_match_end", "blk_tok", "blk_len", "n_cand"):

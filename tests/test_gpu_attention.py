@@ -218,3 +218,37 @@ def test_attention_skip_absent_tiles(G):
                              case["prefix_len"], blk_len, Dmax, "bf16", None)
     err = max(float(np.max(np.abs(outs[1][b, t_] - o))) for (b, t_), o in ref.items())
     assert err <= TOL, err
+
+
+@pytest.mark.parametrize("dtype,dh,G,max_ctas", [("bf16", 128, 4, 0), ("bf16", 128, 4, 5), ("bf16", 128, 8, 30),
+                                                 ("bf16", 128, 1, 2), ("f32", 64, 4, 0)])
+def test_attention_all_rows(dtype, dh, G, max_ctas):
+    """all_rows: every slot's row is written (blk_len not given) as the attention of its q over
+    the prefix and its block's slots up to it, which is the oracle's result for that slot when
+    the slot is present; with the grid capped to max_ctas CTAs as well."""
+    rng = np.random.default_rng(70 + G + dh + max_ctas)
+    Hkv, B, NB, Dmax = 2, 3, 3, 20
+    prefix = [300, 0, 4100]
+    case = _case(rng, B, NB, Dmax, Hkv * G, Hkv, dh, prefix, dtype, q_scale=2.0)
+    dev = "cuda"
+    t = {k: to_device(np.asarray(v), dev) for k, v in case.items()}
+    out = S.ssd_verify_attn(t["q"], t["k_cache"], t["v_cache"], t["k_cand"], t["v_cand"], t["prefix_len"], None, Dmax,
+                            out_f32=True, all_rows=True, max_ctas=max_ctas, NB=NB)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    full = np.full((B, NB), Dmax, np.int32)
+    ref = O.verify_attention(case["q"], case["k_cache"], case["v_cache"], case["k_cand"], case["v_cand"],
+                             case["prefix_len"], full, Dmax, dtype, None)
+    assert len(ref) == B * NB * Dmax
+    err = max(float(np.max(np.abs(got[b, t_] - o))) for (b, t_), o in ref.items())
+    assert err <= TOL, err
+
+
+def test_attention_all_rows_rejects_skip_absent():
+    rng = np.random.default_rng(5)
+    case = _case(rng, 1, 1, 4, 4, 1, 128, [128], "bf16")
+    dev = "cuda"
+    t = {k: to_device(np.asarray(v), dev) for k, v in case.items()}
+    with pytest.raises(S.SsdError):
+        S.ssd_verify_attn(t["q"], t["k_cache"], t["v_cache"], t["k_cand"], t["v_cand"], t["prefix_len"],
+                          to_device(np.array([[4]], np.int32), dev), 4, all_rows=True, skip_absent=True)
