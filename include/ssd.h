@@ -215,7 +215,10 @@ int ssd_gate_retrieve(const int32_t* ctx, int64_t ctx_stride, const int32_t* ctx
  * tensor-core grid to at most max(n, clusters of one CTA) CTAs, one per SM, so
  * that a kernel on another stream can hold the remaining SMs at the same time.
  * Workspace: ssd_verify_attn_workspace_size(a) bytes, 256-byte aligned; its
- * contents need no initialisation. Device-side errors are recorded in it.
+ * contents need no initialisation for the results. Device-side errors are recorded
+ * in its first word, which keeps whatever it held before: zero the header (its first
+ * 256 bytes) once after allocating it, or read it once with ssd_read_device_error,
+ * before relying on that word.
  */
 typedef struct {
   const void* q;
@@ -292,7 +295,8 @@ int ssd_verify_attn(const ssd_attn_args* a, void* ws, size_t ws_bytes, void* str
  * 2 <= V < 2^31; NB*Dmax < 4096;
  * Dmax <= 256; 0 <= chain_blk < NB or chain_blk == -1.
  * Workspace: ssd_accept_workspace_size(a) bytes, 256-byte aligned; its
- * contents need no initialisation. Calls issued one after another on one
+ * contents need no initialisation for the results (the error word in its first
+ * bytes: as for ssd_verify_attn). Calls issued one after another on one
  * stream may share it; calls that overlap on the GPU (other streams) may not.
  */
 typedef struct {
@@ -453,6 +457,24 @@ int ssd_accept_static(const ssd_accept_args* a, void* stream);
  * Errors: SSD_ERR_INVALID (out NULL), SSD_ERR_CUDA.
  */
 int ssd_read_static_error(void* stream, int32_t* out);
+
+/*
+ * ssd_checked_build — 1 for the checked build of the library (libssd_checked.so,
+ * compiled with -DSSD_CHECKS=1), 0 for the normal one. The checked build tests every
+ * guarded device index (token ids, block lengths, prefix lengths, output offsets,
+ * workspace offsets) against the extent it must stay within before the access; a
+ * failed test records SSD_ERR_DEVICE in the call's workspace header, when the call has
+ * one, and in a check word of the library, and the access is skipped. No counterpart
+ * on the pages: a debugging aid for callers and tests.
+ */
+int ssd_checked_build(void);
+
+/*
+ * ssd_read_check_error — SYNCHRONOUS: waits for `stream`, then reads and clears the
+ * library's check words (checked build; always SSD_OK in the normal build). *out gets
+ * SSD_OK or SSD_ERR_DEVICE. `out` is a host pointer. Errors: SSD_ERR_INVALID, SSD_ERR_CUDA.
+ */
+int ssd_read_check_error(void* stream, int32_t* out);
 
 /*
  * ssd_read_probe — measurement tool (no counterpart on the pages): reads `bytes`

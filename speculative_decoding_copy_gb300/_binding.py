@@ -15,6 +15,7 @@ from ctypes import POINTER, c_float, c_int, c_int32, c_int64, c_size_t, c_uint64
 import torch
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libssd.so")
+CHECKED_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libssd_checked.so")
 
 SSD_OK, SSD_ERR_INVALID, SSD_ERR_UNSUPPORTED, SSD_ERR_CUDA, SSD_ERR_WORKSPACE, SSD_ERR_TIMEOUT, SSD_ERR_DEVICE = (
     0, -1, -2, -3, -4, -5, -6)
@@ -28,7 +29,7 @@ EXPORTED = ["ssd_status_string", "ssd_version", "ssd_launch_count", "ssd_gate_ma
             "ssd_read_device_error", "ssd_profile_kernel", "ssd_accept_static", "ssd_gate_retrieve",
             "ssd_selftest_wait", "ssd_commit_kv",
             "ssd_copy_stats", "ssd_lowrank_head_workspace_size", "ssd_lowrank_head", "ssd_read_static_error",
-            "ssd_read_probe"]
+            "ssd_read_probe", "ssd_checked_build", "ssd_read_check_error"]
 SSD_KERNEL = dict(vocab_stats=1, verify_attn=2, attn_combine=3, accept_finish=4, gate_match=6,
                   retrieve=7, head_down=8, head_up=9, head_combine=10)
 
@@ -69,15 +70,42 @@ class AcceptArgs(ctypes.Structure):
 
 
 _lib = None
+_loaded = {}
 
 
 def lib() -> ctypes.CDLL:
-    """Load libssd.so (once). Raises if it has not been built."""
+    """The library every call goes through: libssd.so unless use_library() selected another
+    build. Raises if it has not been built."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is missing: build it with speculative_decoding_copy_gb300.build.build()")
-        L = ctypes.CDLL(LIB_PATH)
+        _lib = load(LIB_PATH)
+    return _lib
+
+
+class use_library:
+    """Context manager: calls inside go through the library at `path` (e.g. the checked build)."""
+
+    def __init__(self, path):
+        self.path = path
+
+    def __enter__(self):
+        global _lib
+        self.prev = _lib
+        _lib = load(self.path)
+        return _lib
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self.prev
+        return False
+
+
+def load(path) -> ctypes.CDLL:
+    """Load one build of the library (once per path) with every entry point's signature."""
+    if path not in _loaded:
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with speculative_decoding_copy_gb300.build.build_all()")
+        L = ctypes.CDLL(path)
         L.ssd_status_string.restype = ctypes.c_char_p
         L.ssd_status_string.argtypes = [c_int]
         L.ssd_version.restype = c_int
@@ -120,8 +148,11 @@ def lib() -> ctypes.CDLL:
         L.ssd_read_static_error.argtypes = [c_void_p, POINTER(c_int32)]
         L.ssd_profile_kernel.restype = c_int
         L.ssd_profile_kernel.argtypes = [c_int, c_void_p, c_void_p]
-        _lib = L
-    return _lib
+        L.ssd_checked_build.restype = c_int
+        L.ssd_read_check_error.restype = c_int
+        L.ssd_read_check_error.argtypes = [c_void_p, POINTER(c_int32)]
+        _loaded[path] = L
+    return _loaded[path]
 
 
 def status_string(status: int) -> str:
@@ -283,7 +314,7 @@ def ssd_verify_attn(q, k_cache, v_cache, k_cand, v_cand, prefix_len, blk_len, Dm
                      skip_absent, all_rows, max_ctas, NB)
     need = ssd_verify_attn_workspace_size(args)
     if ws is None:
-        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+        ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=q.device)
     rc = lib().ssd_verify_attn(ctypes.byref(args), _ptr(ws), ws.numel(), _stream(stream))
     _check("ssd_verify_attn", rc)
     return out
@@ -424,6 +455,13 @@ def ssd_read_probe(buf, nbytes, sink, ctas_per_sm=2, stream=None):
         raise ValueError("nbytes exceeds the buffer")
     _check("ssd_read_probe", lib().ssd_read_probe(_ptr(buf), int(nbytes), int(ctas_per_sm), _ptr(sink),
                                                   _stream(stream)))
+
+
+def ssd_read_check_error(stream=None) -> int:
+    """Read and clear the check words of the checked build (SSD_OK in the normal build)."""
+    v = c_int32(0)
+    _check("ssd_read_check_error", lib().ssd_read_check_error(_stream(stream), ctypes.byref(v)))
+    return int(v.value)
 
 
 def ssd_read_device_error(ws, stream=None) -> int:

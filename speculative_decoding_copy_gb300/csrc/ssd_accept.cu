@@ -16,24 +16,22 @@
 //                   reduces each to max, argmax (greedy only; lowest index on
 //                   ties) and sum of 2^((l - max) log2 e) with warp shuffles; in
 //                   the early mode it streams every row without waiting for the
-//                   kernel before it: only its last CTA waits for that kernel
-//                   (then lets the next kernel launch), the others never wait;
-//   k_accept_finish one cluster of 8 CTAs per sequence: merges the pieces of
-//                   every needed row (one warp per row), runs the acceptance test
-//                   of every candidate token and picks the longest accepted block
-//                   (rank 0), and in sample mode draws the final token from the
-//                   integer weights of the stop row (chunk sums exchanged through
-//                   distributed shared memory, then one block scan in the chunk
-//                   that holds the threshold);
+//                   kernel before it (it only stores after that wait), and only
+//                   its last CTA waits before letting the next kernel launch;
+//   k_accept_finish_wide / k_accept_finish_batch  per sequence (one cluster each):
+//                   merges every needed row's pieces, runs the acceptance test
+//                   of every candidate token and picks the longest accepted block,
+//                   and in sample mode draws the final token from the integer
+//                   weights of the stop row (chunk sums exchanged through
+//                   distributed shared memory, then the chunk, the lane and the
+//                   entry that hold the threshold);
 //   k_probs_out     optional diagnostic copy of p for every needed row.
 #include <math.h>
 
 #include <algorithm>
 #include <mutex>
-#include <type_traits>
 
 #include "ssd_accept.cuh"
-#include "ssd_tc.cuh"
 
 namespace ssd {
 
@@ -139,9 +137,8 @@ __device__ __forceinline__ float vec_elem(const uint4& u, int e) {
   return __uint_as_float(w);
 }
 
-template <bool BF16, bool AMAX, bool FULL, typename Consumed>
-__device__ __forceinline__ RowStat reduce_vecs(const uint4 (&v)[Piece<BF16>::kVec], int n, int e0, int probs,
-                                               Consumed consumed);
+template <bool BF16, bool AMAX, bool FULL>
+__device__ __forceinline__ RowStat reduce_vecs(const uint4 (&v)[Piece<BF16>::kVec], int n, int e0, int probs);
 
 // One warp's statistics of the piece of n elements starting at element e0 of `row`:
 // max, sum of 2^((x - max) log2 e) (not for probabilities) and, with AMAX, the argmax
@@ -182,16 +179,13 @@ __device__ __forceinline__ RowStat reduce_piece(const void* row, int n, int e0, 
       v[j] = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
-  return reduce_vecs<BF16, AMAX, FULL>(v, n, e0, probs, nullptr);
+  return reduce_vecs<BF16, AMAX, FULL>(v, n, e0, probs);
 }
 
 // The reduction of reduce_piece on a piece already in registers: lane's vector j holds
-// elements [e0 + (j*32 + lane)*EPV, +EPV), those at or past n count as -inf. `consumed`
-// (optional) is called once every vector has been used (the max pass reads them all),
-// after which the registers alone carry the piece.
-template <bool BF16, bool AMAX, bool FULL, typename Consumed>
-__device__ __forceinline__ RowStat reduce_vecs(const uint4 (&v)[Piece<BF16>::kVec], int n, int e0, int probs,
-                                               Consumed consumed) {
+// elements [e0 + (j*32 + lane)*EPV, +EPV), those at or past n count as -inf.
+template <bool BF16, bool AMAX, bool FULL>
+__device__ __forceinline__ RowStat reduce_vecs(const uint4 (&v)[Piece<BF16>::kVec], int n, int e0, int probs) {
   constexpr int EPV = Piece<BF16>::kEPV;
   constexpr int kPieceVec = Piece<BF16>::kVec;
   const int lane = threadIdx.x & 31;
@@ -215,7 +209,6 @@ __device__ __forceinline__ RowStat reduce_vecs(const uint4 (&v)[Piece<BF16>::kVe
     }
   }
   float M = AMAX ? av : fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-  if constexpr (!std::is_same<Consumed, decltype(nullptr)>::value) consumed(M);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
@@ -235,6 +228,19 @@ __device__ __forceinline__ RowStat reduce_vecs(const uint4 (&v)[Piece<BF16>::kVe
       for (int e = 0; e < EPV; ++e)
         if (FULL || (j * 32 + lane) * EPV + e < n) s4[e & 3] += ex2_approx(fmaf(vec_elem<BF16>(v[j], e), kLog2e, c));
     S = warp_sum((s4[0] + s4[1]) + (s4[2] + s4[3]));
+  }
+  return RowStat{M, S, av, ai};
+}
+
+__device__ __forceinline__ RowStat warp_merge_stat(float M, float S, float av, int ai) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, M, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
+    const float v2 = __shfl_xor_sync(0xffffffffu, av, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, ai, o);
+    stat_merge(M, S, m2, s2);
+    amax_merge(av, ai, v2, i2);
   }
   return RowStat{M, S, av, ai};
 }
@@ -314,182 +320,6 @@ k_vocab_stats(AcceptParams p) {
   }
 }
 
-// ------------------------------------------------------------------ stats, copy-engine fed
-// k_vocab_stream: the same statistics with the pieces brought into shared memory by
-// bulk copies (the copy engine), so that each SM keeps a whole ring of pieces in flight
-// from one thread instead of from its warps' registers. One CTA per SM; CTA c takes the
-// contiguous range [c T / C, (c+1) T / C) of the T tasks (those some token needs) in
-// order. A ring stage holds the next kStreamSlots pieces of the range (32 KB of fp32 or
-// bf16 entries), fetched by one bulk copy per run of pieces that are consecutive in
-// memory and in the stage (copies of 4 KB or 8 KB move data at about two thirds of the
-// rate of 32 KB ones); piece j of the range goes to slot j % kStreamSlots of stage
-// (j / kStreamSlots) % kStreamStages and to consumer warp j % kStreamWarps. Rows must
-// start on 16-byte boundaries and hold a multiple of 16 bytes (the host checks; other
-// rows take k_vocab_stats).
-constexpr int kStreamWarps = 8;
-constexpr int kStreamThreads = 32 * (kStreamWarps + 1);    // + one producer warp
-constexpr int kStreamStage = 32768;
-constexpr int kStreamStages = 6;
-struct StreamBars {
-  uint64_t full[kStreamStages], empty[kStreamStages];
-  int failed;
-  int issued;
-};
-constexpr size_t kStreamSmem = 128 + static_cast<size_t>(kStreamStages) * kStreamStage + sizeof(StreamBars);
-constexpr unsigned long long kStreamWaitClocks = 1ull << 32;
-
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(tc::smem_u32(bar))
-               : "memory");
-}
-
-// the first task at or after t (below t1) that some token needs, or t1
-__device__ __forceinline__ int next_task_in(const AcceptParams& p, int t, int t1) {
-  if (p.early) return t < t1 ? t : t1;
-  for (; t < t1; ++t) {
-    const int br = t / p.nch;
-    const int b = br / p.NRD, r = br - b * p.NRD;
-    if (row_needed(p, b, r)) break;
-  }
-  return t;
-}
-
-template <bool BF16, bool AMAX>
-__global__ void __launch_bounds__(kStreamThreads, 1)
-k_vocab_stream(AcceptParams p) {
-  constexpr int es = BF16 ? 2 : 4;
-  constexpr int kPieceBytes = kPieceElems * es;
-  constexpr int kSlots = kStreamStage / kPieceBytes;       // 4 fp32 or 8 bf16 pieces per stage
-  extern __shared__ uint8_t sraw[];
-  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sraw) + 127) & ~uintptr_t(127));
-  StreamBars& sb = *reinterpret_cast<StreamBars*>(ring + kStreamStages * kStreamStage);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (tid == 0) {
-    for (int i = 0; i < kStreamStages; ++i) {
-      tc::mbar_init(&sb.full[i], 1);
-      tc::mbar_init(&sb.empty[i], kSlots);
-    }
-    sb.failed = 0;
-    sb.issued = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncthreads();
-  // the dependency rules of k_vocab_stats: in the early mode only the last CTA waits
-  // first, and nothing is written to the workspace before griddepcontrol.wait
-  bool waited = !p.early || blockIdx.x == gridDim.x - 1;
-  if (waited) asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const long long C = gridDim.x;
-  const long long ntask = static_cast<long long>(p.nch) * p.NRD * p.B;
-  const int t0 = static_cast<int>(blockIdx.x * ntask / C), t1 = static_cast<int>((blockIdx.x + 1) * ntask / C);
-  if (warp == kStreamWarps) {
-    // producer: a stage per kSlots pieces, one bulk copy per run of consecutive pieces
-    if (lane == 0) {
-      int j = 0, st = 0;                        // pieces issued, stages issued
-      int t = next_task_in(p, t0, t1);
-      while (t < t1) {
-        const int s = st % kStreamStages;
-        if (st >= kStreamStages &&
-            !mbar_wait_bounded(&sb.empty[s], ((st / kStreamStages) - 1) & 1, &sb.failed, p.hdr, 110,
-                               kStreamWaitClocks))
-          break;
-        // the stage's pieces and their runs
-        const char* run_src = nullptr;
-        uint32_t run_dst = 0, run_bytes = 0, stage_bytes = 0;
-        const uint32_t base = tc::smem_u32(ring + s * kStreamStage);
-        int k = 0;
-        // expect_tx first would need the byte count: count the stage's bytes in a first walk
-        {
-          int tt = t;
-          for (int kk = 0; kk < kSlots && tt < t1; ++kk, tt = next_task_in(p, tt + 1, t1)) {
-            const int c = tt % p.nch;
-            stage_bytes += static_cast<uint32_t>(min(static_cast<int64_t>(kPieceElems), p.V - c * kPieceElems) * es);
-          }
-        }
-        tc::mbar_expect_tx(&sb.full[s], stage_bytes);
-        for (; k < kSlots && t < t1; ++k, ++j, t = next_task_in(p, t + 1, t1)) {
-          const int br = t / p.nch, c = t - br * p.nch;
-          const int b = br / p.NRD, r = br - b * p.NRD;
-          const char* src = static_cast<const char*>(row_ptr(p, b, r)) + static_cast<int64_t>(c) * kPieceBytes;
-          const uint32_t n = static_cast<uint32_t>(min(static_cast<int64_t>(kPieceElems), p.V - c * kPieceElems) * es);
-          const uint32_t dst = base + k * kPieceBytes;
-          if (run_bytes > 0 && src == run_src + run_bytes && dst == run_dst + run_bytes &&
-              run_bytes % kPieceBytes == 0) {
-            run_bytes += n;                    // extends the run (every piece before it was whole)
-          } else {
-            if (run_bytes > 0) bulk_g2s(run_dst, run_src, run_bytes, &sb.full[s]);
-            run_src = src;
-            run_dst = dst;
-            run_bytes = n;
-          }
-        }
-        if (run_bytes > 0) bulk_g2s(run_dst, run_src, run_bytes, &sb.full[s]);
-        ++st;
-      }
-      sb.issued = st;
-    }
-  } else {
-    RowStat held{};
-    int64_t held_at = -1;
-    int nheld = 0;
-    int j = 0;
-    for (int t = next_task_in(p, t0, t1); t < t1; t = next_task_in(p, t + 1, t1), ++j) {
-      if (j % kStreamWarps != warp) continue;
-      const int st = j / kSlots, s = st % kStreamStages, k = j % kSlots;
-      if (!mbar_wait_bounded(&sb.full[s], (st / kStreamStages) & 1, &sb.failed, p.hdr, 111, kStreamWaitClocks)) break;
-      const int br = t / p.nch, c = t - br * p.nch;
-      const int e0 = c * kPieceElems;
-      const int n = static_cast<int>(min(static_cast<int64_t>(kPieceElems), p.V - e0));
-      constexpr int kPieceVec = Piece<BF16>::kVec;
-      const uint32_t src = tc::smem_u32(ring + s * kStreamStage + k * kPieceBytes) + lane * 16;
-      uint4 v[kPieceVec];
-#pragma unroll
-      for (int q = 0; q < kPieceVec; ++q)
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(v[q].x), "=r"(v[q].y), "=r"(v[q].z), "=r"(v[q].w)
-                     : "r"(src + q * 512));
-      // the slot is released once the max pass has used every loaded vector
-      auto release = [&](float) {
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&sb.empty[s]);
-      };
-      const RowStat r = n == kPieceElems ? reduce_vecs<BF16, AMAX, true>(v, n, e0, p.probs, release)
-                                         : reduce_vecs<BF16, AMAX, false>(v, n, e0, p.probs, release);
-      const int64_t at = static_cast<int64_t>(br) * p.nch + c;
-      if (!waited && nheld < 32) {
-        if (lane == nheld) {
-          held = r;
-          held_at = at;
-        }
-        ++nheld;
-        continue;
-      }
-      if (!waited) {
-        asm volatile("griddepcontrol.wait;" ::: "memory");
-        waited = true;
-        if (held_at >= 0) p.part[held_at] = held;
-        held_at = -1;
-      }
-      if (lane == 0) p.part[at] = r;
-    }
-    if (!waited && nheld > 0) {
-      asm volatile("griddepcontrol.wait;" ::: "memory");
-      if (held_at >= 0) p.part[held_at] = held;
-    }
-  }
-  __syncthreads();
-  if (tid == 0 && sb.failed) {
-    // a wait gave up: let the copies still in flight land before the CTA exits (the
-    // last kStreamStages issued stages are distinct)
-    for (int q = max(0, sb.issued - kStreamStages); q < sb.issued; ++q) {
-      const unsigned long long c0 = clock64();
-      while (!mbar_probe(&sb.full[q % kStreamStages], (q / kStreamStages) & 1) && clock64() - c0 < kStreamWaitClocks) {
-      }
-    }
-  }
-}
-
 // ------------------------------------------------------------------ finish
 // k_accept_finish_batch: one cluster of C CTAs (C = 1, 2 or 4; chosen so that the
 // clusters of the whole batch fit on the GPU at once) per sequence does the rest
@@ -552,47 +382,56 @@ __device__ __forceinline__ bool row_needed_s(const AcceptParams& p, const int* l
   return p.chain_blk >= 0 && (r - p.NR) < len_s[p.chain_blk];
 }
 
-__device__ __forceinline__ RowStat warp_merge_stat(float M, float S, float av, int ai) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, M, o);
-    const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
-    const float v2 = __shfl_xor_sync(0xffffffffu, av, o);
-    const int i2 = __shfl_xor_sync(0xffffffffu, ai, o);
-    stat_merge(M, S, m2, s2);
-    amax_merge(av, ai, v2, i2);
-  }
-  return RowStat{M, S, av, ai};
-}
 
-// statistics of rows ra and rb of sequence b (rb < 0: none) merged from their pieces,
-// by one warp; the loads of both rows are in flight together
-__device__ __forceinline__ void merge_rows(const AcceptParams& p, int b, int ra, int rb, RowStat& xa, RowStat& xb) {
+
+
+// Statistics of the needed rows of sequence b merged from their pieces into st[], every
+// warp taking rows warp, warp + nw, ... with the loads of all its rows issued before any
+// merge (one round trip to L2 for up to kRowsPerWarp rows); rows beyond that loop.
+template <int kRowsPerWarp>
+__device__ __forceinline__ void merge_needed_rows(const AcceptParams& p, int b, const int* len_s, RowStat* st,
+                                                  int warp, int nw) {
   const int lane = threadIdx.x & 31;
-  const float4 none = make_float4(-INFINITY, 0.f, -INFINITY, __int_as_float(0x7fffffff));
-  const RowStat* sa = p.part + (static_cast<int64_t>(b) * p.NRD + ra) * p.nch;
-  const RowStat* sb = p.part + (static_cast<int64_t>(b) * p.NRD + (rb >= 0 ? rb : ra)) * p.nch;
-  float Ma = -INFINITY, Sa = 0.f, ava = -INFINITY, Mb = -INFINITY, Sb = 0.f, avb = -INFINITY;
-  int aia = 0x7fffffff, aib = 0x7fffffff;
-  for (int c0 = 0; c0 < p.nch; c0 += 64) {
-    const bool k0 = c0 + lane < p.nch, k1 = c0 + 32 + lane < p.nch;
-    const float4 a0 = k0 ? __ldcg(reinterpret_cast<const float4*>(sa + c0 + lane)) : none;
-    const float4 a1 = k1 ? __ldcg(reinterpret_cast<const float4*>(sa + c0 + 32 + lane)) : none;
-    const float4 b0 = (rb >= 0 && k0) ? __ldcg(reinterpret_cast<const float4*>(sb + c0 + lane)) : none;
-    const float4 b1 = (rb >= 0 && k1) ? __ldcg(reinterpret_cast<const float4*>(sb + c0 + 32 + lane)) : none;
-    stat_merge(Ma, Sa, a0.x, a0.y);
-    stat_merge(Ma, Sa, a1.x, a1.y);
-    amax_merge(ava, aia, a0.z, __float_as_int(a0.w));
-    amax_merge(ava, aia, a1.z, __float_as_int(a1.w));
-    stat_merge(Mb, Sb, b0.x, b0.y);
-    stat_merge(Mb, Sb, b1.x, b1.y);
-    amax_merge(avb, aib, b0.z, __float_as_int(b0.w));
-    amax_merge(avb, aib, b1.z, __float_as_int(b1.w));
+  for (int r0 = warp; r0 < p.NRD; r0 += kRowsPerWarp * nw) {
+    float M[kRowsPerWarp], S[kRowsPerWarp], av[kRowsPerWarp];
+    int ai[kRowsPerWarp];
+#pragma unroll
+    for (int q = 0; q < kRowsPerWarp; ++q) {
+      M[q] = -INFINITY;
+      S[q] = 0.f;
+      av[q] = -INFINITY;
+      ai[q] = 0x7fffffff;
+    }
+    for (int c0 = 0; c0 < p.nch; c0 += 64) {
+      float4 v[kRowsPerWarp][2];
+#pragma unroll
+      for (int q = 0; q < kRowsPerWarp; ++q) {
+        const int r = r0 + q * nw;
+        const bool need = r < p.NRD && row_needed_s(p, len_s, r);
+        const RowStat* src = p.part + (static_cast<int64_t>(b) * p.NRD + (need ? r : 0)) * p.nch;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int c = c0 + h * 32 + lane;
+          v[q][h] = (need && c < p.nch) ? __ldcg(reinterpret_cast<const float4*>(src + c))
+                                        : make_float4(-INFINITY, 0.f, -INFINITY, __int_as_float(0x7fffffff));
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < kRowsPerWarp; ++q)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          stat_merge(M[q], S[q], v[q][h].x, v[q][h].y);
+          amax_merge(av[q], ai[q], v[q][h].z, __float_as_int(v[q][h].w));
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < kRowsPerWarp; ++q) {
+      const int r = r0 + q * nw;
+      const RowStat x = warp_merge_stat(M[q], S[q], av[q], ai[q]);
+      if (lane == 0 && r < p.NRD && row_needed_s(p, len_s, r)) st[r] = x;
+    }
   }
-  xa = warp_merge_stat(Ma, Sa, ava, aia);
-  xb = warp_merge_stat(Mb, Sb, avb, aib);
 }
-
 
 // The weights of the final draw with the row statistics folded in once. p is formed
 // exactly as prob_of forms it (2^(v log2 e - m log2 e) * (1/Z)), with the power of two
@@ -726,24 +565,13 @@ k_accept_finish_batch(AcceptParams p) {
     __syncthreads();
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the piece statistics are complete
 
-    // ---- 2. every needed row merged from its pieces, two rows per warp pass
-    for (int r = warp; r < p.NRD; r += 2 * kFinWarps) {
-      const int r2 = r + kFinWarps;
-      const bool na = row_needed_s(p, sm.len_s, r), nb = r2 < p.NRD && row_needed_s(p, sm.len_s, r2);
-      if (!na && !nb) continue;
-      RowStat xa, xb;
-      merge_rows(p, b, na ? r : r2, (na && nb) ? r2 : -1, xa, xb);
-      if (lane == 0) {
-        const int ra = na ? r : r2;
-        sm.st[ra] = xa;
-        if (rank == 0) p.stat[static_cast<int64_t>(b) * p.NRD + ra] = xa;
-        if (na && nb) {
-          sm.st[r2] = xb;
-          if (rank == 0) p.stat[static_cast<int64_t>(b) * p.NRD + r2] = xb;
-        }
-      }
-    }
+    // ---- 2. every needed row merged from its pieces (rank 0 keeps the merged rows for the
+    //         diagnostic copy of p)
+    merge_needed_rows<4>(p, b, sm.len_s, sm.st, warp, kFinWarps);
     __syncthreads();
+    if (rank == 0)
+      for (int r = tid; r < p.NRD; r += blockDim.x)
+        if (row_needed_s(p, sm.len_s, r)) p.stat[static_cast<int64_t>(b) * p.NRD + r] = sm.st[r];
 
     // ---- 3. acceptance, leading runs, longest block, stop row (outputs by rank 0)
 #pragma unroll
@@ -1058,7 +886,6 @@ constexpr int kWideMaxCTAs = 16;             // ... and up to 512 chunks (a non-
 constexpr int kWideThreads = 1024;
 constexpr int kWideWarps = kWideThreads / 32;
 constexpr int kWideSlotsPer = kMaxSlots / kWideThreads;
-constexpr int kWideMaxChunks = kWideMaxCTAs * kWideWarps;   // one chunk per warp of the cluster
 constexpr size_t kWideDynSmem = 2ull * kWideWarps * kSampleChunk * sizeof(float);
 
 struct __align__(16) WideSmem {
@@ -1138,24 +965,13 @@ k_accept_finish_wide(AcceptParams p) {
     __syncthreads();
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the piece statistics are complete
 
-    // ---- 2. every needed row merged from its pieces, two rows per warp pass
-    for (int r = warp; r < p.NRD; r += 2 * kWideWarps) {
-      const int r2 = r + kWideWarps;
-      const bool na = row_needed_s(p, sm.len_s, r), nb = r2 < p.NRD && row_needed_s(p, sm.len_s, r2);
-      if (!na && !nb) continue;
-      RowStat xa, xb;
-      merge_rows(p, b, na ? r : r2, (na && nb) ? r2 : -1, xa, xb);
-      if (lane == 0) {
-        const int ra = na ? r : r2;
-        sm.st[ra] = xa;
-        if (rank == 0) p.stat[static_cast<int64_t>(b) * p.NRD + ra] = xa;
-        if (na && nb) {
-          sm.st[r2] = xb;
-          if (rank == 0) p.stat[static_cast<int64_t>(b) * p.NRD + r2] = xb;
-        }
-      }
-    }
+    // ---- 2. every needed row merged from its pieces (rank 0 keeps the merged rows for the
+    //         diagnostic copy of p)
+    merge_needed_rows<3>(p, b, sm.len_s, sm.st, warp, kWideWarps);
     __syncthreads();
+    if (rank == 0)
+      for (int r = tid; r < p.NRD; r += blockDim.x)
+        if (row_needed_s(p, sm.len_s, r)) p.stat[static_cast<int64_t>(b) * p.NRD + r] = sm.st[r];
 
     // ---- 3. acceptance, leading runs, longest block, stop row (outputs by rank 0)
 #pragma unroll
@@ -1495,49 +1311,10 @@ AcceptParams accept_params(const ssd_accept_args* a, const AcceptLayout& L, char
   return p;
 }
 
-// SSD_ROWS_KERNEL=stream selects the copy-engine-fed row pass (measured slower than the
-// register-fed one on the 42 MB row pass of the Llama-3.1-8B-shaped step: 18.3 against
-// 14.3 µs per launch; kept as a tested alternative)
-static bool stream_enabled_by_env() {
-  const char* e = getenv("SSD_ROWS_KERNEL");
-  return e != nullptr && e[0] == 's';
-}
-
-// rows the copy engine can bring in: 16-byte aligned starts, whole 16-byte units
-static bool stream_rows_ok(const AcceptParams& p) {
-  const int64_t es = p.bf16 ? 2 : 4;
-  if (((p.V * es) & 15) != 0 || !aligned(p.tgt, 16)) return false;
-  return p.K == 0 || p.drf == nullptr || aligned(p.drf, 16);
-}
-
-// the copy-engine-fed stats kernel: one CTA per SM (or per task, if fewer)
-template <bool BF16, bool AMAX>
-static cudaError_t launch_stream(const AcceptParams& p, cudaStream_t s) {
-  static std::once_flag once[kMaxDevices];
-  static int sms[kMaxDevices];
-  static cudaError_t err[kMaxDevices];
-  const int dev = current_device();
-  if (dev < 0) return cudaErrorInvalidDevice;
-  std::call_once(once[dev], [dev] {
-    sms[dev] = 0;
-    err[dev] = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-    if (err[dev] == cudaSuccess)
-      err[dev] = cudaFuncSetAttribute(k_vocab_stream<BF16, AMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      static_cast<int>(kStreamSmem));
-  });
-  if (err[dev] != cudaSuccess) return err[dev];
-  const long long ntask = static_cast<long long>(p.nch) * p.NRD * p.B;
-  long long g = ntask < sms[dev] ? ntask : sms[dev];
-  if (p.max_ctas > 0 && g > p.max_ctas) g = p.max_ctas;
-  return launch_pdl(k_vocab_stream<BF16, AMAX>, dim3(static_cast<unsigned>(g > 0 ? g : 1)), dim3(kStreamThreads),
-                    kStreamSmem, s, p);
-}
-
 // the stats kernel: a grid of as many CTAs as are resident at once, or with max_ctas one
 // CTA of 16 warps per SM on at most max_ctas SMs
 template <bool BF16, bool AMAX>
 static cudaError_t launch_stats(const AcceptParams& p, cudaStream_t s) {
-  if (stream_rows_ok(p) && stream_enabled_by_env()) return launch_stream<BF16, AMAX>(p, s);
   static std::once_flag once[kMaxDevices];
   static long long cap[kMaxDevices];
   static int sms[kMaxDevices];
@@ -1558,8 +1335,28 @@ static cudaError_t launch_stats(const AcceptParams& p, cudaStream_t s) {
     return launch_pdl(k_vocab_stats<BF16, AMAX, 16>, dim3(static_cast<unsigned>(g > 0 ? g : 1)), dim3(512), 0, s, p);
   }
   const long long want = (ntask + 7) / 8;
-  const dim3 g1(static_cast<unsigned>(want < cap[dev] ? want : cap[dev]));
-  return launch_pdl(k_vocab_stats<BF16, AMAX, 8>, g1, dim3(256), 0, s, p);
+  long long g = want < cap[dev] ? want : cap[dev];
+  // early mode: clusters of 8 CTAs. A grid launched behind a running kernel
+  // (programmatic dependent launch) reaches its SMs about 40 CTAs per microsecond when
+  // its CTAs come one by one, in about two thirds of that time as clusters (304 CTAs:
+  // 7.6 against 5.9 us), which shortens the Llama-3.1-8B-shaped step; the needed-rows
+  // mode of the large batches measured slower as clusters (182 -> 280 us at batch 32)
+  const unsigned cl = (p.early && g >= 64) ? 8u : 1u;
+  if (cl > 1) g = g / cl * cl;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(g));
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cl;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = cl > 1 ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, k_vocab_stats<BF16, AMAX, 8>, p);
 }
 
 int accept_launch(const AcceptParams& p, cudaStream_t s) {
@@ -1695,8 +1492,7 @@ extern "C" int ssd_accept_static(const ssd_accept_args* a, void* stream) {
   const int rc = static_scratch(&ws);
   if (rc != SSD_OK) return rc;
   // Nothing in the scratch has to start at zero: the row pass writes every partial
-  // row statistic and the finish kernel every merged one before either is read. The
-  // error header at its start keeps the first device-side error until
+  // row statistic and the finish kernel every merged one before either is read. The error header at its start keeps the first device-side error until
   // ssd_read_static_error reads and clears it (the array starts zeroed at load).
   const AcceptParams p = accept_params(a, L, static_cast<char*>(ws));
   return accept_launch(p, static_cast<cudaStream_t>(stream));

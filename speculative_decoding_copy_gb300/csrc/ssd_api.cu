@@ -18,6 +18,29 @@ extern "C" const char* ssd_status_string(int status) {
 extern "C" int ssd_version(void) { return 100; }
 
 namespace ssd {
+static CheckWordReader g_check_readers[32];
+static int g_check_reader_count = 0;
+void register_check_word(CheckWordReader f) {
+  if (g_check_reader_count < 32) g_check_readers[g_check_reader_count++] = f;
+}
+}  // namespace ssd
+
+extern "C" int ssd_checked_build(void) { return SSD_CHECKS ? 1 : 0; }
+
+extern "C" int ssd_read_check_error(void* stream, int32_t* out) {
+  if (out == nullptr) return SSD_ERR_INVALID;
+  int32_t first = SSD_OK;
+  for (int i = 0; i < ssd::g_check_reader_count; ++i) {
+    int32_t w = SSD_OK;
+    const int rc = ssd::g_check_readers[i](static_cast<cudaStream_t>(stream), &w);
+    if (rc != SSD_OK) return rc;
+    if (first == SSD_OK) first = w;
+  }
+  *out = first;
+  return SSD_OK;
+}
+
+namespace ssd {
 ProfileHook g_profile;
 }
 

@@ -66,7 +66,8 @@ k_attn_prefix_simt(AttnParams p) {
   const int NT = p.NB * p.Dmax;
   const int rows_total = NT * G;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int P = p.prefix_len[b];
+  int P = p.prefix_len[b];
+  if (!in_range(P, p.P_max + 1, p.hdr, 28)) P = 0;       // a prefix longer than the cache
   const int k0 = split * p.chunk;
   const int k1 = min(P, k0 + p.chunk);
 

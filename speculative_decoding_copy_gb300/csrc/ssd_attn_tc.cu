@@ -42,6 +42,7 @@
 #include <cuda.h>
 #include <math.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "ssd_attn.cuh"
@@ -181,7 +182,9 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
   const int NT = p.NB * p.Dmax;
   const int rows_total = NT * G;
   const int r0 = mt * BM;
-  const int P = p.prefix_len[b];
+  int P = p.prefix_len[b];
+  // a prefix longer than the cache would read another sequence's (or head's) keys
+  if (!in_range(P, (p.block_table != nullptr ? 128LL * p.pages_per_seq : p.P_max) + 1, p.hdr, 27)) P = 0;
   // split 0 also takes the own-block tiles, so its share of the prefix is shorter
   const int k0 = split == 0 ? 0 : p.chunk0 + (split - 1) * p.chunk;
   const int k1 = min(P, k0 + (split == 0 ? p.chunk0 : p.chunk));
@@ -484,12 +487,12 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
   }
   if (warp == 4) {
     // which owned rows belong to tokens that exist: blk_len comes from the retrieval, which
-    // precedes this kernel in the stream
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // precedes this kernel in the stream (with all_rows every slot's row is written)
+    if (!p.all_rows) asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int i = lane; i < nr; i += 32) {
       const int gr = r0 + rb + i;
       const int tt = gr / G;
-      bars.exists[i] = (tt % p.Dmax) < __ldcg(p.blk_len + b * p.NB + tt / p.Dmax) ? 1 : 0;
+      bars.exists[i] = p.all_rows ? 1 : ((tt % p.Dmax) < __ldcg(p.blk_len + b * p.NB + tt / p.Dmax) ? 1 : 0);
     }
   }
   __syncthreads();
@@ -653,8 +656,13 @@ static void choose_split(const ssd_attn_args* a, int mtiles, int* S_out, int* ch
   long long best_cost = -1;
   int best_S = 1;
   for (int S = 1; S <= kMaxSplit && S <= nkt; ++S) {
-    const int active = max_active_clusters(S);
+    int active = max_active_clusters(S);
     if (active <= 0) continue;
+    if (a->max_ctas > 0) {
+      // a grid of at most max_ctas CTAs (whole clusters, at least one per row tile)
+      if (S > 1 && groups * S > a->max_ctas) continue;
+      active = static_cast<int>(std::min<long long>(active, std::max<long long>(1, a->max_ctas / S)));
+    }
     const long long tiles = (nkt + 2 * nc + S - 1) / S;
     const long long waves = (groups + active - 1) / active;
     const long long cost = waves * (tiles + 2) * 16 + S;   // +2 tiles: prologue and merge
@@ -735,6 +743,7 @@ int attn_tc_launch(const ssd_attn_args* a, void* ws, cudaStream_t s) {
   p.pages_per_seq = a->pages_per_seq;
   p.num_pages = a->num_pages;
   p.skip_absent = a->skip_absent;
+  p.all_rows = a->all_rows;
   p.hdr = reinterpret_cast<WsHeader*>(ws);
 
   cudaLaunchConfig_t cfg = {};

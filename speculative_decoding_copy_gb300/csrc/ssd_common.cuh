@@ -108,6 +108,57 @@ __device__ __forceinline__ void record_error(WsHeader* h, int code, int where) {
   if (h != nullptr && atomicCAS(&h->err, 0, code) == 0) h->where = where;
 }
 
+// ---------------------------------------------------------------- checked builds
+// A build with -DSSD_CHECKS=1 (libssd_checked.so) tests every guarded index against the
+// extent it must stay within before the access; a failed test records SSD_ERR_DEVICE with
+// `where` in the call's workspace header (when the call has one) and in the check word of
+// the translation unit (read with ssd_read_check_error), and the access is skipped. In the
+// normal build the tests compile away.
+#ifndef SSD_CHECKS
+#define SSD_CHECKS 0
+#endif
+#if SSD_CHECKS
+static __device__ WsHeader g_check_word;
+#endif
+
+__device__ __forceinline__ bool in_range(long long i, long long n, WsHeader* hdr, int where) {
+#if SSD_CHECKS
+  if (i >= 0 && i < n) return true;
+  record_error(hdr, SSD_ERR_DEVICE, where);
+  record_error(&g_check_word, SSD_ERR_DEVICE, where);
+  return false;
+#else
+  (void)i; (void)n; (void)hdr; (void)where;
+  return true;
+#endif
+}
+
+// host: every translation unit of a checked build registers a reader of its check word
+typedef int (*CheckWordReader)(cudaStream_t s, int32_t* out);
+void register_check_word(CheckWordReader f);
+#if SSD_CHECKS
+static int read_check_word(cudaStream_t s, int32_t* out) {
+  void* a = nullptr;
+  if (cudaGetSymbolAddress(&a, g_check_word) != cudaSuccess) return SSD_ERR_CUDA;
+  int32_t w[2] = {0, 0};
+  if (cudaMemcpyAsync(w, a, sizeof w, cudaMemcpyDeviceToHost, s) != cudaSuccess) return SSD_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SSD_ERR_CUDA;
+  if (w[0] != 0) {
+    const int32_t z[2] = {0, 0};
+    if (cudaMemcpyAsync(a, z, sizeof z, cudaMemcpyHostToDevice, s) != cudaSuccess) return SSD_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SSD_ERR_CUDA;
+  }
+  *out = w[0];
+  return SSD_OK;
+}
+namespace {
+struct CheckWordRegistration {
+  CheckWordRegistration() { register_check_word(&read_check_word); }
+};
+static CheckWordRegistration g_check_word_registration;
+}  // namespace
+#endif
+
 // One probe of an mbarrier phase (shared memory of this CTA): true once the phase of the
 // given parity has completed.
 __device__ __forceinline__ bool mbar_probe(uint64_t* bar, uint32_t parity) {

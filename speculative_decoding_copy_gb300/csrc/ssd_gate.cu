@@ -82,7 +82,8 @@ k_front(const int32_t* __restrict__ ctx, int64_t stride, const int32_t* __restri
   const float* hf = static_cast<const float*>(h) + b * h_stride;
 
   // ---- 1. loads that do not depend on the context length: ctx_len, the first probe pass
-  const int n = __ldg(ctx_len + b);
+  int n = __ldg(ctx_len + b);
+  if (!in_range(n, stride + 1, nullptr, 200)) n = 0;          // a length past the row: nothing is read
   float hv[kProbePer], wv[kProbePer];
   if (GATE) {
 #pragma unroll
@@ -149,7 +150,7 @@ k_front(const int32_t* __restrict__ ctx, int64_t stride, const int32_t* __restri
       }
       __syncthreads();
       if (j_hi == n - 2) {   // the final kappa-gram ctx[n-kappa .. n-1] lies in the first chunk's tile
-        if (tid < kappa) s.g[tid] = s.tile[n - kappa + tid - base];
+        if (tid < kappa && in_range(n - kappa + tid - base, cnt, nullptr, 201)) s.g[tid] = s.tile[n - kappa + tid - base];
         __syncthreads();
       }
       const int before = s.nfound;
@@ -197,7 +198,8 @@ k_front(const int32_t* __restrict__ ctx, int64_t stride, const int32_t* __restri
         for (int idx = tid; idx < (r_hi - r_lo) * D; idx += kFrontThreads) {
           const int rr = r_lo + idx / D, q = idx - (idx / D) * D;
           const int j = s.ends[rr];
-          if (q < min(D, n - 1 - j))
+          if (q < min(D, n - 1 - j) && in_range(j + 1 + q - base, cnt, nullptr, 202) &&
+              in_range(rr * Dmax + q, static_cast<long long>(NB) * Dmax, nullptr, 203))
             blk_tok[(static_cast<int64_t>(b) * NB + rr) * Dmax + q] = s.tile[j + 1 + q - base];
         }
       }

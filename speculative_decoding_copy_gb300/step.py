@@ -153,7 +153,7 @@ class VerifyStep:
                               self.x["v_cand"], self.x["prefix_len"], self.ret_out["blk_len"], wl.Dmax,
                               self.attn_out, skip_absent=self.skip_absent, all_rows=self.all_rows,
                               max_ctas=self.attn_ctas)
-            self.attn_ws = torch.empty(max(256, ssd.ssd_verify_attn_workspace_size(a)), dtype=torch.uint8,
+            self.attn_ws = torch.zeros(max(256, ssd.ssd_verify_attn_workspace_size(a)), dtype=torch.uint8,
                                        device=self.device)
 
     # -------------------------------------------------------------------
