@@ -45,7 +45,11 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama8b")
-    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--e2e-steps", type=int, default=100, help="0 leaves out the end-to-end measurement")
+    ap.add_argument("--copies", type=int, default=0,
+                    help="input copies that rotate through the timed graphs (0: enough for more than twice "
+                         "the L2, at least 3); 1 keeps a small device footprint for profiler captures of "
+                         "workloads far larger than the L2")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-next", action="store_true",
                     help="skip the measurements of the rows after the step (commit, paged cache, tax, head) "
@@ -512,7 +516,7 @@ def run_ours(args):
     blk_len = probe.ret_out["blk_len"].cpu().numpy()
     prefix = inp["prefix_len"]
     ab = WL.algorithmic_bytes(wl, prefix, blk_len)
-    R = max(3, min(16, math.ceil(2 * L2_BYTES / max(ab["total"], 1)) + 1))
+    R = args.copies or max(3, min(16, math.ceil(2 * L2_BYTES / max(ab["total"], 1)) + 1))
     steps = [probe] + [VerifyStep(wl, inp, device=dev, **kw) for _ in range(R - 1)]
     tokens = ab["tokens"]
     K = args.steps
@@ -556,7 +560,7 @@ def run_ours(args):
     del full, seq, full_h, seq_h
 
     # end to end through the public API with host buffers
-    e2e = run_e2e(args, wl, inp, steps[0], main, aux, dev, world)
+    e2e = run_e2e(args, wl, inp, steps[0], main, aux, dev, world) if args.e2e_steps > 0 else None
     nxt = None if args.no_next else {
            "commit_kv": measure_commit(wl, main, dev), "paged_attn": measure_paged(wl, steps[0], main, dev),
            "spec_tax": measure_tax(main, dev), "slimspec_head": measure_head(main, dev)}
@@ -576,7 +580,8 @@ def run_ours(args):
                 "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16/f32", "data": "synthetic",
                 "config": workload_config(wl, tokens, {
-                    "l2": f"{R} rotating input copies ({R * ab['total'] / 2**20:.0f} MiB > 2x L2); no flush",
+                    "l2": f"{R} rotating input copies ({R * ab['total'] / 2**20:.0f} MiB"
+                          f"{' > 2x L2' if R * ab['total'] > 2 * L2_BYTES else ', NOT above 2x L2'}); no flush",
                     "timing": f"median of {REPEATS} timed repeats of the K-step region (each bracketed by a "
                               f"barrier, a synchronize and CUDA events); value and ms_per_step from the median",
                     "parallelism": f"replicas x{world} (independent batches per GPU)",

@@ -121,7 +121,8 @@ __device__ __forceinline__ long long block_excl_scan(long long v, long long* war
 // k_vocab_stats: every warp streams whole pieces of 2048 entries of the rows
 // some token needs (8 KB of fp32 or 4 KB of bf16: 16 or 8 16-byte loads per
 // lane, all in flight together) and reduces each piece alone with warp
-// shuffles; two CTAs of 8 warps per SM keep up to 128 KB of loads in flight per SM.
+// shuffles; two CTAs of 8 warps per SM (one of 16 warps under max_ctas) keep up to
+// 128 KB of loads in flight per SM.
 constexpr int kPieceElems = 2048;
 template <bool BF16>
 struct Piece {

@@ -419,6 +419,8 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
   // is idle) S-1 threads each send one other CTA the rows it owns with one bulk copy,
   // completing on that CTA's mbarrier. Every owner thread then weights and sums the S copies
   // (its own split's rows where they were staged) and writes the rows of tokens that exist.
+  // (Owners reading the peers' staged rows in place with distributed shared memory loads,
+  // with a second cluster barrier before exit, made the step 2 us slower.)
   // Ring layout (bytes): staged rows [BM][kRowB], received rows [sender split][rpc][kRowB].
   uint8_t* stage = smem + OFF_RING;
   uint8_t* recv = stage + BM * kRowB;
