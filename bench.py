@@ -343,9 +343,11 @@ KERNEL_SOURCES = {"vocab_stats": ("ssd_accept.cu", "ssd_accept.cuh", "ssd_common
                   "verify_attn": ("ssd_attn.cu", "ssd_attn_tc.cu", "ssd_attn.cuh", "ssd_tc.cuh", "ssd_common.cuh")}
 
 
-def dram_traffic(kernel, workload):
+def dram_traffic(kernel, workload, alg_bytes=None):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on the
-    current kernel source; else None."""
+    current kernel source; else None. Where the capture's inputs differ from this
+    launch's (same shapes, other draws), its bytes are scaled by the ratio of the two
+    launches' algorithmic bytes."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p) or kernel not in KERNEL_SOURCES:
         return None
@@ -354,7 +356,11 @@ def dram_traffic(kernel, workload):
     e = d.get(f"{kernel}/{workload}")
     if not e or e.get("source_sha") != source_sha(*KERNEL_SOURCES[kernel]):
         return None
-    return e.get("dram_bytes_per_launch")
+    b = e.get("dram_bytes_per_launch")
+    a = e.get("algorithmic_bytes_per_launch")
+    if b is not None and a and alg_bytes and alg_bytes != a:
+        return round(b * alg_bytes / a)
+    return b
 
 
 REPEATS = 7          # timed repeats of the K-step region; the reported step time is their median
@@ -466,13 +472,13 @@ def kernel_roofline(dom, dom_us, wl, ab, blk_len, prefix, hbm, peak_kind, tf_bur
     if t_tc > t_hbm:
         ach = kf[dom] / (dom_us * 1e-6) / 1e12 if dom_us else None
         return {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": tf_burst, "unit": "TFLOP/s",
-                "frac": (ach / tf_burst) if ach else None, "traffic": dram_traffic(dom, wl.name),
+                "frac": (ach / tf_burst) if ach else None, "traffic": dram_traffic(dom, wl.name, kb[dom]),
                 "algorithmic_flops_per_launch": kf[dom], "algorithmic_bytes_per_launch": kb[dom],
                 "launch_us": dom_us, "timing": timing,
                 "peak_source": f"{tf_kind} bf16_tflops (cuBLAS bf16 GEMM, burst: the kernel runs in "
                                f"sub-millisecond regions)",
                 "hbm_view": hbm_view}
-    return dict(hbm_view, kernel=dom, traffic=dram_traffic(dom, wl.name), launch_us=dom_us, timing=timing)
+    return dict(hbm_view, kernel=dom, traffic=dram_traffic(dom, wl.name, kb[dom]), launch_us=dom_us, timing=timing)
 
 
 def step_record(wl, ab, ms_list, K, world, hbm):

@@ -210,7 +210,9 @@ int ssd_gate_retrieve(const int32_t* ctx, int64_t ctx_stride, const int32_t* ctx
  * attention of its q over the prefix and the slots k*Dmax .. t of its block
  * (what the row of a present token holds), and never reads blk_len (it may be
  * NULL), so the call depends on no earlier kernel's output and may run on
- * another stream beside the retrieval. Requires skip_absent == 0.
+ * another stream beside the retrieval. On its own stream it still completes
+ * after the kernel issued before it (it waits for that kernel only after its
+ * rows are written). Requires skip_absent == 0.
  * max_ctas (>= 0): 0 lets the call use the whole GPU; n > 0 sizes the
  * tensor-core grid to at most max(n, clusters of one CTA) CTAs, one per SM, so
  * that a kernel on another stream can hold the remaining SMs at the same time.

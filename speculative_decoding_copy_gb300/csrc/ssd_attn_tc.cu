@@ -570,6 +570,9 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
+  // with all_rows nothing above waited for the kernel before this one: one thread waits for
+  // it here, after the rows are written, so that this grid still completes after it
+  if (p.all_rows && tid == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ host

@@ -24,10 +24,13 @@ batches whose gate sends sequences to the chain draft. In the "attn_first" order
 attention's main loop starts while the retrieval still runs and the row pass, in its
 early mode, streams beside it (measured slower; kept as an option).
 
-In the "split" order the attention writes every slot's row (all_rows), so it depends on
-no earlier kernel of the step: it starts on an auxiliary stream together with the
-retrieval, on at most attn_ctas SMs, while the retrieval, the row pass (early mode, at
-most rows_ctas SMs of one CTA each) and the finish kernel run on the main stream.
+Unless skip_absent is on, the attention writes every slot's row (all_rows): it reads
+nothing that the step's earlier kernels write, so on one stream its merge does not
+wait for the finish kernel to complete (it waits only before the grid ends, after its
+rows are written). In the "split" order it therefore starts on an auxiliary stream
+together with the retrieval, on at most attn_ctas SMs, while the retrieval, the row
+pass (early mode, at most rows_ctas SMs of one CTA each) and the finish kernel run on
+the main stream.
 
 Inputs may sit in one device arena (arena_bytes), so that a caller refreshes all of
 them with a single host-to-device copy. The step issues only library calls; it
@@ -106,7 +109,9 @@ class VerifyStep:
         self.skip_absent = (wl.chain_policy == 1 and wl.B > 1) if skip_absent is None else bool(skip_absent)
         if order == "split":
             self.skip_absent = False          # the attention reads nothing from the retrieval
-        self.all_rows = order == "split"
+        # without skip_absent the attention writes every slot's row: it then reads nothing the
+        # step's earlier kernels write and waits for them only after its last row is written
+        self.all_rows = not self.skip_absent
         self.mode = ssd.SSD_SAMPLE if (mode or wl.mode) == "sample" else ssd.SSD_GREEDY
         if kind is None:
             kind = ssd.SSD_LOGITS_BF16 if wl.logit_dtype == "bf16" else ssd.SSD_LOGITS_F32
