@@ -216,7 +216,11 @@ int ssd_gate_retrieve(const int32_t* ctx, int64_t ctx_stride, const int32_t* ctx
  * max_ctas (>= 0): 0 lets the call use the whole GPU; n > 0 sizes the
  * tensor-core grid to at most max(n, clusters of one CTA) CTAs, one per SM, so
  * that a kernel on another stream can hold the remaining SMs at the same time.
- * Workspace: ssd_verify_attn_workspace_size(a) bytes, 256-byte aligned; its
+ * Workspace: ssd_verify_attn_workspace_size(a) bytes, 256-byte aligned: 256
+ * bytes where the tensor-core path applies (bf16, dh 128, 16-byte aligned
+ * tensors, a GPU of compute capability 10.3), else room for every split's
+ * partial rows; the size is that of the path the same arguments (pointers
+ * included) take on the current device. Its
  * contents need no initialisation for the results. Device-side errors are recorded
  * in its first word, which keeps whatever it held before: zero the header (its first
  * 256 bytes) once after allocating it, or read it once with ssd_read_device_error,

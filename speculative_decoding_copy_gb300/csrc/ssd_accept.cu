@@ -268,20 +268,24 @@ k_vocab_stats(AcceptParams p) {
   // blk_len comes from the retrieval; once it is in, the next kernel of the stream may
   // start (its prologue reads the retrieval's outputs, never this kernel's). The early
   // mode reads no blk_len: every CTA but the last lets the next kernel start at once;
-  // the last CTA first waits for the preceding kernel. So the next kernel starts only
-  // once that kernel (and what it waited for) has completed, and this grid completes
-  // only after it: the next kernel's wait then covers them all.
+  // the last CTA takes no pieces: it waits for the preceding kernel, lets the next one
+  // start and leaves. So the next kernel starts only once that kernel (and what it
+  // waited for) has completed, and this grid completes only after it: the next kernel's
+  // wait then covers them all. (With pieces of its own as well, the waiting CTA, which
+  // starts its pieces only after the retrieval, ended about 5 us after the others.)
   // The workspace may still be read by the kernel before this one (the finish kernel of
   // an earlier call on the same workspace, which lets this grid launch at its start), so
   // no CTA writes it before griddepcontrol.wait: in the early mode each warp keeps up to
   // 32 piece results in its lanes and waits only before its first store.
-  bool waited = !p.early || blockIdx.x == gridDim.x - 1;
+  const bool waiter = p.early && blockIdx.x == gridDim.x - 1;
+  bool waited = !p.early || waiter;
   if (waited) asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (waiter) return;
   constexpr int es = BF16 ? 2 : 4;
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * WARPS + (threadIdx.x >> 5);
-  const int TW = gridDim.x * WARPS;
+  const int TW = (gridDim.x - (p.early ? 1 : 0)) * WARPS;    // the early mode's last CTA takes none
   const int ntask = p.nch * p.NRD * p.B;
   const int per = kPieceElems;
   const bool vec_rows = ((p.V * es) & 15) == 0;
@@ -1330,13 +1334,17 @@ static cudaError_t launch_stats(const AcceptParams& p, cudaStream_t s) {
     sms[dev] = n;
   });
   const long long ntask = static_cast<long long>(p.nch) * p.NRD * p.B;
+  // the early mode adds the CTA that only waits (at least one other takes the pieces)
+  const int extra = p.early ? 1 : 0;
   if (p.max_ctas > 0) {
-    const long long want = (ntask + 15) / 16;
-    const long long g = std::min<long long>(want, std::min<long long>(p.max_ctas, sms[dev]));
-    return launch_pdl(k_vocab_stats<BF16, AMAX, 16>, dim3(static_cast<unsigned>(g > 0 ? g : 1)), dim3(512), 0, s, p);
+    const long long want = (ntask + 15) / 16 + extra;
+    long long g = std::min<long long>(want, std::min<long long>(p.max_ctas, sms[dev]));
+    if (g < 1 + extra) g = 1 + extra;
+    return launch_pdl(k_vocab_stats<BF16, AMAX, 16>, dim3(static_cast<unsigned>(g)), dim3(512), 0, s, p);
   }
-  const long long want = (ntask + 7) / 8;
+  const long long want = (ntask + 7) / 8 + extra;
   long long g = want < cap[dev] ? want : cap[dev];
+  if (g < 1 + extra) g = 1 + extra;
   // early mode: clusters of 8 CTAs. A grid launched behind a running kernel
   // (programmatic dependent launch) reaches its SMs about 40 CTAs per microsecond when
   // its CTAs come one by one, in about two thirds of that time as clusters (304 CTAs:

@@ -344,9 +344,10 @@ using namespace ssd;
 extern "C" size_t ssd_verify_attn_workspace_size(const ssd_attn_args* a) {
   if (validate(a) != SSD_OK) return 0;
   if (a->B == 0) return sizeof(WsHeader);
-  size_t s = attn_layout(a).total;
-  size_t t = attn_tc_workspace_size(a);
-  return s > t ? s : t;
+  // the path the call will take: the tensor-core kernel merges on chip and needs only the
+  // header; the SIMT passes keep every split's partial rows
+  if (attn_tc_applies(a)) return attn_tc_workspace_size(a);
+  return attn_layout(a).total;
 }
 
 extern "C" int ssd_verify_attn(const ssd_attn_args* a, void* ws, size_t ws_bytes, void* stream) {

@@ -13,20 +13,22 @@
 //   warps 0-3  one thread per packed row: online softmax of a 128-key tile read
 //              from TMEM (tcgen05.ld), masked to a contiguous key range; O is
 //              rescaled in TMEM when the row max grows; P goes back to TMEM as
-//              bf16 pairs (tcgen05.st), where the P V product reads it as its
-//              A operand;
-//   warp 4     TMEM allocation, then the TMA producer: Q (a 4-D map lays the G
-//              heads of 128/G tokens out as 128 rows) and a 3-stage ring of K
-//              and V tiles of 128 keys (two 64-wide halves of the head dim,
-//              128-byte swizzle), from the prefix cache (2-D map) or the
-//              candidate keys (3-D map);
+//              bf16 pairs (tcgen05.st) over the first half of the tile's S
+//              buffer, where the P V product reads it as its A operand;
+//   warp 4     TMEM allocation, then the TMA producer of Q (a 4-D map lays the G
+//              heads of 128/G tokens out as 128 rows) and of the K tiles;
+//   warp 6     the TMA producer of the V tiles. K and V tiles of 128 keys (two
+//              64-wide halves of the head dim, 128-byte swizzle) share a 3-stage
+//              ring, from the prefix cache (2-D map) or the candidate keys (3-D
+//              map); a stage's K half is refilled once Q K^T of its tile is done,
+//              its V half once P V is;
 //   warp 5     the single MMA-issuing thread: S = Q K^T (M128 N128, eight K16
-//              steps, both operands in shared memory) into one of two TMEM
-//              buffers, two tiles ahead of the softmax, and O += P V (M128
+//              steps, both operands in shared memory) into one of three TMEM
+//              buffers, three tiles ahead of the softmax, and O += P V (M128
 //              N128, eight K16 steps, A from TMEM, V MN-major in shared memory);
-//   warps 6-11 wait at the first cluster barrier and add threads to the merge.
-// TMEM columns: S buffers 0-127 and 128-255, O 256-383, P buffers 384-447 and
-// 448-511.
+//   warps 6-11 (warp 6 after its loads) add threads to the merge.
+// TMEM columns: S buffers 0-127, 128-255 and 256-383 (P of a tile in the first 64
+// columns of its buffer), O 384-511.
 // Merge: each row's un-normalised O is staged in the CTA's idle ring as 16-bit
 // integers, one power-of-two scale per 64-column half (warps 0-3 stage columns
 // 0-63, warps 6-9 columns 64-127), with the row's max and sum; after a cluster
@@ -57,10 +59,11 @@ constexpr int BN = 128;                   // keys per tile
 constexpr int STAGES = 3;                 // K/V ring depth
 constexpr int kThreads = 384;            // 6 role warps + 6 that join for the merge
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t TM_S = 0;              // two S buffers of BN columns
-constexpr uint32_t TM_O = 2 * BN;         // O: DH columns
-constexpr uint32_t TM_P = TM_O + DH;      // two P buffers of BN/2 columns (bf16 pairs)
-static_assert(TM_P + BN <= kTmemCols, "TMEM budget");
+constexpr int SBUF = 3;                   // S buffers: S runs three tiles ahead of the softmax
+constexpr uint32_t TM_S = 0;              // SBUF S buffers of BN columns; P of a tile overwrites
+                                          // the first BN/2 columns of its S buffer (bf16 pairs)
+constexpr uint32_t TM_O = SBUF * BN;      // O: DH columns
+static_assert(TM_O + DH <= kTmemCols, "TMEM budget");
 constexpr uint32_t kHalf = 128 * 128;     // 128 rows x 64 bf16, one 128-byte-swizzled half: 16 KB
 constexpr uint32_t kStage = 4 * kHalf;    // K and V tiles, two halves each: 64 KB
 constexpr uint32_t OFF_Q = 0;
@@ -71,9 +74,9 @@ constexpr uint32_t kSmemBytes = OFF_BAR + kBarBytes + 1024;   // + slack to alig
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 constexpr unsigned long long kWaitClocks = 1ull << 32;
 struct Bars {
-  uint64_t full_k[STAGES], full_v[STAGES], empty[STAGES];
+  uint64_t full_k[STAGES], full_v[STAGES], empty_k[STAGES], empty_v[STAGES];
   uint64_t q_full;
-  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
+  uint64_t s_full[SBUF], p_full[SBUF], pv_done[2];
   uint64_t recv_full;                     // every other split's copy of the owned rows has arrived
   uint32_t tmem_base;
   int failed;
@@ -228,16 +231,16 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&bars.full_k[s], 1);
       mbar_init(&bars.full_v[s], 1);
-      mbar_init(&bars.empty[s], 1);
+      mbar_init(&bars.empty_k[s], 1);
+      mbar_init(&bars.empty_v[s], 1);
     }
     mbar_init(&bars.q_full, 1);
     mbar_init(&bars.recv_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < SBUF; ++i) {
       mbar_init(&bars.s_full[i], 1);
-      mbar_init(&bars.s_free[i], BM);
       mbar_init(&bars.p_full[i], BM);
-      mbar_init(&bars.pv_done[i], 1);
     }
+    for (int i = 0; i < 2; ++i) mbar_init(&bars.pv_done[i], 1);
     bars.failed = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -263,8 +266,8 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
     const int c_lo = (t / p.Dmax) * p.Dmax;
     const float sl2 = p.scale_log2;
     for (int j = 0; j < nT; ++j) {
-      const int sb = j & 1;
-      mbar_wait(bars, &bars.s_full[sb], (j >> 1) & 1, p.hdr, 10);
+      const int sb = j % SBUF;
+      mbar_wait(bars, &bars.s_full[sb], (j / SBUF) & 1, p.hdr, 10);
       tc_fence_after();
       // valid columns: a contiguous range [v_lo, v_hi) of this tile
       int v_lo, v_hi;
@@ -288,20 +291,14 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
       const bool need = m_new > m + 8.f;
       const float mref = need ? m_new : m;
       const float alpha = need ? ex2_approx(m - m_new) : 1.f;
-      // P buffer sb was last read by the P V product of tile j-2
-      if (j >= 2) {
-        mbar_wait(bars, &bars.pv_done[sb], ((j - 2) >> 1) & 1, p.hdr, 12);
-        tc_fence_after();
-      }
-      // pass 2: P = 2^(s*scale - mref) as bf16 pairs into TMEM, and its row sum
-      const uint32_t pc = tmem + TM_P + sb * (BN / 2) + lane_off;
+      // pass 2: P = 2^(s*scale - mref) as bf16 pairs into the first BN/2 columns of the
+      // same buffer (64 columns of S are read before their 32 columns of P are written, and
+      // the columns written hold S already read), and its row sum
       float rs = 0.f;
 #pragma unroll 1
       for (int h = 0; h < BN / 64; ++h)
-        rs += full ? chunk_exp<false>(sc + h * 64, pc + h * 32, 0, 0, sl2, mref)
-                   : chunk_exp<true>(sc + h * 64, pc + h * 32, v_lo - h * 64, v_hi - h * 64, sl2, mref);
-      tc_fence_before();
-      mbar_arrive(&bars.s_free[sb]);                 // S of this tile is no longer read
+        rs += full ? chunk_exp<false>(sc + h * 64, sc + h * 32, 0, 0, sl2, mref)
+                   : chunk_exp<true>(sc + h * 64, sc + h * 32, v_lo - h * 64, v_hi - h * 64, sl2, mref);
       if (j > 0 && __any_sync(0xffffffffu, need)) {
         // O holds the sum up to tile j-1: wait for its last MMA, then rescale
         mbar_wait(bars, &bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, p.hdr, 11);
@@ -326,27 +323,34 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
       mbar_wait(bars, &bars.pv_done[(nT - 1) & 1], ((nT - 1) >> 1) & 1, p.hdr, 13);
       tc_fence_after();
     }
-  } else if (warp == 4) {
-    // ---------------------------------------------------------- TMA producer
+  } else if (warp == 4 || warp == 6) {
+    // ---------------------------------------------------------- TMA producers
+    // warp 4 loads Q and the K tiles, warp 6 the V tiles: a K slot is free once the
+    // S = Q K^T product of its tile has completed, a V slot only after P V, so the K of
+    // a later tile is not held back behind the V of an earlier one
+    const bool kside = warp == 4;
     if (lane == 0 && nT > 0) {
-      mbar_expect_tx(&bars.q_full, 2 * kHalf);
-      const int qz = b * NT + t_first;                     // rows past the sequence are masked or zero
-      tma_load_4d(sbase + OFF_Q, &tmap_q, 0, 0, kvh, qz, &bars.q_full);
-      tma_load_4d(sbase + OFF_Q + kHalf, &tmap_q, 64, 0, kvh, qz, &bars.q_full);
+      if (kside) {
+        mbar_expect_tx(&bars.q_full, 2 * kHalf);
+        const int qz = b * NT + t_first;                   // rows past the sequence are masked or zero
+        tma_load_4d(sbase + OFF_Q, &tmap_q, 0, 0, kvh, qz, &bars.q_full);
+        tma_load_4d(sbase + OFF_Q + kHalf, &tmap_q, 64, 0, kvh, qz, &bars.q_full);
+      }
       const int y0 = p.block_table != nullptr ? 0 : (b * p.Hkv + kvh) * static_cast<int>(p.P_max) + k0;
+      const CUtensorMap* cand_map = kside ? &tmap_kc : &tmap_vc;
+      const CUtensorMap* pref_map = kside ? &tmap_k : &tmap_v;
       for (int j = 0; j < nT; ++j) {
         const int s = j % STAGES;
-        if (j >= STAGES) mbar_wait(bars, &bars.empty[s], ((j / STAGES) - 1) & 1, p.hdr, 20);
+        uint64_t* empty = kside ? &bars.empty_k[s] : &bars.empty_v[s];
+        uint64_t* full = kside ? &bars.full_k[s] : &bars.full_v[s];
+        if (j >= STAGES) mbar_wait(bars, empty, ((j / STAGES) - 1) & 1, p.hdr, kside ? 20 : 21);
         if (bars.failed) break;
-        const uint32_t kd = sbase + OFF_RING + s * kStage, vd = kd + 2 * kHalf;
-        mbar_expect_tx(&bars.full_k[s], 2 * kHalf);
+        const uint32_t dst = sbase + OFF_RING + s * kStage + (kside ? 0u : 2 * kHalf);
+        mbar_expect_tx(full, 2 * kHalf);
         if (j < nC) {
           const int z = b * NT + s_base + j * BN;          // candidate slot (rows past NT are masked)
-          tma_load_3d(kd, &tmap_kc, 0, kvh, z, &bars.full_k[s]);
-          tma_load_3d(kd + kHalf, &tmap_kc, 64, kvh, z, &bars.full_k[s]);
-          mbar_expect_tx(&bars.full_v[s], 2 * kHalf);
-          tma_load_3d(vd, &tmap_vc, 0, kvh, z, &bars.full_v[s]);
-          tma_load_3d(vd + kHalf, &tmap_vc, 64, kvh, z, &bars.full_v[s]);
+          tma_load_3d(dst, cand_map, 0, kvh, z, full);
+          tma_load_3d(dst + kHalf, cand_map, 64, kvh, z, full);
         } else {
           int y = y0 + (j - nC) * BN;
           if (p.block_table != nullptr) {
@@ -358,19 +362,18 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
             }
             y = (pg * p.Hkv + kvh) * BN;
           }
-          tma_load_2d(kd, &tmap_k, 0, y, &bars.full_k[s]);
-          tma_load_2d(kd + kHalf, &tmap_k, 64, y, &bars.full_k[s]);
-          mbar_expect_tx(&bars.full_v[s], 2 * kHalf);
-          tma_load_2d(vd, &tmap_v, 0, y, &bars.full_v[s]);
-          tma_load_2d(vd + kHalf, &tmap_v, 64, y, &bars.full_v[s]);
+          tma_load_2d(dst, pref_map, 0, y, full);
+          tma_load_2d(dst + kHalf, pref_map, 64, y, full);
         }
       }
     }
+    __syncwarp();                                   // warp 6 joins the merge converged
   } else if (warp == 5) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0 && nT > 0) {
       constexpr uint32_t idS = idesc_bf16(false, BN), idPV = idesc_bf16(true, DH);
-      // S[jj & 1] = Q K_jj^T : M128 N128, eight K16 steps over the head dim
+      // S[jj % SBUF] = Q K_jj^T : M128 N128, eight K16 steps over the head dim; its K slot is
+      // free once these products complete
       auto issue_S = [&](int jj) {
         const int s = jj % STAGES;
         mbar_wait(bars, &bars.full_k[s], (jj / STAGES) & 1, p.hdr, 31);
@@ -380,33 +383,31 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
         for (int ks = 0; ks < DH / 16; ++ks) {
           const uint64_t a = sw128_desc(sbase + OFF_Q + (ks >> 2) * kHalf + (ks & 3) * 32, 16, 1024);
           const uint64_t bd = sw128_desc(kb + (ks >> 2) * kHalf + (ks & 3) * 32, 16, 1024);
-          mma_bf16(tmem + TM_S + (jj & 1) * BN, a, bd, idS, ks > 0 ? 1u : 0u);
+          mma_bf16(tmem + TM_S + (jj % SBUF) * BN, a, bd, idS, ks > 0 ? 1u : 0u);
         }
-        mma_commit(&bars.s_full[jj & 1]);
+        mma_commit(&bars.s_full[jj % SBUF]);
+        mma_commit(&bars.empty_k[s]);
       };
       mbar_wait(bars, &bars.q_full, 0, p.hdr, 30);
-      issue_S(0);
-      if (nT > 1) issue_S(1);
+      for (int jj = 0; jj < SBUF && jj < nT; ++jj) issue_S(jj);
       for (int j = 0; j < nT; ++j) {
         // O += P_j V_j : M128 N128 (head dim), eight K16 steps over the tile's keys, P from TMEM
         const int s = j % STAGES;
-        mbar_wait(bars, &bars.p_full[j & 1], (j >> 1) & 1, p.hdr, 34);
+        mbar_wait(bars, &bars.p_full[j % SBUF], (j / SBUF) & 1, p.hdr, 34);
         mbar_wait(bars, &bars.full_v[s], (j / STAGES) & 1, p.hdr, 35);
         tc_fence_after();
         const uint32_t vb = sbase + OFF_RING + s * kStage + 2 * kHalf;
-        const uint32_t pa = tmem + TM_P + (j & 1) * (BN / 2);
+        const uint32_t pa = tmem + TM_S + (j % SBUF) * BN;
 #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks) {
           const uint64_t bd = sw128_desc(vb + ks * 16 * 128, kHalf, 1024);
           mma_bf16_ts(tmem + TM_O, pa + ks * 8, bd, idPV, (j > 0 || ks > 0) ? 1u : 0u);
         }
         mma_commit(&bars.pv_done[j & 1]);
-        mma_commit(&bars.empty[s]);
-        // S of tile j+2 into the buffer the softmax of tile j has read
-        if (j + 2 < nT) {
-          mbar_wait(bars, &bars.s_free[j & 1], (j >> 1) & 1, p.hdr, 33);
-          issue_S(j + 2);
-        }
+        mma_commit(&bars.empty_v[s]);
+        // S of tile j+SBUF into the buffer that holds P_j: the products of one thread run in
+        // the order issued, so the P V product above has read P_j before it is overwritten
+        if (j + SBUF < nT) issue_S(j + SBUF);
       }
     }
   }
