@@ -22,12 +22,12 @@ def _as_f64(x, dtype):
         return O.to_f64(x, dtype)
 
 
-def _run_attn(case, blk_len, Dmax, dtype, out_f32=False):
+def _run_attn(case, blk_len, Dmax, dtype, out_f32=False, max_ctas=0):
     dev = "cuda"
     t = {k: to_device(np.asarray(v), dev) for k, v in case.items()}
     bl = to_device(blk_len, dev)
     out = S.ssd_verify_attn(t["q"], t["k_cache"], t["v_cache"], t["k_cand"], t["v_cand"], t["prefix_len"], bl, Dmax,
-                            out_f32=out_f32)
+                            out_f32=out_f32, max_ctas=max_ctas)
     torch.cuda.synchronize()
     o = out.cpu()
     return o.numpy() if (dtype == "f32" or out_f32) else o.view(torch.int16).numpy().view(np.uint16)
@@ -43,8 +43,8 @@ def _case(rng, B, NB, Dmax, Hq, Hkv, dh, prefix, dtype, q_scale=1.0):
                 prefix_len=np.asarray(prefix, np.int32))
 
 
-def _check_all(case, blk_len, Dmax, dtype, slots=None, out_f32=False):
-    got = _run_attn(case, blk_len, Dmax, dtype, out_f32)
+def _check_all(case, blk_len, Dmax, dtype, slots=None, out_f32=False, max_ctas=0):
+    got = _run_attn(case, blk_len, Dmax, dtype, out_f32, max_ctas)
     ref = O.verify_attention(case["q"], case["k_cache"], case["v_cache"], case["k_cand"], case["v_cand"],
                              case["prefix_len"], blk_len, Dmax, dtype, slots)
     g = _as_f64(got, "f32" if out_f32 else dtype)
@@ -77,6 +77,35 @@ def test_attention_sharp_and_long(dtype):
     case = _case(rng, 2, 2, 8, 8, 2, 128, [2049, 4100], dtype, q_scale=4.0)
     blk_len = np.array([[8, 3], [6, 8]], np.int32)
     _check_all(case, blk_len, 8, dtype, out_f32=True)
+
+
+@pytest.mark.parametrize("G", [1, 4])
+@pytest.mark.parametrize("max_ctas", [0, 2])
+def test_attention_reference_jumps(G, max_ctas):
+    """Planted keys whose scores jump far above every earlier key of their row (by about
+    20, 40 and 65 in log2 units), each in the second half of its 128-key tile and in
+    ever later tiles (0, 4 and 10), so that the running reference max moves several
+    times and the sum so far is rescaled each time. With max_ctas = 2 each kv head's row
+    tile is one CTA that walks the whole prefix (no split), so every jump happens inside
+    one running sum."""
+    rng = np.random.default_rng(70 + G)
+    Hkv, B, NB, Dmax = 2, 1, 2, 4
+    Hq, dh, P = Hkv * G, 128, 1500
+    NT = NB * Dmax
+    u = rng.standard_normal(dh)
+    u /= np.linalg.norm(u)
+    q = 0.3 * rng.standard_normal((B, NT, Hq, dh)) + 3.0 * u
+    k = 0.3 * rng.standard_normal((B, Hkv, P, dh))
+    for pos, beta in ((100, 52.0), (600, 110.0), (1350, 170.0)):   # columns 100, 88, 70 of tiles 0, 4, 10
+        k[:, :, pos, :] = beta * u
+    cast = WL.f32_to_bf16_bits
+    case = dict(q=cast(q.astype(np.float32)), k_cache=cast(k.astype(np.float32)),
+                v_cache=cast(rng.standard_normal((B, Hkv, P, dh)).astype(np.float32)),
+                k_cand=cast(rng.standard_normal((B, NT, Hkv, dh)).astype(np.float32)),
+                v_cand=cast(rng.standard_normal((B, NT, Hkv, dh)).astype(np.float32)),
+                prefix_len=np.array([P], np.int32))
+    blk_len = np.array([[4, 2]], np.int32)
+    _check_all(case, blk_len, Dmax, "bf16", out_f32=True, max_ctas=max_ctas)
 
 
 def test_attention_tiny_workload():
