@@ -63,11 +63,15 @@ __device__ __forceinline__ long long weight_of(float p) {
   return sh <= -24 ? 0 : (mant >> (-sh));
 }
 
+// (m, s) += (m2, s2) with one exponential: the side with the larger max keeps its sum as is
+// (both lanes of a shuffle pair form the same two terms, so they agree bit for bit)
 __device__ __forceinline__ void stat_merge(float& m, float& s, float m2, float s2) {
-  const float M = fmaxf(m, m2);
-  if (M == -INFINITY) return;
-  s = s * ex2_approx((m - M) * kLog2e) + s2 * ex2_approx((m2 - M) * kLog2e);
-  m = M;
+  if (m2 > m) {
+    s = s * ex2_approx((m - m2) * kLog2e) + s2;   // m = -inf: s is 0 and 2^-inf = 0
+    m = m2;
+  } else if (m2 > -INFINITY) {
+    s += s2 * ex2_approx((m2 - m) * kLog2e);
+  }
 }
 
 __device__ __forceinline__ void amax_merge(float& v, int& i, float v2, int i2) {
@@ -159,7 +163,9 @@ __device__ __forceinline__ RowStat reduce_piece(const void* row, int n, int e0, 
 #pragma unroll
     for (int j = 0; j < kPieceVec; ++j) {
       const int vi = j * 32 + lane;
-      v[j] = (FULL || vi < nv) ? __ldg(src + vi) : make_uint4(0, 0, 0, 0);
+      // streaming loads (evict first): the logits are read once, and the piece statistics
+      // this grid writes should stay in L2 for the finish kernel while the rows stream by
+      v[j] = (FULL || vi < nv) ? __ldcs(src + vi) : make_uint4(0, 0, 0, 0);
     }
   } else {
 #pragma unroll
@@ -387,13 +393,11 @@ __device__ __forceinline__ bool row_needed_s(const AcceptParams& p, const int* l
   return p.chain_blk >= 0 && (r - p.NR) < len_s[p.chain_blk];
 }
 
-
-
-
 // Statistics of the needed rows of sequence b merged from their pieces into st[], every
 // warp taking rows warp, warp + nw, ... with the loads of all its rows issued before any
-// merge (one round trip to L2 for up to kRowsPerWarp rows); rows beyond that loop.
-template <int kRowsPerWarp>
+// merge (one round trip to L2 for up to kRowsPerWarp rows of up to 32 kLoadsPerRow pieces);
+// rows and pieces beyond that loop.
+template <int kRowsPerWarp, int kLoadsPerRow>
 __device__ __forceinline__ void merge_needed_rows(const AcceptParams& p, int b, const int* len_s, RowStat* st,
                                                   int warp, int nw) {
   const int lane = threadIdx.x & 31;
@@ -407,15 +411,15 @@ __device__ __forceinline__ void merge_needed_rows(const AcceptParams& p, int b, 
       av[q] = -INFINITY;
       ai[q] = 0x7fffffff;
     }
-    for (int c0 = 0; c0 < p.nch; c0 += 64) {
-      float4 v[kRowsPerWarp][2];
+    for (int c0 = 0; c0 < p.nch; c0 += 32 * kLoadsPerRow) {
+      float4 v[kRowsPerWarp][kLoadsPerRow];
 #pragma unroll
       for (int q = 0; q < kRowsPerWarp; ++q) {
         const int r = r0 + q * nw;
         const bool need = r < p.NRD && row_needed_s(p, len_s, r);
         const RowStat* src = p.part + (static_cast<int64_t>(b) * p.NRD + (need ? r : 0)) * p.nch;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < kLoadsPerRow; ++h) {
           const int c = c0 + h * 32 + lane;
           v[q][h] = (need && c < p.nch) ? __ldcg(reinterpret_cast<const float4*>(src + c))
                                         : make_float4(-INFINITY, 0.f, -INFINITY, __int_as_float(0x7fffffff));
@@ -424,7 +428,7 @@ __device__ __forceinline__ void merge_needed_rows(const AcceptParams& p, int b, 
 #pragma unroll
       for (int q = 0; q < kRowsPerWarp; ++q)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < kLoadsPerRow; ++h) {
           stat_merge(M[q], S[q], v[q][h].x, v[q][h].y);
           amax_merge(av[q], ai[q], v[q][h].z, __float_as_int(v[q][h].w));
         }
@@ -477,6 +481,38 @@ __device__ __forceinline__ long long draw_weight(float pv, const DrawRow& pr, bo
 }
 
 __device__ __forceinline__ float f4(const float4& v, int e) { return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w; }
+
+// Sums over one lane's run of a chunk (kChunkVec float4 of the target row `a`, and of the draft
+// row `q` when HAS_Q): sp = the bonus weights P, sw = the residual max(0, P - Q) with HAS_Q,
+// else P. Each weight is formed once. P and Q are kept as (hi, lo) = value hi 2^20 + lo with
+// lo < 2^20, so P - Q = (hi_P - hi_Q) 2^20 + (lo_P - lo_Q) with the low difference inside
+// (-2^20, 2^20): it is positive exactly when the high difference is, or when that is zero and
+// the low one is positive. Sums of kLaneEntries entries fit the 32-bit parts.
+template <bool HAS_Q>
+__device__ __forceinline__ void lane_weight_sums(const float4 (&a)[kChunkVec], const float4 (&q)[kChunkVec],
+                                                 const DrawRow& pr, const DrawRow& qr, long long& sp, long long& sw) {
+  uint32_t phi = 0, plo = 0;
+  int32_t whi = 0, wlo = 0;
+#pragma unroll
+  for (int j = 0; j < kChunkVec; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const Split P = weight_split(f4(a[j], e), pr);
+      phi += P.hi;
+      plo += P.lo;
+      if (HAS_Q) {
+        const Split Q = weight_split(f4(q[j], e), qr);
+        const int32_t dh = static_cast<int32_t>(P.hi) - static_cast<int32_t>(Q.hi);
+        const int32_t dl = static_cast<int32_t>(P.lo) - static_cast<int32_t>(Q.lo);
+        if (dh > 0 || (dh == 0 && dl > 0)) {
+          whi += dh;
+          wlo += dl;
+        }
+      }
+    }
+  sp = (static_cast<long long>(phi) << 20) + static_cast<long long>(plo);
+  sw = HAS_Q ? (static_cast<long long>(whi) << 20) + static_cast<long long>(wlo) : sp;
+}
 
 // this lane's entries [lo + lane*kLaneEntries, + kLaneEntries) of a row as kChunkVec float4
 // (entry k of the run is component k%4 of v[k/4]); entries past the row end are -inf
@@ -572,7 +608,7 @@ k_accept_finish_batch(AcceptParams p) {
 
     // ---- 2. every needed row merged from its pieces (rank 0 keeps the merged rows for the
     //         diagnostic copy of p)
-    merge_needed_rows<4>(p, b, sm.len_s, sm.st, warp, kFinWarps);
+    merge_needed_rows<4, 2>(p, b, sm.len_s, sm.st, warp, kFinWarps);
     __syncthreads();
     if (rank == 0)
       for (int r = tid; r < p.NRD; r += blockDim.x)
@@ -689,32 +725,14 @@ k_accept_finish_batch(AcceptParams p) {
     };
     auto lane_sums = [&](int cc, const float4 (&a)[kChunkVec], const float4 (&q)[kChunkVec], long long& sw,
                          long long& sp) {
-      const int64_t l0 = static_cast<int64_t>(cc) * kSampleChunk + static_cast<int64_t>(lane) * kLaneEntries;
-      uint32_t shi = 0, slo = 0;
-#pragma unroll
-      for (int j = 0; j < kChunkVec; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const Split w = weight_split(f4(a[j], e), pr);
-          shi += w.hi;
-          slo += w.lo;
-        }
-      sp = (static_cast<long long>(shi) << 20) + static_cast<long long>(slo);
-      if (si.bonus) {
-        sw = sp;
-      } else if (has_q) {
-        sw = 0;
-#pragma unroll
-        for (int j = 0; j < kChunkVec; ++j)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const long long P = split64(weight_split(f4(a[j], e), pr));
-            const long long Q = split64(weight_split(f4(q[j], e), qr));
-            sw += P > Q ? P - Q : 0LL;
-          }
-      } else {
+      if (has_q && !si.bonus) {
+        lane_weight_sums<true>(a, q, pr, qr, sp, sw);
+        return;
+      }
+      lane_weight_sums<false>(a, q, pr, qr, sp, sw);
+      if (!si.bonus) {
         // a rejected copy token: W = P everywhere but there, where Q = 2^40
-        sw = sp;
+        const int64_t l0 = static_cast<int64_t>(cc) * kSampleChunk + static_cast<int64_t>(lane) * kLaneEntries;
         const int64_t xl = static_cast<int64_t>(si.excl) - l0;
         if (xl >= 0 && xl < kLaneEntries) {
           float pe = 0.f;
@@ -909,7 +927,6 @@ struct __align__(16) WideSmem {
   long long t_rem;
 };
 
-
 __global__ void __launch_bounds__(kWideThreads, 1)
 k_accept_finish_wide(AcceptParams p) {
   __shared__ WideSmem sm;
@@ -972,7 +989,7 @@ k_accept_finish_wide(AcceptParams p) {
 
     // ---- 2. every needed row merged from its pieces (rank 0 keeps the merged rows for the
     //         diagnostic copy of p)
-    merge_needed_rows<3>(p, b, sm.len_s, sm.st, warp, kWideWarps);
+    merge_needed_rows<3, 2>(p, b, sm.len_s, sm.st, warp, kWideWarps);
     __syncthreads();
     if (rank == 0)
       for (int r = tid; r < p.NRD; r += blockDim.x)
@@ -1089,34 +1106,17 @@ k_accept_finish_wide(AcceptParams p) {
         load_lane_run(p, prow, lo, a);
 #pragma unroll
         for (int j = 0; j < kChunkVec; ++j) reinterpret_cast<float4*>(pf)[j] = a[j];
-        uint32_t shi = 0, slo = 0;
-#pragma unroll
-        for (int j = 0; j < kChunkVec; ++j)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const Split w = weight_split(f4(a[j], e), pr);
-            shi += w.hi;
-            slo += w.lo;
-          }
-        sp = (static_cast<long long>(shi) << 20) + static_cast<long long>(slo);
-        if (si.bonus) {
-          sw = sp;
-        } else if (has_q) {
+        if (has_q && !si.bonus) {
           float4 q[kChunkVec];
           load_lane_run(p, qrow, lo, q);
 #pragma unroll
-          for (int j = 0; j < kChunkVec; ++j) {
-            reinterpret_cast<float4*>(qf)[j] = q[j];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const long long P = split64(weight_split(f4(a[j], e), pr));
-              const long long Q = split64(weight_split(f4(q[j], e), qr));
-              sw += P > Q ? P - Q : 0LL;
-            }
-          }
+          for (int j = 0; j < kChunkVec; ++j) reinterpret_cast<float4*>(qf)[j] = q[j];
+          lane_weight_sums<true>(a, q, pr, qr, sp, sw);
         } else {
+          lane_weight_sums<false>(a, a, pr, qr, sp, sw);
+        }
+        if (!si.bonus && !has_q) {
           // a rejected copy token: W = P everywhere but there, where Q = 2^40
-          sw = sp;
           const int64_t xl = static_cast<int64_t>(si.excl) - l0;
           if (xl >= 0 && xl < kLaneEntries) {
             const long long Pe = split64(weight_split(pf[xl], pr));
@@ -1224,7 +1224,6 @@ k_accept_finish_wide(AcceptParams p) {
   }
   // no peer writes to this CTA after the last cluster barrier of its sequences
 }
-
 
 // ------------------------------------------------------------------ diagnostics
 __global__ void __launch_bounds__(kVocabThreads)
