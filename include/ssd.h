@@ -47,6 +47,16 @@
  *     NB = number of blocks, Dmax = slots per block, NT = NB * Dmax.
  *   - Calls are safe from several host threads on distinct streams with
  *     distinct output and workspace buffers.
+ *   - Stream order: the kernels after the first of a call sequence are launched
+ *     with programmatic dependent launch, so a kernel may start before the
+ *     kernel issued before it on the same stream has completed. It completes
+ *     only after that kernel, it writes nothing that kernel may still read or
+ *     write, and results are those of strictly ordered calls. It may read the
+ *     caller's inputs early (the logits in ssd_accept's early_rows mode; with
+ *     all_rows, everything ssd_verify_attn reads). The retrieval kernels
+ *     (ssd_gate_match, ssd_retrieve, ssd_gate_retrieve) are ordinary launches:
+ *     they start only after everything before them on the stream, so a step
+ *     that begins with them sees every earlier write.
  */
 #ifndef SSD_H
 #define SSD_H

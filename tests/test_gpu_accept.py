@@ -384,6 +384,50 @@ def test_gpu_sampler_chi_square(V):
     assert pval > 0.01, (chi2, pval)
 
 
+@pytest.mark.parametrize("name", ["tiny", "llama8b"])
+def test_steps_back_to_back_with_new_inputs(name):
+    """Steps issued back to back on one stream and one set of buffers, the inputs replaced
+    in place between them (ordinary copies on the same stream): the kernels of a step may
+    start while the previous step's kernels still run, and each step's results must be
+    those of its own inputs."""
+    wl = WL.WORKLOADS[name]
+    inps = [WL.make_inputs(wl, 300 + k, full_width=False) for k in range(3)]
+    st = VerifyStep(wl, inps[0], early_rows=True)
+    main = torch.cuda.Stream()
+    got = []
+    with torch.cuda.stream(main):
+        for k, inp in enumerate(inps):
+            if k > 0:
+                for key, t in st.x.items():
+                    t.copy_(to_device(inp[key], t.device).view(t.dtype).view(t.shape), non_blocking=False)
+            st.run(main)
+            got.append({key: v.clone() for key, v in {**st.ret_out, **st.acc_out}.items()})
+            if st.with_attention:
+                got[-1]["attn"] = st.attn_out.clone()
+    torch.cuda.synchronize()
+    for inp, g in zip(inps, got):
+        ref = O.verify_step(inp, wl, attention_slots=None)
+        for key in ("blk_tok", "blk_len", "n_cand"):
+            np.testing.assert_array_equal(g[key].cpu().numpy(), ref[key], err_msg=key)
+        kind = "logits_bf16" if wl.logit_dtype == "bf16" else "logits_f32"
+        res = {key: g[key].cpu().numpy() for key in ("acc_len", "best_blk", "n_out", "out_tok")}
+        for b in range(wl.B):
+            same = all(np.array_equal(res[key][b], ref[key][b]) for key in res)
+            if not same:
+                assert _margins_explain(kind, inp["tgt"], inp.get("drf"), ref["blk_tok"], ref["blk_len"], wl.W,
+                                        wl.chain_policy, inp["u_acc"], inp["u_fin"], res, ref, b)
+        if "attn" in g:
+            bl = ref["blk_len"]
+            slots = [(b, k * wl.Dmax + d) for b in range(wl.B) for k in range(wl.NB) for d in range(bl[b, k])][:24]
+            ra = O.verify_attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["k_cand"], inp["v_cand"],
+                                    inp["prefix_len"], bl, wl.Dmax, wl.kv_dtype, slots)
+            ga = g["attn"].cpu()
+            ga = ga.numpy() if wl.kv_dtype == "f32" else ga.view(torch.int16).numpy().view(np.uint16)
+            with np.errstate(invalid="ignore"):
+                ga = O.to_f64(ga, wl.kv_dtype)
+            assert max(float(np.max(np.abs(ga[b, t] - o))) for (b, t), o in ra.items()) <= 1e-2
+
+
 def test_step_from_one_input_arena_matches_separate_inputs():
     """The inputs placed in one arena (refreshed by a single host-to-device copy) give
     the same step results as separately allocated inputs."""
