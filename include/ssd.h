@@ -47,9 +47,9 @@
  *     NB = number of blocks, Dmax = slots per block, NT = NB * Dmax.
  *   - Calls are safe from several host threads on distinct streams with
  *     distinct output and workspace buffers.
- *   - Stream order: the kernels after the first of a call sequence are launched
- *     with programmatic dependent launch, so a kernel may start before the
- *     kernel issued before it on the same stream has completed. It completes
+ *   - Stream order: most kernels are launched with programmatic dependent
+ *     launch, so such a kernel may start before the kernel issued before it on
+ *     the same stream has completed. It completes
  *     only after that kernel, it writes nothing that kernel may still read or
  *     write, and results are those of strictly ordered calls. It may read the
  *     caller's inputs early (the logits in ssd_accept's early_rows mode; with
