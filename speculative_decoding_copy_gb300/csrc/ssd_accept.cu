@@ -252,11 +252,21 @@ __device__ __forceinline__ RowStat warp_merge_stat(float M, float S, float av, i
   return RowStat{M, S, av, ai};
 }
 
-// next task (sequence, row, piece) at or after t, in steps of `step`, whose row
-// some token needs (every row in the early mode), or ntask; tasks are numbered
-// ((b * NRD) + r) * nch + c
+// next task (sequence, row, piece) at or after t, in steps of `step`, whose row some
+// token needs (in the early mode every row a block length can reach), or ntask; tasks
+// are numbered ((b * NRD) + r) * nch + c
 __device__ __forceinline__ int next_task(const AcceptParams& p, int t, int step, int ntask) {
-  if (p.early) return t < ntask ? t : ntask;
+  if (p.early) {
+    // every row but the chain block's rows at positions K and beyond, which no block
+    // length can reach (the chain block holds at most K tokens)
+    const int c0 = p.chain_blk >= 0 ? 1 + p.chain_blk * p.Dmax + p.K : 0;
+    const int c1 = p.chain_blk >= 0 ? 1 + (p.chain_blk + 1) * p.Dmax : 0;
+    for (; t < ntask; t += step) {
+      const int r = (t / p.nch) % p.NRD;
+      if (r < c0 || r >= c1) break;
+    }
+    return t < ntask ? t : ntask;
+  }
   for (; t < ntask; t += step) {
     const int br = t / p.nch;
     const int b = br / p.NRD, r = br - b * p.NRD;
