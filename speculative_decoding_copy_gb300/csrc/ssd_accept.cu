@@ -63,15 +63,14 @@ __device__ __forceinline__ long long weight_of(float p) {
   return sh <= -24 ? 0 : (mant >> (-sh));
 }
 
-// (m, s) += (m2, s2) with one exponential: the side with the larger max keeps its sum as is
-// (both lanes of a shuffle pair form the same two terms, so they agree bit for bit)
+// (m, s) += (m2, s2) with one exponential and no branch: the side with the larger max keeps
+// its sum as is, the other is scaled by 2^((min - max) log2 e) (0 when the smaller max is
+// -inf). Both lanes of a shuffle pair form the same two terms, so they agree bit for bit.
 __device__ __forceinline__ void stat_merge(float& m, float& s, float m2, float s2) {
-  if (m2 > m) {
-    s = s * ex2_approx((m - m2) * kLog2e) + s2;   // m = -inf: s is 0 and 2^-inf = 0
-    m = m2;
-  } else if (m2 > -INFINITY) {
-    s += s2 * ex2_approx((m2 - m) * kLog2e);
-  }
+  const float hi = fmaxf(m, m2), lo = fminf(m, m2);
+  const float e = lo > -INFINITY ? ex2_approx((lo - hi) * kLog2e) : 0.f;
+  s = m2 > m ? fmaf(s, e, s2) : fmaf(s2, e, s);
+  m = hi;
 }
 
 __device__ __forceinline__ void amax_merge(float& v, int& i, float v2, int i2) {
@@ -239,15 +238,20 @@ __device__ __forceinline__ RowStat reduce_vecs(const uint4 (&v)[Piece<BF16>::kVe
   return RowStat{M, S, av, ai};
 }
 
+// AMAX = false (sample mode, where no decision reads the argmax): max and sum only, half the
+// shuffles
+template <bool AMAX>
 __device__ __forceinline__ RowStat warp_merge_stat(float M, float S, float av, int ai) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float m2 = __shfl_xor_sync(0xffffffffu, M, o);
     const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
-    const float v2 = __shfl_xor_sync(0xffffffffu, av, o);
-    const int i2 = __shfl_xor_sync(0xffffffffu, ai, o);
     stat_merge(M, S, m2, s2);
-    amax_merge(av, ai, v2, i2);
+    if (AMAX) {
+      const float v2 = __shfl_xor_sync(0xffffffffu, av, o);
+      const int i2 = __shfl_xor_sync(0xffffffffu, ai, o);
+      amax_merge(av, ai, v2, i2);
+    }
   }
   return RowStat{M, S, av, ai};
 }
@@ -407,7 +411,7 @@ __device__ __forceinline__ bool row_needed_s(const AcceptParams& p, const int* l
 // warp taking rows warp, warp + nw, ... with the loads of all its rows issued before any
 // merge (one round trip to L2 for up to kRowsPerWarp rows of up to 32 kLoadsPerRow pieces);
 // rows and pieces beyond that loop.
-template <int kRowsPerWarp, int kLoadsPerRow>
+template <int kRowsPerWarp, int kLoadsPerRow, bool AMAX>
 __device__ __forceinline__ void merge_needed_rows(const AcceptParams& p, int b, const int* len_s, RowStat* st,
                                                   int warp, int nw) {
   const int lane = threadIdx.x & 31;
@@ -440,13 +444,13 @@ __device__ __forceinline__ void merge_needed_rows(const AcceptParams& p, int b, 
 #pragma unroll
         for (int h = 0; h < kLoadsPerRow; ++h) {
           stat_merge(M[q], S[q], v[q][h].x, v[q][h].y);
-          amax_merge(av[q], ai[q], v[q][h].z, __float_as_int(v[q][h].w));
+          if (AMAX) amax_merge(av[q], ai[q], v[q][h].z, __float_as_int(v[q][h].w));
         }
     }
 #pragma unroll
     for (int q = 0; q < kRowsPerWarp; ++q) {
       const int r = r0 + q * nw;
-      const RowStat x = warp_merge_stat(M[q], S[q], av[q], ai[q]);
+      const RowStat x = warp_merge_stat<AMAX>(M[q], S[q], av[q], ai[q]);
       if (lane == 0 && r < p.NRD && row_needed_s(p, len_s, r)) st[r] = x;
     }
   }
@@ -618,7 +622,8 @@ k_accept_finish_batch(AcceptParams p) {
 
     // ---- 2. every needed row merged from its pieces (rank 0 keeps the merged rows for the
     //         diagnostic copy of p)
-    merge_needed_rows<4, 2>(p, b, sm.len_s, sm.st, warp, kFinWarps);
+    if (p.sample) merge_needed_rows<4, 2, false>(p, b, sm.len_s, sm.st, warp, kFinWarps);
+    else merge_needed_rows<4, 2, true>(p, b, sm.len_s, sm.st, warp, kFinWarps);
     __syncthreads();
     if (rank == 0)
       for (int r = tid; r < p.NRD; r += blockDim.x)
@@ -999,7 +1004,8 @@ k_accept_finish_wide(AcceptParams p) {
 
     // ---- 2. every needed row merged from its pieces (rank 0 keeps the merged rows for the
     //         diagnostic copy of p)
-    merge_needed_rows<3, 2>(p, b, sm.len_s, sm.st, warp, kWideWarps);
+    if (p.sample) merge_needed_rows<3, 2, false>(p, b, sm.len_s, sm.st, warp, kWideWarps);
+    else merge_needed_rows<3, 2, true>(p, b, sm.len_s, sm.st, warp, kWideWarps);
     __syncthreads();
     if (rank == 0)
       for (int r = tid; r < p.NRD; r += blockDim.x)
