@@ -293,8 +293,9 @@ int ssd_verify_attn(const ssd_attn_args* a, void* ws, size_t ws_bytes, void* str
  *     needed target row is written there (diagnostics; costs a full write)
  *   early_rows: 0 — the row pass waits for the kernel before it on the stream
  *     (the retrieval that wrote blk_len) and reads only the rows a present
- *     token needs; 1 — it starts at once and reads every target row (and
- *     every draft row when chain_blk >= 0), so that it overlaps the kernel
+ *     token needs; 1 — it starts at once and reads every target row a block
+ *     length can reach (all but the chain block's rows at positions K and
+ *     beyond) and every draft row when chain_blk >= 0, so that it overlaps the kernel
  *     launched just before it (the retrieval, or an attention launched after
  *     the retrieval); blk_tok and blk_len are read only after that kernel has
  *     completed, and the call's last kernel starts only then. Results are

@@ -15,9 +15,10 @@
 //                   some token needs (16-byte loads, all in flight together) and
 //                   reduces each to max, argmax (greedy only; lowest index on
 //                   ties) and sum of 2^((l - max) log2 e) with warp shuffles; in
-//                   the early mode it streams every row without waiting for the
-//                   kernel before it (it only stores after that wait), and only
-//                   its last CTA waits before letting the next kernel launch;
+//                   the early mode it streams every row a block length can reach
+//                   without waiting for the kernel before it (it only stores after
+//                   that wait), and only its last CTA, which takes no pieces, waits
+//                   before letting the next kernel launch;
 //   k_accept_finish_wide / k_accept_finish_batch  per sequence (one cluster each):
 //                   merges every needed row's pieces, runs the acceptance test
 //                   of every candidate token and picks the longest accepted block,
