@@ -53,3 +53,23 @@ def test_two_ranks_gloo():
     assert s0 != s1 and d0 != d1                      # independent batches
     assert ms0 == ms1 == 15.0                          # every rank reports the slowest time
     assert v0 == v1 == pytest.approx(2 * 100 / 0.015)  # steps of both ranks per second
+
+
+def test_gpus_flag_starts_its_own_ranks():
+    """`bench.py --gpus 2` outside torchrun starts two ranks itself (torch.distributed.run,
+    rendezvous on 127.0.0.1); with the reference arm only rank 0 works and prints, and the
+    other rank exits 0 without work. Runs on the CPU (the reference arm is the oracle)."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR",
+                                                           "MASTER_PORT")}
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2", "--impl", "reference",
+                        "--workload", "tiny", "--steps", "1", "--warmup", "0"], cwd=root, env=env,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
