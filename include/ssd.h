@@ -208,14 +208,20 @@ int ssd_gate_retrieve(const int32_t* ctx, int64_t ctx_stride, const int32_t* ctx
  * prefix_len[b] <= 128 * pages_per_seq; pages may be shared by sequences). A page
  * index outside [0, num_pages) records SSD_ERR_DEVICE and reads page 0. P_max is
  * then unused.
- * skip_absent (0 or 1; tensor-core path only, ignored by the fp32 / head-dim-64
- * pass): 1 makes every CTA first wait for the kernel before it on the stream
- * (the one whose outputs include blk_len, or a later one) and then skip a tile
- * of 128 packed rows in which no token is present, e.g. the copy-block rows of
- * a sequence whose gate is off. Outputs are identical; the attention then no
- * longer overlaps the tail of that preceding kernel, so it pays off only when
- * many candidate slots are empty. 0: every tile is computed, blk_len is read
- * only before the merge.
+ * skip_absent (0, 1 or 2; tensor-core path only, ignored by the fp32 /
+ * head-dim-64 pass): 1 makes every CTA first wait for the kernel before it on
+ * the stream (the one whose outputs include blk_len, or a later one) and then
+ * skip a tile of 128 packed rows in which no token is present, e.g. the
+ * copy-block rows of a sequence whose gate is off. Outputs are identical; the
+ * attention then no longer overlaps the tail of that preceding kernel, so it
+ * pays off only when many candidate slots are empty. 2 skips the same tiles
+ * without that wait: the caller guarantees that blk_len is complete when the
+ * call's kernel launches, i.e. the kernel that wrote it has completed before
+ * the kernel issued just before this call lets its dependents launch (true
+ * after ssd_accept, whose finish kernel launches only once the retrieval has
+ * completed, or after an event wait); the attention then runs beside the
+ * kernel before it and waits for it only before its grid ends. 0: every tile
+ * is computed, blk_len is read only before the merge.
  * all_rows (0 or 1): 1 writes the row of every slot t, present or not, as the
  * attention of its q over the prefix and the slots k*Dmax .. t of its block
  * (what the row of a present token holds), and never reads blk_len (it may be

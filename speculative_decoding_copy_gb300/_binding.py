@@ -276,7 +276,7 @@ def attn_args(q, k_cache, v_cache, k_cand, v_cand, prefix_len, blk_len, Dmax, ou
     B, NT, Hq, dh = q.shape
     Hkv = k_cache.shape[1]
     NB = blk_len.shape[1] if blk_len is not None else (NB if NB is not None else NT // int(Dmax))
-    tail = (int(bool(skip_absent)), int(bool(all_rows)), int(max_ctas))
+    tail = (int(skip_absent), int(bool(all_rows)), int(max_ctas))
     if block_table is None:
         return AttnArgs(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_cand), _ptr(v_cand), _ptr(out),
                         _ptr(prefix_len), _ptr(blk_len), _elem_type(q), B, NB, int(Dmax), Hq, Hkv, dh,

@@ -301,7 +301,7 @@ static int validate(const ssd_attn_args* a) {
   if (a->dtype != SSD_F32 && a->dtype != SSD_BF16) return SSD_ERR_INVALID;
   if (a->out_dtype != a->dtype && a->out_dtype != SSD_F32) return SSD_ERR_INVALID;
   if (a->Hq % a->Hkv != 0) return SSD_ERR_INVALID;
-  if (a->skip_absent != 0 && a->skip_absent != 1) return SSD_ERR_INVALID;
+  if (a->skip_absent < 0 || a->skip_absent > 2) return SSD_ERR_INVALID;
   if (a->all_rows != 0 && a->all_rows != 1) return SSD_ERR_INVALID;
   if (a->all_rows && a->skip_absent) return SSD_ERR_INVALID;
   if (a->max_ctas < 0) return SSD_ERR_INVALID;

@@ -23,7 +23,8 @@ struct AttnParams {
   const int32_t* block_table;   // tensor-core path: paged cache [B][pages_per_seq], or null
   int pages_per_seq;
   int64_t num_pages;
-  int skip_absent;       // tensor-core path: wait for the predecessor first, skip tiles without a present token
+  int skip_absent;       // tensor-core path: skip tiles without a present token (1: after waiting for the
+                         // predecessor; 2: blk_len complete at launch, only the last CTA waits, at its end)
   int all_rows;          // write every slot's row; blk_len is never read
   WsHeader* hdr;
   float* ws_ml;          // [rows][S][2]  running max and sum per split

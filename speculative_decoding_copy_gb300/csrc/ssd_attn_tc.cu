@@ -204,16 +204,23 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
   const int rb = split * rpc, nr = max(0, min(rv, rb + rpc) - rb);
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // skip_absent 2: blk_len was complete when this grid launched, so nothing waits for the
+  // kernel before this one except the grid's last CTA, before it ends (the grid then still
+  // completes after it)
+  const bool last_cta = blockIdx.x == gridDim.x - 1 && blockIdx.y == gridDim.y - 1 && blockIdx.z == gridDim.z - 1;
   if (p.skip_absent) {
     // a tile none of whose rows belongs to a present token is skipped; the S CTAs of a
     // cluster hold the same rows, so they all leave here together, before any barrier
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (p.skip_absent == 1) asm volatile("griddepcontrol.wait;" ::: "memory");
     int any = 0;
     for (int i = tid; i < rv; i += kThreads) {
       const int tt = (r0 + i) / G;
       any |= (tt % p.Dmax) < __ldcg(p.blk_len + b * p.NB + tt / p.Dmax) ? 1 : 0;
     }
-    if (!__syncthreads_or(any)) return;
+    if (!__syncthreads_or(any)) {
+      if (p.skip_absent == 2 && last_cta && tid == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+      return;
+    }
   }
   if (warp == 4 && lane == 0) {
     // the descriptors are fetched on first use: start those fetches before the first copy
@@ -491,7 +498,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
   if (warp == 4) {
     // which owned rows belong to tokens that exist: blk_len comes from the retrieval, which
     // precedes this kernel in the stream (with all_rows every slot's row is written)
-    if (!p.all_rows) asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (!p.all_rows && p.skip_absent != 2) asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int i = lane; i < nr; i += 32) {
       const int gr = r0 + rb + i;
       const int tt = gr / G;
@@ -571,9 +578,10 @@ k_attn_tc(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CU
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
-  // with all_rows nothing above waited for the kernel before this one: one thread waits for
-  // it here, after the rows are written, so that this grid still completes after it
-  if (p.all_rows && tid == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+  // with all_rows (or skip_absent 2) nothing above waited for the kernel before this one: one
+  // thread waits for it here, after the rows are written, so that this grid still completes
+  // after it
+  if ((p.all_rows || (p.skip_absent == 2 && last_cta)) && tid == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ host

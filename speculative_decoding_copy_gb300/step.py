@@ -180,11 +180,15 @@ class VerifyStep:
         return ssd.ssd_gate_retrieve(x["ctx"], x["ctx_len"], x["h"], x["w"], wl.tau, wl.kappa, wl.W, wl.D, wl.K,
                                      wl.chain_policy, ct, out={**self.gate_out, **self.ret_out}, stream=stream)
 
-    def attention(self, stream=None):
+    def attention(self, stream=None, blk_len_ready=False):
+        """blk_len_ready: the retrieval has completed before this launch (the acceptance chain
+        or an event sits between them), so the attention skips empty tiles without waiting for
+        the kernel before it (skip_absent mode 2)."""
         x = self.x
+        skip = (2 if blk_len_ready else 1) if self.skip_absent else 0
         return ssd.ssd_verify_attn(x["q"], x["k_cache"], x["v_cache"], x["k_cand"], x["v_cand"], x["prefix_len"],
                                    self.ret_out["blk_len"], self.wl.Dmax, out=self.attn_out, ws=self.attn_ws,
-                                   stream=stream, skip_absent=self.skip_absent, all_rows=self.all_rows,
+                                   stream=stream, skip_absent=skip, all_rows=self.all_rows,
                                    max_ctas=self.attn_ctas)
 
     def accept(self, stream=None, early_rows=None):
@@ -219,7 +223,7 @@ class VerifyStep:
             ev = torch.cuda.Event()
             ev.record(main)
             aux.wait_event(ev)
-            self.attention(aux)
+            self.attention(aux, blk_len_ready=True)
             if self.with_accept:
                 self.accept(main)
             ev2 = torch.cuda.Event()
@@ -237,7 +241,9 @@ class VerifyStep:
             if self.with_accept:
                 self.accept(main)
             if self.with_attention:
-                self.attention(main)
+                # after the acceptance chain: its finish kernel launches only once the
+                # retrieval has completed (in either row-pass mode)
+                self.attention(main, blk_len_ready=self.with_accept)
 
     def results(self) -> dict:
         """Copy every output to host numpy arrays (synchronises)."""

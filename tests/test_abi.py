@@ -58,7 +58,7 @@ def test_host_validation_without_gpu(libpath):
     assert L.ssd_verify_attn(ctypes.byref(a), null, 0, null) == b.SSD_ERR_UNSUPPORTED
     a.dh, a.Hkv = 128, 3
     assert L.ssd_verify_attn(ctypes.byref(a), null, 0, null) == b.SSD_ERR_INVALID
-    a.Hkv, a.skip_absent = 2, 2                     # only 0 or 1
+    a.Hkv, a.skip_absent = 2, 3                     # only 0, 1 or 2
     assert L.ssd_verify_attn(ctypes.byref(a), null, 0, null) == b.SSD_ERR_INVALID
     c = b.AcceptArgs()
     c.mode, c.kind, c.V, c.B, c.NB, c.Dmax, c.chain_blk = 7, 0, 100, 1, 1, 4, -1

@@ -218,9 +218,9 @@ def test_attention_paged_bad_page_is_reported():
 
 @pytest.mark.parametrize("G", [4, 8])
 def test_attention_skip_absent_tiles(G):
-    """skip_absent: 128-row tiles in which no token is present are skipped. Present rows
-    equal the full computation bit for bit and the oracle within the bound; absent rows
-    are written by neither."""
+    """skip_absent (both modes): 128-row tiles in which no token is present are skipped.
+    Present rows equal the full computation bit for bit and the oracle within the bound;
+    absent rows are written by none of the three calls."""
     rng = np.random.default_rng(50 + G)
     Hkv, B, NB, Dmax = 2, 4, 3, 20
     prefix = [300, 0, 4100, 129]
@@ -231,7 +231,9 @@ def test_attention_skip_absent_tiles(G):
     t = {k: to_device(np.asarray(v), dev) for k, v in case.items()}
     bl = to_device(blk_len, dev)
     outs = []
-    for skip in (False, True):
+    # 0: every tile; 1: skip after waiting for the kernel before; 2: skip, blk_len complete at
+    # launch (a host copy wrote it), no wait before the grid's end
+    for skip in (0, 1, 2):
         out = torch.full(t["q"].shape, 7.0, dtype=torch.float32, device=dev)
         S.ssd_verify_attn(t["q"], t["k_cache"], t["v_cache"], t["k_cand"], t["v_cand"], t["prefix_len"], bl, Dmax,
                           out=out, skip_absent=skip)
@@ -241,8 +243,10 @@ def test_attention_skip_absent_tiles(G):
     for b in range(B):
         for k in range(NB):
             present[b, k * Dmax:k * Dmax + blk_len[b, k]] = True
-    np.testing.assert_array_equal(outs[1][present], outs[0][present])
-    assert np.all(outs[1][~present] == 7.0) and np.all(outs[0][~present] == 7.0)
+    for mode in (1, 2):
+        np.testing.assert_array_equal(outs[mode][present], outs[0][present])
+        assert np.all(outs[mode][~present] == 7.0)
+    assert np.all(outs[0][~present] == 7.0)
     ref = O.verify_attention(case["q"], case["k_cache"], case["v_cache"], case["k_cand"], case["v_cand"],
                              case["prefix_len"], blk_len, Dmax, "bf16", None)
     err = max(float(np.max(np.abs(outs[1][b, t_] - o))) for (b, t_), o in ref.items())
